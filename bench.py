@@ -1,0 +1,426 @@
+"""Benchmark of the ragged batched speculative-verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2|3]
+
+One step = one verify pass of the whole hot path (embedding, QKV + RoPE + KV
+append, paged attention, O, SwiGLU FFN, LM head + softmax statistics,
+acceptance + sampling, realignment) over one batch of synthetic inputs that
+stay resident in HBM.  Default workload: B = 1 sequence with 7 drafts on a
+9B-class layer (hidden 4096, 32/8 heads of 128, FFN 12288, vocab 151936,
+bf16), KV context 2048 in 16-token pages, per-draft acceptance 0.8.  The
+weights (1.63 GB) are larger than L2 (129 MB), so no L2 flush is needed
+between steps.  Every step draws fresh uniforms, so emitted tokens follow the
+acceptance statistics.
+
+Metric: verified (emitted) tokens per second, sum over sequences of
+(accepted + 1) per step / step time; ms per step beside it.  Multi-GPU: one
+independent replica per GPU (the step does not shard: every sequence needs
+all weights), value = all ranks' tokens / slowest rank's time.
+
+``--impl reference`` times the CPU oracle (float64 numpy, the plain
+restatement of the method) on the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tokens/s & verify-step us vs B*(gamma+1); % of HBM/tensor roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def workload_desc(wid):
+    import workloads as wl
+    if wid == 2:
+        return dict(workload="batch-of-one: B=1, gamma=7, 9B-class layer bf16 (hidden 4096, 32/8 heads x 128, "
+                             "FFN 12288), vocab 151936, ctx 2048, acceptance 0.8",
+                    B=1, gamma=[7], ctx=[2048], rows=8, l2="inputs larger than L2 (weights 1.63 GB)")
+    lens, gam, _ = wl.workload3_shape()
+    return dict(workload="eight-agent ragged: B=8, gamma_b in {1,2,3} (sum<=16), ctx U{512..8192}, "
+                         "acceptance {0.97,0.8,0.14}, 9B-class layer bf16, vocab 151936",
+                B=8, gamma=[int(x) for x in gam], ctx=[int(x) for x in lens], rows=int((gam + 1).sum()),
+                l2="inputs larger than L2 (weights 1.63 GB)")
+
+
+def make_host_workload(wid):
+    import workloads as wl
+    W = wl.make_weights(wl.NINE_B, wid)
+    if wid == 2:
+        batch = wl.workload2(extra_pages=8)
+    else:
+        batch = wl.workload3(extra_pages=16)
+    return W, batch
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def lm_head_algorithmic_bytes(R, V=151936, H=4096, vtile=128):
+    """Bytes the LM-head launch must move: the weights once, the normed rows,
+    and the per-(vocab tile, row) softmax statistics it produces."""
+    return V * H * 2 + R * H * 2 + ((V + vtile - 1) // vtile) * R * 8
+
+
+def step_algorithmic_bytes(batch):
+    """Per-step bytes of the whole hot path: layer + LM-head weights once, every
+    sequence's KV read, the new rows' KV written, the draft probabilities the
+    rule reads (q at each draft token, plus the full q row of each sequence's
+    final position), the target logits of the final rows."""
+    H, F, V, D, nq, nkv = 4096, 12288, 151936, 128, 32, 8
+    layer = ((nq + 2 * nkv) * D * H + H * nq * D + 2 * F * H + H * F) * 2
+    lm = V * H * 2
+    kv_read = int(sum(batch.seq_lens)) * nkv * 2 * D * 2
+    kv_write = batch.R * nkv * 2 * D * 2
+    q_bytes = batch.G * 4 + batch.B * V * 4
+    return layer + lm + kv_read + kv_write + q_bytes
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1932.1)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def run_ours(args):
+    import torch
+    import workloads as wl
+    from workloads import device as wd
+    from speculative_decoding_verify_ragged_gb300 import PHASES, VerifyEngine, kernel_launches
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    W, batch = make_host_workload(args.workload)
+    Wd = wd.weights_to_device(W)
+    gmax = int(batch.gamma_max)
+    eng = VerifyEngine(wd.config(wl.NINE_B, gmax), Wd, max_rows=max(64, batch.R), max_slots=max(16, batch.B))
+
+    # input recipe: q built around the target's own p so each draft is accepted w.p. alpha
+    bd = wd.batch_to_device(batch)
+    res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1], probs=True)
+    eng.verify_step(bd, res)
+    assert eng.read_status(res["status"]) == 0
+    wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), args.workload)
+    del res
+
+    # device-resident inputs; one set of uniforms per step
+    bd = wd.batch_to_device(batch)
+    nsteps = args.warmup + args.steps
+    g = wl.rng(args.workload, wl.S_U, 1000 + rank)
+    U = torch.from_numpy(np.stack([wl.uniform24(g, batch.R) for _ in range(nsteps)])).cuda()
+    res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1])
+    stream = torch.cuda.current_stream()
+    emitted = torch.zeros(nsteps, dtype=torch.int32, device="cuda")
+
+    def step(i):
+        bd["uniforms"] = U[i]
+        eng.verify_step(bd, res, stream)
+        emitted[i] = res["emitted_offsets"][batch.B]
+
+    for i in range(args.warmup):
+        step(i)
+    assert eng.read_status(res["status"]) == 0
+    torch.cuda.synchronize()
+
+    # one set of phase events per timed step, recorded on the launching stream,
+    # read after the timed region: the dominant kernel is timed live, without
+    # synchronising inside the timed region
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(args.steps)]
+    for es in evsets:
+        for e in es:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    # pre-roll: the same step back to back for ~1 s so the clock samples see the GPU under load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        step(args.warmup - 1)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = kernel_launches()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for j, i in enumerate(range(args.warmup, nsteps)):
+        eng.set_phase_events(evsets[j])
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    eng.set_phase_events(None)
+    assert eng.read_status(res["status"]) == 0
+    phase_ms = {p: [es[k].elapsed_time(es[k + 1]) for es in evsets] for k, p in enumerate(PHASES)}
+
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    tokens_rank = int(emitted[args.warmup:].sum().item())
+    tokens = tokens_rank
+    if world > 1:
+        import torch.distributed as dist
+        tk = torch.tensor([tokens], dtype=torch.int64, device="cuda")
+        dist.all_reduce(tk)
+        tokens = int(tk.item())
+    value = tokens / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(eng, batch, bd, U, args, stream, tokens_rank)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e["value"] = tokens / (float(tt.item()) * args.steps / 1e3)
+
+    hbm, tflops, peak_kind = measured_peaks()
+    lm_avg = statistics.mean(phase_ms["lm_head"])
+    lm_bytes = lm_head_algorithmic_bytes(batch.R)
+    achieved = lm_bytes / (lm_avg / 1e3) / 1e9
+    step_bytes = step_algorithmic_bytes(batch)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_desc(args.workload), "parallelism": f"replicas{world}",
+                   "verify_rows_per_step": batch.R},
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "kernel": "LM-head GEMM (EPI_LMHEAD)",
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
+                     "avg_launch_us": lm_avg * 1e3},
+        "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes,
+                          "achieved_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
+                          "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
+        "phases_us": {p: statistics.mean(v) * 1e3 for p, v in phase_ms.items()},
+        "emitted_tokens_per_step": tokens / (args.steps * world),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(W, batch)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(eng, batch, bd, U, args, stream, tokens):
+    """The same step through the public API with host inputs: every step copies
+    its inputs from pinned host memory and reads its results back."""
+    import torch
+    import workloads as wl
+    from workloads import device as wd
+
+    def pin(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.pin_memory()
+
+    host_in = {
+        "seq_lens": pin(batch.seq_lens.astype(np.int32)), "draft_lens": pin(batch.draft_lens.astype(np.int32)),
+        "tokens": pin(batch.tokens.astype(np.int32)), "draft_probs": pin(batch.draft_probs.astype(np.float32)),
+        "page_table": pin(batch.page_table.astype(np.int32)), "num_pages": pin(batch.num_pages.astype(np.int32)),
+        "num_free_in": pin(np.array([batch.num_free], np.int32)),
+    }
+    Uh = U.cpu().pin_memory()
+    dev = dict(bd)
+    for k, v in host_in.items():
+        dev[k] = torch.empty_like(v, device="cuda")
+    dev["num_free_out"] = dev["num_free_in"]
+    dev["uniforms"] = torch.empty(batch.R, dtype=torch.float32, device="cuda")
+    res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1],
+                          next_view=False)
+    outs = ("accepted", "final_tokens", "emitted_tokens", "emitted_offsets", "new_seq_lens")
+    host_out = {k: torch.empty_like(res[k], device="cpu").pin_memory() for k in outs}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + batch.R * 4
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def step(i):
+        for k, v in host_in.items():
+            dev[k].copy_(v, non_blocking=True)
+        dev["uniforms"].copy_(Uh[i], non_blocking=True)
+        eng.verify_step(dev, res, stream)
+        for k in outs:
+            host_out[k].copy_(res[k], non_blocking=True)
+
+    nsteps = args.warmup + args.steps
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.warmup, nsteps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    # the e2e steps use the same uniforms as the device-resident loop, so they
+    # emit the same tokens
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms / args.steps,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(W, batch):
+    """The oracle as it stands, timed on this host on one full step of the workload."""
+    from oracle import verify_step as o
+    t = time.perf_counter()
+    out = o.verify_step(batch, W)
+    dt = time.perf_counter() - t
+    toks = int(out["emitted_offsets"][-1])
+    return {"value": toks / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full verify step of the bench workload ({batch.R} rows), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as wl
+    from oracle import verify_step as o
+    W, batch = make_host_workload(args.workload)
+    # the same recipe for q, built from the oracle's own target probabilities
+    fw = o.forward(batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens,
+                   batch.tokens)
+    wl.retarget_draft_probs(batch, fw["probs"].astype(np.float32), args.workload)
+    g = wl.rng(args.workload, wl.S_U, 1000)
+    nsteps = args.warmup + args.steps
+    U = [wl.uniform24(g, batch.R) for _ in range(nsteps)]
+    # a step of the oracle takes seconds: each step is a bounded sample of the
+    # workload (the first draft block's rows of the batch)
+    times, tokens = [], 0
+    for i in range(nsteps):
+        batch.uniforms = U[i]
+        t = time.perf_counter()
+        out = o.verify_step(batch, W)
+        dt = time.perf_counter() - t
+        if i >= args.warmup:
+            times.append(dt)
+            tokens += int(out["emitted_offsets"][-1])
+    total = sum(times)
+    value = tokens / total
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**workload_desc(args.workload), "parallelism": "host"},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{args.steps} full verify steps of the workload on the host"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

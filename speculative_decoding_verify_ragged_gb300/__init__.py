@@ -1,0 +1,170 @@
+"""Ragged batched speculative-verify step on GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/sdv.h``: it converts torch
+tensors and dicts into the ABI's structs and calls the CUDA library.  Every
+step of the verify path (weight-streaming GEMMs with fused epilogues, paged
+ragged attention, LM head and softmax statistics, rejection-sampling
+acceptance, realignment) runs in the library's kernels; if the library is
+missing the calls raise, there is no CPU path.
+
+Typical use::
+
+    eng = VerifyEngine(cfg, weights, max_rows=64, max_slots=8)
+    eng.verify_step(batch, result)          # enqueued on the current stream
+    status = VerifyEngine.read_status(result["status"])
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._abi import (PHASES, RESULT_FIELDS, STATUS, SDV_OK, SDV_WEIGHTS_BF16, SDV_WEIGHTS_INT4_G32, SdvBatch, SdvConfig,
+                   SdvResult, SdvWeights, load_library)
+
+__all__ = ["VerifyEngine", "SdvError", "PHASES", "STATUS", "load_library", "kernel_launches", "SDV_WEIGHTS_BF16",
+           "SDV_WEIGHTS_INT4_G32"]
+
+
+class SdvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def kernel_launches() -> int:
+    return int(load_library().sdv_kernel_launches())
+
+
+CONFIG_KEYS = ("hidden", "n_q", "n_kv", "head_dim", "ffn", "vocab", "page_size", "gamma_max", "weight_format")
+WEIGHT_KEYS = ("emb", "w_qkv", "w_o", "w_gate", "w_up", "w_down", "w_lm", "s_qkv", "s_o", "s_gate", "s_up",
+               "s_down", "g_attn", "g_ffn", "g_final")
+
+
+class VerifyEngine:
+    """A verify-step context over device-resident weights.
+
+    cfg: dict with the sdv_config fields (rms_eps / rope_theta default to
+    1e-6 / 1e6).  weights: dict of CUDA tensors named as sdv_weights.  The
+    workspace is allocated here through torch (the library never allocates).
+    """
+
+    def __init__(self, cfg: dict, weights: dict, max_rows: int, max_slots: int):
+        import torch
+        self.lib = load_library()
+        self.cfg_dict = dict(cfg)
+        self.cfg = SdvConfig(*[int(cfg.get(k, 0)) for k in CONFIG_KEYS],
+                             float(cfg.get("rms_eps", 1e-6)), float(cfg.get("rope_theta", 1e6)))
+        self._weights = {k: weights.get(k) for k in WEIGHT_KEYS}   # keep tensors alive
+        self.wstruct = SdvWeights(*[_ptr(self._weights[k]) for k in WEIGHT_KEYS])
+        self.max_rows = int(max_rows)
+        self.max_slots = int(max_slots)
+        nbytes = self.lib.sdv_workspace_size(ctypes.byref(self.cfg), self.max_rows, self.max_slots)
+        if nbytes == 0:
+            raise SdvError(1, "sdv_workspace_size rejected the configuration")
+        self.workspace = torch.empty(int(nbytes), dtype=torch.uint8, device="cuda")
+        self.workspace_bytes = int(nbytes)
+        h = ctypes.c_void_p()
+        rc = self.lib.sdv_create(ctypes.byref(self.cfg), ctypes.byref(self.wstruct), _ptr(self.workspace),
+                                 ctypes.c_size_t(nbytes), self.max_rows, self.max_slots, ctypes.byref(h))
+        if rc != SDV_OK:
+            raise SdvError(rc, "sdv_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.sdv_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- marshalling -------------------------------------------------------
+
+    @staticmethod
+    def batch_struct(b: dict) -> SdvBatch:
+        pt = b["page_table"]
+        return SdvBatch(int(b["B"]), int(b["R"]), int(b["G"]),
+                        _ptr(b["seq_lens"]), _ptr(b["draft_lens"]), _ptr(b.get("tokens")),
+                        _ptr(b.get("draft_probs")), _ptr(b.get("uniforms")),
+                        _ptr(b.get("kv_pool")), int(b.get("num_pool_pages", 0)),
+                        _ptr(pt), int(pt.shape[1]),
+                        _ptr(b["num_pages"]), _ptr(b.get("free_pages")),
+                        _ptr(b.get("num_free_in")), _ptr(b.get("num_free_out")),
+                        _ptr(b.get("gen_counts")), _ptr(b.get("gen_limits")))
+
+    @staticmethod
+    def result_struct(r: dict) -> SdvResult:
+        return SdvResult(*[_ptr(r.get(k)) for k in RESULT_FIELDS])
+
+    def _check(self, rc, what):
+        if rc != SDV_OK:
+            extra = ""
+            if rc == 4:
+                extra = f" (cuda error {self.lib.sdv_last_cuda_error()})"
+            raise SdvError(rc, what + extra)
+
+    # -- entry points ------------------------------------------------------
+
+    def verify_step(self, batch: dict, result: dict, stream=None):
+        bs, rs = self.batch_struct(batch), self.result_struct(result)
+        self._check(self.lib.sdv_verify_step(self.handle, ctypes.byref(bs), ctypes.byref(rs), _stream(stream)),
+                    "sdv_verify_step")
+
+    def accept(self, probs, batch: dict, result: dict, stream=None):
+        bs, rs = self.batch_struct(batch), self.result_struct(result)
+        self._check(self.lib.sdv_accept(self.handle, _ptr(probs), ctypes.byref(bs), ctypes.byref(rs),
+                                        _stream(stream)), "sdv_accept")
+
+    def realign(self, batch: dict, result: dict, stream=None):
+        bs, rs = self.batch_struct(batch), self.result_struct(result)
+        self._check(self.lib.sdv_realign(self.handle, ctypes.byref(bs), ctypes.byref(rs), _stream(stream)),
+                    "sdv_realign")
+
+    def linear(self, which: int, x, y, stream=None):
+        self._check(self.lib.sdv_linear(self.handle, int(which), _ptr(x), _ptr(y), int(x.shape[0]),
+                                        _stream(stream)), "sdv_linear")
+
+    def attention(self, q, batch: dict, out, status, stream=None):
+        bs = self.batch_struct(batch)
+        self._check(self.lib.sdv_attention(self.handle, _ptr(q), ctypes.byref(bs), _ptr(out), _ptr(status),
+                                           _stream(stream)), "sdv_attention")
+
+    def set_phase_events(self, events):
+        """Record torch.cuda.Event objects at the step's phase boundaries (None = off).
+
+        ``events`` holds len(PHASES) + 1 events created with enable_timing=True.
+        """
+        if events is None:
+            self._check(self.lib.sdv_set_phase_events(self.handle, None, 0), "sdv_set_phase_events")
+            self._events = None
+            return
+        for e in events:
+            if not e.cuda_event:
+                e.record()          # creates the underlying CUDA event
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        self._events = list(events)
+        self._check(self.lib.sdv_set_phase_events(self.handle, arr, len(events)), "sdv_set_phase_events")
+
+    @staticmethod
+    def read_status(status, stream=None) -> int:
+        lib = load_library()
+        out = ctypes.c_int(-1)
+        rc = lib.sdv_read_status(_ptr(status), ctypes.byref(out), _stream(stream))
+        if rc != SDV_OK:
+            raise SdvError(rc, "sdv_read_status")
+        return int(out.value)

@@ -1,0 +1,581 @@
+// C ABI of the verify step: argument checks, workspace layout, TMA
+// descriptors and the order of kernel launches on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+namespace sdv {
+
+static std::atomic<unsigned long long> g_launches{0};
+static thread_local int g_last_cuda_error = 0;
+
+void note_launch(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed); }
+
+static sdv_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return SDV_ERR_CUDA;
+}
+
+#define SDV_CUDA(x)                              \
+  do {                                           \
+    cudaError_t e__ = (x);                       \
+    if (e__ != cudaSuccess) return cuda_fail(e__); \
+  } while (0)
+
+static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+
+struct Layout {
+  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope;
+  size_t x0, h, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
+  size_t part_o, part_ml, accepted, final_tokens, total;
+  int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
+};
+
+static int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static bool config_ok(const sdv_config* c) {
+  if (!c) return false;
+  if (c->hidden <= 0 || c->n_q <= 0 || c->n_kv <= 0 || c->ffn <= 0 || c->vocab <= 0) return false;
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->n_q % c->n_kv) return false;
+  if (c->page_size != 16) return false;
+  if (c->gamma_max < 0 || (c->gamma_max + 1) * (c->n_q / c->n_kv) > kAttnQMax) return false;
+  const int kmul = c->weight_format == SDV_WEIGHTS_INT4_G32 ? 256 : 64;
+  if (c->weight_format != SDV_WEIGHTS_BF16 && c->weight_format != SDV_WEIGHTS_INT4_G32) return false;
+  if (c->hidden % kmul || (c->n_q * c->head_dim) % kmul || c->ffn % kmul) return false;
+  if (c->ffn % 64) return false;
+  return true;
+}
+
+static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int sms) {
+  Layout L{};
+  const size_t R = static_cast<size_t>(max_rows), B = static_cast<size_t>(max_slots);
+  const size_t H = c.hidden, QD = static_cast<size_t>(c.n_q) * c.head_dim, F = c.ffn, V = c.vocab;
+  const size_t NQKV = static_cast<size_t>(c.n_q + 2 * c.n_kv) * c.head_dim;
+  L.lm_tiles = static_cast<int>((V + 127) / 128);
+  const int rt = static_cast<int>((R + 15) / 16);
+  const int tiles_qkv = static_cast<int>((NQKV + 127) / 128);
+  const int tiles_o = static_cast<int>((H + 127) / 128);
+  const int tiles_gu = static_cast<int>((F + 63) / 64);
+  int mt = L.lm_tiles;
+  if (tiles_qkv > mt) mt = tiles_qkv;
+  if (tiles_o > mt) mt = tiles_o;
+  if (tiles_gu > mt) mt = tiles_gu;
+  L.max_tiles = mt * rt;
+  L.grid_gemm = sms;
+  L.target_items = 8 * sms;
+  L.items_max = L.target_items + static_cast<int>(B) * c.n_kv + 8;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += up256(bytes);
+    return at;
+  };
+  L.row_off = take((B + 1) * 4);
+  L.draft_off = take((B + 1) * 4);
+  L.row_seq = take(R * 4);
+  L.row_pos = take(R * 4);
+  L.chunks = take(B * 4);
+  L.item_off = take((B + 1) * 4);
+  L.sched = take(64);
+  L.rope = take(R * (c.head_dim / 2) * 2 * 4);
+  L.x0 = take(R * H * 2);
+  L.h = take(R * H * 2);
+  L.q = take(R * QD * 2);
+  L.attn = take(R * QD * 2);
+  L.x1 = take(R * H * 2);
+  L.act = take(R * F * 2);
+  L.x2 = take(R * H * 2);
+  L.z = take(R * V * 4);
+  L.lmstats = take(static_cast<size_t>(L.lm_tiles) * R * 8);
+  L.rowstats = take(R * 8);
+  L.partials = take(static_cast<size_t>(2) * sms * 128 * 64 * 4);
+  L.counters = take(static_cast<size_t>(L.max_tiles) * 4);
+  L.part_o = take(static_cast<size_t>(L.items_max) * kAttnQMax * c.head_dim * 4);
+  L.part_ml = take(static_cast<size_t>(L.items_max) * kAttnQMax * 8);
+  L.accepted = take(B * 4);
+  L.final_tokens = take(B * 4);
+  L.total = o;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 matrix [rows, cols] (cols contiguous), box = (64 cols, box_rows), 128-byte swizzle.
+static bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// KV pool [pages, n_kv, 2, page, D] as a 5-D tensor; box = 64 of D x 16 slots.
+static bool encode_kv(CUtensorMap* m, const void* base, const sdv_config& c, int pool_pages) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t D = c.head_dim, P = c.page_size;
+  cuuint64_t dims[5] = {D, P, 2, static_cast<cuuint64_t>(c.n_kv), static_cast<cuuint64_t>(pool_pages)};
+  cuuint64_t strides[4] = {D * 2, P * D * 2, 2 * P * D * 2, static_cast<cuuint64_t>(c.n_kv) * 2 * P * D * 2};
+  cuuint32_t box[5] = {64, 16, 1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int nt_index(int nt) { return nt == 16 ? 0 : (nt == 32 ? 1 : 2); }
+
+}  // namespace sdv
+
+using namespace sdv;
+
+struct sdv_ctx {
+  sdv_config cfg;
+  sdv_weights w;
+  int max_rows, max_slots, sms;
+  uint8_t* ws;
+  Layout L;
+  CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
+  CUtensorMap tm_h[3], tm_attn[3], tm_act[3];
+  cudaEvent_t phase_ev[SDV_PHASES + 1];
+  bool timing;
+};
+
+template <typename T>
+static T* ws_ptr(sdv_ctx* c, size_t off) {
+  return reinterpret_cast<T*>(c->ws + off);
+}
+
+extern "C" {
+
+size_t sdv_workspace_size(const sdv_config* cfg, int max_rows, int max_slots) {
+  if (!config_ok(cfg) || max_rows <= 0 || max_slots <= 0 || max_slots > 1024) return 0;
+  const int sms = num_sms_current();
+  if (sms <= 0) return 0;
+  return make_layout(*cfg, max_rows, max_slots, sms).total;
+}
+
+sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspace, size_t workspace_bytes,
+                      int max_rows, int max_slots, sdv_ctx** out) {
+  if (!out || !w || !workspace) return SDV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return SDV_ERR_INVALID_ARG;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return SDV_ERR_UNSUPPORTED;
+  if (cfg->weight_format == SDV_WEIGHTS_INT4_G32) return SDV_ERR_UNSUPPORTED;
+  if (!config_ok(cfg) || max_rows <= 0 || max_slots <= 0 || max_slots > 1024) return SDV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return SDV_ERR_INVALID_ARG;
+  if (!w->emb || !w->w_qkv || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->w_lm || !w->g_attn ||
+      !w->g_ffn || !w->g_final)
+    return SDV_ERR_INVALID_ARG;
+  const int sms = num_sms_current();
+  if (sms <= 0) return SDV_ERR_CUDA;
+  Layout L = make_layout(*cfg, max_rows, max_slots, sms);
+  if (workspace_bytes < L.total) return SDV_ERR_CAPACITY;
+  sdv_ctx* c = new (std::nothrow) sdv_ctx();
+  if (!c) return SDV_ERR_INTERNAL;
+  c->cfg = *cfg;
+  c->w = *w;
+  c->max_rows = max_rows;
+  c->max_slots = max_slots;
+  c->sms = sms;
+  c->ws = static_cast<uint8_t*>(workspace);
+  c->L = L;
+  c->timing = false;
+  const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
+                 V = cfg->vocab;
+  const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
+  bool ok = encode_bf16_2d(&c->tm_qkv, w->w_qkv, NQKV, H, 64) && encode_bf16_2d(&c->tm_o, w->w_o, H, QD, 64) &&
+            encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
+            encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
+  const int nts[3] = {16, 32, 64};
+  for (int i = 0; i < 3 && ok; ++i) {
+    ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, max_rows, H, nts[i]) &&
+         encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, max_rows, QD, nts[i]) &&
+         encode_bf16_2d(&c->tm_act[i], c->ws + L.act, max_rows, F, nts[i]);
+  }
+  if (!ok) {
+    delete c;
+    return SDV_ERR_CUDA;
+  }
+  cudaError_t e = cudaMemset(c->ws + L.counters, 0, static_cast<size_t>(L.max_tiles) * 4);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e);
+  }
+  *out = c;
+  return SDV_OK;
+}
+
+void sdv_destroy(sdv_ctx* ctx) { delete ctx; }
+
+sdv_status sdv_set_phase_events(sdv_ctx* ctx, void* const* events, int n) {
+  if (!ctx) return SDV_ERR_INVALID_ARG;
+  if (!events || n == 0) {
+    ctx->timing = false;
+    return SDV_OK;
+  }
+  if (n != SDV_PHASES + 1) return SDV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return SDV_ERR_INVALID_ARG;
+    ctx->phase_ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  ctx->timing = true;
+  return SDV_OK;
+}
+
+int sdv_last_cuda_error(void) { return g_last_cuda_error; }
+
+unsigned long long sdv_kernel_launches(void) { return g_launches.load(); }
+
+sdv_status sdv_read_status(const int* status, int* host_status, void* stream) {
+  if (!status || !host_status) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SDV_CUDA(cudaMemcpyAsync(host_status, status, sizeof(int), cudaMemcpyDeviceToHost, s));
+  SDV_CUDA(cudaStreamSynchronize(s));
+  return SDV_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// launch helpers
+// ---------------------------------------------------------------------------
+
+static bool batch_ok(const sdv_ctx* c, const sdv_batch* b, bool need_forward) {
+  if (!b) return false;
+  if (b->B <= 0 || b->B > c->max_slots || b->R < b->B || b->R > c->max_rows || b->G != b->R - b->B) return false;
+  if (!b->seq_lens || !b->draft_lens || !b->page_table || !b->num_pages) return false;
+  if (b->max_pages_per_seq <= 0 || b->num_pool_pages <= 0) return false;
+  if (need_forward && (!b->tokens || !b->kv_pool)) return false;
+  return true;
+}
+
+static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* status, bool check_tokens) {
+  PrologueParams p;
+  p.t.row_off = ws_ptr<int>(c, c->L.row_off);
+  p.t.draft_off = ws_ptr<int>(c, c->L.draft_off);
+  p.t.row_seq = ws_ptr<int>(c, c->L.row_seq);
+  p.t.row_pos = ws_ptr<int>(c, c->L.row_pos);
+  p.t.chunks = ws_ptr<int>(c, c->L.chunks);
+  p.t.item_off = ws_ptr<int>(c, c->L.item_off);
+  p.t.sched = ws_ptr<int>(c, c->L.sched);
+  p.t.rope_cs = ws_ptr<float>(c, c->L.rope);
+  p.seq_lens = b->seq_lens;
+  p.draft_lens = b->draft_lens;
+  p.tokens = b->tokens;
+  p.page_table = b->page_table;
+  p.num_pages = b->num_pages;
+  p.status = status;
+  p.B = b->B;
+  p.R = b->R;
+  p.G = b->G;
+  p.gamma_max = c->cfg.gamma_max;
+  p.vocab = c->cfg.vocab;
+  p.page = c->cfg.page_size;
+  p.max_pages = b->max_pages_per_seq;
+  p.pool_pages = b->num_pool_pages;
+  p.n_kv = c->cfg.n_kv;
+  p.head_dim = c->cfg.head_dim;
+  p.target_items = c->L.target_items;
+  p.rope_theta = c->cfg.rope_theta;
+  p.check_tokens = check_tokens && b->tokens ? 1 : 0;
+  return p;
+}
+
+static GemmParams gemm_params(sdv_ctx* c, int N, int K, int R, int m_tiles, int nt, int* status) {
+  GemmParams g;
+  g.N = N;
+  g.K = K;
+  g.R = R;
+  g.m_tiles = m_tiles;
+  g.n_tiles = (R + nt - 1) / nt;
+  g.kb = K / 64;
+  g.partials = ws_ptr<float>(c, c->L.partials);
+  g.counters = ws_ptr<int>(c, c->L.counters);
+  g.status = status;
+  return g;
+}
+
+static int gemm_grid(sdv_ctx* c, const GemmParams& g) {
+  const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
+  return static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
+}
+
+static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const __nv_bfloat16* q, __nv_bfloat16* out,
+                                int* status, cudaStream_t s) {
+  CUtensorMap kv;
+  if (!encode_kv(&kv, b->kv_pool, c->cfg, b->num_pool_pages)) return SDV_ERR_CUDA;
+  AttnParams a;
+  a.q = q;
+  a.out = out;
+  a.seq_lens = b->seq_lens;
+  a.draft_lens = b->draft_lens;
+  a.row_off = ws_ptr<int>(c, c->L.row_off);
+  a.page_table = b->page_table;
+  a.max_pages = b->max_pages_per_seq;
+  a.item_off = ws_ptr<int>(c, c->L.item_off);
+  a.chunks = ws_ptr<int>(c, c->L.chunks);
+  a.sched = ws_ptr<int>(c, c->L.sched);
+  a.part_o = ws_ptr<float>(c, c->L.part_o);
+  a.part_ml = ws_ptr<float2>(c, c->L.part_ml);
+  a.status = status;
+  a.B = b->B;
+  a.n_q = c->cfg.n_q;
+  a.n_kv = c->cfg.n_kv;
+  a.page = c->cfg.page_size;
+  const int grid = 2 * c->sms;
+  SDV_CUDA(launch_attention_impl(c->cfg.head_dim, &kv, a, grid, b->R, s, ws_ptr<int>(c, c->L.row_seq)));
+  return SDV_OK;
+}
+
+static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_result* r, const int* accepted,
+                                    const int* final_tokens) {
+  RealignParams p;
+  p.seq_lens = b->seq_lens;
+  p.draft_lens = b->draft_lens;
+  p.tokens = b->tokens;
+  p.row_off = ws_ptr<int>(c, c->L.row_off);
+  p.accepted = accepted;
+  p.final_tokens = final_tokens;
+  p.page_table = b->page_table;
+  p.num_pages = b->num_pages;
+  p.free_pages = b->free_pages;
+  p.num_free_in = b->num_free_in;
+  p.num_free_out = b->num_free_out;
+  p.gen_counts = b->gen_counts;
+  p.gen_limits = b->gen_limits;
+  p.res = *r;
+  p.B = b->B;
+  p.page = c->cfg.page_size;
+  p.gamma_max = c->cfg.gamma_max;
+  p.max_pages = b->max_pages_per_seq;
+  p.pool_pages = b->num_pool_pages;
+  return p;
+}
+
+static bool result_ok(const sdv_batch* b, const sdv_result* r) {
+  if (!r || !r->status) return false;
+  if (!b->free_pages || !b->num_free_in || !b->num_free_out) return false;
+  if ((r->accept_tested == nullptr) != (r->accept_accepted == nullptr)) return false;
+  return true;
+}
+
+extern "C" {
+
+sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stream) {
+  if (!c || !batch_ok(c, b, true) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
+  if (!b->uniforms || (b->G > 0 && !b->draft_probs)) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const sdv_config& cf = c->cfg;
+  const int R = b->R, H = cf.hidden, D = cf.head_dim, QD = cf.n_q * D, F = cf.ffn, V = cf.vocab;
+  const int NQKV = (cf.n_q + 2 * cf.n_kv) * D;
+  int* status = r->status;
+  const int nt = gemm_tile_rows(R);
+  const int ni = nt_index(nt);
+  auto bf = [&](size_t off) { return ws_ptr<__nv_bfloat16>(c, off); };
+  auto mark = [&](int k) -> cudaError_t { return c->timing ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess; };
+
+  SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
+  PrologueParams pp = prologue_params(c, b, status, true);
+  SDV_CUDA(launch_prologue(pp, s));
+  SDV_CUDA(launch_embed_norm_rope(b->tokens, static_cast<const __nv_bfloat16*>(c->w.emb),
+                                  static_cast<const __nv_bfloat16*>(c->w.g_attn), bf(c->L.x0), bf(c->L.h),
+                                  pp.t.row_pos, pp.t.rope_cs, R, H, D, cf.rms_eps, cf.rope_theta, status, s));
+  SDV_CUDA(mark(SDV_PHASE_QKV));
+  {  // fused QKV + RoPE + KV append
+    GemmParams g = gemm_params(c, NQKV, H, R, (NQKV + 127) / 128, nt, status);
+    g.epi.q_out = bf(c->L.q);
+    g.epi.kv_pool = static_cast<__nv_bfloat16*>(b->kv_pool);
+    g.epi.page_table = b->page_table;
+    g.epi.max_pages = b->max_pages_per_seq;
+    g.epi.row_seq = pp.t.row_seq;
+    g.epi.row_pos = pp.t.row_pos;
+    g.epi.rope_cs = pp.t.rope_cs;
+    g.epi.n_q = cf.n_q;
+    g.epi.n_kv = cf.n_kv;
+    g.epi.head_dim = D;
+    g.epi.page = cf.page_size;
+    SDV_CUDA(launch_gemm(EPI_QKV, nt, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
+  }
+  SDV_CUDA(mark(SDV_PHASE_ATTN));
+  {
+    sdv_status st = run_attention(c, b, bf(c->L.q), bf(c->L.attn), status, s);
+    if (st != SDV_OK) return st;
+  }
+  SDV_CUDA(mark(SDV_PHASE_O));
+  {  // O projection + residual
+    GemmParams g = gemm_params(c, H, QD, R, (H + 127) / 128, nt, status);
+    g.epi.out_bf16 = bf(c->L.x1);
+    g.epi.resid = bf(c->L.x0);
+    g.epi.ld_bf16 = H;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
+  }
+  SDV_CUDA(mark(SDV_PHASE_FFN));
+  SDV_CUDA(launch_rmsnorm(bf(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn), bf(c->L.h), R, H,
+                          cf.rms_eps, status, s));
+  {  // gate/up + SwiGLU
+    GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, nt, status);
+    g.epi.out_bf16 = bf(c->L.act);
+    g.epi.ld_bf16 = F;
+    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
+  }
+  {  // down projection + residual
+    GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, nt, status);
+    g.epi.out_bf16 = bf(c->L.x2);
+    g.epi.resid = bf(c->L.x1);
+    g.epi.ld_bf16 = H;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
+  }
+  SDV_CUDA(launch_rmsnorm(bf(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final), bf(c->L.h), R, H,
+                          cf.rms_eps, status, s));
+  float* z = r->logits ? r->logits : ws_ptr<float>(c, c->L.z);
+  SDV_CUDA(mark(SDV_PHASE_LMHEAD));
+  {  // LM head + per-tile softmax statistics
+    GemmParams g = gemm_params(c, V, H, R, c->L.lm_tiles, nt, status);
+    g.epi.out_f32 = z;
+    g.epi.ld_f32 = V;
+    g.epi.stats = ws_ptr<float2>(c, c->L.lmstats);
+    g.epi.stats_ld = c->max_rows;
+    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, &c->tm_lm, &c->tm_lm, &c->tm_h[ni], g, gemm_grid(c, g), s));
+  }
+  int* accepted = r->accepted ? r->accepted : ws_ptr<int>(c, c->L.accepted);
+  int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
+  SDV_CUDA(mark(SDV_PHASE_ACCEPT));
+  {
+    AcceptParams a;
+    a.z = z;
+    a.tile_stats = ws_ptr<float2>(c, c->L.lmstats);
+    a.m_tiles = c->L.lm_tiles;
+    a.stats_ld = c->max_rows;
+    a.draft_probs = b->draft_probs;
+    a.uniforms = b->uniforms;
+    a.tokens = b->tokens;
+    a.draft_lens = b->draft_lens;
+    a.row_off = pp.t.row_off;
+    a.draft_off = pp.t.draft_off;
+    a.row_stats = ws_ptr<float2>(c, c->L.rowstats);
+    a.accepted = accepted;
+    a.final_tokens = final_tokens;
+    a.status = status;
+    a.B = b->B;
+    a.V = V;
+    SDV_CUDA(launch_accept(a, true, s));
+  }
+  if (r->probs) SDV_CUDA(launch_probs(z, ws_ptr<float2>(c, c->L.rowstats), r->probs, R, V, status, s));
+  SDV_CUDA(mark(SDV_PHASE_REALIGN));
+  RealignParams rp = realign_params(c, b, r, accepted, final_tokens);
+  SDV_CUDA(launch_realign(rp, s));
+  SDV_CUDA(mark(SDV_PHASES));
+  return SDV_OK;
+}
+
+sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_result* r, void* stream) {
+  if (!c || !probs || !batch_ok(c, b, false) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
+  if (!b->tokens || !b->uniforms || (b->G > 0 && !b->draft_probs)) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrologueParams pp = prologue_params(c, b, r->status, true);
+  SDV_CUDA(launch_prologue(pp, s));
+  int* accepted = r->accepted ? r->accepted : ws_ptr<int>(c, c->L.accepted);
+  int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
+  AcceptParams a;
+  a.probs = probs;
+  a.draft_probs = b->draft_probs;
+  a.uniforms = b->uniforms;
+  a.tokens = b->tokens;
+  a.draft_lens = b->draft_lens;
+  a.row_off = pp.t.row_off;
+  a.draft_off = pp.t.draft_off;
+  a.accepted = accepted;
+  a.final_tokens = final_tokens;
+  a.status = r->status;
+  a.B = b->B;
+  a.V = c->cfg.vocab;
+  SDV_CUDA(launch_accept(a, false, s));
+  RealignParams rp = realign_params(c, b, r, accepted, final_tokens);
+  SDV_CUDA(launch_realign(rp, s));
+  return SDV_OK;
+}
+
+sdv_status sdv_realign(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stream) {
+  if (!c || !batch_ok(c, b, false) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
+  if (!r->accepted || !r->final_tokens || !b->tokens) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrologueParams pp = prologue_params(c, b, r->status, false);
+  SDV_CUDA(launch_prologue(pp, s));
+  RealignParams rp = realign_params(c, b, r, r->accepted, r->final_tokens);
+  SDV_CUDA(launch_realign(rp, s));
+  return SDV_OK;
+}
+
+sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, float* y, int rows, void* stream) {
+  if (!c || !x || !y || rows <= 0 || rows > c->max_rows || which < 0 || which > 5) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const sdv_config& cf = c->cfg;
+  const int H = cf.hidden, QD = cf.n_q * cf.head_dim, F = cf.ffn;
+  const int NQKV = (cf.n_q + 2 * cf.n_kv) * cf.head_dim;
+  const CUtensorMap* wm = nullptr;
+  int N = 0, K = 0;
+  switch (which) {
+    case 0: wm = &c->tm_qkv; N = NQKV; K = H; break;
+    case 1: wm = &c->tm_o; N = H; K = QD; break;
+    case 2: wm = &c->tm_gate; N = F; K = H; break;
+    case 3: wm = &c->tm_up; N = F; K = H; break;
+    case 4: wm = &c->tm_down; N = H; K = F; break;
+    default: wm = &c->tm_lm; N = cf.vocab; K = H; break;
+  }
+  const int nt = gemm_tile_rows(rows);
+  CUtensorMap xm;
+  if (!encode_bf16_2d(&xm, x, rows, K, nt)) return SDV_ERR_CUDA;
+  // a private status word: the sentinel region after the attention schedule
+  int* status = ws_ptr<int>(c, c->L.sched) + 8;
+  SDV_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
+  GemmParams g = gemm_params(c, N, K, rows, (N + 127) / 128, nt, status);
+  g.epi.out_f32 = y;
+  g.epi.ld_f32 = N;
+  SDV_CUDA(launch_gemm(EPI_F32, nt, wm, wm, &xm, g, gemm_grid(c, g), s));
+  return SDV_OK;
+}
+
+sdv_status sdv_attention(sdv_ctx* c, const void* q, const sdv_batch* b, void* out, int* status, void* stream) {
+  if (!c || !q || !out || !status || !batch_ok(c, b, false) || !b->kv_pool) return SDV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PrologueParams pp = prologue_params(c, b, status, false);
+  SDV_CUDA(launch_prologue(pp, s));
+  return run_attention(c, b, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), status, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,384 @@
+// Block-causal GQA attention of the verify rows over each sequence's paged KV cache.
+//
+// Row i of sequence b sits at position L_b + i and attends to positions
+// 0 .. L_b + i of its own sequence: the whole cached context plus the draft
+// rows before it ("Speculative Decoding and Batching Compete for the Same
+// Compute Slack on RDNA4", section "What is the ragged tensor problem...":
+// every sequence keeps its own positions, masks and KV length).  Each
+// sequence's cache is read once for all of its rows and all query heads that
+// share a KV head, and that read does not amortise across the batch ("Why
+// Static Batching Wastes an RX 9070 XT Agent Swarm", section "The catch is
+// prefill, and it points back at admission"), so the kernel is bound by KV
+// bytes:
+//
+//  * work item = (sequence, KV head, chunk of pages); a device-side schedule
+//    sizes the chunks so that the items cover all SMs, whatever the mix of
+//    context lengths (a batch of one long sequence and a swarm of 128 alike);
+//  * a producer warp streams each (page, KV head) block -- 16 keys and 16
+//    values of head_dim -- with 128-byte-swizzled TMA loads into an 8-stage
+//    ring; three consumer warps each own 16 query vectors (draft rows x query
+//    heads of the group) and run QK^T and PV on bf16 mma.sync with an online
+//    softmax in fp32;
+//  * items that cover a whole sequence write the bf16 output directly; split
+//    sequences write (max, sum, unnormalised output) partials that a merge
+//    kernel combines (log-sum-exp in base 2).
+#include "common.cuh"
+#include "internal.h"
+
+namespace sdv {
+
+namespace {
+
+constexpr int kConsumers = 3;  // x 16 query vectors = kAttnQMax
+constexpr int kThreads = (kConsumers + 1) * kWarp;
+
+template <int D>
+struct ACfg {
+  static constexpr int STAGES = 8;
+  static constexpr int BOX = 64 * 16 * 2;             // one 64-wide half of 16 rows: 2 KB
+  static constexpr int HALVES = D / 64;
+  static constexpr int PAGE_BYTES = 2 * HALVES * BOX;  // K and V of one (page, kv head)
+  static constexpr int QLD = D + 8;                   // padded Q row (bf16 elements)
+  static constexpr int Q_BYTES = kAttnQMax * QLD * 2;
+  static constexpr int SMEM = 1024 + STAGES * PAGE_BYTES + Q_BYTES + 2 * STAGES * 8 + 64;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+struct Item {
+  int b, g, c, chunks, p0, p1, L, gamma, r0;
+};
+
+__device__ __forceinline__ Item decode_item(const AttnParams& p, int item, int chunk_pages) {
+  // slot = last b with item_off[b] <= item
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.item_off[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.b = lo;
+  it.chunks = p.chunks[lo];
+  const int rem = item - p.item_off[lo];
+  it.g = rem / it.chunks;
+  it.c = rem - it.g * it.chunks;
+  it.L = p.seq_lens[lo];
+  it.gamma = p.draft_lens[lo];
+  it.r0 = p.row_off[lo];
+  const int len = it.L + it.gamma + 1;
+  const int pages = (len + p.page - 1) / p.page;
+  it.p0 = it.c * chunk_pages;
+  it.p1 = min(pages, it.p0 + chunk_pages);
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
+  using C = ACfg<D>;
+  constexpr int KK = D / 16;  // k16 steps over the head dimension
+  constexpr int NF = D / 8;   // n8 fragments of the output
+  extern __shared__ uint8_t smem_raw[];
+  if (read_status(p.status) != 0) return;
+
+  uint8_t* smem = align1024(smem_raw);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + C::STAGES * C::PAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::PAGE_BYTES + C::Q_BYTES);
+  uint64_t* empty = full + C::STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int chunk_pages = p.sched[0];
+  const int total_items = p.sched[1];
+  const int group = p.n_q / p.n_kv;
+
+  if (warp == kConsumers) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool dead = false;
+      for (int item = blockIdx.x; item < total_items && !dead; item += gridDim.x) {
+        const Item it = decode_item(p, item, chunk_pages);
+        for (int pi = it.p0; pi < it.p1; ++pi) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            set_status(p.status, SDV_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          const int pg = p.page_table[(long long)it.b * p.max_pages + pi];
+          uint8_t* dst = smem + stage * C::PAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::PAGE_BYTES);
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h)
+              tma_load_5d(dst + (kv * C::HALVES + h) * C::BOX, &tmKV, &full[stage], h * 64, 0, kv, it.g, pg);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // tail: wait until the consumers have released every stage
+      for (int i = 0; i < C::STAGES && !dead; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1)) {
+          set_status(p.status, SDV_ERR_TIMEOUT);
+          break;
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  // a timed-out wait marks the CTA dead (see the GEMM kernel): no early return
+  bool dead = false;
+  const int g8 = lane >> 2, t = lane & 3;
+  const int mat = lane >> 3, rr = lane & 7;
+  const float scale = kLog2e / sqrtf(static_cast<float>(D));
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+    const Item it = decode_item(p, item, chunk_pages);
+    const int nqv = (it.gamma + 1) * group;
+
+    // Q tile: query vector v = row i * group + head-in-group
+    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < kAttnQMax * CPR; idx += kConsumers * kWarp) {
+      const int v = idx / CPR, ch = idx - v * CPR;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (v < nqv) {
+        const int i = v / group, h = it.g * group + (v - (v / group) * group);
+        val = *reinterpret_cast<const uint4*>(p.q + ((long long)(it.r0 + i) * p.n_q + h) * D + ch * 8);
+      }
+      *reinterpret_cast<uint4*>(qs + v * C::QLD + ch * 8) = val;
+    }
+    named_sync(1, kConsumers * kWarp);
+
+    const bool active = warp * 16 < nqv;
+    uint32_t qa[KK][4];
+    if (active) {
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+        const int row = warp * 16 + (mat & 1) * 8 + rr;
+        const int col = kk * 16 + (mat >> 1) * 8;
+        ldsm_x4(smem_u32(qs + row * C::QLD + col), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    // query positions of this thread's two rows
+    const int v0 = warp * 16 + g8, v1 = v0 + 8;
+    const int qpos0 = it.L + v0 / group, qpos1 = it.L + v1 / group;
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[NF][4];
+#pragma unroll
+    for (int nf = 0; nf < NF; ++nf) o[nf][0] = o[nf][1] = o[nf][2] = o[nf][3] = 0.f;
+
+    for (int pi = it.p0; pi < it.p1; ++pi) {
+      if (!dead && !mbar_wait(&full[stage], phase)) {
+        set_status(p.status, SDV_ERR_TIMEOUT);
+        dead = true;
+      }
+      if (active) {
+        const uint32_t kbase = smem_u32(smem + stage * C::PAGE_BYTES);
+        const uint32_t vbase = kbase + C::HALVES * C::BOX;
+        float s[2][4];
+#pragma unroll
+        for (int nf = 0; nf < 2; ++nf) s[nf][0] = s[nf][1] = s[nf][2] = s[nf][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KK; ++kk) {
+          const int key = (mat >> 1) * 8 + rr;
+          const int chunk = kk * 2 + (mat & 1);
+          const uint32_t addr = kbase + (chunk >> 3) * C::BOX + key * 128 + (((chunk & 7) ^ rr) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma_bf16(s[0], qa[kk], b0, b1);
+          mma_bf16(s[1], qa[kk], b2, b3);
+        }
+        // scale to base-2 logits and apply the block-causal mask
+        const int kp0 = pi * p.page;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nf = 0; nf < 2; ++nf)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kp = kp0 + nf * 8 + 2 * t + e;
+            s[nf][e] = kp <= qpos0 ? s[nf][e] * scale : -INFINITY;
+            s[nf][2 + e] = kp <= qpos1 ? s[nf][2 + e] * scale : -INFINITY;
+            mx0 = fmaxf(mx0, s[nf][e]);
+            mx1 = fmaxf(mx1, s[nf][2 + e]);
+          }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float base0 = n0 == -INFINITY ? 0.f : n0;
+        const float base1 = n1 == -INFINITY ? 0.f : n1;
+        const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
+        m0 = n0;
+        m1 = n1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nf = 0; nf < 2; ++nf)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            s[nf][e] = exp2f(s[nf][e] - base0);
+            s[nf][2 + e] = exp2f(s[nf][2 + e] - base1);
+            ps0 += s[nf][e];
+            ps1 += s[nf][2 + e];
+          }
+        l0 = l0 * a0 + ps0;
+        l1 = l1 * a1 + ps1;
+#pragma unroll
+        for (int nf = 0; nf < NF; ++nf) {
+          o[nf][0] *= a0;
+          o[nf][1] *= a0;
+          o[nf][2] *= a1;
+          o[nf][3] *= a1;
+        }
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+#pragma unroll
+        for (int nf = 0; nf < NF; nf += 2) {
+          const int key = (mat & 1) * 8 + rr;
+          const int chunk = nf + (mat >> 1);
+          const uint32_t addr = vbase + (chunk >> 3) * C::BOX + key * 128 + (((chunk & 7) ^ rr) << 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma_bf16(o[nf], pa, b0, b1);
+          mma_bf16(o[nf + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+
+    if (active) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+      l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+      if (it.chunks == 1) {
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int v = half ? v1 : v0;
+          if (v < nqv) {
+            const float inv = half ? i1 : i0;
+            const int i = v / group, h = it.g * group + (v - (v / group) * group);
+            __nv_bfloat16* dst = p.out + ((long long)(it.r0 + i) * p.n_q + h) * D;
+#pragma unroll
+            for (int nf = 0; nf < NF; ++nf) {
+              const int d = nf * 8 + 2 * t;
+              *reinterpret_cast<uint32_t*>(dst + d) =
+                  pack_bf16x2(o[nf][half * 2] * inv, o[nf][half * 2 + 1] * inv);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int v = half ? v1 : v0;
+          if (v < nqv) {
+            float* dst = p.part_o + ((long long)item * kAttnQMax + v) * D;
+#pragma unroll
+            for (int nf = 0; nf < NF; ++nf) {
+              const int d = nf * 8 + 2 * t;
+              *reinterpret_cast<float2*>(dst + d) = make_float2(o[nf][half * 2], o[nf][half * 2 + 1]);
+            }
+            if (t == 0)
+              p.part_ml[(long long)item * kAttnQMax + v] = make_float2(half ? m1 : m0, half ? l1 : l0);
+          }
+        }
+      }
+    }
+    named_sync(1, kConsumers * kWarp);  // Q tile is rewritten by the next item
+  }
+}
+
+// One warp per (row, query head) of a split sequence: combine the chunks.
+template <int D>
+__global__ void attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
+  if (read_status(p.status) != 0) return;
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= R * p.n_q) return;
+  const int r = wid / p.n_q, h = wid - (wid / p.n_q) * p.n_q;
+  const int b = row_seq[r];
+  const int chunks = p.chunks[b];
+  if (chunks == 1) return;
+  const int group = p.n_q / p.n_kv;
+  const int i = r - p.row_off[b];
+  const int g = h / group;
+  const int v = i * group + (h - g * group);
+  const int item0 = p.item_off[b] + g * chunks;
+  float M = -INFINITY;
+  for (int c = 0; c < chunks; ++c) M = fmaxf(M, p.part_ml[(long long)(item0 + c) * kAttnQMax + v].x);
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int c = 0; c < chunks; ++c) {
+    const float2 ml = p.part_ml[(long long)(item0 + c) * kAttnQMax + v];
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    L += w * ml.y;
+    const float* src = p.part_o + ((long long)(item0 + c) * kAttnQMax + v) * D;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += w * src[lane + 32 * e];
+  }
+  const float inv = 1.f / L;
+  __nv_bfloat16* dst = p.out + ((long long)r * p.n_q + h) * D;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = f2bf(acc[e] * inv);
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, int R, cudaStream_t stream,
+                     const int* row_seq) {
+  auto kern = attn_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ACfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, ACfg<D>::SMEM, stream>>>(*kv_map, p);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int warps = R * p.n_q;
+  attn_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p, row_seq, R);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_smem_bytes(int head_dim) { return head_dim == 64 ? ACfg<64>::SMEM : ACfg<128>::SMEM; }
+
+cudaError_t launch_attention_impl(int head_dim, const CUtensorMap* kv_map, const AttnParams& p, int grid, int R,
+                                  cudaStream_t stream, const int* row_seq) {
+  if (head_dim == 128) return launch_d<128>(kv_map, p, grid, R, stream, row_seq);
+  if (head_dim == 64) return launch_d<64>(kv_map, p, grid, R, stream, row_seq);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sdv

@@ -1,0 +1,412 @@
+// Weight-streaming GEMM for the verify step: y[r, n] = sum_k x[r, k] W[n, k].
+//
+// The verify pass multiplies a few hundred rows at most (sum over sequences of
+// gamma_b + 1) by every weight matrix of the layer and by the LM head, so it
+// is bound by reading the weights once from HBM ("Speculative Decoding at
+// High Batch Size", section "What does one speculative iteration actually
+// cost?": at small batch the step is bound by weight and KV reads that do not
+// depend on how many tokens are verified).  The kernel is built for that:
+//
+//  * one TMA producer warp streams 128-row x 64-k weight tiles (two 64-row
+//    boxes, 128-byte swizzle) and the matching activation tile into a deep
+//    shared-memory ring (7-10 stages, ~180 KB in flight per SM);
+//  * four consumer warps run bf16 mma.sync (m16n8k16, fp32 accumulate) with
+//    the weights as the 16-row A operand and the activations as the 8-column
+//    B operand, so a handful of rows costs no padding of the weight side;
+//  * work is split stream-K: the (tile, k-block) units of the whole matrix are
+//    cut into one contiguous range per CTA (one CTA per SM), so every SM
+//    streams the same number of bytes whatever the matrix shape.  A tile cut
+//    between CTAs is finished by the last CTA to arrive, which sums the
+//    partial tiles in a fixed order (deterministic, no spin-waits);
+//  * epilogues are fused: RoPE + K/V page scatter after QKV, residual add after
+//    O and down, silu(gate) * up after the gate/up pair, and logits plus
+//    per-tile softmax statistics after the LM head.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sdv {
+
+namespace {
+
+constexpr int BM = 128;               // weight rows per tile
+constexpr int BK = 64;                // k per stage: 128 bytes of bf16 per row
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int CONSUMERS = 4;
+constexpr int THREADS = (CONSUMERS + 1) * kWarp;
+
+template <int NT>
+struct Cfg {
+  static constexpr int B_BYTES = NT * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = NT == 64 ? 7 : (NT == 32 ? 9 : 10);
+  static constexpr int EPI_LD = BM + 4;  // padded row of the staged accumulator tile
+  static constexpr int EPI_BYTES = NT * EPI_LD * 4;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_BYTES + 2 * STAGES * 8 + 16;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// CTA c of P owns units [c*T/P, (c+1)*T/P); the CTA owning unit u:
+__device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) {
+  return static_cast<int>(((u + 1) * P - 1) / total);
+}
+
+template <int EPI, int NT>
+__device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* epi, int tm, int tn, int tid) {
+  constexpr int LD = Cfg<NT>::EPI_LD;
+  const EpiParams& e = p.epi;
+  if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
+    const int col = tm * BM + tid;
+    if (col < p.N) {
+      for (int n = 0; n < NT; ++n) {
+        const int r = tn * NT + n;
+        if (r >= p.R) break;
+        const float v = epi[n * LD + tid];
+        if constexpr (EPI == EPI_F32) {
+          e.out_f32[(long long)r * e.ld_f32 + col] = v;
+        } else {
+          const long long o = (long long)r * e.ld_bf16 + col;
+          e.out_bf16[o] = f2bf(v + bf2f(e.resid[o]));
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    const int j = tid & 63;
+    const int f = tm * 64 + j;
+    if (f < p.N) {
+      for (int n = tid >> 6; n < NT; n += 2) {
+        const int r = tn * NT + n;
+        if (r >= p.R) break;
+        const float gt = epi[n * LD + j];
+        const float up = epi[n * LD + 64 + j];
+        const float s = gt / (1.0f + expf(-gt));
+        e.out_bf16[(long long)r * e.ld_bf16 + f] = f2bf(s * up);
+      }
+    }
+  } else if constexpr (EPI == EPI_QKV) {
+    const int D = e.head_dim;
+    const int half = D >> 1;
+    const int f = tm * BM + tid;
+    if (f < p.N) {
+      const int hq = f / D;
+      const int j = f - hq * D;
+      const bool rot = hq < e.n_q + e.n_kv;
+      const int jj = j < half ? j : j - half;
+      for (int n = 0; n < NT; ++n) {
+        const int r = tn * NT + n;
+        if (r >= p.R) break;
+        float x = epi[n * LD + tid];
+        if (rot) {
+          const float c = e.rope_cs[((long long)r * half + jj) * 2];
+          const float s = e.rope_cs[((long long)r * half + jj) * 2 + 1];
+          if (j < half) {
+            const float y = epi[n * LD + tid + half];
+            x = x * c - y * s;
+          } else {
+            const float y = epi[n * LD + tid - half];
+            x = x * c + y * s;
+          }
+        }
+        const __nv_bfloat16 v = f2bf(x);
+        if (hq < e.n_q) {
+          e.q_out[(long long)r * (e.n_q * D) + f] = v;
+        } else {
+          const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
+          const int g = hq - e.n_q - kv * e.n_kv;
+          const int b = e.row_seq[r];
+          const int pos = e.row_pos[r];
+          const int pg = e.page_table[(long long)b * e.max_pages + pos / e.page];
+          const int slot = pos - (pos / e.page) * e.page;
+          const long long idx = ((((long long)pg * e.n_kv + g) * 2 + kv) * e.page + slot) * D + j;
+          e.kv_pool[idx] = v;
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_LMHEAD) {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int n = warp; n < NT; n += CONSUMERS) {
+      const int r = tn * NT + n;
+      if (r >= p.R) break;
+      float v[4];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = tm * BM + lane + 32 * i;
+        v[i] = epi[n * LD + lane + 32 * i];
+        if (col < p.N) {
+          e.out_f32[(long long)r * e.ld_f32 + col] = v[i];
+          mx = fmaxf(mx, v[i]);
+        }
+      }
+      mx = warp_max(mx);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = tm * BM + lane + 32 * i;
+        if (col < p.N) s += exp2f((v[i] - mx) * kLog2e);
+      }
+      s = warp_sum(s);
+      if (lane == 0) e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
+    }
+  }
+}
+
+template <int EPI, int NT>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
+  using C = Cfg<NT>;
+  constexpr int NF = NT / 8;  // n8 fragments
+  extern __shared__ uint8_t smem_raw[];
+  if (read_status(p.status) != 0) return;
+
+  uint8_t* smem = align1024(smem_raw);
+  float* epi = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::EPI_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  volatile int* flag = reinterpret_cast<volatile int*>(empty + C::STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CONSUMERS);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const long long total = (long long)p.m_tiles * p.n_tiles * p.kb;
+  const int P = gridDim.x;
+  const int c = blockIdx.x;
+  const long long u_begin = (long long)c * total / P;
+  const long long u_end = (long long)(c + 1) * total / P;
+
+  if (warp == CONSUMERS) {
+    // ---------------- producer: one elected lane issues all TMA loads ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool dead = false;
+      for (long long u = u_begin; u < u_end && !dead;) {
+        const int tile = static_cast<int>(u / p.kb);
+        const int k0 = static_cast<int>(u - (long long)tile * p.kb);
+        const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
+        const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+        const int rowA0 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM;
+        const int rowA1 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM + 64;
+        for (int k = k0; k < k1 && !dead; ++k) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            set_status(p.status, SDV_ERR_TIMEOUT);
+            dead = true;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::STAGE;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+          tma_load_2d_hint(sa, &tmA0, &full[stage], k * BK, rowA0, pol);
+          tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], k * BK, rowA1, pol);
+          tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        u += k1 - k0;
+      }
+      // tail: stay until the consumers have released every stage, so no copy
+      // into this CTA's shared memory is still in flight when it exits
+      for (int i = 0; i < C::STAGES && !dead; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1)) {
+          set_status(p.status, SDV_ERR_TIMEOUT);
+          break;
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  // A timed-out wait marks the CTA dead: no more waiting, no early return (the
+  // other consumer warps still meet at the named barriers); outputs are then
+  // garbage but every access stays in bounds and the status word says why.
+  bool dead = false;
+  const int g = lane >> 2, t = lane & 3;
+  const int mat = lane >> 3, rr = lane & 7;
+  float acc[2][NF][4];
+  int stage = 0;
+  uint32_t phase = 0;
+
+  for (long long u = u_begin; u < u_end;) {
+    const int tile = static_cast<int>(u / p.kb);
+    const int k0 = static_cast<int>(u - (long long)tile * p.kb);
+    const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
+    const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int nj = 0; nj < NF; ++nj)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[mi][nj][q] = 0.f;
+
+    for (int k = k0; k < k1; ++k) {
+      if (!dead && !mbar_wait(&full[stage], phase)) {
+        set_status(p.status, SDV_ERR_TIMEOUT);
+        dead = true;
+      }
+      const uint32_t a_base = smem_u32(smem + stage * C::STAGE);
+      const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          const int row = warp * 32 + mi * 16 + (mat & 1) * 8 + rr;
+          const int chunk = kk * 2 + (mat >> 1);
+          ldsm_x4(a_base + row * 128 + ((chunk ^ rr) << 4), a[mi][0], a[mi][1], a[mi][2], a[mi][3]);
+        }
+#pragma unroll
+        for (int nj = 0; nj < NF; nj += 2) {
+          const int nrow = (nj + (mat >> 1)) * 8 + rr;
+          const int chunk = kk * 2 + (mat & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(b_base + nrow * 128 + ((chunk ^ rr) << 4), b0, b1, b2, b3);
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            mma_bf16(acc[mi][nj], a[mi], b0, b1);
+            mma_bf16(acc[mi][nj + 1], a[mi], b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+
+    // ---------------- stream-K: tiles cut between CTAs ----------------
+    if (!(k0 == 0 && k1 == p.kb)) {
+      const long long tu = (long long)tile * p.kb;
+      const int c_first = cta_of_unit(tu, total, P);
+      const int c_last = cta_of_unit(tu + p.kb - 1, total, P);
+      const int my_slot = 2 * c + (tile == static_cast<int>(u_begin / p.kb) ? 0 : 1);
+      float4* dst = reinterpret_cast<float4*>(p.partials + (size_t)my_slot * BM * NT);
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < NF; ++nj)
+          __stcg(&dst[((warp * 2 + mi) * NF + nj) * 32 + lane],
+                 make_float4(acc[mi][nj][0], acc[mi][nj][1], acc[mi][nj][2], acc[mi][nj][3]));
+      __threadfence();
+      named_sync(1, CONSUMERS * kWarp);
+      if (threadIdx.x == 0) {
+        const int old = atomicAdd(&p.counters[tile], 1);
+        *flag = (old == c_last - c_first) ? 1 : 0;
+      }
+      named_sync(1, CONSUMERS * kWarp);
+      const bool last = *flag != 0;
+      if (!last) {
+        u += k1 - k0;
+        continue;
+      }
+      __threadfence();
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < NF; ++nj)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[mi][nj][q] = 0.f;
+      for (int cc = c_first; cc <= c_last; ++cc) {
+        const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
+        const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
+        const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)slot * BM * NT);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int nj = 0; nj < NF; ++nj) {
+            const float4 v = __ldcg(&src[((warp * 2 + mi) * NF + nj) * 32 + lane]);
+            acc[mi][nj][0] += v.x;
+            acc[mi][nj][1] += v.y;
+            acc[mi][nj][2] += v.z;
+            acc[mi][nj][3] += v.w;
+          }
+      }
+      if (threadIdx.x == 0) p.counters[tile] = 0;  // ready for the next launch
+    }
+
+    // ---------------- fused epilogue ----------------
+    constexpr int LD = C::EPI_LD;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+      for (int nj = 0; nj < NF; ++nj) {
+        const int m = warp * 32 + mi * 16 + g;
+        const int n = nj * 8 + 2 * t;
+        epi[n * LD + m] = acc[mi][nj][0];
+        epi[(n + 1) * LD + m] = acc[mi][nj][1];
+        epi[n * LD + m + 8] = acc[mi][nj][2];
+        epi[(n + 1) * LD + m + 8] = acc[mi][nj][3];
+      }
+    named_sync(1, CONSUMERS * kWarp);
+    epilogue_pass<EPI, NT>(p, epi, tm, tn, threadIdx.x);
+    named_sync(1, CONSUMERS * kWarp);
+    u += k1 - k0;
+  }
+}
+
+template <int EPI, int NT>
+cudaError_t launch_t(const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x, const GemmParams& p,
+                     int grid, cudaStream_t stream) {
+  auto kern = gemm_ws_kernel<EPI, NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT>::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, THREADS, Cfg<NT>::SMEM, stream>>>(*a0, *a1, *x, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_nt(int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
+                      const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (nt) {
+    case 16: return launch_t<EPI, 16>(a0, a1, x, p, grid, stream);
+    case 32: return launch_t<EPI, 32>(a0, a1, x, p, grid, stream);
+    case 64: return launch_t<EPI, 64>(a0, a1, x, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int gemm_tile_rows(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+
+size_t gemm_smem_bytes(int nt, int /*int4*/) {
+  switch (nt) {
+    case 16: return Cfg<16>::SMEM;
+    case 32: return Cfg<32>::SMEM;
+    default: return Cfg<64>::SMEM;
+  }
+}
+
+cudaError_t launch_gemm(int epi, int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
+                        const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (epi) {
+    case EPI_F32: return launch_nt<EPI_F32>(nt, a0, a1, x, p, grid, stream);
+    case EPI_RESID: return launch_nt<EPI_RESID>(nt, a0, a1, x, p, grid, stream);
+    case EPI_SWIGLU: return launch_nt<EPI_SWIGLU>(nt, a0, a1, x, p, grid, stream);
+    case EPI_QKV: return launch_nt<EPI_QKV>(nt, a0, a1, x, p, grid, stream);
+    case EPI_LMHEAD: return launch_nt<EPI_LMHEAD>(nt, a0, a1, x, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sdv

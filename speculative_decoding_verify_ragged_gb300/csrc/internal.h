@@ -1,0 +1,175 @@
+// Internal host-side interfaces between the C-ABI glue and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sdv.h"
+
+namespace sdv {
+
+// ---------------------------------------------------------------------------
+// weight-streaming GEMM  y[r, n] = sum_k x[r, k] * W[n, k]
+// ---------------------------------------------------------------------------
+
+enum Epi : int {
+  EPI_F32 = 0,     // y fp32, no rounding
+  EPI_RESID = 1,   // out bf16 = round(acc + resid)
+  EPI_SWIGLU = 2,  // tile = 64 gate rows + 64 up rows of the same features: out = round(silu(g) * u)
+  EPI_QKV = 3,     // RoPE on q/k heads, q -> q buffer, k/v -> KV pages at (seq, pos)
+  EPI_LMHEAD = 4   // logits fp32 + per (vocab tile, row) max and sum of exp
+};
+
+struct EpiParams {
+  float* out_f32 = nullptr;  // F32 / LMHEAD: [R, ld_f32]
+  long long ld_f32 = 0;
+  __nv_bfloat16* out_bf16 = nullptr;  // RESID / SWIGLU: [R, ld_bf16]
+  const __nv_bfloat16* resid = nullptr;
+  int ld_bf16 = 0;
+  // QKV
+  __nv_bfloat16* q_out = nullptr;  // [R, n_q * head_dim]
+  __nv_bfloat16* kv_pool = nullptr;
+  const int* page_table = nullptr;
+  int max_pages = 0;
+  const int* row_seq = nullptr;
+  const int* row_pos = nullptr;
+  const float* rope_cs = nullptr;  // [R, head_dim/2, 2] (cos, sin)
+  int n_q = 0, n_kv = 0, head_dim = 0, page = 0;
+  // LMHEAD
+  float2* stats = nullptr;  // [m_tiles, stats_ld]
+  int stats_ld = 0;
+};
+
+struct GemmParams {
+  int N = 0;        // output features (SWIGLU: ffn features)
+  int K = 0;
+  int R = 0;        // activation rows
+  int m_tiles = 0;  // weight tiles (128 rows; SWIGLU: 64 features)
+  int n_tiles = 0;  // activation-row tiles
+  int kb = 0;       // k-blocks of 64 per tile
+  int int4 = 0;     // weights are int4 group-32
+  float* partials = nullptr;  // stream-K partial tiles [2 * grid, 128 * NT]
+  int* counters = nullptr;    // per-tile arrival counters, zero between launches
+  int* status = nullptr;
+  EpiParams epi;
+};
+
+// Choose the activation tile for R rows (16, 32 or 64).
+int gemm_tile_rows(int R);
+// Launch the weight-streaming GEMM. a0/a1: weight maps for the two 64-row
+// halves of a 128-row tile (same map for plain GEMMs); x: activation map
+// whose box is (64, nt); s0/s1: int4 scale maps (nullptr for bf16).
+cudaError_t launch_gemm(int epi, int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
+                        const GemmParams& p, int grid, cudaStream_t stream);
+size_t gemm_smem_bytes(int nt, int int4);
+
+// ---------------------------------------------------------------------------
+// attention over the paged cache
+// ---------------------------------------------------------------------------
+
+struct AttnParams {
+  const __nv_bfloat16* q = nullptr;  // [R, n_q, D]
+  __nv_bfloat16* out = nullptr;      // [R, n_q * D]
+  const int* seq_lens = nullptr;
+  const int* draft_lens = nullptr;
+  const int* row_off = nullptr;   // [B+1]
+  const int* page_table = nullptr;
+  int max_pages = 0;
+  const int* item_off = nullptr;  // [B+1] first work item of each slot
+  const int* chunks = nullptr;    // [B] key chunks per (slot, kv head)
+  const int* sched = nullptr;     // [0] chunk pages, [1] total items
+  float* part_o = nullptr;        // [items, QMAX, D]
+  float2* part_ml = nullptr;      // [items, QMAX]
+  int* status = nullptr;
+  int B = 0, n_q = 0, n_kv = 0, page = 0;
+};
+constexpr int kAttnQMax = 48;  // query vectors per (slot, kv head): (gamma+1) * group
+
+// Attention kernel plus the merge of split sequences (row_seq [R] maps rows to slots).
+cudaError_t launch_attention_impl(int head_dim, const CUtensorMap* kv_map, const AttnParams& p, int grid, int R,
+                                  cudaStream_t stream, const int* row_seq);
+size_t attention_smem_bytes(int head_dim);
+
+// ---------------------------------------------------------------------------
+// small kernels of the step
+// ---------------------------------------------------------------------------
+
+struct StepTables {
+  int* row_off = nullptr;    // [B+1]
+  int* draft_off = nullptr;  // [B+1]
+  int* row_seq = nullptr;    // [R]
+  int* row_pos = nullptr;    // [R]
+  int* chunks = nullptr;     // [B]
+  int* item_off = nullptr;   // [B+1]
+  int* sched = nullptr;      // [4]
+  float* rope_cs = nullptr;  // [R, D/2, 2]
+};
+
+struct PrologueParams {
+  StepTables t;
+  const int* seq_lens = nullptr;
+  const int* draft_lens = nullptr;
+  const int* tokens = nullptr;
+  const int* page_table = nullptr;
+  const int* num_pages = nullptr;
+  int* status = nullptr;
+  int B = 0, R = 0, G = 0, gamma_max = 0, vocab = 0, page = 0, max_pages = 0, pool_pages = 0;
+  int n_kv = 0, head_dim = 0, target_items = 0;
+  float rope_theta = 0.f;
+  int check_tokens = 1;
+};
+cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
+
+// x0 = emb[tokens], h = RMSNorm(x0) * gain, plus each row's rotary (cos, sin) table.
+cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
+                                   __nv_bfloat16* x0, __nv_bfloat16* h, const int* row_pos, float* rope_cs, int R,
+                                   int H, int head_dim, float eps, float theta, const int* status,
+                                   cudaStream_t stream);
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* h, int R, int H,
+                           float eps, const int* status, cudaStream_t stream);
+
+struct AcceptParams {
+  const float* z = nullptr;        // logits [R, V] (from_logits)
+  const float2* tile_stats = nullptr;  // [m_tiles, stats_ld]
+  int m_tiles = 0, stats_ld = 0;
+  const float* probs = nullptr;    // [R, V] (given probabilities)
+  const float* draft_probs = nullptr;
+  const float* uniforms = nullptr;
+  const int* tokens = nullptr;
+  const int* draft_lens = nullptr;
+  const int* row_off = nullptr;
+  const int* draft_off = nullptr;
+  float2* row_stats = nullptr;     // [R] (max, sum) written when from logits
+  int* accepted = nullptr;
+  int* final_tokens = nullptr;
+  int* status = nullptr;
+  int B = 0, V = 0;
+};
+cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream);
+cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, int R, int V, const int* status,
+                         cudaStream_t stream);
+
+struct RealignParams {
+  const int* seq_lens = nullptr;
+  const int* draft_lens = nullptr;
+  const int* tokens = nullptr;
+  const int* row_off = nullptr;
+  const int* accepted = nullptr;
+  const int* final_tokens = nullptr;
+  int* page_table = nullptr;
+  int* num_pages = nullptr;
+  int* free_pages = nullptr;
+  const int* num_free_in = nullptr;
+  int* num_free_out = nullptr;
+  const int* gen_counts = nullptr;
+  const int* gen_limits = nullptr;
+  sdv_result res;
+  int B = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0;
+};
+cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream);
+
+// count of kernels launched by this library
+void note_launch(int n = 1);
+
+}  // namespace sdv

@@ -43,8 +43,7 @@ S_WEIGHTS, S_KV, S_TOKENS, S_Q, S_U, S_SEQ = range(6)
 
 def rng(workload: int, stream: int, sub: int = 0) -> np.random.Generator:
     """Philox generator for (workload, stream, sub-stream)."""
-    key = (((0x5D5EED00 + workload) << 8) | stream) << 32 | (sub & 0xFFFFFFFF)
-    return np.random.Generator(np.random.Philox(key=key))
+    return np.random.Generator(np.random.Philox(key=_key(workload, stream, sub)))
 
 
 # ---------------------------------------------------------------------------
@@ -58,13 +57,45 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return (b >> np.uint32(16)).astype(np.uint16)
 
 
-def normal_bf16(g: np.random.Generator, shape, std: float, mean: float = 0.0) -> np.ndarray:
-    x = g.standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        x *= np.float32(std)
-    if mean != 0.0:
-        x += np.float32(mean)
-    return f32_to_bf16_bits(x)
+def _key(workload: int, stream: int, sub: int = 0) -> int:
+    return (((0x5D5EED00 + workload) << 8) | stream) << 32 | (sub & 0xFFFFFFFF)
+
+
+def normal_bf16(key: int, shape, std: float, mean: float = 0.0, chunk: int = 1 << 22) -> np.ndarray:
+    """bf16 bits of N(mean, std^2) draws.
+
+    The array is cut into chunks of ``chunk`` elements; chunk i is drawn from
+    Philox(key) jumped i + 1 times (independent streams), so the values do not
+    depend on how many threads fill the chunks.
+    """
+    from concurrent.futures import ThreadPoolExecutor
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    base = np.random.Philox(key=key)
+
+    def fill(i):
+        c0, c1 = i * chunk, min(n, (i + 1) * chunk)
+        g = np.random.Generator(base.jumped(i + 1))
+        x = g.standard_normal(size=c1 - c0, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        if mean != 0.0:
+            x += np.float32(mean)
+        b = x.view(np.uint32)
+        t = b >> np.uint32(16)
+        np.bitwise_and(t, np.uint32(1), out=t)
+        np.add(t, np.uint32(0x7FFF), out=t)
+        np.add(b, t, out=b)
+        np.right_shift(b, np.uint32(16), out=b)
+        out[c0:c1] = b
+
+    nchunks = (n + chunk - 1) // chunk
+    if nchunks == 1:
+        fill(0)
+    else:
+        with ThreadPoolExecutor(max_workers=min(16, nchunks)) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out.reshape(shape)
 
 
 def uniform24(g: np.random.Generator, n: int) -> np.ndarray:
@@ -140,7 +171,7 @@ def make_weights(dims: dict, workload: int, fmt: str = "bf16", std: float = 0.02
     def nxt():
         nonlocal sub
         sub += 1
-        return rng(workload, S_WEIGHTS, sub)
+        return _key(workload, S_WEIGHTS, sub)
 
     emb = normal_bf16(nxt(), (V, H), std)
     # gains near one (not exactly one, so a dropped gain is visible)
@@ -154,7 +185,7 @@ def make_weights(dims: dict, workload: int, fmt: str = "bf16", std: float = 0.02
         if fmt == "bf16":
             proj[name] = normal_bf16(nxt(), (n, k), std)
         elif fmt == "int4":
-            proj[name] = _int4_proj(nxt(), n, k, std)
+            proj[name] = _int4_proj(np.random.Generator(np.random.Philox(key=nxt())), n, k, std)
         else:
             raise ValueError(fmt)
     return Weights(dims=dims, fmt=fmt, emb=emb, g_attn=g_attn, g_ffn=g_ffn,
@@ -266,7 +297,7 @@ def fill_kv_normal(kv: np.ndarray, workload: int, chunk: int = 512) -> None:
     """Fill a KV pool with bf16 N(0,1), one Philox sub-stream per chunk of pages."""
     for c0 in range(0, kv.shape[0], chunk):
         c1 = min(kv.shape[0], c0 + chunk)
-        kv[c0:c1] = normal_bf16(rng(workload, S_KV, c0 // chunk), kv[c0:c1].shape, 1.0)
+        kv[c0:c1] = normal_bf16(_key(workload, S_KV, c0 // chunk), kv[c0:c1].shape, 1.0)
 
 
 def row_offsets(draft_lens: np.ndarray) -> np.ndarray:

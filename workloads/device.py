@@ -1,0 +1,76 @@
+"""Move the seeded host inputs to a CUDA device and allocate result buffers.
+
+Plumbing for the tests and the bench (torch tensors for device memory); no
+arithmetic of the verify step happens here.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import NINE_B, RMS_EPS, ROPE_THETA, TINY, Batch, Weights  # noqa: F401
+
+
+def _t(a: np.ndarray, dev, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(dev, non_blocking=False)
+
+
+def config(dims: dict, gamma_max: int, fmt: str = "bf16") -> dict:
+    return dict(hidden=dims["hidden"], n_q=dims["n_q"], n_kv=dims["n_kv"], head_dim=dims["head_dim"],
+                ffn=dims["ffn"], vocab=dims["vocab"], page_size=dims["page"], gamma_max=gamma_max,
+                weight_format=0 if fmt == "bf16" else 1, rms_eps=RMS_EPS, rope_theta=ROPE_THETA)
+
+
+def weights_to_device(W: Weights, dev="cuda") -> dict:
+    bf = torch.bfloat16
+    d = dict(emb=_t(W.emb.view(np.int16), dev, bf), w_lm=_t(W.w_lm.view(np.int16), dev, bf),
+             g_attn=_t(W.g_attn.view(np.int16), dev, bf), g_ffn=_t(W.g_ffn.view(np.int16), dev, bf),
+             g_final=_t(W.g_final.view(np.int16), dev, bf))
+    for name in ("qkv", "o", "gate", "up", "down"):
+        w = W.proj[name]
+        if isinstance(w, tuple):
+            d["w_" + name] = _t(w[0], dev)
+            d["s_" + name] = _t(w[1].view(np.int16), dev, torch.float16)
+        else:
+            d["w_" + name] = _t(w.view(np.int16), dev, bf)
+    return d
+
+
+def batch_to_device(b: Batch, dev="cuda") -> dict:
+    i32 = np.int32
+    d = dict(B=b.B, R=b.R, G=b.G,
+             seq_lens=_t(b.seq_lens.astype(i32), dev), draft_lens=_t(b.draft_lens.astype(i32), dev),
+             tokens=_t(b.tokens.astype(i32), dev),
+             draft_probs=_t(b.draft_probs.astype(np.float32).reshape(max(b.G, 0), -1), dev),
+             uniforms=_t(b.uniforms.astype(np.float32), dev),
+             kv_pool=_t(b.kv_pool.view(np.int16), dev, torch.bfloat16),
+             num_pool_pages=int(b.kv_pool.shape[0]),
+             page_table=_t(b.page_table.astype(i32), dev), num_pages=_t(b.num_pages.astype(i32), dev),
+             free_pages=_t(b.free_pages.astype(i32), dev),
+             num_free_in=_t(np.array([b.num_free], i32), dev))
+    d["num_free_out"] = d["num_free_in"]
+    if b.gen_counts is not None:
+        d["gen_counts"] = _t(b.gen_counts.astype(i32), dev)
+    if b.gen_limits is not None:
+        d["gen_limits"] = _t(b.gen_limits.astype(i32), dev)
+    return d
+
+
+def alloc_result(B: int, R: int, V: int, gamma_max: int, max_pages: int, dev="cuda",
+                 logits: bool = False, probs: bool = False, next_view: bool = True) -> dict:
+    z = lambda n: torch.zeros(n, dtype=torch.int32, device=dev)  # noqa: E731
+    r = dict(accepted=z(B), final_tokens=z(B), emitted_tokens=z(R), emitted_offsets=z(B + 1),
+             new_seq_lens=z(B), finished=z(B), new_gen_counts=z(B),
+             accept_tested=z(max(gamma_max, 1)), accept_accepted=z(max(gamma_max, 1)), status=z(1))
+    if next_view:
+        r.update(next_src=z(B), num_live=z(1), next_seq_lens=z(B), next_num_pages=z(B),
+                 next_page_table=torch.full((B, max_pages), -1, dtype=torch.int32, device=dev),
+                 next_gen_counts=z(B))
+    if logits:
+        r["logits"] = torch.zeros((R, V), dtype=torch.float32, device=dev)
+    if probs:
+        r["probs"] = torch.zeros((R, V), dtype=torch.float32, device=dev)
+    return r
