@@ -181,12 +181,15 @@ sdv_status sdv_realign(sdv_ctx *ctx, const sdv_batch *batch, sdv_result *result,
 
 /* y = x W^T for one of the context's projections, fp32 output without
  * rounding (parity tests of the weight-streaming GEMM).  which: 0 qkv, 1 o,
- * 2 gate, 3 up, 4 down, 5 lm_head.  x bf16 [rows, K] (device), y fp32
- * [rows, N] (device).  rows <= the context's max_rows. */
-sdv_status sdv_linear(sdv_ctx *ctx, int which, const void *x, float *y, int rows, void *stream);
+ * 2 gate, 3 up, 4 down, 5 lm_head.  x [rows, K] (device): x_format 0 = bf16,
+ * 1 = fp32 (each value enters the MMAs as a bf16 hi + lo pair, the path the
+ * step's layer GEMMs take).  y fp32 [rows, N] (device).  rows <= max_rows.
+ * The GEMM's own status word is internal: a device-side timeout cannot be
+ * read back from this entry point (the step's entry points report it). */
+sdv_status sdv_linear(sdv_ctx *ctx, int which, const void *x, int x_format, float *y, int rows, void *stream);
 
-/* Step (b) alone: q bf16 [R, n_q, head_dim] already rotated, the cache
- * already holding every row's K/V at L_b + i.  out bf16 [R, n_q*head_dim].
+/* Step (b) alone: q fp32 [R, n_q, head_dim] already rotated, the cache
+ * already holding every row's K/V at L_b + i.  out fp32 [R, n_q*head_dim].
  * Uses batch->seq_lens, draft_lens, page_table, kv_pool, B, R. */
 sdv_status sdv_attention(sdv_ctx *ctx, const void *q, const sdv_batch *batch, void *out,
                          int *status, void *stream);

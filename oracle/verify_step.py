@@ -34,11 +34,12 @@ Readings where the pages are silent:
   biases, rotate-half RoPE (theta 1e6) on q and k at absolute position, GQA
   with n_q / n_kv query heads per KV head, SwiGLU FFN, final RMSNorm, untied
   LM head, temperature 1.
-* Storage points: every intermediate the GPU stores as bf16 is rounded to
-  bf16 here too (round to nearest even): the normed inputs, q/k/v after RoPE,
-  the attention output, the residual stream after each residual add, the
-  SwiGLU product.  Logits and probabilities are produced in float64 and
-  returned as float32.
+* Storage points: weights, embeddings and the KV cache are bf16, so K and V
+  of every verified row are rounded to bf16 (round to nearest even) when they
+  enter the cache, and the final normed row is rounded to bf16 as the LM
+  head's input.  Every other intermediate (q, the attention output, the
+  residual stream, the norms, the SwiGLU product) is carried unrounded.
+  Logits and probabilities are produced in float64 and returned as float32.
 * Rows: row 0 of sequence b carries the last committed token at position L_b
   (not yet in the cache), row i the draft token i at position L_b + i; all
   gamma_b + 1 rows write K/V at their positions; row i attends to positions
@@ -233,14 +234,14 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
 
     # embedding + attention pre-norm
     x0 = bf16_to_f64(weights.emb[tok])
-    h1 = round_bf16(rmsnorm(x0, bf16_to_f64(weights.g_attn), eps))
+    h1 = rmsnorm(x0, bf16_to_f64(weights.g_attn), eps)
 
-    # fused QKV projection, RoPE on q and k, bf16 storage
+    # fused QKV projection, RoPE on q and k; K and V enter the bf16 cache
     qkv = linear(h1, weights.proj["qkv"])
     q = qkv[:, : nq * d].reshape(-1, nq, d)
     k = qkv[:, nq * d: (nq + nkv) * d].reshape(-1, nkv, d)
     v = qkv[:, (nq + nkv) * d:].reshape(-1, nkv, d)
-    q = round_bf16(rope(q, row_pos, theta))
+    q = rope(q, row_pos, theta)
     k = round_bf16(rope(k, row_pos, theta))
     v = round_bf16(v)
 
@@ -278,17 +279,17 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
         for h in range(nq):
             g = h // group
             o[n, h] = attention_one(q[n, h], Kc[g, : t + 1], Vc[g, : t + 1])
-    o = round_bf16(o.reshape(len(rows), nq * d))
+    o = o.reshape(len(rows), nq * d)
 
     # output projection + residual
-    x1 = round_bf16(x0 + linear(o, weights.proj["o"]))
+    x1 = x0 + linear(o, weights.proj["o"])
     # FFN pre-norm, SwiGLU, down projection + residual
-    h2 = round_bf16(rmsnorm(x1, bf16_to_f64(weights.g_ffn), eps))
+    h2 = rmsnorm(x1, bf16_to_f64(weights.g_ffn), eps)
     gate = linear(h2, weights.proj["gate"])
     up = linear(h2, weights.proj["up"])
-    act = round_bf16(silu(gate) * up)
-    x2 = round_bf16(x1 + linear(act, weights.proj["down"]))
-    # final norm + LM head + softmax
+    act = silu(gate) * up
+    x2 = x1 + linear(act, weights.proj["down"])
+    # final norm (bf16 LM-head input) + LM head + softmax
     h3 = round_bf16(rmsnorm(x2, bf16_to_f64(weights.g_final), eps))
     logits = linear(h3, weights.w_lm)
     probs = softmax(logits)

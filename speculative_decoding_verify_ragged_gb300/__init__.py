@@ -136,7 +136,10 @@ class VerifyEngine:
                     "sdv_realign")
 
     def linear(self, which: int, x, y, stream=None):
-        self._check(self.lib.sdv_linear(self.handle, int(which), _ptr(x), _ptr(y), int(x.shape[0]),
+        """y = x W^T (fp32); x bf16 or fp32 [rows, K]."""
+        import torch
+        fmt = 1 if x.dtype == torch.float32 else 0
+        self._check(self.lib.sdv_linear(self.handle, int(which), _ptr(x), fmt, _ptr(y), int(x.shape[0]),
                                         _stream(stream)), "sdv_linear")
 
     def attention(self, q, batch: dict, out, status, stream=None):

@@ -91,7 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_realign.restype = c_int
     lib.sdv_realign.argtypes = [c_void_p, P(SdvBatch), P(SdvResult), c_void_p]
     lib.sdv_linear.restype = c_int
-    lib.sdv_linear.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p]
+    lib.sdv_linear.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]
     lib.sdv_attention.restype = c_int
     lib.sdv_attention.argtypes = [c_void_p, c_void_p, P(SdvBatch), c_void_p, c_void_p, c_void_p]
     lib.sdv_set_phase_events.restype = c_int

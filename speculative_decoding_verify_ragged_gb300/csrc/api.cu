@@ -35,7 +35,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope;
-  size_t x0, h, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
+  size_t x0, h, h3, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, total;
   int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
 };
@@ -93,13 +93,15 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.item_off = take((B + 1) * 4);
   L.sched = take(64);
   L.rope = take(R * (c.head_dim / 2) * 2 * 4);
-  L.x0 = take(R * H * 2);
-  L.h = take(R * H * 2);
-  L.q = take(R * QD * 2);
-  L.attn = take(R * QD * 2);
-  L.x1 = take(R * H * 2);
-  L.act = take(R * F * 2);
-  L.x2 = take(R * H * 2);
+  // activations are carried in fp32; the LM head reads a bf16 copy of the final norm
+  L.x0 = take(R * H * 4);
+  L.h = take(R * H * 4);
+  L.h3 = take(R * H * 2);
+  L.q = take(R * QD * 4);
+  L.attn = take(R * QD * 4);
+  L.x1 = take(R * H * 4);
+  L.act = take(R * F * 4);
+  L.x2 = take(R * H * 4);
   L.z = take(R * V * 4);
   L.lmstats = take(static_cast<size_t>(L.lm_tiles) * R * 8);
   L.rowstats = take(R * 8);
@@ -143,6 +145,19 @@ static bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 matrix [rows, cols], box = (32 cols, box_rows), 128-byte swizzle.
+static bool encode_f32_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // KV pool [pages, n_kv, 2, page, D] as a 5-D tensor; box = 64 of D x 16 slots.
 static bool encode_kv(CUtensorMap* m, const void* base, const sdv_config& c, int pool_pages) {
   auto fn = encode_fn();
@@ -170,7 +185,7 @@ struct sdv_ctx {
   uint8_t* ws;
   Layout L;
   CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
-  CUtensorMap tm_h[3], tm_attn[3], tm_act[3];
+  CUtensorMap tm_h[3], tm_attn[3], tm_act[3], tm_h3[3];
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -223,9 +238,10 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
             encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
   const int nts[3] = {16, 32, 64};
   for (int i = 0; i < 3 && ok; ++i) {
-    ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, max_rows, H, nts[i]) &&
-         encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, max_rows, QD, nts[i]) &&
-         encode_bf16_2d(&c->tm_act[i], c->ws + L.act, max_rows, F, nts[i]);
+    ok = encode_f32_2d(&c->tm_h[i], c->ws + L.h, max_rows, H, nts[i]) &&
+         encode_f32_2d(&c->tm_attn[i], c->ws + L.attn, max_rows, QD, nts[i]) &&
+         encode_f32_2d(&c->tm_act[i], c->ws + L.act, max_rows, F, nts[i]) &&
+         encode_bf16_2d(&c->tm_h3[i], c->ws + L.h3, max_rows, H, nts[i]);
   }
   if (!ok) {
     delete c;
@@ -335,8 +351,8 @@ static int gemm_grid(sdv_ctx* c, const GemmParams& g) {
   return static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
 }
 
-static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const __nv_bfloat16* q, __nv_bfloat16* out,
-                                int* status, cudaStream_t s) {
+static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, float* out, int* status,
+                                cudaStream_t s) {
   CUtensorMap kv;
   if (!encode_kv(&kv, b->kv_pool, c->cfg, b->num_pool_pages)) return SDV_ERR_CUDA;
   AttnParams a;
@@ -406,19 +422,19 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   int* status = r->status;
   const int nt = gemm_tile_rows(R);
   const int ni = nt_index(nt);
-  auto bf = [&](size_t off) { return ws_ptr<__nv_bfloat16>(c, off); };
+  auto f32 = [&](size_t off) { return ws_ptr<float>(c, off); };
   auto mark = [&](int k) -> cudaError_t { return c->timing ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess; };
 
   SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
   PrologueParams pp = prologue_params(c, b, status, true);
   SDV_CUDA(launch_prologue(pp, s));
   SDV_CUDA(launch_embed_norm_rope(b->tokens, static_cast<const __nv_bfloat16*>(c->w.emb),
-                                  static_cast<const __nv_bfloat16*>(c->w.g_attn), bf(c->L.x0), bf(c->L.h),
+                                  static_cast<const __nv_bfloat16*>(c->w.g_attn), f32(c->L.x0), f32(c->L.h),
                                   pp.t.row_pos, pp.t.rope_cs, R, H, D, cf.rms_eps, cf.rope_theta, status, s));
   SDV_CUDA(mark(SDV_PHASE_QKV));
   {  // fused QKV + RoPE + KV append
     GemmParams g = gemm_params(c, NQKV, H, R, (NQKV + 127) / 128, nt, status);
-    g.epi.q_out = bf(c->L.q);
+    g.epi.out_f32 = f32(c->L.q);
     g.epi.kv_pool = static_cast<__nv_bfloat16*>(b->kv_pool);
     g.epi.page_table = b->page_table;
     g.epi.max_pages = b->max_pages_per_seq;
@@ -429,39 +445,39 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.n_kv = cf.n_kv;
     g.epi.head_dim = D;
     g.epi.page = cf.page_size;
-    SDV_CUDA(launch_gemm(EPI_QKV, nt, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(launch_gemm(EPI_QKV, nt, true, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
   }
   SDV_CUDA(mark(SDV_PHASE_ATTN));
   {
-    sdv_status st = run_attention(c, b, bf(c->L.q), bf(c->L.attn), status, s);
+    sdv_status st = run_attention(c, b, f32(c->L.q), f32(c->L.attn), status, s);
     if (st != SDV_OK) return st;
   }
   SDV_CUDA(mark(SDV_PHASE_O));
   {  // O projection + residual
     GemmParams g = gemm_params(c, H, QD, R, (H + 127) / 128, nt, status);
-    g.epi.out_bf16 = bf(c->L.x1);
-    g.epi.resid = bf(c->L.x0);
-    g.epi.ld_bf16 = H;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
+    g.epi.out_f32 = f32(c->L.x1);
+    g.epi.resid_f32 = f32(c->L.x0);
+    g.epi.ld_f32 = H;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, true, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
   }
   SDV_CUDA(mark(SDV_PHASE_FFN));
-  SDV_CUDA(launch_rmsnorm(bf(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn), bf(c->L.h), R, H,
-                          cf.rms_eps, status, s));
+  SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn), f32(c->L.h), nullptr, R,
+                          H, cf.rms_eps, status, s));
   {  // gate/up + SwiGLU
     GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, nt, status);
-    g.epi.out_bf16 = bf(c->L.act);
-    g.epi.ld_bf16 = F;
-    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    g.epi.out_f32 = f32(c->L.act);
+    g.epi.ld_f32 = F;
+    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, true, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
   }
   {  // down projection + residual
     GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, nt, status);
-    g.epi.out_bf16 = bf(c->L.x2);
-    g.epi.resid = bf(c->L.x1);
-    g.epi.ld_bf16 = H;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
+    g.epi.out_f32 = f32(c->L.x2);
+    g.epi.resid_f32 = f32(c->L.x1);
+    g.epi.ld_f32 = H;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, true, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
   }
-  SDV_CUDA(launch_rmsnorm(bf(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final), bf(c->L.h), R, H,
-                          cf.rms_eps, status, s));
+  SDV_CUDA(launch_rmsnorm(f32(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final), nullptr,
+                          ws_ptr<__nv_bfloat16>(c, c->L.h3), R, H, cf.rms_eps, status, s));
   float* z = r->logits ? r->logits : ws_ptr<float>(c, c->L.z);
   SDV_CUDA(mark(SDV_PHASE_LMHEAD));
   {  // LM head + per-tile softmax statistics
@@ -470,7 +486,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.ld_f32 = V;
     g.epi.stats = ws_ptr<float2>(c, c->L.lmstats);
     g.epi.stats_ld = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, &c->tm_lm, &c->tm_lm, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, false, &c->tm_lm, &c->tm_lm, &c->tm_h3[ni], g, gemm_grid(c, g), s));
   }
   int* accepted = r->accepted ? r->accepted : ws_ptr<int>(c, c->L.accepted);
   int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
@@ -541,8 +557,9 @@ sdv_status sdv_realign(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stre
   return SDV_OK;
 }
 
-sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, float* y, int rows, void* stream) {
+sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float* y, int rows, void* stream) {
   if (!c || !x || !y || rows <= 0 || rows > c->max_rows || which < 0 || which > 5) return SDV_ERR_INVALID_ARG;
+  if (x_format != 0 && x_format != 1) return SDV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const sdv_config& cf = c->cfg;
   const int H = cf.hidden, QD = cf.n_q * cf.head_dim, F = cf.ffn;
@@ -559,14 +576,15 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, float* y, int rows, 
   }
   const int nt = gemm_tile_rows(rows);
   CUtensorMap xm;
-  if (!encode_bf16_2d(&xm, x, rows, K, nt)) return SDV_ERR_CUDA;
+  const bool xf32 = x_format == 1;
+  if (!(xf32 ? encode_f32_2d(&xm, x, rows, K, nt) : encode_bf16_2d(&xm, x, rows, K, nt))) return SDV_ERR_CUDA;
   // a private status word: the sentinel region after the attention schedule
   int* status = ws_ptr<int>(c, c->L.sched) + 8;
   SDV_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
   GemmParams g = gemm_params(c, N, K, rows, (N + 127) / 128, nt, status);
   g.epi.out_f32 = y;
   g.epi.ld_f32 = N;
-  SDV_CUDA(launch_gemm(EPI_F32, nt, wm, wm, &xm, g, gemm_grid(c, g), s));
+  SDV_CUDA(launch_gemm(EPI_F32, nt, xf32, wm, wm, &xm, g, gemm_grid(c, g), s));
   return SDV_OK;
 }
 
@@ -575,7 +593,7 @@ sdv_status sdv_attention(sdv_ctx* c, const void* q, const sdv_batch* b, void* ou
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrologueParams pp = prologue_params(c, b, status, false);
   SDV_CUDA(launch_prologue(pp, s));
-  return run_attention(c, b, static_cast<const __nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(out), status, s);
+  return run_attention(c, b, static_cast<const float*>(q), static_cast<float*>(out), status, s);
 }
 
 }  // extern "C"

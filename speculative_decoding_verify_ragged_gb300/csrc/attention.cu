@@ -18,8 +18,10 @@
 //    values of head_dim -- with 128-byte-swizzled TMA loads into an 8-stage
 //    ring; three consumer warps each own 16 query vectors (draft rows x query
 //    heads of the group) and run QK^T and PV on bf16 mma.sync with an online
-//    softmax in fp32;
-//  * items that cover a whole sequence write the bf16 output directly; split
+//    softmax in fp32.  q (fp32) and the softmax weights enter the MMAs as
+//    bf16 hi + lo pairs, so the output keeps ~17 significant bits against the
+//    bf16 cache;
+//  * items that cover a whole sequence write the fp32 output directly; split
 //    sequences write (max, sum, unnormalised output) partials that a merge
 //    kernel combines (log-sum-exp in base 2).
 #include "common.cuh"
@@ -39,7 +41,7 @@ struct ACfg {
   static constexpr int HALVES = D / 64;
   static constexpr int PAGE_BYTES = 2 * HALVES * BOX;  // K and V of one (page, kv head)
   static constexpr int QLD = D + 8;                   // padded Q row (bf16 elements)
-  static constexpr int Q_BYTES = kAttnQMax * QLD * 2;
+  static constexpr int Q_BYTES = 2 * kAttnQMax * QLD * 2;  // hi and lo tiles
   static constexpr int SMEM = 1024 + STAGES * PAGE_BYTES + Q_BYTES + 2 * STAGES * 8 + 64;
 };
 
@@ -78,6 +80,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
   using C = ACfg<D>;
   constexpr int KK = D / 16;  // k16 steps over the head dimension
+  constexpr int QT = kAttnQMax * ACfg<D>::QLD;  // elements of one Q tile
   constexpr int NF = D / 8;   // n8 fragments of the output
   extern __shared__ uint8_t smem_raw[];
   if (read_status(p.status) != 0) return;
@@ -156,27 +159,32 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     const Item it = decode_item(p, item, chunk_pages);
     const int nqv = (it.gamma + 1) * group;
 
-    // Q tile: query vector v = row i * group + head-in-group
-    constexpr int CPR = D / 8;  // 16-byte chunks per row
+    // Q tiles (hi, lo): query vector v = row i * group + head-in-group
+    constexpr int CPR = D / 4;  // float4 per row
     for (int idx = threadIdx.x; idx < kAttnQMax * CPR; idx += kConsumers * kWarp) {
       const int v = idx / CPR, ch = idx - v * CPR;
-      uint4 val = make_uint4(0, 0, 0, 0);
+      float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
       if (v < nqv) {
         const int i = v / group, h = it.g * group + (v - (v / group) * group);
-        val = *reinterpret_cast<const uint4*>(p.q + ((long long)(it.r0 + i) * p.n_q + h) * D + ch * 8);
+        val = *reinterpret_cast<const float4*>(p.q + ((long long)(it.r0 + i) * p.n_q + h) * D + ch * 4);
       }
-      *reinterpret_cast<uint4*>(qs + v * C::QLD + ch * 8) = val;
+      uint2 hi, lo;
+      split_bf16x2(val.x, val.y, hi.x, lo.x);
+      split_bf16x2(val.z, val.w, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(qs + v * C::QLD + ch * 4) = hi;
+      *reinterpret_cast<uint2*>(qs + QT + v * C::QLD + ch * 4) = lo;
     }
     named_sync(1, kConsumers * kWarp);
 
     const bool active = warp * 16 < nqv;
-    uint32_t qa[KK][4];
+    uint32_t qa[KK][4], ql[KK][4];
     if (active) {
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
         const int row = warp * 16 + (mat & 1) * 8 + rr;
         const int col = kk * 16 + (mat >> 1) * 8;
         ldsm_x4(smem_u32(qs + row * C::QLD + col), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+        ldsm_x4(smem_u32(qs + QT + row * C::QLD + col), ql[kk][0], ql[kk][1], ql[kk][2], ql[kk][3]);
       }
     }
     // query positions of this thread's two rows
@@ -208,6 +216,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           ldsm_x4(addr, b0, b1, b2, b3);
           mma_bf16(s[0], qa[kk], b0, b1);
           mma_bf16(s[1], qa[kk], b2, b3);
+          mma_bf16(s[0], ql[kk], b0, b1);
+          mma_bf16(s[1], ql[kk], b2, b3);
         }
         // scale to base-2 logits and apply the block-causal mask
         const int kp0 = pi * p.page;
@@ -251,11 +261,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           o[nf][2] *= a1;
           o[nf][3] *= a1;
         }
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
-        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
-        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
-        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+        // P enters the PV product as a bf16 pair hi + lo (about 16 significant
+        // bits): a single bf16 P would add ~0.1 % noise to every output
+        uint32_t pa[4], pl[4];
+        split_bf16x2(s[0][0], s[0][1], pa[0], pl[0]);
+        split_bf16x2(s[0][2], s[0][3], pa[1], pl[1]);
+        split_bf16x2(s[1][0], s[1][1], pa[2], pl[2]);
+        split_bf16x2(s[1][2], s[1][3], pa[3], pl[3]);
 #pragma unroll
         for (int nf = 0; nf < NF; nf += 2) {
           const int key = (mat & 1) * 8 + rr;
@@ -265,6 +277,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           ldsm_x4_t(addr, b0, b1, b2, b3);
           mma_bf16(o[nf], pa, b0, b1);
           mma_bf16(o[nf + 1], pa, b2, b3);
+          mma_bf16(o[nf], pl, b0, b1);
+          mma_bf16(o[nf + 1], pl, b2, b3);
         }
       }
       __syncwarp();
@@ -288,12 +302,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           if (v < nqv) {
             const float inv = half ? i1 : i0;
             const int i = v / group, h = it.g * group + (v - (v / group) * group);
-            __nv_bfloat16* dst = p.out + ((long long)(it.r0 + i) * p.n_q + h) * D;
+            float* dst = p.out + ((long long)(it.r0 + i) * p.n_q + h) * D;
 #pragma unroll
             for (int nf = 0; nf < NF; ++nf) {
               const int d = nf * 8 + 2 * t;
-              *reinterpret_cast<uint32_t*>(dst + d) =
-                  pack_bf16x2(o[nf][half * 2] * inv, o[nf][half * 2 + 1] * inv);
+              *reinterpret_cast<float2*>(dst + d) = make_float2(o[nf][half * 2] * inv, o[nf][half * 2 + 1] * inv);
             }
           }
         }
@@ -350,9 +363,9 @@ __global__ void attn_merge_kernel(const AttnParams p, const int* row_seq, int R)
     for (int e = 0; e < PER; ++e) acc[e] += w * src[lane + 32 * e];
   }
   const float inv = 1.f / L;
-  __nv_bfloat16* dst = p.out + ((long long)r * p.n_q + h) * D;
+  float* dst = p.out + ((long long)r * p.n_q + h) * D;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = f2bf(acc[e] * inv);
+  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = acc[e] * inv;
 }
 
 template <int D>

@@ -12,7 +12,12 @@
 //    shared-memory ring (7-10 stages, ~180 KB in flight per SM);
 //  * four consumer warps run bf16 mma.sync (m16n8k16, fp32 accumulate) with
 //    the weights as the 16-row A operand and the activations as the 8-column
-//    B operand, so a handful of rows costs no padding of the weight side;
+//    B operand, so a handful of rows costs no padding of the weight side.
+//    Activations arrive either as bf16 (the LM head's input) or as fp32, in
+//    which case each value is split into bf16 hi + lo parts and both are
+//    multiplied (about 17 significant bits): the layer's activations are
+//    carried in fp32, so no rounding of them compounds from one GEMM to the
+//    next;
 //  * work is split stream-K: the (tile, k-block) units of the whole matrix are
 //    cut into one contiguous range per CTA (one CTA per SM), so every SM
 //    streams the same number of bytes whatever the matrix shape.  A tile cut
@@ -34,14 +39,20 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int CONSUMERS = 4;
 constexpr int THREADS = (CONSUMERS + 1) * kWarp;
 
-template <int NT>
+constexpr int kSmemBudget = 227 * 1024;
+
+template <int NT, bool XF32>
 struct Cfg {
-  static constexpr int B_BYTES = NT * BK * 2;
+  static constexpr int B_BYTES = NT * BK * (XF32 ? 4 : 2);  // fp32: two 32-wide boxes
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = NT == 64 ? 7 : (NT == 32 ? 9 : 10);
   static constexpr int EPI_LD = BM + 4;  // padded row of the staged accumulator tile
   static constexpr int EPI_BYTES = NT * EPI_LD * 4;
+  static constexpr int FIXED = 1024 + EPI_BYTES + 512;
+  static constexpr int FIT = (kSmemBudget - FIXED) / STAGE;
+  static constexpr int STAGES = FIT > 10 ? 10 : FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_BYTES + 2 * STAGES * 8 + 16;
+  static_assert(STAGES >= 3, "pipeline too shallow");
+  static_assert(SMEM <= kSmemBudget, "shared memory");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -53,9 +64,9 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) 
   return static_cast<int>(((u + 1) * P - 1) / total);
 }
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool XF32>
 __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* epi, int tm, int tn, int tid) {
-  constexpr int LD = Cfg<NT>::EPI_LD;
+  constexpr int LD = Cfg<NT, XF32>::EPI_LD;
   const EpiParams& e = p.epi;
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int col = tm * BM + tid;
@@ -63,12 +74,12 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
       for (int n = 0; n < NT; ++n) {
         const int r = tn * NT + n;
         if (r >= p.R) break;
+        const long long o = (long long)r * e.ld_f32 + col;
         const float v = epi[n * LD + tid];
         if constexpr (EPI == EPI_F32) {
-          e.out_f32[(long long)r * e.ld_f32 + col] = v;
+          e.out_f32[o] = v;
         } else {
-          const long long o = (long long)r * e.ld_bf16 + col;
-          e.out_bf16[o] = f2bf(v + bf2f(e.resid[o]));
+          e.out_f32[o] = v + e.resid_f32[o];
         }
       }
     }
@@ -82,7 +93,7 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
         const float gt = epi[n * LD + j];
         const float up = epi[n * LD + 64 + j];
         const float s = gt / (1.0f + expf(-gt));
-        e.out_bf16[(long long)r * e.ld_bf16 + f] = f2bf(s * up);
+        e.out_f32[(long long)r * e.ld_f32 + f] = s * up;
       }
     }
   } else if constexpr (EPI == EPI_QKV) {
@@ -109,10 +120,10 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
             x = x * c + y * s;
           }
         }
-        const __nv_bfloat16 v = f2bf(x);
         if (hq < e.n_q) {
-          e.q_out[(long long)r * (e.n_q * D) + f] = v;
+          e.out_f32[(long long)r * (e.n_q * D) + f] = x;  // q stays fp32
         } else {
+          // K and V enter the bf16 cache at (sequence, position)
           const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
           const int g = hq - e.n_q - kv * e.n_kv;
           const int b = e.row_seq[r];
@@ -120,7 +131,7 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
           const int pg = e.page_table[(long long)b * e.max_pages + pos / e.page];
           const int slot = pos - (pos / e.page) * e.page;
           const long long idx = ((((long long)pg * e.n_kv + g) * 2 + kv) * e.page + slot) * D + j;
-          e.kv_pool[idx] = v;
+          e.kv_pool[idx] = f2bf(x);
         }
       }
     }
@@ -153,11 +164,11 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
   }
 }
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool XF32>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
-  using C = Cfg<NT>;
+  using C = Cfg<NT, XF32>;
   constexpr int NF = NT / 8;  // n8 fragments
   extern __shared__ uint8_t smem_raw[];
   if (read_status(p.status) != 0) return;
@@ -208,7 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(&full[stage], C::STAGE);
           tma_load_2d_hint(sa, &tmA0, &full[stage], k * BK, rowA0, pol);
           tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], k * BK, rowA1, pol);
-          tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
+          if constexpr (XF32) {
+            tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
+            tma_load_2d(sa + A_BYTES + NT * 128, &tmX, &full[stage], k * BK + 32, tn * NT);
+          } else {
+            tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
@@ -272,16 +288,43 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int chunk = kk * 2 + (mat >> 1);
           ldsm_x4(a_base + row * 128 + ((chunk ^ rr) << 4), a[mi][0], a[mi][1], a[mi][2], a[mi][3]);
         }
+        if constexpr (XF32) {
+          // fp32 activations, 128-byte swizzled 32-wide boxes: thread (g, t) needs
+          // x[n = 8 nj + g][16 kk + 2t .. +1] and [.. + 8 .. + 9]; each pair is
+          // split into bf16 hi and lo and multiplied twice
+          const uint32_t box = b_base + (kk >> 1) * (NT * 128);
+          const int c0 = (kk & 1) * 4 + (t >> 1);
+          const int within = (t & 1) * 8;
 #pragma unroll
-        for (int nj = 0; nj < NF; nj += 2) {
-          const int nrow = (nj + (mat >> 1)) * 8 + rr;
-          const int chunk = kk * 2 + (mat & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(b_base + nrow * 128 + ((chunk ^ rr) << 4), b0, b1, b2, b3);
+          for (int nj = 0; nj < NF; ++nj) {
+            const int n = nj * 8 + g;
+            const uint32_t row = box + n * 128 + within;
+            float2 v0, v1;
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v0.x), "=f"(v0.y) : "r"(row + (((c0) ^ (n & 7)) << 4)));
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(v1.x), "=f"(v1.y)
+                         : "r"(row + (((c0 + 2) ^ (n & 7)) << 4)));
+            uint32_t h0, l0, h1, l1;
+            split_bf16x2(v0.x, v0.y, h0, l0);
+            split_bf16x2(v1.x, v1.y, h1, l1);
 #pragma unroll
-          for (int mi = 0; mi < 2; ++mi) {
-            mma_bf16(acc[mi][nj], a[mi], b0, b1);
-            mma_bf16(acc[mi][nj + 1], a[mi], b2, b3);
+            for (int mi = 0; mi < 2; ++mi) {
+              mma_bf16(acc[mi][nj], a[mi], h0, h1);
+              mma_bf16(acc[mi][nj], a[mi], l0, l1);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int nj = 0; nj < NF; nj += 2) {
+            const int nrow = (nj + (mat >> 1)) * 8 + rr;
+            const int chunk = kk * 2 + (mat & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(b_base + nrow * 128 + ((chunk ^ rr) << 4), b0, b1, b2, b3);
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi) {
+              mma_bf16(acc[mi][nj], a[mi], b0, b1);
+              mma_bf16(acc[mi][nj + 1], a[mi], b2, b3);
+            }
           }
         }
       }
@@ -357,54 +400,54 @@ __global__ void __launch_bounds__(THREADS, 1)
         epi[(n + 1) * LD + m + 8] = acc[mi][nj][3];
       }
     named_sync(1, CONSUMERS * kWarp);
-    epilogue_pass<EPI, NT>(p, epi, tm, tn, threadIdx.x);
+    epilogue_pass<EPI, NT, XF32>(p, epi, tm, tn, threadIdx.x);
     named_sync(1, CONSUMERS * kWarp);
     u += k1 - k0;
   }
 }
 
-template <int EPI, int NT>
+template <int EPI, int NT, bool XF32>
 cudaError_t launch_t(const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x, const GemmParams& p,
                      int grid, cudaStream_t stream) {
-  auto kern = gemm_ws_kernel<EPI, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<NT>::SMEM);
+  auto kern = gemm_ws_kernel<EPI, NT, XF32>;
+  constexpr int smem = Cfg<NT, XF32>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, Cfg<NT>::SMEM, stream>>>(*a0, *a1, *x, p);
+  kern<<<grid, THREADS, smem, stream>>>(*a0, *a1, *x, p);
   note_launch();
   return cudaGetLastError();
 }
 
-template <int EPI>
+template <int EPI, bool XF32>
 cudaError_t launch_nt(int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
                       const GemmParams& p, int grid, cudaStream_t stream) {
   switch (nt) {
-    case 16: return launch_t<EPI, 16>(a0, a1, x, p, grid, stream);
-    case 32: return launch_t<EPI, 32>(a0, a1, x, p, grid, stream);
-    case 64: return launch_t<EPI, 64>(a0, a1, x, p, grid, stream);
+    case 16: return launch_t<EPI, 16, XF32>(a0, a1, x, p, grid, stream);
+    case 32: return launch_t<EPI, 32, XF32>(a0, a1, x, p, grid, stream);
+    case 64: return launch_t<EPI, 64, XF32>(a0, a1, x, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+template <int EPI>
+cudaError_t launch_x(int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
+                     const GemmParams& p, int grid, cudaStream_t stream) {
+  return xf32 ? launch_nt<EPI, true>(nt, a0, a1, x, p, grid, stream)
+              : launch_nt<EPI, false>(nt, a0, a1, x, p, grid, stream);
 }
 
 }  // namespace
 
 int gemm_tile_rows(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
 
-size_t gemm_smem_bytes(int nt, int /*int4*/) {
-  switch (nt) {
-    case 16: return Cfg<16>::SMEM;
-    case 32: return Cfg<32>::SMEM;
-    default: return Cfg<64>::SMEM;
-  }
-}
-
-cudaError_t launch_gemm(int epi, int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
-                        const GemmParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(int epi, int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1,
+                        const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream) {
   switch (epi) {
-    case EPI_F32: return launch_nt<EPI_F32>(nt, a0, a1, x, p, grid, stream);
-    case EPI_RESID: return launch_nt<EPI_RESID>(nt, a0, a1, x, p, grid, stream);
-    case EPI_SWIGLU: return launch_nt<EPI_SWIGLU>(nt, a0, a1, x, p, grid, stream);
-    case EPI_QKV: return launch_nt<EPI_QKV>(nt, a0, a1, x, p, grid, stream);
-    case EPI_LMHEAD: return launch_nt<EPI_LMHEAD>(nt, a0, a1, x, p, grid, stream);
+    case EPI_F32: return launch_x<EPI_F32>(nt, xf32, a0, a1, x, p, grid, stream);
+    case EPI_RESID: return launch_x<EPI_RESID>(nt, xf32, a0, a1, x, p, grid, stream);
+    case EPI_SWIGLU: return launch_x<EPI_SWIGLU>(nt, xf32, a0, a1, x, p, grid, stream);
+    case EPI_QKV: return launch_x<EPI_QKV>(nt, xf32, a0, a1, x, p, grid, stream);
+    case EPI_LMHEAD: return launch_nt<EPI_LMHEAD, false>(nt, a0, a1, x, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -22,13 +22,10 @@ enum Epi : int {
 };
 
 struct EpiParams {
-  float* out_f32 = nullptr;  // F32 / LMHEAD: [R, ld_f32]
+  float* out_f32 = nullptr;  // output [R, ld_f32] (QKV: q [R, n_q * head_dim])
   long long ld_f32 = 0;
-  __nv_bfloat16* out_bf16 = nullptr;  // RESID / SWIGLU: [R, ld_bf16]
-  const __nv_bfloat16* resid = nullptr;
-  int ld_bf16 = 0;
+  const float* resid_f32 = nullptr;  // RESID: residual [R, ld_f32]
   // QKV
-  __nv_bfloat16* q_out = nullptr;  // [R, n_q * head_dim]
   __nv_bfloat16* kv_pool = nullptr;
   const int* page_table = nullptr;
   int max_pages = 0;
@@ -58,19 +55,18 @@ struct GemmParams {
 // Choose the activation tile for R rows (16, 32 or 64).
 int gemm_tile_rows(int R);
 // Launch the weight-streaming GEMM. a0/a1: weight maps for the two 64-row
-// halves of a 128-row tile (same map for plain GEMMs); x: activation map
-// whose box is (64, nt); s0/s1: int4 scale maps (nullptr for bf16).
-cudaError_t launch_gemm(int epi, int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
-                        const GemmParams& p, int grid, cudaStream_t stream);
-size_t gemm_smem_bytes(int nt, int int4);
+// halves of a 128-row tile (same map for plain GEMMs); x: activation map,
+// bf16 with box (64, nt), or fp32 (xf32) with box (32, nt).
+cudaError_t launch_gemm(int epi, int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1,
+                        const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // attention over the paged cache
 // ---------------------------------------------------------------------------
 
 struct AttnParams {
-  const __nv_bfloat16* q = nullptr;  // [R, n_q, D]
-  __nv_bfloat16* out = nullptr;      // [R, n_q * D]
+  const float* q = nullptr;  // [R, n_q, D], rotated
+  float* out = nullptr;      // [R, n_q * D]
   const int* seq_lens = nullptr;
   const int* draft_lens = nullptr;
   const int* row_off = nullptr;   // [B+1]
@@ -121,13 +117,13 @@ struct PrologueParams {
 };
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
 
-// x0 = emb[tokens], h = RMSNorm(x0) * gain, plus each row's rotary (cos, sin) table.
+// x0 = emb[tokens] (fp32), h = RMSNorm(x0) * gain (fp32), plus each row's rotary (cos, sin) table.
 cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
-                                   __nv_bfloat16* x0, __nv_bfloat16* h, const int* row_pos, float* rope_cs, int R,
-                                   int H, int head_dim, float eps, float theta, const int* status,
-                                   cudaStream_t stream);
-cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* h, int R, int H,
-                           float eps, const int* status, cudaStream_t stream);
+                                   float* x0, float* h, const int* row_pos, float* rope_cs, int R, int H,
+                                   int head_dim, float eps, float theta, const int* status, cudaStream_t stream);
+// h = RMSNorm(x) * gain, written as fp32 (h_f32) or rounded to bf16 (h_bf16).
+cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
+                           int H, float eps, const int* status, cudaStream_t stream);
 
 struct AcceptParams {
   const float* z = nullptr;        // logits [R, V] (from_logits)

@@ -157,32 +157,28 @@ __device__ float block_sum_256(float v, float* s) {
   return t;
 }
 
-// x [H] bf16 -> h = round(x / sqrt(mean(x^2) + eps) * gain)
-__device__ void norm_row(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* h, __nv_bfloat16* copy,
-                         int H, float eps, float* s_red) {
+// h = x / sqrt(mean(x^2) + eps) * gain for one row; x fp32, h fp32 or bf16.
+template <typename Out>
+__device__ void norm_row(const float* x, const __nv_bfloat16* gain, Out* h, int H, float eps, float* s_red) {
   float ss = 0.f;
-  for (int k = threadIdx.x * 8; k < H; k += blockDim.x * 8) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + k);
-    if (copy) *reinterpret_cast<uint4*>(copy + k) = raw;
-    const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float f = bf2f(v[e]);
-      ss += f * f;
-    }
+  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + k);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = block_sum_256(ss, s_red);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
-  for (int k = threadIdx.x * 8; k < H; k += blockDim.x * 8) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(x + k);
-    const uint4 gr = *reinterpret_cast<const uint4*>(gain + k);
-    const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
-    const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(&gr);
-    uint4 outw;
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(&outw);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = f2bf(bf2f(v[e]) * inv * bf2f(gg[e]));
-    *reinterpret_cast<uint4*>(h + k) = outw;
+  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + k);
+    const float y0 = v.x * inv * bf2f(gain[k]), y1 = v.y * inv * bf2f(gain[k + 1]);
+    const float y2 = v.z * inv * bf2f(gain[k + 2]), y3 = v.w * inv * bf2f(gain[k + 3]);
+    if constexpr (sizeof(Out) == 4) {
+      *reinterpret_cast<float4*>(h + k) = make_float4(y0, y1, y2, y3);
+    } else {
+      uint2 w;
+      w.x = pack_bf16x2(y0, y1);
+      w.y = pack_bf16x2(y2, y3);
+      *reinterpret_cast<uint2*>(h + k) = w;
+    }
   }
 }
 
@@ -190,8 +186,8 @@ struct EmbedParams {
   const int* tokens;
   const __nv_bfloat16* emb;
   const __nv_bfloat16* gain;
-  __nv_bfloat16* x0;
-  __nv_bfloat16* h;
+  float* x0;
+  float* h;
   const int* row_pos;
   float* rope_cs;
   int H, head_dim;
@@ -205,8 +201,17 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const EmbedParams p) {
   if (read_status(p.status) != 0) return;
   const int r = blockIdx.x;
   const int tok = p.tokens[r];
-  norm_row(p.emb + (long long)tok * p.H, p.gain, p.h + (long long)r * p.H, p.x0 + (long long)r * p.H, p.H, p.eps,
-           s_red);
+  // the embedding row enters the fp32 residual stream
+  const __nv_bfloat16* e = p.emb + (long long)tok * p.H;
+  float* x0 = p.x0 + (long long)r * p.H;
+  for (int k = threadIdx.x * 8; k < p.H; k += blockDim.x * 8) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(e + k);
+    const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
+    *reinterpret_cast<float4*>(x0 + k) = make_float4(bf2f(v[0]), bf2f(v[1]), bf2f(v[2]), bf2f(v[3]));
+    *reinterpret_cast<float4*>(x0 + k + 4) = make_float4(bf2f(v[4]), bf2f(v[5]), bf2f(v[6]), bf2f(v[7]));
+  }
+  __syncthreads();
+  norm_row<float>(x0, p.gain, p.h + (long long)r * p.H, p.H, p.eps, s_red);
   // rotary table of this row: angle = pos * theta^(-2j/d), reduced mod 2 pi in double
   const int half = p.head_dim >> 1;
   const int pos = p.row_pos[r];
@@ -222,12 +227,13 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const EmbedParams p) {
   }
 }
 
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* x, const __nv_bfloat16* gain,
-                                                      __nv_bfloat16* h, int H, float eps, const int* status) {
+template <typename Out>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, Out* h, int H,
+                                                      float eps, const int* status) {
   __shared__ float s_red[32];
   if (read_status(status) != 0) return;
   const int r = blockIdx.x;
-  norm_row(x + (long long)r * H, gain, h + (long long)r * H, nullptr, H, eps, s_red);
+  norm_row<Out>(x + (long long)r * H, gain, h + (long long)r * H, H, eps, s_red);
 }
 
 // ---------------------------------------------------------------------------
@@ -553,18 +559,18 @@ cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
-                                   __nv_bfloat16* x0, __nv_bfloat16* h, const int* row_pos, float* rope_cs, int R,
-                                   int H, int head_dim, float eps, float theta, const int* status,
-                                   cudaStream_t stream) {
+                                   float* x0, float* h, const int* row_pos, float* rope_cs, int R, int H,
+                                   int head_dim, float eps, float theta, const int* status, cudaStream_t stream) {
   EmbedParams e{tokens, emb, gain, x0, h, row_pos, rope_cs, H, head_dim, eps, log2(static_cast<double>(theta)), status};
   embed_norm_kernel<<<R, 256, 0, stream>>>(e);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, __nv_bfloat16* h, int R, int H,
-                           float eps, const int* status, cudaStream_t stream) {
-  rmsnorm_kernel<<<R, 256, 0, stream>>>(x, gain, h, H, eps, status);
+cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
+                           int H, float eps, const int* status, cudaStream_t stream) {
+  if (h_f32) rmsnorm_kernel<float><<<R, 256, 0, stream>>>(x, gain, h_f32, H, eps, status);
+  else rmsnorm_kernel<__nv_bfloat16><<<R, 256, 0, stream>>>(x, gain, h_bf16, H, eps, status);
   note_launch();
   return cudaGetLastError();
 }

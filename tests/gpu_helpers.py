@@ -8,12 +8,11 @@ import numpy as np
 from oracle import verify_step as o
 import workloads as wl
 
-# the benchmark spec tolerances for the bf16 forward
+# tolerances stated for the bf16 forward (bf16 weights and KV cache)
 LOGIT_TOL_REL_RMS = 1e-2      # max |dlogit| <= 1e-2 * rms(logits)
 PROB_TOL_ABS = 1e-3           # max |dp| <= 1e-3
-# derived: |dz| <= 1e-2 rms with rms ~1.3 moves p by at most exp(2.6e-2) - 1 < 3 %;
-# 5 % leaves room for the normaliser
-PROB_TOL_REL = 5e-2
+# derived: |dz| <= 1e-2 rms with rms <= 1.3 moves p by at most exp(2 * 1.3e-2) - 1 < 3 %
+PROB_TOL_REL = 3e-2
 # an acceptance decision or a sampled token is only required to agree when
 # the oracle's margin exceeds what that probability error can move
 DECISION_REL = 3e-2

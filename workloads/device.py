@@ -44,7 +44,7 @@ def batch_to_device(b: Batch, dev="cuda") -> dict:
     d = dict(B=b.B, R=b.R, G=b.G,
              seq_lens=_t(b.seq_lens.astype(i32), dev), draft_lens=_t(b.draft_lens.astype(i32), dev),
              tokens=_t(b.tokens.astype(i32), dev),
-             draft_probs=_t(b.draft_probs.astype(np.float32).reshape(max(b.G, 0), -1), dev),
+             draft_probs=_t(b.draft_probs.astype(np.float32).reshape(b.G, b.dims["vocab"]), dev),
              uniforms=_t(b.uniforms.astype(np.float32), dev),
              kv_pool=_t(b.kv_pool.view(np.int16), dev, torch.bfloat16),
              num_pool_pages=int(b.kv_pool.shape[0]),
