@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling run: no clock pre-roll, no e2e or CPU legs (its numbers are not bench values)")
     return ap.parse_args()
 
 
@@ -165,6 +167,26 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def box_copy_gbps():
+    """This box's device-to-device copy bandwidth (torch copy of 1 Gi bf16, best of 5):
+    context for comparing runs on different boxes; the roofline uses the peaks file."""
+    import torch
+    a = torch.empty(1 << 30, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    best = None
+    for _ in range(6):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    del a, b
+    return 2 * (1 << 30) * 2 / (best / 1e3) / 1e9
+
+
 def run_ours(args):
     import torch
     import workloads as wl
@@ -196,30 +218,33 @@ def run_ours(args):
     U = torch.from_numpy(np.stack([wl.uniform24(g, batch.R) for _ in range(nsteps)])).cuda()
     res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1])
     stream = torch.cuda.current_stream()
-    emitted = torch.zeros(nsteps, dtype=torch.int32, device="cuda")
+    # one emitted-offsets row per step, so the step count is read after the timed region
+    EO = torch.zeros((nsteps, batch.B + 1), dtype=torch.int32, device="cuda")
 
     def step(i):
         bd["uniforms"] = U[i]
+        res["emitted_offsets"] = EO[i]
         eng.verify_step(bd, res, stream)
-        emitted[i] = res["emitted_offsets"][batch.B]
 
     for i in range(args.warmup):
         step(i)
     assert eng.read_status(res["status"]) == 0
     torch.cuda.synchronize()
 
-    # one set of phase events per timed step, recorded on the launching stream,
-    # read after the timed region: the dominant kernel is timed live, without
-    # synchronising inside the timed region
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(args.steps)]
-    for es in evsets:
-        for e in es:
-            e.record(stream)
+    # the dominant kernel (LM head) is timed live inside the timed region with one
+    # event pair per step on the launching stream, read after the region; no
+    # other boundary is recorded, so the other kernels keep overlapping
+    K_LM = PHASES.index("lm_head")
+    lm_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for a_, b_ in lm_pairs:
+        a_.record(stream)
+        b_.record(stream)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local) if not args.quick else None
     # pre-roll: the same step back to back for ~1 s so the clock samples see the GPU under load
-    t_end = time.perf_counter() + 1.0
+    t_end = time.perf_counter() + (0.0 if args.quick else 1.0)
     while time.perf_counter() < t_end:
         step(args.warmup - 1)
         torch.cuda.synchronize()
@@ -231,14 +256,26 @@ def run_ours(args):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for j, i in enumerate(range(args.warmup, nsteps)):
-        eng.set_phase_events(evsets[j])
+        evs = [None] * (len(PHASES) + 1)
+        evs[K_LM], evs[K_LM + 1] = lm_pairs[j]
+        eng.set_phase_events(evs)
         step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     launches = kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
+    lm_ms = [a_.elapsed_time(b_) for a_, b_ in lm_pairs]
+
+    # phase breakdown (informational, outside the timed region): every boundary
+    # recorded, which serialises the kernels at the boundaries
+    nph = min(20, args.steps)
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
+    for j in range(nph):
+        eng.set_phase_events(evsets[j])
+        step(args.warmup + j)
+    torch.cuda.synchronize()
     eng.set_phase_events(None)
     assert eng.read_status(res["status"]) == 0
     phase_ms = {p: [es[k].elapsed_time(es[k + 1]) for es in evsets] for k, p in enumerate(PHASES)}
@@ -249,7 +286,7 @@ def run_ours(args):
         tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
-    tokens_rank = int(emitted[args.warmup:].sum().item())
+    tokens_rank = int(EO[args.warmup:, batch.B].sum().item())
     tokens = tokens_rank
     if world > 1:
         import torch.distributed as dist
@@ -260,15 +297,16 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(eng, batch, bd, U, args, stream, tokens_rank)
-    if world > 1:
+    e2e = run_e2e(eng, batch, bd, U, args, stream, tokens_rank) if not args.quick else None
+    if world > 1 and e2e is not None:
         import torch.distributed as dist
         tt = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e["value"] = tokens / (float(tt.item()) * args.steps / 1e3)
 
+    copy_gbs = box_copy_gbps() if not args.quick else None
     hbm, tflops, peak_kind = measured_peaks()
-    lm_avg = statistics.mean(phase_ms["lm_head"])
+    lm_avg = statistics.mean(lm_ms)
     lm_bytes = lm_head_algorithmic_bytes(batch.R)
     achieved = lm_bytes / (lm_avg / 1e3) / 1e9
     step_bytes = step_algorithmic_bytes(batch)
@@ -288,10 +326,11 @@ def run_ours(args):
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes,
                           "achieved_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
                           "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
-        "phases_us": {p: statistics.mean(v) * 1e3 for p, v in phase_ms.items()},
+        "phases_us_serialised": {p: statistics.mean(v) * 1e3 for p, v in phase_ms.items()},
         "emitted_tokens_per_step": tokens / (args.steps * world),
+        "box_copy_GBps": copy_gbs,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_baseline(W, batch)
     if world > 1:
         import torch.distributed as dist

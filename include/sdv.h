@@ -210,8 +210,11 @@ enum {
 /* Optional phase timing.  events: n = SDV_PHASES + 1 cudaEvent_t handles
  * (passed as void*, created by the caller); each later sdv_verify_step on
  * this context records events[k] on its stream when phase k starts and
- * events[SDV_PHASES] after the last phase.  events = NULL (n = 0) turns it
- * off.  The context keeps the handles, not ownership. */
+ * events[SDV_PHASES] after the last phase.  A NULL entry skips that
+ * boundary: an event recorded between two kernels stops the second from
+ * starting while the first finishes, so record only the boundaries you read.
+ * events = NULL (n = 0) turns timing off.  The context keeps the handles,
+ * not ownership. */
 sdv_status sdv_set_phase_events(sdv_ctx *ctx, void *const *events, int n);
 
 /* Synchronise `stream` and copy the device status word to *host_status. */

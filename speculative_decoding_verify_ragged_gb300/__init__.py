@@ -150,16 +150,18 @@ class VerifyEngine:
     def set_phase_events(self, events):
         """Record torch.cuda.Event objects at the step's phase boundaries (None = off).
 
-        ``events`` holds len(PHASES) + 1 events created with enable_timing=True.
+        ``events`` holds len(PHASES) + 1 events created with enable_timing=True, or None
+        for boundaries not to record (each recorded event blocks the overlap of the two
+        kernels it separates).
         """
         if events is None:
             self._check(self.lib.sdv_set_phase_events(self.handle, None, 0), "sdv_set_phase_events")
             self._events = None
             return
         for e in events:
-            if not e.cuda_event:
+            if e is not None and not e.cuda_event:
                 e.record()          # creates the underlying CUDA event
-        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        arr = (ctypes.c_void_p * len(events))(*[(e.cuda_event if e is not None else None) for e in events])
         self._events = list(events)
         self._check(self.lib.sdv_set_phase_events(self.handle, arr, len(events)), "sdv_set_phase_events")
 

@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -15,6 +16,14 @@ static std::atomic<unsigned long long> g_launches{0};
 static thread_local int g_last_cuda_error = 0;
 
 void note_launch(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("SDV_NO_PDL");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
 
 static sdv_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -36,7 +45,8 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Layout {
   size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope;
   size_t x0, h, h3, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
-  size_t part_o, part_ml, accepted, final_tokens, total;
+  size_t part_o, part_ml, accepted, final_tokens, p_draft, slot_count, chunk_count, chunk_sums, total;
+  int chunk_ld;
   int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
 };
 
@@ -58,6 +68,7 @@ static bool config_ok(const sdv_config* c) {
   if (c->weight_format != SDV_WEIGHTS_BF16 && c->weight_format != SDV_WEIGHTS_INT4_G32) return false;
   if (c->hidden % kmul || (c->n_q * c->head_dim) % kmul || c->ffn % kmul) return false;
   if (c->ffn % 64) return false;
+  if (c->vocab > 256 * 4096) return false;  // sampling chunk table
   return true;
 }
 
@@ -111,6 +122,11 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.part_ml = take(static_cast<size_t>(L.items_max) * kAttnQMax * 8);
   L.accepted = take(B * 4);
   L.final_tokens = take(B * 4);
+  L.p_draft = take(R * 4);
+  L.chunk_ld = accept_chunks(c.vocab);
+  L.slot_count = take(B * 4);
+  L.chunk_count = take(B * 4);
+  L.chunk_sums = take(B * 2 * static_cast<size_t>(L.chunk_ld) * 8);
   L.total = o;
   return L;
 }
@@ -247,7 +263,11 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
     delete c;
     return SDV_ERR_CUDA;
   }
+  // arrival counters start at zero; every kernel that uses one resets it
   cudaError_t e = cudaMemset(c->ws + L.counters, 0, static_cast<size_t>(L.max_tiles) * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->ws + L.slot_count, 0, static_cast<size_t>(max_slots) * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->ws + L.chunk_count, 0, static_cast<size_t>(max_slots) * 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e);
@@ -265,10 +285,7 @@ sdv_status sdv_set_phase_events(sdv_ctx* ctx, void* const* events, int n) {
     return SDV_OK;
   }
   if (n != SDV_PHASES + 1) return SDV_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i) {
-    if (!events[i]) return SDV_ERR_INVALID_ARG;
-    ctx->phase_ev[i] = static_cast<cudaEvent_t>(events[i]);
-  }
+  for (int i = 0; i < n; ++i) ctx->phase_ev[i] = static_cast<cudaEvent_t>(events[i]);
   ctx->timing = true;
   return SDV_OK;
 }
@@ -378,6 +395,15 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   return SDV_OK;
 }
 
+static void fill_accept_scratch(sdv_ctx* c, AcceptParams& a, const PrologueParams& pp) {
+  a.row_seq = pp.t.row_seq;
+  a.p_draft = ws_ptr<float>(c, c->L.p_draft);
+  a.slot_count = ws_ptr<int>(c, c->L.slot_count);
+  a.chunk_count = ws_ptr<int>(c, c->L.chunk_count);
+  a.chunk_sums = ws_ptr<unsigned long long>(c, c->L.chunk_sums);
+  a.chunk_ld = c->L.chunk_ld;
+}
+
 static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_result* r, const int* accepted,
                                     const int* final_tokens) {
   RealignParams p;
@@ -423,7 +449,9 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   const int nt = gemm_tile_rows(R);
   const int ni = nt_index(nt);
   auto f32 = [&](size_t off) { return ws_ptr<float>(c, off); };
-  auto mark = [&](int k) -> cudaError_t { return c->timing ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess; };
+  auto mark = [&](int k) -> cudaError_t {
+    return c->timing && c->phase_ev[k] ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess;
+  };
 
   SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
   PrologueParams pp = prologue_params(c, b, status, true);
@@ -504,12 +532,13 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     a.row_off = pp.t.row_off;
     a.draft_off = pp.t.draft_off;
     a.row_stats = ws_ptr<float2>(c, c->L.rowstats);
+    fill_accept_scratch(c, a, pp);
     a.accepted = accepted;
     a.final_tokens = final_tokens;
     a.status = status;
     a.B = b->B;
     a.V = V;
-    SDV_CUDA(launch_accept(a, true, s));
+    SDV_CUDA(launch_accept(a, true, R, s));
   }
   if (r->probs) SDV_CUDA(launch_probs(z, ws_ptr<float2>(c, c->L.rowstats), r->probs, R, V, status, s));
   SDV_CUDA(mark(SDV_PHASE_REALIGN));
@@ -535,12 +564,13 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
   a.draft_lens = b->draft_lens;
   a.row_off = pp.t.row_off;
   a.draft_off = pp.t.draft_off;
+  fill_accept_scratch(c, a, pp);
   a.accepted = accepted;
   a.final_tokens = final_tokens;
   a.status = r->status;
   a.B = b->B;
   a.V = c->cfg.vocab;
-  SDV_CUDA(launch_accept(a, false, s));
+  SDV_CUDA(launch_accept(a, false, b->R, s));
   RealignParams rp = realign_params(c, b, r, accepted, final_tokens);
   SDV_CUDA(launch_realign(rp, s));
   return SDV_OK;

@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   constexpr int QT = kAttnQMax * ACfg<D>::QLD;  // elements of one Q tile
   constexpr int NF = D / 8;   // n8 fragments of the output
   extern __shared__ uint8_t smem_raw[];
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(p.status) != 0) return;
 
   uint8_t* smem = align1024(smem_raw);
@@ -331,14 +333,18 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   }
 }
 
-// One warp per (row, query head) of a split sequence: combine the chunks.
+// One thread per output element (row, query head, d) of a split sequence:
+// combine the chunks' (max, sum, unnormalised output) partials.
 template <int D>
-__global__ void attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
+__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(p.status) != 0) return;
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (wid >= R * p.n_q) return;
-  const int r = wid / p.n_q, h = wid - (wid / p.n_q) * p.n_q;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (long long)R * p.n_q * D) return;
+  const int d = static_cast<int>(gid % D);
+  const int rh = static_cast<int>(gid / D);
+  const int r = rh / p.n_q, h = rh - (rh / p.n_q) * p.n_q;
   const int b = row_seq[r];
   const int chunks = p.chunks[b];
   if (chunks == 1) return;
@@ -346,26 +352,21 @@ __global__ void attn_merge_kernel(const AttnParams p, const int* row_seq, int R)
   const int i = r - p.row_off[b];
   const int g = h / group;
   const int v = i * group + (h - g * group);
-  const int item0 = p.item_off[b] + g * chunks;
+  const long long item0 = p.item_off[b] + (long long)g * chunks;
+  const float2* ml = p.part_ml + item0 * kAttnQMax + v;
+  const float* po = p.part_o + (item0 * kAttnQMax + v) * D + d;
   float M = -INFINITY;
-  for (int c = 0; c < chunks; ++c) M = fmaxf(M, p.part_ml[(long long)(item0 + c) * kAttnQMax + v].x);
-  constexpr int PER = D / 32;
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < chunks; ++c) M = fmaxf(M, ml[(long long)c * kAttnQMax].x);
+  float acc = 0.f, L = 0.f;
+#pragma unroll 8
   for (int c = 0; c < chunks; ++c) {
-    const float2 ml = p.part_ml[(long long)(item0 + c) * kAttnQMax + v];
-    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-    L += w * ml.y;
-    const float* src = p.part_o + ((long long)(item0 + c) * kAttnQMax + v) * D;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += w * src[lane + 32 * e];
+    const float2 m = ml[(long long)c * kAttnQMax];
+    const float w = m.x == -INFINITY ? 0.f : exp2f(m.x - M);
+    L += w * m.y;
+    acc += w * po[(long long)c * kAttnQMax * D];
   }
-  const float inv = 1.f / L;
-  float* dst = p.out + ((long long)r * p.n_q + h) * D;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = acc[e] * inv;
+  p.out[((long long)r * p.n_q + h) * D + d] = acc / L;
 }
 
 template <int D>
@@ -374,13 +375,11 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
   auto kern = attn_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ACfg<D>::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, ACfg<D>::SMEM, stream>>>(*kv_map, p);
-  note_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int warps = R * p.n_q;
-  attn_merge_kernel<D><<<(warps + 7) / 8, 256, 0, stream>>>(p, row_seq, R);
-  note_launch();
-  return cudaGetLastError();
+  if ((e = launch_pdl(kern, dim3(grid), dim3(kThreads), ACfg<D>::SMEM, stream, *kv_map, p)) != cudaSuccess)
+    return e;
+  const long long n = (long long)R * p.n_q * D;
+  return launch_pdl(attn_merge_kernel<D>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream, p,
+                    row_seq, R);
 }
 
 }  // namespace

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   using C = Cfg<NT, XF32>;
   constexpr int NF = NT / 8;  // n8 fragments
   extern __shared__ uint8_t smem_raw[];
-  if (read_status(p.status) != 0) return;
+  griddep_launch_dependents();
 
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
@@ -199,38 +199,61 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- producer: one elected lane issues all TMA loads ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      bool dead = false;
-      for (long long u = u_begin; u < u_end && !dead;) {
+      const int my_units = static_cast<int>(u_end - u_begin);
+      const int pre = my_units < C::STAGES ? my_units : C::STAGES;
+      auto weights = [&](int j, int stage) {  // weight half-tiles of unit j into a stage
+        const long long u = u_begin + j;
         const int tile = static_cast<int>(u / p.kb);
-        const int k0 = static_cast<int>(u - (long long)tile * p.kb);
-        const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
-        const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+        const int k = static_cast<int>(u - (long long)tile * p.kb);
+        const int tm = tile / p.n_tiles;
         const int rowA0 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM;
         const int rowA1 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM + 64;
-        for (int k = k0; k < k1 && !dead; ++k) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            set_status(p.status, SDV_ERR_TIMEOUT);
-            dead = true;
-            break;
-          }
-          uint8_t* sa = smem + stage * C::STAGE;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE);
-          tma_load_2d_hint(sa, &tmA0, &full[stage], k * BK, rowA0, pol);
-          tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], k * BK, rowA1, pol);
-          if constexpr (XF32) {
-            tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
-            tma_load_2d(sa + A_BYTES + NT * 128, &tmX, &full[stage], k * BK + 32, tn * NT);
-          } else {
-            tma_load_2d(sa + A_BYTES, &tmX, &full[stage], k * BK, tn * NT);
-          }
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+        uint8_t* sa = smem + stage * C::STAGE;
+        tma_load_2d_hint(sa, &tmA0, &full[stage], k * BK, rowA0, pol);
+        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], k * BK, rowA1, pol);
+      };
+      auto acts = [&](int j, int stage) {  // activation tile of unit j into a stage
+        const long long u = u_begin + j;
+        const int tile = static_cast<int>(u / p.kb);
+        const int k = static_cast<int>(u - (long long)tile * p.kb);
+        const int tn = tile - (tile / p.n_tiles) * p.n_tiles;
+        uint8_t* sb = smem + stage * C::STAGE + A_BYTES;
+        tma_load_2d(sb, &tmX, &full[stage], k * BK, tn * NT);
+        if constexpr (XF32) tma_load_2d(sb + NT * 128, &tmX, &full[stage], k * BK + 32, tn * NT);
+      };
+      // the weights do not depend on earlier kernels: start streaming them
+      // before waiting for the kernel that writes the activations
+      for (int j = 0; j < pre; ++j) {
+        mbar_expect_tx(&full[j], A_BYTES);
+        weights(j, j);
+      }
+      griddep_wait();
+      if (read_status(p.status) != 0) {
+        // an earlier kernel failed: let the weight copies land, then leave
+        for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
+        for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
+        return;
+      }
+      for (int j = 0; j < pre; ++j) {
+        mbar_arrive_expect_tx(&full[j], C::STAGE - A_BYTES);
+        acts(j, j);
+      }
+      int stage = pre % C::STAGES;
+      uint32_t phase = pre == C::STAGES ? 1u : 0u;
+      bool dead = false;
+      for (int j = pre; j < my_units; ++j) {
+        if (!mbar_wait(&empty[stage], phase ^ 1)) {
+          set_status(p.status, SDV_ERR_TIMEOUT);
+          dead = true;
+          break;
         }
-        u += k1 - k0;
+        mbar_arrive_expect_tx(&full[stage], C::STAGE);
+        weights(j, stage);
+        acts(j, stage);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
       // tail: stay until the consumers have released every stage, so no copy
       // into this CTA's shared memory is still in flight when it exits
@@ -249,6 +272,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---------------- consumers ----------------
+  griddep_wait();
+  if (read_status(p.status) != 0) return;  // the producer drains its copies
   // A timed-out wait marks the CTA dead: no more waiting, no early return (the
   // other consumer warps still meet at the named barriers); outputs are then
   // garbage but every access stays in bounds and the status word says why.
@@ -413,9 +438,7 @@ cudaError_t launch_t(const CUtensorMap* a0, const CUtensorMap* a1, const CUtenso
   constexpr int smem = Cfg<NT, XF32>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, smem, stream>>>(*a0, *a1, *x, p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), smem, stream, *a0, *a1, *x, p);
 }
 
 template <int EPI, bool XF32>

@@ -137,12 +137,20 @@ struct AcceptParams {
   const int* row_off = nullptr;
   const int* draft_off = nullptr;
   float2* row_stats = nullptr;     // [R] (max, sum) written when from logits
+  const int* row_seq = nullptr;    // [R]
+  float* p_draft = nullptr;        // [R] target probability of the next draft token
+  int* slot_count = nullptr;       // [B] rows finished per slot (zero between calls)
+  int* chunk_count = nullptr;      // [B] sampling chunks finished per slot (zero between calls)
+  unsigned long long* chunk_sums = nullptr;  // [B, 2, chunk_ld]
+  int chunk_ld = 0;
   int* accepted = nullptr;
   int* final_tokens = nullptr;
   int* status = nullptr;
   int B = 0, V = 0;
 };
-cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream);
+// Acceptance (one block per row) then final-token sampling (one block per vocab chunk and slot).
+cudaError_t launch_accept(const AcceptParams& p, bool from_logits, int R, cudaStream_t stream);
+int accept_chunks(int V);
 cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, int R, int V, const int* status,
                          cudaStream_t stream);
 
@@ -167,5 +175,28 @@ cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream);
 
 // count of kernels launched by this library
 void note_launch(int n = 1);
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream finishes; it orders itself with
+// griddepcontrol.wait where it reads that kernel's results.
+// SDV_NO_PDL=1 in the environment launches without the attribute (A/B timing).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  note_launch();
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 }  // namespace sdv

@@ -67,6 +67,9 @@ __device__ int block_exscan(int v, int* total, int* s_warp) {
 __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const PrologueParams p) {
   __shared__ int s_warp[80];
   __shared__ int s_err;
+  __shared__ int s_poff[kScanThreads + 1];  // first page-check index of each slot
+  griddep_launch_dependents();
+  griddep_wait();  // the previous step's realignment rewrites page tables and counters
   const int b = threadIdx.x;
   if (b == 0) {
     *p.status = 0;
@@ -84,10 +87,14 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
     else if ((long long)npg * p.page < (long long)L + gam + 1) err = SDV_ERR_PAGE_RANGE;
   }
   if (err) atomicCAS(&s_err, 0, err);
-  int tot_r, tot_g;
+  const int used = (slot && !err) ? (L + gam + 1 + p.page - 1) / p.page : 0;
+  int tot_r, tot_g, tot_pages;
   const int roff = block_exscan(slot ? gam + 1 : 0, &tot_r, s_warp);
   const int goff = block_exscan(slot ? gam : 0, &tot_g, s_warp);
+  const int poff = block_exscan(used, &tot_pages, s_warp);
   if (b == 0 && (tot_r != p.R || tot_g != p.G)) atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+  if (b < p.B) s_poff[b] = poff;
+  if (b == 0) s_poff[p.B] = tot_pages;
   __syncthreads();
   if (s_err) {
     if (b == 0) set_status(p.status, s_err);
@@ -100,18 +107,21 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
       p.t.row_seq[roff + i] = b;
       p.t.row_pos[roff + i] = L + i;
     }
-    const int used = (L + gam + 1 + p.page - 1) / p.page;
-    for (int j = 0; j < used; ++j) {
-      const int pg = p.page_table[(long long)b * p.max_pages + j];
-      if (pg < 0 || pg >= p.pool_pages) {
-        atomicCAS(&s_err, 0, SDV_ERR_PAGE_RANGE);
-        break;
-      }
-    }
   }
   if (b == 0) {
     p.t.row_off[p.B] = tot_r;
     p.t.draft_off[p.B] = tot_g;
+  }
+  // every page a row reads or writes must be a pool page: one flat loop over
+  // all (slot, page) pairs, the slot found by binary search over s_poff
+  for (int idx = threadIdx.x; idx < tot_pages; idx += blockDim.x) {
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_poff[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int pg = p.page_table[(long long)lo * p.max_pages + (idx - s_poff[lo])];
+    if (pg < 0 || pg >= p.pool_pages) atomicCAS(&s_err, 0, SDV_ERR_PAGE_RANGE);
   }
   if (p.check_tokens) {
     for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
@@ -120,13 +130,10 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
     }
   }
   // attention schedule: chunks of pages sized so that items cover the GPU
-  const int pages_b = slot ? (L + gam + 1 + p.page - 1) / p.page : 0;
-  int tot_pages;
-  block_exscan(pages_b, &tot_pages, s_warp);
   const long long units = (long long)tot_pages * p.n_kv;
   int chunk = static_cast<int>((units + p.target_items - 1) / p.target_items);
   chunk = max(chunk, 4);
-  const int chunks_b = slot ? (pages_b + chunk - 1) / chunk : 0;
+  const int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
   int tot_items;
   const int ioff = block_exscan(chunks_b * p.n_kv, &tot_items, s_warp);
   if (slot) {
@@ -198,6 +205,8 @@ struct EmbedParams {
 
 __global__ void __launch_bounds__(256) embed_norm_kernel(const EmbedParams p) {
   __shared__ float s_red[32];
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(p.status) != 0) return;
   const int r = blockIdx.x;
   const int tok = p.tokens[r];
@@ -231,20 +240,29 @@ template <typename Out>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, Out* h, int H,
                                                       float eps, const int* status) {
   __shared__ float s_red[32];
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(status) != 0) return;
   const int r = blockIdx.x;
   norm_row<Out>(x + (long long)r * H, gain, h + (long long)r * H, H, eps, s_red);
 }
 
 // ---------------------------------------------------------------------------
-// acceptance + final-token sampling: one block per slot
+// acceptance + final-token sampling
+//
+// Kernel A (one block per verify row): the row's softmax normaliser from the
+// LM head's per-tile statistics and the target probability of the next draft
+// token; the last row of a sequence to finish runs the acceptance scan.
+// Kernel B (one block per (vocab chunk, sequence)): integer weight sums of the
+// final row over the chunk (residual and plain), the last chunk to finish
+// draws the token.  Integer sums make the draw independent of block order.
 // ---------------------------------------------------------------------------
 
-constexpr int kAccThreads = 512;
+constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
-constexpr int kChunk = 1024;        // elements per chunk sum
-constexpr int kMaxChunks = 512;     // vocab up to 524288
-constexpr int kMaxRowsPerSlot = 64; // gamma_max + 1
+constexpr int kVChunk = 4096;       // vocab entries per sampling block
+constexpr int kPerThread = kVChunk / kAccThreads;
+constexpr int kMaxSampleChunks = 256;  // vocab up to 1M
 
 template <bool FROM_LOGITS>
 struct PSource {
@@ -259,182 +277,241 @@ struct PSource {
   }
 };
 
-template <bool FROM_LOGITS>
-__device__ __forceinline__ unsigned long long weight_at(const PSource<FROM_LOGITS>& src, int row, float M, float S,
-                                                        const float* qrow, int j) {
-  float w = src.p(row, j, M, S);
-  if (qrow) w = fmaxf(0.f, w - qrow[j]);
+__device__ __forceinline__ unsigned long long fixed_weight(float w) {
   return static_cast<unsigned long long>(w * 4294967296.0f);
 }
 
+__device__ __forceinline__ void merge_ms(float& M, float& S, float oM, float oS) {
+  const float nm = fmaxf(M, oM);
+  S = (M == -INFINITY ? 0.f : S * exp2f((M - nm) * kLog2e)) + (oM == -INFINITY ? 0.f : oS * exp2f((oM - nm) * kLog2e));
+  M = nm;
+}
+
 template <bool FROM_LOGITS>
-__global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams p) {
-  __shared__ unsigned long long s_csum[kMaxChunks];
-  __shared__ float s_M[kMaxRowsPerSlot], s_S[kMaxRowsPerSlot];
-  __shared__ float s_redm[kAccWarps], s_reds[kAccWarps];
-  __shared__ int s_a, s_chunk, s_tok, s_resid;
-  __shared__ unsigned long long s_T, s_base;
+__global__ void __launch_bounds__(kAccThreads) accept_rows_kernel(const AcceptParams p) {
+  __shared__ float s_m[kAccWarps], s_s[kAccWarps];
+  __shared__ int s_last;
+  __shared__ int s_ok[64];
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(p.status) != 0) return;
-  if (threadIdx.x == 0) s_tok = -1;
-  const int b = blockIdx.x;
-  const int gam = p.draft_lens[b];
+  const int r = blockIdx.x;
+  const int b = p.row_seq[r];
   const int r0 = p.row_off[b];
-  const int g0 = p.draft_off[b];
-  const int V = p.V;
+  const int i = r - r0;
+  const int gam = p.draft_lens[b];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
-
-  // softmax normaliser of every row of this slot from the LM head's tile statistics
+  const int V = p.V;
+  float M = 0.f, S = 1.f;
   if constexpr (FROM_LOGITS) {
-    for (int i = 0; i <= gam; ++i) {
-      const int r = r0 + i;
-      float M = -INFINITY, S = 0.f;
-      for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
-        const float2 st = p.tile_stats[(long long)tt * p.stats_ld + r];
-        const float nm = fmaxf(M, st.x);
-        S = S * exp2f((M - nm) * kLog2e) + st.y * exp2f((st.x - nm) * kLog2e);
-        M = nm;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float oM = __shfl_xor_sync(0xffffffffu, M, o);
-        const float oS = __shfl_xor_sync(0xffffffffu, S, o);
-        const float nm = fmaxf(M, oM);
-        S = (M == -INFINITY ? 0.f : S * exp2f((M - nm) * kLog2e)) +
-            (oM == -INFINITY ? 0.f : oS * exp2f((oM - nm) * kLog2e));
-        M = nm;
-      }
-      if (lane == 0) {
-        s_redm[warp] = M;
-        s_reds[warp] = S;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float MM = -INFINITY, SS = 0.f;
-        for (int w = 0; w < kAccWarps; ++w) {
-          const float nm = fmaxf(MM, s_redm[w]);
-          SS = (MM == -INFINITY ? 0.f : SS * exp2f((MM - nm) * kLog2e)) +
-               (s_redm[w] == -INFINITY ? 0.f : s_reds[w] * exp2f((s_redm[w] - nm) * kLog2e));
-          MM = nm;
-        }
-        s_M[i] = MM;
-        s_S[i] = SS;
-        p.row_stats[r] = make_float2(MM, SS);
-      }
-      __syncthreads();
+    M = -INFINITY;
+    S = 0.f;
+    for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
+      const float2 st = p.tile_stats[(long long)tt * p.stats_ld + r];
+      merge_ms(M, S, st.x, st.y);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oM = __shfl_xor_sync(0xffffffffu, M, o);
+      const float oS = __shfl_xor_sync(0xffffffffu, S, o);
+      merge_ms(M, S, oM, oS);
+    }
+    if (lane == 0) {
+      s_m[warp] = M;
+      s_s[warp] = S;
+    }
+    __syncthreads();
+    M = -INFINITY;
+    S = 0.f;
+    for (int w = 0; w < kAccWarps; ++w) merge_ms(M, S, s_m[w], s_s[w]);
   }
-
-  // acceptance: first draft that fails u < min(1, p/q) ends the prefix
+  if (threadIdx.x == 0) {
+    if constexpr (FROM_LOGITS) p.row_stats[r] = make_float2(M, S);
+    if (i < gam) {
+      const int x = p.tokens[r + 1];
+      PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
+      p.p_draft[r] = src.p(r, x, M, S);
+    }
+    __threadfence();
+    const int old = atomicAdd(&p.slot_count[b], 1);
+    s_last = old == gam ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // last row of the sequence: every draft's test in parallel, then the first
+  // draft failing u < min(1, p/q) ends the accepted prefix
+  __threadfence();
+  const int g0 = p.draft_off[b];
+  if (threadIdx.x < gam) {
+    const int k = threadIdx.x;
+    const int x = p.tokens[r0 + k + 1];
+    const float pk = __ldcg(&p.p_draft[r0 + k]);
+    const float qk = p.draft_probs[(long long)(g0 + k) * V + x];
+    const float uk = p.uniforms[r0 + k];
+    s_ok[k] = ((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk)) ? 1 : 0;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     int a = gam;
-    for (int i = 0; i < gam; ++i) {
-      const int x = p.tokens[r0 + i + 1];
-      const float pi = src.p(r0 + i, x, FROM_LOGITS ? s_M[i] : 0.f, FROM_LOGITS ? s_S[i] : 1.f);
-      const float qi = p.draft_probs[(long long)(g0 + i) * V + x];
-      const float ui = p.uniforms[r0 + i];
-      const bool ok = (pi >= qi && pi > 0.f) || (__fmul_rn(ui, qi) < pi);
-      if (!ok) {
-        a = i;
+    for (int k = 0; k < gam; ++k) {
+      if (!s_ok[k]) {
+        a = k;
         break;
       }
     }
-    s_a = a;
-    s_resid = a < gam ? 1 : 0;
+    p.accepted[b] = a;
+    p.slot_count[b] = 0;  // ready for the next call
+  }
+}
+
+template <bool FROM_LOGITS>
+__global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams p) {
+  __shared__ unsigned long long s_red[2][kAccWarps];
+  __shared__ unsigned long long s_scan[kAccWarps];
+  __shared__ int s_last, s_mode, s_chunk, s_tok;
+  __shared__ unsigned long long s_T, s_base;
+  __shared__ unsigned long long s_cs[2][kMaxSampleChunks];
+  griddep_launch_dependents();
+  griddep_wait();
+  if (read_status(p.status) != 0) return;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int nch = gridDim.x;
+  const int V = p.V;
+  const int gam = p.draft_lens[b];
+  const int a = p.accepted[b];
+  const int rf = p.row_off[b] + a;
+  const float* qrow = a < gam ? p.draft_probs + (long long)(p.draft_off[b] + a) * V : nullptr;
+  float M = 0.f, S = 1.f;
+  if constexpr (FROM_LOGITS) {
+    const float2 st = p.row_stats[rf];
+    M = st.x;
+    S = st.y;
+  }
+  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // chunk sums of the residual weights max(0, p - q) and of the plain weights p
+  unsigned long long sr = 0, sp = 0;
+  for (int e = threadIdx.x; e < kVChunk; e += kAccThreads) {
+    const int j = c * kVChunk + e;
+    if (j < V) {
+      const float pj = src.p(rf, j, M, S);
+      sp += fixed_weight(pj);
+      if (qrow) sr += fixed_weight(fmaxf(0.f, pj - qrow[j]));
+    }
+  }
+  sr = warp_sum_u64(sr);
+  sp = warp_sum_u64(sp);
+  if (lane == 0) {
+    s_red[0][warp] = sr;
+    s_red[1][warp] = sp;
   }
   __syncthreads();
-  const int a = s_a;
-  const int rf = r0 + a;
-  const float M = FROM_LOGITS ? s_M[a] : 0.f;
-  const float S = FROM_LOGITS ? s_S[a] : 1.f;
-  const int nch = (V + kChunk - 1) / kChunk;
-
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    const float* qrow = s_resid ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
-    for (int c = warp; c < nch; c += kAccWarps) {
-      unsigned long long acc = 0;
-      for (int e = lane; e < kChunk; e += 32) {
-        const int j = c * kChunk + e;
-        if (j < V) acc += weight_at(src, rf, M, S, qrow, j);
-      }
-      acc = warp_sum_u64(acc);
-      if (lane == 0) s_csum[c] = acc;
+  if (threadIdx.x == 0) {
+    unsigned long long tr = 0, tp = 0;
+    for (int w = 0; w < kAccWarps; ++w) {
+      tr += s_red[0][w];
+      tp += s_red[1][w];
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long tot = 0;
-      for (int c = 0; c < nch; ++c) tot += s_csum[c];
-      if (tot == 0 && s_resid) {
-        s_resid = 0;  // max(0, p - q) has no mass: fall back to p
-        s_chunk = -2;
-      } else if (tot == 0) {
-        s_chunk = -1;
-      } else {
-        const unsigned long long U = static_cast<unsigned long long>(p.uniforms[r0 + gam] * 16777216.0f);
-        const unsigned long long hi = __umul64hi(tot, U), lo = tot * U;
-        const unsigned long long T = (hi << 40) | (lo >> 24);
-        unsigned long long cum = 0;
-        int c = 0;
-        while (c < nch - 1 && cum + s_csum[c] <= T) cum += s_csum[c++];
-        s_chunk = c;
-        s_T = T;
-        s_base = cum;
-      }
-    }
-    __syncthreads();
-    if (s_chunk != -2) break;
+    unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
+    cs[c] = tr;
+    cs[p.chunk_ld + c] = tp;
+    __threadfence();
+    const int old = atomicAdd(&p.chunk_count[b], 1);
+    s_last = old == nch - 1 ? 1 : 0;
   }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
 
-  if (s_chunk == -1) {
+  // last chunk of this sequence: pick the mode, the target and the chunk
+  {
+    const unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
+    for (int k = threadIdx.x; k < nch; k += kAccThreads) {
+      s_cs[0][k] = __ldcg(&cs[k]);
+      s_cs[1][k] = __ldcg(&cs[p.chunk_ld + k]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long tr = 0, tp = 0;
+    for (int k = 0; k < nch; ++k) {
+      tr += s_cs[0][k];
+      tp += s_cs[1][k];
+    }
+    // residual after a rejection; plain p for the bonus, or when the residual has no mass
+    const int mode = (qrow && tr > 0) ? 0 : 1;
+    const unsigned long long tot = mode == 0 ? tr : tp;
+    s_mode = mode;
+    if (tot == 0) {
+      s_chunk = -1;
+    } else {
+      const unsigned long long U = static_cast<unsigned long long>(p.uniforms[p.row_off[b] + gam] * 16777216.0f);
+      const unsigned long long hi = __umul64hi(tot, U), lo = tot * U;
+      const unsigned long long T = (hi << 40) | (lo >> 24);
+      unsigned long long cum = 0;
+      int k = 0;
+      const unsigned long long* arr = s_cs[mode];
+      while (k < nch - 1 && cum + arr[k] <= T) cum += arr[k++];
+      s_chunk = k;
+      s_T = T;
+      s_base = cum;
+    }
+    s_tok = -1;
+    p.chunk_count[b] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (s_chunk < 0) {
     if (threadIdx.x == 0) {
       set_status(p.status, SDV_ERR_BAD_INPUT);
-      p.accepted[b] = a;
       p.final_tokens[b] = -1;
     }
     return;
   }
-  if (warp == 0) {
-    const float* qrow = s_resid ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
-    const int c = s_chunk;
-    const unsigned long long T = s_T;
-    const int j0 = c * kChunk + lane * 32;
-    unsigned long long mine = 0;
-    for (int e = 0; e < 32; ++e) {
-      const int j = j0 + e;
-      if (j < V) mine += weight_at(src, rf, M, S, qrow, j);
+  // within the chunk: each thread owns kPerThread consecutive entries
+  const int mode = s_mode;
+  const int j0 = s_chunk * kVChunk + threadIdx.x * kPerThread;
+  unsigned long long mine = 0;
+  for (int e = 0; e < kPerThread; ++e) {
+    const int j = j0 + e;
+    if (j < V) {
+      const float pj = src.p(rf, j, M, S);
+      mine += fixed_weight(mode == 0 ? fmaxf(0.f, pj - qrow[j]) : pj);
     }
-    unsigned long long incl = mine;
+  }
+  unsigned long long incl = mine;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned long long excl = incl - mine;
-    const unsigned long long lo_b = s_base + excl, hi_b = s_base + incl;
-    if (lo_b <= T && T < hi_b) {
-      unsigned long long run = lo_b;
-      int pick = -1;
-      for (int e = 0; e < 32; ++e) {
-        const int j = j0 + e;
-        if (j >= V) break;
-        run += weight_at(src, rf, M, S, qrow, j);
-        if (run > T) {
-          pick = j;
-          break;
-        }
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  unsigned long long woff = 0;
+  for (int w = 0; w < warp; ++w) woff += s_scan[w];
+  const unsigned long long lo_b = s_base + woff + incl - mine, hi_b = s_base + woff + incl;
+  const unsigned long long T = s_T;
+  if (lo_b <= T && T < hi_b) {
+    unsigned long long run = lo_b;
+    for (int e = 0; e < kPerThread; ++e) {
+      const int j = j0 + e;
+      if (j >= V) break;
+      const float pj = src.p(rf, j, M, S);
+      run += fixed_weight(mode == 0 ? fmaxf(0.f, pj - qrow[j]) : pj);
+      if (run > T) {
+        s_tok = j;
+        break;
       }
-      s_tok = pick;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    p.accepted[b] = a;
-    p.final_tokens[b] = s_tok;
-  }
+  if (threadIdx.x == 0) p.final_tokens[b] = s_tok;
 }
 
 __global__ void probs_kernel(const float* z, const float2* row_stats, float* probs, int R, int V,
                              const int* status) {
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(status) != 0) return;
   const long long n = (long long)R * V;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -451,6 +528,8 @@ __global__ void probs_kernel(const float* z, const float2* row_stats, float* pro
 __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignParams p) {
   __shared__ int s_warp[80];
   __shared__ int s_err;
+  griddep_launch_dependents();
+  griddep_wait();
   if (read_status(p.res.status) != 0) return;
   const int b = threadIdx.x;
   const bool slot = b < p.B;
@@ -553,49 +632,45 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
 }  // namespace
 
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream) {
-  prologue_kernel<<<1, kScanThreads, 0, stream>>>(p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(prologue_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
 }
 
 cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
                                    float* x0, float* h, const int* row_pos, float* rope_cs, int R, int H,
                                    int head_dim, float eps, float theta, const int* status, cudaStream_t stream) {
   EmbedParams e{tokens, emb, gain, x0, h, row_pos, rope_cs, H, head_dim, eps, log2(static_cast<double>(theta)), status};
-  embed_norm_kernel<<<R, 256, 0, stream>>>(e);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(embed_norm_kernel, dim3(R), dim3(256), 0, stream, e);
 }
 
 cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
                            int H, float eps, const int* status, cudaStream_t stream) {
-  if (h_f32) rmsnorm_kernel<float><<<R, 256, 0, stream>>>(x, gain, h_f32, H, eps, status);
-  else rmsnorm_kernel<__nv_bfloat16><<<R, 256, 0, stream>>>(x, gain, h_bf16, H, eps, status);
-  note_launch();
-  return cudaGetLastError();
+  if (h_f32) return launch_pdl(rmsnorm_kernel<float>, dim3(R), dim3(256), 0, stream, x, gain, h_f32, H, eps, status);
+  return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(R), dim3(256), 0, stream, x, gain, h_bf16, H, eps, status);
 }
 
-cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
-  if (from_logits) accept_kernel<true><<<p.B, kAccThreads, 0, stream>>>(p);
-  else accept_kernel<false><<<p.B, kAccThreads, 0, stream>>>(p);
-  note_launch();
-  return cudaGetLastError();
+cudaError_t launch_accept(const AcceptParams& p, bool from_logits, int R, cudaStream_t stream) {
+  const dim3 grid((p.V + kVChunk - 1) / kVChunk, p.B);
+  cudaError_t e;
+  if (from_logits) {
+    if ((e = launch_pdl(accept_rows_kernel<true>, dim3(R), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
+    return launch_pdl(sample_kernel<true>, grid, dim3(kAccThreads), 0, stream, p);
+  }
+  if ((e = launch_pdl(accept_rows_kernel<false>, dim3(R), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
+  return launch_pdl(sample_kernel<false>, grid, dim3(kAccThreads), 0, stream, p);
 }
+
+int accept_chunks(int V) { return (V + kVChunk - 1) / kVChunk; }
 
 cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, int R, int V, const int* status,
                          cudaStream_t stream) {
   const long long n = (long long)R * V;
   const long long blocks = (n + 255) / 256;
   const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
-  probs_kernel<<<grid, 256, 0, stream>>>(z, row_stats, probs, R, V, status);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(probs_kernel, dim3(grid), dim3(256), 0, stream, z, row_stats, probs, R, V, status);
 }
 
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream) {
-  realign_kernel<<<1, kScanThreads, 0, stream>>>(p);
-  note_launch();
-  return cudaGetLastError();
+  return launch_pdl(realign_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
 }
 
 }  // namespace sdv

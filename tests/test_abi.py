@@ -81,7 +81,7 @@ def test_host_errors_without_device(lib):
     assert lib.sdv_verify_step(None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_accept(None, None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_realign(None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
-    assert lib.sdv_linear(None, 0, None, None, 1, None) == _abi.SDV_ERR_INVALID_ARG
+    assert lib.sdv_linear(None, 0, None, 0, None, 1, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_attention(None, None, None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_read_status(None, None, None) == _abi.SDV_ERR_INVALID_ARG
     bad = _abi.SdvConfig(256, 4, 3, 64, 768, 1024, 16, 3, 0, 1e-6, 1e6)     # n_q not a multiple of n_kv
