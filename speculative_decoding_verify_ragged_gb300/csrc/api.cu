@@ -43,7 +43,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 // ---------------------------------------------------------------------------
 
 struct Layout {
-  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope;
+  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope, kv_row_off, inv_freq;
   size_t x0, h, h3, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, p_draft, slot_count, chunk_count, chunk_sums, total;
   int chunk_ld;
@@ -69,6 +69,7 @@ static bool config_ok(const sdv_config* c) {
   if (c->hidden % kmul || (c->n_q * c->head_dim) % kmul || c->ffn % kmul) return false;
   if (c->ffn % 64) return false;
   if (c->vocab > 256 * 4096) return false;  // sampling chunk table
+  if (c->hidden > 8 * 1024) return false;   // embedding row held in registers
   return true;
 }
 
@@ -88,7 +89,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   if (tiles_gu > mt) mt = tiles_gu;
   L.max_tiles = mt * rt;
   L.grid_gemm = sms;
-  L.target_items = 8 * sms;
+  L.target_items = 4 * sms;
   L.items_max = L.target_items + static_cast<int>(B) * c.n_kv + 8;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -104,6 +105,8 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.item_off = take((B + 1) * 4);
   L.sched = take(64);
   L.rope = take(R * (c.head_dim / 2) * 2 * 4);
+  L.kv_row_off = take(R * 8);
+  L.inv_freq = take(static_cast<size_t>(c.head_dim / 2) * 8);
   // activations are carried in fp32; the LM head reads a bf16 copy of the final norm
   L.x0 = take(R * H * 4);
   L.h = take(R * H * 4);
@@ -267,6 +270,13 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   cudaError_t e = cudaMemset(c->ws + L.counters, 0, static_cast<size_t>(L.max_tiles) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->ws + L.slot_count, 0, static_cast<size_t>(max_slots) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->ws + L.chunk_count, 0, static_cast<size_t>(max_slots) * 4);
+  if (e == cudaSuccess) {
+    // rotary inverse frequencies theta^(-2j/d), in double, computed once
+    double inv[128];
+    const int half = cfg->head_dim / 2;
+    for (int j = 0; j < half; ++j) inv[j] = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * j / cfg->head_dim);
+    e = cudaMemcpy(c->ws + L.inv_freq, inv, sizeof(double) * half, cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete c;
@@ -327,6 +337,7 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   p.t.item_off = ws_ptr<int>(c, c->L.item_off);
   p.t.sched = ws_ptr<int>(c, c->L.sched);
   p.t.rope_cs = ws_ptr<float>(c, c->L.rope);
+  p.t.kv_row_off = ws_ptr<long long>(c, c->L.kv_row_off);
   p.seq_lens = b->seq_lens;
   p.draft_lens = b->draft_lens;
   p.tokens = b->tokens;
@@ -455,10 +466,14 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
 
   SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
   PrologueParams pp = prologue_params(c, b, status, true);
+  pp.emb = static_cast<const __nv_bfloat16*>(c->w.emb);
+  pp.gain = static_cast<const __nv_bfloat16*>(c->w.g_attn);
+  pp.x0 = f32(c->L.x0);
+  pp.h = f32(c->L.h);
+  pp.H = H;
+  pp.eps = cf.rms_eps;
+  pp.inv_freq = ws_ptr<double>(c, c->L.inv_freq);
   SDV_CUDA(launch_prologue(pp, s));
-  SDV_CUDA(launch_embed_norm_rope(b->tokens, static_cast<const __nv_bfloat16*>(c->w.emb),
-                                  static_cast<const __nv_bfloat16*>(c->w.g_attn), f32(c->L.x0), f32(c->L.h),
-                                  pp.t.row_pos, pp.t.rope_cs, R, H, D, cf.rms_eps, cf.rope_theta, status, s));
   SDV_CUDA(mark(SDV_PHASE_QKV));
   {  // fused QKV + RoPE + KV append
     GemmParams g = gemm_params(c, NQKV, H, R, (NQKV + 127) / 128, nt, status);
@@ -469,6 +484,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.row_seq = pp.t.row_seq;
     g.epi.row_pos = pp.t.row_pos;
     g.epi.rope_cs = pp.t.rope_cs;
+    g.epi.kv_row_off = pp.t.kv_row_off;
     g.epi.n_q = cf.n_q;
     g.epi.n_kv = cf.n_kv;
     g.epi.head_dim = D;

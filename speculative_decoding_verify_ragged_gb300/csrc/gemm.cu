@@ -68,18 +68,30 @@ template <int EPI, int NT, bool XF32>
 __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* epi, int tm, int tn, int tid) {
   constexpr int LD = Cfg<NT, XF32>::EPI_LD;
   const EpiParams& e = p.epi;
+  // rows of this tile that exist; every per-row global load of a batch of
+  // rows is issued before any is used, so the epilogue pays one memory
+  // latency per batch instead of one per row
+  const int rows = min(NT, p.R - tn * NT);
+  constexpr int RB = 16;  // rows per batch
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int col = tm * BM + tid;
     if (col < p.N) {
-      for (int n = 0; n < NT; ++n) {
-        const int r = tn * NT + n;
-        if (r >= p.R) break;
-        const long long o = (long long)r * e.ld_f32 + col;
-        const float v = epi[n * LD + tid];
-        if constexpr (EPI == EPI_F32) {
-          e.out_f32[o] = v;
-        } else {
-          e.out_f32[o] = v + e.resid_f32[o];
+      for (int n0 = 0; n0 < rows; n0 += RB) {
+        float res[RB];
+        if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+          for (int q = 0; q < RB; ++q) {
+            const int n = n0 + q;
+            res[q] = n < rows ? e.resid_f32[(long long)(tn * NT + n) * e.ld_f32 + col] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          if (n < rows) {
+            const float v = epi[n * LD + tid];
+            e.out_f32[(long long)(tn * NT + n) * e.ld_f32 + col] = EPI == EPI_RESID ? v + res[q] : v;
+          }
         }
       }
     }
@@ -87,9 +99,8 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
     const int j = tid & 63;
     const int f = tm * 64 + j;
     if (f < p.N) {
-      for (int n = tid >> 6; n < NT; n += 2) {
+      for (int n = tid >> 6; n < rows; n += 2) {
         const int r = tn * NT + n;
-        if (r >= p.R) break;
         const float gt = epi[n * LD + j];
         const float up = epi[n * LD + 64 + j];
         const float s = gt / (1.0f + expf(-gt));
@@ -105,33 +116,32 @@ __device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* 
       const int j = f - hq * D;
       const bool rot = hq < e.n_q + e.n_kv;
       const int jj = j < half ? j : j - half;
-      for (int n = 0; n < NT; ++n) {
-        const int r = tn * NT + n;
-        if (r >= p.R) break;
-        float x = epi[n * LD + tid];
-        if (rot) {
-          const float c = e.rope_cs[((long long)r * half + jj) * 2];
-          const float s = e.rope_cs[((long long)r * half + jj) * 2 + 1];
-          if (j < half) {
-            const float y = epi[n * LD + tid + half];
-            x = x * c - y * s;
-          } else {
-            const float y = epi[n * LD + tid - half];
-            x = x * c + y * s;
-          }
+      const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
+      const long long head_off = hq < e.n_q ? 0 : ((long long)(hq - e.n_q - kv * e.n_kv) * 2 + kv) * e.page * D + j;
+      for (int n0 = 0; n0 < rows; n0 += RB) {
+        float2 cs[RB];
+        long long dst[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          const int r = tn * NT + (n < rows ? n : 0);
+          cs[q] = rot ? *reinterpret_cast<const float2*>(e.rope_cs + ((long long)r * half + jj) * 2)
+                      : make_float2(1.f, 0.f);
+          dst[q] = hq < e.n_q ? 0 : e.kv_row_off[r];
         }
-        if (hq < e.n_q) {
-          e.out_f32[(long long)r * (e.n_q * D) + f] = x;  // q stays fp32
-        } else {
-          // K and V enter the bf16 cache at (sequence, position)
-          const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
-          const int g = hq - e.n_q - kv * e.n_kv;
-          const int b = e.row_seq[r];
-          const int pos = e.row_pos[r];
-          const int pg = e.page_table[(long long)b * e.max_pages + pos / e.page];
-          const int slot = pos - (pos / e.page) * e.page;
-          const long long idx = ((((long long)pg * e.n_kv + g) * 2 + kv) * e.page + slot) * D + j;
-          e.kv_pool[idx] = f2bf(x);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          if (n < rows) {
+            const int r = tn * NT + n;
+            float x = epi[n * LD + tid];
+            if (rot) {
+              const float y = j < half ? -epi[n * LD + tid + half] : epi[n * LD + tid - half];
+              x = x * cs[q].x + y * cs[q].y;
+            }
+            if (hq < e.n_q) e.out_f32[(long long)r * (e.n_q * D) + f] = x;  // q stays fp32
+            else e.kv_pool[dst[q] + head_off] = f2bf(x);  // K, V enter the bf16 cache
+          }
         }
       }
     }
@@ -201,31 +211,47 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol = policy_evict_first();
       const int my_units = static_cast<int>(u_end - u_begin);
       const int pre = my_units < C::STAGES ? my_units : C::STAGES;
-      auto weights = [&](int j, int stage) {  // weight half-tiles of unit j into a stage
-        const long long u = u_begin + j;
-        const int tile = static_cast<int>(u / p.kb);
-        const int k = static_cast<int>(u - (long long)tile * p.kb);
-        const int tm = tile / p.n_tiles;
-        const int rowA0 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM;
-        const int rowA1 = EPI == EPI_SWIGLU ? tm * 64 : tm * BM + 64;
-        uint8_t* sa = smem + stage * C::STAGE;
-        tma_load_2d_hint(sa, &tmA0, &full[stage], k * BK, rowA0, pol);
-        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], k * BK, rowA1, pol);
+      // unit cursors advance by one k-block at a time: no division per stage
+      struct Cursor {
+        int tile, k, tm, tn;
       };
-      auto acts = [&](int j, int stage) {  // activation tile of unit j into a stage
-        const long long u = u_begin + j;
-        const int tile = static_cast<int>(u / p.kb);
-        const int k = static_cast<int>(u - (long long)tile * p.kb);
-        const int tn = tile - (tile / p.n_tiles) * p.n_tiles;
+      auto start_at = [&](long long u) {
+        Cursor c;
+        c.tile = static_cast<int>(u / p.kb);
+        c.k = static_cast<int>(u - (long long)c.tile * p.kb);
+        c.tm = c.tile / p.n_tiles;
+        c.tn = c.tile - c.tm * p.n_tiles;
+        return c;
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.k == p.kb) {
+          c.k = 0;
+          ++c.tile;
+          if (++c.tn == p.n_tiles) {
+            c.tn = 0;
+            ++c.tm;
+          }
+        }
+      };
+      auto weights = [&](const Cursor& c, int stage) {
+        const int rowA0 = EPI == EPI_SWIGLU ? c.tm * 64 : c.tm * BM;
+        const int rowA1 = EPI == EPI_SWIGLU ? c.tm * 64 : c.tm * BM + 64;
+        uint8_t* sa = smem + stage * C::STAGE;
+        tma_load_2d_hint(sa, &tmA0, &full[stage], c.k * BK, rowA0, pol);
+        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], c.k * BK, rowA1, pol);
+      };
+      auto acts = [&](const Cursor& c, int stage) {
         uint8_t* sb = smem + stage * C::STAGE + A_BYTES;
-        tma_load_2d(sb, &tmX, &full[stage], k * BK, tn * NT);
-        if constexpr (XF32) tma_load_2d(sb + NT * 128, &tmX, &full[stage], k * BK + 32, tn * NT);
+        tma_load_2d(sb, &tmX, &full[stage], c.k * BK, c.tn * NT);
+        if constexpr (XF32) tma_load_2d(sb + NT * 128, &tmX, &full[stage], c.k * BK + 32, c.tn * NT);
       };
       // the weights do not depend on earlier kernels: start streaming them
       // before waiting for the kernel that writes the activations
+      Cursor cw = start_at(u_begin);
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], A_BYTES);
-        weights(j, j);
+        weights(cw, j);
+        advance(cw);
       }
       griddep_wait();
       if (read_status(p.status) != 0) {
@@ -234,9 +260,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
         return;
       }
+      Cursor ca = start_at(u_begin);
       for (int j = 0; j < pre; ++j) {
         mbar_arrive_expect_tx(&full[j], C::STAGE - A_BYTES);
-        acts(j, j);
+        acts(ca, j);
+        advance(ca);
       }
       int stage = pre % C::STAGES;
       uint32_t phase = pre == C::STAGES ? 1u : 0u;
@@ -248,8 +276,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[stage], C::STAGE);
-        weights(j, stage);
-        acts(j, stage);
+        weights(cw, stage);
+        acts(cw, stage);
+        advance(cw);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
@@ -393,20 +422,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int nj = 0; nj < NF; ++nj)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[mi][nj][q] = 0.f;
-      for (int cc = c_first; cc <= c_last; ++cc) {
-        const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
-        const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
-        const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)slot * BM * NT);
+      // pieces are summed in CTA order; the loads of up to four pieces are
+      // issued together
+      for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+        float4 v[4][2][NF];
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
+        for (int q = 0; q < 4; ++q) {
+          const int cc = c0 + q;
+          if (cc <= c_last) {
+            const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
+            const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
+            const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)slot * BM * NT);
 #pragma unroll
-          for (int nj = 0; nj < NF; ++nj) {
-            const float4 v = __ldcg(&src[((warp * 2 + mi) * NF + nj) * 32 + lane]);
-            acc[mi][nj][0] += v.x;
-            acc[mi][nj][1] += v.y;
-            acc[mi][nj][2] += v.z;
-            acc[mi][nj][3] += v.w;
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+              for (int nj = 0; nj < NF; ++nj) v[q][mi][nj] = __ldcg(&src[((warp * 2 + mi) * NF + nj) * 32 + lane]);
           }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (c0 + q <= c_last) {
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+              for (int nj = 0; nj < NF; ++nj) {
+                acc[mi][nj][0] += v[q][mi][nj].x;
+                acc[mi][nj][1] += v[q][mi][nj].y;
+                acc[mi][nj][2] += v[q][mi][nj].z;
+                acc[mi][nj][3] += v[q][mi][nj].w;
+              }
+          }
+        }
       }
       if (threadIdx.x == 0) p.counters[tile] = 0;  // ready for the next launch
     }

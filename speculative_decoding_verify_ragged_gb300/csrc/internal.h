@@ -32,6 +32,7 @@ struct EpiParams {
   const int* row_seq = nullptr;
   const int* row_pos = nullptr;
   const float* rope_cs = nullptr;  // [R, head_dim/2, 2] (cos, sin)
+  const long long* kv_row_off = nullptr;  // [R] element offset of (page, slot) of each row's K/V
   int n_q = 0, n_kv = 0, head_dim = 0, page = 0;
   // LMHEAD
   float2* stats = nullptr;  // [m_tiles, stats_ld]
@@ -100,6 +101,7 @@ struct StepTables {
   int* item_off = nullptr;   // [B+1]
   int* sched = nullptr;      // [4]
   float* rope_cs = nullptr;  // [R, D/2, 2]
+  long long* kv_row_off = nullptr;  // [R]
 };
 
 struct PrologueParams {
@@ -114,13 +116,19 @@ struct PrologueParams {
   int n_kv = 0, head_dim = 0, target_items = 0;
   float rope_theta = 0.f;
   int check_tokens = 1;
+  // embedding + attention pre-norm of every row (verify step only; emb = nullptr skips)
+  const __nv_bfloat16* emb = nullptr;
+  const __nv_bfloat16* gain = nullptr;
+  float* x0 = nullptr;
+  float* h = nullptr;
+  const double* inv_freq = nullptr;  // [head_dim/2] theta^(-2j/head_dim)
+  int H = 0;
+  float eps = 0.f;
 };
+// Validation, row tables and attention schedule (block 0), and with emb set the
+// embedding + RMSNorm + rotary table + KV destination of each row (one block per row).
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
 
-// x0 = emb[tokens] (fp32), h = RMSNorm(x0) * gain (fp32), plus each row's rotary (cos, sin) table.
-cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
-                                   float* x0, float* h, const int* row_pos, float* rope_cs, int R, int H,
-                                   int head_dim, float eps, float theta, const int* status, cudaStream_t stream);
 // h = RMSNorm(x) * gain, written as fp32 (h_f32) or rounded to bf16 (h_bf16).
 cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
                            int H, float eps, const int* status, cudaStream_t stream);

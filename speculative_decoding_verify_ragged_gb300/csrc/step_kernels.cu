@@ -64,12 +64,9 @@ __device__ int block_exscan(int v, int* total, int* s_warp) {
 // prologue: validation + tables + attention schedule (one block)
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kScanThreads) prologue_kernel(const PrologueParams p) {
-  __shared__ int s_warp[80];
+// Block 0: validation, row tables, attention schedule.
+__device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s_poff) {
   __shared__ int s_err;
-  __shared__ int s_poff[kScanThreads + 1];  // first page-check index of each slot
-  griddep_launch_dependents();
-  griddep_wait();  // the previous step's realignment rewrites page tables and counters
   const int b = threadIdx.x;
   if (b == 0) {
     *p.status = 0;
@@ -132,7 +129,7 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
   // attention schedule: chunks of pages sized so that items cover the GPU
   const long long units = (long long)tot_pages * p.n_kv;
   int chunk = static_cast<int>((units + p.target_items - 1) / p.target_items);
-  chunk = max(chunk, 4);
+  chunk = max(chunk, 8);
   const int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
   int tot_items;
   const int ioff = block_exscan(chunks_b * p.n_kv, &tot_items, s_warp);
@@ -189,51 +186,86 @@ __device__ void norm_row(const float* x, const __nv_bfloat16* gain, Out* h, int 
   }
 }
 
-struct EmbedParams {
-  const int* tokens;
-  const __nv_bfloat16* emb;
-  const __nv_bfloat16* gain;
-  float* x0;
-  float* h;
-  const int* row_pos;
-  float* rope_cs;
-  int H, head_dim;
-  float eps;
-  double log2_theta;
-  const int* status;
-};
-
-__global__ void __launch_bounds__(256) embed_norm_kernel(const EmbedParams p) {
+// Every block r: row r's slot and position (scan of the draft lengths), the
+// embedding row into the fp32 residual stream, the attention pre-norm, the
+// rotary (cos, sin) table and the element offset of the row's K/V in the cache.
+// Inputs that would make an access leave its buffer skip the access; block 0
+// reports them in the status word.
+__device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
+  __shared__ int s_b, s_i;
   __shared__ float s_red[32];
-  griddep_launch_dependents();
-  griddep_wait();
-  if (read_status(p.status) != 0) return;
-  const int r = blockIdx.x;
-  const int tok = p.tokens[r];
-  // the embedding row enters the fp32 residual stream
-  const __nv_bfloat16* e = p.emb + (long long)tok * p.H;
-  float* x0 = p.x0 + (long long)r * p.H;
-  for (int k = threadIdx.x * 8; k < p.H; k += blockDim.x * 8) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(e + k);
-    const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(&raw);
-    *reinterpret_cast<float4*>(x0 + k) = make_float4(bf2f(v[0]), bf2f(v[1]), bf2f(v[2]), bf2f(v[3]));
-    *reinterpret_cast<float4*>(x0 + k + 4) = make_float4(bf2f(v[4]), bf2f(v[5]), bf2f(v[6]), bf2f(v[7]));
+  const int t = threadIdx.x;
+  const int gam = t < p.B ? p.draft_lens[t] : 0;
+  int tot;
+  const int roff = block_exscan(t < p.B ? max(gam, 0) + 1 : 0, &tot, s_warp);
+  if (t == 0) s_b = -1;
+  __syncthreads();
+  if (t < p.B && r >= roff && r < roff + max(gam, 0) + 1) {
+    s_b = t;
+    s_i = r - roff;
   }
   __syncthreads();
-  norm_row<float>(x0, p.gain, p.h + (long long)r * p.H, p.H, p.eps, s_red);
-  // rotary table of this row: angle = pos * theta^(-2j/d), reduced mod 2 pi in double
+  const int b = s_b;
+  if (b < 0) return;
+  const int pos = p.seq_lens[b] + s_i;
+  const int tok = p.tokens[r];
+  if (t == 0) {
+    const int pi = pos / p.page;
+    long long off = 0;
+    if (pos >= 0 && pi < p.num_pages[b] && pi < p.max_pages) {
+      const int pg = p.page_table[(long long)b * p.max_pages + pi];
+      if (pg >= 0 && pg < p.pool_pages)
+        off = (long long)pg * p.n_kv * 2 * p.page * p.head_dim + (long long)(pos - pi * p.page) * p.head_dim;
+    }
+    p.t.kv_row_off[r] = off;
+  }
+  // rotary table: angle = pos * inv_freq_j (double), reduced mod 2 pi, then fp32 sincos
   const int half = p.head_dim >> 1;
-  const int pos = p.row_pos[r];
-  for (int j = threadIdx.x; j < half; j += blockDim.x) {
-    const double inv = exp2(-(2.0 * j / p.head_dim) * p.log2_theta);
-    const double ang = static_cast<double>(pos) * inv;
+  for (int j = t; j < half; j += blockDim.x) {
     const double two_pi = 6.283185307179586476925286766559;
-    const double red = ang - two_pi * rint(ang / two_pi);
+    const double ang = static_cast<double>(pos) * p.inv_freq[j];
+    const double red = fma(-rint(ang * (1.0 / two_pi)), two_pi, ang);
     float sn, cs;
     sincosf(static_cast<float>(red), &sn, &cs);
-    p.rope_cs[((long long)r * half + j) * 2] = cs;
-    p.rope_cs[((long long)r * half + j) * 2 + 1] = sn;
+    p.t.rope_cs[((long long)r * half + j) * 2] = cs;
+    p.t.rope_cs[((long long)r * half + j) * 2 + 1] = sn;
   }
+  if (tok < 0 || tok >= p.vocab) return;
+  // embedding row (bf16) -> fp32 residual stream; RMSNorm from registers
+  constexpr int PER = 8;  // values per thread: hidden <= 8 * blockDim
+  const __nv_bfloat16* e = p.emb + (long long)tok * p.H;
+  float* x0 = p.x0 + (long long)r * p.H;
+  float v[PER];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int k = t + q * blockDim.x;
+    v[q] = k < p.H ? bf2f(e[k]) : 0.f;
+    ss += v[q] * v[q];
+  }
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int k = t + q * blockDim.x;
+    if (k < p.H) x0[k] = v[q];
+  }
+  ss = block_sum_256(ss, s_red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
+  float* h = p.h + (long long)r * p.H;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int k = t + q * blockDim.x;
+    if (k < p.H) h[k] = v[q] * inv * bf2f(p.gain[k]);
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) prologue_kernel(const PrologueParams p) {
+  __shared__ int s_warp[80];
+  __shared__ int s_poff[kScanThreads + 1];
+  griddep_launch_dependents();
+  griddep_wait();  // the previous step's realignment rewrites page tables and counters
+  // block 0 validates and builds the tables; block r + 1 prepares row r
+  if (blockIdx.x == 0) validate_and_tables(p, s_warp, s_poff);
+  else embed_row(p, blockIdx.x - 1, s_warp);
 }
 
 template <typename Out>
@@ -632,14 +664,8 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
 }  // namespace
 
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream) {
-  return launch_pdl(prologue_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
-}
-
-cudaError_t launch_embed_norm_rope(const int* tokens, const __nv_bfloat16* emb, const __nv_bfloat16* gain,
-                                   float* x0, float* h, const int* row_pos, float* rope_cs, int R, int H,
-                                   int head_dim, float eps, float theta, const int* status, cudaStream_t stream) {
-  EmbedParams e{tokens, emb, gain, x0, h, row_pos, rope_cs, H, head_dim, eps, log2(static_cast<double>(theta)), status};
-  return launch_pdl(embed_norm_kernel, dim3(R), dim3(256), 0, stream, e);
+  const int grid = p.emb ? p.R + 1 : 1;
+  return launch_pdl(prologue_kernel, dim3(grid), dim3(kScanThreads), 0, stream, p);
 }
 
 cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
