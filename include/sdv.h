@@ -174,6 +174,22 @@ sdv_status sdv_verify_step(sdv_ctx *ctx, const sdv_batch *batch, sdv_result *res
 sdv_status sdv_accept(sdv_ctx *ctx, const float *probs, const sdv_batch *batch,
                       sdv_result *result, void *stream);
 
+/* sdv_accept without a context, a workspace or any allocation.  The pages
+ * describe no such call: it is here for callers that cannot allocate device
+ * memory when they verify (memory carved up once at start-up, work recorded
+ * inside a CUDA-graph capture where cudaMalloc is not allowed, a plugin whose
+ * host owns every allocation).  Same inputs, rule and outputs as sdv_accept;
+ * cfg supplies vocab, page_size, gamma_max (<= 63), n_kv and head_dim.
+ * Scratch lives in one static device array of about 1.4 MB that every GPU
+ * loading the library holds until exit.  Limits: B <= 256, R <= 2048,
+ * vocab <= 262144; beyond them SDV_ERR_CAPACITY and nothing is enqueued.
+ * The first call on a device looks the array up (cudaGetSymbolAddress) with
+ * that device current; make it before any stream capture.  All calls on a
+ * device share the array and it keeps the last call's contents (its
+ * counters are cleared by every call); calls that overlap on the GPU race. */
+sdv_status sdv_accept_static(const sdv_config *cfg, const float *probs, const sdv_batch *batch,
+                             sdv_result *result, void *stream);
+
 /* Step (e) alone from given accepted counts and final tokens (device [B] each,
  * read from result->accepted / result->final_tokens).  Writes emitted
  * tokens/offsets, lengths, pages, free stack and the next-slot view. */

@@ -88,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_verify_step.argtypes = [c_void_p, P(SdvBatch), P(SdvResult), c_void_p]
     lib.sdv_accept.restype = c_int
     lib.sdv_accept.argtypes = [c_void_p, c_void_p, P(SdvBatch), P(SdvResult), c_void_p]
+    lib.sdv_accept_static.restype = c_int
+    lib.sdv_accept_static.argtypes = [P(SdvConfig), c_void_p, P(SdvBatch), P(SdvResult), c_void_p]
     lib.sdv_realign.restype = c_int
     lib.sdv_realign.argtypes = [c_void_p, P(SdvBatch), P(SdvResult), c_void_p]
     lib.sdv_linear.restype = c_int
