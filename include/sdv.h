@@ -180,7 +180,7 @@ sdv_status sdv_accept(sdv_ctx *ctx, const float *probs, const sdv_batch *batch,
  * inside a CUDA-graph capture where cudaMalloc is not allowed, a plugin whose
  * host owns every allocation).  Same inputs, rule and outputs as sdv_accept;
  * cfg supplies vocab, page_size, gamma_max (<= 63), n_kv and head_dim.
- * Scratch lives in one static device array of about 1.4 MB that every GPU
+ * Scratch lives in one static device array of about 1.1 MB that every GPU
  * loading the library holds until exit.  Limits: B <= 256, R <= 2048,
  * vocab <= 262144; beyond them SDV_ERR_CAPACITY and nothing is enqueued.
  * The first call on a device looks the array up (cudaGetSymbolAddress) with

@@ -79,7 +79,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   const size_t H = c.hidden, QD = static_cast<size_t>(c.n_q) * c.head_dim, F = c.ffn, V = c.vocab;
   const size_t NQKV = static_cast<size_t>(c.n_q + 2 * c.n_kv) * c.head_dim;
   L.lm_tiles = static_cast<int>((V + 127) / 128);
-  const int rt = static_cast<int>((R + 15) / 16);
+  const int rt = static_cast<int>((R + 7) / 8);
   const int tiles_qkv = static_cast<int>((NQKV + 127) / 128);
   const int tiles_o = static_cast<int>((H + 127) / 128);
   const int tiles_gu = static_cast<int>((F + 63) / 64);
@@ -191,7 +191,7 @@ static bool encode_kv(CUtensorMap* m, const void* base, const sdv_config& c, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int nt_index(int nt) { return nt == 16 ? 0 : (nt == 32 ? 1 : 2); }
+static int nt_index(int nt) { return nt == 8 ? 0 : (nt == 16 ? 1 : (nt == 32 ? 2 : 3)); }
 
 }  // namespace sdv
 
@@ -204,7 +204,7 @@ struct sdv_ctx {
   uint8_t* ws;
   Layout L;
   CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
-  CUtensorMap tm_h[3], tm_attn[3], tm_act[3], tm_h3[3];
+  CUtensorMap tm_h[4], tm_attn[4], tm_act[4], tm_h3[4];
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -255,8 +255,8 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   bool ok = encode_bf16_2d(&c->tm_qkv, w->w_qkv, NQKV, H, 64) && encode_bf16_2d(&c->tm_o, w->w_o, H, QD, 64) &&
             encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
             encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
-  const int nts[3] = {16, 32, 64};
-  for (int i = 0; i < 3 && ok; ++i) {
+  const int nts[4] = {8, 16, 32, 64};
+  for (int i = 0; i < 4 && ok; ++i) {
     ok = encode_f32_2d(&c->tm_h[i], c->ws + L.h, max_rows, H, nts[i]) &&
          encode_f32_2d(&c->tm_attn[i], c->ws + L.attn, max_rows, QD, nts[i]) &&
          encode_f32_2d(&c->tm_act[i], c->ws + L.act, max_rows, F, nts[i]) &&

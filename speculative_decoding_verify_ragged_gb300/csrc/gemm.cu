@@ -367,6 +367,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               mma_bf16(acc[mi][nj], a[mi], l0, l1);
             }
           }
+        } else if constexpr (NF == 1) {
+          // a single n8 fragment: ldmatrix of the two k-halves of rows 0..7
+          const int chunk = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1;
+          ldsm_x2(b_base + rr * 128 + ((chunk ^ rr) << 4), b0, b1);
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) mma_bf16(acc[mi][0], a[mi], b0, b1);
         } else {
 #pragma unroll
           for (int nj = 0; nj < NF; nj += 2) {
@@ -491,6 +498,7 @@ template <int EPI, bool XF32>
 cudaError_t launch_nt(int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
                       const GemmParams& p, int grid, cudaStream_t stream) {
   switch (nt) {
+    case 8: return launch_t<EPI, 8, XF32>(a0, a1, x, p, grid, stream);
     case 16: return launch_t<EPI, 16, XF32>(a0, a1, x, p, grid, stream);
     case 32: return launch_t<EPI, 32, XF32>(a0, a1, x, p, grid, stream);
     case 64: return launch_t<EPI, 64, XF32>(a0, a1, x, p, grid, stream);
@@ -507,7 +515,7 @@ cudaError_t launch_x(int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap
 
 }  // namespace
 
-int gemm_tile_rows(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+int gemm_tile_rows(int R) { return R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64)); }
 
 cudaError_t launch_gemm(int epi, int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1,
                         const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream) {

@@ -29,7 +29,7 @@ namespace {
 constexpr int kMaxSlots = 256;
 constexpr int kMaxRows = 2048;
 constexpr int kMaxVocab = 262144;
-constexpr int kChunkLd = (kMaxVocab + 4095) / 4096;
+constexpr int kChunkLd = (kMaxVocab + 1023) / 1024;  // sampling chunks of 1024 vocab entries
 
 // Layout (bytes, 256-aligned regions).
 constexpr size_t kAlign = 256;
@@ -86,6 +86,7 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
       b->max_pages_per_seq <= 0 || b->num_pool_pages <= 0)
     return SDV_ERR_INVALID_ARG;
   if (b->B > kMaxSlots || b->R > kMaxRows || cfg->vocab > kMaxVocab) return SDV_ERR_CAPACITY;
+  if (accept_chunks(cfg->vocab) > kChunkLd) return SDV_ERR_INTERNAL;
 
   unsigned char* s = nullptr;
   cudaError_t e = scratch_for_current_device(&s);

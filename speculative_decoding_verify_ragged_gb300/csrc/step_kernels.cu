@@ -292,9 +292,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
-constexpr int kVChunk = 4096;       // vocab entries per sampling block
+constexpr int kVChunk = 1024;       // vocab entries per sampling block
 constexpr int kPerThread = kVChunk / kAccThreads;
-constexpr int kMaxSampleChunks = 256;  // vocab up to 1M
+constexpr int kMaxSampleChunks = 1024;  // vocab up to 1M
 
 template <bool FROM_LOGITS>
 struct PSource {
@@ -465,32 +465,75 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     }
   }
   __syncthreads();
+  // totals of both weight kinds (each thread owns 4 consecutive chunks)
+  unsigned long long own[4];
+  {
+    unsigned long long r4 = 0, p4 = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = threadIdx.x * 4 + q;
+      r4 += k < nch ? s_cs[0][k] : 0ull;
+      p4 += k < nch ? s_cs[1][k] : 0ull;
+    }
+    r4 = warp_sum_u64(r4);
+    p4 = warp_sum_u64(p4);
+    if (lane == 0) {
+      s_red[0][warp] = r4;
+      s_red[1][warp] = p4;
+    }
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     unsigned long long tr = 0, tp = 0;
-    for (int k = 0; k < nch; ++k) {
-      tr += s_cs[0][k];
-      tp += s_cs[1][k];
+    for (int w = 0; w < kAccWarps; ++w) {
+      tr += s_red[0][w];
+      tp += s_red[1][w];
     }
     // residual after a rejection; plain p for the bonus, or when the residual has no mass
     const int mode = (qrow && tr > 0) ? 0 : 1;
     const unsigned long long tot = mode == 0 ? tr : tp;
     s_mode = mode;
-    if (tot == 0) {
-      s_chunk = -1;
-    } else {
+    s_chunk = tot == 0 ? -1 : 0;
+    if (tot != 0) {
       const unsigned long long U = static_cast<unsigned long long>(p.uniforms[p.row_off[b] + gam] * 16777216.0f);
       const unsigned long long hi = __umul64hi(tot, U), lo = tot * U;
-      const unsigned long long T = (hi << 40) | (lo >> 24);
-      unsigned long long cum = 0;
-      int k = 0;
-      const unsigned long long* arr = s_cs[mode];
-      while (k < nch - 1 && cum + arr[k] <= T) cum += arr[k++];
-      s_chunk = k;
-      s_T = T;
-      s_base = cum;
+      s_T = (hi << 40) | (lo >> 24);
     }
     s_tok = -1;
     p.chunk_count[b] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (s_chunk >= 0) {
+    // block-wide exclusive scan of the chosen chunk sums; the thread whose
+    // range holds T names the chunk
+    const unsigned long long* arr = s_cs[s_mode];
+    unsigned long long local = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = threadIdx.x * 4 + q;
+      own[q] = k < nch ? arr[k] : 0ull;
+      local += own[q];
+    }
+    unsigned long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    __syncthreads();
+    unsigned long long run = incl - local;
+    for (int w = 0; w < warp; ++w) run += s_scan[w];
+    const unsigned long long T = s_T;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = threadIdx.x * 4 + q;
+      if (k < nch && run <= T && T < run + own[q]) {
+        s_chunk = k;
+        s_base = run;
+      }
+      run += own[q];
+    }
   }
   __syncthreads();
   if (s_chunk < 0) {
