@@ -158,6 +158,28 @@ def step_algorithmic_bytes(batch):
     return layer + lm + kv_read + kv_write + q_bytes
 
 
+# DRAM traffic of one LM-head launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
+# recorded with a hash of the GEMM sources it was taken on; once those sources change the number no
+# longer describes the kernel and the bench reports null.  Source: profiles/lm_head_gemm_batch_of_one_9b.md
+LM_HEAD_TRAFFIC = {"sources_sha": "be7f323e5fa012a4", "bytes": {2: 1249.52e6}}
+
+
+def gemm_sources_sha():
+    import hashlib
+    d = os.path.join(ROOT, "speculative_decoding_verify_ragged_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def lm_head_traffic(workload):
+    if gemm_sources_sha() != LM_HEAD_TRAFFIC["sources_sha"]:
+        return None
+    return LM_HEAD_TRAFFIC["bytes"].get(workload)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -320,7 +342,8 @@ def run_ours(args):
         "gpu_launches": int(launches),
         "clocks": clk,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "kernel": "LM-head GEMM (EPI_LMHEAD)",
+                     "frac": achieved / hbm, "traffic": lm_head_traffic(args.workload),
+                     "kernel": "LM-head GEMM (EPI_LMHEAD)",
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
                      "avg_launch_us": lm_avg * 1e3},
         "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes,
