@@ -107,14 +107,15 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.rope = take(R * (c.head_dim / 2) * 2 * 4);
   L.kv_row_off = take(R * 8);
   L.inv_freq = take(static_cast<size_t>(c.head_dim / 2) * 8);
-  // activations are carried in fp32; the LM head reads a bf16 copy of the final norm
+  // the residual stream is fp32; GEMM inputs are bf16 hi + lo planes [2, R, K];
+  // the LM head reads one bf16 plane of the final norm
   L.x0 = take(R * H * 4);
-  L.h = take(R * H * 4);
+  L.h = take(2 * R * H * 2);
   L.h3 = take(R * H * 2);
   L.q = take(R * QD * 4);
-  L.attn = take(R * QD * 4);
+  L.attn = take(2 * R * QD * 2);
   L.x1 = take(R * H * 4);
-  L.act = take(R * F * 4);
+  L.act = take(2 * R * (F > QD ? (F > H ? F : H) : (QD > H ? QD : H)) * 2);
   L.x2 = take(R * H * 4);
   L.z = take(R * V * 4);
   L.lmstats = take(static_cast<size_t>(L.lm_tiles) * R * 8);
@@ -257,9 +258,9 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
             encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
   const int nts[4] = {8, 16, 32, 64};
   for (int i = 0; i < 4 && ok; ++i) {
-    ok = encode_f32_2d(&c->tm_h[i], c->ws + L.h, max_rows, H, nts[i]) &&
-         encode_f32_2d(&c->tm_attn[i], c->ws + L.attn, max_rows, QD, nts[i]) &&
-         encode_f32_2d(&c->tm_act[i], c->ws + L.act, max_rows, F, nts[i]) &&
+    ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, 2ull * max_rows, H, nts[i]) &&
+         encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, 2ull * max_rows, QD, nts[i]) &&
+         encode_bf16_2d(&c->tm_act[i], c->ws + L.act, 2ull * max_rows, F, nts[i]) &&
          encode_bf16_2d(&c->tm_h3[i], c->ws + L.h3, max_rows, H, nts[i]);
   }
   if (!ok) {
@@ -379,13 +380,14 @@ static int gemm_grid(sdv_ctx* c, const GemmParams& g) {
   return static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
 }
 
-static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, float* out, int* status,
-                                cudaStream_t s) {
+static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,
+                                long long out_lo_off, int* status, cudaStream_t s) {
   CUtensorMap kv;
   if (!encode_kv(&kv, b->kv_pool, c->cfg, b->num_pool_pages)) return SDV_ERR_CUDA;
   AttnParams a;
   a.q = q;
   a.out = out;
+  a.out_lo_off = out_lo_off;
   a.seq_lens = b->seq_lens;
   a.draft_lens = b->draft_lens;
   a.row_off = ws_ptr<int>(c, c->L.row_off);
@@ -469,7 +471,8 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   pp.emb = static_cast<const __nv_bfloat16*>(c->w.emb);
   pp.gain = static_cast<const __nv_bfloat16*>(c->w.g_attn);
   pp.x0 = f32(c->L.x0);
-  pp.h = f32(c->L.h);
+  pp.h = ws_ptr<__nv_bfloat16>(c, c->L.h);
+  pp.h_lo_off = (long long)c->max_rows * H;
   pp.H = H;
   pp.eps = cf.rms_eps;
   pp.inv_freq = ws_ptr<double>(c, c->L.inv_freq);
@@ -489,11 +492,13 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.n_kv = cf.n_kv;
     g.epi.head_dim = D;
     g.epi.page = cf.page_size;
-    SDV_CUDA(launch_gemm(EPI_QKV, nt, true, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    g.x_lo_row = c->max_rows;
+    SDV_CUDA(launch_gemm(EPI_QKV, nt, 2, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
   }
   SDV_CUDA(mark(SDV_PHASE_ATTN));
   {
-    sdv_status st = run_attention(c, b, f32(c->L.q), f32(c->L.attn), status, s);
+    sdv_status st = run_attention(c, b, f32(c->L.q), ws_ptr<__nv_bfloat16>(c, c->L.attn),
+                                  (long long)c->max_rows * QD, status, s);
     if (st != SDV_OK) return st;
   }
   SDV_CUDA(mark(SDV_PHASE_O));
@@ -502,26 +507,31 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.out_f32 = f32(c->L.x1);
     g.epi.resid_f32 = f32(c->L.x0);
     g.epi.ld_f32 = H;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, true, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
+    g.x_lo_row = c->max_rows;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, 2, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
   }
   SDV_CUDA(mark(SDV_PHASE_FFN));
-  SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn), f32(c->L.h), nullptr, R,
-                          H, cf.rms_eps, status, s));
+  SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn),
+                          ws_ptr<__nv_bfloat16>(c, c->L.h), (long long)c->max_rows * H, R, H, cf.rms_eps, status,
+                          s));
   {  // gate/up + SwiGLU
     GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, nt, status);
-    g.epi.out_f32 = f32(c->L.act);
-    g.epi.ld_f32 = F;
-    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, true, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    g.epi.out_bf16 = ws_ptr<__nv_bfloat16>(c, c->L.act);
+    g.epi.out_lo_off = (long long)c->max_rows * F;
+    g.epi.ld_bf16 = F;
+    g.x_lo_row = c->max_rows;
+    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, 2, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
   }
   {  // down projection + residual
     GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, nt, status);
     g.epi.out_f32 = f32(c->L.x2);
     g.epi.resid_f32 = f32(c->L.x1);
     g.epi.ld_f32 = H;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, true, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
+    g.x_lo_row = c->max_rows;
+    SDV_CUDA(launch_gemm(EPI_RESID, nt, 2, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
   }
-  SDV_CUDA(launch_rmsnorm(f32(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final), nullptr,
-                          ws_ptr<__nv_bfloat16>(c, c->L.h3), R, H, cf.rms_eps, status, s));
+  SDV_CUDA(launch_rmsnorm(f32(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final),
+                          ws_ptr<__nv_bfloat16>(c, c->L.h3), 0, R, H, cf.rms_eps, status, s));
   float* z = r->logits ? r->logits : ws_ptr<float>(c, c->L.z);
   SDV_CUDA(mark(SDV_PHASE_LMHEAD));
   {  // LM head + per-tile softmax statistics
@@ -530,7 +540,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.ld_f32 = V;
     g.epi.stats = ws_ptr<float2>(c, c->L.lmstats);
     g.epi.stats_ld = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, false, &c->tm_lm, &c->tm_lm, &c->tm_h3[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, 1, &c->tm_lm, &c->tm_lm, &c->tm_h3[ni], g, gemm_grid(c, g), s));
   }
   int* accepted = r->accepted ? r->accepted : ws_ptr<int>(c, c->L.accepted);
   int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
@@ -623,14 +633,22 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
   const int nt = gemm_tile_rows(rows);
   CUtensorMap xm;
   const bool xf32 = x_format == 1;
-  if (!(xf32 ? encode_f32_2d(&xm, x, rows, K, nt) : encode_bf16_2d(&xm, x, rows, K, nt))) return SDV_ERR_CUDA;
   // a private status word: the sentinel region after the attention schedule
   int* status = ws_ptr<int>(c, c->L.sched) + 8;
   SDV_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
   GemmParams g = gemm_params(c, N, K, rows, (N + 127) / 128, nt, status);
+  if (xf32) {
+    // fp32 input: split into bf16 hi + lo planes [2, rows, K] in the workspace
+    __nv_bfloat16* planes = ws_ptr<__nv_bfloat16>(c, c->L.act);
+    SDV_CUDA(launch_split_planes(static_cast<const float*>(x), planes, (long long)rows * K, (long long)rows * K, s));
+    if (!encode_bf16_2d(&xm, planes, 2ull * rows, K, nt)) return SDV_ERR_CUDA;
+    g.x_lo_row = rows;
+  } else if (!encode_bf16_2d(&xm, x, rows, K, nt)) {
+    return SDV_ERR_CUDA;
+  }
   g.epi.out_f32 = y;
   g.epi.ld_f32 = N;
-  SDV_CUDA(launch_gemm(EPI_F32, nt, xf32, wm, wm, &xm, g, gemm_grid(c, g), s));
+  SDV_CUDA(launch_gemm(EPI_F32, nt, xf32 ? 2 : 1, wm, wm, &xm, g, gemm_grid(c, g), s));
   return SDV_OK;
 }
 
@@ -639,7 +657,14 @@ sdv_status sdv_attention(sdv_ctx* c, const void* q, const sdv_batch* b, void* ou
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrologueParams pp = prologue_params(c, b, status, false);
   SDV_CUDA(launch_prologue(pp, s));
-  return run_attention(c, b, static_cast<const float*>(q), static_cast<float*>(out), status, s);
+  // the kernel writes bf16 hi + lo planes; a plain fp32 result is their sum,
+  // so stage the planes in the workspace and add them into `out`
+  __nv_bfloat16* planes = ws_ptr<__nv_bfloat16>(c, c->L.attn);
+  const long long n = (long long)b->R * c->cfg.n_q * c->cfg.head_dim;
+  sdv_status st = run_attention(c, b, static_cast<const float*>(q), planes, n, status, s);
+  if (st != SDV_OK) return st;
+  SDV_CUDA(launch_join_planes(planes, n, static_cast<float*>(out), n, s));
+  return SDV_OK;
 }
 
 }  // extern "C"

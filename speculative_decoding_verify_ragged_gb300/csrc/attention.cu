@@ -21,9 +21,10 @@
 //    softmax in fp32.  q (fp32) and the softmax weights enter the MMAs as
 //    bf16 hi + lo pairs, so the output keeps ~17 significant bits against the
 //    bf16 cache;
-//  * items that cover a whole sequence write the fp32 output directly; split
-//    sequences write (max, sum, unnormalised output) partials that a merge
-//    kernel combines (log-sum-exp in base 2).
+//  * items that cover a whole sequence write the output directly (as bf16 hi +
+//    lo planes, the O projection's input); split sequences write (max, sum,
+//    unnormalised output) partials that a merge kernel combines (log-sum-exp
+//    in base 2).
 #include "common.cuh"
 #include "internal.h"
 
@@ -304,11 +305,14 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           if (v < nqv) {
             const float inv = half ? i1 : i0;
             const int i = v / group, h = it.g * group + (v - (v / group) * group);
-            float* dst = p.out + ((long long)(it.r0 + i) * p.n_q + h) * D;
+            const long long base = ((long long)(it.r0 + i) * p.n_q + h) * D;
 #pragma unroll
             for (int nf = 0; nf < NF; ++nf) {
               const int d = nf * 8 + 2 * t;
-              *reinterpret_cast<float2*>(dst + d) = make_float2(o[nf][half * 2] * inv, o[nf][half * 2 + 1] * inv);
+              uint32_t hi, lo;
+              split_bf16x2(o[nf][half * 2] * inv, o[nf][half * 2 + 1] * inv, hi, lo);
+              *reinterpret_cast<uint32_t*>(p.out + base + d) = hi;
+              *reinterpret_cast<uint32_t*>(p.out + p.out_lo_off + base + d) = lo;
             }
           }
         }
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
     L += w * m.y;
     acc += w * po[(long long)c * kAttnQMax * D];
   }
-  p.out[((long long)r * p.n_q + h) * D + d] = acc / L;
+  store_planes(p.out, p.out_lo_off, ((long long)r * p.n_q + h) * D + d, acc / L);
 }
 
 template <int D>

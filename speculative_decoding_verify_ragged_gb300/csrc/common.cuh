@@ -207,6 +207,13 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = *reinterpret_cast<uint32_t*>(&lv);
 }
 
+// x ~ hi + lo stored in two bf16 planes lo_off elements apart (lo_off == 0: hi only)
+__device__ __forceinline__ void store_planes(__nv_bfloat16* hi, long long lo_off, long long idx, float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  hi[idx] = h;
+  if (lo_off) hi[idx + lo_off] = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -13,11 +13,10 @@
 //  * four consumer warps run bf16 mma.sync (m16n8k16, fp32 accumulate) with
 //    the weights as the 16-row A operand and the activations as the 8-column
 //    B operand, so a handful of rows costs no padding of the weight side.
-//    Activations arrive either as bf16 (the LM head's input) or as fp32, in
-//    which case each value is split into bf16 hi + lo parts and both are
-//    multiplied (about 17 significant bits): the layer's activations are
-//    carried in fp32, so no rounding of them compounds from one GEMM to the
-//    next;
+//    Activations arrive as one bf16 plane (the LM head's input) or as two
+//    bf16 planes hi + lo of an fp32 value (about 17 significant bits), each
+//    multiplied by the weights: the layer's activations are carried at that
+//    precision, so no rounding of them compounds from one GEMM to the next;
 //  * work is split stream-K: the (tile, k-block) units of the whole matrix are
 //    cut into one contiguous range per CTA (one CTA per SM), so every SM
 //    streams the same number of bytes whatever the matrix shape.  A tile cut
@@ -26,24 +25,19 @@
 //  * epilogues are fused: RoPE + K/V page scatter after QKV, residual add after
 //    O and down, silu(gate) * up after the gate/up pair, and logits plus
 //    per-tile softmax statistics after the LM head.
-#include "common.cuh"
-#include "internal.h"
+#include "gemm_common.cuh"
 
 namespace sdv {
 
 namespace {
 
-constexpr int BM = 128;               // weight rows per tile
-constexpr int BK = 64;                // k per stage: 128 bytes of bf16 per row
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+using namespace gemm;
 constexpr int CONSUMERS = 4;
 constexpr int THREADS = (CONSUMERS + 1) * kWarp;
 
-constexpr int kSmemBudget = 227 * 1024;
-
-template <int NT, bool XF32>
+template <int NT, int XP>
 struct Cfg {
-  static constexpr int B_BYTES = NT * BK * (XF32 ? 4 : 2);  // fp32: two 32-wide boxes
+  static constexpr int B_BYTES = XP * NT * BK * 2;  // XP activation planes of NT rows x 64 k
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int EPI_LD = BM + 4;  // padded row of the staged accumulator tile
   static constexpr int EPI_BYTES = NT * EPI_LD * 4;
@@ -55,130 +49,11 @@ struct Cfg {
   static_assert(SMEM <= kSmemBudget, "shared memory");
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// CTA c of P owns units [c*T/P, (c+1)*T/P); the CTA owning unit u:
-__device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) {
-  return static_cast<int>(((u + 1) * P - 1) / total);
-}
-
-template <int EPI, int NT, bool XF32>
-__device__ __forceinline__ void epilogue_pass(const GemmParams& p, const float* epi, int tm, int tn, int tid) {
-  constexpr int LD = Cfg<NT, XF32>::EPI_LD;
-  const EpiParams& e = p.epi;
-  // rows of this tile that exist; every per-row global load of a batch of
-  // rows is issued before any is used, so the epilogue pays one memory
-  // latency per batch instead of one per row
-  const int rows = min(NT, p.R - tn * NT);
-  constexpr int RB = 16;  // rows per batch
-  if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
-    const int col = tm * BM + tid;
-    if (col < p.N) {
-      for (int n0 = 0; n0 < rows; n0 += RB) {
-        float res[RB];
-        if constexpr (EPI == EPI_RESID) {
-#pragma unroll
-          for (int q = 0; q < RB; ++q) {
-            const int n = n0 + q;
-            res[q] = n < rows ? e.resid_f32[(long long)(tn * NT + n) * e.ld_f32 + col] : 0.f;
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < RB; ++q) {
-          const int n = n0 + q;
-          if (n < rows) {
-            const float v = epi[n * LD + tid];
-            e.out_f32[(long long)(tn * NT + n) * e.ld_f32 + col] = EPI == EPI_RESID ? v + res[q] : v;
-          }
-        }
-      }
-    }
-  } else if constexpr (EPI == EPI_SWIGLU) {
-    const int j = tid & 63;
-    const int f = tm * 64 + j;
-    if (f < p.N) {
-      for (int n = tid >> 6; n < rows; n += 2) {
-        const int r = tn * NT + n;
-        const float gt = epi[n * LD + j];
-        const float up = epi[n * LD + 64 + j];
-        const float s = gt / (1.0f + expf(-gt));
-        e.out_f32[(long long)r * e.ld_f32 + f] = s * up;
-      }
-    }
-  } else if constexpr (EPI == EPI_QKV) {
-    const int D = e.head_dim;
-    const int half = D >> 1;
-    const int f = tm * BM + tid;
-    if (f < p.N) {
-      const int hq = f / D;
-      const int j = f - hq * D;
-      const bool rot = hq < e.n_q + e.n_kv;
-      const int jj = j < half ? j : j - half;
-      const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
-      const long long head_off = hq < e.n_q ? 0 : ((long long)(hq - e.n_q - kv * e.n_kv) * 2 + kv) * e.page * D + j;
-      for (int n0 = 0; n0 < rows; n0 += RB) {
-        float2 cs[RB];
-        long long dst[RB];
-#pragma unroll
-        for (int q = 0; q < RB; ++q) {
-          const int n = n0 + q;
-          const int r = tn * NT + (n < rows ? n : 0);
-          cs[q] = rot ? *reinterpret_cast<const float2*>(e.rope_cs + ((long long)r * half + jj) * 2)
-                      : make_float2(1.f, 0.f);
-          dst[q] = hq < e.n_q ? 0 : e.kv_row_off[r];
-        }
-#pragma unroll
-        for (int q = 0; q < RB; ++q) {
-          const int n = n0 + q;
-          if (n < rows) {
-            const int r = tn * NT + n;
-            float x = epi[n * LD + tid];
-            if (rot) {
-              const float y = j < half ? -epi[n * LD + tid + half] : epi[n * LD + tid - half];
-              x = x * cs[q].x + y * cs[q].y;
-            }
-            if (hq < e.n_q) e.out_f32[(long long)r * (e.n_q * D) + f] = x;  // q stays fp32
-            else e.kv_pool[dst[q] + head_off] = f2bf(x);  // K, V enter the bf16 cache
-          }
-        }
-      }
-    }
-  } else if constexpr (EPI == EPI_LMHEAD) {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int n = warp; n < NT; n += CONSUMERS) {
-      const int r = tn * NT + n;
-      if (r >= p.R) break;
-      float v[4];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = tm * BM + lane + 32 * i;
-        v[i] = epi[n * LD + lane + 32 * i];
-        if (col < p.N) {
-          e.out_f32[(long long)r * e.ld_f32 + col] = v[i];
-          mx = fmaxf(mx, v[i]);
-        }
-      }
-      mx = warp_max(mx);
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = tm * BM + lane + 32 * i;
-        if (col < p.N) s += exp2f((v[i] - mx) * kLog2e);
-      }
-      s = warp_sum(s);
-      if (lane == 0) e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
-    }
-  }
-}
-
-template <int EPI, int NT, bool XF32>
+template <int EPI, int NT, int XP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
-  using C = Cfg<NT, XF32>;
+  using C = Cfg<NT, XP>;
   constexpr int NF = NT / 8;  // n8 fragments
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
@@ -216,34 +91,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         int tile, k, tm, tn;
       };
       auto start_at = [&](long long u) {
-        Cursor c;
-        c.tile = static_cast<int>(u / p.kb);
-        c.k = static_cast<int>(u - (long long)c.tile * p.kb);
-        c.tm = c.tile / p.n_tiles;
-        c.tn = c.tile - c.tm * p.n_tiles;
-        return c;
+        Cursor cu;
+        cu.tile = static_cast<int>(u / p.kb);
+        cu.k = static_cast<int>(u - (long long)cu.tile * p.kb);
+        cu.tm = cu.tile / p.n_tiles;
+        cu.tn = cu.tile - cu.tm * p.n_tiles;
+        return cu;
       };
-      auto advance = [&](Cursor& c) {
-        if (++c.k == p.kb) {
-          c.k = 0;
-          ++c.tile;
-          if (++c.tn == p.n_tiles) {
-            c.tn = 0;
-            ++c.tm;
+      auto advance = [&](Cursor& cu) {
+        if (++cu.k == p.kb) {
+          cu.k = 0;
+          ++cu.tile;
+          if (++cu.tn == p.n_tiles) {
+            cu.tn = 0;
+            ++cu.tm;
           }
         }
       };
-      auto weights = [&](const Cursor& c, int stage) {
-        const int rowA0 = EPI == EPI_SWIGLU ? c.tm * 64 : c.tm * BM;
-        const int rowA1 = EPI == EPI_SWIGLU ? c.tm * 64 : c.tm * BM + 64;
+      auto weights = [&](const Cursor& cu, int stage) {
+        const int rowA0 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM;
+        const int rowA1 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM + 64;
         uint8_t* sa = smem + stage * C::STAGE;
-        tma_load_2d_hint(sa, &tmA0, &full[stage], c.k * BK, rowA0, pol);
-        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], c.k * BK, rowA1, pol);
+        tma_load_2d_hint(sa, &tmA0, &full[stage], cu.k * BK, rowA0, pol);
+        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, pol);
       };
-      auto acts = [&](const Cursor& c, int stage) {
+      auto acts = [&](const Cursor& cu, int stage) {
         uint8_t* sb = smem + stage * C::STAGE + A_BYTES;
-        tma_load_2d(sb, &tmX, &full[stage], c.k * BK, c.tn * NT);
-        if constexpr (XF32) tma_load_2d(sb + NT * 128, &tmX, &full[stage], c.k * BK + 32, c.tn * NT);
+        tma_load_2d(sb, &tmX, &full[stage], cu.k * BK, cu.tn * NT);
+        if constexpr (XP == 2) tma_load_2d(sb + NT * 128, &tmX, &full[stage], cu.k * BK, p.x_lo_row + cu.tn * NT);
       };
       // the weights do not depend on earlier kernels: start streaming them
       // before waiting for the kernel that writes the activations
@@ -332,7 +207,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         dead = true;
       }
       const uint32_t a_base = smem_u32(smem + stage * C::STAGE);
-      const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         uint32_t a[2][4];
@@ -342,49 +216,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int chunk = kk * 2 + (mat >> 1);
           ldsm_x4(a_base + row * 128 + ((chunk ^ rr) << 4), a[mi][0], a[mi][1], a[mi][2], a[mi][3]);
         }
-        if constexpr (XF32) {
-          // fp32 activations, 128-byte swizzled 32-wide boxes: thread (g, t) needs
-          // x[n = 8 nj + g][16 kk + 2t .. +1] and [.. + 8 .. + 9]; each pair is
-          // split into bf16 hi and lo and multiplied twice
-          const uint32_t box = b_base + (kk >> 1) * (NT * 128);
-          const int c0 = (kk & 1) * 4 + (t >> 1);
-          const int within = (t & 1) * 8;
 #pragma unroll
-          for (int nj = 0; nj < NF; ++nj) {
-            const int n = nj * 8 + g;
-            const uint32_t row = box + n * 128 + within;
-            float2 v0, v1;
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v0.x), "=f"(v0.y) : "r"(row + (((c0) ^ (n & 7)) << 4)));
-            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                         : "=f"(v1.x), "=f"(v1.y)
-                         : "r"(row + (((c0 + 2) ^ (n & 7)) << 4)));
-            uint32_t h0, l0, h1, l1;
-            split_bf16x2(v0.x, v0.y, h0, l0);
-            split_bf16x2(v1.x, v1.y, h1, l1);
+        for (int pl = 0; pl < XP; ++pl) {
+          const uint32_t b_base = a_base + A_BYTES + pl * (NT * 128);
+          if constexpr (NF == 1) {
+            // a single n8 fragment: ldmatrix of the two k-halves of rows 0..7
+            const int chunk = kk * 2 + ((lane >> 3) & 1);
+            uint32_t b0, b1;
+            ldsm_x2(b_base + rr * 128 + ((chunk ^ rr) << 4), b0, b1);
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-              mma_bf16(acc[mi][nj], a[mi], h0, h1);
-              mma_bf16(acc[mi][nj], a[mi], l0, l1);
-            }
-          }
-        } else if constexpr (NF == 1) {
-          // a single n8 fragment: ldmatrix of the two k-halves of rows 0..7
-          const int chunk = kk * 2 + ((lane >> 3) & 1);
-          uint32_t b0, b1;
-          ldsm_x2(b_base + rr * 128 + ((chunk ^ rr) << 4), b0, b1);
+            for (int mi = 0; mi < 2; ++mi) mma_bf16(acc[mi][0], a[mi], b0, b1);
+          } else {
 #pragma unroll
-          for (int mi = 0; mi < 2; ++mi) mma_bf16(acc[mi][0], a[mi], b0, b1);
-        } else {
+            for (int nj = 0; nj < NF; nj += 2) {
+              const int nrow = (nj + (mat >> 1)) * 8 + rr;
+              const int chunk = kk * 2 + (mat & 1);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(b_base + nrow * 128 + ((chunk ^ rr) << 4), b0, b1, b2, b3);
 #pragma unroll
-          for (int nj = 0; nj < NF; nj += 2) {
-            const int nrow = (nj + (mat >> 1)) * 8 + rr;
-            const int chunk = kk * 2 + (mat & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(b_base + nrow * 128 + ((chunk ^ rr) << 4), b0, b1, b2, b3);
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-              mma_bf16(acc[mi][nj], a[mi], b0, b1);
-              mma_bf16(acc[mi][nj + 1], a[mi], b2, b3);
+              for (int mi = 0; mi < 2; ++mi) {
+                mma_bf16(acc[mi][nj], a[mi], b0, b1);
+                mma_bf16(acc[mi][nj + 1], a[mi], b2, b3);
+              }
             }
           }
         }
@@ -478,53 +331,53 @@ __global__ void __launch_bounds__(THREADS, 1)
         epi[(n + 1) * LD + m + 8] = acc[mi][nj][3];
       }
     named_sync(1, CONSUMERS * kWarp);
-    epilogue_pass<EPI, NT, XF32>(p, epi, tm, tn, threadIdx.x);
+    epilogue_rows<EPI, LD>(p, epi, tm, tn * NT, min(NT, p.R - tn * NT), threadIdx.x);
     named_sync(1, CONSUMERS * kWarp);
     u += k1 - k0;
   }
 }
 
-template <int EPI, int NT, bool XF32>
+template <int EPI, int NT, int XP>
 cudaError_t launch_t(const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x, const GemmParams& p,
                      int grid, cudaStream_t stream) {
-  auto kern = gemm_ws_kernel<EPI, NT, XF32>;
-  constexpr int smem = Cfg<NT, XF32>::SMEM;
+  auto kern = gemm_ws_kernel<EPI, NT, XP>;
+  constexpr int smem = Cfg<NT, XP>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), smem, stream, *a0, *a1, *x, p);
 }
 
-template <int EPI, bool XF32>
+template <int EPI, int XP>
 cudaError_t launch_nt(int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
                       const GemmParams& p, int grid, cudaStream_t stream) {
   switch (nt) {
-    case 8: return launch_t<EPI, 8, XF32>(a0, a1, x, p, grid, stream);
-    case 16: return launch_t<EPI, 16, XF32>(a0, a1, x, p, grid, stream);
-    case 32: return launch_t<EPI, 32, XF32>(a0, a1, x, p, grid, stream);
-    case 64: return launch_t<EPI, 64, XF32>(a0, a1, x, p, grid, stream);
+    case 8: return launch_t<EPI, 8, XP>(a0, a1, x, p, grid, stream);
+    case 16: return launch_t<EPI, 16, XP>(a0, a1, x, p, grid, stream);
+    case 32: return launch_t<EPI, 32, XP>(a0, a1, x, p, grid, stream);
+    case 64: return launch_t<EPI, 64, XP>(a0, a1, x, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int EPI>
-cudaError_t launch_x(int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
+cudaError_t launch_x(int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
                      const GemmParams& p, int grid, cudaStream_t stream) {
-  return xf32 ? launch_nt<EPI, true>(nt, a0, a1, x, p, grid, stream)
-              : launch_nt<EPI, false>(nt, a0, a1, x, p, grid, stream);
+  return xp == 2 ? launch_nt<EPI, 2>(nt, a0, a1, x, p, grid, stream)
+                 : launch_nt<EPI, 1>(nt, a0, a1, x, p, grid, stream);
 }
 
 }  // namespace
 
 int gemm_tile_rows(int R) { return R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64)); }
 
-cudaError_t launch_gemm(int epi, int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1,
+cudaError_t launch_gemm(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                         const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream) {
   switch (epi) {
-    case EPI_F32: return launch_x<EPI_F32>(nt, xf32, a0, a1, x, p, grid, stream);
-    case EPI_RESID: return launch_x<EPI_RESID>(nt, xf32, a0, a1, x, p, grid, stream);
-    case EPI_SWIGLU: return launch_x<EPI_SWIGLU>(nt, xf32, a0, a1, x, p, grid, stream);
-    case EPI_QKV: return launch_x<EPI_QKV>(nt, xf32, a0, a1, x, p, grid, stream);
-    case EPI_LMHEAD: return launch_nt<EPI_LMHEAD, false>(nt, a0, a1, x, p, grid, stream);
+    case EPI_F32: return launch_x<EPI_F32>(nt, xp, a0, a1, x, p, grid, stream);
+    case EPI_RESID: return launch_x<EPI_RESID>(nt, xp, a0, a1, x, p, grid, stream);
+    case EPI_SWIGLU: return launch_x<EPI_SWIGLU>(nt, xp, a0, a1, x, p, grid, stream);
+    case EPI_QKV: return launch_x<EPI_QKV>(nt, xp, a0, a1, x, p, grid, stream);
+    case EPI_LMHEAD: return launch_nt<EPI_LMHEAD, 1>(nt, a0, a1, x, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

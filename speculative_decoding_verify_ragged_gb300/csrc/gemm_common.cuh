@@ -1,0 +1,139 @@
+// Pieces shared by the two weight-streaming GEMM kernels (bf16 mma.sync in
+// gemm.cu, tcgen05 with TMEM accumulators in gemm_tc.cu): tile constants, the
+// stream-K split, and the fused epilogues.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sdv {
+namespace gemm {
+
+constexpr int BM = 128;               // weight rows per tile
+constexpr int BK = 64;                // k per stage: 128 bytes of bf16 per row
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int kSmemBudget = 227 * 1024;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// CTA c of P owns units [c*T/P, (c+1)*T/P); the CTA owning unit u:
+__device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) {
+  return static_cast<int>(((u + 1) * P - 1) / total);
+}
+
+// Fused epilogue over rows [row0, row0 + nrows) of one output tile, staged in
+// shared memory as epi[n * LD + m] (n = activation row within the run, m =
+// weight row within the tile); 128 threads, tid = m for the column-wise kinds.
+// Every per-row global load of a batch of rows is issued before any is used,
+// so a batch costs one memory latency instead of one per row.
+template <int EPI, int LD>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const float* epi, int tm, int row0, int nrows,
+                                              int tid) {
+  const EpiParams& e = p.epi;
+  constexpr int RB = 16;  // rows per batch
+  if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
+    const int col = tm * BM + tid;
+    if (col < p.N) {
+      for (int n0 = 0; n0 < nrows; n0 += RB) {
+        float res[RB];
+        if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+          for (int q = 0; q < RB; ++q) {
+            const int n = n0 + q;
+            res[q] = n < nrows ? e.resid_f32[(long long)(row0 + n) * e.ld_f32 + col] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          if (n < nrows) {
+            const float v = epi[n * LD + tid];
+            e.out_f32[(long long)(row0 + n) * e.ld_f32 + col] = EPI == EPI_RESID ? v + res[q] : v;
+          }
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // tile = 64 gate rows + the 64 up rows of the same features; the product
+    // is the next GEMM's input, written as bf16 hi + lo planes
+    const int j = tid & 63;
+    const int f = tm * 64 + j;
+    if (f < p.N) {
+      for (int n = tid >> 6; n < nrows; n += 2) {
+        const float gt = epi[n * LD + j];
+        const float up = epi[n * LD + 64 + j];
+        const float s = gt / (1.0f + expf(-gt));
+        store_planes(e.out_bf16, e.out_lo_off, (long long)(row0 + n) * e.ld_bf16 + f, s * up);
+      }
+    }
+  } else if constexpr (EPI == EPI_QKV) {
+    const int D = e.head_dim;
+    const int half = D >> 1;
+    const int f = tm * BM + tid;
+    if (f < p.N) {
+      const int hq = f / D;
+      const int j = f - hq * D;
+      const bool rot = hq < e.n_q + e.n_kv;
+      const int jj = j < half ? j : j - half;
+      const int kv = hq < e.n_q + e.n_kv ? 0 : 1;
+      const long long head_off =
+          hq < e.n_q ? 0 : ((long long)(hq - e.n_q - kv * e.n_kv) * 2 + kv) * e.page * D + j;
+      for (int n0 = 0; n0 < nrows; n0 += RB) {
+        float2 cs[RB];
+        long long dst[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          const int r = row0 + (n < nrows ? n : 0);
+          cs[q] = rot ? *reinterpret_cast<const float2*>(e.rope_cs + ((long long)r * half + jj) * 2)
+                      : make_float2(1.f, 0.f);
+          dst[q] = hq < e.n_q ? 0 : e.kv_row_off[r];
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          if (n < nrows) {
+            const int r = row0 + n;
+            float x = epi[n * LD + tid];
+            if (rot) {
+              const float y = j < half ? -epi[n * LD + tid + half] : epi[n * LD + tid - half];
+              x = x * cs[q].x + y * cs[q].y;
+            }
+            if (hq < e.n_q) e.out_f32[(long long)r * (e.n_q * D) + f] = x;  // q stays fp32
+            else e.kv_pool[dst[q] + head_off] = f2bf(x);                   // K, V enter the bf16 cache
+          }
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_LMHEAD) {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int n = warp; n < nrows; n += 4) {
+      const int r = row0 + n;
+      float v[4];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = tm * BM + lane + 32 * i;
+        v[i] = epi[n * LD + lane + 32 * i];
+        if (col < p.N) {
+          e.out_f32[(long long)r * e.ld_f32 + col] = v[i];
+          mx = fmaxf(mx, v[i]);
+        }
+      }
+      mx = warp_max(mx);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = tm * BM + lane + 32 * i;
+        if (col < p.N) s += exp2f((v[i] - mx) * kLog2e);
+      }
+      s = warp_sum(s);
+      if (lane == 0) e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
+    }
+  }
+}
+
+}  // namespace gemm
+}  // namespace sdv

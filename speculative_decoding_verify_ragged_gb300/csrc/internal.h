@@ -24,6 +24,9 @@ enum Epi : int {
 struct EpiParams {
   float* out_f32 = nullptr;  // output [R, ld_f32] (QKV: q [R, n_q * head_dim])
   long long ld_f32 = 0;
+  __nv_bfloat16* out_bf16 = nullptr;  // SWIGLU: hi plane [R, ld_bf16]; lo plane out_lo_off further
+  long long out_lo_off = 0;
+  int ld_bf16 = 0;
   const float* resid_f32 = nullptr;  // RESID: residual [R, ld_f32]
   // QKV
   __nv_bfloat16* kv_pool = nullptr;
@@ -46,6 +49,7 @@ struct GemmParams {
   int m_tiles = 0;  // weight tiles (128 rows; SWIGLU: 64 features)
   int n_tiles = 0;  // activation-row tiles
   int kb = 0;       // k-blocks of 64 per tile
+  int x_lo_row = 0; // two-plane activations: row of the lo plane in the activation map
   int int4 = 0;     // weights are int4 group-32
   float* partials = nullptr;  // stream-K partial tiles [2 * grid, 128 * NT]
   int* counters = nullptr;    // per-tile arrival counters, zero between launches
@@ -56,18 +60,26 @@ struct GemmParams {
 // Choose the activation tile for R rows (16, 32 or 64).
 int gemm_tile_rows(int R);
 // Launch the weight-streaming GEMM. a0/a1: weight maps for the two 64-row
-// halves of a 128-row tile (same map for plain GEMMs); x: activation map,
-// bf16 with box (64, nt), or fp32 (xf32) with box (32, nt).
-cudaError_t launch_gemm(int epi, int nt, bool xf32, const CUtensorMap* a0, const CUtensorMap* a1,
+// halves of a 128-row tile (same map for plain GEMMs); x: bf16 activation map
+// with box (64, nt); xp = 1 (one plane) or 2 (hi plane at row 0, lo plane at
+// row p.x_lo_row).
+cudaError_t launch_gemm(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                         const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
+// out[i] = hi[i] + hi[i + lo_off] for i < n (fp32 view of a two-plane activation).
+cudaError_t launch_join_planes(const __nv_bfloat16* hi, long long lo_off, float* out, long long n,
+                               cudaStream_t stream);
+// Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
+cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo_off, long long n,
+                                cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // attention over the paged cache
 // ---------------------------------------------------------------------------
 
 struct AttnParams {
-  const float* q = nullptr;  // [R, n_q, D], rotated
-  float* out = nullptr;      // [R, n_q * D]
+  const float* q = nullptr;           // [R, n_q, D], rotated
+  __nv_bfloat16* out = nullptr;       // hi plane [R, n_q * D]
+  long long out_lo_off = 0;           // lo plane offset (elements)
   const int* seq_lens = nullptr;
   const int* draft_lens = nullptr;
   const int* row_off = nullptr;   // [B+1]
@@ -120,7 +132,8 @@ struct PrologueParams {
   const __nv_bfloat16* emb = nullptr;
   const __nv_bfloat16* gain = nullptr;
   float* x0 = nullptr;
-  float* h = nullptr;
+  __nv_bfloat16* h = nullptr;  // hi plane [R, H]
+  long long h_lo_off = 0;      // lo plane offset (elements)
   const double* inv_freq = nullptr;  // [head_dim/2] theta^(-2j/head_dim)
   int H = 0;
   float eps = 0.f;
@@ -129,8 +142,9 @@ struct PrologueParams {
 // embedding + RMSNorm + rotary table + KV destination of each row (one block per row).
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
 
-// h = RMSNorm(x) * gain, written as fp32 (h_f32) or rounded to bf16 (h_bf16).
-cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
+// h = RMSNorm(x) * gain as bf16 hi + lo planes (lo_off elements apart), or
+// rounded to one bf16 plane (lo_off == 0).
+cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h, long long lo_off, int R,
                            int H, float eps, const int* status, cudaStream_t stream);
 
 struct AcceptParams {

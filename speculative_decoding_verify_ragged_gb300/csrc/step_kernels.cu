@@ -161,9 +161,10 @@ __device__ float block_sum_256(float v, float* s) {
   return t;
 }
 
-// h = x / sqrt(mean(x^2) + eps) * gain for one row; x fp32, h fp32 or bf16.
-template <typename Out>
-__device__ void norm_row(const float* x, const __nv_bfloat16* gain, Out* h, int H, float eps, float* s_red) {
+// h = x / sqrt(mean(x^2) + eps) * gain for one row; x fp32; h as bf16 hi + lo
+// planes lo_off elements apart (lo_off == 0: one rounded plane).
+__device__ void norm_row(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h, long long lo_off, int H,
+                         float eps, float* s_red) {
   float ss = 0.f;
   for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
     const float4 v = *reinterpret_cast<const float4*>(x + k);
@@ -173,16 +174,10 @@ __device__ void norm_row(const float* x, const __nv_bfloat16* gain, Out* h, int 
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
   for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
     const float4 v = *reinterpret_cast<const float4*>(x + k);
-    const float y0 = v.x * inv * bf2f(gain[k]), y1 = v.y * inv * bf2f(gain[k + 1]);
-    const float y2 = v.z * inv * bf2f(gain[k + 2]), y3 = v.w * inv * bf2f(gain[k + 3]);
-    if constexpr (sizeof(Out) == 4) {
-      *reinterpret_cast<float4*>(h + k) = make_float4(y0, y1, y2, y3);
-    } else {
-      uint2 w;
-      w.x = pack_bf16x2(y0, y1);
-      w.y = pack_bf16x2(y2, y3);
-      *reinterpret_cast<uint2*>(h + k) = w;
-    }
+    store_planes(h, lo_off, k, v.x * inv * bf2f(gain[k]));
+    store_planes(h, lo_off, k + 1, v.y * inv * bf2f(gain[k + 1]));
+    store_planes(h, lo_off, k + 2, v.z * inv * bf2f(gain[k + 2]));
+    store_planes(h, lo_off, k + 3, v.w * inv * bf2f(gain[k + 3]));
   }
 }
 
@@ -250,11 +245,11 @@ __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
   }
   ss = block_sum_256(ss, s_red);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
-  float* h = p.h + (long long)r * p.H;
+  __nv_bfloat16* h = p.h + (long long)r * p.H;
 #pragma unroll
   for (int q = 0; q < PER; ++q) {
     const int k = t + q * blockDim.x;
-    if (k < p.H) h[k] = v[q] * inv * bf2f(p.gain[k]);
+    if (k < p.H) store_planes(h, p.h_lo_off, k, v[q] * inv * bf2f(p.gain[k]));
   }
 }
 
@@ -268,15 +263,28 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
   else embed_row(p, blockIdx.x - 1, s_warp);
 }
 
-template <typename Out>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, Out* h, int H,
-                                                      float eps, const int* status) {
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h,
+                                                      long long lo_off, int H, float eps, const int* status) {
   __shared__ float s_red[32];
   griddep_launch_dependents();
   griddep_wait();
   if (read_status(status) != 0) return;
   const int r = blockIdx.x;
-  norm_row<Out>(x + (long long)r * H, gain, h + (long long)r * H, H, eps, s_red);
+  norm_row(x + (long long)r * H, gain, h + (long long)r * H, lo_off, H, eps, s_red);
+}
+
+__global__ void join_planes_kernel(const __nv_bfloat16* hi, long long lo_off, float* out, long long n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    out[i] = __bfloat162float(hi[i]) + __bfloat162float(hi[i + lo_off]);
+}
+
+__global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long long lo_off, long long n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    store_planes(out, lo_off, i, x[i]);
 }
 
 // ---------------------------------------------------------------------------
@@ -711,10 +719,23 @@ cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream) {
   return launch_pdl(prologue_kernel, dim3(grid), dim3(kScanThreads), 0, stream, p);
 }
 
-cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, float* h_f32, __nv_bfloat16* h_bf16, int R,
+cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h, long long lo_off, int R,
                            int H, float eps, const int* status, cudaStream_t stream) {
-  if (h_f32) return launch_pdl(rmsnorm_kernel<float>, dim3(R), dim3(256), 0, stream, x, gain, h_f32, H, eps, status);
-  return launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(R), dim3(256), 0, stream, x, gain, h_bf16, H, eps, status);
+  return launch_pdl(rmsnorm_kernel, dim3(R), dim3(256), 0, stream, x, gain, h, lo_off, H, eps, status);
+}
+
+cudaError_t launch_join_planes(const __nv_bfloat16* hi, long long lo_off, float* out, long long n,
+                               cudaStream_t stream) {
+  const long long blocks = (n + 255) / 256;
+  const int grid = static_cast<int>(blocks < 2048 ? blocks : 2048);
+  return launch_pdl(join_planes_kernel, dim3(grid), dim3(256), 0, stream, hi, lo_off, out, n);
+}
+
+cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo_off, long long n,
+                                cudaStream_t stream) {
+  const long long blocks = (n + 255) / 256;
+  const int grid = static_cast<int>(blocks < 2048 ? blocks : 2048);
+  return launch_pdl(split_planes_kernel, dim3(grid), dim3(256), 0, stream, x, out, lo_off, n);
 }
 
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, int R, cudaStream_t stream) {
