@@ -233,6 +233,14 @@ enum {
  * not ownership. */
 sdv_status sdv_set_phase_events(sdv_ctx *ctx, void *const *events, int n);
 
+/* Which kernel runs the context's GEMMs: SDV_GEMM_AUTO (by row count),
+ * SDV_GEMM_MMA_SYNC (bf16 mma.sync, built for a handful of rows) or
+ * SDV_GEMM_TCGEN05 (5th-generation tensor cores with TMEM accumulators, for
+ * row counts where the contraction is dense).  Results agree up to fp32
+ * summation order.  Host-side setting; takes effect on the next call. */
+enum { SDV_GEMM_AUTO = 0, SDV_GEMM_MMA_SYNC = 1, SDV_GEMM_TCGEN05 = 2 };
+sdv_status sdv_set_gemm_path(sdv_ctx *ctx, int path);
+
 /* Synchronise `stream` and copy the device status word to *host_status. */
 sdv_status sdv_read_status(const int *status, int *host_status, void *stream);
 

@@ -91,6 +91,25 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return b.view(np.float64)
 
 
+def round_bf16_other(x: np.ndarray, nearest: np.ndarray) -> np.ndarray:
+    """The bf16 neighbour of x on the far side from its nearest bf16 value.
+
+    bf16 is sign-magnitude, so the adjacent value away from zero has magnitude
+    bits one higher and the one towards zero one lower; from zero the step
+    goes to the smallest subnormal of x's sign.  A value that is itself bf16
+    has no other neighbour and is returned unchanged.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    nearest = np.asarray(nearest, dtype=np.float64)
+    bits = f64_to_bf16_bits(nearest).astype(np.int32)
+    sign = bits & 0x8000
+    mag = bits & 0x7FFF
+    away = np.abs(x) > np.abs(nearest)
+    step = np.where(away, mag + 1, mag - 1)
+    out = np.where(nearest == 0, np.where(x < 0, 0x8001, 0x0001), sign | step)
+    return np.where(x == nearest, nearest, bf16_to_f64(out.astype(np.uint16)))
+
+
 def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float64 values that are already bf16-representable -> uint16 bits."""
     return (np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
@@ -207,13 +226,21 @@ def gather_kv(kv_pool_f64: np.ndarray, page_table_row: np.ndarray, n: int, page:
 
 def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarray,
             seq_lens, draft_lens, tokens, eps: float = 1e-6, theta: float = 1e6,
-            slots=None):
+            slots=None, flips=None):
     """Target-model forward over every verify row of the selected slots.
 
-    Returns (logits float64 [R, V], probs float64 [R, V], kv_rows) where
+    Returns a dict with logits and probs (float64 [rows, V]), kv_rows where
     kv_rows[(b, pos)] = (k bf16 values [n_kv, d], v [n_kv, d]) for every row
-    written this step.  ``slots`` restricts the pass to some sequences (each
-    sequence's rows depend only on its own cache, so a subset is exact).
+    written this step, the intermediates, and the three rounded quantities
+    before rounding (k_pre, v_pre [rows, n_kv, d]; h3_pre [rows, H]).
+    ``slots`` restricts the pass to some sequences (each sequence's rows
+    depend only on its own cache, so a subset is exact).
+
+    ``flips``: keys ("k" | "v", row, kv_head, j) or ("h3", row, j), row being
+    the global row index; those bf16 roundings take the other neighbour of the
+    exact value instead of the nearest one.  A value within the arithmetic
+    error of a rounding tie may round either way in a finite-precision
+    evaluation; this lets a caller reproduce such a choice.
     """
     H, nq, nkv, d, P = dims["hidden"], dims["n_q"], dims["n_kv"], dims["head_dim"], dims["page"]
     seq_lens = np.asarray(seq_lens)
@@ -242,8 +269,16 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
     k = qkv[:, nq * d: (nq + nkv) * d].reshape(-1, nkv, d)
     v = qkv[:, (nq + nkv) * d:].reshape(-1, nkv, d)
     q = rope(q, row_pos, theta)
-    k = round_bf16(rope(k, row_pos, theta))
-    v = round_bf16(v)
+    k_pre = rope(k, row_pos, theta)
+    v_pre = v
+    k = round_bf16(k_pre)
+    v = round_bf16(v_pre)
+    local = {int(r): n for n, r in enumerate(rows)}
+    for key in (flips or ()):
+        if key[0] in ("k", "v") and int(key[1]) in local:
+            n, hk, j = local[int(key[1])], int(key[2]), int(key[3])
+            tgt, pre = (k, k_pre) if key[0] == "k" else (v, v_pre)
+            tgt[n, hk, j] = round_bf16_other(pre[n, hk, j], tgt[n, hk, j])
 
     # every row's K/V goes into its sequence's pages at its position
     kv_rows = {}
@@ -290,11 +325,17 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
     act = silu(gate) * up
     x2 = x1 + linear(act, weights.proj["down"])
     # final norm (bf16 LM-head input) + LM head + softmax
-    h3 = round_bf16(rmsnorm(x2, bf16_to_f64(weights.g_final), eps))
+    h3_pre = rmsnorm(x2, bf16_to_f64(weights.g_final), eps)
+    h3 = round_bf16(h3_pre)
+    for key in (flips or ()):
+        if key[0] == "h3" and int(key[1]) in local:
+            n, j = local[int(key[1])], int(key[2])
+            h3[n, j] = round_bf16_other(h3_pre[n, j], h3[n, j])
     logits = linear(h3, weights.w_lm)
     probs = softmax(logits)
     return dict(rows=rows, logits=logits, probs=probs, kv_rows=kv_rows,
-                h1=h1, q=q, o=o, x1=x1, act=act, x2=x2, h3=h3)
+                h1=h1, q=q, o=o, x1=x1, act=act, x2=x2, h3=h3,
+                k_pre=k_pre, v_pre=v_pre, h3_pre=h3_pre)
 
 
 # ---------------------------------------------------------------------------

@@ -147,6 +147,10 @@ class VerifyEngine:
         self._check(self.lib.sdv_attention(self.handle, _ptr(q), ctypes.byref(bs), _ptr(out), _ptr(status),
                                            _stream(stream)), "sdv_attention")
 
+    def set_gemm_path(self, path: int):
+        """0 auto (by row count), 1 bf16 mma.sync, 2 tcgen05 with TMEM accumulators."""
+        self._check(self.lib.sdv_set_gemm_path(self.handle, int(path)), "sdv_set_gemm_path")
+
     def set_phase_events(self, events):
         """Record torch.cuda.Event objects at the step's phase boundaries (None = off).
 

@@ -30,6 +30,7 @@ STATUS = {
 SDV_OK, SDV_ERR_INVALID_ARG, SDV_ERR_CAPACITY, SDV_ERR_PAGE_RANGE, SDV_ERR_CUDA, SDV_ERR_TIMEOUT, \
     SDV_ERR_BAD_INPUT, SDV_ERR_UNSUPPORTED, SDV_ERR_INTERNAL = range(9)
 SDV_WEIGHTS_BF16, SDV_WEIGHTS_INT4_G32 = 0, 1
+SDV_GEMM_AUTO, SDV_GEMM_MMA_SYNC, SDV_GEMM_TCGEN05 = 0, 1, 2
 PHASES = ("prologue", "qkv", "attention", "o_proj", "ffn", "lm_head", "accept", "realign")
 
 
@@ -96,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_linear.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_void_p]
     lib.sdv_attention.restype = c_int
     lib.sdv_attention.argtypes = [c_void_p, c_void_p, P(SdvBatch), c_void_p, c_void_p, c_void_p]
+    lib.sdv_set_gemm_path.restype = c_int
+    lib.sdv_set_gemm_path.argtypes = [c_void_p, c_int]
     lib.sdv_set_phase_events.restype = c_int
     lib.sdv_set_phase_events.argtypes = [c_void_p, P(c_void_p), c_int]
     lib.sdv_read_status.restype = c_int

@@ -120,7 +120,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.z = take(R * V * 4);
   L.lmstats = take(static_cast<size_t>(L.lm_tiles) * R * 8);
   L.rowstats = take(R * 8);
-  L.partials = take(static_cast<size_t>(2) * sms * 128 * 64 * 4);
+  L.partials = take(static_cast<size_t>(2) * sms * 128 * 256 * 4);  // two pieces per CTA, tiles up to 256 rows
   L.counters = take(static_cast<size_t>(L.max_tiles) * 4);
   L.part_o = take(static_cast<size_t>(L.items_max) * kAttnQMax * c.head_dim * 4);
   L.part_ml = take(static_cast<size_t>(L.items_max) * kAttnQMax * 8);
@@ -192,7 +192,16 @@ static bool encode_kv(CUtensorMap* m, const void* base, const sdv_config& c, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int nt_index(int nt) { return nt == 8 ? 0 : (nt == 16 ? 1 : (nt == 32 ? 2 : 3)); }
+static int nt_index(int nt) {
+  switch (nt) {
+    case 8: return 0;
+    case 16: return 1;
+    case 32: return 2;
+    case 64: return 3;
+    case 128: return 4;
+    default: return 5;
+  }
+}
 
 }  // namespace sdv
 
@@ -205,7 +214,8 @@ struct sdv_ctx {
   uint8_t* ws;
   Layout L;
   CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
-  CUtensorMap tm_h[4], tm_attn[4], tm_act[4], tm_h3[4];
+  CUtensorMap tm_h[6], tm_attn[6], tm_act[6], tm_h3[6];  // activation tiles of 8..256 rows
+  int gemm_path;
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -250,14 +260,15 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   c->ws = static_cast<uint8_t*>(workspace);
   c->L = L;
   c->timing = false;
+  c->gemm_path = SDV_GEMM_AUTO;
   const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
                  V = cfg->vocab;
   const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
   bool ok = encode_bf16_2d(&c->tm_qkv, w->w_qkv, NQKV, H, 64) && encode_bf16_2d(&c->tm_o, w->w_o, H, QD, 64) &&
             encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
             encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
-  const int nts[4] = {8, 16, 32, 64};
-  for (int i = 0; i < 4 && ok; ++i) {
+  const int nts[6] = {8, 16, 32, 64, 128, 256};
+  for (int i = 0; i < 6 && ok; ++i) {
     ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, 2ull * max_rows, H, nts[i]) &&
          encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, 2ull * max_rows, QD, nts[i]) &&
          encode_bf16_2d(&c->tm_act[i], c->ws + L.act, 2ull * max_rows, F, nts[i]) &&
@@ -288,6 +299,12 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
 }
 
 void sdv_destroy(sdv_ctx* ctx) { delete ctx; }
+
+sdv_status sdv_set_gemm_path(sdv_ctx* ctx, int path) {
+  if (!ctx || path < SDV_GEMM_AUTO || path > SDV_GEMM_TCGEN05) return SDV_ERR_INVALID_ARG;
+  ctx->gemm_path = path;
+  return SDV_OK;
+}
 
 sdv_status sdv_set_phase_events(sdv_ctx* ctx, void* const* events, int n) {
   if (!ctx) return SDV_ERR_INVALID_ARG;
@@ -361,13 +378,12 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   return p;
 }
 
-static GemmParams gemm_params(sdv_ctx* c, int N, int K, int R, int m_tiles, int nt, int* status) {
+static GemmParams gemm_params(sdv_ctx* c, int N, int K, int R, int m_tiles, int* status) {
   GemmParams g;
   g.N = N;
   g.K = K;
   g.R = R;
   g.m_tiles = m_tiles;
-  g.n_tiles = (R + nt - 1) / nt;
   g.kb = K / 64;
   g.partials = ws_ptr<float>(c, c->L.partials);
   g.counters = ws_ptr<int>(c, c->L.counters);
@@ -375,9 +391,21 @@ static GemmParams gemm_params(sdv_ctx* c, int N, int K, int R, int m_tiles, int 
   return g;
 }
 
-static int gemm_grid(sdv_ctx* c, const GemmParams& g) {
+// Rows at and above which the tcgen05 kernel takes the context's GEMMs in
+// SDV_GEMM_AUTO mode (below it the mma.sync kernel's 8-row tiles waste less).
+constexpr int kTcRows = 17;
+
+// Run one GEMM: pick the kernel and the activation tile height, then launch
+// over min(SMs, units) CTAs.  xmaps: the activation map for each tile height.
+static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
+                            const CUtensorMap* xmaps, GemmParams g, cudaStream_t s) {
+  const bool tc = c->gemm_path == SDV_GEMM_TCGEN05 || (c->gemm_path == SDV_GEMM_AUTO && g.R >= kTcRows);
+  const int nt = tc ? gemm_tc_tile_rows(g.R) : gemm_tile_rows(g.R);
+  g.n_tiles = (g.R + nt - 1) / nt;
   const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
-  return static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
+  const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
+  const CUtensorMap* x = &xmaps[nt_index(nt)];
+  return tc ? launch_gemm_tc(epi, nt, xp, a0, a1, x, g, grid, s) : launch_gemm(epi, nt, xp, a0, a1, x, g, grid, s);
 }
 
 static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,
@@ -459,8 +487,6 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   const int R = b->R, H = cf.hidden, D = cf.head_dim, QD = cf.n_q * D, F = cf.ffn, V = cf.vocab;
   const int NQKV = (cf.n_q + 2 * cf.n_kv) * D;
   int* status = r->status;
-  const int nt = gemm_tile_rows(R);
-  const int ni = nt_index(nt);
   auto f32 = [&](size_t off) { return ws_ptr<float>(c, off); };
   auto mark = [&](int k) -> cudaError_t {
     return c->timing && c->phase_ev[k] ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess;
@@ -479,7 +505,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   SDV_CUDA(launch_prologue(pp, s));
   SDV_CUDA(mark(SDV_PHASE_QKV));
   {  // fused QKV + RoPE + KV append
-    GemmParams g = gemm_params(c, NQKV, H, R, (NQKV + 127) / 128, nt, status);
+    GemmParams g = gemm_params(c, NQKV, H, R, (NQKV + 127) / 128, status);
     g.epi.out_f32 = f32(c->L.q);
     g.epi.kv_pool = static_cast<__nv_bfloat16*>(b->kv_pool);
     g.epi.page_table = b->page_table;
@@ -493,7 +519,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.head_dim = D;
     g.epi.page = cf.page_size;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_QKV, nt, 2, &c->tm_qkv, &c->tm_qkv, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(run_gemm(c, EPI_QKV, 2, &c->tm_qkv, &c->tm_qkv, c->tm_h, g, s));
   }
   SDV_CUDA(mark(SDV_PHASE_ATTN));
   {
@@ -503,44 +529,44 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   }
   SDV_CUDA(mark(SDV_PHASE_O));
   {  // O projection + residual
-    GemmParams g = gemm_params(c, H, QD, R, (H + 127) / 128, nt, status);
+    GemmParams g = gemm_params(c, H, QD, R, (H + 127) / 128, status);
     g.epi.out_f32 = f32(c->L.x1);
     g.epi.resid_f32 = f32(c->L.x0);
     g.epi.ld_f32 = H;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, 2, &c->tm_o, &c->tm_o, &c->tm_attn[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_o, &c->tm_o, c->tm_attn, g, s));
   }
   SDV_CUDA(mark(SDV_PHASE_FFN));
   SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn),
                           ws_ptr<__nv_bfloat16>(c, c->L.h), (long long)c->max_rows * H, R, H, cf.rms_eps, status,
                           s));
   {  // gate/up + SwiGLU
-    GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, nt, status);
+    GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, status);
     g.epi.out_bf16 = ws_ptr<__nv_bfloat16>(c, c->L.act);
     g.epi.out_lo_off = (long long)c->max_rows * F;
     g.epi.ld_bf16 = F;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_SWIGLU, nt, 2, &c->tm_gate, &c->tm_up, &c->tm_h[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(run_gemm(c, EPI_SWIGLU, 2, &c->tm_gate, &c->tm_up, c->tm_h, g, s));
   }
   {  // down projection + residual
-    GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, nt, status);
+    GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, status);
     g.epi.out_f32 = f32(c->L.x2);
     g.epi.resid_f32 = f32(c->L.x1);
     g.epi.ld_f32 = H;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_RESID, nt, 2, &c->tm_down, &c->tm_down, &c->tm_act[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_down, &c->tm_down, c->tm_act, g, s));
   }
   SDV_CUDA(launch_rmsnorm(f32(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final),
                           ws_ptr<__nv_bfloat16>(c, c->L.h3), 0, R, H, cf.rms_eps, status, s));
   float* z = r->logits ? r->logits : ws_ptr<float>(c, c->L.z);
   SDV_CUDA(mark(SDV_PHASE_LMHEAD));
   {  // LM head + per-tile softmax statistics
-    GemmParams g = gemm_params(c, V, H, R, c->L.lm_tiles, nt, status);
+    GemmParams g = gemm_params(c, V, H, R, c->L.lm_tiles, status);
     g.epi.out_f32 = z;
     g.epi.ld_f32 = V;
     g.epi.stats = ws_ptr<float2>(c, c->L.lmstats);
     g.epi.stats_ld = c->max_rows;
-    SDV_CUDA(launch_gemm(EPI_LMHEAD, nt, 1, &c->tm_lm, &c->tm_lm, &c->tm_h3[ni], g, gemm_grid(c, g), s));
+    SDV_CUDA(run_gemm(c, EPI_LMHEAD, 1, &c->tm_lm, &c->tm_lm, c->tm_h3, g, s));
   }
   int* accepted = r->accepted ? r->accepted : ws_ptr<int>(c, c->L.accepted);
   int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
@@ -630,25 +656,26 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
     case 4: wm = &c->tm_down; N = H; K = F; break;
     default: wm = &c->tm_lm; N = cf.vocab; K = H; break;
   }
-  const int nt = gemm_tile_rows(rows);
-  CUtensorMap xm;
   const bool xf32 = x_format == 1;
   // a private status word: the sentinel region after the attention schedule
   int* status = ws_ptr<int>(c, c->L.sched) + 8;
   SDV_CUDA(cudaMemsetAsync(status, 0, sizeof(int), s));
-  GemmParams g = gemm_params(c, N, K, rows, (N + 127) / 128, nt, status);
+  GemmParams g = gemm_params(c, N, K, rows, (N + 127) / 128, status);
+  const void* xsrc = x;
   if (xf32) {
     // fp32 input: split into bf16 hi + lo planes [2, rows, K] in the workspace
     __nv_bfloat16* planes = ws_ptr<__nv_bfloat16>(c, c->L.act);
     SDV_CUDA(launch_split_planes(static_cast<const float*>(x), planes, (long long)rows * K, (long long)rows * K, s));
-    if (!encode_bf16_2d(&xm, planes, 2ull * rows, K, nt)) return SDV_ERR_CUDA;
+    xsrc = planes;
     g.x_lo_row = rows;
-  } else if (!encode_bf16_2d(&xm, x, rows, K, nt)) {
-    return SDV_ERR_CUDA;
   }
+  CUtensorMap xm[6];
+  const int nts[6] = {8, 16, 32, 64, 128, 256};
+  for (int i = 0; i < 6; ++i)
+    if (!encode_bf16_2d(&xm[i], xsrc, (xf32 ? 2ull : 1ull) * rows, K, nts[i])) return SDV_ERR_CUDA;
   g.epi.out_f32 = y;
   g.epi.ld_f32 = N;
-  SDV_CUDA(launch_gemm(EPI_F32, nt, xf32 ? 2 : 1, wm, wm, &xm, g, gemm_grid(c, g), s));
+  SDV_CUDA(run_gemm(c, EPI_F32, xf32 ? 2 : 1, wm, wm, xm, g, s));
   return SDV_OK;
 }
 

@@ -68,6 +68,10 @@ cudaError_t launch_gemm(int epi, int nt, int xp, const CUtensorMap* a0, const CU
 // out[i] = hi[i] + hi[i + lo_off] for i < n (fp32 view of a two-plane activation).
 cudaError_t launch_join_planes(const __nv_bfloat16* hi, long long lo_off, float* out, long long n,
                                cudaStream_t stream);
+// The same GEMM on tcgen05 / TMEM (nt in {16, 32, 64, 128, 256}).
+int gemm_tc_tile_rows(int R);
+cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
+                           const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
 cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo_off, long long n,
                                 cudaStream_t stream);

@@ -26,3 +26,14 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def nine_b_weights():
+    """The 9B-class layer + LM head (seed 2) on the host and on cuda:0, shared by the GPU modules."""
+    import torch
+    assert torch.cuda.is_available()
+    import workloads as wl
+    from workloads import device as wd
+    W = wl.make_weights(wl.NINE_B, 2)
+    return W, wd.weights_to_device(W)

@@ -50,17 +50,121 @@ def to_numpy(d: dict) -> dict:
     return out
 
 
-def compare_logits(z_gpu, z_or, p_gpu=None, p_or=None):
-    rms = float(np.sqrt(np.mean(z_or ** 2)))
-    dz = float(np.max(np.abs(z_gpu.astype(np.float64) - z_or)))
-    assert dz <= LOGIT_TOL_REL_RMS * rms, f"logits: max|d| {dz:.3e} > {LOGIT_TOL_REL_RMS} * rms {rms:.3e}"
+# ---------------------------------------------------------------------------
+# roundings that either side may take
+# ---------------------------------------------------------------------------
+# K, V and the LM-head input are rounded to bf16 from values the GPU carries
+# with an absolute error of about 2^-18 times the rms of the vector they
+# belong to (one K/V head, or the row of h3): fp32 activations enter the
+# tensor cores as bf16 hi + lo (16 significant bits) and fp32 accumulation
+# adds less; the largest disagreement seen on the 9B-class layer is 2^-17.
+# Any bf16 value that rounds from a point within TIE_WINDOW * rms of the exact
+# value is a valid result: the nearest one, its other neighbour when the
+# exact value sits near a tie, and, for elements much smaller than the rms,
+# values a few spacings away.  The window is 8x the largest seen error.
+TIE_WINDOW = 2.0 ** -14
+MAX_CANDIDATES = 12
+
+
+def _tie_distance(pre, axis):
+    near = o.round_bf16(pre)
+    far = o.round_bf16_other(pre, near)
+    scale = np.sqrt(np.mean(pre ** 2, axis=axis, keepdims=True))
+    d = np.abs(pre - 0.5 * (near + far)) / np.maximum(scale, 1e-300)
+    return np.where(near == pre, np.inf, d), near, far
+
+
+def check_kv_written(batch, fw, pool, pt_before):
+    """Each verified row's K/V sits in its page at position L + i and is a bf16
+    rounding of a point within TIE_WINDOW * rms of the oracle's exact value.
+    Returns the number of elements that differ from the nearest rounding."""
+    page = batch.dims["page"]
+    offs = wl.row_offsets(batch.draft_lens)
+    local = {int(r): n for n, r in enumerate(fw["rows"])}
+    other = 0
+    for (b, pos) in fw["kv_rows"]:
+        n = local[int(offs[b]) + pos - int(batch.seq_lens[b])]
+        pg = pt_before[b, pos // page]
+        for kind, kv in (("k", 0), ("v", 1)):
+            got = o.bf16_to_f64(pool[pg, :, kv, pos % page, :])
+            pre = fw[kind + "_pre"][n]
+            e = TIE_WINDOW * np.sqrt(np.mean(pre ** 2, axis=1, keepdims=True))
+            ok = (o.round_bf16(pre - e) <= got) & (got <= o.round_bf16(pre + e))
+            assert ok.all(), (kind, b, pos, np.argwhere(~ok)[:4])
+            other += int(np.count_nonzero(got != o.round_bf16(pre)))
+    return other
+
+
+def _row_errors(z_gpu, p_gpu, z_or, p_or, tol):
+    dz = np.max(np.abs(z_gpu.astype(np.float64) - z_or), axis=-1)
+    bad = dz > tol
     if p_gpu is not None:
         dp = np.abs(p_gpu.astype(np.float64) - p_or)
-        assert float(dp.max()) <= PROB_TOL_ABS, f"probs: max|d| {dp.max():.3e}"
-        big = p_or > 1e-7
-        rel = float((dp[big] / p_or[big]).max())
-        assert rel <= PROB_TOL_REL, f"probs: max rel {rel:.3e}"
-    return dz / rms
+        rel = np.where(p_or > 1e-7, dp / np.maximum(p_or, 1e-300), 0.0)
+        bad |= (dp.max(-1) > PROB_TOL_ABS) | (rel.max(-1) > PROB_TOL_REL)
+    return dz, bad
+
+
+def compare_step(batch, W, fw, z_gpu, p_gpu=None):
+    """Logits within LOGIT_TOL_REL_RMS * rms and probabilities within PROB_TOL_ABS
+    (and PROB_TOL_REL) of the oracle.  A sequence with a row outside must match,
+    within the same tolerances, the oracle's result under some choice of the
+    other rounding for K/V/h3 values inside the tie window (its rows up to the
+    failing one, the nearest MAX_CANDIDATES ties): a result that is just as
+    valid.  Returns (probs the acceptance check should use, {slot: flips}).
+    """
+    z_or, p_or = fw["logits"], fw["probs"]
+    rms = float(np.sqrt(np.mean(z_or ** 2)))
+    tol = LOGIT_TOL_REL_RMS * rms
+    dz, bad = _row_errors(z_gpu, p_gpu, z_or, p_or, tol)
+    p_valid = p_or.copy()
+    explained = {}
+    if not bad.any():
+        return p_valid, explained
+    offs = wl.row_offsets(batch.draft_lens)
+    row_slot = np.repeat(np.arange(batch.B), np.asarray(batch.draft_lens) + 1)
+    slots = sorted(set(int(row_slot[r]) for r in np.nonzero(bad)[0]))
+    assert len(slots) <= max(2, batch.B // 4), f"{len(slots)} sequences outside tolerance: {dz.max() / rms:.3e} rms"
+    args = (batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens, batch.tokens)
+    for b in slots:
+        r0, r1 = int(offs[b]), int(offs[b + 1])
+        bad_rows = [r for r in range(r0, r1) if bad[r]]
+        last = max(bad_rows)
+        cands = []
+        for r in range(r0, last + 1):
+            for kind in ("k", "v"):
+                d = _tie_distance(fw[kind + "_pre"][r], axis=1)[0]
+                for h, j in np.argwhere(d <= TIE_WINDOW):
+                    cands.append((float(d[h, j]), (kind, r, int(h), int(j))))
+        for r in bad_rows:
+            d = _tie_distance(fw["h3_pre"][r], axis=0)[0]
+            for j in np.nonzero(d <= TIE_WINDOW)[0]:
+                cands.append((float(d[j]), ("h3", r, int(j))))
+        cands = [c for _, c in sorted(cands)[:MAX_CANDIDATES]]
+        assert cands, f"slot {b}: rows {bad_rows} outside tolerance ({dz[bad_rows].max() / rms:.3e} rms), no tie in reach"
+        sel = [r - r0 for r in bad_rows]
+        err = (z_gpu[bad_rows].astype(np.float64) - z_or[bad_rows]).ravel()
+        eff = np.stack([(o.forward(*args, slots=[b], flips={c})["logits"][sel] - z_or[bad_rows]).ravel()
+                        for c in cands])
+        # fewest flips first: the first choice that leaves the rows well inside the
+        # tolerance (half of it, before the exact re-run), else the closest one
+        best, best_res = None, np.inf
+        for mask in sorted(range(1, 1 << len(cands)), key=lambda m: (bin(m).count("1"), m)):
+            pick = [i for i in range(len(cands)) if mask >> i & 1]
+            res = float(np.max(np.abs(err - eff[pick].sum(0))))
+            if res < best_res:
+                best, best_res = pick, res
+            if res <= 0.5 * tol:
+                break
+        flips = {cands[i] for i in best}
+        alt = o.forward(*args, slots=[b], flips=flips)
+        _, still = _row_errors(z_gpu[r0:r1], None if p_gpu is None else p_gpu[r0:r1], alt["logits"],
+                               alt["probs"], tol)
+        assert not still.any(), (f"slot {b}: rows {bad_rows} outside tolerance ({dz[bad_rows].max() / rms:.3e} rms) "
+                                 f"under every tie choice tried")
+        p_valid[r0:r1] = alt["probs"]
+        explained[b] = sorted(flips)
+    return p_valid, explained
 
 
 def _ambiguous(p, q, u, rel=DECISION_REL):

@@ -84,6 +84,7 @@ def test_host_errors_without_device(lib):
     assert lib.sdv_linear(None, 0, None, 0, None, 1, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_attention(None, None, None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_read_status(None, None, None) == _abi.SDV_ERR_INVALID_ARG
+    assert lib.sdv_set_gemm_path(None, 0) == _abi.SDV_ERR_INVALID_ARG
     bad = _abi.SdvConfig(256, 4, 3, 64, 768, 1024, 16, 3, 0, 1e-6, 1e6)     # n_q not a multiple of n_kv
     assert lib.sdv_workspace_size(ctypes.byref(bad), 8, 2) == 0
 

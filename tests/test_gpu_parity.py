@@ -65,13 +65,6 @@ def test_linear_tiny(tiny_engine, rows, which, xfmt):
     assert err <= tol * scale + 1e-6, (err, scale)
 
 
-@pytest.fixture(scope="module")
-def nine_b_weights(torch_cuda):
-    from workloads import device as wd
-    W = wl.make_weights(wl.NINE_B, 2)
-    return W, wd.weights_to_device(W)
-
-
 @pytest.mark.parametrize("rows", [8, 24, 64])
 def test_linear_lm_head_full_size_sampled(nine_b_weights, rows):
     """LM head at full size (151936 x 4096): sampled output columns against float64 dots."""
@@ -264,16 +257,11 @@ def _full_step_check(eng, W, batch, name):
     assert status == 0, f"{name}: status {status}"
     ref = o.verify_step(batch, W)
     fw = ref["forward"]
-    gh.compare_logits(res["logits"], fw["logits"], res["probs"], fw["probs"])
-    # every row's K/V landed in its page at position L + i
-    P = batch.dims["page"]
-    pool = dev["kv_pool"]
-    for (b, pos), (k, v) in fw["kv_rows"].items():
-        pg = pt_before[b, pos // P]
-        for kv, ref_rows in ((0, k), (1, v)):
-            got = o.bf16_to_f64(pool[pg, :, kv, pos % P, :])
-            assert np.all(np.abs(got - ref_rows) <= 2 ** -7 * np.abs(ref_rows) + 2e-3), (name, b, pos, kv)
-    judged = gh.check_acceptance(batch, fw["probs"], res["accepted"], res["final_tokens"])
+    p_valid, explained = gh.compare_step(batch, W, fw, res["logits"], res["probs"])
+    # every row's K/V landed in its page at position L + i, rounded as the oracle
+    # rounds it (or, within the tie window, to the other neighbour)
+    gh.check_kv_written(batch, fw, dev["kv_pool"], pt_before)
+    judged = gh.check_acceptance(batch, p_valid, res["accepted"], res["final_tokens"])
     if np.array_equal(res["accepted"], ref["accepted"]):
         ra = ref["realign"]
         assert np.array_equal(res["new_seq_lens"], ra["new_seq_lens"])

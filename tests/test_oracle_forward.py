@@ -35,6 +35,25 @@ def test_round_bf16_matches_torch():
     assert o.round_bf16(np.array([-(1 + 2 ** -8 + 2 ** -30)]))[0] == -(1 + 2 ** -7)
 
 
+def test_round_bf16_other_is_the_far_neighbour():
+    """The other rounding of x is the adjacent bf16 value on x's far side."""
+    g = np.random.default_rng(5)
+    x32 = (g.standard_normal(50000) * np.exp(g.uniform(-10, 10, 50000))).astype(np.float32)
+    x = x32.astype(np.float64)
+    near = o.round_bf16(x)
+    far = o.round_bf16_other(x, near)
+    t = torch.from_numpy(near.astype(np.float32)).to(torch.bfloat16)
+    up = torch.nextafter(t, torch.full_like(t, float("inf"))).double().numpy()
+    down = torch.nextafter(t, torch.full_like(t, float("-inf"))).double().numpy()
+    exact = x == near
+    assert np.array_equal(far[exact], near[exact])
+    m = ~exact
+    assert np.array_equal(far[m], np.where(x[m] > near[m], up[m], down[m]))
+    # across a power of two the spacing changes: 1 - 2^-10 rounds to 1, its far neighbour is 1 - 2^-8
+    assert o.round_bf16_other(np.array([1 - 2 ** -10]), np.array([1.0]))[0] == 1 - 2 ** -8
+    assert o.round_bf16_other(np.array([1 + 2 ** -9]), np.array([1.0]))[0] == 1 + 2 ** -7
+
+
 def test_bf16_decode_matches_torch():
     bits = np.arange(0, 65536, 7, dtype=np.uint16)
     bits = bits[((bits >> 7) & 0xFF) != 0xFF]          # skip inf/nan
@@ -200,6 +219,32 @@ def test_kv_written_at_row_positions(tiny):
     h1 = torch.from_numpy(fw["h1"][0:1])
     k_raw = F.linear(h1, _w(W.proj["qkv"]))[0, nq * d:(nq + nkv) * d].reshape(nkv, d)
     assert np.allclose(fw["kv_rows"][(0, 0)][0], _bf(k_raw.numpy()).numpy(), rtol=2 ** -8, atol=0)
+
+
+def test_forward_flips_take_the_other_rounding(tiny):
+    """A flipped K/V element holds the far bf16 neighbour of its exact value; a flipped
+    h3 element moves the logits by exactly (its change) x (its LM-head column)."""
+    W, batch = tiny
+    args = (batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens, batch.tokens)
+    fw = o.forward(*args)
+    same = o.forward(*args, flips=set())
+    assert np.array_equal(fw["logits"], same["logits"])
+    r = int(wl.row_offsets(batch.draft_lens)[2]) + 1          # slot 2, draft row 1
+    pos = int(batch.seq_lens[2]) + 1
+    fk = o.forward(*args, flips={("k", r, 1, 5), ("v", r, 0, 7)})
+    k0, v0 = fw["kv_rows"][(2, pos)]
+    k1, v1 = fk["kv_rows"][(2, pos)]
+    assert np.count_nonzero(k0 != k1) == 1 and np.count_nonzero(v0 != v1) == 1
+    assert k1[1, 5] == o.round_bf16_other(fw["k_pre"][r, 1, 5], k0[1, 5])
+    assert v1[0, 7] == o.round_bf16_other(fw["v_pre"][r, 0, 7], v0[0, 7])
+    # rows before the flipped one in its sequence, and other sequences, are unchanged
+    assert np.array_equal(fk["logits"][:r], fw["logits"][:r])
+    assert not np.array_equal(fk["logits"][r], fw["logits"][r])
+    fh = o.forward(*args, flips={("h3", r, 11)})
+    dh = fh["h3"][r, 11] - fw["h3"][r, 11]
+    assert dh != 0 and np.array_equal(np.delete(fh["h3"][r], 11), np.delete(fw["h3"][r], 11))
+    col = o.bf16_to_f64(W.w_lm[:, 11])
+    assert np.allclose(fh["logits"][r] - fw["logits"][r], dh * col, rtol=1e-9, atol=1e-12)
 
 
 def test_causal_inside_draft_block(tiny):
