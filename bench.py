@@ -49,6 +49,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling run: no clock pre-roll, no e2e or CPU legs (its numbers are not bench values)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="roofline crossover sweep: B in {1,4,16,32,64,128} x gamma in {0,1,2,3,4,7,8}, ctx 2048; "
+                         "one JSON line per point, then a summary line")
+    ap.add_argument("--sweep-points", default=None,
+                    help="subset of the sweep as B:gamma pairs, e.g. 1:7,32:7,128:8")
+    ap.add_argument("--gemm-path", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM kernel: 0 auto by row count, 1 mma.sync, 2 tcgen05")
     return ap.parse_args()
 
 
@@ -149,13 +156,35 @@ def step_algorithmic_bytes(batch):
     sequence's KV read, the new rows' KV written, the draft probabilities the
     rule reads (q at each draft token, plus the full q row of each sequence's
     final position), the target logits of the final rows."""
+    return sum(b for _, b in phase_work(batch).values())
+
+
+def phase_work(batch):
+    """Algorithmic (flops, bytes) of each phase of one step on the 9B-class layer.
+
+    Flops count the contraction once (2 per multiply-add), whatever the
+    kernel's operand split; attention counts QK^T and PV over each row's
+    visible positions.  Bytes count what the phase must move at least once:
+    weights, KV read and written, activations in and out, draft
+    probabilities read by the rule.
+    """
     H, F, V, D, nq, nkv = 4096, 12288, 151936, 128, 32, 8
-    layer = ((nq + 2 * nkv) * D * H + H * nq * D + 2 * F * H + H * F) * 2
-    lm = V * H * 2
+    R, B, G = int(batch.R), int(batch.B), int(batch.G)
+    nqkv = (nq + 2 * nkv) * D
+    vis = sum(int(L) * (int(g) + 1) + (int(g) + 1) * (int(g) + 2) // 2
+              for L, g in zip(batch.seq_lens, batch.draft_lens))
     kv_read = int(sum(batch.seq_lens)) * nkv * 2 * D * 2
-    kv_write = batch.R * nkv * 2 * D * 2
-    q_bytes = batch.G * 4 + batch.B * V * 4
-    return layer + lm + kv_read + kv_write + q_bytes
+    kv_write = R * nkv * 2 * D * 2
+    return {
+        "prologue": (0, R * H * 2 + R * H * 4),
+        "qkv": (2 * R * nqkv * H, nqkv * H * 2 + kv_write + R * nq * D * 4),
+        "attention": (4 * vis * nq * D, kv_read + kv_write + 2 * R * nq * D * 4),
+        "o_proj": (2 * R * H * nq * D, H * nq * D * 2 + 2 * R * H * 4),
+        "ffn": (2 * R * 3 * F * H, 3 * F * H * 2 + 2 * R * H * 4),
+        "lm_head": (2 * R * V * H, V * H * 2 + R * H * 2 + ((V + 127) // 128) * R * 8),
+        "accept": (0, G * 4 + B * V * 4),
+        "realign": (0, 0),
+    }
 
 
 # DRAM traffic of one LM-head launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
@@ -363,6 +392,131 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# roofline crossover sweep (9B-class layer, ctx 2048, uniform gamma)
+# ---------------------------------------------------------------------------
+
+SWEEP_B = (1, 4, 16, 32, 64, 128)
+SWEEP_GAMMA = (0, 1, 2, 3, 4, 7, 8)
+
+
+def run_sweep(args):
+    import torch
+    import workloads as wl
+    from workloads import device as wd
+    from speculative_decoding_verify_ragged_gb300 import PHASES, VerifyEngine
+
+    torch.cuda.set_device(0)
+    if args.sweep_points:
+        points = [tuple(int(v) for v in pt.split(":")) for pt in args.sweep_points.split(",")]
+    else:
+        points = [(B, g) for B in SWEEP_B for g in SWEEP_GAMMA]
+    max_rows = max(B * (g + 1) for B, g in points)
+    max_slots = max(B for B, _ in points)
+    W = wl.make_weights(wl.NINE_B, 4)
+    Wd = wd.weights_to_device(W)
+    del W
+    eng = VerifyEngine(wd.config(wl.NINE_B, 8), Wd, max_rows=max_rows, max_slots=max_slots)
+    eng.set_gemm_path(args.gemm_path)
+    hbm, tflops, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream()
+    results = []
+    for B, g in points:
+        batch = wl.workload4(B, g, kv_fill="lazy", extra_pages=4 * B + 8)
+        bd = wd.batch_to_device(batch)
+        # the KV pool: bf16 N(0,1) drawn on the device (seeded), the same recipe as the host fill
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(4_000_000 + 1000 * B + g)
+        bd["kv_pool"].normal_(generator=gen)
+        # q rebuilt around the target's p for per-draft acceptance 0.8
+        if batch.G > 0:
+            res = wd.alloc_result(B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1],
+                                  probs=True)
+            eng.verify_step(bd, res)
+            assert eng.read_status(res["status"]) == 0
+            wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), 4)
+            del res
+            bd["draft_probs"] = torch.from_numpy(batch.draft_probs.reshape(batch.G, -1)).cuda()
+            # the prepass realigned the page tables: put the step's inputs back
+            bd["page_table"].copy_(torch.from_numpy(batch.page_table))
+            bd["num_pages"].copy_(torch.from_numpy(batch.num_pages))
+            bd["free_pages"].copy_(torch.from_numpy(batch.free_pages))
+            bd["num_free_in"].fill_(batch.num_free)
+        nsteps = args.warmup + args.steps
+        gu = wl.rng(4, wl.S_U, 1000 + B * 16 + g)
+        U = torch.from_numpy(np.stack([wl.uniform24(gu, batch.R) for _ in range(nsteps)])).cuda()
+        res = wd.alloc_result(B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1])
+        EO = torch.zeros((nsteps, B + 1), dtype=torch.int32, device="cuda")
+
+        def step(i):
+            bd["uniforms"] = U[i]
+            res["emitted_offsets"] = EO[i]
+            eng.verify_step(bd, res, stream)
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.warmup, nsteps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        assert eng.read_status(res["status"]) == 0
+        ms = t0.elapsed_time(t1) / args.steps
+        tokens = int(EO[args.warmup:, B].sum().item())
+        # phases, every boundary recorded (serialised), outside the timed loop
+        nph = min(10, args.steps)
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
+        for j in range(nph):
+            eng.set_phase_events(evsets[j])
+            step(args.warmup + j)
+        torch.cuda.synchronize()
+        eng.set_phase_events(None)
+        ph_us = {p: statistics.mean(es[k].elapsed_time(es[k + 1]) for es in evsets) * 1e3
+                 for k, p in enumerate(PHASES)}
+        work = phase_work(batch)
+        flops = sum(f for f, _ in work.values())
+        nbytes = sum(b for _, b in work.values())
+        t_hbm = nbytes / (hbm * 1e9) * 1e6
+        t_tc = flops / (tflops * 1e12) * 1e6
+        phases = {}
+        for p in PHASES:
+            f, b = work[p]
+            t = ph_us[p] * 1e-6
+            phases[p] = {"us": ph_us[p], "hbm_frac": b / t / 1e9 / hbm if t > 0 else None,
+                         "tensor_frac": f / t / 1e12 / tflops if t > 0 else None}
+        gemm = ("qkv", "o_proj", "ffn", "lm_head")
+        g_t = sum(ph_us[p] for p in gemm) * 1e-6
+        g_f = sum(work[p][0] for p in gemm)
+        g_b = sum(work[p][1] for p in gemm)
+        pt = {"sweep": "crossover", "B": B, "gamma": g, "rows": batch.R, "ms_per_step": ms,
+              "tokens_per_s": tokens / (ms * args.steps / 1e3), "rows_per_s": batch.R / (ms / 1e3),
+              "step_bound": "tensor" if t_tc > t_hbm else "hbm",
+              "step_roofline_us": max(t_hbm, t_tc), "step_frac": max(t_hbm, t_tc) / (ms * 1e3),
+              "t_hbm_us": t_hbm, "t_tensor_us": t_tc,
+              "gemm_hbm_frac": g_b / g_t / 1e9 / hbm, "gemm_tensor_frac": g_f / g_t / 1e12 / tflops,
+              "phases": phases, "gemm_path": args.gemm_path}
+        results.append(pt)
+        print(json.dumps(pt), flush=True)
+        del bd, res, U, EO
+        torch.cuda.empty_cache()
+    # crossover: the first row count whose GEMMs run closer to the tensor peak than to the HBM peak
+    cross = None
+    for pt in sorted(results, key=lambda x: x["rows"]):
+        if pt["gemm_tensor_frac"] >= pt["gemm_hbm_frac"]:
+            cross = pt["rows"]
+            break
+    # the weights' bytes against the flops per row they carry (2 per weight)
+    w_bytes = 2 * (48 * 128 * 4096 + 4096 * 4096 + 3 * 12288 * 4096 + 151936 * 4096)
+    model = (w_bytes / (hbm * 1e9)) / (w_bytes / (tflops * 1e12))
+    print(json.dumps({"sweep": "crossover-summary", "points": len(results), "measured_crossover_rows": cross,
+                      "model_crossover_rows": model, "peaks": {"hbm_GBps": hbm, "bf16_TFLOPs": tflops,
+                                                               "kind": peak_kind},
+                      "gemm_path": args.gemm_path}), flush=True)
+
+
 def run_e2e(eng, batch, bd, U, args, stream, tokens):
     """The same step through the public API with host inputs: every step copies
     its inputs from pinned host memory and reads its results back."""
@@ -480,6 +634,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -165,6 +165,32 @@ static bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte matrix [rows, cols] (int4 codes, two per byte), box = (128 bytes, 64 rows), 128-byte swizzle.
+static bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, 64};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D fp16 matrix [rows, cols] (int4 group scales), box = (8 cols, 64 rows), no swizzle.
+static bool encode_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {8, 64};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D fp32 matrix [rows, cols], box = (32 cols, box_rows), 128-byte swizzle.
 static bool encode_f32_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -213,7 +239,10 @@ struct sdv_ctx {
   int max_rows, max_slots, sms;
   uint8_t* ws;
   Layout L;
+  // layer weights: bf16 maps, or for int4 the code maps (tm_*) and the scale maps (ts_*)
   CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
+  CUtensorMap ts_qkv, ts_o, ts_gate, ts_up, ts_down;
+  bool int4;
   CUtensorMap tm_h[6], tm_attn[6], tm_act[6], tm_h3[6];  // activation tiles of 8..256 rows
   int gemm_path;
   cudaEvent_t phase_ev[SDV_PHASES + 1];
@@ -240,12 +269,13 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   *out = nullptr;
   if (!cfg) return SDV_ERR_INVALID_ARG;
   if (cfg->head_dim != 64 && cfg->head_dim != 128) return SDV_ERR_UNSUPPORTED;
-  if (cfg->weight_format == SDV_WEIGHTS_INT4_G32) return SDV_ERR_UNSUPPORTED;
   if (!config_ok(cfg) || max_rows <= 0 || max_slots <= 0 || max_slots > 1024) return SDV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return SDV_ERR_INVALID_ARG;
   if (!w->emb || !w->w_qkv || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->w_lm || !w->g_attn ||
       !w->g_ffn || !w->g_final)
     return SDV_ERR_INVALID_ARG;
+  const bool int4 = cfg->weight_format == SDV_WEIGHTS_INT4_G32;
+  if (int4 && (!w->s_qkv || !w->s_o || !w->s_gate || !w->s_up || !w->s_down)) return SDV_ERR_INVALID_ARG;
   const int sms = num_sms_current();
   if (sms <= 0) return SDV_ERR_CUDA;
   Layout L = make_layout(*cfg, max_rows, max_slots, sms);
@@ -264,9 +294,19 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
                  V = cfg->vocab;
   const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
-  bool ok = encode_bf16_2d(&c->tm_qkv, w->w_qkv, NQKV, H, 64) && encode_bf16_2d(&c->tm_o, w->w_o, H, QD, 64) &&
-            encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
-            encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64) && encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
+  c->int4 = int4;
+  bool ok = encode_bf16_2d(&c->tm_lm, w->w_lm, V, H, 64);
+  if (int4) {
+    ok = ok && encode_u8_2d(&c->tm_qkv, w->w_qkv, NQKV, H / 2) && encode_f16_2d(&c->ts_qkv, w->s_qkv, NQKV, H / 32) &&
+         encode_u8_2d(&c->tm_o, w->w_o, H, QD / 2) && encode_f16_2d(&c->ts_o, w->s_o, H, QD / 32) &&
+         encode_u8_2d(&c->tm_gate, w->w_gate, F, H / 2) && encode_f16_2d(&c->ts_gate, w->s_gate, F, H / 32) &&
+         encode_u8_2d(&c->tm_up, w->w_up, F, H / 2) && encode_f16_2d(&c->ts_up, w->s_up, F, H / 32) &&
+         encode_u8_2d(&c->tm_down, w->w_down, H, F / 2) && encode_f16_2d(&c->ts_down, w->s_down, H, F / 32);
+  } else {
+    ok = ok && encode_bf16_2d(&c->tm_qkv, w->w_qkv, NQKV, H, 64) && encode_bf16_2d(&c->tm_o, w->w_o, H, QD, 64) &&
+         encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
+         encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64);
+  }
   const int nts[6] = {8, 16, 32, 64, 128, 256};
   for (int i = 0; i < 6 && ok; ++i) {
     ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, 2ull * max_rows, H, nts[i]) &&
@@ -391,14 +431,28 @@ static GemmParams gemm_params(sdv_ctx* c, int N, int K, int R, int m_tiles, int*
   return g;
 }
 
+// The scale map of an int4 projection, or null for bf16 weights.
+static const CUtensorMap* q4(const sdv_ctx* c, const CUtensorMap& scales) { return c->int4 ? &scales : nullptr; }
+
 // Rows at and above which the tcgen05 kernel takes the context's GEMMs in
 // SDV_GEMM_AUTO mode (below it the mma.sync kernel's 8-row tiles waste less).
 constexpr int kTcRows = 17;
 
 // Run one GEMM: pick the kernel and the activation tile height, then launch
-// over min(SMs, units) CTAs.  xmaps: the activation map for each tile height.
+// over min(SMs, units) CTAs.  xmaps: the activation map for each tile height;
+// s0, s1: the scale maps of int4 weights (a0, a1 are then code maps).
 static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
-                            const CUtensorMap* xmaps, GemmParams g, cudaStream_t s) {
+                            const CUtensorMap* xmaps, GemmParams g, cudaStream_t s,
+                            const CUtensorMap* s0 = nullptr, const CUtensorMap* s1 = nullptr) {
+  if (s0) {
+    const int nt = gemm_q4_tile_rows(g.R);
+    g.kb = g.K / 256;
+    g.int4 = 1;
+    g.n_tiles = (g.R + nt - 1) / nt;
+    const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
+    const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
+    return launch_gemm_q4(epi, nt, xp, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
+  }
   const bool tc = c->gemm_path == SDV_GEMM_TCGEN05 || (c->gemm_path == SDV_GEMM_AUTO && g.R >= kTcRows);
   const int nt = tc ? gemm_tc_tile_rows(g.R) : gemm_tile_rows(g.R);
   g.n_tiles = (g.R + nt - 1) / nt;
@@ -519,7 +573,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.head_dim = D;
     g.epi.page = cf.page_size;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(run_gemm(c, EPI_QKV, 2, &c->tm_qkv, &c->tm_qkv, c->tm_h, g, s));
+    SDV_CUDA(run_gemm(c, EPI_QKV, 2, &c->tm_qkv, &c->tm_qkv, c->tm_h, g, s, q4(c, c->ts_qkv), q4(c, c->ts_qkv)));
   }
   SDV_CUDA(mark(SDV_PHASE_ATTN));
   {
@@ -534,7 +588,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.resid_f32 = f32(c->L.x0);
     g.epi.ld_f32 = H;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_o, &c->tm_o, c->tm_attn, g, s));
+    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_o, &c->tm_o, c->tm_attn, g, s, q4(c, c->ts_o), q4(c, c->ts_o)));
   }
   SDV_CUDA(mark(SDV_PHASE_FFN));
   SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn),
@@ -546,7 +600,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.out_lo_off = (long long)c->max_rows * F;
     g.epi.ld_bf16 = F;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(run_gemm(c, EPI_SWIGLU, 2, &c->tm_gate, &c->tm_up, c->tm_h, g, s));
+    SDV_CUDA(run_gemm(c, EPI_SWIGLU, 2, &c->tm_gate, &c->tm_up, c->tm_h, g, s, q4(c, c->ts_gate), q4(c, c->ts_up)));
   }
   {  // down projection + residual
     GemmParams g = gemm_params(c, H, F, R, (H + 127) / 128, status);
@@ -554,7 +608,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.resid_f32 = f32(c->L.x1);
     g.epi.ld_f32 = H;
     g.x_lo_row = c->max_rows;
-    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_down, &c->tm_down, c->tm_act, g, s));
+    SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_down, &c->tm_down, c->tm_act, g, s, q4(c, c->ts_down), q4(c, c->ts_down)));
   }
   SDV_CUDA(launch_rmsnorm(f32(c->L.x2), static_cast<const __nv_bfloat16*>(c->w.g_final),
                           ws_ptr<__nv_bfloat16>(c, c->L.h3), 0, R, H, cf.rms_eps, status, s));
@@ -646,14 +700,14 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
   const sdv_config& cf = c->cfg;
   const int H = cf.hidden, QD = cf.n_q * cf.head_dim, F = cf.ffn;
   const int NQKV = (cf.n_q + 2 * cf.n_kv) * cf.head_dim;
-  const CUtensorMap* wm = nullptr;
+  const CUtensorMap *wm = nullptr, *sm = nullptr;
   int N = 0, K = 0;
   switch (which) {
-    case 0: wm = &c->tm_qkv; N = NQKV; K = H; break;
-    case 1: wm = &c->tm_o; N = H; K = QD; break;
-    case 2: wm = &c->tm_gate; N = F; K = H; break;
-    case 3: wm = &c->tm_up; N = F; K = H; break;
-    case 4: wm = &c->tm_down; N = H; K = F; break;
+    case 0: wm = &c->tm_qkv; sm = q4(c, c->ts_qkv); N = NQKV; K = H; break;
+    case 1: wm = &c->tm_o; sm = q4(c, c->ts_o); N = H; K = QD; break;
+    case 2: wm = &c->tm_gate; sm = q4(c, c->ts_gate); N = F; K = H; break;
+    case 3: wm = &c->tm_up; sm = q4(c, c->ts_up); N = F; K = H; break;
+    case 4: wm = &c->tm_down; sm = q4(c, c->ts_down); N = H; K = F; break;
     default: wm = &c->tm_lm; N = cf.vocab; K = H; break;
   }
   const bool xf32 = x_format == 1;
@@ -675,7 +729,7 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
     if (!encode_bf16_2d(&xm[i], xsrc, (xf32 ? 2ull : 1ull) * rows, K, nts[i])) return SDV_ERR_CUDA;
   g.epi.out_f32 = y;
   g.epi.ld_f32 = N;
-  SDV_CUDA(run_gemm(c, EPI_F32, xf32 ? 2 : 1, wm, wm, xm, g, s));
+  SDV_CUDA(run_gemm(c, EPI_F32, xf32 ? 2 : 1, wm, wm, xm, g, s, sm, sm));
   return SDV_OK;
 }
 

@@ -182,7 +182,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   // other consumer warps still meet at the named barriers); outputs are then
   // garbage but every access stays in bounds and the status word says why.
   bool dead = false;
-  const int g = lane >> 2, t = lane & 3;
   const int mat = lane >> 3, rr = lane & 7;
   float acc[2][NF][4];
   int stage = 0;
@@ -192,8 +191,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tile = static_cast<int>(u / p.kb);
     const int k0 = static_cast<int>(u - (long long)tile * p.kb);
     const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
-    const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
-
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
@@ -250,89 +247,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
 
-    // ---------------- stream-K: tiles cut between CTAs ----------------
-    if (!(k0 == 0 && k1 == p.kb)) {
-      const long long tu = (long long)tile * p.kb;
-      const int c_first = cta_of_unit(tu, total, P);
-      const int c_last = cta_of_unit(tu + p.kb - 1, total, P);
-      const int my_slot = 2 * c + (tile == static_cast<int>(u_begin / p.kb) ? 0 : 1);
-      float4* dst = reinterpret_cast<float4*>(p.partials + (size_t)my_slot * BM * NT);
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int nj = 0; nj < NF; ++nj)
-          __stcg(&dst[((warp * 2 + mi) * NF + nj) * 32 + lane],
-                 make_float4(acc[mi][nj][0], acc[mi][nj][1], acc[mi][nj][2], acc[mi][nj][3]));
-      __threadfence();
-      named_sync(1, CONSUMERS * kWarp);
-      if (threadIdx.x == 0) {
-        const int old = atomicAdd(&p.counters[tile], 1);
-        *flag = (old == c_last - c_first) ? 1 : 0;
-      }
-      named_sync(1, CONSUMERS * kWarp);
-      const bool last = *flag != 0;
-      if (!last) {
-        u += k1 - k0;
-        continue;
-      }
-      __threadfence();
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int nj = 0; nj < NF; ++nj)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[mi][nj][q] = 0.f;
-      // pieces are summed in CTA order; the loads of up to four pieces are
-      // issued together
-      for (int c0 = c_first; c0 <= c_last; c0 += 4) {
-        float4 v[4][2][NF];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cc = c0 + q;
-          if (cc <= c_last) {
-            const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
-            const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
-            const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)slot * BM * NT);
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-              for (int nj = 0; nj < NF; ++nj) v[q][mi][nj] = __ldcg(&src[((warp * 2 + mi) * NF + nj) * 32 + lane]);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (c0 + q <= c_last) {
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-              for (int nj = 0; nj < NF; ++nj) {
-                acc[mi][nj][0] += v[q][mi][nj].x;
-                acc[mi][nj][1] += v[q][mi][nj].y;
-                acc[mi][nj][2] += v[q][mi][nj].z;
-                acc[mi][nj][3] += v[q][mi][nj].w;
-              }
-          }
-        }
-      }
-      if (threadIdx.x == 0) p.counters[tile] = 0;  // ready for the next launch
-    }
-
-    // ---------------- fused epilogue ----------------
-    constexpr int LD = C::EPI_LD;
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-      for (int nj = 0; nj < NF; ++nj) {
-        const int m = warp * 32 + mi * 16 + g;
-        const int n = nj * 8 + 2 * t;
-        epi[n * LD + m] = acc[mi][nj][0];
-        epi[(n + 1) * LD + m] = acc[mi][nj][1];
-        epi[n * LD + m + 8] = acc[mi][nj][2];
-        epi[(n + 1) * LD + m + 8] = acc[mi][nj][3];
-      }
-    named_sync(1, CONSUMERS * kWarp);
-    epilogue_rows<EPI, LD>(p, epi, tm, tn * NT, min(NT, p.R - tn * NT), threadIdx.x);
-    named_sync(1, CONSUMERS * kWarp);
+    // stream-K fixup of tiles cut between CTAs, then the fused epilogue
+    finish_tile_mma<EPI, NT, C::EPI_LD>(p, acc, tile, k0, k1, total, u_begin, epi, flag);
     u += k1 - k0;
   }
 }

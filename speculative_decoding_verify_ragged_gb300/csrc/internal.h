@@ -68,6 +68,12 @@ cudaError_t launch_gemm(int epi, int nt, int xp, const CUtensorMap* a0, const CU
 // out[i] = hi[i] + hi[i + lo_off] for i < n (fp32 view of a two-plane activation).
 cudaError_t launch_join_planes(const __nv_bfloat16* hi, long long lo_off, float* out, long long n,
                                cudaStream_t stream);
+// The same GEMM over int4 group-32 weights (code maps q0, q1; scale maps s0,
+// s1; kb counts 256-k blocks; nt in {8, 16, 32}).
+int gemm_q4_tile_rows(int R);
+cudaError_t launch_gemm_q4(int epi, int nt, int xp, const CUtensorMap* q0, const CUtensorMap* q1,
+                           const CUtensorMap* s0, const CUtensorMap* s1, const CUtensorMap* x, const GemmParams& p,
+                           int grid, cudaStream_t stream);
 // The same GEMM on tcgen05 / TMEM (nt in {16, 32, 64, 128, 256}).
 int gemm_tc_tile_rows(int R);
 cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
