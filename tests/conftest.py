@@ -37,3 +37,14 @@ def nine_b_weights():
     from workloads import device as wd
     W = wl.make_weights(wl.NINE_B, 2)
     return W, wd.weights_to_device(W)
+
+
+@pytest.fixture(scope="session")
+def nine_b_int4():
+    """The 9B-class layer with int4 group-32 projections (seed 5), bf16 LM head, host and cuda:0."""
+    import torch
+    assert torch.cuda.is_available()
+    import workloads as wl
+    from workloads import device as wd
+    W = wl.make_weights(wl.NINE_B, 5, fmt="int4")
+    return W, wd.weights_to_device(W)

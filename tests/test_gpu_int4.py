@@ -96,15 +96,6 @@ def test_step_tiny_int4(tiny_int4):
     _full_step_check(eng, W, b3, "tiny-int4-wide")
 
 
-@pytest.fixture(scope="module")
-def nine_b_int4():
-    import torch
-    assert torch.cuda.is_available()
-    from workloads import device as wd
-    W = wl.make_weights(wl.NINE_B, 5, fmt="int4")
-    return W, wd.weights_to_device(W)
-
-
 def test_step_nine_b_int4(nine_b_int4):
     """9B-class int4 layer: a swarm-like ragged batch (contexts 1k..16k, gamma 0..3)."""
     from tests.test_gpu_parity import _retargeted

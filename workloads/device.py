@@ -74,3 +74,27 @@ def alloc_result(B: int, R: int, V: int, gamma_max: int, max_pages: int, dev="cu
     if probs:
         r["probs"] = torch.zeros((R, V), dtype=torch.float32, device=dev)
     return r
+
+
+# ---------------------------------------------------------------------------
+# inputs drawn on the device (full-size runs whose KV pool and draft
+# distributions are too large to draw on the host every step)
+# ---------------------------------------------------------------------------
+
+def _generator(key: int):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(key & ((1 << 63) - 1))
+    return g
+
+
+def normal_bf16_device_(t: torch.Tensor, key: int) -> torch.Tensor:
+    """Fill a bf16 device tensor with N(0, 1) draws from a seeded device generator."""
+    return t.normal_(generator=_generator(key))
+
+
+def draft_probs_device(G: int, V: int, key: int, sigma: float = 2.0) -> torch.Tensor:
+    """q = softmax(N(0, sigma^2) logits) per draft row, fp32 [G, V], drawn on the device."""
+    if G == 0:
+        return torch.zeros((0, V), dtype=torch.float32, device="cuda")
+    z = torch.randn((G, V), generator=_generator(key), device="cuda", dtype=torch.float32)
+    return torch.softmax(z * sigma, dim=1)
