@@ -331,29 +331,16 @@ def run_ours(args):
     assert eng.read_status(res["status"]) == 0
     phase_ms = {p: [es[k].elapsed_time(es[k + 1]) for es in evsets] for k, p in enumerate(PHASES)}
 
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
     tokens_rank = int(EO[args.warmup:, batch.B].sum().item())
-    tokens = tokens_rank
-    if world > 1:
-        import torch.distributed as dist
-        tk = torch.tensor([tokens], dtype=torch.int64, device="cuda")
-        dist.all_reduce(tk)
-        tokens = int(tk.item())
-    value = tokens / (elapsed_ms / 1e3)
-    ms_per_step = elapsed_ms / args.steps
-
     # ---- end to end through the public API with host buffers ----
     e2e = run_e2e(eng, batch, bd, U, args, stream, tokens_rank) if not args.quick else None
-    if world > 1 and e2e is not None:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e["value"] = tokens / (float(tt.item()) * args.steps / 1e3)
+    elapsed_ms, tokens, e2e_ms = reduce_over_ranks(t0.elapsed_time(t1), tokens_rank,
+                                                   e2e["ms_per_step"] if e2e else None, "cuda")
+    value = tokens / (elapsed_ms / 1e3)
+    ms_per_step = elapsed_ms / args.steps
+    if e2e is not None:
+        e2e["ms_per_step"] = e2e_ms
+        e2e["value"] = tokens / (e2e_ms * args.steps / 1e3)
 
     copy_gbs = box_copy_gbps() if not args.quick else None
     hbm, tflops, peak_kind = measured_peaks()
@@ -515,6 +502,21 @@ def run_sweep(args):
                       "model_crossover_rows": model, "peaks": {"hbm_GBps": hbm, "bf16_TFLOPs": tflops,
                                                                "kind": peak_kind},
                       "gemm_path": args.gemm_path}), flush=True)
+
+
+def reduce_over_ranks(elapsed_ms: float, tokens: int, e2e_ms_per_step, device):
+    """Whole-job numbers over the replicas: the slowest rank's times and every
+    rank's emitted tokens.  One process: the inputs unchanged."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return elapsed_ms, tokens, e2e_ms_per_step
+    t = torch.tensor([elapsed_ms, -1.0 if e2e_ms_per_step is None else e2e_ms_per_step], dtype=torch.float64,
+                     device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    k = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(k)
+    return float(t[0].item()), int(k[0].item()), (None if e2e_ms_per_step is None else float(t[1].item()))
 
 
 def run_e2e(eng, batch, bd, U, args, stream, tokens):

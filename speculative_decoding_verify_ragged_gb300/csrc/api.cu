@@ -43,7 +43,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 // ---------------------------------------------------------------------------
 
 struct Layout {
-  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, rope, kv_row_off, inv_freq;
+  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, items, rope, kv_row_off, inv_freq;
   size_t x0, h, h3, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, p_draft, slot_count, chunk_count, chunk_sums, total;
   int chunk_ld;
@@ -104,6 +104,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.chunks = take(B * 4);
   L.item_off = take((B + 1) * 4);
   L.sched = take(64);
+  L.items = take(static_cast<size_t>(L.items_max) * 32);
   L.rope = take(R * (c.head_dim / 2) * 2 * 4);
   L.kv_row_off = take(R * 8);
   L.inv_freq = take(static_cast<size_t>(c.head_dim / 2) * 8);
@@ -188,19 +189,6 @@ static bool encode_f16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint6
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 2-D fp32 matrix [rows, cols], box = (32 cols, box_rows), 128-byte swizzle.
-static bool encode_f32_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 4};
-  cuuint32_t box[2] = {32, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -394,6 +382,7 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   p.t.chunks = ws_ptr<int>(c, c->L.chunks);
   p.t.item_off = ws_ptr<int>(c, c->L.item_off);
   p.t.sched = ws_ptr<int>(c, c->L.sched);
+  p.t.items = ws_ptr<int4>(c, c->L.items);
   p.t.rope_cs = ws_ptr<float>(c, c->L.rope);
   p.t.kv_row_off = ws_ptr<long long>(c, c->L.kv_row_off);
   p.seq_lens = b->seq_lens;
@@ -478,6 +467,7 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   a.item_off = ws_ptr<int>(c, c->L.item_off);
   a.chunks = ws_ptr<int>(c, c->L.chunks);
   a.sched = ws_ptr<int>(c, c->L.sched);
+  a.items = ws_ptr<int4>(c, c->L.items);
   a.part_o = ws_ptr<float>(c, c->L.part_o);
   a.part_ml = ws_ptr<float2>(c, c->L.part_ml);
   a.status = status;
@@ -485,7 +475,7 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   a.n_q = c->cfg.n_q;
   a.n_kv = c->cfg.n_kv;
   a.page = c->cfg.page_size;
-  const int grid = 2 * c->sms;
+  const int grid = c->sms;  // one CTA per SM (the ring and the combine buffer take most of shared memory)
   SDV_CUDA(launch_attention_impl(c->cfg.head_dim, &kv, a, grid, b->R, s, ws_ptr<int>(c, c->L.row_seq)));
   return SDV_OK;
 }

@@ -16,11 +16,16 @@
 //    context lengths (a batch of one long sequence and a swarm of 128 alike);
 //  * a producer warp streams each (page, KV head) block -- 16 keys and 16
 //    values of head_dim -- with 128-byte-swizzled TMA loads into an 8-stage
-//    ring; three consumer warps each own 16 query vectors (draft rows x query
-//    heads of the group) and run QK^T and PV on bf16 mma.sync with an online
-//    softmax in fp32.  q (fp32) and the softmax weights enter the MMAs as
-//    bf16 hi + lo pairs, so the output keeps ~17 significant bits against the
-//    bf16 cache;
+//    ring; seven consumer warps run QK^T and PV on bf16 mma.sync with an
+//    online softmax in fp32.  The item's query vectors (draft rows x query
+//    heads of the group, at most 48) form 1-3 tiles of 16; the warps split
+//    as (query tile) x (key phase), each key phase taking every KS-th page,
+//    so a 16-vector item still keeps seven warps busy, and the phases'
+//    (max, sum, output) states are combined in shared memory at the end of
+//    the item.  q (fp32) and the softmax weights enter the MMAs as bf16 hi +
+//    lo pairs, so the output keeps ~17 significant bits against the bf16
+//    cache; the hi and lo products and even and odd k steps accumulate
+//    separately, so no MMA waits on more than three others;
 //  * items that cover a whole sequence write the output directly (as bf16 hi +
 //    lo planes, the O projection's input); split sequences write (max, sum,
 //    unnormalised output) partials that a merge kernel combines (log-sum-exp
@@ -32,7 +37,7 @@ namespace sdv {
 
 namespace {
 
-constexpr int kConsumers = 3;  // x 16 query vectors = kAttnQMax
+constexpr int kConsumers = 7;  // + the producer: 256 threads, so up to 255 registers a thread
 constexpr int kThreads = (kConsumers + 1) * kWarp;
 
 template <int D>
@@ -43,7 +48,10 @@ struct ACfg {
   static constexpr int PAGE_BYTES = 2 * HALVES * BOX;  // K and V of one (page, kv head)
   static constexpr int QLD = D + 8;                   // padded Q row (bf16 elements)
   static constexpr int Q_BYTES = 2 * kAttnQMax * QLD * 2;  // hi and lo tiles
-  static constexpr int SMEM = 1024 + STAGES * PAGE_BYTES + Q_BYTES + 2 * STAGES * 8 + 64;
+  static constexpr int OREG = D / 2;                  // output accumulators per thread
+  // per-warp softmax states for the key-phase combine: [warp][register][lane]
+  static constexpr int COMB_BYTES = kConsumers * (OREG + 4) * kWarp * 4;
+  static constexpr int SMEM = 1024 + STAGES * PAGE_BYTES + Q_BYTES + COMB_BYTES + 2 * STAGES * 8 + 64;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -51,34 +59,26 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 struct Item {
-  int b, g, c, chunks, p0, p1, L, gamma, r0;
+  int b, g, p0, p1, L, gamma, r0, chunks;
 };
 
-__device__ __forceinline__ Item decode_item(const AttnParams& p, int item, int chunk_pages) {
-  // slot = last b with item_off[b] <= item
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (p.item_off[mid] <= item) lo = mid; else hi = mid - 1;
-  }
+// The prologue wrote one record per work item: no search, one round trip.
+__device__ __forceinline__ Item load_item(const AttnParams& p, int item) {
+  const int4 a = p.items[2 * item], c = p.items[2 * item + 1];
   Item it;
-  it.b = lo;
-  it.chunks = p.chunks[lo];
-  const int rem = item - p.item_off[lo];
-  it.g = rem / it.chunks;
-  it.c = rem - it.g * it.chunks;
-  it.L = p.seq_lens[lo];
-  it.gamma = p.draft_lens[lo];
-  it.r0 = p.row_off[lo];
-  const int len = it.L + it.gamma + 1;
-  const int pages = (len + p.page - 1) / p.page;
-  it.p0 = it.c * chunk_pages;
-  it.p1 = min(pages, it.p0 + chunk_pages);
+  it.b = a.x;
+  it.g = a.y;
+  it.p0 = a.z;
+  it.p1 = a.w;
+  it.L = c.x;
+  it.gamma = c.y;
+  it.r0 = c.z;
+  it.chunks = c.w;
   return it;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
   using C = ACfg<D>;
   constexpr int KK = D / 16;  // k16 steps over the head dimension
   constexpr int QT = kAttnQMax * ACfg<D>::QLD;  // elements of one Q tile
@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 
   uint8_t* smem = align1024(smem_raw);
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + C::STAGES * C::PAGE_BYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::PAGE_BYTES + C::Q_BYTES);
+  float* comb = reinterpret_cast<float*>(smem + C::STAGES * C::PAGE_BYTES + C::Q_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::PAGE_BYTES + C::Q_BYTES + C::COMB_BYTES);
   uint64_t* empty = full + C::STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,38 +104,50 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   }
   __syncthreads();
 
-  const int chunk_pages = p.sched[0];
   const int total_items = p.sched[1];
   const int group = p.n_q / p.n_kv;
 
   if (warp == kConsumers) {
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool dead = false;
-      for (int item = blockIdx.x; item < total_items && !dead; item += gridDim.x) {
-        const Item it = decode_item(p, item, chunk_pages);
-        for (int pi = it.p0; pi < it.p1; ++pi) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            set_status(p.status, SDV_ERR_TIMEOUT);
+    // producer warp: the lanes fetch up to 32 page indices of the item at once,
+    // lane 0 issues the TMA loads of those pages in order
+    int stage = 0;
+    uint32_t phase = 0;
+    bool dead = false;
+    for (int item = blockIdx.x; item < total_items && !dead; item += gridDim.x) {
+      const Item it = load_item(p, item);
+      for (int base = it.p0; base < it.p1 && !dead; base += kWarp) {
+        const int n = min(kWarp, it.p1 - base);
+        const int my_pg = lane < n ? p.page_table[(long long)it.b * p.max_pages + base + lane] : 0;
+        for (int j = 0; j < n; ++j) {
+          const int pg = __shfl_sync(0xffffffffu, my_pg, j);
+          int ok = 1;
+          if (lane == 0) {
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+              set_status(p.status, SDV_ERR_TIMEOUT);
+              ok = 0;
+            } else {
+              uint8_t* dst = smem + stage * C::PAGE_BYTES;
+              mbar_arrive_expect_tx(&full[stage], C::PAGE_BYTES);
+#pragma unroll
+              for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                for (int h = 0; h < C::HALVES; ++h)
+                  tma_load_5d(dst + (kv * C::HALVES + h) * C::BOX, &tmKV, &full[stage], h * 64, 0, kv, it.g, pg);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
             dead = true;
             break;
           }
-          const int pg = p.page_table[(long long)it.b * p.max_pages + pi];
-          uint8_t* dst = smem + stage * C::PAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::PAGE_BYTES);
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-            for (int h = 0; h < C::HALVES; ++h)
-              tma_load_5d(dst + (kv * C::HALVES + h) * C::BOX, &tmKV, &full[stage], h * 64, 0, kv, it.g, pg);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      // tail: wait until the consumers have released every stage
+    }
+    // tail: wait until the consumers have released every stage
+    if (lane == 0) {
       for (int i = 0; i < C::STAGES && !dead; ++i) {
         if (!mbar_wait(&empty[stage], phase ^ 1)) {
           set_status(p.status, SDV_ERR_TIMEOUT);
@@ -159,12 +172,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   uint32_t phase = 0;
 
   for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-    const Item it = decode_item(p, item, chunk_pages);
+    const Item it = load_item(p, item);
     const int nqv = (it.gamma + 1) * group;
+    const int qtiles = (nqv + 15) >> 4;
+    const int ks_n = kConsumers / qtiles;  // key phases
+    const int qt = warp % qtiles, ks = warp / qtiles;
+    const bool active = ks < ks_n;
 
     // Q tiles (hi, lo): query vector v = row i * group + head-in-group
     constexpr int CPR = D / 4;  // float4 per row
-    for (int idx = threadIdx.x; idx < kAttnQMax * CPR; idx += kConsumers * kWarp) {
+    for (int idx = threadIdx.x; idx < qtiles * 16 * CPR; idx += kConsumers * kWarp) {
       const int v = idx / CPR, ch = idx - v * CPR;
       float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
       if (v < nqv) {
@@ -179,19 +196,18 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     }
     named_sync(1, kConsumers * kWarp);
 
-    const bool active = warp * 16 < nqv;
     uint32_t qa[KK][4], ql[KK][4];
     if (active) {
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
-        const int row = warp * 16 + (mat & 1) * 8 + rr;
+        const int row = qt * 16 + (mat & 1) * 8 + rr;
         const int col = kk * 16 + (mat >> 1) * 8;
         ldsm_x4(smem_u32(qs + row * C::QLD + col), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
         ldsm_x4(smem_u32(qs + QT + row * C::QLD + col), ql[kk][0], ql[kk][1], ql[kk][2], ql[kk][3]);
       }
     }
     // query positions of this thread's two rows
-    const int v0 = warp * 16 + g8, v1 = v0 + 8;
+    const int v0 = qt * 16 + g8, v1 = v0 + 8;
     const int qpos0 = it.L + v0 / group, qpos1 = it.L + v1 / group;
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -204,12 +220,15 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         set_status(p.status, SDV_ERR_TIMEOUT);
         dead = true;
       }
-      if (active) {
+      if (active && (pi - it.p0) % ks_n == ks) {
         const uint32_t kbase = smem_u32(smem + stage * C::PAGE_BYTES);
         const uint32_t vbase = kbase + C::HALVES * C::BOX;
-        float s[2][4];
+        // four independent accumulator sets: (hi, lo) x (even, odd k step)
+        float sa[4][2][4];
 #pragma unroll
-        for (int nf = 0; nf < 2; ++nf) s[nf][0] = s[nf][1] = s[nf][2] = s[nf][3] = 0.f;
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int nf = 0; nf < 2; ++nf) sa[a][nf][0] = sa[a][nf][1] = sa[a][nf][2] = sa[a][nf][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KK; ++kk) {
           const int key = (mat >> 1) * 8 + rr;
@@ -217,11 +236,17 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
           const uint32_t addr = kbase + (chunk >> 3) * C::BOX + key * 128 + (((chunk & 7) ^ rr) << 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4(addr, b0, b1, b2, b3);
-          mma_bf16(s[0], qa[kk], b0, b1);
-          mma_bf16(s[1], qa[kk], b2, b3);
-          mma_bf16(s[0], ql[kk], b0, b1);
-          mma_bf16(s[1], ql[kk], b2, b3);
+          const int par = kk & 1;
+          mma_bf16(sa[par][0], qa[kk], b0, b1);
+          mma_bf16(sa[par][1], qa[kk], b2, b3);
+          mma_bf16(sa[2 + par][0], ql[kk], b0, b1);
+          mma_bf16(sa[2 + par][1], ql[kk], b2, b3);
         }
+        float s[2][4];
+#pragma unroll
+        for (int nf = 0; nf < 2; ++nf)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[nf][e] = (sa[0][nf][e] + sa[1][nf][e]) + (sa[2][nf][e] + sa[3][nf][e]);
         // scale to base-2 logits and apply the block-causal mask
         const int kp0 = pi * p.page;
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -297,6 +322,59 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    }
+    // combine the key phases of each query tile: phase 0's warp sums the others'
+    // states (in phase order) scaled to the common maximum
+    if (ks_n > 1) {
+      if (active && ks > 0) {
+        float* dst = comb + (size_t)warp * (C::OREG + 4) * kWarp;
+        dst[0 * kWarp + lane] = m0;
+        dst[1 * kWarp + lane] = m1;
+        dst[2 * kWarp + lane] = l0;
+        dst[3 * kWarp + lane] = l1;
+#pragma unroll
+        for (int nf = 0; nf < NF; ++nf)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[(4 + nf * 4 + e) * kWarp + lane] = o[nf][e];
+      }
+      named_sync(1, kConsumers * kWarp);
+      if (active && ks == 0) {
+        float M0 = m0, M1 = m1;
+        for (int k = 1; k < ks_n; ++k) {
+          const float* src = comb + (size_t)(k * qtiles + qt) * (C::OREG + 4) * kWarp;
+          M0 = fmaxf(M0, src[0 * kWarp + lane]);
+          M1 = fmaxf(M1, src[1 * kWarp + lane]);
+        }
+        const float B0 = M0 == -INFINITY ? 0.f : M0, B1 = M1 == -INFINITY ? 0.f : M1;
+        const float w0 = exp2f(m0 - B0), w1 = exp2f(m1 - B1);
+        l0 *= w0;
+        l1 *= w1;
+#pragma unroll
+        for (int nf = 0; nf < NF; ++nf) {
+          o[nf][0] *= w0;
+          o[nf][1] *= w0;
+          o[nf][2] *= w1;
+          o[nf][3] *= w1;
+        }
+        for (int k = 1; k < ks_n; ++k) {
+          const float* src = comb + (size_t)(k * qtiles + qt) * (C::OREG + 4) * kWarp;
+          const float u0 = exp2f(src[0 * kWarp + lane] - B0), u1 = exp2f(src[1 * kWarp + lane] - B1);
+          l0 += u0 * src[2 * kWarp + lane];
+          l1 += u1 * src[3 * kWarp + lane];
+#pragma unroll
+          for (int nf = 0; nf < NF; ++nf) {
+            o[nf][0] += u0 * src[(4 + nf * 4 + 0) * kWarp + lane];
+            o[nf][1] += u0 * src[(4 + nf * 4 + 1) * kWarp + lane];
+            o[nf][2] += u1 * src[(4 + nf * 4 + 2) * kWarp + lane];
+            o[nf][3] += u1 * src[(4 + nf * 4 + 3) * kWarp + lane];
+          }
+        }
+        m0 = M0;
+        m1 = M1;
+      }
+    }
+
+    if (active && ks == 0) {
       if (it.chunks == 1) {
         const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
@@ -333,7 +411,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         }
       }
     }
-    named_sync(1, kConsumers * kWarp);  // Q tile is rewritten by the next item
+    named_sync(1, kConsumers * kWarp);  // Q tile and combine buffer are rewritten by the next item
   }
 }
 

@@ -98,6 +98,7 @@ struct AttnParams {
   const int* item_off = nullptr;  // [B+1] first work item of each slot
   const int* chunks = nullptr;    // [B] key chunks per (slot, kv head)
   const int* sched = nullptr;     // [0] chunk pages, [1] total items
+  const int4* items = nullptr;    // [items, 2]: (slot, kv head, first page, end page), (L, gamma, row 0, chunks)
   float* part_o = nullptr;        // [items, QMAX, D]
   float2* part_ml = nullptr;      // [items, QMAX]
   int* status = nullptr;
@@ -122,6 +123,7 @@ struct StepTables {
   int* chunks = nullptr;     // [B]
   int* item_off = nullptr;   // [B+1]
   int* sched = nullptr;      // [4]
+  int4* items = nullptr;     // [items, 2] attention work items (null: not built)
   float* rope_cs = nullptr;  // [R, D/2, 2]
   long long* kv_row_off = nullptr;  // [R]
 };

@@ -136,6 +136,16 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   if (slot) {
     p.t.chunks[b] = chunks_b;
     p.t.item_off[b] = ioff;
+    if (p.t.items) {
+      // one record per (kv head, chunk) of this slot, in item order
+      for (int g = 0; g < p.n_kv; ++g)
+        for (int c = 0; c < chunks_b; ++c) {
+          const int item = ioff + g * chunks_b + c;
+          const int p0 = c * chunk;
+          p.t.items[2 * item] = make_int4(b, g, p0, min(used, p0 + chunk));
+          p.t.items[2 * item + 1] = make_int4(L, gam, roff, chunks_b);
+        }
+    }
   }
   if (b == 0) {
     p.t.item_off[p.B] = tot_items;
