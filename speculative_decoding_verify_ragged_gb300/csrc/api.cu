@@ -44,8 +44,8 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, items, rope, kv_row_off, inv_freq;
-  size_t x0, h, h3, q, attn, x1, act, x2, z, lmstats, rowstats, partials, counters;
-  size_t part_o, part_ml, accepted, final_tokens, p_draft, slot_count, chunk_count, chunk_sums, total;
+  size_t x0, h, h3, q, attn, x1, x1sq, act, x2, z, lmstats, rowstats, partials, counters;
+  size_t part_o, part_ml, accepted, final_tokens, chunk_count, chunk_sums, total;
   int chunk_ld;
   int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
 };
@@ -116,6 +116,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.q = take(R * QD * 4);
   L.attn = take(2 * R * QD * 2);
   L.x1 = take(R * H * 4);
+  L.x1sq = take(static_cast<size_t>(H / 32) * R * 4);  // per-32-column partial sums of x1^2
   L.act = take(2 * R * (F > QD ? (F > H ? F : H) : (QD > H ? QD : H)) * 2);
   L.x2 = take(R * H * 4);
   L.z = take(R * V * 4);
@@ -127,9 +128,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.part_ml = take(static_cast<size_t>(L.items_max) * kAttnQMax * 8);
   L.accepted = take(B * 4);
   L.final_tokens = take(B * 4);
-  L.p_draft = take(R * 4);
   L.chunk_ld = accept_chunks(c.vocab);
-  L.slot_count = take(B * 4);
   L.chunk_count = take(B * 4);
   L.chunk_sums = take(B * 2 * static_cast<size_t>(L.chunk_ld) * 8);
   L.total = o;
@@ -308,7 +307,6 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   }
   // arrival counters start at zero; every kernel that uses one resets it
   cudaError_t e = cudaMemset(c->ws + L.counters, 0, static_cast<size_t>(L.max_tiles) * 4);
-  if (e == cudaSuccess) e = cudaMemset(c->ws + L.slot_count, 0, static_cast<size_t>(max_slots) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->ws + L.chunk_count, 0, static_cast<size_t>(max_slots) * 4);
   if (e == cudaSuccess) {
     // rotary inverse frequencies theta^(-2j/d), in double, computed once
@@ -427,6 +425,10 @@ static const CUtensorMap* q4(const sdv_ctx* c, const CUtensorMap& scales) { retu
 // SDV_GEMM_AUTO mode (below it the mma.sync kernel's 8-row tiles waste less).
 constexpr int kTcRows = 17;
 
+static bool use_tc(const sdv_ctx* c, int R) {
+  return c->gemm_path == SDV_GEMM_TCGEN05 || (c->gemm_path == SDV_GEMM_AUTO && R >= kTcRows);
+}
+
 // Run one GEMM: pick the kernel and the activation tile height, then launch
 // over min(SMs, units) CTAs.  xmaps: the activation map for each tile height;
 // s0, s1: the scale maps of int4 weights (a0, a1 are then code maps).
@@ -442,7 +444,7 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
     const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
     return launch_gemm_q4(epi, nt, xp, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
   }
-  const bool tc = c->gemm_path == SDV_GEMM_TCGEN05 || (c->gemm_path == SDV_GEMM_AUTO && g.R >= kTcRows);
+  const bool tc = use_tc(c, g.R);
   const int nt = tc ? gemm_tc_tile_rows(g.R) : gemm_tile_rows(g.R);
   g.n_tiles = (g.R + nt - 1) / nt;
   const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
@@ -480,10 +482,7 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   return SDV_OK;
 }
 
-static void fill_accept_scratch(sdv_ctx* c, AcceptParams& a, const PrologueParams& pp) {
-  a.row_seq = pp.t.row_seq;
-  a.p_draft = ws_ptr<float>(c, c->L.p_draft);
-  a.slot_count = ws_ptr<int>(c, c->L.slot_count);
+static void fill_accept_scratch(sdv_ctx* c, AcceptParams& a) {
   a.chunk_count = ws_ptr<int>(c, c->L.chunk_count);
   a.chunk_sums = ws_ptr<unsigned long long>(c, c->L.chunk_sums);
   a.chunk_ld = c->L.chunk_ld;
@@ -577,15 +576,23 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.out_f32 = f32(c->L.x1);
     g.epi.resid_f32 = f32(c->L.x0);
     g.epi.ld_f32 = H;
+    // the FFN pre-norm: x1 * g_ffn as the gate/up input, sums of x1^2 for the row scale
+    g.epi.norm_gain = static_cast<const __nv_bfloat16*>(c->w.g_ffn);
+    g.epi.norm_out = ws_ptr<__nv_bfloat16>(c, c->L.h);
+    g.epi.norm_lo_off = (long long)c->max_rows * H;
+    g.epi.sq_out = f32(c->L.x1sq);
+    g.epi.sq_ld = c->max_rows;
     g.x_lo_row = c->max_rows;
     SDV_CUDA(run_gemm(c, EPI_RESID, 2, &c->tm_o, &c->tm_o, c->tm_attn, g, s, q4(c, c->ts_o), q4(c, c->ts_o)));
   }
   SDV_CUDA(mark(SDV_PHASE_FFN));
-  SDV_CUDA(launch_rmsnorm(f32(c->L.x1), static_cast<const __nv_bfloat16*>(c->w.g_ffn),
-                          ws_ptr<__nv_bfloat16>(c, c->L.h), (long long)c->max_rows * H, R, H, cf.rms_eps, status,
-                          s));
-  {  // gate/up + SwiGLU
+  {  // gate/up + RMSNorm row scale + SwiGLU
     GemmParams g = gemm_params(c, F, H, R, (F + 63) / 64, status);
+    g.epi.sq_in = f32(c->L.x1sq);
+    g.epi.sq_parts = H / 32;
+    g.epi.sq_ld = c->max_rows;
+    g.epi.sq_inv_n = 1.0f / static_cast<float>(H);
+    g.epi.sq_eps = cf.rms_eps;
     g.epi.out_bf16 = ws_ptr<__nv_bfloat16>(c, c->L.act);
     g.epi.out_lo_off = (long long)c->max_rows * F;
     g.epi.ld_bf16 = F;
@@ -628,13 +635,14 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     a.row_off = pp.t.row_off;
     a.draft_off = pp.t.draft_off;
     a.row_stats = ws_ptr<float2>(c, c->L.rowstats);
-    fill_accept_scratch(c, a, pp);
+    fill_accept_scratch(c, a);
     a.accepted = accepted;
     a.final_tokens = final_tokens;
     a.status = status;
     a.B = b->B;
     a.V = V;
-    SDV_CUDA(launch_accept(a, true, R, s));
+    a.R = b->R;
+    SDV_CUDA(launch_accept(a, true, s));
   }
   if (r->probs) SDV_CUDA(launch_probs(z, ws_ptr<float2>(c, c->L.rowstats), r->probs, R, V, status, s));
   SDV_CUDA(mark(SDV_PHASE_REALIGN));
@@ -660,13 +668,14 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
   a.draft_lens = b->draft_lens;
   a.row_off = pp.t.row_off;
   a.draft_off = pp.t.draft_off;
-  fill_accept_scratch(c, a, pp);
+  fill_accept_scratch(c, a);
   a.accepted = accepted;
   a.final_tokens = final_tokens;
   a.status = r->status;
   a.B = b->B;
   a.V = c->cfg.vocab;
-  SDV_CUDA(launch_accept(a, false, b->R, s));
+  a.R = b->R;
+  SDV_CUDA(launch_accept(a, false, s));
   RealignParams rp = realign_params(c, b, r, accepted, final_tokens);
   SDV_CUDA(launch_realign(rp, s));
   return SDV_OK;

@@ -234,4 +234,11 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Merge two softmax partial states (max M, sum of exp(z - M)) into one.
+__device__ __forceinline__ void merge_ms(float& M, float& S, float oM, float oS) {
+  const float nm = fmaxf(M, oM);
+  S = (M == -INFINITY ? 0.f : S * exp2f((M - nm) * kLog2e)) + (oM == -INFINITY ? 0.f : oS * exp2f((oM - nm) * kLog2e));
+  M = nm;
+}
+
 }  // namespace sdv

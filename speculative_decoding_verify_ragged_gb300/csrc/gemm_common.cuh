@@ -29,10 +29,43 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) 
 // Every per-row global load of a batch of rows is issued before any is used,
 // so a batch costs one memory latency instead of one per row.
 template <int EPI, int LD>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, const float* epi, int tm, int row0, int nrows,
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, int tm, int row0, int nrows,
                                               int tid) {
   const EpiParams& e = p.epi;
   constexpr int RB = 16;  // rows per batch
+  if constexpr (EPI == EPI_RESID) {
+    if (e.norm_gain) {
+      // residual output that an RMSNorm reads next: x, the planes of x * gain,
+      // and each warp's 32-column sum of x^2 per row
+      const int col = tm * BM + tid;
+      const bool ok = col < p.N;
+      const int lane = tid & 31;
+      const float gn = ok ? bf2f(e.norm_gain[col]) : 0.f;
+      for (int n0 = 0; n0 < nrows; n0 += RB) {
+        float res[RB];
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          res[q] = (ok && n < nrows) ? e.resid_f32[(long long)(row0 + n) * e.ld_f32 + col] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < RB; ++q) {
+          const int n = n0 + q;
+          if (n < nrows) {
+            const float x = ok ? epi[n * LD + tid] + res[q] : 0.f;
+            if (ok) {
+              const long long idx = (long long)(row0 + n) * e.ld_f32 + col;
+              e.out_f32[idx] = x;
+              store_planes(e.norm_out, e.norm_lo_off, idx, x * gn);
+            }
+            const float ss = warp_sum(x * x);
+            if (lane == 0) e.sq_out[(long long)(col >> 5) * e.sq_ld + row0 + n] = ss;
+          }
+        }
+      }
+      return;
+    }
+  }
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const int col = tm * BM + tid;
     if (col < p.N) {
@@ -60,10 +93,22 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, const float* 
     // is the next GEMM's input, written as bf16 hi + lo planes
     const int j = tid & 63;
     const int f = tm * 64 + j;
+    if (e.sq_in) {
+      // the input was x * gain: each row's 1 / rms(x) from the partial sums of x^2
+      const int warp = tid >> 5, lane = tid & 31;
+      for (int n = warp; n < nrows; n += 4) {
+        float ss = 0.f;
+        for (int q = lane; q < e.sq_parts; q += 32) ss += e.sq_in[(long long)q * e.sq_ld + row0 + n];
+        ss = warp_sum(ss);
+        if (lane == 0) epi[n * LD + BM] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
+      }
+      named_sync(1, 4 * kWarp);
+    }
     if (f < p.N) {
       for (int n = tid >> 6; n < nrows; n += 2) {
-        const float gt = epi[n * LD + j];
-        const float up = epi[n * LD + 64 + j];
+        const float sc = e.sq_in ? epi[n * LD + BM] : 1.f;
+        const float gt = epi[n * LD + j] * sc;
+        const float up = epi[n * LD + 64 + j] * sc;
         const float s = gt / (1.0f + expf(-gt));
         store_planes(e.out_bf16, e.out_lo_off, (long long)(row0 + n) * e.ld_bf16 + f, s * up);
       }

@@ -28,6 +28,17 @@ struct EpiParams {
   long long out_lo_off = 0;
   int ld_bf16 = 0;
   const float* resid_f32 = nullptr;  // RESID: residual [R, ld_f32]
+  // RESID feeding an RMSNorm: also the next GEMM's input x * gain as bf16 hi + lo
+  // planes and per-32-column partial sums of x^2, [N / 32, sq_ld]
+  const __nv_bfloat16* norm_gain = nullptr;
+  __nv_bfloat16* norm_out = nullptr;
+  long long norm_lo_off = 0;
+  float* sq_out = nullptr;
+  int sq_ld = 0;
+  // SWIGLU after such a norm: each row scaled by 1 / sqrt(sum(partials) * sq_inv_n + sq_eps)
+  const float* sq_in = nullptr;
+  int sq_parts = 0;
+  float sq_inv_n = 0.f, sq_eps = 0.f;
   // QKV
   __nv_bfloat16* kv_pool = nullptr;
   const int* page_table = nullptr;
@@ -161,8 +172,6 @@ cudaError_t launch_rmsnorm(const float* x, const __nv_bfloat16* gain, __nv_bfloa
 
 struct AcceptParams {
   const float* z = nullptr;        // logits [R, V] (from_logits)
-  const float2* tile_stats = nullptr;  // [m_tiles, stats_ld]
-  int m_tiles = 0, stats_ld = 0;
   const float* probs = nullptr;    // [R, V] (given probabilities)
   const float* draft_probs = nullptr;
   const float* uniforms = nullptr;
@@ -170,20 +179,20 @@ struct AcceptParams {
   const int* draft_lens = nullptr;
   const int* row_off = nullptr;
   const int* draft_off = nullptr;
-  float2* row_stats = nullptr;     // [R] (max, sum) written when from logits
-  const int* row_seq = nullptr;    // [R]
-  float* p_draft = nullptr;        // [R] target probability of the next draft token
-  int* slot_count = nullptr;       // [B] rows finished per slot (zero between calls)
+  const float2* tile_stats = nullptr;  // [m_tiles, stats_ld] LM head's per-tile (max, sum) (from_logits)
+  int m_tiles = 0, stats_ld = 0;
+  float2* row_stats = nullptr;         // [R] (max, sum) of each row's logits (from_logits)
   int* chunk_count = nullptr;      // [B] sampling chunks finished per slot (zero between calls)
   unsigned long long* chunk_sums = nullptr;  // [B, 2, chunk_ld]
   int chunk_ld = 0;
   int* accepted = nullptr;
   int* final_tokens = nullptr;
   int* status = nullptr;
-  int B = 0, V = 0;
+  int B = 0, V = 0, R = 0;
 };
-// Acceptance (one block per row) then final-token sampling (one block per vocab chunk and slot).
-cudaError_t launch_accept(const AcceptParams& p, bool from_logits, int R, cudaStream_t stream);
+// Acceptance (one block per slot: its rows' softmax normalisers, then the
+// draft tests) and final-token sampling (one block per vocab chunk and slot).
+cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream);
 int accept_chunks(int V);
 cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, int R, int V, const int* status,
                          cudaStream_t stream);

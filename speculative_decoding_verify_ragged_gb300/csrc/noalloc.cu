@@ -41,11 +41,10 @@ constexpr size_t kRowPos = kRowSeq + al(kMaxRows * 4);
 constexpr size_t kChunks = kRowPos + al(kMaxRows * 4);
 constexpr size_t kItemOff = kChunks + al(kMaxSlots * 4);
 constexpr size_t kSched = kItemOff + al((kMaxSlots + 1) * 4);
-constexpr size_t kPDraft = kSched + al(64);
-constexpr size_t kAccepted = kPDraft + al(kMaxRows * 4);
+constexpr size_t kAccepted = kSched + al(64);
 constexpr size_t kFinal = kAccepted + al(kMaxSlots * 4);
-constexpr size_t kCounters = kFinal + al(kMaxSlots * 4);  // slot_count then chunk_count
-constexpr size_t kChunkSums = kCounters + al(2 * kMaxSlots * 4);
+constexpr size_t kCounters = kFinal + al(kMaxSlots * 4);  // sampling chunks finished per slot
+constexpr size_t kChunkSums = kCounters + al(kMaxSlots * 4);
 constexpr size_t kScratchBytes = kChunkSums + al((size_t)kMaxSlots * 2 * kChunkLd * 8);
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
@@ -93,7 +92,7 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
   if (e != cudaSuccess) return SDV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the arrival counters must start at zero whatever the last call left
-  if (cudaMemsetAsync(s + kCounters, 0, 2 * kMaxSlots * 4, st) != cudaSuccess) return SDV_ERR_CUDA;
+  if (cudaMemsetAsync(s + kCounters, 0, kMaxSlots * 4, st) != cudaSuccess) return SDV_ERR_CUDA;
 
   PrologueParams pp;
   pp.t.row_off = reinterpret_cast<int*>(s + kRowOff);
@@ -133,10 +132,7 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
   a.draft_lens = b->draft_lens;
   a.row_off = pp.t.row_off;
   a.draft_off = pp.t.draft_off;
-  a.row_seq = pp.t.row_seq;
-  a.p_draft = reinterpret_cast<float*>(s + kPDraft);
-  a.slot_count = reinterpret_cast<int*>(s + kCounters);
-  a.chunk_count = reinterpret_cast<int*>(s + kCounters) + kMaxSlots;
+  a.chunk_count = reinterpret_cast<int*>(s + kCounters);
   a.chunk_sums = reinterpret_cast<unsigned long long*>(s + kChunkSums);
   a.chunk_ld = kChunkLd;
   a.accepted = accepted;
@@ -144,7 +140,8 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
   a.status = r->status;
   a.B = b->B;
   a.V = cfg->vocab;
-  if (launch_accept(a, false, b->R, st) != cudaSuccess) return SDV_ERR_CUDA;
+  a.R = b->R;
+  if (launch_accept(a, false, st) != cudaSuccess) return SDV_ERR_CUDA;
 
   RealignParams rp;
   rp.seq_lens = b->seq_lens;

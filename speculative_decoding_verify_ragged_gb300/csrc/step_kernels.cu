@@ -300,12 +300,13 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 // ---------------------------------------------------------------------------
 // acceptance + final-token sampling
 //
-// Kernel A (one block per verify row): the row's softmax normaliser from the
-// LM head's per-tile statistics and the target probability of the next draft
-// token; the last row of a sequence to finish runs the acceptance scan.
+// Kernel A (one block per sequence): the softmax normalisers of the
+// sequence's rows from the LM head's per-tile statistics, then every draft's
+// test in parallel; the first failing u < min(1, p/q) ends the accepted prefix.
 // Kernel B (one block per (vocab chunk, sequence)): integer weight sums of the
-// final row over the chunk (residual and plain), the last chunk to finish
+// final row over the chunk (residual and plain); the last chunk to finish
 // draws the token.  Integer sums make the draw independent of block order.
+// Both read the caller's draft inputs before waiting for the kernel ahead.
 // ---------------------------------------------------------------------------
 
 constexpr int kAccThreads = 256;
@@ -331,87 +332,104 @@ __device__ __forceinline__ unsigned long long fixed_weight(float w) {
   return static_cast<unsigned long long>(w * 4294967296.0f);
 }
 
-__device__ __forceinline__ void merge_ms(float& M, float& S, float oM, float oS) {
-  const float nm = fmaxf(M, oM);
-  S = (M == -INFINITY ? 0.f : S * exp2f((M - nm) * kLog2e)) + (oM == -INFINITY ? 0.f : oS * exp2f((oM - nm) * kLog2e));
-  M = nm;
+// First row of slot b: the sum of (gamma + 1) over the earlier slots, from the
+// caller's draft lengths (so it can be read before the kernel ahead finishes).
+__device__ int slot_row0(const int* draft_lens, int b, int* s_tmp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int part = 0;
+  for (int j = threadIdx.x; j < b; j += kAccThreads) part += draft_lens[j] + 1;
+  part = warp_sum(part);
+  if (lane == 0) s_tmp[warp] = part;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < kAccWarps; ++w) t += s_tmp[w];
+  __syncthreads();
+  return t;
 }
 
 template <bool FROM_LOGITS>
-__global__ void __launch_bounds__(kAccThreads) accept_rows_kernel(const AcceptParams p) {
-  __shared__ float s_m[kAccWarps], s_s[kAccWarps];
-  __shared__ int s_last;
-  __shared__ int s_ok[64];
+__global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams p) {
+  __shared__ int s_tmp[kAccWarps];
+  __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
+  __shared__ float2 s_st[64];
+  __shared__ int s_a;
   griddep_launch_dependents();
+  const int b = blockIdx.x;
+  const int V = p.V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gam = p.draft_lens[b];
+  const int r0 = slot_row0(p.draft_lens, b, s_tmp);
+  const int g0 = r0 - b;  // draft rows of the earlier slots
+  // inputs are validated by the prologue; until its verdict is read every read is bounds-checked
+  const bool in_range = gam >= 0 && gam < 64 && r0 >= 0 && r0 + gam < p.R;
+  int x = 0;
+  float qk = 0.f, uk = 0.f;
+  if (in_range && threadIdx.x < gam) {
+    x = p.tokens[r0 + threadIdx.x + 1];
+    if (x >= 0 && x < V) {
+      qk = p.draft_probs[(long long)(g0 + threadIdx.x) * V + x];
+      uk = p.uniforms[r0 + threadIdx.x];
+    }
+  }
+  if (threadIdx.x == 0) s_a = gam;
   griddep_wait();
   if (read_status(p.status) != 0) return;
-  const int r = blockIdx.x;
-  const int b = p.row_seq[r];
-  const int r0 = p.row_off[b];
-  const int i = r - r0;
-  const int gam = p.draft_lens[b];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int V = p.V;
-  float M = 0.f, S = 1.f;
+  __syncthreads();  // s_a is set before any test lowers it
+  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
+  float zx = 0.f;
   if constexpr (FROM_LOGITS) {
-    M = -INFINITY;
-    S = 0.f;
-    for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
-      const float2 st = p.tile_stats[(long long)tt * p.stats_ld + r];
-      merge_ms(M, S, st.x, st.y);
-    }
+    if (threadIdx.x < gam) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
+    // softmax normalisers of rows r0 .. r0 + gam: each thread merges a slice of
+    // the vocabulary tiles of 8 rows at a time (all its loads in flight together)
+    for (int n0 = 0; n0 <= gam; n0 += 8) {
+      const int nr = min(8, gam + 1 - n0);
+      float M[8], S[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oM = __shfl_xor_sync(0xffffffffu, M, o);
-      const float oS = __shfl_xor_sync(0xffffffffu, S, o);
-      merge_ms(M, S, oM, oS);
+      for (int q = 0; q < 8; ++q) {
+        M[q] = -INFINITY;
+        S[q] = 0.f;
+      }
+#pragma unroll 2
+      for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
+        float2 st[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st[q] = q < nr ? p.tile_stats[(long long)tt * p.stats_ld + r0 + n0 + q] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) merge_ms(M[q], S[q], st[q].x, st[q].y);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float oM = __shfl_xor_sync(0xffffffffu, M[q], o);
+          const float oS = __shfl_xor_sync(0xffffffffu, S[q], o);
+          merge_ms(M[q], S[q], oM, oS);
+        }
+        if (lane == 0) {
+          s_m[warp][q] = M[q];
+          s_s[warp][q] = S[q];
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x < nr) {
+        float Mr = -INFINITY, Sr = 0.f;
+        for (int w = 0; w < kAccWarps; ++w) merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
+        s_st[n0 + threadIdx.x] = make_float2(Mr, Sr);
+        p.row_stats[r0 + n0 + threadIdx.x] = make_float2(Mr, Sr);
+      }
+      __syncthreads();
     }
-    if (lane == 0) {
-      s_m[warp] = M;
-      s_s[warp] = S;
-    }
-    __syncthreads();
-    M = -INFINITY;
-    S = 0.f;
-    for (int w = 0; w < kAccWarps; ++w) merge_ms(M, S, s_m[w], s_s[w]);
   }
-  if (threadIdx.x == 0) {
-    if constexpr (FROM_LOGITS) p.row_stats[r] = make_float2(M, S);
-    if (i < gam) {
-      const int x = p.tokens[r + 1];
-      PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
-      p.p_draft[r] = src.p(r, x, M, S);
-    }
-    __threadfence();
-    const int old = atomicAdd(&p.slot_count[b], 1);
-    s_last = old == gam ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  // last row of the sequence: every draft's test in parallel, then the first
-  // draft failing u < min(1, p/q) ends the accepted prefix
-  __threadfence();
-  const int g0 = p.draft_off[b];
   if (threadIdx.x < gam) {
     const int k = threadIdx.x;
-    const int x = p.tokens[r0 + k + 1];
-    const float pk = __ldcg(&p.p_draft[r0 + k]);
-    const float qk = p.draft_probs[(long long)(g0 + k) * V + x];
-    const float uk = p.uniforms[r0 + k];
-    s_ok[k] = ((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk)) ? 1 : 0;
+    float pk;
+    if constexpr (FROM_LOGITS) pk = expf(zx - s_st[k].x) / s_st[k].y;
+    else pk = src.p(r0 + k, x, 0.f, 1.f);
+    if (!((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk))) atomicMin(&s_a, k);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int a = gam;
-    for (int k = 0; k < gam; ++k) {
-      if (!s_ok[k]) {
-        a = k;
-        break;
-      }
-    }
-    p.accepted[b] = a;
-    p.slot_count[b] = 0;  // ready for the next call
-  }
+  if (threadIdx.x == 0) p.accepted[b] = s_a;
 }
 
 template <bool FROM_LOGITS>
@@ -419,18 +437,22 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   __shared__ unsigned long long s_red[2][kAccWarps];
   __shared__ unsigned long long s_scan[kAccWarps];
   __shared__ int s_last, s_mode, s_chunk, s_tok;
+  __shared__ int s_tmp[kAccWarps];
   __shared__ unsigned long long s_T, s_base;
   __shared__ unsigned long long s_cs[2][kMaxSampleChunks];
   griddep_launch_dependents();
-  griddep_wait();
-  if (read_status(p.status) != 0) return;
   const int c = blockIdx.x, b = blockIdx.y;
   const int nch = gridDim.x;
   const int V = p.V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gam = p.draft_lens[b];
+  const int r0 = slot_row0(p.draft_lens, b, s_tmp);
+  const int g0 = r0 - b;
+  griddep_wait();
+  if (read_status(p.status) != 0) return;
   const int a = p.accepted[b];
-  const int rf = p.row_off[b] + a;
-  const float* qrow = a < gam ? p.draft_probs + (long long)(p.draft_off[b] + a) * V : nullptr;
+  const int rf = r0 + a;
+  const float* qrow = a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
   float M = 0.f, S = 1.f;
   if constexpr (FROM_LOGITS) {
     const float2 st = p.row_stats[rf];
@@ -438,7 +460,6 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     S = st.y;
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // chunk sums of the residual weights max(0, p - q) and of the plain weights p
   unsigned long long sr = 0, sp = 0;
@@ -748,14 +769,14 @@ cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo
   return launch_pdl(split_planes_kernel, dim3(grid), dim3(256), 0, stream, x, out, lo_off, n);
 }
 
-cudaError_t launch_accept(const AcceptParams& p, bool from_logits, int R, cudaStream_t stream) {
+cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
   const dim3 grid((p.V + kVChunk - 1) / kVChunk, p.B);
   cudaError_t e;
   if (from_logits) {
-    if ((e = launch_pdl(accept_rows_kernel<true>, dim3(R), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
+    if ((e = launch_pdl(accept_kernel<true>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
     return launch_pdl(sample_kernel<true>, grid, dim3(kAccThreads), 0, stream, p);
   }
-  if ((e = launch_pdl(accept_rows_kernel<false>, dim3(R), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(accept_kernel<false>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
   return launch_pdl(sample_kernel<false>, grid, dim3(kAccThreads), 0, stream, p);
 }
 
