@@ -15,14 +15,16 @@
 //    sizes the chunks so that the items cover all SMs, whatever the mix of
 //    context lengths (a batch of one long sequence and a swarm of 128 alike);
 //  * a producer warp streams each (page, KV head) block -- 16 keys and 16
-//    values of head_dim -- with 128-byte-swizzled TMA loads into an 8-stage
+//    values of head_dim -- with 128-byte-swizzled TMA loads into a 16-stage
 //    ring; seven consumer warps run QK^T and PV on bf16 mma.sync with an
 //    online softmax in fp32.  The item's query vectors (draft rows x query
 //    heads of the group, at most 48) form 1-3 tiles of 16; the warps split
 //    as (query tile) x (key phase), each key phase taking every KS-th page,
 //    so a 16-vector item still keeps seven warps busy, and the phases'
 //    (max, sum, output) states are combined in shared memory at the end of
-//    the item.  q (fp32) and the softmax weights enter the MMAs as bf16 hi +
+//    the item.  A warp waits only for the pages it reads and releases them
+//    itself (the query-tile-0 warp of a page arrives for the warps that skip
+//    it), so up to seven pages are in work while the rest of the ring fills;  q (fp32) and the softmax weights enter the MMAs as bf16 hi +
 //    lo pairs, so the output keeps ~17 significant bits against the bf16
 //    cache; the hi and lo products and even and odd k steps accumulate
 //    separately, so no MMA waits on more than three others;
@@ -42,7 +44,8 @@ constexpr int kThreads = (kConsumers + 1) * kWarp;
 
 template <int D>
 struct ACfg {
-  static constexpr int STAGES = 8;
+  // pages in work (one per consumer warp) plus ~8 in flight from HBM
+  static constexpr int STAGES = 16;
   static constexpr int BOX = 64 * 16 * 2;             // one 64-wide half of 16 rows: 2 KB
   static constexpr int HALVES = D / 64;
   static constexpr int PAGE_BYTES = 2 * HALVES * BOX;  // K and V of one (page, kv head)
@@ -216,11 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int nf = 0; nf < NF; ++nf) o[nf][0] = o[nf][1] = o[nf][2] = o[nf][3] = 0.f;
 
     for (int pi = it.p0; pi < it.p1; ++pi) {
-      if (!dead && !mbar_wait(&full[stage], phase)) {
+      const bool mine = active && (pi - it.p0) % ks_n == ks;
+      if (mine && !dead && !mbar_wait(&full[stage], phase)) {
         set_status(p.status, SDV_ERR_TIMEOUT);
         dead = true;
       }
-      if (active && (pi - it.p0) % ks_n == ks) {
+      if (mine && !dead) {
         const uint32_t kbase = smem_u32(smem + stage * C::PAGE_BYTES);
         const uint32_t vbase = kbase + C::HALVES * C::BOX;
         // four independent accumulator sets: (hi, lo) x (even, odd k step)
@@ -309,8 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
           mma_bf16(o[nf + 1], pl, b2, b3);
         }
       }
+      // the page's readers release it: kConsumers arrivals in all, the
+      // query-tile-0 reader standing in for the warps that do not read it
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (mine && lane == 0) mbar_arrive_count(&empty[stage], qt == 0 ? kConsumers - qtiles + 1 : 1);
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1;

@@ -303,9 +303,10 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 // Kernel A (one block per sequence): the softmax normalisers of the
 // sequence's rows from the LM head's per-tile statistics, then every draft's
 // test in parallel; the first failing u < min(1, p/q) ends the accepted prefix.
-// Kernel B (one block per (vocab chunk, sequence)): integer weight sums of the
-// final row over the chunk (residual and plain); the last chunk to finish
-// draws the token.  Integer sums make the draw independent of block order.
+// Kernel B (a few blocks per sequence, one warp per 1024-entry vocab chunk):
+// integer weight sums of the final row over each chunk (residual and plain);
+// the sequence's last block to finish draws the token.  Integer sums make the
+// draw independent of block order.
 // Both read the caller's draft inputs before waiting for the kernel ahead.
 // ---------------------------------------------------------------------------
 
@@ -432,6 +433,24 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   if (threadIdx.x == 0) p.accepted[b] = s_a;
 }
 
+// Fixed-point weights of one float4 of p (and of the residual against q).
+template <bool FROM_LOGITS>
+__device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M, float S, unsigned long long& sr,
+                                         unsigned long long& sp) {
+  float pj[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (FROM_LOGITS) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pj[e] = expf(pj[e] - M) / S;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sp += fixed_weight(pj[e]);
+  if (has_q) {
+    const float qj[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sr += fixed_weight(fmaxf(0.f, pj[e] - qj[e]));
+  }
+}
+
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams p) {
   __shared__ unsigned long long s_red[2][kAccWarps];
@@ -441,9 +460,9 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   __shared__ unsigned long long s_T, s_base;
   __shared__ unsigned long long s_cs[2][kMaxSampleChunks];
   griddep_launch_dependents();
-  const int c = blockIdx.x, b = blockIdx.y;
-  const int nch = gridDim.x;
+  const int b = blockIdx.y;
   const int V = p.V;
+  const int nch = (V + kVChunk - 1) / kVChunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gam = p.draft_lens[b];
   const int r0 = slot_row0(p.draft_lens, b, s_tmp);
@@ -461,43 +480,63 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
 
-  // chunk sums of the residual weights max(0, p - q) and of the plain weights p
-  unsigned long long sr = 0, sp = 0;
-  for (int e = threadIdx.x; e < kVChunk; e += kAccThreads) {
-    const int j = c * kVChunk + e;
-    if (j < V) {
-      const float pj = src.p(rf, j, M, S);
-      sp += fixed_weight(pj);
-      if (qrow) sr += fixed_weight(fmaxf(0.f, pj - qrow[j]));
+  // chunk sums of the residual weights max(0, p - q) and of the plain weights
+  // p: warp w of block x takes chunks x * warps + w, stepping over the slot's
+  // blocks; each lane issues all its loads of a chunk before using them
+  unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
+  const float* prow = (FROM_LOGITS ? p.z : p.probs) + (long long)rf * V;
+  const bool vec = (V & 3) == 0;  // rows are 16-byte aligned: float4 loads
+  constexpr int kVecPerLane = kVChunk / (4 * kWarp);
+  for (int c = blockIdx.x * kAccWarps + warp; c < nch; c += gridDim.x * kAccWarps) {
+    unsigned long long sr = 0, sp = 0;
+    const int j0 = c * kVChunk;
+    if (vec) {
+      const bool has_q = qrow != nullptr;
+      float4 zv[kVecPerLane], qv[kVecPerLane];
+#pragma unroll
+      for (int e = 0; e < kVecPerLane; ++e) {
+        const int j = j0 + (e * kWarp + lane) * 4;
+        zv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[e] = zv[e];
+        if (j < V) {
+          zv[e] = __ldcs(reinterpret_cast<const float4*>(prow + j));
+          if (has_q) qv[e] = __ldcs(reinterpret_cast<const float4*>(qrow + j));
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < kVecPerLane; ++e) {
+        const int j = j0 + (e * kWarp + lane) * 4;
+        if (j < V) weights4<FROM_LOGITS>(zv[e], qv[e], has_q, M, S, sr, sp);
+      }
+    } else {
+      for (int e = lane; e < kVChunk; e += kWarp) {
+        const int j = j0 + e;
+        if (j < V) {
+          const float pj = src.p(rf, j, M, S);
+          sp += fixed_weight(pj);
+          if (qrow) sr += fixed_weight(fmaxf(0.f, pj - qrow[j]));
+        }
+      }
     }
-  }
-  sr = warp_sum_u64(sr);
-  sp = warp_sum_u64(sp);
-  if (lane == 0) {
-    s_red[0][warp] = sr;
-    s_red[1][warp] = sp;
+    sr = warp_sum_u64(sr);
+    sp = warp_sum_u64(sp);
+    if (lane == 0) {
+      cs[c] = sr;
+      cs[p.chunk_ld + c] = sp;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned long long tr = 0, tp = 0;
-    for (int w = 0; w < kAccWarps; ++w) {
-      tr += s_red[0][w];
-      tp += s_red[1][w];
-    }
-    unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
-    cs[c] = tr;
-    cs[p.chunk_ld + c] = tp;
     __threadfence();
     const int old = atomicAdd(&p.chunk_count[b], 1);
-    s_last = old == nch - 1 ? 1 : 0;
+    s_last = old == (int)gridDim.x - 1 ? 1 : 0;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
-  // last chunk of this sequence: pick the mode, the target and the chunk
+  // last block of this sequence: pick the mode, the target and the chunk
   {
-    const unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
     for (int k = threadIdx.x; k < nch; k += kAccThreads) {
       s_cs[0][k] = __ldcg(&cs[k]);
       s_cs[1][k] = __ldcg(&cs[p.chunk_ld + k]);
@@ -769,8 +808,26 @@ cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo
   return launch_pdl(split_planes_kernel, dim3(grid), dim3(256), 0, stream, x, out, lo_off, n);
 }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+static int sms_of_current_device() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
-  const dim3 grid((p.V + kVChunk - 1) / kVChunk, p.B);
+  // sampling: about two blocks per SM over the whole batch, never more blocks
+  // per slot than its vocabulary has chunks for (one warp per chunk)
+  const int nch = (p.V + kVChunk - 1) / kVChunk;
+  const int max_per_slot = (nch + kAccWarps - 1) / kAccWarps;
+  const int want = (2 * sms_of_current_device() + p.B - 1) / p.B;
+  const dim3 grid(want < 1 ? 1 : (want > max_per_slot ? max_per_slot : want), p.B);
   cudaError_t e;
   if (from_logits) {
     if ((e = launch_pdl(accept_kernel<true>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
