@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[2, 3])
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling run: no clock pre-roll, no e2e or CPU legs (its numbers are not bench values)")
@@ -504,6 +504,164 @@ def run_sweep(args):
                       "gemm_path": args.gemm_path}), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the agent swarm: continuous batching with the budget rule (int4 layer)
+# ---------------------------------------------------------------------------
+
+SWARM = dict(slots=128, budget=512, gamma_max=3, ctx=(1024, 16384), outs=(40, 900), requests=4096)
+
+
+def swarm_desc():
+    s = SWARM
+    return dict(workload=f"agent swarm: {s['slots']} slots refilled every step from a queue (continuous batching), "
+                         f"gamma = clamp((512 - B) / B, 0, 3), ctx U{{1024..16384}}, outputs log-uniform 40..900, "
+                         f"acceptance {{0.97, 0.8, 0.14}} per sequence, 9B-class layer int4 g32 + bf16 LM head, "
+                         f"vocab 151936",
+                slots=s["slots"], budget_rows=s["budget"], gamma_max=s["gamma_max"],
+                l2="inputs larger than L2 (KV ~4.5 GB per step)")
+
+
+class SwarmDrafter:
+    """Stand-in for the drafters: tokens uniform over the vocabulary, q built around
+    the target's own p (a prepass of the forward on a copy of the slot state) so each
+    draft is accepted with its sequence's alpha, uniforms on the 24-bit grid."""
+
+    def __init__(self, eng, run, alphas, V, max_rows):
+        import torch
+        self.eng, self.run, self.V = eng, run, V
+        self.alphas = torch.as_tensor(alphas, dtype=torch.float64)
+        self.probs = torch.empty((max_rows, V), dtype=torch.float32, device="cuda")
+        self.pstatus = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.n = 0
+
+    def __call__(self, st, batch):
+        import torch
+        import workloads as wl
+        from workloads import device as wd
+        k = self.n
+        self.n += 1
+        R, G, B, gam = st["rows"], st["drafts"], st["live"], st["gamma"]
+        g = wl.rng(5, wl.S_TOKENS, k)
+        batch["tokens"] = torch.from_numpy(g.integers(0, self.V, size=R).astype(np.int32)).cuda()
+        batch["uniforms"] = torch.from_numpy(wl.uniform24(wl.rng(5, wl.S_U, k), R)).cuda()
+        q = wd.draft_probs_device(G, self.V, wl._key(5, wl.S_Q, k))
+        batch["draft_probs"] = q
+        if G == 0:
+            return
+        # prepass on a copy of the state realignment moves (page rows, counts, free stack)
+        pt, npg = batch["page_table"].clone(), batch["num_pages"].clone()
+        fp, nf = self.run.free_pages.clone(), self.run.num_free.clone()
+        self.pstatus.zero_()
+        self.eng.verify_step(batch, dict(probs=self.probs[:R], status=self.pstatus))
+        batch["page_table"].copy_(pt)
+        batch["num_pages"].copy_(npg)
+        self.run.free_pages.copy_(fp)
+        self.run.num_free.copy_(nf)
+        ids = torch.tensor(st["ids"], dtype=torch.long)
+        wd.retarget_draft_probs_device(q, self.probs[:R], batch["tokens"], gam, self.alphas[ids])
+
+
+def swarm_step_bytes(seq_lens, R, B, G, V=151936):
+    """Algorithmic bytes of one swarm step: int4 layer weights (codes + fp16 group
+    scales) and the bf16 LM head once, every sequence's KV read, the new rows' KV
+    written, q at the draft tokens plus each sequence's final q row, activations."""
+    H, F, D, nq, nkv = 4096, 12288, 128, 32, 8
+    layer = ((nq + 2 * nkv) * D * H + H * nq * D + 3 * F * H)
+    w = layer // 2 + layer // 32 * 2 + V * H * 2
+    kv = int(sum(seq_lens)) * nkv * 2 * D * 2 + R * nkv * 2 * D * 2
+    return w + kv + G * 4 + B * V * 4 + R * H * 2
+
+
+def run_swarm(args):
+    import torch
+    import workloads as wl
+    from workloads import device as wd
+    from speculative_decoding_verify_ragged_gb300 import PHASES, VerifyEngine, kernel_launches
+    from speculative_decoding_verify_ragged_gb300.serve import SwarmRunner
+
+    torch.cuda.set_device(0)
+    S = SWARM
+    slots, budget, gmax, page, V = S["slots"], S["budget"], S["gamma_max"], 16, wl.NINE_B["vocab"]
+    W = wl.make_weights(wl.NINE_B, 5, fmt="int4")
+    Wd = wd.weights_to_device(W)
+    del W
+    eng = VerifyEngine(wd.config(wl.NINE_B, gmax, fmt="int4"), Wd, max_rows=budget, max_slots=slots)
+    max_pages = (S["ctx"][1] + S["outs"][1] + 2 * gmax + 1 + page - 1) // page + 1
+    pool_pages = slots * max_pages
+    pool = torch.empty((pool_pages, 8, 2, page, 128), dtype=torch.bfloat16, device="cuda")
+    wd.normal_bf16_device_(pool, wl._key(5, wl.S_KV, 0))
+    perm = torch.from_numpy(wl.rng(5, wl.S_SEQ, 3).permutation(pool_pages).astype(np.int32))
+    run = SwarmRunner(eng, pool, pool_pages, slots, budget, max_pages, free_order=perm)
+    lens, limits, alphas = wl.swarm_requests(S["requests"], ctx=S["ctx"], outs=S["outs"])
+    for i in range(len(lens)):
+        run.submit(i, int(lens[i]), int(limits[i]))
+    drafter = SwarmDrafter(eng, run, alphas, V, budget)
+    stream = torch.cuda.current_stream()
+
+    def one(timed):
+        m = run.sched.slots()
+        st, batch = run.plan()
+        ctx_now = m["seq_lens"] + st["admit_ctx"]
+        drafter(st, batch)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        run.verify(st, batch, stream)
+        e1.record(stream)
+        run.complete(st)
+        wall = time.perf_counter() - t0
+        return st, ctx_now, e0, e1, wall
+
+    for _ in range(args.warmup):
+        one(False)
+    clocks = ClockSampler(0)
+    n0 = kernel_launches()
+    e_before = run.sched.stats()["emitted"]
+    recs = [one(True) for _ in range(args.steps)]
+    launches = kernel_launches() - n0
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    emitted = run.sched.stats()["emitted"] - e_before
+    ms = [r[2].elapsed_time(r[3]) for r in recs]
+    total_ms = sum(ms)
+    hbm, tflops, peak_kind = measured_peaks()
+    step_bytes = [swarm_step_bytes(r[1], r[0]["rows"], r[0]["live"], r[0]["drafts"]) for r in recs]
+    achieved = sum(step_bytes) / (total_ms / 1e3) / 1e9
+    # phases of a few more steps, every boundary recorded (serialised), for the dominant kernel
+    nph = 5
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
+    ph_ctx = []
+    for j in range(nph):
+        eng.set_phase_events(evsets[j])
+        st, ctx_now, *_ = one(False)
+        ph_ctx.append((st, ctx_now))
+    eng.set_phase_events(None)
+    torch.cuda.synchronize()
+    ph_us = {p: statistics.mean(es[k].elapsed_time(es[k + 1]) for es in evsets) * 1e3 for k, p in enumerate(PHASES)}
+    kv_bytes = statistics.mean(int(sum(c)) * 4096 + st["rows"] * 4096 for st, c in ph_ctx)
+    attn_gbs = kv_bytes / (ph_us["attention"] * 1e-6) / 1e9
+    live = [r[0]["live"] for r in recs]
+    line = {"metric": METRIC, "value": emitted / (total_ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {**swarm_desc(), "parallelism": "replicas1",
+                       "mean_live": statistics.mean(live), "mean_rows": statistics.mean(r[0]["rows"] for r in recs),
+                       "mean_ctx": statistics.mean(statistics.mean(r[1]) for r in recs)},
+            "gpu_launches": int(launches), "clocks": clk,
+            "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+                         "traffic": None, "kernel": "paged attention (phase, serialised events)",
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": kv_bytes,
+                         "avg_launch_us": ph_us["attention"]},
+            "step_roofline": {"bound": "hbm", "achieved_GBps": achieved, "frac": achieved / hbm,
+                              "algorithmic_bytes": statistics.mean(step_bytes)},
+            "phases_us_serialised": ph_us,
+            "loop_wall_ms_per_step": statistics.mean(r[4] for r in recs) * 1e3,
+            "emitted_tokens_per_step": emitted / args.steps,
+            "finished_sequences": run.sched.stats()["finished"]}
+    print(json.dumps(line), flush=True)
+
+
 def reduce_over_ranks(elapsed_ms: float, tokens: int, e2e_ms_per_step, device):
     """Whole-job numbers over the replicas: the slowest rank's times and every
     rank's emitted tokens.  One process: the inputs unchanged."""
@@ -638,6 +796,8 @@ def main():
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.workload == 5:
+        run_swarm(args)
     else:
         run_ours(args)
 

@@ -195,6 +195,41 @@ sdv_status sdv_accept_static(const sdv_config *cfg, const float *probs, const sd
  * tokens/offsets, lengths, pages, free stack and the next-slot view. */
 sdv_status sdv_realign(sdv_ctx *ctx, const sdv_batch *batch, sdv_result *result, void *stream);
 
+/* Admission of new sequences into a slot table, the device half of continuous
+ * batching ("Why Static Batching Wastes an RX 9070 XT Agent Swarm and
+ * Continuous Batching Wins It Back", section "Continuous batching refills the
+ * slot instead of freezing it": a finished sequence's slot takes a waiting
+ * one on the very next step).  The table is the realignment's next-slot view
+ * (result->next_seq_lens, next_num_pages, next_page_table, next_gen_counts)
+ * holding `live` survivors; newcomer j goes to slot live + j with length
+ * ctx_lens[j] (positions already cached: prefill is not part of the step),
+ * generated count 0, output length out_lens[j], and
+ * ceil((ctx_lens[j] + gamma_max + 1) / page_size) pages popped from the top of
+ * the free stack in admission order (newcomer j's k-th page is the k-th popped
+ * for it); the rest of its page-table row is -1.  When gen_limits_prev and
+ * next_src are given, the survivors' output lengths are first gathered into
+ * gen_limits[0, live) (gen_limits_prev must not alias gen_limits).
+ * Host errors: live + n > slots, aliasing, null table pointers.  Device
+ * errors in *status: *num_live != live or a negative length (SDV_ERR_BAD_INPUT),
+ * too few free pages or a row wider than max_pages_per_seq (SDV_ERR_CAPACITY);
+ * nothing is written then.  A nonzero *status on entry makes it a no-op. */
+typedef struct {
+  int live;                   /* host: survivors already at slots [0, live) */
+  int n;                      /* host: sequences appended at slots [live, live + n), n <= 1024 */
+  int slots;                  /* host: rows of the slot table */
+  const int *num_live;        /* device scalar or NULL: the realignment's survivor count */
+  const int *next_src;        /* device [live] or NULL: old slot of each survivor */
+  const int *gen_limits_prev; /* device [old B] or NULL: output lengths before the compaction */
+  const int *ctx_lens;        /* device [n] */
+  const int *out_lens;        /* device [n] */
+  int *seq_lens, *num_pages, *gen_counts, *gen_limits; /* device [slots] */
+  int *page_table;            /* device [slots, max_pages_per_seq] */
+  int max_pages_per_seq;
+  int *free_pages;            /* device free stack, top at *num_free - 1 */
+  int *num_free;              /* device scalar, lowered by the pages popped */
+} sdv_admission;
+sdv_status sdv_admit(sdv_ctx *ctx, const sdv_admission *a, int *status, void *stream);
+
 /* y = x W^T for one of the context's projections, fp32 output without
  * rounding (parity tests of the weight-streaming GEMM).  which: 0 qkv, 1 o,
  * 2 gate, 3 up, 4 down, 5 lm_head.  x [rows, K] (device): x_format 0 = bf16,

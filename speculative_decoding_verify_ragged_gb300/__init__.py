@@ -17,8 +17,8 @@ from __future__ import annotations
 
 import ctypes
 
-from ._abi import (PHASES, RESULT_FIELDS, STATUS, SDV_OK, SDV_WEIGHTS_BF16, SDV_WEIGHTS_INT4_G32, SdvBatch, SdvConfig,
-                   SdvResult, SdvWeights, load_library)
+from ._abi import (PHASES, RESULT_FIELDS, STATUS, SDV_OK, SDV_WEIGHTS_BF16, SDV_WEIGHTS_INT4_G32, SdvAdmission,
+                   SdvBatch, SdvConfig, SdvResult, SdvWeights, load_library)
 
 __all__ = ["VerifyEngine", "SdvError", "PHASES", "STATUS", "load_library", "kernel_launches", "SDV_WEIGHTS_BF16",
            "SDV_WEIGHTS_INT4_G32"]
@@ -146,6 +146,21 @@ class VerifyEngine:
         bs = self.batch_struct(batch)
         self._check(self.lib.sdv_attention(self.handle, _ptr(q), ctypes.byref(bs), _ptr(out), _ptr(status),
                                            _stream(stream)), "sdv_attention")
+
+    def admit(self, table: dict, live: int, ctx_lens, out_lens, free_pages, num_free, status,
+              num_live=None, next_src=None, gen_limits_prev=None, stream=None):
+        """Append newcomers to a device slot table (sdv_admit).
+
+        table: dict of device int32 tensors seq_lens, num_pages, gen_counts,
+        gen_limits [slots] and page_table [slots, max_pages]; ctx_lens /
+        out_lens: device int32 [n]."""
+        pt = table["page_table"]
+        n = 0 if ctx_lens is None else int(ctx_lens.numel())
+        a = SdvAdmission(int(live), n, int(pt.shape[0]), _ptr(num_live), _ptr(next_src), _ptr(gen_limits_prev),
+                         _ptr(ctx_lens), _ptr(out_lens), _ptr(table["seq_lens"]), _ptr(table["num_pages"]),
+                         _ptr(table["gen_counts"]), _ptr(table["gen_limits"]), _ptr(pt), int(pt.shape[1]),
+                         _ptr(free_pages), _ptr(num_free))
+        self._check(self.lib.sdv_admit(self.handle, ctypes.byref(a), _ptr(status), _stream(stream)), "sdv_admit")
 
     def set_gemm_path(self, path: int):
         """0 auto (by row count), 1 bf16 mma.sync, 2 tcgen05 with TMEM accumulators."""

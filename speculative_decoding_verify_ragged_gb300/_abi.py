@@ -66,6 +66,32 @@ class SdvResult(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in RESULT_FIELDS]
 
 
+class SdvAdmission(ctypes.Structure):
+    _fields_ = [("live", c_int), ("n", c_int), ("slots", c_int),
+                ("num_live", c_void_p), ("next_src", c_void_p), ("gen_limits_prev", c_void_p),
+                ("ctx_lens", c_void_p), ("out_lens", c_void_p),
+                ("seq_lens", c_void_p), ("num_pages", c_void_p), ("gen_counts", c_void_p), ("gen_limits", c_void_p),
+                ("page_table", c_void_p), ("max_pages_per_seq", c_int),
+                ("free_pages", c_void_p), ("num_free", c_void_p)]
+
+
+SDV_SCHED_CONTINUOUS, SDV_SCHED_STATIC, SDV_SCHED_STATIC_SHRINK = 0, 1, 2
+
+
+class SdvSchedConfig(ctypes.Structure):
+    _fields_ = [(n, c_int) for n in ("max_slots", "gamma_max", "budget_rows", "page_size", "pool_pages",
+                                     "max_pages_per_seq", "policy")]
+
+
+class SdvSchedStep(ctypes.Structure):
+    _fields_ = [(n, c_int) for n in ("live", "width", "gamma", "rows", "drafts", "admitted")]
+
+
+class SdvSchedStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_longlong) for n in ("steps", "emitted", "slot_steps_paid", "slot_steps_live",
+                                                 "finished", "admitted")] + [("queued", c_int), ("free_pages", c_int), ("live", c_int)]
+
+
 _lib = None
 
 
@@ -107,6 +133,25 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_last_cuda_error.argtypes = []
     lib.sdv_kernel_launches.restype = ctypes.c_ulonglong
     lib.sdv_kernel_launches.argtypes = []
+    lib.sdv_admit.restype = c_int
+    lib.sdv_admit.argtypes = [c_void_p, P(SdvAdmission), c_void_p, c_void_p]
+    c_ll = ctypes.c_longlong
+    lib.sdv_sched_gamma.restype = c_int
+    lib.sdv_sched_gamma.argtypes = [c_int, c_int, c_int]
+    lib.sdv_sched_create.restype = c_int
+    lib.sdv_sched_create.argtypes = [P(SdvSchedConfig), P(c_void_p)]
+    lib.sdv_sched_destroy.restype = None
+    lib.sdv_sched_destroy.argtypes = [c_void_p]
+    lib.sdv_sched_submit.restype = c_int
+    lib.sdv_sched_submit.argtypes = [c_void_p, c_ll, c_int, c_int]
+    lib.sdv_sched_plan.restype = c_int
+    lib.sdv_sched_plan.argtypes = [c_void_p, P(SdvSchedStep), P(c_int), P(c_int), P(c_ll)]
+    lib.sdv_sched_complete.restype = c_int
+    lib.sdv_sched_complete.argtypes = [c_void_p, P(c_int), P(c_ll), P(c_int)]
+    lib.sdv_sched_get_stats.restype = c_int
+    lib.sdv_sched_get_stats.argtypes = [c_void_p, P(SdvSchedStats)]
+    lib.sdv_sched_slots.restype = c_int
+    lib.sdv_sched_slots.argtypes = [c_void_p, P(c_int), P(c_int), P(c_int), P(c_int)]
     _lib = lib
     return lib
 

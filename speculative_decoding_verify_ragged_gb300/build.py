@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdv.so")
-SOURCES = ("api.cu", "gemm.cu", "gemm_tc.cu", "gemm_q4.cu", "attention.cu", "step_kernels.cu", "noalloc.cu")
+SOURCES = ("api.cu", "gemm.cu", "gemm_tc.cu", "gemm_q4.cu", "attention.cu", "step_kernels.cu", "noalloc.cu", "sched.cpp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,7 +34,7 @@ def flags(extra=()):
 
 
 def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + (".cpp.o" if src.endswith(".cpp") else ".o"))
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + flags(extra)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

@@ -692,6 +692,24 @@ sdv_status sdv_realign(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stre
   return SDV_OK;
 }
 
+sdv_status sdv_admit(sdv_ctx* c, const sdv_admission* a, int* status, void* stream) {
+  if (!c || !a || !status) return SDV_ERR_INVALID_ARG;
+  if (a->live < 0 || a->n < 0 || a->n > 1024 || a->slots < 0 || a->live + a->n > a->slots) return SDV_ERR_INVALID_ARG;
+  if (a->n > 0 && (!a->ctx_lens || !a->out_lens || !a->seq_lens || !a->num_pages || !a->gen_counts ||
+                   !a->page_table || !a->free_pages))
+    return SDV_ERR_INVALID_ARG;
+  if (!a->num_free || !a->gen_limits || a->max_pages_per_seq < 1) return SDV_ERR_INVALID_ARG;
+  if ((a->gen_limits_prev == nullptr) != (a->next_src == nullptr)) return SDV_ERR_INVALID_ARG;
+  if (a->gen_limits_prev && a->gen_limits_prev == a->gen_limits) return SDV_ERR_INVALID_ARG;
+  AdmitParams p;
+  p.a = *a;
+  p.gamma_max = c->cfg.gamma_max;
+  p.page = c->cfg.page_size;
+  p.status = status;
+  SDV_CUDA(launch_admit(p, static_cast<cudaStream_t>(stream)));
+  return SDV_OK;
+}
+
 sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float* y, int rows, void* stream) {
   if (!c || !x || !y || rows <= 0 || rows > c->max_rows || which < 0 || which > 5) return SDV_ERR_INVALID_ARG;
   if (x_format != 0 && x_format != 1) return SDV_ERR_INVALID_ARG;

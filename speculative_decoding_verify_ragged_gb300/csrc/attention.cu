@@ -39,7 +39,8 @@ namespace sdv {
 
 namespace {
 
-constexpr int kConsumers = 7;  // + the producer: 256 threads, so up to 255 registers a thread
+constexpr int kConsumers = 7;
+constexpr float kLazy = 8.f;   // log2 headroom of the lazily moved softmax reference  // + the producer: 256 threads, so up to 255 registers a thread
 constexpr int kThreads = (kConsumers + 1) * kWarp;
 
 template <int D>
@@ -268,12 +269,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float base0 = n0 == -INFINITY ? 0.f : n0;
-        const float base1 = n1 == -INFINITY ? 0.f : n1;
-        const float a0 = exp2f(m0 - base0), a1 = exp2f(m1 - base1);
-        m0 = n0;
-        m1 = n1;
+        // lazy rescaling: the reference maximum moves only when a logit
+        // exceeds it by more than kLazy (so every weight stays <= 2^kLazy);
+        // o and l always share the reference, so the result is unchanged
+        if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+          const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+          const float a0 = exp2f(m0 - (n0 == -INFINITY ? 0.f : n0));
+          const float a1 = exp2f(m1 - (n1 == -INFINITY ? 0.f : n1));
+          m0 = n0;
+          m1 = n1;
+          l0 *= a0;
+          l1 *= a1;
+#pragma unroll
+          for (int nf = 0; nf < NF; ++nf) {
+            o[nf][0] *= a0;
+            o[nf][1] *= a0;
+            o[nf][2] *= a1;
+            o[nf][3] *= a1;
+          }
+        }
+        const float base0 = m0 == -INFINITY ? 0.f : m0;
+        const float base1 = m1 == -INFINITY ? 0.f : m1;
         float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
         for (int nf = 0; nf < 2; ++nf)
@@ -284,15 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             ps0 += s[nf][e];
             ps1 += s[nf][2 + e];
           }
-        l0 = l0 * a0 + ps0;
-        l1 = l1 * a1 + ps1;
-#pragma unroll
-        for (int nf = 0; nf < NF; ++nf) {
-          o[nf][0] *= a0;
-          o[nf][1] *= a0;
-          o[nf][2] *= a1;
-          o[nf][3] *= a1;
-        }
+        l0 += ps0;
+        l1 += ps1;
         // P enters the PV product as a bf16 pair hi + lo (about 16 significant
         // bits): a single bf16 P would add ~0.1 % noise to every output
         uint32_t pa[4], pl[4];

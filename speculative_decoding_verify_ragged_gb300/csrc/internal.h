@@ -216,6 +216,14 @@ struct RealignParams {
 };
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream);
 
+struct AdmitParams {
+  sdv_admission a;
+  int gamma_max = 0, page = 0;
+  int* status = nullptr;
+};
+// Append admitted sequences to a slot table (one block).
+cudaError_t launch_admit(const AdmitParams& p, cudaStream_t stream);
+
 // count of kernels launched by this library
 void note_launch(int n = 1);
 

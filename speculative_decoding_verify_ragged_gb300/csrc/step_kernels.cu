@@ -847,6 +847,68 @@ cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, 
   return launch_pdl(probs_kernel, dim3(grid), dim3(256), 0, stream, z, row_stats, probs, R, V, status);
 }
 
+// ---------------------------------------------------------------------------
+// admission (one block, one thread per newcomer)
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kScanThreads) admit_kernel(const AdmitParams p) {
+  __shared__ int s_warp[80];
+  __shared__ int s_err;
+  __shared__ int s_need[kScanThreads], s_off[kScanThreads];
+  griddep_launch_dependents();
+  griddep_wait();
+  if (read_status(p.status) != 0) return;
+  const sdv_admission& a = p.a;
+  const int t = threadIdx.x;
+  if (t == 0) s_err = 0;
+  __syncthreads();
+  if (t == 0 && a.num_live && *a.num_live != a.live) atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+  const bool mine = t < a.n;
+  int ctx = 0, need = 0;
+  if (mine) {
+    ctx = a.ctx_lens[t];
+    if (ctx < 0) atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+    need = (ctx + p.gamma_max + 1 + p.page - 1) / p.page;
+    if (need > a.max_pages_per_seq) atomicCAS(&s_err, 0, SDV_ERR_CAPACITY);
+  }
+  int total;
+  const int off = block_exscan(mine ? need : 0, &total, s_warp);
+  const int top = *a.num_free;
+  if (t == 0 && (total > top || top < 0)) atomicCAS(&s_err, 0, SDV_ERR_CAPACITY);
+  if (mine) {
+    s_need[t] = need;
+    s_off[t] = off;
+  }
+  __syncthreads();
+  if (s_err) {
+    if (t == 0) set_status(p.status, s_err);
+    return;
+  }
+  if (a.gen_limits_prev && a.next_src)
+    for (int j = t; j < a.live; j += blockDim.x) a.gen_limits[j] = a.gen_limits_prev[a.next_src[j]];
+  if (mine) {
+    const int slot = a.live + t;
+    a.seq_lens[slot] = ctx;
+    a.num_pages[slot] = need;
+    a.gen_counts[slot] = 0;
+    a.gen_limits[slot] = a.out_lens[t];
+  }
+  // page-table rows of the newcomers, all threads over all entries
+  const long long n = (long long)a.n * a.max_pages_per_seq;
+  for (long long idx = t; idx < n; idx += blockDim.x) {
+    const int j = static_cast<int>(idx / a.max_pages_per_seq);
+    const int k = static_cast<int>(idx - (long long)j * a.max_pages_per_seq);
+    a.page_table[(long long)(a.live + j) * a.max_pages_per_seq + k] =
+        k < s_need[j] ? a.free_pages[top - 1 - (s_off[j] + k)] : -1;
+  }
+  __syncthreads();  // every pop read the old top before the height moves
+  if (t == 0) *a.num_free = top - total;
+}
+
+cudaError_t launch_admit(const AdmitParams& p, cudaStream_t stream) {
+  return launch_pdl(admit_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
+}
+
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream) {
   return launch_pdl(realign_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
 }

@@ -21,10 +21,14 @@ def lib():
     return _abi.load_library()
 
 
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
+
+
 def test_library_exports_every_declared_symbol(lib):
     from speculative_decoding_verify_ragged_gb300 import _abi
-    names = _abi.header_symbols(HEADER)
-    assert len(names) >= 10
+    names = sorted({n for h in HEADERS for n in _abi.header_symbols(h)})
+    assert len(names) >= 20 and "sdv_admit" in names and "sdv_sched_plan" in names
     out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     missing = [n for n in names if n not in exported]
@@ -36,11 +40,14 @@ def test_library_exports_every_declared_symbol(lib):
 PROBE = r"""
 #include <stdio.h>
 #include <stddef.h>
-#include "sdv.h"
+#include "sdv_sched.h"
 #define F(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
 int main(void) {
   printf("sdv_config %zu\nsdv_weights %zu\nsdv_batch %zu\nsdv_result %zu\n",
          sizeof(sdv_config), sizeof(sdv_weights), sizeof(sdv_batch), sizeof(sdv_result));
+  printf("sdv_admission %zu\nsdv_sched_config %zu\nsdv_sched_step %zu\nsdv_sched_stats %zu\n",
+         sizeof(sdv_admission), sizeof(sdv_sched_config), sizeof(sdv_sched_step), sizeof(sdv_sched_stats));
+  F(sdv_admission, max_pages_per_seq) F(sdv_admission, num_free) F(sdv_sched_stats, live)
   F(sdv_config, rope_theta) F(sdv_weights, g_final) F(sdv_batch, num_pool_pages)
   F(sdv_batch, max_pages_per_seq) F(sdv_batch, gen_limits) F(sdv_result, logits) F(sdv_result, status)
   return 0;
@@ -67,6 +74,13 @@ def test_ctypes_layout_matches_header(tmp_path):
     assert int(vals["sdv_batch.gen_limits"]) == _abi.SdvBatch.gen_limits.offset
     assert int(vals["sdv_result.logits"]) == _abi.SdvResult.logits.offset
     assert int(vals["sdv_result.status"]) == _abi.SdvResult.status.offset
+    assert int(vals["sdv_admission"]) == ctypes.sizeof(_abi.SdvAdmission)
+    assert int(vals["sdv_sched_config"]) == ctypes.sizeof(_abi.SdvSchedConfig)
+    assert int(vals["sdv_sched_step"]) == ctypes.sizeof(_abi.SdvSchedStep)
+    assert int(vals["sdv_sched_stats"]) == ctypes.sizeof(_abi.SdvSchedStats)
+    assert int(vals["sdv_admission.max_pages_per_seq"]) == _abi.SdvAdmission.max_pages_per_seq.offset
+    assert int(vals["sdv_admission.num_free"]) == _abi.SdvAdmission.num_free.offset
+    assert int(vals["sdv_sched_stats.live"]) == _abi.SdvSchedStats.live.offset
 
 
 def test_host_errors_without_device(lib):
@@ -85,6 +99,7 @@ def test_host_errors_without_device(lib):
     assert lib.sdv_attention(None, None, None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_read_status(None, None, None) == _abi.SDV_ERR_INVALID_ARG
     assert lib.sdv_set_gemm_path(None, 0) == _abi.SDV_ERR_INVALID_ARG
+    assert lib.sdv_admit(None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     bad = _abi.SdvConfig(256, 4, 3, 64, 768, 1024, 16, 3, 0, 1e-6, 1e6)     # n_q not a multiple of n_kv
     assert lib.sdv_workspace_size(ctypes.byref(bad), 8, 2) == 0
 

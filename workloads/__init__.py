@@ -402,3 +402,13 @@ def workload5_shape(workload: int = 5, B: int = 128):
     limits = loguniform_lengths(g, B)
     gam = np.full(B, swarm_gamma(B), dtype=np.int32)
     return lens, gam, alphas, limits
+
+
+def swarm_requests(n: int, workload: int = 5, ctx=(1024, 16384), outs=(40, 900)):
+    """The swarm's arrival queue: n sequences with context U{ctx}, output length
+    log-uniform in outs, and a target acceptance from ALPHA_MIX (recipe only)."""
+    g = rng(workload, S_SEQ, 7)
+    lens = g.integers(ctx[0], ctx[1] + 1, size=n).astype(np.int32)
+    limits = loguniform_lengths(g, n, *outs)
+    alphas = np.array(ALPHA_MIX)[g.integers(0, 3, size=n)]
+    return lens, limits, alphas

@@ -98,3 +98,25 @@ def draft_probs_device(G: int, V: int, key: int, sigma: float = 2.0) -> torch.Te
         return torch.zeros((0, V), dtype=torch.float32, device="cuda")
     z = torch.randn((G, V), generator=_generator(key), device="cuda", dtype=torch.float32)
     return torch.softmax(z * sigma, dim=1)
+
+
+def retarget_draft_probs_device(q: torch.Tensor, probs: torch.Tensor, tokens: torch.Tensor, gamma: int,
+                                alphas: torch.Tensor) -> None:
+    """Device form of the input recipe of ``retarget_draft_probs`` for a batch in
+    which every slot drafts ``gamma`` tokens: q_i(x_{i+1}) = p_i(x_{i+1}) / alpha_b,
+    the rest of q_i rescaled to sum to one, so every draft is accepted with
+    probability alpha_b.  q [B*gamma, V] is rewritten in place; probs [B*(gamma+1), V]
+    are the target's probabilities from a prepass; alphas [B] float64."""
+    if gamma == 0 or q.shape[0] == 0:
+        return
+    B = alphas.shape[0]
+    b = torch.arange(B, device=q.device).repeat_interleave(gamma)
+    i = torch.arange(gamma, device=q.device).repeat(B)
+    r = b * (gamma + 1) + i
+    x = tokens[r + 1].long()
+    g = torch.arange(B * gamma, device=q.device)
+    target = probs[r, x].double() / alphas.to(q.device)[b]
+    qx = q[g, x].double()
+    scale = ((1.0 - target) / (1.0 - qx)).float()
+    q.mul_(scale[:, None])
+    q[g, x] = target.float()
