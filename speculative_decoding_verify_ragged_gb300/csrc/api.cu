@@ -436,12 +436,14 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
                             const CUtensorMap* xmaps, GemmParams g, cudaStream_t s,
                             const CUtensorMap* s0 = nullptr, const CUtensorMap* s1 = nullptr) {
   if (s0) {
-    const int nt = gemm_q4_tile_rows(g.R);
+    const bool tcq = use_tc(c, g.R) && xp == 2;
+    const int nt = tcq ? gemm_tc_q4_tile_rows(g.R) : gemm_q4_tile_rows(g.R);
     g.kb = g.K / 256;
     g.int4 = 1;
     g.n_tiles = (g.R + nt - 1) / nt;
     const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
     const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
+    if (tcq) return launch_gemm_tc_q4(epi, nt, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
     return launch_gemm_q4(epi, nt, xp, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
   }
   const bool tc = use_tc(c, g.R);

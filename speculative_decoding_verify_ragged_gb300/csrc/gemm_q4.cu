@@ -28,10 +28,6 @@ namespace {
 using namespace gemm;
 constexpr int CONSUMERS = 4;
 constexpr int THREADS = (CONSUMERS + 1) * kWarp;
-constexpr int QK = 256;                   // k per stage
-constexpr int Q_CODE_BYTES = BM * QK / 2; // 16 KB of packed codes
-constexpr int Q_SCALE_BYTES = BM * (QK / 32) * 2;  // 2 KB of scales
-constexpr int Q_A_BYTES = Q_CODE_BYTES + Q_SCALE_BYTES;
 
 template <int NT, int XP>
 struct QCfg {
@@ -48,23 +44,6 @@ struct QCfg {
   static_assert(STAGES >= 2, "pipeline too shallow");
   static_assert(SMEM <= kSmemBudget, "shared memory");
 };
-
-// Four code bytes (eight int4 codes, low nibble first) -> four bf16 pairs.
-__device__ __forceinline__ void codes_to_bf16(uint32_t x, uint32_t (&r)[4]) {
-  const uint32_t v = x ^ 0x88888888u;  // code + 8 in each nibble: 0..15
-  const uint32_t lo = v & 0x0F0F0F0Fu;
-  const uint32_t hi = (v >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    // byte 0: low nibble of byte j; byte 2: its high nibble; 0x43 above each
-    const uint32_t sel = j | (j << 4) | ((4 + j) << 8) | ((4 + j) << 12);
-    const uint32_t m = (__byte_perm(lo, hi, sel) & 0x00FF00FFu) | 0x43004300u;  // bf16 (128 + code + 8)
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&m);
-    const uint32_t k136 = 0x43084308u;  // bf16 136 in both halves
-    b = __hsub2(b, *reinterpret_cast<const __nv_bfloat162*>(&k136));  // exact: code in [-8, 7]
-    r[j] = *reinterpret_cast<uint32_t*>(&b);
-  }
-}
 
 template <int EPI, int NT, int XP>
 __global__ void __launch_bounds__(THREADS, 1)

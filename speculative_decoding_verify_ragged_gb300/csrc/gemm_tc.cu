@@ -20,12 +20,14 @@
 //    then the stream-K partial/fixup and the fused epilogue shared with the
 //    mma.sync kernel, while the MMAs fill the other accumulator.
 #include "gemm_common.cuh"
+#include "tcgen05.cuh"
 
 namespace sdv {
 
 namespace {
 
 using namespace gemm;
+using namespace tc;
 constexpr int TC_THREADS = 6 * kWarp;
 constexpr int EC = 16;  // accumulator columns per tcgen05.ld / epilogue chunk
 
@@ -44,61 +46,6 @@ struct TcCfg {
   static_assert(SMEM <= kSmemBudget, "shared memory");
   static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "tcgen05 N for M = 128");
 };
-
-// ---- tcgen05 wrappers -------------------------------------------------------
-
-// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle atoms of
-// 8 rows x 128 bytes (the layout a 64-wide bf16 TMA box with SWIZZLE_128B
-// writes); stride between 8-row groups 1024 bytes; descriptor version 1.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused for swizzled K-major)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;                  // version
-  d |= static_cast<uint64_t>(2) << 61;                  // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n"
-      " .reg .pred p;\n"
-      " setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 16 consecutive 32-bit columns, one lane per thread of the warp.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 template <int EPI, int NT, int XP>
 __global__ void __launch_bounds__(TC_THREADS, 1)

@@ -86,6 +86,11 @@ cudaError_t launch_gemm_q4(int epi, int nt, int xp, const CUtensorMap* q0, const
                            const CUtensorMap* s0, const CUtensorMap* s1, const CUtensorMap* x, const GemmParams& p,
                            int grid, cudaStream_t stream);
 // The same GEMM on tcgen05 / TMEM (nt in {16, 32, 64, 128, 256}).
+int gemm_tc_q4_tile_rows(int R);
+// int4 group-32 weights on tcgen05 (activations always as bf16 hi + lo planes)
+cudaError_t launch_gemm_tc_q4(int epi, int nt, const CUtensorMap* q0, const CUtensorMap* q1, const CUtensorMap* s0,
+                              const CUtensorMap* s1, const CUtensorMap* x, const GemmParams& p, int grid,
+                              cudaStream_t stream);
 int gemm_tc_tile_rows(int R);
 cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                            const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);

@@ -108,3 +108,27 @@ def test_step_nine_b_int4(nine_b_int4):
     batch = wl.make_batch(wl.NINE_B, 5, seq_lens=lens, draft_lens=gam, gamma_max=3,
                           alphas=[0.97, 0.8, 0.14, 0.8, 0.97, 0.14], extra_pages=12)
     _full_step_check(eng, W, _retargeted(batch, W, 5), "nine-b-int4")
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("rows", [16, 40, 128, 300])
+@pytest.mark.parametrize("which", [0, 2, 4])
+def test_linear_int4_nine_b_both_kernels(nine_b_int4, rows, which, path):
+    """9B-class int4 projections through the mma.sync (path 1) and tcgen05 (path 2)
+    kernels, fp32 activations, on sampled output columns (all rows)."""
+    import torch
+    W, Wd = nine_b_int4
+    eng = gh.engine_for(wl.NINE_B, 3, Wd, max_rows=320, max_slots=16, fmt="int4")
+    eng.set_gemm_path(path)
+    w = W.proj[NAMES[which]]
+    N, K = w[0].shape[0], w[0].shape[1] * 2
+    x32 = np.random.default_rng(7000 + rows + which).standard_normal((rows, K)).astype(np.float32)
+    y = torch.empty((rows, N), dtype=torch.float32, device="cuda")
+    eng.linear(which, torch.from_numpy(x32).cuda(), y)
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(rows * 7 + which).choice(N, size=48, replace=False)
+    wf = o.dequant_int4_g32(w[0][cols], w[1][cols])
+    ref = x32.astype(np.float64) @ wf.T
+    got = y.cpu().numpy()[:, cols]
+    scale = np.sqrt((x32.astype(np.float64) ** 2).sum(1)).max() * np.abs(wf).max()
+    assert np.abs(got - ref).max() <= 3e-5 * scale
