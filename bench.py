@@ -403,12 +403,23 @@ def run_sweep(args):
     W = wl.make_weights(wl.NINE_B, 4)
     Wd = wd.weights_to_device(W)
     del W
-    eng = VerifyEngine(wd.config(wl.NINE_B, 8), Wd, max_rows=max_rows, max_slots=max_slots)
-    eng.set_gemm_path(args.gemm_path)
+    engines = {}
+
+    def engine_for(g):
+        # one context per draft length: gamma_max sizes the attention's query tile
+        gm = max(1, g)
+        if gm not in engines:
+            engines.clear()
+            torch.cuda.empty_cache()
+            e = VerifyEngine(wd.config(wl.NINE_B, gm), Wd, max_rows=max_rows, max_slots=max_slots)
+            e.set_gemm_path(args.gemm_path)
+            engines[gm] = e
+        return engines[gm]
     hbm, tflops, peak_kind = measured_peaks()
     stream = torch.cuda.current_stream()
     results = []
     for B, g in points:
+        eng = engine_for(g)
         batch = wl.workload4(B, g, kv_fill="lazy", extra_pages=4 * B + 8)
         bd = wd.batch_to_device(batch)
         # the KV pool: bf16 N(0,1) drawn on the device (seeded), the same recipe as the host fill

@@ -276,6 +276,13 @@ sdv_status sdv_set_phase_events(sdv_ctx *ctx, void *const *events, int n);
 enum { SDV_GEMM_AUTO = 0, SDV_GEMM_MMA_SYNC = 1, SDV_GEMM_TCGEN05 = 2 };
 sdv_status sdv_set_gemm_path(sdv_ctx *ctx, int path);
 
+/* Which kernel runs the step's attention: SDV_GEMM_AUTO (tcgen05 when
+ * head_dim is 128 and (gamma_max + 1) * n_q / n_kv <= 32, else mma.sync),
+ * SDV_GEMM_MMA_SYNC, or SDV_GEMM_TCGEN05 (SDV_ERR_UNSUPPORTED from the step
+ * and sdv_attention when the shape does not fit it).  Results agree up to
+ * fp32 summation order.  Host-side setting; takes effect on the next call. */
+sdv_status sdv_set_attention_path(sdv_ctx *ctx, int path);
+
 /* Synchronise `stream` and copy the device status word to *host_status. */
 sdv_status sdv_read_status(const int *status, int *host_status, void *stream);
 

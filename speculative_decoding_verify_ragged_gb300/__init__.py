@@ -166,6 +166,10 @@ class VerifyEngine:
         """0 auto (by row count), 1 bf16 mma.sync, 2 tcgen05 with TMEM accumulators."""
         self._check(self.lib.sdv_set_gemm_path(self.handle, int(path)), "sdv_set_gemm_path")
 
+    def set_attention_path(self, path: int):
+        """0 auto, 1 mma.sync, 2 tcgen05 (head_dim 128, <= 32 query vectors per item)."""
+        self._check(self.lib.sdv_set_attention_path(self.handle, int(path)), "sdv_set_attention_path")
+
     def set_phase_events(self, events):
         """Record torch.cuda.Event objects at the step's phase boundaries (None = off).
 

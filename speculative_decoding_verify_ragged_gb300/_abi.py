@@ -125,6 +125,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_attention.argtypes = [c_void_p, c_void_p, P(SdvBatch), c_void_p, c_void_p, c_void_p]
     lib.sdv_set_gemm_path.restype = c_int
     lib.sdv_set_gemm_path.argtypes = [c_void_p, c_int]
+    lib.sdv_set_attention_path.restype = c_int
+    lib.sdv_set_attention_path.argtypes = [c_void_p, c_int]
     lib.sdv_set_phase_events.restype = c_int
     lib.sdv_set_phase_events.argtypes = [c_void_p, P(c_void_p), c_int]
     lib.sdv_read_status.restype = c_int

@@ -232,6 +232,7 @@ struct sdv_ctx {
   bool int4;
   CUtensorMap tm_h[6], tm_attn[6], tm_act[6], tm_h3[6];  // activation tiles of 8..256 rows
   int gemm_path;
+  int attn_path;
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -278,6 +279,7 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   c->L = L;
   c->timing = false;
   c->gemm_path = SDV_GEMM_AUTO;
+  c->attn_path = SDV_GEMM_AUTO;
   const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
                  V = cfg->vocab;
   const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
@@ -329,6 +331,12 @@ void sdv_destroy(sdv_ctx* ctx) { delete ctx; }
 sdv_status sdv_set_gemm_path(sdv_ctx* ctx, int path) {
   if (!ctx || path < SDV_GEMM_AUTO || path > SDV_GEMM_TCGEN05) return SDV_ERR_INVALID_ARG;
   ctx->gemm_path = path;
+  return SDV_OK;
+}
+
+sdv_status sdv_set_attention_path(sdv_ctx* ctx, int path) {
+  if (!ctx || path < SDV_GEMM_AUTO || path > SDV_GEMM_TCGEN05) return SDV_ERR_INVALID_ARG;
+  ctx->attn_path = path;
   return SDV_OK;
 }
 
@@ -480,6 +488,15 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   a.n_kv = c->cfg.n_kv;
   a.page = c->cfg.page_size;
   const int grid = c->sms;  // one CTA per SM (the ring and the combine buffer take most of shared memory)
+  // tcgen05 kernel: head_dim 128 and at most 32 query vectors per (sequence, KV head)
+  const int nqv_max = (c->cfg.gamma_max + 1) * (c->cfg.n_q / c->cfg.n_kv);
+  const bool tc = c->attn_path != SDV_GEMM_MMA_SYNC && c->cfg.head_dim == 128 && nqv_max <= 32;
+  if (c->attn_path == SDV_GEMM_TCGEN05 && !tc) return SDV_ERR_UNSUPPORTED;
+  if (tc) {
+    SDV_CUDA(launch_attention_tc(nqv_max <= 16 ? 16 : 32, &kv, a, grid, s));
+    SDV_CUDA(launch_attention_merge(c->cfg.head_dim, a, b->R, s, ws_ptr<int>(c, c->L.row_seq)));
+    return SDV_OK;
+  }
   SDV_CUDA(launch_attention_impl(c->cfg.head_dim, &kv, a, grid, b->R, s, ws_ptr<int>(c, c->L.row_seq)));
   return SDV_OK;
 }

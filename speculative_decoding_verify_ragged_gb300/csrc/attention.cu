@@ -483,6 +483,14 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
 
 size_t attention_smem_bytes(int head_dim) { return head_dim == 64 ? ACfg<64>::SMEM : ACfg<128>::SMEM; }
 
+cudaError_t launch_attention_merge(int head_dim, const AttnParams& p, int R, cudaStream_t stream, const int* row_seq) {
+  const long long n = (long long)R * p.n_q * head_dim;
+  const dim3 grid(static_cast<unsigned>((n + 255) / 256));
+  if (head_dim == 128) return launch_pdl(attn_merge_kernel<128>, grid, dim3(256), 0, stream, p, row_seq, R);
+  if (head_dim == 64) return launch_pdl(attn_merge_kernel<64>, grid, dim3(256), 0, stream, p, row_seq, R);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_attention_impl(int head_dim, const CUtensorMap* kv_map, const AttnParams& p, int grid, int R,
                                   cudaStream_t stream, const int* row_seq) {
   if (head_dim == 128) return launch_d<128>(kv_map, p, grid, R, stream, row_seq);

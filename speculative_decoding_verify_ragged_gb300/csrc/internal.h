@@ -122,6 +122,10 @@ struct AttnParams {
 };
 constexpr int kAttnQMax = 48;  // query vectors per (slot, kv head): (gamma+1) * group
 
+// The tcgen05 attention kernel (head_dim 128, nq = 16 or 32 query vectors per
+// item); split sequences still need launch_attention_merge afterwards.
+cudaError_t launch_attention_tc(int nq, const CUtensorMap* kv_map, const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attention_merge(int head_dim, const AttnParams& p, int R, cudaStream_t stream, const int* row_seq);
 // Attention kernel plus the merge of split sequences (row_seq [R] maps rows to slots).
 cudaError_t launch_attention_impl(int head_dim, const CUtensorMap* kv_map, const AttnParams& p, int grid, int R,
                                   cudaStream_t stream, const int* row_seq);

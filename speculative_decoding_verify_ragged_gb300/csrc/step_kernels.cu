@@ -129,7 +129,7 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   // attention schedule: chunks of pages sized so that items cover the GPU
   const long long units = (long long)tot_pages * p.n_kv;
   int chunk = static_cast<int>((units + p.target_items - 1) / p.target_items);
-  chunk = max(chunk, 8);
+  chunk = (max(chunk, 8) + 7) & ~7;  // whole 128-key blocks
   const int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
   int tot_items;
   const int ioff = block_exscan(chunks_b * p.n_kv, &tot_items, s_warp);

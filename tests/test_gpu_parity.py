@@ -124,9 +124,17 @@ def _attention_ref(dims, b, q):
     (wl.TINY, [300, 16, 15, 1000], [3, 3, 3, 0], 3),
     (wl.NINE_B, [2048], [7], 7),
     (wl.NINE_B, [513, 8000, 1, 4096, 77, 2047, 12000, 640], [3, 1, 2, 0, 3, 2, 1, 3], 3),
+    (wl.NINE_B, [16000, 0, 15, 16, 17, 127, 128, 129], [3, 0, 3, 1, 2, 3, 0, 1], 3),
+    (wl.NINE_B, [int(x) for x in np.random.default_rng(77).integers(0, 3000, size=40)],
+     [int(x) for x in np.random.default_rng(78).integers(0, 4, size=40)], 3),
 ])
-def test_attention_matches_oracle(torch_cuda, case):
+@pytest.mark.parametrize("path", [1, 2])
+def test_attention_matches_oracle(torch_cuda, case, path):
+    """Both attention kernels (1: mma.sync, 2: tcgen05 for head_dim 128) against
+    the float64 definition, over ragged lengths, split sequences and partial blocks."""
     dims, lens, gams, gmax = case
+    if path == 2 and dims["head_dim"] != 128:
+        pytest.skip("the tcgen05 kernel serves head_dim 128")
     torch = torch_cuda
     from workloads import device as wd
     W = wl.make_weights(wl.TINY, 1) if dims is wl.TINY else None
@@ -138,6 +146,7 @@ def test_attention_matches_oracle(torch_cuda, case):
         eng = VerifyEngine(cfg, Wsmall, max_rows=64, max_slots=16)
     else:
         eng = _attn_only_engine(cfg, torch)
+    eng.set_attention_path(path)
     b, q, bd, qd, out, st = _attention_case(dims, lens, gams, gmax, 40 + len(lens), torch)
     eng.attention(qd, bd, out, st)
     assert eng.read_status(st) == 0
@@ -161,7 +170,7 @@ def _attn_only_engine(cfg, torch):
     z = lambda *s: torch.zeros(*s, dtype=torch.bfloat16, device="cuda")  # noqa: E731
     Wd = dict(emb=z(8, H), w_qkv=z(nqkv, H), w_o=z(H, qd), w_gate=z(F, H), w_up=z(F, H), w_down=z(H, F),
               w_lm=z(V, H), g_attn=z(H), g_ffn=z(H), g_final=z(H))
-    return VerifyEngine(cfg, Wd, max_rows=64, max_slots=16)
+    return VerifyEngine(cfg, Wd, max_rows=192, max_slots=48)
 
 
 # ---------------------------------------------------------------------------
