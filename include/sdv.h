@@ -277,7 +277,8 @@ enum { SDV_GEMM_AUTO = 0, SDV_GEMM_MMA_SYNC = 1, SDV_GEMM_TCGEN05 = 2 };
 sdv_status sdv_set_gemm_path(sdv_ctx *ctx, int path);
 
 /* Which kernel runs the step's attention: SDV_GEMM_AUTO (tcgen05 when
- * head_dim is 128 and (gamma_max + 1) * n_q / n_kv <= 32, else mma.sync),
+ * head_dim is 128, (gamma_max + 1) * n_q / n_kv <= 32 and the batch has at
+ * least 4 sequences, else mma.sync),
  * SDV_GEMM_MMA_SYNC, or SDV_GEMM_TCGEN05 (SDV_ERR_UNSUPPORTED from the step
  * and sdv_attention when the shape does not fit it).  Results agree up to
  * fp32 summation order.  Host-side setting; takes effect on the next call. */

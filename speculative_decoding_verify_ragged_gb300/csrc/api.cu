@@ -433,6 +433,9 @@ static const CUtensorMap* q4(const sdv_ctx* c, const CUtensorMap& scales) { retu
 // SDV_GEMM_AUTO mode (below it the mma.sync kernel's 8-row tiles waste less).
 constexpr int kTcRows = 17;
 
+// Slots at and above which auto mode runs attention on tcgen05.
+constexpr int kTcAttnSlots = 4;
+
 static bool use_tc(const sdv_ctx* c, int R) {
   return c->gemm_path == SDV_GEMM_TCGEN05 || (c->gemm_path == SDV_GEMM_AUTO && R >= kTcRows);
 }
@@ -490,8 +493,12 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   const int grid = c->sms;  // one CTA per SM (the ring and the combine buffer take most of shared memory)
   // tcgen05 kernel: head_dim 128 and at most 32 query vectors per (sequence, KV head)
   const int nqv_max = (c->cfg.gamma_max + 1) * (c->cfg.n_q / c->cfg.n_kv);
-  const bool tc = c->attn_path != SDV_GEMM_MMA_SYNC && c->cfg.head_dim == 128 && nqv_max <= 32;
-  if (c->attn_path == SDV_GEMM_TCGEN05 && !tc) return SDV_ERR_UNSUPPORTED;
+  const bool fits = c->cfg.head_dim == 128 && nqv_max <= 32;
+  if (c->attn_path == SDV_GEMM_TCGEN05 && !fits) return SDV_ERR_UNSUPPORTED;
+  // in auto mode a batch of fewer than kTcAttnSlots sequences keeps the
+  // mma.sync kernel: too little KV per CTA to hide the tcgen05 pipeline's fill
+  const bool tc = fits && (c->attn_path == SDV_GEMM_TCGEN05 ||
+                           (c->attn_path == SDV_GEMM_AUTO && b->B >= kTcAttnSlots));
   if (tc) {
     SDV_CUDA(launch_attention_tc(nqv_max <= 16 ? 16 : 32, &kv, a, grid, s));
     SDV_CUDA(launch_attention_merge(c->cfg.head_dim, a, b->R, s, ws_ptr<int>(c, c->L.row_seq)));

@@ -110,15 +110,27 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
     p.t.draft_off[p.B] = tot_g;
   }
   // every page a row reads or writes must be a pool page: one flat loop over
-  // all (slot, page) pairs, the slot found by binary search over s_poff
-  for (int idx = threadIdx.x; idx < tot_pages; idx += blockDim.x) {
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_poff[mid] <= idx) lo = mid; else hi = mid - 1;
+  // all (slot, page) pairs, the slot found by binary search over s_poff; eight
+  // loads per thread in flight at a time
+  constexpr int kUnroll = 8;
+  for (int base = threadIdx.x; base < tot_pages; base += blockDim.x * kUnroll) {
+    int pg[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int idx = base + u * blockDim.x;
+      pg[u] = 0;
+      if (idx < tot_pages) {
+        int lo = 0, hi = p.B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_poff[mid] <= idx) lo = mid; else hi = mid - 1;
+        }
+        pg[u] = p.page_table[(long long)lo * p.max_pages + (idx - s_poff[lo])];
+      }
     }
-    const int pg = p.page_table[(long long)lo * p.max_pages + (idx - s_poff[lo])];
-    if (pg < 0 || pg >= p.pool_pages) atomicCAS(&s_err, 0, SDV_ERR_PAGE_RANGE);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (pg[u] < 0 || pg[u] >= p.pool_pages) atomicCAS(&s_err, 0, SDV_ERR_PAGE_RANGE);
   }
   if (p.check_tokens) {
     for (int r = threadIdx.x; r < p.R; r += blockDim.x) {
@@ -322,15 +334,23 @@ struct PSource {
   int V;
   __device__ __forceinline__ float p(int row, int j, float M, float S) const {
     if constexpr (FROM_LOGITS) {
-      return expf(base[(long long)row * V + j] - M) / S;
+      return expf(base[(long long)row * V + j] - M) * S;  // S: the reciprocal of the row's sum
     } else {
       return base[(long long)row * V + j];
     }
   }
 };
 
+// floor(w * 2^32) for w in [0, 2), from the bits: w = m * 2^(e - 150) with the
+// 24-bit significand m, so w * 2^32 = m * 2^(e - 118); the same value as the
+// truncating float -> uint64 conversion, in integer shifts.
 __device__ __forceinline__ unsigned long long fixed_weight(float w) {
-  return static_cast<unsigned long long>(w * 4294967296.0f);
+  const uint32_t bits = __float_as_uint(w);
+  const int e = static_cast<int>((bits >> 23) & 0xFFu);
+  if (e == 0 || (bits >> 31)) return 0ull;  // zero, subnormal (< 2^-126) or negative
+  const unsigned long long m = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 118;
+  return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
 }
 
 // First row of slot b: the sum of (gamma + 1) over the earlier slots, from the
@@ -440,7 +460,7 @@ __device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M
   float pj[4] = {v.x, v.y, v.z, v.w};
   if constexpr (FROM_LOGITS) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pj[e] = expf(pj[e] - M) / S;
+    for (int e = 0; e < 4; ++e) pj[e] = expf(pj[e] - M) * S;  // S: the reciprocal of the row's sum
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) sp += fixed_weight(pj[e]);
@@ -476,7 +496,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   if constexpr (FROM_LOGITS) {
     const float2 st = p.row_stats[rf];
     M = st.x;
-    S = st.y;
+    S = 1.f / st.y;  // weights as exp(z - M) times the reciprocal of the sum
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
 
@@ -681,6 +701,7 @@ __global__ void probs_kernel(const float* z, const float2* row_stats, float* pro
 __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignParams p) {
   __shared__ int s_warp[80];
   __shared__ int s_err;
+  __shared__ int s_need[kScanThreads], s_src[kScanThreads];
   griddep_launch_dependents();
   griddep_wait();
   if (read_status(p.res.status) != 0) return;
@@ -764,7 +785,9 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   if (b == 0) *p.num_free_out = top + tot_s - tot_d;
 
   // stable compaction of the surviving slots
+  if (slot) s_need[b] = need;
   if (slot && !fin) {
+    s_src[loff] = b;
     if (res.next_src) res.next_src[loff] = b;
     if (res.next_seq_lens) res.next_seq_lens[loff] = newlen;
     if (res.next_num_pages) res.next_num_pages[loff] = need;
@@ -772,12 +795,29 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   }
   if (b == 0 && res.num_live) *res.num_live = tot_live;
   __syncthreads();
-  if (res.next_page_table && res.next_src) {
+  if (res.next_page_table) {
+    // a survivor's row holds its `need` pages, then -1 (the trim above cleared
+    // the rest), so only the first `need` entries are read; eight in flight
+    constexpr int kUnroll = 8;
     const long long n = (long long)tot_live * p.max_pages;
-    for (long long idx = threadIdx.x; idx < n; idx += blockDim.x) {
-      const int dst = static_cast<int>(idx / p.max_pages);
-      const int col = static_cast<int>(idx - (long long)dst * p.max_pages);
-      res.next_page_table[idx] = p.page_table[(long long)res.next_src[dst] * p.max_pages + col];
+    for (long long base = threadIdx.x; base < n; base += (long long)blockDim.x * kUnroll) {
+      int v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long idx = base + (long long)u * blockDim.x;
+        v[u] = -1;
+        if (idx < n) {
+          const int dst = static_cast<int>(idx / p.max_pages);
+          const int col = static_cast<int>(idx - (long long)dst * p.max_pages);
+          const int src = s_src[dst];
+          if (col < s_need[src]) v[u] = p.page_table[(long long)src * p.max_pages + col];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long idx = base + (long long)u * blockDim.x;
+        if (idx < n) res.next_page_table[idx] = v[u];
+      }
     }
   }
 }
