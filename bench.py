@@ -509,10 +509,15 @@ def run_sweep(args):
     # the weights' bytes against the flops per row they carry (2 per weight)
     w_bytes = 2 * (48 * 128 * 4096 + 4096 * 4096 + 3 * 12288 * 4096 + 151936 * 4096)
     model = (w_bytes / (hbm * 1e9)) / (w_bytes / (tflops * 1e12))
+    # the pages' step model fitted to these steps (ms): B*, best gamma per B, break-even
+    from speculative_decoding_verify_ragged_gb300 import roofline as rf
+    fitted = rf.fit_regimes([(pt["B"], pt["gamma"] + 1, pt["ms_per_step"]) for pt in results]) \
+        if len(results) >= 3 else None
     print(json.dumps({"sweep": "crossover-summary", "points": len(results), "measured_crossover_rows": cross,
                       "model_crossover_rows": model, "peaks": {"hbm_GBps": hbm, "bf16_TFLOPs": tflops,
                                                                "kind": peak_kind},
-                      "gemm_path": args.gemm_path}), flush=True)
+                      "step_model_ms": rf.report(fitted) if fitted else None,
+                      "gemm_path": args.gemm_path}, default=str), flush=True)
 
 
 # ---------------------------------------------------------------------------
