@@ -276,6 +276,22 @@ sdv_status sdv_set_phase_events(sdv_ctx *ctx, void *const *events, int n);
 enum { SDV_GEMM_AUTO = 0, SDV_GEMM_MMA_SYNC = 1, SDV_GEMM_TCGEN05 = 2 };
 sdv_status sdv_set_gemm_path(sdv_ctx *ctx, int path);
 
+/* How the step verifies drafts and draws the final token.
+ * SDV_SAMPLING_STOCHASTIC (default): rejection sampling against the draft
+ *   distributions -- keep draft i+1 iff u < min(1, p/q), then draw from the
+ *   residual max(0, p - q) or, with every draft kept, from p ("Speculative
+ *   Decoding at High Batch Size", FAQ "Does speculative decoding change the
+ *   output of the model?"; splicedso primer, section "The idea").
+ * SDV_SAMPLING_GREEDY: the temperature -> 0 case, the usual pairing with
+ *   copy-style (n-gram) drafts (splicedso primer, section "When it works"):
+ *   keep draft i+1 iff it is the argmax of p at row i (smallest index among
+ *   equal maxima), then emit the argmax of the first row not kept.  The output
+ *   is then exactly what greedy decoding of the target produces.  draft_probs
+ *   and uniforms are not read (may be NULL).
+ * Applies to sdv_verify_step and sdv_accept on this context. */
+enum { SDV_SAMPLING_STOCHASTIC = 0, SDV_SAMPLING_GREEDY = 1 };
+sdv_status sdv_set_sampling(sdv_ctx *ctx, int mode);
+
 /* Which kernel runs the step's attention: SDV_GEMM_AUTO (tcgen05 when
  * head_dim is 128, (gamma_max + 1) * n_q / n_kv <= 32 and the batch has at
  * least 4 sequences, else mma.sync),

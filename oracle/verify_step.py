@@ -394,12 +394,29 @@ def accept_and_sample(p_rows: np.ndarray, q_rows: np.ndarray, drafts, u: np.ndar
     return a, t
 
 
-def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens):
+def greedy_accept(rows: np.ndarray, drafts):
+    """Greedy verification of one sequence (temperature -> 0): draft i + 1 is kept
+    iff it is the argmax of row i, the first draft that is not ends the prefix,
+    and the final token is the argmax of the row after the kept prefix (the
+    target's own next token).  Argmax = the smallest index among equal maxima.
+    rows: [gamma + 1, V] (probabilities or logits: the same argmax).
+    """
+    gamma = len(drafts)
+    a = gamma
+    for i in range(gamma):
+        if int(drafts[i]) != int(np.argmax(rows[i])):
+            a = i
+            break
+    return a, int(np.argmax(rows[a]))
+
+
+def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens, greedy: bool = False):
     """Every sequence of a batch: accepted counts, emitted tokens, emitted offsets.
 
     p float32 [R, V], q float32 [G, V]; emitted tokens of sequence b are its
     accepted drafts followed by its final token, packed at
-    offset sum_{j<b}(a_j + 1).
+    offset sum_{j<b}(a_j + 1).  greedy: the argmax rule of greedy_accept
+    (q and uniforms are not read).
     """
     draft_lens = np.asarray(draft_lens)
     B = len(draft_lens)
@@ -411,8 +428,11 @@ def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens):
         g = int(draft_lens[b])
         r0 = int(roff[b])
         drafts = np.asarray(tokens)[r0 + 1: r0 + 1 + g]
-        a, t = accept_and_sample(p[r0: r0 + g + 1], q[int(goff[b]): int(goff[b]) + g],
-                                 drafts, np.asarray(uniforms, dtype=np.float32)[r0: r0 + g + 1])
+        if greedy:
+            a, t = greedy_accept(p[r0: r0 + g + 1], drafts)
+        else:
+            a, t = accept_and_sample(p[r0: r0 + g + 1], q[int(goff[b]): int(goff[b]) + g],
+                                     drafts, np.asarray(uniforms, dtype=np.float32)[r0: r0 + g + 1])
         acc[b] = a
         fin[b] = t
     eoff = np.concatenate([[0], np.cumsum(acc.astype(np.int64) + 1)]).astype(np.int32)
@@ -527,12 +547,13 @@ def realign(seq_lens, accepted, page_table, num_pages, free_pages, num_free: int
 # ---------------------------------------------------------------------------
 
 
-def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=None):
+def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=None, greedy: bool = False):
     """Forward, acceptance, sampling and realignment of one batch.
 
     ``batch`` and ``weights`` are the seeded inputs (workloads.Batch /
     workloads.Weights).  With ``slots`` the forward, acceptance and sampling
-    run for those sequences only (realignment is skipped).
+    run for those sequences only (realignment is skipped).  ``greedy``:
+    greedy verification on the float64 logits (greedy_accept).
     """
     dims = batch.dims
     fw = forward(dims, weights, batch.kv_pool, batch.page_table, batch.seq_lens,
@@ -556,8 +577,8 @@ def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=Non
             n += g + 1
         out["per_slot"] = res
         return out
-    acc, emitted, eoff, fin = accept_batch(p32, batch.draft_probs, batch.tokens,
-                                           batch.uniforms, batch.draft_lens)
+    acc, emitted, eoff, fin = accept_batch(fw["logits"] if greedy else p32, batch.draft_probs, batch.tokens,
+                                           batch.uniforms, batch.draft_lens, greedy=greedy)
     ra = realign(batch.seq_lens, acc, batch.page_table, batch.num_pages, batch.free_pages,
                  batch.num_free, dims["page"], batch.gamma_max,
                  gen_counts=batch.gen_counts, gen_limits=batch.gen_limits)

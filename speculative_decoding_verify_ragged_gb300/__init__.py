@@ -166,6 +166,10 @@ class VerifyEngine:
         """0 auto (by row count), 1 bf16 mma.sync, 2 tcgen05 with TMEM accumulators."""
         self._check(self.lib.sdv_set_gemm_path(self.handle, int(path)), "sdv_set_gemm_path")
 
+    def set_sampling(self, mode: int):
+        """0 stochastic (rejection sampling, default), 1 greedy (argmax tests and final token)."""
+        self._check(self.lib.sdv_set_sampling(self.handle, int(mode)), "sdv_set_sampling")
+
     def set_attention_path(self, path: int):
         """0 auto, 1 mma.sync, 2 tcgen05 (head_dim 128, <= 32 query vectors per item)."""
         self._check(self.lib.sdv_set_attention_path(self.handle, int(path)), "sdv_set_attention_path")

@@ -31,6 +31,7 @@ SDV_OK, SDV_ERR_INVALID_ARG, SDV_ERR_CAPACITY, SDV_ERR_PAGE_RANGE, SDV_ERR_CUDA,
     SDV_ERR_BAD_INPUT, SDV_ERR_UNSUPPORTED, SDV_ERR_INTERNAL = range(9)
 SDV_WEIGHTS_BF16, SDV_WEIGHTS_INT4_G32 = 0, 1
 SDV_GEMM_AUTO, SDV_GEMM_MMA_SYNC, SDV_GEMM_TCGEN05 = 0, 1, 2
+SDV_SAMPLING_STOCHASTIC, SDV_SAMPLING_GREEDY = 0, 1
 PHASES = ("prologue", "qkv", "attention", "o_proj", "ffn", "lm_head", "accept", "realign")
 
 
@@ -125,6 +126,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_attention.argtypes = [c_void_p, c_void_p, P(SdvBatch), c_void_p, c_void_p, c_void_p]
     lib.sdv_set_gemm_path.restype = c_int
     lib.sdv_set_gemm_path.argtypes = [c_void_p, c_int]
+    lib.sdv_set_sampling.restype = c_int
+    lib.sdv_set_sampling.argtypes = [c_void_p, c_int]
     lib.sdv_set_attention_path.restype = c_int
     lib.sdv_set_attention_path.argtypes = [c_void_p, c_int]
     lib.sdv_set_phase_events.restype = c_int
@@ -138,6 +141,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_admit.restype = c_int
     lib.sdv_admit.argtypes = [c_void_p, P(SdvAdmission), c_void_p, c_void_p]
     c_ll = ctypes.c_longlong
+    lib.sdv_ngram_draft.restype = c_int
+    lib.sdv_ngram_draft.argtypes = [P(c_int), c_int, c_int, c_int, c_int, P(c_int)]
+    lib.sdv_ngram_draft_batch.restype = c_int
+    lib.sdv_ngram_draft_batch.argtypes = [P(c_int), P(c_ll), c_int, c_int, c_int, c_int, P(c_int), P(c_int)]
     lib.sdv_sched_gamma.restype = c_int
     lib.sdv_sched_gamma.argtypes = [c_int, c_int, c_int]
     lib.sdv_sched_create.restype = c_int

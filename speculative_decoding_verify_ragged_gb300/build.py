@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdv.so")
-SOURCES = ("api.cu", "gemm.cu", "gemm_tc.cu", "gemm_tc_q4.cu", "gemm_q4.cu", "attention.cu", "attention_tc.cu", "step_kernels.cu", "noalloc.cu", "sched.cpp")
+SOURCES = ("api.cu", "gemm.cu", "gemm_tc.cu", "gemm_tc_q4.cu", "gemm_q4.cu", "attention.cu", "attention_tc.cu", "step_kernels.cu", "noalloc.cu", "sched.cpp", "ngram.cpp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -44,7 +44,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
   size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, items, rope, kv_row_off, inv_freq;
-  size_t x0, h, h3, q, attn, x1, x1sq, act, x2, z, lmstats, rowstats, partials, counters;
+  size_t x0, h, h3, q, attn, x1, x1sq, act, x2, z, lmstats, lmargmax, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, chunk_count, chunk_sums, total;
   int chunk_ld;
   int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
@@ -121,6 +121,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.x2 = take(R * H * 4);
   L.z = take(R * V * 4);
   L.lmstats = take(static_cast<size_t>(L.lm_tiles) * R * 8);
+  L.lmargmax = take(static_cast<size_t>(L.lm_tiles) * R * 4);
   L.rowstats = take(R * 8);
   L.partials = take(static_cast<size_t>(2) * sms * 128 * 256 * 4);  // two pieces per CTA, tiles up to 256 rows
   L.counters = take(static_cast<size_t>(L.max_tiles) * 4);
@@ -233,6 +234,7 @@ struct sdv_ctx {
   CUtensorMap tm_h[6], tm_attn[6], tm_act[6], tm_h3[6];  // activation tiles of 8..256 rows
   int gemm_path;
   int attn_path;
+  int sampling;
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -280,6 +282,7 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   c->timing = false;
   c->gemm_path = SDV_GEMM_AUTO;
   c->attn_path = SDV_GEMM_AUTO;
+  c->sampling = SDV_SAMPLING_STOCHASTIC;
   const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
                  V = cfg->vocab;
   const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
@@ -331,6 +334,12 @@ void sdv_destroy(sdv_ctx* ctx) { delete ctx; }
 sdv_status sdv_set_gemm_path(sdv_ctx* ctx, int path) {
   if (!ctx || path < SDV_GEMM_AUTO || path > SDV_GEMM_TCGEN05) return SDV_ERR_INVALID_ARG;
   ctx->gemm_path = path;
+  return SDV_OK;
+}
+
+sdv_status sdv_set_sampling(sdv_ctx* ctx, int mode) {
+  if (!ctx || (mode != SDV_SAMPLING_STOCHASTIC && mode != SDV_SAMPLING_GREEDY)) return SDV_ERR_INVALID_ARG;
+  ctx->sampling = mode;
   return SDV_OK;
 }
 
@@ -550,7 +559,8 @@ extern "C" {
 
 sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stream) {
   if (!c || !batch_ok(c, b, true) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
-  if (!b->uniforms || (b->G > 0 && !b->draft_probs)) return SDV_ERR_INVALID_ARG;
+  const bool greedy = c->sampling == SDV_SAMPLING_GREEDY;
+  if (!greedy && (!b->uniforms || (b->G > 0 && !b->draft_probs))) return SDV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const sdv_config& cf = c->cfg;
   const int R = b->R, H = cf.hidden, D = cf.head_dim, QD = cf.n_q * D, F = cf.ffn, V = cf.vocab;
@@ -642,6 +652,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.out_f32 = z;
     g.epi.ld_f32 = V;
     g.epi.stats = ws_ptr<float2>(c, c->L.lmstats);
+    if (c->sampling == SDV_SAMPLING_GREEDY) g.epi.argmax = ws_ptr<int>(c, c->L.lmargmax);
     g.epi.stats_ld = c->max_rows;
     SDV_CUDA(run_gemm(c, EPI_LMHEAD, 1, &c->tm_lm, &c->tm_lm, c->tm_h3, g, s));
   }
@@ -652,6 +663,8 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     AcceptParams a;
     a.z = z;
     a.tile_stats = ws_ptr<float2>(c, c->L.lmstats);
+    a.tile_argmax = ws_ptr<int>(c, c->L.lmargmax);
+    a.greedy = c->sampling == SDV_SAMPLING_GREEDY ? 1 : 0;
     a.m_tiles = c->L.lm_tiles;
     a.stats_ld = c->max_rows;
     a.draft_probs = b->draft_probs;
@@ -680,7 +693,8 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
 
 sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_result* r, void* stream) {
   if (!c || !probs || !batch_ok(c, b, false) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
-  if (!b->tokens || !b->uniforms || (b->G > 0 && !b->draft_probs)) return SDV_ERR_INVALID_ARG;
+  if (!b->tokens) return SDV_ERR_INVALID_ARG;
+  if (c->sampling != SDV_SAMPLING_GREEDY && (!b->uniforms || (b->G > 0 && !b->draft_probs))) return SDV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrologueParams pp = prologue_params(c, b, r->status, true);
   SDV_CUDA(launch_prologue(pp, s));
@@ -688,6 +702,7 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
   int* final_tokens = r->final_tokens ? r->final_tokens : ws_ptr<int>(c, c->L.final_tokens);
   AcceptParams a;
   a.probs = probs;
+  a.greedy = c->sampling == SDV_SAMPLING_GREEDY ? 1 : 0;
   a.draft_probs = b->draft_probs;
   a.uniforms = b->uniforms;
   a.tokens = b->tokens;

@@ -192,13 +192,24 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, i
       }
       mx = warp_max(mx);
       float s = 0.f;
+      int arg = 0x7FFFFFFF;  // smallest column holding the tile's maximum (greedy verification)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int col = tm * BM + lane + 32 * i;
-        if (col < p.N) s += exp2f((v[i] - mx) * kLog2e);
+        if (col < p.N) {
+          s += exp2f((v[i] - mx) * kLog2e);
+          if (v[i] == mx) arg = min(arg, col);
+        }
       }
       s = warp_sum(s);
-      if (lane == 0) e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
+      if (e.argmax) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
+      }
+      if (lane == 0) {
+        e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
+        if (e.argmax) e.argmax[(long long)tm * e.stats_ld + r] = arg;
+      }
     }
   }
 }

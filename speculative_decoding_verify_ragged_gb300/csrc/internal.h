@@ -50,6 +50,7 @@ struct EpiParams {
   int n_q = 0, n_kv = 0, head_dim = 0, page = 0;
   // LMHEAD
   float2* stats = nullptr;  // [m_tiles, stats_ld]
+  int* argmax = nullptr;    // [m_tiles, stats_ld] or null: smallest column of each tile's row maximum
   int stats_ld = 0;
 };
 
@@ -191,6 +192,8 @@ struct AcceptParams {
   const float2* tile_stats = nullptr;  // [m_tiles, stats_ld] LM head's per-tile (max, sum) (from_logits)
   int m_tiles = 0, stats_ld = 0;
   float2* row_stats = nullptr;         // [R] (max, sum) of each row's logits (from_logits)
+  const int* tile_argmax = nullptr;    // [m_tiles, stats_ld] per-tile argmax (from_logits, greedy)
+  int greedy = 0;                      // greedy verification: argmax tests, argmax final token
   int* chunk_count = nullptr;      // [B] sampling chunks finished per slot (zero between calls)
   unsigned long long* chunk_sums = nullptr;  // [B, 2, chunk_ld]
   int chunk_ld = 0;

@@ -368,11 +368,21 @@ __device__ int slot_row0(const int* draft_lens, int b, int* s_tmp) {
   return t;
 }
 
+// Argmax merge: the larger value wins, equal values keep the smaller index.
+__device__ __forceinline__ void merge_arg(float& m, int& a, float om, int oa) {
+  if (om > m || (om == m && oa < a)) {
+    m = om;
+    a = oa;
+  }
+}
+
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams p) {
   __shared__ int s_tmp[kAccWarps];
   __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
+  __shared__ int s_g[kAccWarps][8];
   __shared__ float2 s_st[64];
+  __shared__ int s_arg[64];
   __shared__ int s_a;
   griddep_launch_dependents();
   const int b = blockIdx.x;
@@ -387,7 +397,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   float qk = 0.f, uk = 0.f;
   if (in_range && threadIdx.x < gam) {
     x = p.tokens[r0 + threadIdx.x + 1];
-    if (x >= 0 && x < V) {
+    if (x >= 0 && x < V && !p.greedy) {
       qk = p.draft_probs[(long long)(g0 + threadIdx.x) * V + x];
       uk = p.uniforms[r0 + threadIdx.x];
     }
@@ -404,11 +414,14 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     // the vocabulary tiles of 8 rows at a time (all its loads in flight together)
     for (int n0 = 0; n0 <= gam; n0 += 8) {
       const int nr = min(8, gam + 1 - n0);
-      float M[8], S[8];
+      float M[8], S[8], GM[8];
+      int GA[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         M[q] = -INFINITY;
         S[q] = 0.f;
+        GM[q] = -INFINITY;
+        GA[q] = 0x7FFFFFFF;
       }
 #pragma unroll 2
       for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
@@ -416,6 +429,11 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           st[q] = q < nr ? p.tile_stats[(long long)tt * p.stats_ld + r0 + n0 + q] : make_float2(-INFINITY, 0.f);
+        if (p.greedy) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < nr) merge_arg(GM[q], GA[q], st[q].x, p.tile_argmax[(long long)tt * p.stats_ld + r0 + n0 + q]);
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) merge_ms(M[q], S[q], st[q].x, st[q].y);
       }
@@ -426,21 +444,71 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
           const float oM = __shfl_xor_sync(0xffffffffu, M[q], o);
           const float oS = __shfl_xor_sync(0xffffffffu, S[q], o);
           merge_ms(M[q], S[q], oM, oS);
+          if (p.greedy) {
+            const float gM = __shfl_xor_sync(0xffffffffu, GM[q], o);
+            const int gA = __shfl_xor_sync(0xffffffffu, GA[q], o);
+            merge_arg(GM[q], GA[q], gM, gA);
+          }
         }
         if (lane == 0) {
           s_m[warp][q] = M[q];
           s_s[warp][q] = S[q];
+          s_g[warp][q] = GA[q];
         }
       }
       __syncthreads();
       if (threadIdx.x < nr) {
-        float Mr = -INFINITY, Sr = 0.f;
-        for (int w = 0; w < kAccWarps; ++w) merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
+        float Mr = -INFINITY, Sr = 0.f, Gm = -INFINITY;
+        int Ga = 0x7FFFFFFF;
+        for (int w = 0; w < kAccWarps; ++w) {
+          merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
+          merge_arg(Gm, Ga, s_m[w][threadIdx.x], s_g[w][threadIdx.x]);
+        }
         s_st[n0 + threadIdx.x] = make_float2(Mr, Sr);
         p.row_stats[r0 + n0 + threadIdx.x] = make_float2(Mr, Sr);
+        s_arg[n0 + threadIdx.x] = Ga;
       }
       __syncthreads();
     }
+  }
+  if (p.greedy) {
+    // greedy verification (temperature -> 0): draft i + 1 is kept iff it is the
+    // argmax of row i (the smallest index among equal maxima); the token after
+    // the kept prefix is the argmax of its row
+    if constexpr (!FROM_LOGITS) {
+      // given probabilities: a block-wide argmax of each row
+      for (int n = 0; n <= gam; ++n) {
+        const float* row = p.probs + (long long)(r0 + n) * V;
+        float m = -INFINITY;
+        int a = 0x7FFFFFFF;
+        for (int j = threadIdx.x; j < V; j += kAccThreads) merge_arg(m, a, row[j], j);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float om = __shfl_xor_sync(0xffffffffu, m, o);
+          const int oa = __shfl_xor_sync(0xffffffffu, a, o);
+          merge_arg(m, a, om, oa);
+        }
+        if (lane == 0) {
+          s_m[warp][0] = m;
+          s_g[warp][0] = a;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          float bm = -INFINITY;
+          int ba = 0x7FFFFFFF;
+          for (int w = 0; w < kAccWarps; ++w) merge_arg(bm, ba, s_m[w][0], s_g[w][0]);
+          s_arg[n] = ba;
+        }
+        __syncthreads();
+      }
+    }
+    if (threadIdx.x < gam && x != s_arg[threadIdx.x]) atomicMin(&s_a, static_cast<int>(threadIdx.x));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      p.accepted[b] = s_a;
+      p.final_tokens[b] = s_arg[s_a];
+    }
+    return;
   }
   if (threadIdx.x < gam) {
     const int k = threadIdx.x;
@@ -871,10 +939,10 @@ cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t 
   cudaError_t e;
   if (from_logits) {
     if ((e = launch_pdl(accept_kernel<true>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
-    return launch_pdl(sample_kernel<true>, grid, dim3(kAccThreads), 0, stream, p);
+    return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<true>, grid, dim3(kAccThreads), 0, stream, p);
   }
   if ((e = launch_pdl(accept_kernel<false>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
-  return launch_pdl(sample_kernel<false>, grid, dim3(kAccThreads), 0, stream, p);
+  return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<false>, grid, dim3(kAccThreads), 0, stream, p);
 }
 
 int accept_chunks(int V) { return (V + kVChunk - 1) / kVChunk; }
