@@ -224,9 +224,27 @@ def gather_kv(kv_pool_f64: np.ndarray, page_table_row: np.ndarray, n: int, page:
 # ---------------------------------------------------------------------------
 
 
+def tree_depths(parents) -> list:
+    """Depth of every node of a tree given each node's parent (node 0 the root,
+    parent[0] = -1, parent[i] < i)."""
+    depth = []
+    for i, par in enumerate(parents):
+        depth.append(0 if i == 0 else depth[int(par)] + 1)
+    return depth
+
+
+def tree_ancestors(parents, i: int) -> list:
+    """Node i and its ancestors up to the root, in increasing index order."""
+    out = [i]
+    while i > 0:
+        i = int(parents[i])
+        out.append(i)
+    return sorted(out)
+
+
 def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarray,
             seq_lens, draft_lens, tokens, eps: float = 1e-6, theta: float = 1e6,
-            slots=None, flips=None):
+            slots=None, flips=None, parents=None):
     """Target-model forward over every verify row of the selected slots.
 
     Returns a dict with logits and probs (float64 [rows, V]), kv_rows where
@@ -241,6 +259,12 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
     exact value instead of the nearest one.  A value within the arithmetic
     error of a rounding tie may round either way in a finite-precision
     evaluation; this lets a caller reproduce such a choice.
+
+    ``parents`` (token trees): [R] parent of every row within its sequence
+    (-1 for row 0, the root; parent < own index).  Row i then sits at position
+    L + depth(i) (its rotary angle) while its K/V goes to cache slot L + i, and
+    it attends to the cached context and to its own ancestors and itself only.
+    None: every sequence is a chain (row i's parent is row i - 1).
     """
     H, nq, nkv, d, P = dims["hidden"], dims["n_q"], dims["n_kv"], dims["head_dim"], dims["page"]
     seq_lens = np.asarray(seq_lens)
@@ -249,12 +273,19 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
     offs = np.concatenate([[0], np.cumsum(draft_lens + 1)])
     if slots is None:
         slots = list(range(B))
-    rows, row_seq, row_pos = [], [], []
+    rows, row_seq, row_pos, row_slot, row_keys = [], [], [], [], []
     for b in slots:
-        for i in range(int(draft_lens[b]) + 1):
+        n_b = int(draft_lens[b]) + 1
+        par = list(range(-1, n_b - 1)) if parents is None else \
+            [int(x) for x in np.asarray(parents)[int(offs[b]): int(offs[b]) + n_b]]
+        depth = tree_depths(par)
+        L = int(seq_lens[b])
+        for i in range(n_b):
             rows.append(int(offs[b]) + i)
             row_seq.append(b)
-            row_pos.append(int(seq_lens[b]) + i)
+            row_pos.append(L + depth[i])
+            row_slot.append(L + i)
+            row_keys.append(list(range(L)) + [L + j for j in tree_ancestors(par, i)])
     rows = np.array(rows, dtype=np.int64)
     row_pos = np.array(row_pos, dtype=np.int64)
     tok = np.asarray(tokens)[rows]
@@ -284,7 +315,7 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
     kv_rows = {}
     kv_seq = {}
     for n, b in enumerate(row_seq):
-        kv_rows[(b, int(row_pos[n]))] = (k[n], v[n])
+        kv_rows[(b, int(row_slot[n]))] = (k[n], v[n])
     for b in slots:
         L = int(seq_lens[b])
         n_total = L + int(draft_lens[b]) + 1
@@ -305,15 +336,16 @@ def forward(dims: dict, weights, kv_pool_bits: np.ndarray, page_table: np.ndarra
             Vc[:, L + i] = vv
         kv_seq[b] = (Kc, Vc)
 
-    # block-causal GQA attention: row at position t sees positions 0..t
+    # block-causal GQA attention: a row sees the cached context and the rows of
+    # its own draft block on its path from the root (for a chain: positions 0..t)
     group = nq // nkv
     o = np.zeros((len(rows), nq, d))
     for n, b in enumerate(row_seq):
         Kc, Vc = kv_seq[b]
-        t = int(row_pos[n])
+        keys = np.array(row_keys[n], dtype=np.int64)
         for h in range(nq):
             g = h // group
-            o[n, h] = attention_one(q[n, h], Kc[g, : t + 1], Vc[g, : t + 1])
+            o[n, h] = attention_one(q[n, h], Kc[g][keys], Vc[g][keys])
     o = o.reshape(len(rows), nq * d)
 
     # output projection + residual
@@ -410,7 +442,28 @@ def greedy_accept(rows: np.ndarray, drafts):
     return a, int(np.argmax(rows[a]))
 
 
-def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens, greedy: bool = False):
+def greedy_tree_accept(rows: np.ndarray, node_tokens, parents):
+    """Greedy verification of one sequence's token tree: from the root, descend
+    into the child whose token is the argmax of the current node's row (the
+    smallest such child index if several), as long as there is one; the final
+    token is the argmax at the node reached.  rows [T, V] (logits or
+    probabilities), node_tokens [T] (node 0 the root), parents [T].
+    Returns (accepted count = depth reached, final token, path of node indices
+    at depths 1..a)."""
+    T = len(parents)
+    v, path = 0, []
+    while True:
+        want = int(np.argmax(rows[v]))
+        kids = [c for c in range(1, T) if int(parents[c]) == v and int(node_tokens[c]) == want]
+        if not kids:
+            break
+        v = kids[0]
+        path.append(v)
+    return len(path), int(np.argmax(rows[v])), path
+
+
+def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens, greedy: bool = False,
+                 parents=None):
     """Every sequence of a batch: accepted counts, emitted tokens, emitted offsets.
 
     p float32 [R, V], q float32 [G, V]; emitted tokens of sequence b are its
@@ -424,11 +477,18 @@ def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens, gre
     goff = np.concatenate([[0], np.cumsum(draft_lens)])
     acc = np.zeros(B, dtype=np.int32)
     fin = np.zeros(B, dtype=np.int32)
+    paths = []
     for b in range(B):
         g = int(draft_lens[b])
         r0 = int(roff[b])
         drafts = np.asarray(tokens)[r0 + 1: r0 + 1 + g]
-        if greedy:
+        if parents is not None:
+            if not greedy:
+                raise ValueError("token trees are verified greedily")
+            a, t, path = greedy_tree_accept(p[r0: r0 + g + 1], np.asarray(tokens)[r0: r0 + g + 1],
+                                            np.asarray(parents)[r0: r0 + g + 1])
+            paths.append(path)
+        elif greedy:
             a, t = greedy_accept(p[r0: r0 + g + 1], drafts)
         else:
             a, t = accept_and_sample(p[r0: r0 + g + 1], q[int(goff[b]): int(goff[b]) + g],
@@ -440,8 +500,11 @@ def accept_batch(p: np.ndarray, q: np.ndarray, tokens, uniforms, draft_lens, gre
     for b in range(B):
         r0 = int(roff[b])
         a = int(acc[b])
-        emitted[eoff[b]: eoff[b] + a] = np.asarray(tokens)[r0 + 1: r0 + 1 + a]
+        nodes = [r0 + c for c in paths[b]] if parents is not None else list(range(r0 + 1, r0 + 1 + a))
+        emitted[eoff[b]: eoff[b] + a] = np.asarray(tokens)[nodes]
         emitted[eoff[b] + a] = fin[b]
+    if parents is not None:
+        return acc, emitted, eoff, fin, paths
     return acc, emitted, eoff, fin
 
 
@@ -547,7 +610,25 @@ def realign(seq_lens, accepted, page_table, num_pages, free_pages, num_free: int
 # ---------------------------------------------------------------------------
 
 
-def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=None, greedy: bool = False):
+def compact_kv(pool_bits: np.ndarray, page_table, seq_lens, paths, page: int) -> np.ndarray:
+    """After a token tree's verification: the K/V of the node at depth k of
+    sequence b's accepted path moves from cache slot L_b + node to slot L_b + k,
+    so the accepted tokens sit at consecutive positions (a chain's path is
+    already in place).  Returns the moved pool (bf16 bits)."""
+    out = np.array(pool_bits, copy=True)
+    for b, path in enumerate(paths):
+        L = int(seq_lens[b])
+        for k, node in enumerate(path, start=1):
+            src, dst = L + int(node), L + k
+            if src == dst:
+                continue
+            ps, pd = page_table[b][src // page], page_table[b][dst // page]
+            out[pd, :, :, dst % page, :] = pool_bits[ps, :, :, src % page, :]
+    return out
+
+
+def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=None, greedy: bool = False,
+                parents=None):
     """Forward, acceptance, sampling and realignment of one batch.
 
     ``batch`` and ``weights`` are the seeded inputs (workloads.Batch /
@@ -557,7 +638,7 @@ def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=Non
     """
     dims = batch.dims
     fw = forward(dims, weights, batch.kv_pool, batch.page_table, batch.seq_lens,
-                 batch.draft_lens, batch.tokens, eps=eps, theta=theta, slots=slots)
+                 batch.draft_lens, batch.tokens, eps=eps, theta=theta, slots=slots, parents=parents)
     p32 = fw["probs"].astype(np.float32)
     out = dict(forward=fw, logits=fw["logits"], probs=fw["probs"], rows=fw["rows"])
     if slots is not None:
@@ -577,8 +658,13 @@ def verify_step(batch, weights, eps: float = 1e-6, theta: float = 1e6, slots=Non
             n += g + 1
         out["per_slot"] = res
         return out
-    acc, emitted, eoff, fin = accept_batch(fw["logits"] if greedy else p32, batch.draft_probs, batch.tokens,
-                                           batch.uniforms, batch.draft_lens, greedy=greedy)
+    if parents is not None:
+        acc, emitted, eoff, fin, paths = accept_batch(fw["logits"], None, batch.tokens, None, batch.draft_lens,
+                                                      greedy=True, parents=parents)
+        out["paths"] = paths
+    else:
+        acc, emitted, eoff, fin = accept_batch(fw["logits"] if greedy else p32, batch.draft_probs, batch.tokens,
+                                               batch.uniforms, batch.draft_lens, greedy=greedy)
     ra = realign(batch.seq_lens, acc, batch.page_table, batch.num_pages, batch.free_pages,
                  batch.num_free, dims["page"], batch.gamma_max,
                  gen_counts=batch.gen_counts, gen_limits=batch.gen_limits)
