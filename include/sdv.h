@@ -108,7 +108,22 @@ typedef struct {
  *                  updated in place (entries at and above the old top).
  *  num_free_in / num_free_out: device scalars (may be the same pointer).
  *  gen_counts / gen_limits [B] or NULL: tokens generated so far and the output
- *                  length at which a sequence finishes (both NULL = none finish). */
+ *                  length at which a sequence finishes (both NULL = none finish).
+ *  tree_parents [R] or NULL: token trees ("Speculative Decoding and Batching
+ *                  Compete for the Same Compute Slack on RDNA4", table in "What
+ *                  the budget says to build": a small tree at low batch).  Row i
+ *                  of slot b is a tree node whose parent is row tree_parents[...]
+ *                  of the same slot (-1 for row 0, the root; otherwise < i;
+ *                  up to 64 rows per slot).  Node i sits at position L_b +
+ *                  depth(i), writes its K/V at slot L_b + i, and attends to the
+ *                  cache and its own ancestors.  Trees are verified greedily
+ *                  (sdv_set_sampling(SDV_SAMPLING_GREEDY); SDV_ERR_UNSUPPORTED
+ *                  otherwise): from the root, descend into the child carrying
+ *                  the argmax of the current row (the smallest such index); the
+ *                  accepted count is the depth reached, the emitted tokens are
+ *                  the path's tokens and the argmax at its end, and realignment
+ *                  moves the path's K/V rows to slots L_b + 1 .. L_b + a_b.
+ *                  NULL: every slot is a chain (row i's parent is row i - 1). */
 typedef struct {
   int B, R, G;
   const int *seq_lens, *draft_lens, *tokens;
@@ -122,6 +137,7 @@ typedef struct {
   const int *num_free_in;
   int *num_free_out;
   const int *gen_counts, *gen_limits;
+  const int *tree_parents;
 } sdv_batch;
 
 /* One verify step's outputs (device pointers; NULL = not wanted, except status).

@@ -105,7 +105,7 @@ class VerifyEngine:
                         _ptr(pt), int(pt.shape[1]),
                         _ptr(b["num_pages"]), _ptr(b.get("free_pages")),
                         _ptr(b.get("num_free_in")), _ptr(b.get("num_free_out")),
-                        _ptr(b.get("gen_counts")), _ptr(b.get("gen_limits")))
+                        _ptr(b.get("gen_counts")), _ptr(b.get("gen_limits")), _ptr(b.get("tree_parents")))
 
     @staticmethod
     def result_struct(r: dict) -> SdvResult:

@@ -54,7 +54,7 @@ class SdvBatch(ctypes.Structure):
                 ("page_table", c_void_p), ("max_pages_per_seq", c_int),
                 ("num_pages", c_void_p), ("free_pages", c_void_p),
                 ("num_free_in", c_void_p), ("num_free_out", c_void_p),
-                ("gen_counts", c_void_p), ("gen_limits", c_void_p)]
+                ("gen_counts", c_void_p), ("gen_limits", c_void_p), ("tree_parents", c_void_p)]
 
 
 RESULT_FIELDS = ("accepted", "final_tokens", "emitted_tokens", "emitted_offsets", "new_seq_lens",

@@ -43,7 +43,8 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 // ---------------------------------------------------------------------------
 
 struct Layout {
-  size_t row_off, draft_off, row_seq, row_pos, chunks, item_off, sched, items, rope, kv_row_off, inv_freq;
+  size_t row_off, draft_off, row_seq, row_pos, row_anc, tree_path, chunks, item_off, sched, items, rope, kv_row_off,
+      inv_freq;
   size_t x0, h, h3, q, attn, x1, x1sq, act, x2, z, lmstats, lmargmax, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, chunk_count, chunk_sums, total;
   int chunk_ld;
@@ -101,6 +102,8 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.draft_off = take((B + 1) * 4);
   L.row_seq = take(R * 4);
   L.row_pos = take(R * 4);
+  L.row_anc = take(R * 8);
+  L.tree_path = take(R * 4);
   L.chunks = take(B * 4);
   L.item_off = take((B + 1) * 4);
   L.sched = take(64);
@@ -400,6 +403,8 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   p.t.items = ws_ptr<int4>(c, c->L.items);
   p.t.rope_cs = ws_ptr<float>(c, c->L.rope);
   p.t.kv_row_off = ws_ptr<long long>(c, c->L.kv_row_off);
+  p.t.row_anc = ws_ptr<unsigned long long>(c, c->L.row_anc);
+  p.tree_parents = b->tree_parents;
   p.seq_lens = b->seq_lens;
   p.draft_lens = b->draft_lens;
   p.tokens = b->tokens;
@@ -494,6 +499,7 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   a.items = ws_ptr<int4>(c, c->L.items);
   a.part_o = ws_ptr<float>(c, c->L.part_o);
   a.part_ml = ws_ptr<float2>(c, c->L.part_ml);
+  a.row_anc = b->tree_parents ? ws_ptr<unsigned long long>(c, c->L.row_anc) : nullptr;
   a.status = status;
   a.B = b->B;
   a.n_q = c->cfg.n_q;
@@ -539,6 +545,12 @@ static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_re
   p.num_free_out = b->num_free_out;
   p.gen_counts = b->gen_counts;
   p.gen_limits = b->gen_limits;
+  if (b->tree_parents) {
+    p.tree_path = ws_ptr<int>(c, c->L.tree_path);
+    p.kv_pool = static_cast<__nv_bfloat16*>(b->kv_pool);
+    p.n_kv = c->cfg.n_kv;
+    p.head_dim = c->cfg.head_dim;
+  }
   p.res = *r;
   p.B = b->B;
   p.page = c->cfg.page_size;
@@ -546,6 +558,20 @@ static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_re
   p.max_pages = b->max_pages_per_seq;
   p.pool_pages = b->num_pool_pages;
   return p;
+}
+
+// Token trees are verified greedily and need the cache their path moves in.
+static sdv_status tree_check(const sdv_ctx* c, const sdv_batch* b) {
+  if (!b->tree_parents) return SDV_OK;
+  if (c->sampling != SDV_SAMPLING_GREEDY) return SDV_ERR_UNSUPPORTED;
+  if (!b->kv_pool || !b->tokens) return SDV_ERR_INVALID_ARG;
+  return SDV_OK;
+}
+
+// The accept kernel's tree fields.
+static void tree_accept(sdv_ctx* c, const sdv_batch* b, AcceptParams& a) {
+  a.tree_parents = b->tree_parents;
+  a.tree_path = b->tree_parents ? ws_ptr<int>(c, c->L.tree_path) : nullptr;
 }
 
 static bool result_ok(const sdv_batch* b, const sdv_result* r) {
@@ -561,6 +587,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   if (!c || !batch_ok(c, b, true) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
   const bool greedy = c->sampling == SDV_SAMPLING_GREEDY;
   if (!greedy && (!b->uniforms || (b->G > 0 && !b->draft_probs))) return SDV_ERR_INVALID_ARG;
+  if (const sdv_status ts = tree_check(c, b); ts != SDV_OK) return ts;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const sdv_config& cf = c->cfg;
   const int R = b->R, H = cf.hidden, D = cf.head_dim, QD = cf.n_q * D, F = cf.ffn, V = cf.vocab;
@@ -674,6 +701,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     a.row_off = pp.t.row_off;
     a.draft_off = pp.t.draft_off;
     a.row_stats = ws_ptr<float2>(c, c->L.rowstats);
+    tree_accept(c, b, a);
     fill_accept_scratch(c, a);
     a.accepted = accepted;
     a.final_tokens = final_tokens;
@@ -695,6 +723,7 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
   if (!c || !probs || !batch_ok(c, b, false) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
   if (!b->tokens) return SDV_ERR_INVALID_ARG;
   if (c->sampling != SDV_SAMPLING_GREEDY && (!b->uniforms || (b->G > 0 && !b->draft_probs))) return SDV_ERR_INVALID_ARG;
+  if (const sdv_status ts = tree_check(c, b); ts != SDV_OK) return ts;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrologueParams pp = prologue_params(c, b, r->status, true);
   SDV_CUDA(launch_prologue(pp, s));
@@ -709,6 +738,7 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
   a.draft_lens = b->draft_lens;
   a.row_off = pp.t.row_off;
   a.draft_off = pp.t.draft_off;
+  tree_accept(c, b, a);
   fill_accept_scratch(c, a);
   a.accepted = accepted;
   a.final_tokens = final_tokens;
@@ -725,6 +755,7 @@ sdv_status sdv_accept(sdv_ctx* c, const float* probs, const sdv_batch* b, sdv_re
 sdv_status sdv_realign(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* stream) {
   if (!c || !batch_ok(c, b, false) || !result_ok(b, r)) return SDV_ERR_INVALID_ARG;
   if (!r->accepted || !r->final_tokens || !b->tokens) return SDV_ERR_INVALID_ARG;
+  if (b->tree_parents) return SDV_ERR_UNSUPPORTED;  // the accepted path is not an input
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PrologueParams pp = prologue_params(c, b, r->status, false);
   SDV_CUDA(launch_prologue(pp, s));

@@ -252,16 +252,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         for (int nf = 0; nf < 2; ++nf)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[nf][e] = (sa[0][nf][e] + sa[1][nf][e]) + (sa[2][nf][e] + sa[3][nf][e]);
-        // scale to base-2 logits and apply the block-causal mask
+        // scale to base-2 logits and apply the block-causal mask; in a token
+        // tree a key at L + d (d >= 0) counts for a row iff node d is the row's
+        // node or one of its ancestors
         const int kp0 = pi * p.page;
+        const bool tree_tail = p.row_anc != nullptr && kp0 + p.page > it.L;
+        unsigned long long anc0 = 0ull, anc1 = 0ull;
+        if (tree_tail) {
+          if (v0 < nqv) anc0 = p.row_anc[it.r0 + v0 / group];
+          if (v1 < nqv) anc1 = p.row_anc[it.r0 + v1 / group];
+        }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int nf = 0; nf < 2; ++nf)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int kp = kp0 + nf * 8 + 2 * t + e;
-            s[nf][e] = kp <= qpos0 ? s[nf][e] * scale : -INFINITY;
-            s[nf][2 + e] = kp <= qpos1 ? s[nf][2 + e] * scale : -INFINITY;
+            bool in0 = kp <= qpos0, in1 = kp <= qpos1;
+            if (tree_tail) {
+              // (padding rows keep the chain's mask: their lanes still vote on rescaling)
+              const int d = kp - it.L;
+              if (v0 < nqv) in0 = d < 0 || (d < 64 && ((anc0 >> d) & 1ull));
+              if (v1 < nqv) in1 = d < 0 || (d < 64 && ((anc1 >> d) & 1ull));
+            }
+            s[nf][e] = in0 ? s[nf][e] * scale : -INFINITY;
+            s[nf][2 + e] = in1 ? s[nf][2 + e] * scale : -INFINITY;
             mx0 = fmaxf(mx0, s[nf][e]);
             mx1 = fmaxf(mx1, s[nf][2 + e]);
           }

@@ -390,10 +390,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const Item it = load_item(p, item);
       const int nqv = (it.gamma + 1) * group;
       const int nblk = (it.p1 - it.p0 + PAGES - 1) / PAGES;
-      // the last key position each of the group's query vectors may see (-1: padding)
+      // the last key position each of the group's query vectors may see (-1:
+      // padding); in a token tree every node's keys end within L + 63 and the
+      // ancestor sets decide the rest
+      const bool tree = p.row_anc != nullptr;
       int qlim[NH];
 #pragma unroll
-      for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (col0 + j) / group : -1;
+      for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (tree ? 63 : (col0 + j) / group) : -1;
 
       // Q rows of this group as bf16 hi + lo (zero rows past nqv), once the
       // previous item's last QK^T has read the buffer
@@ -442,10 +445,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int page = it.p0 + b * PAGES + (t >> 4);
         const int key = page < it.p1 ? page * 16 + (t & 15) : 0x7FFFFFFF;
         bool up = false;
+        if (tree && key >= it.L && key <= it.L + 63) {
+          // token tree, key L + d: visible to the columns whose node has node d
+          // among its ancestors (or is node d)
+          const int d = key - it.L;
 #pragma unroll
-        for (int j = 0; j < NH; ++j) {
-          s[j] = key <= qlim[j] ? s[j] * scale : -INFINITY;
-          up |= s[j] > m[j] + kLazy;
+          for (int j = 0; j < NH; ++j) {
+            const bool in = col0 + j < nqv && ((p.row_anc[it.r0 + (col0 + j) / group] >> d) & 1ull);
+            s[j] = in ? s[j] * scale : -INFINITY;
+            up |= s[j] > m[j] + kLazy;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NH; ++j) {
+            s[j] = key <= qlim[j] ? s[j] * scale : -INFINITY;
+            up |= s[j] > m[j] + kLazy;
+          }
         }
         // does any logit of the block exceed its reference by more than kLazy?
         const unsigned any_w = __ballot_sync(0xffffffffu, up);

@@ -118,6 +118,7 @@ struct AttnParams {
   const int4* items = nullptr;    // [items, 2]: (slot, kv head, first page, end page), (L, gamma, row 0, chunks)
   float* part_o = nullptr;        // [items, QMAX, D]
   float2* part_ml = nullptr;      // [items, QMAX]
+  const unsigned long long* row_anc = nullptr;  // [R] token trees: ancestor sets (null: block-causal chains)
   int* status = nullptr;
   int B = 0, n_q = 0, n_kv = 0, page = 0;
 };
@@ -147,6 +148,7 @@ struct StepTables {
   int4* items = nullptr;     // [items, 2] attention work items (null: not built)
   float* rope_cs = nullptr;  // [R, D/2, 2]
   long long* kv_row_off = nullptr;  // [R]
+  unsigned long long* row_anc = nullptr;  // [R] token trees: bit j = node j is the row's ancestor or itself
 };
 
 struct PrologueParams {
@@ -156,6 +158,7 @@ struct PrologueParams {
   const int* tokens = nullptr;
   const int* page_table = nullptr;
   const int* num_pages = nullptr;
+  const int* tree_parents = nullptr;  // [R] token trees (null: chains)
   int* status = nullptr;
   int B = 0, R = 0, G = 0, gamma_max = 0, vocab = 0, page = 0, max_pages = 0, pool_pages = 0;
   int n_kv = 0, head_dim = 0, target_items = 0;
@@ -194,6 +197,8 @@ struct AcceptParams {
   float2* row_stats = nullptr;         // [R] (max, sum) of each row's logits (from_logits)
   const int* tile_argmax = nullptr;    // [m_tiles, stats_ld] per-tile argmax (from_logits, greedy)
   int greedy = 0;                      // greedy verification: argmax tests, argmax final token
+  const int* tree_parents = nullptr;   // [R] token trees (greedy only; null: chains)
+  int* tree_path = nullptr;            // [G] accepted path of each slot, from its draft offset
   int* chunk_count = nullptr;      // [B] sampling chunks finished per slot (zero between calls)
   unsigned long long* chunk_sums = nullptr;  // [B, 2, chunk_ld]
   int chunk_ld = 0;
@@ -223,6 +228,11 @@ struct RealignParams {
   int* num_free_out = nullptr;
   const int* gen_counts = nullptr;
   const int* gen_limits = nullptr;
+  // token trees: the accepted path of each slot (from its draft offset) and the
+  // cache its K/V rows move in (null: chains, nothing moves)
+  const int* tree_path = nullptr;
+  __nv_bfloat16* kv_pool = nullptr;
+  int n_kv = 0, head_dim = 0;
   sdv_result res;
   int B = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0;
 };

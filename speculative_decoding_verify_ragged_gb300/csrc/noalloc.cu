@@ -81,6 +81,7 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
       !b->free_pages || !b->num_free_in || !b->num_free_out || (b->G > 0 && !b->draft_probs))
     return SDV_ERR_INVALID_ARG;
   if ((r->accept_tested == nullptr) != (r->accept_accepted == nullptr)) return SDV_ERR_INVALID_ARG;
+  if (b->tree_parents) return SDV_ERR_UNSUPPORTED;  // token trees are verified greedily, with a context
   if (cfg->vocab <= 0 || cfg->page_size <= 0 || cfg->gamma_max < 0 || cfg->gamma_max > 63 ||
       b->max_pages_per_seq <= 0 || b->num_pool_pages <= 0)
     return SDV_ERR_INVALID_ARG;

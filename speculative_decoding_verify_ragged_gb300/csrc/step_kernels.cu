@@ -90,6 +90,16 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   const int goff = block_exscan(slot ? gam : 0, &tot_g, s_warp);
   const int poff = block_exscan(used, &tot_pages, s_warp);
   if (b == 0 && (tot_r != p.R || tot_g != p.G)) atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+  if (slot && !err && p.tree_parents) {
+    // a token tree: at most 64 nodes, node 0 the root, every other node's
+    // parent an earlier node of the same slot
+    bool ok = gam < 64 && roff + gam < p.R;
+    for (int i = 0; ok && i <= gam; ++i) {
+      const int par = p.tree_parents[roff + i];
+      ok = i == 0 ? par == -1 : (par >= 0 && par < i);
+    }
+    if (!ok) atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+  }
   if (b < p.B) s_poff[b] = poff;
   if (b == 0) s_poff[p.B] = tot_pages;
   __syncthreads();
@@ -100,9 +110,26 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   if (slot) {
     p.t.row_off[b] = roff;
     p.t.draft_off[b] = goff;
-    for (int i = 0; i <= gam; ++i) {
-      p.t.row_seq[roff + i] = b;
-      p.t.row_pos[roff + i] = L + i;
+    if (p.tree_parents) {
+      // depth and ancestor set (the node itself included) of every node, in
+      // index order: a parent's entries are written before its children read them
+      for (int i = 0; i <= gam; ++i) {
+        int pos = L;
+        unsigned long long anc = 1ull;
+        if (i > 0) {
+          const int par = p.tree_parents[roff + i];
+          pos = p.t.row_pos[roff + par] + 1;
+          anc = p.t.row_anc[roff + par] | (1ull << i);
+        }
+        p.t.row_seq[roff + i] = b;
+        p.t.row_pos[roff + i] = pos;
+        p.t.row_anc[roff + i] = anc;
+      }
+    } else {
+      for (int i = 0; i <= gam; ++i) {
+        p.t.row_seq[roff + i] = b;
+        p.t.row_pos[roff + i] = L + i;
+      }
     }
   }
   if (b == 0) {
@@ -206,10 +233,12 @@ __device__ void norm_row(const float* x, const __nv_bfloat16* gain, __nv_bfloat1
 // Every block r: row r's slot and position (scan of the draft lengths), the
 // embedding row into the fp32 residual stream, the attention pre-norm, the
 // rotary (cos, sin) table and the element offset of the row's K/V in the cache.
+// Row i of a slot writes its K/V at cache slot L + i; its rotary position is
+// L + i in a chain and L + depth(i) in a token tree.
 // Inputs that would make an access leave its buffer skip the access; block 0
 // reports them in the status word.
 __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
-  __shared__ int s_b, s_i;
+  __shared__ int s_b, s_i, s_depth;
   __shared__ float s_red[32];
   const int t = threadIdx.x;
   const int gam = t < p.B ? p.draft_lens[t] : 0;
@@ -224,15 +253,33 @@ __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
   __syncthreads();
   const int b = s_b;
   if (b < 0) return;
-  const int pos = p.seq_lens[b] + s_i;
+  const int slot_pos = p.seq_lens[b] + s_i;  // cache slot of the row's K/V
+  int depth = s_i;
+  if (p.tree_parents) {
+    if (t == 0) {
+      // parents up to the root; a malformed table ends the walk (block 0 reports it)
+      const int r0 = r - s_i;
+      int v = s_i, d = 0;
+      while (v > 0 && d < 64) {
+        const int par = p.tree_parents[r0 + v];
+        if (par < 0 || par >= v) break;
+        v = par;
+        ++d;
+      }
+      s_depth = d;
+    }
+    __syncthreads();
+    depth = s_depth;
+  }
+  const int pos = p.seq_lens[b] + depth;  // rotary position
   const int tok = p.tokens[r];
   if (t == 0) {
-    const int pi = pos / p.page;
+    const int pi = slot_pos / p.page;
     long long off = 0;
-    if (pos >= 0 && pi < p.num_pages[b] && pi < p.max_pages) {
+    if (slot_pos >= 0 && pi < p.num_pages[b] && pi < p.max_pages) {
       const int pg = p.page_table[(long long)b * p.max_pages + pi];
       if (pg >= 0 && pg < p.pool_pages)
-        off = (long long)pg * p.n_kv * 2 * p.page * p.head_dim + (long long)(pos - pi * p.page) * p.head_dim;
+        off = (long long)pg * p.n_kv * 2 * p.page * p.head_dim + (long long)(slot_pos - pi * p.page) * p.head_dim;
     }
     p.t.kv_row_off[r] = off;
   }
@@ -383,6 +430,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   __shared__ int s_g[kAccWarps][8];
   __shared__ float2 s_st[64];
   __shared__ int s_arg[64];
+  __shared__ int s_par[64], s_tok[64];  // token trees: parent and token of each node
   __shared__ int s_a;
   griddep_launch_dependents();
   const int b = blockIdx.x;
@@ -400,6 +448,10 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     if (x >= 0 && x < V && !p.greedy) {
       qk = p.draft_probs[(long long)(g0 + threadIdx.x) * V + x];
       uk = p.uniforms[r0 + threadIdx.x];
+    }
+    if (p.tree_parents) {
+      s_par[threadIdx.x + 1] = p.tree_parents[r0 + threadIdx.x + 1];
+      s_tok[threadIdx.x + 1] = x;
     }
   }
   if (threadIdx.x == 0) s_a = gam;
@@ -501,6 +553,33 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
         }
         __syncthreads();
       }
+    }
+    if (p.tree_parents) {
+      // token tree: from the root, step into the child (smallest index first)
+      // whose token is the current node's argmax; the accepted count is the
+      // depth reached and the final token the argmax where the walk stops.
+      // Every step moves to a larger node index, so the walk ends within gam
+      // steps (parents were validated by the prologue).
+      if (warp == 0) {
+        int node = 0, depth = 0;
+        for (int step = 0; step < 64; ++step) {
+          const int want = s_arg[node];
+          const int c0 = lane, c1 = lane + 32;
+          const bool m0 = c0 >= 1 && c0 <= gam && s_par[c0] == node && s_tok[c0] == want;
+          const bool m1 = c1 <= gam && s_par[c1] == node && s_tok[c1] == want;
+          const unsigned b0 = __ballot_sync(0xffffffffu, m0), b1 = __ballot_sync(0xffffffffu, m1);
+          if (b0 == 0u && b1 == 0u) break;
+          const int child = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+          if (lane == 0) p.tree_path[g0 + depth] = child;
+          ++depth;
+          node = child;
+        }
+        if (lane == 0) {
+          p.accepted[b] = depth;
+          p.final_tokens[b] = s_arg[node];
+        }
+      }
+      return;
     }
     if (threadIdx.x < gam && x != s_arg[threadIdx.x]) atomicMin(&s_a, static_cast<int>(threadIdx.x));
     __syncthreads();
@@ -770,6 +849,7 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   __shared__ int s_warp[80];
   __shared__ int s_err;
   __shared__ int s_need[kScanThreads], s_src[kScanThreads];
+  __shared__ int s_amax;
   griddep_launch_dependents();
   griddep_wait();
   if (read_status(p.res.status) != 0) return;
@@ -808,7 +888,12 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   if (slot) {
     const int r0 = p.row_off[b];
     if (res.emitted_tokens) {
-      for (int i = 0; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + 1 + i];
+      if (p.tree_path) {
+        const int* path = p.tree_path + (r0 - b);  // from the slot's draft offset
+        for (int i = 0; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + path[i]];
+      } else {
+        for (int i = 0; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + 1 + i];
+      }
       res.emitted_tokens[eoff + a] = p.final_tokens[b];
     }
     if (res.emitted_offsets) res.emitted_offsets[b] = eoff;
@@ -830,6 +915,41 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
       *p.num_free_out = top;
     }
     return;
+  }
+
+  // token trees: the K/V of the accepted path's node at depth k moves from
+  // cache slot L + node to slot L + k, one depth at a time.  A node's index is
+  // at least its depth, so a move never reads a slot that a shallower move
+  // wrote; all slots read lie below L + gamma + 1, inside pages the trim keeps.
+  if (p.tree_path && p.kv_pool) {
+    if (b == 0) s_amax = 0;
+    __syncthreads();
+    if (slot && a > 0) atomicMax(&s_amax, a);
+    if (slot) s_need[b] = -1;
+    __syncthreads();
+    const int vec = p.head_dim / 8;       // 16-byte vectors of one head row
+    const int per_row = p.n_kv * 2 * vec;  // vectors of one position's K and V
+    const long long head_stride = (long long)p.page * p.head_dim;
+    for (int k = 1; k <= s_amax; ++k) {
+      // s_need[b]: this depth's source slot of sequence b, or -1
+      if (slot) s_need[b] = k <= a ? L + p.tree_path[p.row_off[b] - b + k - 1] : -1;
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < p.B * per_row; idx += blockDim.x) {
+        const int sb = idx / per_row, e = idx - sb * per_row;
+        const int src = s_need[sb];
+        if (src < 0) continue;
+        const int dst = p.seq_lens[sb] + k;
+        if (src == dst) continue;
+        const int hk = e / vec, v = e - hk * vec;  // (head, K or V), vector
+        const int* pt = p.page_table + (long long)sb * p.max_pages;
+        const long long so = ((long long)pt[src / p.page] * p.n_kv * 2 + hk) * head_stride +
+                             (long long)(src % p.page) * p.head_dim + v * 8;
+        const long long dof = ((long long)pt[dst / p.page] * p.n_kv * 2 + hk) * head_stride +
+                              (long long)(dst % p.page) * p.head_dim + v * 8;
+        *reinterpret_cast<uint4*>(p.kv_pool + dof) = *reinterpret_cast<const uint4*>(p.kv_pool + so);
+      }
+      __syncthreads();
+    }
   }
 
   // push every slot's surplus tail pages above the old top, in slot order

@@ -49,7 +49,7 @@ int main(void) {
          sizeof(sdv_admission), sizeof(sdv_sched_config), sizeof(sdv_sched_step), sizeof(sdv_sched_stats));
   F(sdv_admission, max_pages_per_seq) F(sdv_admission, num_free) F(sdv_sched_stats, live)
   F(sdv_config, rope_theta) F(sdv_weights, g_final) F(sdv_batch, num_pool_pages)
-  F(sdv_batch, max_pages_per_seq) F(sdv_batch, gen_limits) F(sdv_result, logits) F(sdv_result, status)
+  F(sdv_batch, max_pages_per_seq) F(sdv_batch, gen_limits) F(sdv_batch, tree_parents) F(sdv_result, logits) F(sdv_result, status)
   return 0;
 }
 """
@@ -72,6 +72,7 @@ def test_ctypes_layout_matches_header(tmp_path):
     assert int(vals["sdv_batch.num_pool_pages"]) == _abi.SdvBatch.num_pool_pages.offset
     assert int(vals["sdv_batch.max_pages_per_seq"]) == _abi.SdvBatch.max_pages_per_seq.offset
     assert int(vals["sdv_batch.gen_limits"]) == _abi.SdvBatch.gen_limits.offset
+    assert int(vals["sdv_batch.tree_parents"]) == _abi.SdvBatch.tree_parents.offset
     assert int(vals["sdv_result.logits"]) == _abi.SdvResult.logits.offset
     assert int(vals["sdv_result.status"]) == _abi.SdvResult.status.offset
     assert int(vals["sdv_admission"]) == ctypes.sizeof(_abi.SdvAdmission)
