@@ -306,5 +306,66 @@ __device__ __forceinline__ void finish_tile_mma(const GemmParams& p, float (&acc
   named_sync(1, NTHREADS);
 }
 
+// A CTA's part of a tile cut between CTAs in the tcgen05 kernels: four
+// epilogue warps, thread m = weight row m; the part is stored column-major in
+// the CTA's partial slot, [column][128 weight rows], so that each warp's 32
+// rows of one column are 128 contiguous bytes.
+__device__ __forceinline__ void tc_store_part16(float* slot_base, int c0, int m, const float (&v)[16]) {
+#pragma unroll
+  for (int n = 0; n < 16; ++n) __stcg(slot_base + (size_t)(c0 + n) * BM + m, v[n]);
+}
+
+// Fixup of a tile cut between CTAs in the tcgen05 kernels, run by the CTA
+// that arrives last: the parts of CTAs c_first .. c_last are summed in CTA
+// order, 16 columns at a time, and each 16-column chunk goes through the fused
+// epilogue.  The loads of up to four parts are issued together, and the next
+// chunk's first loads are in flight while the current chunk's epilogue runs.
+template <int EPI, int NT, int LD>
+__device__ __forceinline__ void tc_fixup_tile(const GemmParams& p, int tile, int c_first, int c_last,
+                                              long long total, float* epi, int m, int rows) {
+  const int P = gridDim.x;
+  const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
+  auto src_of = [&](int cc, int c0) {
+    const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
+    const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
+    return p.partials + (size_t)slot * BM * NT + (size_t)c0 * BM + m;
+  };
+  auto issue = [&](float (&w)[4][16], int cc0, int c0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (cc0 + q <= c_last) {
+        const float* s = src_of(cc0 + q, c0);
+#pragma unroll
+        for (int n = 0; n < 16; ++n) w[q][n] = __ldcg(s + (size_t)n * BM);
+      }
+  };
+  auto add = [&](float (&v)[16], const float (&w)[4][16], int cc0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (cc0 + q <= c_last) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) v[n] += w[q][n];
+      }
+  };
+  float w[4][16];
+  issue(w, c_first, 0);
+  for (int c0 = 0; c0 < rows; c0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) v[n] = 0.f;
+    add(v, w, c_first);
+    for (int cc0 = c_first + 4; cc0 <= c_last; cc0 += 4) {
+      issue(w, cc0, c0);
+      add(v, w, cc0);
+    }
+    if (c0 + 16 < rows) issue(w, c_first, c0 + 16);
+#pragma unroll
+    for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
+    named_sync(1, 4 * kWarp);
+    epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(16, rows - c0), m);
+    named_sync(1, 4 * kWarp);
+  }
+}
+
 }  // namespace gemm
 }  // namespace sdv

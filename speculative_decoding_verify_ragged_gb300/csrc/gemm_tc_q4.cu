@@ -404,13 +404,11 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
         const int c_first = cta_of_unit(tu, total, P);
         const int c_last = cta_of_unit(tu + p.kb - 1, total, P);
         const int my_slot = 2 * c + (tile == static_cast<int>(u_begin / p.kb) ? 0 : 1);
-        float* mine = p.partials + (size_t)my_slot * BM * NT + (size_t)m * NT;
+        float* mine = p.partials + (size_t)my_slot * BM * NT;
         for (int c0 = 0; c0 < cols; c0 += EC) {
           float v[16];
           tmem_ld_sum(t_row + c0, NT, v);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            __stcg(reinterpret_cast<float4*>(mine + c0) + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          tc_store_part16(mine, c0, m, v);
         }
         tc_fence_before();
         __syncwarp();
@@ -425,32 +423,8 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
         const bool last = *flag != 0;
         if (last) {
           __threadfence();
-          for (int c0 = 0; c0 < rows; c0 += EC) {
-            float v[16];
-#pragma unroll
-            for (int n = 0; n < 16; ++n) v[n] = 0.f;
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
-              const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
-              const float4* src =
-                  reinterpret_cast<const float4*>(p.partials + (size_t)slot * BM * NT + (size_t)m * NT + c0);
-              float4 w[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) w[i] = __ldcg(src + i);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                v[4 * i] += w[i].x;
-                v[4 * i + 1] += w[i].y;
-                v[4 * i + 2] += w[i].z;
-                v[4 * i + 3] += w[i].w;
-              }
-            }
-#pragma unroll
-            for (int n = 0; n < EC; ++n) epi[n * LD + m] = v[n];
-            named_sync(1, 4 * kWarp);
-            epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(EC, rows - c0), tid);
-            named_sync(1, 4 * kWarp);
-          }
+          static_assert(EC == 16, "16-column epilogue chunks");
+          tc_fixup_tile<EPI, NT, LD>(p, tile, c_first, c_last, total, epi, m, rows);
           if (m == 0) p.counters[tile] = 0;  // ready for the next launch
         }
       }
