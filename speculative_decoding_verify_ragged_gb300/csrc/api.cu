@@ -447,6 +447,11 @@ static const CUtensorMap* q4(const sdv_ctx* c, const CUtensorMap& scales) { retu
 // SDV_GEMM_AUTO mode (below it the mma.sync kernel's 8-row tiles waste less).
 constexpr int kTcRows = 17;
 
+// Activation tile heights at and above which the tcgen05 GEMMs leave their
+// cut tiles to the parallel fixup kernel (one 16-row chunk per block) rather
+// than to the last CTA to arrive, which would walk every chunk of the tile.
+constexpr int kDeferFixupRows = 32;
+
 // Slots at and above which auto mode runs attention on tcgen05.
 constexpr int kTcAttnSlots = 4;
 
@@ -468,8 +473,11 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
     g.n_tiles = (g.R + nt - 1) / nt;
     const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
     const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
-    if (tcq) return launch_gemm_tc_q4(epi, nt, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
-    return launch_gemm_q4(epi, nt, xp, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
+    if (!tcq) return launch_gemm_q4(epi, nt, xp, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
+    g.defer_fixup = nt >= kDeferFixupRows ? 1 : 0;
+    cudaError_t e = launch_gemm_tc_q4(epi, nt, a0, a1, s0, s1, &xmaps[nt_index(nt)], g, grid, s);
+    if (e == cudaSuccess && g.defer_fixup) e = launch_gemm_tc_fixup(epi, nt, g, grid, s);
+    return e;
   }
   const bool tc = use_tc(c, g.R);
   const int nt = tc ? gemm_tc_tile_rows(g.R) : gemm_tile_rows(g.R);
@@ -477,7 +485,11 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
   const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
   const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
   const CUtensorMap* x = &xmaps[nt_index(nt)];
-  return tc ? launch_gemm_tc(epi, nt, xp, a0, a1, x, g, grid, s) : launch_gemm(epi, nt, xp, a0, a1, x, g, grid, s);
+  if (!tc) return launch_gemm(epi, nt, xp, a0, a1, x, g, grid, s);
+  g.defer_fixup = nt >= kDeferFixupRows ? 1 : 0;
+  cudaError_t e = launch_gemm_tc(epi, nt, xp, a0, a1, x, g, grid, s);
+  if (e == cudaSuccess && g.defer_fixup) e = launch_gemm_tc_fixup(epi, nt, g, grid, s);
+  return e;
 }
 
 static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,

@@ -445,17 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
   }
 }
 
-// One thread per output element (row, query head, d) of a split sequence:
-// combine the chunks' (max, sum, unnormalised output) partials.
+// Merge of a split sequence's chunk partials, four consecutive head-dim
+// elements of one (row, query head) per thread: one pass over the chunks in
+// chunk order with a running maximum (the unnormalised output and the sum of
+// weights are rescaled whenever the maximum moves), loads of four chunks in
+// flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
+  constexpr int DV = D / 4;
   griddep_launch_dependents();
   griddep_wait();
   if (read_status(p.status) != 0) return;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= (long long)R * p.n_q * D) return;
-  const int d = static_cast<int>(gid % D);
-  const int rh = static_cast<int>(gid / D);
+  if (gid >= (long long)R * p.n_q * DV) return;
+  const int d4 = static_cast<int>(gid % DV);
+  const int rh = static_cast<int>(gid / DV);
   const int r = rh / p.n_q, h = rh - (rh / p.n_q) * p.n_q;
   const int b = row_seq[r];
   const int chunks = p.chunks[b];
@@ -466,19 +470,41 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   const int v = i * group + (h - g * group);
   const long long item0 = p.item_off[b] + (long long)g * chunks;
   const float2* ml = p.part_ml + item0 * kAttnQMax + v;
-  const float* po = p.part_o + (item0 * kAttnQMax + v) * D + d;
-  float M = -INFINITY;
-#pragma unroll 8
-  for (int c = 0; c < chunks; ++c) M = fmaxf(M, ml[(long long)c * kAttnQMax].x);
-  float acc = 0.f, L = 0.f;
-#pragma unroll 8
-  for (int c = 0; c < chunks; ++c) {
-    const float2 m = ml[(long long)c * kAttnQMax];
-    const float w = m.x == -INFINITY ? 0.f : exp2f(m.x - M);
-    L += w * m.y;
-    acc += w * po[(long long)c * kAttnQMax * D];
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (item0 * kAttnQMax + v) * D) + d4;
+  constexpr long long kO4 = (long long)kAttnQMax * D / 4;  // float4 stride between chunks
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < chunks; c0 += 4) {
+    float2 m[4];
+    float4 o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (c0 + q < chunks) {
+        m[q] = ml[(long long)(c0 + q) * kAttnQMax];
+        o[q] = po[(long long)(c0 + q) * kO4];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (c0 + q < chunks && m[q].x != -INFINITY) {
+        const float nm = fmaxf(M, m[q].x);
+        const float a = M == -INFINITY ? 0.f : exp2f(M - nm);
+        const float w = exp2f(m[q].x - nm);
+        L = L * a + w * m[q].y;
+        acc.x = acc.x * a + w * o[q].x;
+        acc.y = acc.y * a + w * o[q].y;
+        acc.z = acc.z * a + w * o[q].z;
+        acc.w = acc.w * a + w * o[q].w;
+        M = nm;
+      }
+    }
   }
-  store_planes(p.out, p.out_lo_off, ((long long)r * p.n_q + h) * D + d, acc / L);
+  const float inv = 1.f / L;
+  const long long base = ((long long)r * p.n_q + h) * D + d4 * 4;
+  store_planes(p.out, p.out_lo_off, base, acc.x * inv);
+  store_planes(p.out, p.out_lo_off, base + 1, acc.y * inv);
+  store_planes(p.out, p.out_lo_off, base + 2, acc.z * inv);
+  store_planes(p.out, p.out_lo_off, base + 3, acc.w * inv);
 }
 
 template <int D>
@@ -489,7 +515,7 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
   if (e != cudaSuccess) return e;
   if ((e = launch_pdl(kern, dim3(grid), dim3(kThreads), ACfg<D>::SMEM, stream, *kv_map, p)) != cudaSuccess)
     return e;
-  const long long n = (long long)R * p.n_q * D;
+  const long long n = (long long)R * p.n_q * (D / 4);
   return launch_pdl(attn_merge_kernel<D>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream, p,
                     row_seq, R);
 }
@@ -499,7 +525,7 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
 size_t attention_smem_bytes(int head_dim) { return head_dim == 64 ? ACfg<64>::SMEM : ACfg<128>::SMEM; }
 
 cudaError_t launch_attention_merge(int head_dim, const AttnParams& p, int R, cudaStream_t stream, const int* row_seq) {
-  const long long n = (long long)R * p.n_q * head_dim;
+  const long long n = (long long)R * p.n_q * (head_dim / 4);
   const dim3 grid(static_cast<unsigned>((n + 255) / 256));
   if (head_dim == 128) return launch_pdl(attn_merge_kernel<128>, grid, dim3(256), 0, stream, p, row_seq, R);
   if (head_dim == 64) return launch_pdl(attn_merge_kernel<64>, grid, dim3(256), 0, stream, p, row_seq, R);

@@ -294,6 +294,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (p.defer_fixup) {  // the fixup kernel sums the parts once this grid is done
+          u += k1 - k0;
+          continue;
+        }
         __threadfence();
         named_sync(1, 4 * kWarp);
         if (m == 0) {
@@ -346,7 +350,87 @@ cudaError_t launch_tc_x(int nt, int xp, const CUtensorMap* a0, const CUtensorMap
                  : launch_tc_nt<EPI, 1>(nt, a0, a1, x, p, grid, stream);
 }
 
+// Deferred stream-K fixup: block (b, chunk) handles the tile holding the
+// first unit of CTA b + 1 of the GEMM's grid, when that CTA boundary cuts the
+// tile and is the tile's first such boundary (the tile's other boundaries
+// exit), for 16-row chunk `chunk` of the tile; 128 threads, thread m = weight
+// row m.  The parts are summed in CTA order, exactly as the last-arriving CTA
+// would, so the result does not depend on the mode.
+template <int EPI, int NT>
+__global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, int P) {
+  constexpr int LD = BM + 4;
+  __shared__ float epi[16 * LD];
+  griddep_launch_dependents();
+  griddep_wait();
+  if (read_status(p.status) != 0) return;
+  const long long total = (long long)p.m_tiles * p.n_tiles * p.kb;
+  const int c = blockIdx.x + 1;
+  const long long ub = (long long)c * total / P;
+  const int tile = static_cast<int>(ub / p.kb);
+  const long long t0 = (long long)tile * p.kb;
+  if (ub == t0) return;                                 // the boundary falls on a tile edge
+  if (c > 1 && (long long)(c - 1) * total / P > t0) return;  // an earlier boundary cuts the same tile
+  const int tn = tile % p.n_tiles;
+  const int rows = min(NT, p.R - tn * NT);
+  const int c0 = blockIdx.y * 16;
+  if (c0 >= rows) return;
+  const int m = threadIdx.x;
+  const int c_first = cta_of_unit(t0, total, P);
+  const int c_last = cta_of_unit(t0 + p.kb - 1, total, P);
+  float v[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) v[n] = 0.f;
+  for (int cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+    float w[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (cc0 + q <= c_last) {
+        const int cc = cc0 + q;
+        const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
+        const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
+        const float* src = p.partials + (size_t)slot * BM * NT + (size_t)c0 * BM + m;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) w[q][n] = __ldcg(src + (size_t)n * BM);
+      }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (cc0 + q <= c_last) {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) v[n] += w[q][n];
+      }
+  }
+#pragma unroll
+  for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
+  __syncthreads();
+  epilogue_rows<EPI, LD>(p, epi, tile / p.n_tiles, tn * NT + c0, min(16, rows - c0), m);
+}
+
+template <int EPI>
+cudaError_t launch_fixup_e(int nt, const GemmParams& p, int grid, cudaStream_t stream) {
+  if (grid < 2) return cudaSuccess;  // one CTA cuts no tile
+  const dim3 g(grid - 1, (nt + 15) / 16);
+  switch (nt) {
+    case 16: return launch_pdl(gemm_tc_fixup_kernel<EPI, 16>, g, dim3(128), 0, stream, p, grid);
+    case 32: return launch_pdl(gemm_tc_fixup_kernel<EPI, 32>, g, dim3(128), 0, stream, p, grid);
+    case 64: return launch_pdl(gemm_tc_fixup_kernel<EPI, 64>, g, dim3(128), 0, stream, p, grid);
+    case 128: return launch_pdl(gemm_tc_fixup_kernel<EPI, 128>, g, dim3(128), 0, stream, p, grid);
+    case 256: return launch_pdl(gemm_tc_fixup_kernel<EPI, 256>, g, dim3(128), 0, stream, p, grid);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (epi) {
+    case EPI_F32: return launch_fixup_e<EPI_F32>(nt, p, grid, stream);
+    case EPI_RESID: return launch_fixup_e<EPI_RESID>(nt, p, grid, stream);
+    case EPI_SWIGLU: return launch_fixup_e<EPI_SWIGLU>(nt, p, grid, stream);
+    case EPI_QKV: return launch_fixup_e<EPI_QKV>(nt, p, grid, stream);
+    case EPI_LMHEAD: return launch_fixup_e<EPI_LMHEAD>(nt, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 int gemm_tc_tile_rows(int R) {
   if (R <= 16) return 16;

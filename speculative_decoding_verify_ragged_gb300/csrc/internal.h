@@ -65,6 +65,10 @@ struct GemmParams {
   int int4 = 0;     // weights are int4 group-32
   float* partials = nullptr;  // stream-K partial tiles [2 * grid, 128 * NT]
   int* counters = nullptr;    // per-tile arrival counters, zero between launches
+  // tcgen05 kernels: leave tiles cut between CTAs as stored parts for the
+  // fixup kernel (one block per cut tile and 16-row chunk) instead of having
+  // the last CTA to arrive sum them
+  int defer_fixup = 0;
   int* status = nullptr;
   EpiParams epi;
 };
@@ -93,6 +97,10 @@ cudaError_t launch_gemm_tc_q4(int epi, int nt, const CUtensorMap* q0, const CUte
                               const CUtensorMap* s1, const CUtensorMap* x, const GemmParams& p, int grid,
                               cudaStream_t stream);
 int gemm_tc_tile_rows(int R);
+// The deferred fixup of a tcgen05 GEMM launched with p.defer_fixup over
+// `grid` CTAs: every tile cut between CTAs, summed in CTA order, then the
+// GEMM's fused epilogue, in parallel over (cut tile, 16-row chunk).
+cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                            const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
