@@ -169,21 +169,27 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   const long long units = (long long)tot_pages * p.n_kv;
   int chunk = static_cast<int>((units + p.target_items - 1) / p.target_items);
   chunk = (max(chunk, 8) + 7) & ~7;  // whole 128-key blocks
-  const int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
+  // a sequence's pages in chunks of `chunk`; a remainder of at most a quarter
+  // chunk joins the last whole chunk (an item of a few leftover pages would pay
+  // a whole item's pipeline fill)
+  int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
+  if (chunks_b > 1 && used - (chunks_b - 1) * chunk <= chunk / 4) --chunks_b;
   int tot_items;
   const int ioff = block_exscan(chunks_b * p.n_kv, &tot_items, s_warp);
   if (slot) {
     p.t.chunks[b] = chunks_b;
     p.t.item_off[b] = ioff;
     if (p.t.items) {
-      // one record per (kv head, chunk) of this slot, in item order
-      for (int g = 0; g < p.n_kv; ++g)
-        for (int c = 0; c < chunks_b; ++c) {
+      // one record per (kv head, chunk) of this slot, item = (kv head) * chunks + chunk
+      for (int c = 0; c < chunks_b; ++c) {
+        const int p0 = c * chunk;
+        const int p1 = c == chunks_b - 1 ? used : p0 + chunk;
+        for (int g = 0; g < p.n_kv; ++g) {
           const int item = ioff + g * chunks_b + c;
-          const int p0 = c * chunk;
-          p.t.items[2 * item] = make_int4(b, g, p0, min(used, p0 + chunk));
+          p.t.items[2 * item] = make_int4(b, g, p0, p1);
           p.t.items[2 * item + 1] = make_int4(L, gam, roff, chunks_b);
         }
+      }
     }
   }
   if (b == 0) {
