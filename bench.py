@@ -56,6 +56,12 @@ def parse():
                     help="subset of the sweep as B:gamma pairs, e.g. 1:7,32:7,128:8")
     ap.add_argument("--gemm-path", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM kernel: 0 auto by row count, 1 mma.sync, 2 tcgen05")
+    ap.add_argument("--timeline", action="store_true",
+                    help="kernel timeline of one step (builds and loads libsdv_trace.so): per kernel the entry, "
+                         "the end of its wait for the kernel ahead and the exit, medians over --steps steps; "
+                         "a markdown table, not a bench line")
+    ap.add_argument("--timeline-shapes", default=None,
+                    help="timeline of the ctx-2048 sweep shapes instead of --workload, as B:gamma pairs")
     return ap.parse_args()
 
 
@@ -804,12 +810,124 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# kernel timeline (libsdv_trace.so): where a live step's time goes, with the
+# kernels overlapping as in the bench (programmatic dependent launch)
+# ---------------------------------------------------------------------------
+
+TIMELINE_ROWS = ["prologue", "QKV GEMM", "attention", "attention merge", "O GEMM", "gate/up GEMM", "down GEMM",
+                 "final RMSNorm", "LM-head GEMM", "acceptance", "sampling", "realignment", "probabilities",
+                 "admission", "planes", "other GEMM"]
+TIMELINE_ORDER = [0, 1, 17, 2, 3, 4, 20, 5, 21, 6, 22, 7, 8, 24, 9, 10, 11]
+
+
+def timeline_name(k):
+    return TIMELINE_ROWS[k] if k < 16 else TIMELINE_ROWS[k - 16] + " fixup"
+
+
+def timeline_of(eng, step, steps):
+    """Medians over `steps` traced steps of (entry, wait done, exit) per
+    kernel, in us from the prologue's entry, and the untraced step time."""
+    import torch
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(steps):
+        step(i)
+    e1.record(s)
+    torch.cuda.synchronize()
+    live_us = e0.elapsed_time(e1) / steps * 1e3
+    table = torch.zeros((32, 3), dtype=torch.int64, device="cuda")
+    eng.set_trace(table)
+    rows = []
+    try:
+        for i in range(steps):
+            table[:, 0:2] = 2 ** 62
+            table[:, 2] = 0
+            step(i)
+            torch.cuda.synchronize()
+            rows.append(table.cpu().numpy().astype(np.float64))
+    finally:
+        eng.set_trace(None)
+    a = np.stack(rows)
+    t0 = a[:, 0, 0]
+    out = []
+    for k in TIMELINE_ORDER:
+        if not (a[:, k, 2] > 0).all():
+            continue
+        rel = lambda col: float(np.median(a[:, k, col] - t0)) / 1e3  # noqa: E731
+        out.append((k, rel(0), rel(1), rel(2)))
+    return live_us, out
+
+
+def print_timeline(title, live_us, out):
+    print(f"\n### {title}: step {live_us:.1f} us (untraced, back to back)\n")
+    print("| kernel | entry (us) | wait done | exit | busy (exit - max(wait done, previous exit)) |")
+    print("|---|---|---|---|---|")
+    prev = 0.0
+    for k, ent, wt, ex in out:
+        print(f"| {timeline_name(k)} | {ent:.1f} | {wt:.1f} | {ex:.1f} | {ex - max(wt, prev):.1f} |")
+        prev = ex
+    print(flush=True)
+
+
+def run_timeline(args):
+    import torch
+    import workloads as wl
+    from workloads import device as wd
+    from speculative_decoding_verify_ragged_gb300 import VerifyEngine, _abi, build
+    build.build(trace=True)
+    torch.cuda.set_device(0)
+    W = wl.make_weights(wl.NINE_B, 2)
+    Wd = wd.weights_to_device(W)
+    if args.timeline_shapes:
+        cases = [(int(x.split(":")[0]), int(x.split(":")[1])) for x in args.timeline_shapes.split(",")]
+    else:
+        cases = [None]
+    for case in cases:
+        if case is None:
+            batch = wl.workload2(extra_pages=8) if args.workload == 2 else wl.workload3(extra_pages=16)
+            wid, title = args.workload, workload_desc(args.workload)["workload"]
+        else:
+            batch = wl.workload4(case[0], case[1], kv_fill="lazy", extra_pages=4 * case[0] + 8)
+            wid, title = 4, f"B = {case[0]}, gamma = {case[1]}, ctx 2048 (R = {batch.R})"
+        gmax = int(batch.gamma_max)
+        eng = VerifyEngine(wd.config(wl.NINE_B, gmax), Wd, max_rows=max(64, batch.R), max_slots=max(16, batch.B),
+                           lib_path=_abi.TRACE_LIB_PATH)
+        eng.set_gemm_path(args.gemm_path)
+        bd = wd.batch_to_device(batch)
+        res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1], probs=True)
+        eng.verify_step(bd, res)
+        assert eng.read_status(res["status"]) == 0
+        wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), wid)
+        bd = wd.batch_to_device(batch)
+        res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1])
+        g = wl.rng(wid, wl.S_U, 1000)
+        U = torch.from_numpy(np.stack([wl.uniform24(g, batch.R) for _ in range(args.steps)])).cuda()
+
+        def step(i):
+            bd["uniforms"] = U[i]
+            eng.verify_step(bd, res)
+
+        for i in range(args.warmup):
+            step(i % args.steps)
+        torch.cuda.synchronize()
+        assert eng.read_status(res["status"]) == 0
+        live_us, out = timeline_of(eng, step, args.steps)
+        assert eng.read_status(res["status"]) == 0
+        print_timeline(title, live_us, out)
+        del eng
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.timeline:
+        run_timeline(args)
     elif args.sweep:
         run_sweep(args)
     elif args.workload == 5:

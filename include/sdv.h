@@ -325,6 +325,21 @@ int sdv_last_cuda_error(void);
 /* Number of kernels the library has launched since load (all contexts). */
 unsigned long long sdv_kernel_launches(void);
 
+/* Step timeline (a library built with -DSDV_TRACE; SDV_ERR_UNSUPPORTED from
+ * any other build).  table: device memory of 32 x 3 unsigned 64-bit words,
+ * owned by the caller, or NULL to stop.  Every kernel the library launches
+ * afterwards stamps the GPU global timer (ns) into its row: word 0 the
+ * earliest CTA entry (atomic min), word 1 the earliest warp past its wait for
+ * the kernel ahead (atomic min), word 2 the latest warp exit (atomic max).
+ * The caller fills words 0-1 with a large value and word 2 with 0 before the
+ * calls it wants to see.  Rows: 0 prologue, 1 QKV, 2 attention, 3 attention
+ * merge, 4 O projection, 5 gate/up, 6 down, 7 final RMSNorm, 8 LM head,
+ * 9 acceptance, 10 sampling, 11 realignment, 12 probabilities, 13 admission,
+ * 14 plane join/split, 15 other GEMMs (sdv_linear), 16 + r the deferred
+ * fixup of the GEMM in row r.  The library must not be in use on another
+ * stream while the table is switched (the address is a device constant). */
+sdv_status sdv_trace_enable(void *table);
+
 #ifdef __cplusplus
 }
 #endif

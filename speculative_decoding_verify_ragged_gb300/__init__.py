@@ -60,9 +60,9 @@ class VerifyEngine:
     workspace is allocated here through torch (the library never allocates).
     """
 
-    def __init__(self, cfg: dict, weights: dict, max_rows: int, max_slots: int):
+    def __init__(self, cfg: dict, weights: dict, max_rows: int, max_slots: int, lib_path: str | None = None):
         import torch
-        self.lib = load_library()
+        self.lib = load_library(lib_path) if lib_path else load_library()
         self.cfg_dict = dict(cfg)
         self.cfg = SdvConfig(*[int(cfg.get(k, 0)) for k in CONFIG_KEYS],
                              float(cfg.get("rms_eps", 1e-6)), float(cfg.get("rope_theta", 1e6)))
@@ -169,6 +169,11 @@ class VerifyEngine:
     def set_sampling(self, mode: int):
         """0 stochastic (rejection sampling, default), 1 greedy (argmax tests and final token)."""
         self._check(self.lib.sdv_set_sampling(self.handle, int(mode)), "sdv_set_sampling")
+
+    def set_trace(self, table):
+        """Point the step timeline at a device int64 tensor [32, 3] (None stops
+        it); only the timeline build libsdv_trace.so accepts it."""
+        self._check(self.lib.sdv_trace_enable(_ptr(table)), "sdv_trace_enable")
 
     def set_attention_path(self, path: int):
         """0 auto, 1 mma.sync, 2 tcgen05 (head_dim 128, <= 32 query vectors per item)."""

@@ -93,14 +93,15 @@ class SdvSchedStats(ctypes.Structure):
                                                  "finished", "admitted")] + [("queued", c_int), ("free_pages", c_int), ("live", c_int)]
 
 
-_lib = None
+TRACE_LIB_PATH = os.path.join(HERE, "libsdv_trace.so")
+_libs: dict = {}
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libsdv.so (built by ``build.py``); raise if it is not there."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load libsdv.so (built by ``build.py``), or another build of it such as
+    the timeline build libsdv_trace.so; raise if it is not there."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library not built: {path} is missing "
                            "(run python -m speculative_decoding_verify_ragged_gb300.build)")
@@ -138,6 +139,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_last_cuda_error.argtypes = []
     lib.sdv_kernel_launches.restype = ctypes.c_ulonglong
     lib.sdv_kernel_launches.argtypes = []
+    lib.sdv_trace_enable.restype = c_int
+    lib.sdv_trace_enable.argtypes = [c_void_p]
     lib.sdv_admit.restype = c_int
     lib.sdv_admit.argtypes = [c_void_p, P(SdvAdmission), c_void_p, c_void_p]
     c_ll = ctypes.c_longlong
@@ -161,7 +164,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_sched_get_stats.argtypes = [c_void_p, P(SdvSchedStats)]
     lib.sdv_sched_slots.restype = c_int
     lib.sdv_sched_slots.argtypes = [c_void_p, P(c_int), P(c_int), P(c_int), P(c_int)]
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 

@@ -17,6 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdv.so")
+BUILD_TRACE = os.path.join(HERE, "_build_trace")
+LIB_TRACE = os.path.join(HERE, "libsdv_trace.so")
 SOURCES = ("api.cu", "gemm.cu", "gemm_tc.cu", "gemm_tc_q4.cu", "gemm_q4.cu", "attention.cu", "attention_tc.cu", "step_kernels.cu", "noalloc.cu", "sched.cpp", "ngram.cpp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -33,8 +35,8 @@ def flags(extra=()):
                    "-I", os.path.join(ROOT, "include")] + list(extra)
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + (".cpp.o" if src.endswith(".cpp") else ".o"))
+def _compile(src: str, extra, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + (".cpp.o" if src.endswith(".cpp") else ".o"))
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + flags(extra)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -44,20 +46,25 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra=(), trace: bool = False) -> str:
+    """Build libsdv.so; trace=True builds libsdv_trace.so instead, the same
+    library with the step-timeline stamps compiled in (sdv_trace_enable)."""
+    build_dir, lib = (BUILD_TRACE, LIB_TRACE) if trace else (BUILD, LIB)
+    extra = tuple(extra) + (("-DSDV_TRACE",) if trace else ())
+    os.makedirs(build_dir, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(verbose=True, extra=sys.argv[1:])
+    args = sys.argv[1:]
+    build(verbose=True, extra=[a for a in args if a != "--trace"], trace="--trace" in args)

@@ -368,6 +368,20 @@ int sdv_last_cuda_error(void) { return g_last_cuda_error; }
 
 unsigned long long sdv_kernel_launches(void) { return g_launches.load(); }
 
+sdv_status sdv_trace_enable(void* table) {
+#ifdef SDV_TRACE
+  auto* t = static_cast<unsigned long long*>(table);
+  cudaError_t (*const set[])(unsigned long long*) = {trace_set_attention, trace_set_attention_tc, trace_set_gemm,
+                                                     trace_set_gemm_q4,   trace_set_gemm_tc,      trace_set_gemm_tc_q4,
+                                                     trace_set_step_kernels};
+  for (auto f : set) SDV_CUDA(f(t));
+  return SDV_OK;
+#else
+  (void)table;
+  return SDV_ERR_UNSUPPORTED;
+#endif
+}
+
 sdv_status sdv_read_status(const int* status, int* host_status, void* stream) {
   if (!status || !host_status) return SDV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

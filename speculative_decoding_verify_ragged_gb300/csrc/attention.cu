@@ -83,13 +83,14 @@ __device__ __forceinline__ Item load_item(const AttnParams& p, int item) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
+  SDV_TRACE_SCOPE(kTrAttention);
   using C = ACfg<D>;
   constexpr int KK = D / 16;  // k16 steps over the head dimension
   constexpr int QT = kAttnQMax * ACfg<D>::QLD;  // elements of one Q tile
   constexpr int NF = D / 8;   // n8 fragments of the output
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
 
   uint8_t* smem = align1024(smem_raw);
@@ -452,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
+  SDV_TRACE_SCOPE(kTrMerge);
   constexpr int DV = D / 4;
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (long long)R * p.n_q * DV) return;
@@ -538,5 +540,7 @@ cudaError_t launch_attention_impl(int head_dim, const CUtensorMap* kv_map, const
   if (head_dim == 64) return launch_d<64>(kv_map, p, grid, R, stream, row_seq);
   return cudaErrorInvalidValue;
 }
+
+SDV_TRACE_UNIT(attention)
 
 }  // namespace sdv

@@ -141,6 +141,7 @@ __device__ __forceinline__ Item load_item(const AttnParams& p, int item) {
 template <int NQ>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmKV, const AttnParams p) {
+  SDV_TRACE_SCOPE(kTrAttention);
   using C = TaCfg<NQ>;
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t t_s0 = tmem, t_o = tmem + 4 * NQ;  // S buffers at columns [0, 4 NQ), O after them
 
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   const bool ok = read_status(p.status) == 0;
   const int total_items = ok ? p.sched[1] : 0;
 
@@ -596,5 +597,7 @@ cudaError_t launch_attention_tc(int nq, const CUtensorMap* kv_map, const AttnPar
   if (nq == 32) return launch_nq<32>(kv_map, p, grid, stream);
   return cudaErrorInvalidValue;
 }
+
+SDV_TRACE_UNIT(attention_tc)
 
 }  // namespace sdv

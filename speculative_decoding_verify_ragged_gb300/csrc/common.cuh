@@ -181,6 +181,74 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// step timeline (builds with -DSDV_TRACE only; other builds compile the
+// stamps away).  Each kernel launch stamps the global timer into its slot of
+// a device table of kTraceSlots x 3 64-bit words: the earliest CTA's entry,
+// the earliest warp past its wait for the kernel ahead, and the latest warp's
+// exit.  The table's address is a per-translation-unit constant set through
+// the unit's trace_set_<unit>() (SDV_TRACE_UNIT); null disables the stamps.
+// ---------------------------------------------------------------------------
+
+constexpr int kTraceSlots = 32;
+enum TraceSlot {
+  kTrPrologue = 0, kTrQkv = 1, kTrAttention = 2, kTrMerge = 3, kTrO = 4, kTrGateUp = 5, kTrDown = 6,
+  kTrFinalNorm = 7, kTrLmHead = 8, kTrAccept = 9, kTrSample = 10, kTrRealign = 11, kTrProbs = 12,
+  kTrAdmit = 13, kTrPlanes = 14, kTrLinear = 15, kTrFixup = 16  // kTrFixup + the GEMM's own slot
+};
+
+#ifdef SDV_TRACE
+static __constant__ unsigned long long* c_trace;
+
+__device__ __forceinline__ unsigned long long trace_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct TraceScope {
+  int slot;
+  __device__ explicit TraceScope(int s) : slot(s) {
+    if (c_trace && threadIdx.x == 0) atomicMin(&c_trace[3 * slot], trace_clock());
+  }
+  __device__ ~TraceScope() {
+    if (c_trace && (threadIdx.x & 31) == 0) atomicMax(&c_trace[3 * slot + 2], trace_clock());
+  }
+};
+
+__device__ __forceinline__ void trace_wait(int slot) {
+  if (c_trace && (threadIdx.x & 31) == 0) atomicMin(&c_trace[3 * slot + 1], trace_clock());
+}
+
+#define SDV_TRACE_SCOPE(slot_expr)          \
+  const int sdv_trace_slot_ = (slot_expr); \
+  ::sdv::TraceScope sdv_trace_scope_(sdv_trace_slot_)
+#define SDV_GRIDDEP_WAIT()                   \
+  do {                                       \
+    ::sdv::griddep_wait();                   \
+    ::sdv::trace_wait(sdv_trace_slot_);      \
+  } while (0)
+#define SDV_TRACE_UNIT(unit)                                          \
+  cudaError_t trace_set_##unit(unsigned long long* table) {           \
+    return cudaMemcpyToSymbol(c_trace, &table, sizeof(table));        \
+  }
+#else
+#define SDV_TRACE_SCOPE(slot_expr) \
+  do {                             \
+  } while (0)
+#define SDV_GRIDDEP_WAIT() ::sdv::griddep_wait()
+#define SDV_TRACE_UNIT(unit)
+#endif
+
+// The timeline slot of a GEMM launch, from its epilogue (the two residual
+// GEMMs told apart by the RMSNorm that only the O projection feeds).
+#define SDV_GEMM_SLOT(kind, params)                                                          \
+  ((kind) == EPI_QKV      ? ::sdv::kTrQkv                                                    \
+   : (kind) == EPI_SWIGLU ? ::sdv::kTrGateUp                                                 \
+   : (kind) == EPI_LMHEAD ? ::sdv::kTrLmHead                                                 \
+   : (kind) == EPI_RESID  ? ((params).epi.norm_gain ? ::sdv::kTrO : ::sdv::kTrDown)          \
+                          : ::sdv::kTrLinear)
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }

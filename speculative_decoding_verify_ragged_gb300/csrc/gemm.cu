@@ -53,6 +53,7 @@ template <int EPI, int NT, int XP>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
+  SDV_TRACE_SCOPE(SDV_GEMM_SLOT(EPI, p));
   using C = Cfg<NT, XP>;
   constexpr int NF = NT / 8;  // n8 fragments
   extern __shared__ uint8_t smem_raw[];
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         weights(cw, j);
         advance(cw);
       }
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       if (read_status(p.status) != 0) {
         // an earlier kernel failed: let the weight copies land, then leave
         for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---------------- consumers ----------------
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;  // the producer drains its copies
   // A timed-out wait marks the CTA dead: no more waiting, no early return (the
   // other consumer warps still meet at the named barriers); outputs are then
@@ -297,5 +298,7 @@ cudaError_t launch_gemm(int epi, int nt, int xp, const CUtensorMap* a0, const CU
     default: return cudaErrorInvalidValue;
   }
 }
+
+SDV_TRACE_UNIT(gemm)
 
 }  // namespace sdv

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_q4_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                    const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
+  SDV_TRACE_SCOPE(SDV_GEMM_SLOT(EPI, p));
   using C = QCfg<NT, XP>;
   constexpr int NF = NT / 8;
   extern __shared__ uint8_t smem_raw[];
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         weights(cw, j);
         advance(cw);
       }
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       if (read_status(p.status) != 0) {
         for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
         for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---------------- consumers ----------------
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   bool dead = false;
   const int g = lane >> 2, t = lane & 3;
@@ -336,5 +337,7 @@ cudaError_t launch_gemm_q4(int epi, int nt, int xp, const CUtensorMap* q0, const
     default: return cudaErrorInvalidValue;
   }
 }
+
+SDV_TRACE_UNIT(gemm_q4)
 
 }  // namespace sdv

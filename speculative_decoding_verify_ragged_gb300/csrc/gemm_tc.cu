@@ -51,6 +51,7 @@ template <int EPI, int NT, int XP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
+  SDV_TRACE_SCOPE(SDV_GEMM_SLOT(EPI, p));
   using C = TcCfg<NT, XP>;
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         weights(cw, j);
         advance(cw);
       }
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       if (read_status(p.status) != 0) {
         for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
         for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       if (read_status(p.status) == 0) {
         constexpr uint32_t idesc = idesc_bf16(BM, NT);
         bool dead = false;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
   const int m = quarter * 32 + lane;     // weight row within the tile
   const int tid = m;
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) == 0) {
     constexpr int LD = C::EPI_LD;
     bool dead = false;
@@ -358,10 +359,11 @@ cudaError_t launch_tc_x(int nt, int xp, const CUtensorMap* a0, const CUtensorMap
 // would, so the result does not depend on the mode.
 template <int EPI, int NT>
 __global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, int P) {
+  SDV_TRACE_SCOPE(kTrFixup + SDV_GEMM_SLOT(EPI, p));
   constexpr int LD = BM + 4;
   __shared__ float epi[16 * LD];
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   const long long total = (long long)p.m_tiles * p.n_tiles * p.kb;
   const int c = blockIdx.x + 1;
@@ -451,5 +453,7 @@ cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const
     default: return cudaErrorInvalidValue;
   }
 }
+
+SDV_TRACE_UNIT(gemm_tc)
 
 }  // namespace sdv

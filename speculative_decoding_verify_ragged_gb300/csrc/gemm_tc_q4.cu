@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
     gemm_tc_q4_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                       const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                       const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
+  SDV_TRACE_SCOPE(SDV_GEMM_SLOT(EPI, p));
   using C = TqCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
       // code stages first: they do not depend on the kernel that writes the activations
       const int pre = my_units < C::QS ? my_units : C::QS;
       for (int j = 0; j < pre; ++j) codes(u_begin + j, j);
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       bool dead = false;
       int qs = pre % C::QS;
       uint32_t qph = pre == C::QS ? 1u : 0u;
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
   if (warp >= 6) {
     // ---------------- converters: codes x scales -> bf16 hi + lo, one row per thread ----------------
     const int row = (warp - 6) * kWarp + lane;
-    griddep_wait();
+    SDV_GRIDDEP_WAIT();
     if (read_status(p.status) != 0) return;
     bool dead = false;
     int qs = 0, cs = 0;
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
   if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      griddep_wait();
+      SDV_GRIDDEP_WAIT();
       if (read_status(p.status) == 0) {
         constexpr uint32_t idesc = idesc_bf16(BM, NT);
         bool dead = false;
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
   const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
   const int m = quarter * 32 + lane;     // weight row within the tile
   const int tid = m;
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) == 0) {
     constexpr int LD = C::EPI_LD;
     bool dead = false;
@@ -482,5 +483,7 @@ cudaError_t launch_gemm_tc_q4(int epi, int nt, const CUtensorMap* q0, const CUte
     default: return cudaErrorInvalidValue;
   }
 }
+
+SDV_TRACE_UNIT(gemm_tc_q4)
 
 }  // namespace sdv

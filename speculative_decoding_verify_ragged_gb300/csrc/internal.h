@@ -101,6 +101,17 @@ int gemm_tc_tile_rows(int R);
 // `grid` CTAs: every tile cut between CTAs, summed in CTA order, then the
 // GEMM's fused epilogue, in parallel over (cut tile, 16-row chunk).
 cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid, cudaStream_t stream);
+
+#ifdef SDV_TRACE
+// Set the timeline table of each translation unit's kernels (SDV_TRACE_UNIT).
+cudaError_t trace_set_attention(unsigned long long* table);
+cudaError_t trace_set_attention_tc(unsigned long long* table);
+cudaError_t trace_set_gemm(unsigned long long* table);
+cudaError_t trace_set_gemm_q4(unsigned long long* table);
+cudaError_t trace_set_gemm_tc(unsigned long long* table);
+cudaError_t trace_set_gemm_tc_q4(unsigned long long* table);
+cudaError_t trace_set_step_kernels(unsigned long long* table);
+#endif
 cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                            const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.

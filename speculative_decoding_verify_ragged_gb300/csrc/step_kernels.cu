@@ -329,10 +329,11 @@ __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
 }
 
 __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const PrologueParams p) {
+  SDV_TRACE_SCOPE(kTrPrologue);
   __shared__ int s_warp[80];
   __shared__ int s_poff[kScanThreads + 1];
   griddep_launch_dependents();
-  griddep_wait();  // the previous step's realignment rewrites page tables and counters
+  SDV_GRIDDEP_WAIT();  // the previous step's realignment rewrites page tables and counters
   // block 0 validates and builds the tables; block r + 1 prepares row r
   if (blockIdx.x == 0) validate_and_tables(p, s_warp, s_poff);
   else embed_row(p, blockIdx.x - 1, s_warp);
@@ -340,24 +341,27 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
 
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h,
                                                       long long lo_off, int H, float eps, const int* status) {
+  SDV_TRACE_SCOPE(kTrFinalNorm);
   __shared__ float s_red[32];
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(status) != 0) return;
   const int r = blockIdx.x;
   norm_row(x + (long long)r * H, gain, h + (long long)r * H, lo_off, H, eps, s_red);
 }
 
 __global__ void join_planes_kernel(const __nv_bfloat16* hi, long long lo_off, float* out, long long n) {
+  SDV_TRACE_SCOPE(kTrPlanes);
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     out[i] = __bfloat162float(hi[i]) + __bfloat162float(hi[i + lo_off]);
 }
 
 __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long long lo_off, long long n) {
+  SDV_TRACE_SCOPE(kTrPlanes);
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
     store_planes(out, lo_off, i, x[i]);
 }
@@ -431,6 +435,7 @@ __device__ __forceinline__ void merge_arg(float& m, int& a, float om, int oa) {
 
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams p) {
+  SDV_TRACE_SCOPE(kTrAccept);
   __shared__ int s_tmp[kAccWarps];
   __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
   __shared__ int s_g[kAccWarps][8];
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     }
   }
   if (threadIdx.x == 0) s_a = gam;
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   __syncthreads();  // s_a is set before any test lowers it
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
@@ -626,6 +631,7 @@ __device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M
 
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams p) {
+  SDV_TRACE_SCOPE(kTrSample);
   __shared__ unsigned long long s_red[2][kAccWarps];
   __shared__ unsigned long long s_scan[kAccWarps];
   __shared__ int s_last, s_mode, s_chunk, s_tok;
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   const int gam = p.draft_lens[b];
   const int r0 = slot_row0(p.draft_lens, b, s_tmp);
   const int g0 = r0 - b;
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   const int a = p.accepted[b];
   const int rf = r0 + a;
@@ -836,8 +842,9 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
 
 __global__ void probs_kernel(const float* z, const float2* row_stats, float* probs, int R, int V,
                              const int* status) {
+  SDV_TRACE_SCOPE(kTrProbs);
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(status) != 0) return;
   const long long n = (long long)R * V;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -852,12 +859,13 @@ __global__ void probs_kernel(const float* z, const float2* row_stats, float* pro
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignParams p) {
+  SDV_TRACE_SCOPE(kTrRealign);
   __shared__ int s_warp[80];
   __shared__ int s_err;
   __shared__ int s_need[kScanThreads], s_src[kScanThreads];
   __shared__ int s_amax;
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.res.status) != 0) return;
   const int b = threadIdx.x;
   const bool slot = b < p.B;
@@ -1086,11 +1094,12 @@ cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, 
 // ---------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kScanThreads) admit_kernel(const AdmitParams p) {
+  SDV_TRACE_SCOPE(kTrAdmit);
   __shared__ int s_warp[80];
   __shared__ int s_err;
   __shared__ int s_need[kScanThreads], s_off[kScanThreads];
   griddep_launch_dependents();
-  griddep_wait();
+  SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   const sdv_admission& a = p.a;
   const int t = threadIdx.x;
@@ -1146,5 +1155,7 @@ cudaError_t launch_admit(const AdmitParams& p, cudaStream_t stream) {
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream) {
   return launch_pdl(realign_kernel, dim3(1), dim3(kScanThreads), 0, stream, p);
 }
+
+SDV_TRACE_UNIT(step_kernels)
 
 }  // namespace sdv

@@ -123,3 +123,11 @@ def test_product_has_no_cpu_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_timeline_needs_the_trace_build():
+    """The product library has no timeline stamps: sdv_trace_enable refuses
+    (without touching the GPU)."""
+    from speculative_decoding_verify_ragged_gb300 import _abi
+    lib = _abi.load_library()
+    assert lib.sdv_trace_enable(None) == _abi.SDV_ERR_UNSUPPORTED
