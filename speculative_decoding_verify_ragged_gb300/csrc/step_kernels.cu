@@ -236,50 +236,78 @@ __device__ void norm_row(const float* x, const __nv_bfloat16* gain, __nv_bfloat1
   }
 }
 
-// Every block r: row r's slot and position (scan of the draft lengths), the
-// embedding row into the fp32 residual stream, the attention pre-norm, the
-// rotary (cos, sin) table and the element offset of the row's K/V in the cache.
-// Row i of a slot writes its K/V at cache slot L + i; its rotary position is
-// L + i in a chain and L + depth(i) in a token tree.
+// Rows of the embedding blocks: four per 1024-thread block, a 256-thread
+// group each.
+constexpr int kRowsPerBlock = 4;
+constexpr int kRowThreads = kScanThreads / kRowsPerBlock;
+
+// Sum over the 256 threads of group g (named barrier 1 + g); s: 8 floats of
+// the group's own.
+__device__ float group_sum_256(float v, float* s, int g) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, w = (threadIdx.x % kRowThreads) >> 5;
+  if (lane == 0) s[w] = v;
+  named_sync(1 + g, kRowThreads);
+  float t = 0.f;
+  for (int i = 0; i < kRowThreads / 32; ++i) t += s[i];
+  named_sync(1 + g, kRowThreads);
+  return t;
+}
+
+// Every embedding block: rows r_first .. r_first + 3, one 256-thread group
+// each: the row's slot and position (one scan of the draft lengths for the
+// block), the embedding row into the fp32 residual stream, the attention
+// pre-norm, the rotary (cos, sin) table and the element offset of the row's
+// K/V in the cache.  Row i of a slot writes its K/V at cache slot L + i; its
+// rotary position is L + i in a chain and L + depth(i) in a token tree.
 // Inputs that would make an access leave its buffer skip the access; block 0
 // reports them in the status word.
-__device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
-  __shared__ int s_b, s_i, s_depth;
-  __shared__ float s_red[32];
+__device__ void embed_rows(const PrologueParams& p, int r_first, int* s_warp) {
+  __shared__ int s_b[kRowsPerBlock], s_i[kRowsPerBlock], s_depth[kRowsPerBlock];
+  __shared__ float s_red[kRowsPerBlock][kRowThreads / 32];
   const int t = threadIdx.x;
   const int gam = t < p.B ? p.draft_lens[t] : 0;
   int tot;
   const int roff = block_exscan(t < p.B ? max(gam, 0) + 1 : 0, &tot, s_warp);
-  if (t == 0) s_b = -1;
+  if (t < kRowsPerBlock) s_b[t] = -1;
   __syncthreads();
-  if (t < p.B && r >= roff && r < roff + max(gam, 0) + 1) {
-    s_b = t;
-    s_i = r - roff;
+  if (t < p.B) {
+    for (int q = 0; q < kRowsPerBlock; ++q) {
+      const int rq = r_first + q;
+      if (rq >= roff && rq < roff + max(gam, 0) + 1) {
+        s_b[q] = t;
+        s_i[q] = rq - roff;
+      }
+    }
   }
   __syncthreads();
-  const int b = s_b;
-  if (b < 0) return;
-  const int slot_pos = p.seq_lens[b] + s_i;  // cache slot of the row's K/V
-  int depth = s_i;
+  // from here on each group works alone (named barrier 1 + g)
+  const int g = t / kRowThreads, u = t % kRowThreads;
+  const int r = r_first + g;
+  const int b = s_b[g];
+  if (b < 0 || r >= p.R) return;
+  const int si = s_i[g];
+  const int slot_pos = p.seq_lens[b] + si;  // cache slot of the row's K/V
+  int depth = si;
   if (p.tree_parents) {
-    if (t == 0) {
+    if (u == 0) {
       // parents up to the root; a malformed table ends the walk (block 0 reports it)
-      const int r0 = r - s_i;
-      int v = s_i, d = 0;
+      const int r0 = r - si;
+      int v = si, d = 0;
       while (v > 0 && d < 64) {
         const int par = p.tree_parents[r0 + v];
         if (par < 0 || par >= v) break;
         v = par;
         ++d;
       }
-      s_depth = d;
+      s_depth[g] = d;
     }
-    __syncthreads();
-    depth = s_depth;
+    named_sync(1 + g, kRowThreads);
+    depth = s_depth[g];
   }
   const int pos = p.seq_lens[b] + depth;  // rotary position
   const int tok = p.tokens[r];
-  if (t == 0) {
+  if (u == 0) {
     const int pi = slot_pos / p.page;
     long long off = 0;
     if (slot_pos >= 0 && pi < p.num_pages[b] && pi < p.max_pages) {
@@ -291,7 +319,7 @@ __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
   }
   // rotary table: angle = pos * inv_freq_j (double), reduced mod 2 pi, then fp32 sincos
   const int half = p.head_dim >> 1;
-  for (int j = t; j < half; j += blockDim.x) {
+  for (int j = u; j < half; j += kRowThreads) {
     const double two_pi = 6.283185307179586476925286766559;
     const double ang = static_cast<double>(pos) * p.inv_freq[j];
     const double red = fma(-rint(ang * (1.0 / two_pi)), two_pi, ang);
@@ -301,30 +329,55 @@ __device__ void embed_row(const PrologueParams& p, int r, int* s_warp) {
     p.t.rope_cs[((long long)r * half + j) * 2 + 1] = sn;
   }
   if (tok < 0 || tok >= p.vocab) return;
-  // embedding row (bf16) -> fp32 residual stream; RMSNorm from registers
-  constexpr int PER = 8;  // values per thread: hidden <= 8 * blockDim
-  const __nv_bfloat16* e = p.emb + (long long)tok * p.H;
-  float* x0 = p.x0 + (long long)r * p.H;
-  float v[PER];
+  // embedding row (bf16, eight per 16-byte load) -> fp32 residual stream;
+  // RMSNorm from registers; the normalised row as bf16 hi + lo planes
+  constexpr int PER8 = 4;  // 8-element vectors per thread: hidden <= 8 * 4 * 256
+  const uint4* e8 = reinterpret_cast<const uint4*>(p.emb + (long long)tok * p.H);
+  const uint4* g8 = reinterpret_cast<const uint4*>(p.gain);
+  const int n8 = p.H >> 3;
+  uint4 raw[PER8], gr[PER8];
+#pragma unroll
+  for (int q = 0; q < PER8; ++q) {
+    const int k = u + q * kRowThreads;
+    raw[q] = k < n8 ? e8[k] : make_uint4(0u, 0u, 0u, 0u);
+    gr[q] = k < n8 ? g8[k] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  auto lo16 = [](uint32_t w) { return __uint_as_float(w << 16); };
+  auto hi16 = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
   float ss = 0.f;
+  float4* x0 = reinterpret_cast<float4*>(p.x0 + (long long)r * p.H);
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int k = t + q * blockDim.x;
-    v[q] = k < p.H ? bf2f(e[k]) : 0.f;
-    ss += v[q] * v[q];
-  }
+  for (int q = 0; q < PER8; ++q) {
+    const int k = u + q * kRowThreads;
+    const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+    float v[8];
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int k = t + q * blockDim.x;
-    if (k < p.H) x0[k] = v[q];
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = lo16(w[i]);
+      v[2 * i + 1] = hi16(w[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += v[i] * v[i];
+    if (k < n8) {
+      x0[2 * k] = make_float4(v[0], v[1], v[2], v[3]);
+      x0[2 * k + 1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
   }
-  ss = block_sum_256(ss, s_red);
+  ss = group_sum_256(ss, s_red[g], g);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
   __nv_bfloat16* h = p.h + (long long)r * p.H;
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const int k = t + q * blockDim.x;
-    if (k < p.H) store_planes(h, p.h_lo_off, k, v[q] * inv * bf2f(p.gain[k]));
+  for (int q = 0; q < PER8; ++q) {
+    const int k = u + q * kRowThreads;
+    if (k >= n8) continue;
+    const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+    const uint32_t gw[4] = {gr[q].x, gr[q].y, gr[q].z, gr[q].w};
+    uint32_t hv[4], lv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      split_bf16x2(lo16(w[i]) * inv * lo16(gw[i]), hi16(w[i]) * inv * hi16(gw[i]), hv[i], lv[i]);
+    *reinterpret_cast<uint4*>(h + 8 * k) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(h + p.h_lo_off + 8 * k) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
   }
 }
 
@@ -336,7 +389,7 @@ __global__ void __launch_bounds__(kScanThreads) prologue_kernel(const ProloguePa
   SDV_GRIDDEP_WAIT();  // the previous step's realignment rewrites page tables and counters
   // block 0 validates and builds the tables; block r + 1 prepares row r
   if (blockIdx.x == 0) validate_and_tables(p, s_warp, s_poff);
-  else embed_row(p, blockIdx.x - 1, s_warp);
+  else embed_rows(p, (blockIdx.x - 1) * kRowsPerBlock, s_warp);
 }
 
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h,
@@ -1027,7 +1080,7 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
 }  // namespace
 
 cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream) {
-  const int grid = p.emb ? p.R + 1 : 1;
+  const int grid = p.emb ? (p.R + kRowsPerBlock - 1) / kRowsPerBlock + 1 : 1;
   return launch_pdl(prologue_kernel, dim3(grid), dim3(kScanThreads), 0, stream, p);
 }
 
@@ -1064,8 +1117,9 @@ static int sms_of_current_device() {
 }
 
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
-  // sampling: about two blocks per SM over the whole batch, never more blocks
-  // per slot than its vocabulary has chunks for (one warp per chunk)
+  // sampling: about two blocks per SM over the whole batch (what the kernel's
+  // registers let an SM hold), never more blocks per slot than its vocabulary
+  // has chunks for (one warp per chunk)
   const int nch = (p.V + kVChunk - 1) / kVChunk;
   const int max_per_slot = (nch + kAccWarps - 1) / kAccWarps;
   const int want = (2 * sms_of_current_device() + p.B - 1) / p.B;
