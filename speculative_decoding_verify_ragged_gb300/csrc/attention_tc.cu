@@ -219,35 +219,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     bool dead = false;
     for (int item = blockIdx.x; item < total_items && !dead; item += gridDim.x) {
       const Item it = load_item(p, item);
-      for (int base = it.p0; base < it.p1 && !dead; base += PAGES) {
-        const int n = min(PAGES, it.p1 - base);
-        const int my_pg = lane < n ? p.page_table[(long long)it.b * p.max_pages + base + lane] : 0;
-        int okw = 1;
-        if (lane == 0) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            set_status(p.status, SDV_ERR_TIMEOUT);
-            okw = 0;
-          } else {
-            mbar_arrive_expect_tx(&full[stage], n * 2 * (16 * 128));
-          }
-        }
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) {
-          dead = true;
-          break;
-        }
-        uint8_t* dst = ring + stage * STAGE_BYTES;
-        for (int j = 0; j < n; ++j) {
-          const int pg = __shfl_sync(0xffffffffu, my_pg, j);
+      // the lanes fetch the page indices of up to four blocks (32 pages) per round trip
+      for (int base32 = it.p0; base32 < it.p1 && !dead; base32 += kWarp) {
+        const int n32 = min(kWarp, it.p1 - base32);
+        const int my_pg = lane < n32 ? p.page_table[(long long)it.b * p.max_pages + base32 + lane] : 0;
+        for (int o = 0; o < n32 && !dead; o += PAGES) {
+          const int n = min(PAGES, n32 - o);
+          int okw = 1;
           if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_5d(dst + h * HALF + j * (16 * 128), &tmKV, &full[stage], h * 64, 0, kv, it.g, pg);
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+              set_status(p.status, SDV_ERR_TIMEOUT);
+              okw = 0;
+            } else {
+              mbar_arrive_expect_tx(&full[stage], n * 2 * (16 * 128));
+            }
           }
-        }
-        if (++stage == NS) {
-          stage = 0;
-          phase ^= 1;
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) {
+            dead = true;
+            break;
+          }
+          uint8_t* dst = ring + stage * STAGE_BYTES;
+          for (int j = 0; j < n; ++j) {
+            const int pg = __shfl_sync(0xffffffffu, my_pg, o + j);
+            if (lane == 0) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_5d(dst + h * HALF + j * (16 * 128), &tmKV, &full[stage], h * 64, 0, kv, it.g, pg);
+            }
+          }
+          if (++stage == NS) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
     }
