@@ -520,12 +520,17 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   }
   if (threadIdx.x == 0) s_a = gam;
   SDV_GRIDDEP_WAIT();
-  if (read_status(p.status) != 0) return;
-  __syncthreads();  // s_a is set before any test lowers it
-  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
+  // the status word and the drafts' logits are loaded together (the logit
+  // loads stay inside the buffer whatever the verdict)
+  const int st = read_status(p.status);
   float zx = 0.f;
   if constexpr (FROM_LOGITS) {
-    if (threadIdx.x < gam) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
+    if (in_range && threadIdx.x < gam && x >= 0 && x < V) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
+  }
+  if (st != 0) return;
+  __syncthreads();  // s_a is set before any test lowers it
+  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
+  if constexpr (FROM_LOGITS) {
     // softmax normalisers of rows r0 .. r0 + gam: each thread merges a slice of
     // the vocabulary tiles of 8 rows at a time (all its loads in flight together)
     for (int n0 = 0; n0 <= gam; n0 += 8) {
@@ -700,15 +705,24 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   const int r0 = slot_row0(p.draft_lens, b, s_tmp);
   const int g0 = r0 - b;
   SDV_GRIDDEP_WAIT();
-  if (read_status(p.status) != 0) return;
+  // the status word, the accepted count and the statistics of every row the
+  // final token may come from are loaded together
+  __shared__ float2 s_rst[64];
+  const int st = read_status(p.status);
   const int a = p.accepted[b];
+  if constexpr (FROM_LOGITS) {
+    if (threadIdx.x <= gam && threadIdx.x < 64 && r0 + (int)threadIdx.x < p.R)
+      s_rst[threadIdx.x] = p.row_stats[r0 + threadIdx.x];
+  }
+  if (st != 0) return;
+  __syncthreads();
   const int rf = r0 + a;
   const float* qrow = a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
   float M = 0.f, S = 1.f;
   if constexpr (FROM_LOGITS) {
-    const float2 st = p.row_stats[rf];
-    M = st.x;
-    S = 1.f / st.y;  // weights as exp(z - M) times the reciprocal of the sum
+    const float2 rs = s_rst[a];
+    M = rs.x;
+    S = 1.f / rs.y;  // weights as exp(z - M) times the reciprocal of the sum
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
 
