@@ -64,8 +64,8 @@ struct TaCfg {
   static constexpr int OFF_Q = OFF_V + VS * STAGE_BYTES;
   static constexpr int OFF_P = OFF_Q + 2 * Q_HALF;
   static constexpr int OFF_RED = OFF_P + 2 * P_BUF;             // two P buffers
-  // per group: [4 quarters][NQ / 2] maxima or sums, 4 flags; then the rescale factors [NQ]
-  static constexpr int RED_BYTES = 2 * (4 * (NQ / 2) * 4 + 16) + NQ * 4 + 64;
+  // per group and block parity: [4 quarters][NQ / 2] maxima or sums, 4 flags
+  static constexpr int RED_BYTES = 2 * 2 * (4 * (NQ / 2) * 4 + 16) + 64;
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int NBAR = 2 * KS + 2 * VS + 2 * 2 + 2 * 2 + 2 + 2;  // k, v, s(2), p(2), q, o (full + empty)
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
@@ -161,7 +161,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* o_full = q_empty + 1;
   uint64_t* o_empty = o_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
-  float* ascale = reinterpret_cast<float*>(smem + C::OFF_RED + 2 * (4 * (NQ / 2) * 4 + 16));  // [NQ]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // stale ring contents must be finite: keys of partial blocks meet weight 0
@@ -369,8 +368,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int t = quarter * 32 + lane;           // key lane of S, head dim of O
     const int col0 = grp * NH;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float* red = reinterpret_cast<float*>(smem + C::OFF_RED + grp * (4 * NH * 4 + 16));  // [4][NH]
-    int* flags = reinterpret_cast<int*>(red + 4 * NH);                                    // [4]
+    // [2 block parities][4][NH] maxima or sums, then 4 flags: consecutive blocks
+    // use alternate halves, so no barrier is needed before the next block writes
+    float* red2 = reinterpret_cast<float*>(smem + C::OFF_RED + grp * 2 * (4 * NH * 4 + 16));
     const int bar_id = 3 + grp;
     const int group = p.n_q / p.n_kv;
     const float scale = kLog2e / sqrtf(static_cast<float>(D));
@@ -434,6 +434,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int p_half = t >> 6, p_chunk = (t & 63) >> 3, p_byte = (t & 7) * 2;
       for (int b = 0; b < nblk; ++b, ++nb) {
         const int sb = nb & 1;
+        float* redb = red2 + sb * (4 * NH + 4);               // this block's half of the scratch
+        int* flags = reinterpret_cast<int*>(redb + 4 * NH);  // [4]
         wait(&s_full[sb], (nb >> 1) & 1);
         float s[NH];
         {
@@ -473,25 +475,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         named_sync(bar_id, 128);
         const bool need = (flags[0] | flags[1] | flags[2] | flags[3]) != 0;
         bool rescale = false;
+        float sc[NH];  // each column's rescale factor of O (every thread holds them all)
         if (need) {
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
             const int wm = __reduce_max_sync(0xffffffffu, f2ord(s[j]));
-            if (lane == 0) red[quarter * NH + j] = ord2f(wm);
+            if (lane == 0) redb[quarter * NH + j] = ord2f(wm);
           }
           named_sync(bar_id, 128);
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            const float bm = fmaxf(fmaxf(red[j], red[NH + j]), fmaxf(red[2 * NH + j], red[3 * NH + j]));
+            const float bm = fmaxf(fmaxf(redb[j], redb[NH + j]), fmaxf(redb[2 * NH + j], redb[3 * NH + j]));
             const float mn = fmaxf(m[j], bm);
             const float av = mn == -INFINITY ? 1.f : exp2f(m[j] - mn);
             rescale |= av != 1.f;
             m[j] = mn;
             l[j] *= av;
-            if (t == 0) ascale[col0 + j] = av;
+            sc[j] = av;
           }
         }
-        named_sync(bar_id, 128);  // flags and red are rewritten by the next block
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           s[j] = exp2f(s[j] - (m[j] == -INFINITY ? 0.f : m[j]));  // the weight p, in place
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float o[NH];
             ld_cols(ta, o);
 #pragma unroll
-            for (int j = 0; j < NH; ++j) o[j] *= ascale[col0 + j];
+            for (int j = 0; j < NH; ++j) o[j] *= sc[j];
             if constexpr (NH == 16) {
               tmem_st16(ta, o);
             } else {
@@ -549,14 +551,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);
       // row sums: per-lane partial sums over the keys, summed over the 128 lanes
+      // (in the half of the scratch the next block will use: its last readers,
+      // two blocks back, have all passed the last block's barrier)
+      float* redr = red2 + (nb & 1) * (4 * NH + 4);
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
         const float ws = warp_sum(l[j]);
-        if (lane == 0) red[quarter * NH + j] = ws;
+        if (lane == 0) redr[quarter * NH + j] = ws;
       }
       named_sync(bar_id, 128);
 #pragma unroll
-      for (int j = 0; j < NH; ++j) l[j] = (red[j] + red[NH + j]) + (red[2 * NH + j] + red[3 * NH + j]);
+      for (int j = 0; j < NH; ++j) l[j] = (redr[j] + redr[NH + j]) + (redr[2 * NH + j] + redr[3 * NH + j]);
       named_sync(bar_id, 128);
       if (!dead) {
         if (it.chunks == 1) {
