@@ -391,8 +391,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
     int nb = 0;     // blocks this CTA has processed
     int kitem = 0;  // items this CTA has processed
+    // Q rows are read from global memory one item ahead (and the item records
+    // two ahead), so an item's start does not wait on a memory round trip
+    constexpr int QPT = NH * (D / 4) / 128;  // float4s of Q per thread
+    static_assert(NH * (D / 4) % 128 == 0, "Q rows split evenly over the group");
+    auto fetch_q = [&](const Item& iq, float4 (&dst)[QPT]) {
+      const int nq = (iq.gamma + 1) * group;
+#pragma unroll
+      for (int q = 0; q < QPT; ++q) {
+        const int idx = t + q * 128;
+        const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
+        dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < nq) {
+          const int i = v / group, h = iq.g * group + (v - i * group);
+          dst[q] = *reinterpret_cast<const float4*>(p.q + ((long long)(iq.r0 + i) * p.n_q + h) * D + ch * 4);
+        }
+      }
+    };
+    float4 qpre[QPT];
+    Item it_cur{}, it_nxt{};
+    if (blockIdx.x < total_items) it_cur = load_item(p, blockIdx.x);
+    if (blockIdx.x + gridDim.x < total_items) it_nxt = load_item(p, blockIdx.x + gridDim.x);
+    if (blockIdx.x < total_items) fetch_q(it_cur, qpre);
     for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++kitem) {
-      const Item it = load_item(p, item);
+      const Item it = it_cur;
       const int nqv = (it.gamma + 1) * group;
       const int nblk = (it.p1 - it.p0 + PAGES - 1) / PAGES;
       // the last key position each of the group's query vectors may see (-1:
@@ -406,13 +428,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // Q rows of this group as bf16 hi + lo (zero rows past nqv), once the
       // previous item's last QK^T has read the buffer
       if (kitem > 0) wait(q_empty, (kitem - 1) & 1);
-      for (int idx = t; idx < NH * (D / 4); idx += 128) {
+#pragma unroll
+      for (int q = 0; q < QPT; ++q) {
+        const int idx = t + q * 128;
         const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
-        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (v < nqv) {
-          const int i = v / group, h = it.g * group + (v - i * group);
-          val = *reinterpret_cast<const float4*>(p.q + ((long long)(it.r0 + i) * p.n_q + h) * D + ch * 4);
-        }
+        const float4 val = qpre[q];
         uint2 hi, lo;
         split_bf16x2(val.x, val.y, hi.x, lo.x);
         split_bf16x2(val.z, val.w, hi.y, lo.y);
@@ -423,6 +443,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
+      // the next item's Q rows (its record is here already) and the record after it
+      if (item + gridDim.x < total_items) fetch_q(it_nxt, qpre);
+      it_cur = it_nxt;
+      if (item + 2 * gridDim.x < total_items) it_nxt = load_item(p, item + 2 * gridDim.x);
 
       float m[NH], l[NH];
 #pragma unroll
