@@ -62,12 +62,13 @@ struct TaCfg {
   static constexpr int P_HALF = 2 * NQ * 128;    // one 64-key half of the 2 NQ P rows
   static constexpr int P_BUF = 2 * P_HALF;
   static constexpr int OFF_Q = OFF_V + VS * STAGE_BYTES;
-  static constexpr int OFF_P = OFF_Q + 2 * Q_HALF;
+  static constexpr int Q_BUF = 2 * Q_HALF;      // one item's Q; two buffers (the next item's is written early)
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BUF;
   static constexpr int OFF_RED = OFF_P + 2 * P_BUF;             // two P buffers
   // per group and block parity: [4 quarters][NQ / 2] maxima or sums, 4 flags
   static constexpr int RED_BYTES = 2 * 2 * (4 * (NQ / 2) * 4 + 16) + 64;
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-  static constexpr int NBAR = 2 * KS + 2 * VS + 2 * 2 + 2 * 2 + 2 + 2;  // k, v, s(2), p(2), q, o (full + empty)
+  static constexpr int NBAR = 2 * KS + 2 * VS + 2 * 2 + 2 * 2 + 2 * 2 + 2;  // k, v, s(2), p(2), q(2), o (full + empty)
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   // S0, S1 and O, each 2 NQ columns (hi part, lo part)
   static constexpr int TMEM_COLS = 6 * NQ <= 32 ? 32 : (6 * NQ <= 64 ? 64 : (6 * NQ <= 128 ? 128 : 256));
@@ -156,9 +157,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* s_empty = s_full + 2;     // [2]
   uint64_t* p_full = s_empty + 2;    // [2]
   uint64_t* p_empty = p_full + 2;    // [2]
-  uint64_t* q_full = p_empty + 2;
-  uint64_t* q_empty = q_full + 1;
-  uint64_t* o_full = q_empty + 1;
+  uint64_t* q_full = p_empty + 2;   // [2]
+  uint64_t* q_empty = q_full + 2;   // [2]
+  uint64_t* o_full = q_empty + 2;
   uint64_t* o_empty = o_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + C::NBAR);
 
@@ -184,8 +185,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&p_full[s], SM_WARPS);
       mbar_init(&p_empty[s], 1);
     }
-    mbar_init(q_full, SM_WARPS);
-    mbar_init(q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], SM_WARPS);
+      mbar_init(&q_empty[s], 1);
+    }
     mbar_init(o_full, 1);
     mbar_init(o_empty, SM_WARPS);
     fence_barrier_init();
@@ -288,7 +291,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
       uint32_t sph[2] = {0, 0};
-      uint32_t qph = 0;
       int blk_total = 0;  // S and P buffers = running block count & 1
       int kitem = 0;      // items this CTA has started
       // PV of one block: 8 pages x (P hi, P lo)
@@ -311,15 +313,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int item = blockIdx.x; item < total_items && !dead; item += gridDim.x) {
         const Item it = load_item(p, item);
         const int nblk = (it.p1 - it.p0 + PAGES - 1) / PAGES;
-        wait(q_full, qph);
-        qph ^= 1;
+        const int qb = kitem & 1;  // this item's Q buffer
+        wait(&q_full[qb], (kitem >> 1) & 1);
         int prev_n = -1;
         for (int b = 0; b < nblk; ++b) {
           const int sb = blk_total & 1;
           wait(&k_full[ks], kph);
           wait(&s_empty[sb], sph[sb] ^ 1);
           const uint32_t kbase = sm + ks * STAGE_BYTES;
-          const uint32_t qbase = sm + C::OFF_Q;
+          const uint32_t qbase = sm + C::OFF_Q + qb * C::Q_BUF;
           const uint32_t d = t_s0 + sb * 2 * NQ;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ks = 0;
             kph ^= 1;
           }
-          if (b == nblk - 1) umma_commit(q_empty);  // the item's last read of Q
+          if (b == nblk - 1) umma_commit(&q_empty[qb]);  // the item's last read of Q
           sph[sb] ^= 1;
           ++blk_total;
           if (b > 0) {
@@ -391,8 +393,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     };
     int nb = 0;     // blocks this CTA has processed
     int kitem = 0;  // items this CTA has processed
-    // Q rows are read from global memory one item ahead (and the item records
-    // two ahead), so an item's start does not wait on a memory round trip
+    // Q buffers alternate by item: item k + 1's Q rows are written at item
+    // k's start (from registers loaded at the end of item k - 1, with item
+    // records read two items ahead), so the MMA can start item k + 1's QK^T
+    // while this group still finishes item k
     constexpr int QPT = NH * (D / 4) / 128;  // float4s of Q per thread
     static_assert(NH * (D / 4) % 128 == 0, "Q rows split evenly over the group");
     auto fetch_q = [&](const Item& iq, float4 (&dst)[QPT]) {
@@ -408,11 +412,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     };
+    auto store_q = [&](const float4 (&src)[QPT], int buf) {
+      uint8_t* qdst = smem + C::OFF_Q + buf * C::Q_BUF;
+#pragma unroll
+      for (int q = 0; q < QPT; ++q) {
+        const int idx = t + q * 128;
+        const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
+        uint2 hi, lo;
+        split_bf16x2(src[q].x, src[q].y, hi.x, lo.x);
+        split_bf16x2(src[q].z, src[q].w, hi.y, lo.y);
+        const int off = (ch >> 4) * C::Q_HALF + v * 128 + ((((ch & 15) >> 1) ^ (v & 7)) << 4) + (ch & 1) * 8;
+        *reinterpret_cast<uint2*>(qdst + off) = hi;
+        *reinterpret_cast<uint2*>(qdst + NQ * 128 + off) = lo;  // lo rows follow the hi rows
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[buf]);
+    };
     float4 qpre[QPT];
     Item it_cur{}, it_nxt{};
-    if (blockIdx.x < total_items) it_cur = load_item(p, blockIdx.x);
-    if (blockIdx.x + gridDim.x < total_items) it_nxt = load_item(p, blockIdx.x + gridDim.x);
-    if (blockIdx.x < total_items) fetch_q(it_cur, qpre);
+    if (blockIdx.x < total_items) {
+      it_cur = load_item(p, blockIdx.x);
+      fetch_q(it_cur, qpre);
+      store_q(qpre, 0);
+    }
+    if (blockIdx.x + gridDim.x < total_items) {
+      it_nxt = load_item(p, blockIdx.x + gridDim.x);
+      fetch_q(it_nxt, qpre);
+    }
     for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++kitem) {
       const Item it = it_cur;
       const int nqv = (it.gamma + 1) * group;
@@ -425,28 +452,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
       for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (tree ? 63 : (col0 + j) / group) : -1;
 
-      // Q rows of this group as bf16 hi + lo (zero rows past nqv), once the
-      // previous item's last QK^T has read the buffer
-      if (kitem > 0) wait(q_empty, (kitem - 1) & 1);
-#pragma unroll
-      for (int q = 0; q < QPT; ++q) {
-        const int idx = t + q * 128;
-        const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
-        const float4 val = qpre[q];
-        uint2 hi, lo;
-        split_bf16x2(val.x, val.y, hi.x, lo.x);
-        split_bf16x2(val.z, val.w, hi.y, lo.y);
-        const int off = (ch >> 4) * C::Q_HALF + v * 128 + ((((ch & 15) >> 1) ^ (v & 7)) << 4) + (ch & 1) * 8;
-        *reinterpret_cast<uint2*>(smem + C::OFF_Q + off) = hi;
-        *reinterpret_cast<uint2*>(smem + C::OFF_Q + NQ * 128 + off) = lo;  // lo rows follow the hi rows
+      // the next item's Q rows into the other buffer, once item k - 1's last
+      // QK^T has read it; then the Q rows and the record of the item after it
+      const int n1 = item + gridDim.x, n2 = n1 + gridDim.x;
+      Item it_n2{};
+      if (n2 < total_items) it_n2 = load_item(p, n2);
+      if (n1 < total_items) {
+        const int buf = (kitem + 1) & 1;
+        if (kitem >= 1) wait(&q_empty[buf], ((kitem - 1) >> 1) & 1);
+        store_q(qpre, buf);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-      // the next item's Q rows (its record is here already) and the record after it
-      if (item + gridDim.x < total_items) fetch_q(it_nxt, qpre);
-      it_cur = it_nxt;
-      if (item + 2 * gridDim.x < total_items) it_nxt = load_item(p, item + 2 * gridDim.x);
 
       float m[NH], l[NH];
 #pragma unroll
@@ -560,6 +575,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[nb & 1]);
       }
+
+      // item k + 2's Q rows, in flight during this item's epilogue, written at the next item's start
+      if (n2 < total_items) fetch_q(it_n2, qpre);
+      it_cur = it_nxt;
+      it_nxt = it_n2;
 
       // the item's O: lane = head dim t, this group's columns
       wait(o_full, kitem & 1);
