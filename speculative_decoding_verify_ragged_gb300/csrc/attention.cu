@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 // Merge of a split sequence's chunk partials, four consecutive head-dim
 // elements of one (row, query head) per thread: one pass over the chunks in
 // chunk order with a running maximum (the unnormalised output and the sum of
-// weights are rescaled whenever the maximum moves), loads of four chunks in
+// weights are rescaled whenever the maximum moves), loads of eight chunks in
 // flight at a time.
 template <int D>
 __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, const int* row_seq, int R) {
@@ -457,13 +457,16 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   constexpr int DV = D / 4;
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
-  if (read_status(p.status) != 0) return;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gid >= (long long)R * p.n_q * DV) return;
   const int d4 = static_cast<int>(gid % DV);
   const int rh = static_cast<int>(gid / DV);
   const int r = rh / p.n_q, h = rh - (rh / p.n_q) * p.n_q;
+  // the status word is read alongside the row's slot (row_seq lies inside
+  // its table whatever the verdict; nothing else is read before the check)
+  const int st = read_status(p.status);
   const int b = row_seq[r];
+  if (st != 0) return;
   const int chunks = p.chunks[b];
   if (chunks == 1) return;
   const int group = p.n_q / p.n_kv;
@@ -476,18 +479,18 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   constexpr long long kO4 = (long long)kAttnQMax * D / 4;  // float4 stride between chunks
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < chunks; c0 += 4) {
-    float2 m[4];
-    float4 o[4];
+  for (int c0 = 0; c0 < chunks; c0 += 8) {
+    float2 m[8];
+    float4 o[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       if (c0 + q < chunks) {
         m[q] = ml[(long long)(c0 + q) * kAttnQMax];
         o[q] = po[(long long)(c0 + q) * kO4];
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 8; ++q) {
       if (c0 + q < chunks && m[q].x != -INFINITY) {
         const float nm = fmaxf(M, m[q].x);
         const float a = M == -INFINITY ? 0.f : exp2f(M - nm);
