@@ -398,9 +398,37 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv
   __shared__ float s_red[32];
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
-  if (read_status(status) != 0) return;
+  // the row is loaded alongside the status word (it lies inside the buffer
+  // whatever the verdict); the sums run over the same elements in the same
+  // order as norm_row
+  constexpr int PER4 = 8;  // float4s per thread: hidden <= 8 * 4 * 256
   const int r = blockIdx.x;
-  norm_row(x + (long long)r * H, gain, h + (long long)r * H, lo_off, H, eps, s_red);
+  const float4* xr = reinterpret_cast<const float4*>(x + (long long)r * H);
+  const int n4 = H >> 2;
+  const int st = read_status(status);
+  float4 v[PER4];
+#pragma unroll
+  for (int q = 0; q < PER4; ++q) {
+    const int k = threadIdx.x + q * 256;
+    v[q] = k < n4 ? xr[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (st != 0) return;
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < PER4; ++q) ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+  ss = block_sum_256(ss, s_red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+  __nv_bfloat16* hr = h + (long long)r * H;
+#pragma unroll
+  for (int q = 0; q < PER4; ++q) {
+    const int k = threadIdx.x + q * 256;
+    if (k < n4) {
+      store_planes(hr, lo_off, 4 * k, v[q].x * inv * bf2f(gain[4 * k]));
+      store_planes(hr, lo_off, 4 * k + 1, v[q].y * inv * bf2f(gain[4 * k + 1]));
+      store_planes(hr, lo_off, 4 * k + 2, v[q].z * inv * bf2f(gain[4 * k + 2]));
+      store_planes(hr, lo_off, 4 * k + 3, v[q].w * inv * bf2f(gain[4 * k + 3]));
+    }
+  }
 }
 
 __global__ void join_planes_kernel(const __nv_bfloat16* hi, long long lo_off, float* out, long long n) {
@@ -933,21 +961,29 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   __shared__ int s_amax;
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
-  if (read_status(p.res.status) != 0) return;
   const int b = threadIdx.x;
   const bool slot = b < p.B;
+  // the status word and the slot's inputs are loaded together (all inside
+  // their buffers whatever the verdict); nothing is written before the check
+  const int st = read_status(p.res.status);
   const int top = *p.num_free_in;
-  if (b == 0) s_err = 0;
-  __syncthreads();
-  int a = 0, L = 0, gam = 0, npg = 0, newlen = 0, need = 0, fin = 0, gen = 0;
+  int a = 0, L = 0, gam = 0, npg = 0, gc = 0, gl = 0;
   if (slot) {
     a = p.accepted[b];
     L = p.seq_lens[b];
     gam = p.draft_lens[b];
     npg = p.num_pages[b];
+    if (p.gen_counts) gc = p.gen_counts[b];
+    if (p.gen_limits) gl = p.gen_limits[b];
+  }
+  if (st != 0) return;
+  if (b == 0) s_err = 0;
+  __syncthreads();
+  int newlen = 0, need = 0, fin = 0, gen = 0;
+  if (slot) {
     newlen = L + a + 1;
-    if (p.gen_counts) gen = p.gen_counts[b] + a + 1;
-    if (p.gen_counts && p.gen_limits) fin = gen >= p.gen_limits[b] ? 1 : 0;
+    if (p.gen_counts) gen = gc + a + 1;
+    if (p.gen_counts && p.gen_limits) fin = gen >= gl ? 1 : 0;
     need = fin ? 0 : (newlen + p.gamma_max + 1 + p.page - 1) / p.page;
     if (need > p.max_pages) atomicCAS(&s_err, 0, SDV_ERR_CAPACITY);
   }
