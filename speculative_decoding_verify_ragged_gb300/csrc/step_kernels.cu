@@ -216,26 +216,6 @@ __device__ float block_sum_256(float v, float* s) {
   return t;
 }
 
-// h = x / sqrt(mean(x^2) + eps) * gain for one row; x fp32; h as bf16 hi + lo
-// planes lo_off elements apart (lo_off == 0: one rounded plane).
-__device__ void norm_row(const float* x, const __nv_bfloat16* gain, __nv_bfloat16* h, long long lo_off, int H,
-                         float eps, float* s_red) {
-  float ss = 0.f;
-  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(x + k);
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  }
-  ss = block_sum_256(ss, s_red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
-  for (int k = threadIdx.x * 4; k < H; k += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(x + k);
-    store_planes(h, lo_off, k, v.x * inv * bf2f(gain[k]));
-    store_planes(h, lo_off, k + 1, v.y * inv * bf2f(gain[k + 1]));
-    store_planes(h, lo_off, k + 2, v.z * inv * bf2f(gain[k + 2]));
-    store_planes(h, lo_off, k + 3, v.w * inv * bf2f(gain[k + 3]));
-  }
-}
-
 // Rows of the embedding blocks: four per 1024-thread block, a 256-thread
 // group each.
 constexpr int kRowsPerBlock = 4;
@@ -399,8 +379,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const __nv
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
   // the row is loaded alongside the status word (it lies inside the buffer
-  // whatever the verdict); the sums run over the same elements in the same
-  // order as norm_row
+  // whatever the verdict); h = x / sqrt(mean(x^2) + eps) * gain as bf16 hi + lo
+  // planes lo_off elements apart (lo_off == 0: one rounded plane)
   constexpr int PER4 = 8;  // float4s per thread: hidden <= 8 * 4 * 256
   const int r = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (long long)r * H);
@@ -457,6 +437,9 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 // integer weight sums of the final row over each chunk (residual and plain);
 // the sequence's last block to finish draws the token.  Integer sums make the
 // draw independent of block order.
+// Stochastic verification from logits runs kernel A's work inside each block
+// of kernel B (one launch, one kernel boundary fewer); greedy verification,
+// token trees and given probabilities keep kernel A.
 // Both read the caller's draft inputs before waiting for the kernel ahead.
 // ---------------------------------------------------------------------------
 
@@ -514,12 +497,81 @@ __device__ __forceinline__ void merge_arg(float& m, int& a, float om, int oa) {
   }
 }
 
+// Softmax normalisers (max, sum of exp) of rows r0 .. r0 + gam from the LM
+// head's per-tile statistics, into s_st, and (greedy) each row's argmax into
+// s_arg; write_rows: also into p.row_stats.  Each thread merges a slice of the
+// vocabulary tiles of 8 rows at a time (all its loads in flight together).
+// The whole block calls it.
+__device__ void merge_slot_stats(const AcceptParams& p, int r0, int gam, float2* s_st, int* s_arg, bool write_rows) {
+  __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
+  __shared__ int s_g[kAccWarps][8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int n0 = 0; n0 <= gam; n0 += 8) {
+    const int nr = min(8, gam + 1 - n0);
+    float M[8], S[8], GM[8];
+    int GA[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      M[q] = -INFINITY;
+      S[q] = 0.f;
+      GM[q] = -INFINITY;
+      GA[q] = 0x7FFFFFFF;
+    }
+#pragma unroll 2
+    for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
+      float2 st[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st[q] = q < nr ? p.tile_stats[(long long)tt * p.stats_ld + r0 + n0 + q] : make_float2(-INFINITY, 0.f);
+      if (p.greedy) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < nr) merge_arg(GM[q], GA[q], st[q].x, p.tile_argmax[(long long)tt * p.stats_ld + r0 + n0 + q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) merge_ms(M[q], S[q], st[q].x, st[q].y);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oM = __shfl_xor_sync(0xffffffffu, M[q], o);
+        const float oS = __shfl_xor_sync(0xffffffffu, S[q], o);
+        merge_ms(M[q], S[q], oM, oS);
+        if (p.greedy) {
+          const float gM = __shfl_xor_sync(0xffffffffu, GM[q], o);
+          const int gA = __shfl_xor_sync(0xffffffffu, GA[q], o);
+          merge_arg(GM[q], GA[q], gM, gA);
+        }
+      }
+      if (lane == 0) {
+        s_m[warp][q] = M[q];
+        s_s[warp][q] = S[q];
+        s_g[warp][q] = GA[q];
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < nr) {
+      float Mr = -INFINITY, Sr = 0.f, Gm = -INFINITY;
+      int Ga = 0x7FFFFFFF;
+      for (int w = 0; w < kAccWarps; ++w) {
+        merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
+        merge_arg(Gm, Ga, s_m[w][threadIdx.x], s_g[w][threadIdx.x]);
+      }
+      s_st[n0 + threadIdx.x] = make_float2(Mr, Sr);
+      if (write_rows) p.row_stats[r0 + n0 + threadIdx.x] = make_float2(Mr, Sr);
+      s_arg[n0 + threadIdx.x] = Ga;
+    }
+    __syncthreads();
+  }
+}
+
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams p) {
   SDV_TRACE_SCOPE(kTrAccept);
   __shared__ int s_tmp[kAccWarps];
-  __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
-  __shared__ int s_g[kAccWarps][8];
+  __shared__ float s_m[kAccWarps];  // given probabilities, greedy: per-warp row maxima
+  __shared__ int s_g[kAccWarps];
   __shared__ float2 s_st[64];
   __shared__ int s_arg[64];
   __shared__ int s_par[64], s_tok[64];  // token trees: parent and token of each node
@@ -559,66 +611,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   __syncthreads();  // s_a is set before any test lowers it
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
   if constexpr (FROM_LOGITS) {
-    // softmax normalisers of rows r0 .. r0 + gam: each thread merges a slice of
-    // the vocabulary tiles of 8 rows at a time (all its loads in flight together)
-    for (int n0 = 0; n0 <= gam; n0 += 8) {
-      const int nr = min(8, gam + 1 - n0);
-      float M[8], S[8], GM[8];
-      int GA[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        M[q] = -INFINITY;
-        S[q] = 0.f;
-        GM[q] = -INFINITY;
-        GA[q] = 0x7FFFFFFF;
-      }
-#pragma unroll 2
-      for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
-        float2 st[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st[q] = q < nr ? p.tile_stats[(long long)tt * p.stats_ld + r0 + n0 + q] : make_float2(-INFINITY, 0.f);
-        if (p.greedy) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (q < nr) merge_arg(GM[q], GA[q], st[q].x, p.tile_argmax[(long long)tt * p.stats_ld + r0 + n0 + q]);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) merge_ms(M[q], S[q], st[q].x, st[q].y);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float oM = __shfl_xor_sync(0xffffffffu, M[q], o);
-          const float oS = __shfl_xor_sync(0xffffffffu, S[q], o);
-          merge_ms(M[q], S[q], oM, oS);
-          if (p.greedy) {
-            const float gM = __shfl_xor_sync(0xffffffffu, GM[q], o);
-            const int gA = __shfl_xor_sync(0xffffffffu, GA[q], o);
-            merge_arg(GM[q], GA[q], gM, gA);
-          }
-        }
-        if (lane == 0) {
-          s_m[warp][q] = M[q];
-          s_s[warp][q] = S[q];
-          s_g[warp][q] = GA[q];
-        }
-      }
-      __syncthreads();
-      if (threadIdx.x < nr) {
-        float Mr = -INFINITY, Sr = 0.f, Gm = -INFINITY;
-        int Ga = 0x7FFFFFFF;
-        for (int w = 0; w < kAccWarps; ++w) {
-          merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
-          merge_arg(Gm, Ga, s_m[w][threadIdx.x], s_g[w][threadIdx.x]);
-        }
-        s_st[n0 + threadIdx.x] = make_float2(Mr, Sr);
-        p.row_stats[r0 + n0 + threadIdx.x] = make_float2(Mr, Sr);
-        s_arg[n0 + threadIdx.x] = Ga;
-      }
-      __syncthreads();
-    }
+    merge_slot_stats(p, r0, gam, s_st, s_arg, true);
   }
   if (p.greedy) {
     // greedy verification (temperature -> 0): draft i + 1 is kept iff it is the
@@ -638,14 +631,14 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
           merge_arg(m, a, om, oa);
         }
         if (lane == 0) {
-          s_m[warp][0] = m;
-          s_g[warp][0] = a;
+          s_m[warp] = m;
+          s_g[warp] = a;
         }
         __syncthreads();
         if (threadIdx.x == 0) {
           float bm = -INFINITY;
           int ba = 0x7FFFFFFF;
-          for (int w = 0; w < kAccWarps; ++w) merge_arg(bm, ba, s_m[w][0], s_g[w][0]);
+          for (int w = 0; w < kAccWarps; ++w) merge_arg(bm, ba, s_m[w], s_g[w]);
           s_arg[n] = ba;
         }
         __syncthreads();
@@ -715,8 +708,13 @@ __device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M
   }
 }
 
-template <bool FROM_LOGITS>
+// FUSED (from logits, stochastic): every block of a slot also merges the
+// slot's row statistics and runs the draft tests itself (the same arithmetic
+// in the same order as the acceptance kernel, so all blocks agree on the
+// accepted count); block 0 stores the count and the row statistics.
+template <bool FROM_LOGITS, bool FUSED>
 __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams p) {
+  static_assert(FROM_LOGITS || !FUSED, "the fused tests read logits");
   SDV_TRACE_SCOPE(kTrSample);
   __shared__ unsigned long long s_red[2][kAccWarps];
   __shared__ unsigned long long s_scan[kAccWarps];
@@ -732,18 +730,51 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   const int gam = p.draft_lens[b];
   const int r0 = slot_row0(p.draft_lens, b, s_tmp);
   const int g0 = r0 - b;
-  SDV_GRIDDEP_WAIT();
-  // the status word, the accepted count and the statistics of every row the
-  // final token may come from are loaded together
   __shared__ float2 s_rst[64];
-  const int st = read_status(p.status);
-  const int a = p.accepted[b];
-  if constexpr (FROM_LOGITS) {
-    if (threadIdx.x <= gam && threadIdx.x < 64 && r0 + (int)threadIdx.x < p.R)
-      s_rst[threadIdx.x] = p.row_stats[r0 + threadIdx.x];
+  int a;
+  if constexpr (FUSED) {
+    __shared__ int s_arg[64], s_a;
+    // the drafts' tokens, q values and uniforms are the caller's: read before
+    // the wait, bounds-checked until the prologue's verdict is known
+    const bool in_range = gam >= 0 && gam < 64 && r0 >= 0 && r0 + gam < p.R;
+    int x = 0;
+    float qk = 0.f, uk = 0.f;
+    if (in_range && threadIdx.x < gam) {
+      x = p.tokens[r0 + threadIdx.x + 1];
+      if (x >= 0 && x < V) {
+        qk = p.draft_probs[(long long)(g0 + threadIdx.x) * V + x];
+        uk = p.uniforms[r0 + threadIdx.x];
+      }
+    }
+    if (threadIdx.x == 0) s_a = gam;
+    SDV_GRIDDEP_WAIT();
+    const int st = read_status(p.status);
+    float zx = 0.f;
+    if (in_range && threadIdx.x < gam && x >= 0 && x < V) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
+    if (st != 0) return;
+    __syncthreads();  // s_a is set before any test lowers it
+    merge_slot_stats(p, r0, gam, s_rst, s_arg, blockIdx.x == 0);
+    if (threadIdx.x < gam) {
+      const int k = threadIdx.x;
+      const float pk = expf(zx - s_rst[k].x) / s_rst[k].y;
+      if (!((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk))) atomicMin(&s_a, k);
+    }
+    __syncthreads();
+    a = s_a;
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.accepted[b] = a;
+  } else {
+    SDV_GRIDDEP_WAIT();
+    // the status word, the accepted count and the statistics of every row the
+    // final token may come from are loaded together
+    const int st = read_status(p.status);
+    a = p.accepted[b];
+    if constexpr (FROM_LOGITS) {
+      if (threadIdx.x <= gam && threadIdx.x < 64 && r0 + (int)threadIdx.x < p.R)
+        s_rst[threadIdx.x] = p.row_stats[r0 + threadIdx.x];
+    }
+    if (st != 0) return;
+    __syncthreads();
   }
-  if (st != 0) return;
-  __syncthreads();
   const int rf = r0 + a;
   const float* qrow = a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
   float M = 0.f, S = 1.f;
@@ -1176,11 +1207,14 @@ cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t 
   const dim3 grid(want < 1 ? 1 : (want > max_per_slot ? max_per_slot : want), p.B);
   cudaError_t e;
   if (from_logits) {
+    // stochastic from logits: the tests run inside the sampling blocks
+    if (!p.greedy && !p.tree_parents)
+      return launch_pdl(sample_kernel<true, true>, grid, dim3(kAccThreads), 0, stream, p);
     if ((e = launch_pdl(accept_kernel<true>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
-    return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<true>, grid, dim3(kAccThreads), 0, stream, p);
+    return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<true, false>, grid, dim3(kAccThreads), 0, stream, p);
   }
   if ((e = launch_pdl(accept_kernel<false>, dim3(p.B), dim3(kAccThreads), 0, stream, p)) != cudaSuccess) return e;
-  return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<false>, grid, dim3(kAccThreads), 0, stream, p);
+  return p.greedy ? cudaSuccess : launch_pdl(sample_kernel<false, false>, grid, dim3(kAccThreads), 0, stream, p);
 }
 
 int accept_chunks(int V) { return (V + kVChunk - 1) / kVChunk; }

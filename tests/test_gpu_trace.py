@@ -10,7 +10,9 @@ from tests import gpu_helpers as gh
 
 pytestmark = pytest.mark.gpu
 
-STEP_ROWS = [0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11]  # prologue .. realignment, mma.sync paths at R = 6
+# prologue .. realignment, mma.sync paths at R = 6; stochastic verification
+# from logits runs the draft tests inside the sampling kernel (no row 9)
+STEP_ROWS = [0, 1, 2, 3, 4, 5, 6, 7, 8, 10, 11]
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +49,7 @@ def test_timeline_rows_and_order(trace_engine):
             assert wt >= prev_exit, (k, wt, prev_exit)
         prev_exit = ex
     # rows of kernels the step does not launch stay as they were set
-    assert (t[12:16, 2] == 0).all() and (t[16:, 2] == 0).all()
+    assert t[9, 2] == 0 and (t[12:16, 2] == 0).all() and (t[16:, 2] == 0).all()
     # stamps stop once the table is switched off
     before = table.clone()
     gh.run_step(eng, wl.workload1(), logits=False, probs=False)
