@@ -11,7 +11,7 @@ Typical use::
 
     eng = VerifyEngine(cfg, weights, max_rows=64, max_slots=8)
     eng.verify_step(batch, result)          # enqueued on the current stream
-    status = VerifyEngine.read_status(result["status"])
+    status = eng.read_status(result["status"])
 """
 from __future__ import annotations
 
@@ -197,11 +197,11 @@ class VerifyEngine:
         self._events = list(events)
         self._check(self.lib.sdv_set_phase_events(self.handle, arr, len(events)), "sdv_set_phase_events")
 
-    @staticmethod
-    def read_status(status, stream=None) -> int:
-        lib = load_library()
+    def read_status(self, status, stream=None) -> int:
+        """The step's status word, read through this engine's library (the
+        timeline build may be the only one present)."""
         out = ctypes.c_int(-1)
-        rc = lib.sdv_read_status(_ptr(status), ctypes.byref(out), _stream(stream))
+        rc = self.lib.sdv_read_status(_ptr(status), ctypes.byref(out), _stream(stream))
         if rc != SDV_OK:
             raise SdvError(rc, "sdv_read_status")
         return int(out.value)

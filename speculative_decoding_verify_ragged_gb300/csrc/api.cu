@@ -69,7 +69,7 @@ static bool config_ok(const sdv_config* c) {
   if (c->weight_format != SDV_WEIGHTS_BF16 && c->weight_format != SDV_WEIGHTS_INT4_G32) return false;
   if (c->hidden % kmul || (c->n_q * c->head_dim) % kmul || c->ffn % kmul) return false;
   if (c->ffn % 64) return false;
-  if (c->vocab > 256 * 4096) return false;  // sampling chunk table
+  if (c->vocab > kMaxSampleChunks * kSampleChunk) return false;  // sampling chunk table
   if (c->hidden > 8 * 1024) return false;   // embedding row held in registers
   return true;
 }

@@ -227,7 +227,9 @@ struct AcceptParams {
   int B = 0, V = 0, R = 0;
 };
 // Acceptance (one block per slot: its rows' softmax normalisers, then the
-// draft tests) and final-token sampling (one block per vocab chunk and slot).
+// draft tests) and final-token sampling (one warp per vocab chunk and slot).
+constexpr int kSampleChunk = 512;         // vocab entries per sampling chunk
+constexpr int kMaxSampleChunks = 2048;    // vocab up to 1M
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream);
 int accept_chunks(int V);
 cudaError_t launch_probs(const float* z, const float2* row_stats, float* probs, int R, int V, const int* status,

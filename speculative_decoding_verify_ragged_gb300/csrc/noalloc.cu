@@ -29,7 +29,7 @@ namespace {
 constexpr int kMaxSlots = 256;
 constexpr int kMaxRows = 2048;
 constexpr int kMaxVocab = 262144;
-constexpr int kChunkLd = (kMaxVocab + 1023) / 1024;  // sampling chunks of 1024 vocab entries
+constexpr int kChunkLd = (kMaxVocab + kSampleChunk - 1) / kSampleChunk;  // sampling chunks
 
 // Layout (bytes, 256-aligned regions).
 constexpr size_t kAlign = 256;

@@ -433,7 +433,7 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 // Kernel A (one block per sequence): the softmax normalisers of the
 // sequence's rows from the LM head's per-tile statistics, then every draft's
 // test in parallel; the first failing u < min(1, p/q) ends the accepted prefix.
-// Kernel B (a few blocks per sequence, one warp per 1024-entry vocab chunk):
+// Kernel B (a few blocks per sequence, one warp per 512-entry vocab chunk):
 // integer weight sums of the final row over each chunk (residual and plain);
 // the sequence's last block to finish draws the token.  Integer sums make the
 // draw independent of block order.
@@ -445,9 +445,9 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
-constexpr int kVChunk = 1024;       // vocab entries per sampling block
+constexpr int kVChunk = kSampleChunk;  // vocab entries per sampling warp
 constexpr int kPerThread = kVChunk / kAccThreads;
-constexpr int kMaxSampleChunks = 1024;  // vocab up to 1M
+constexpr int kChunksPerThread = kMaxSampleChunks / kAccThreads;  // last block's scan
 
 template <bool FROM_LOGITS>
 struct PSource {
@@ -499,65 +499,81 @@ __device__ __forceinline__ void merge_arg(float& m, int& a, float om, int oa) {
 
 // Softmax normalisers (max, sum of exp) of rows r0 .. r0 + gam from the LM
 // head's per-tile statistics, into s_st, and (greedy) each row's argmax into
-// s_arg; write_rows: also into p.row_stats.  Each thread merges a slice of the
-// vocabulary tiles of 8 rows at a time (all its loads in flight together).
-// The whole block calls it.
+// s_arg; write_rows: also into p.row_stats.  The whole block calls it.
+// Rows go 8 (or fewer: rounded up to a power of two, rp) at a time; thread t
+// takes row t % rp over tiles t / rp, t / rp + 256 / rp, ...: kMergeBatch
+// tiles' loads in flight, their maximum first, then each tile's sum scaled by
+// one exponential.  Lanes of one row meet by shuffles, warps through shared
+// memory (maximum first again).  The order is fixed: every block of a slot
+// that calls it gets the same values.
+constexpr int kMergeBatch = 16;
+
 __device__ void merge_slot_stats(const AcceptParams& p, int r0, int gam, float2* s_st, int* s_arg, bool write_rows) {
   __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
   __shared__ int s_g[kAccWarps][8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int n0 = 0; n0 <= gam; n0 += 8) {
     const int nr = min(8, gam + 1 - n0);
-    float M[8], S[8], GM[8];
-    int GA[8];
+    const int lg = nr > 4 ? 3 : (nr > 2 ? 2 : (nr > 1 ? 1 : 0));
+    const int rp = 1 << lg;
+    const int q = threadIdx.x & (rp - 1);
+    const int tstep = kAccThreads >> lg;
+    const bool live = q < nr;
+    const long long col = r0 + n0 + q;
+    float M = -INFINITY, S = 0.f, GM = -INFINITY;
+    int GA = 0x7FFFFFFF;
+    for (int t0 = threadIdx.x >> lg; t0 < p.m_tiles; t0 += kMergeBatch * tstep) {
+      float2 st[kMergeBatch];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      M[q] = -INFINITY;
-      S[q] = 0.f;
-      GM[q] = -INFINITY;
-      GA[q] = 0x7FFFFFFF;
-    }
-#pragma unroll 2
-    for (int tt = threadIdx.x; tt < p.m_tiles; tt += kAccThreads) {
-      float2 st[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st[q] = q < nr ? p.tile_stats[(long long)tt * p.stats_ld + r0 + n0 + q] : make_float2(-INFINITY, 0.f);
+      for (int i = 0; i < kMergeBatch; ++i) {
+        const int tt = t0 + i * tstep;
+        st[i] = live && tt < p.m_tiles ? p.tile_stats[(long long)tt * p.stats_ld + col] : make_float2(-INFINITY, 0.f);
+      }
       if (p.greedy) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < nr) merge_arg(GM[q], GA[q], st[q].x, p.tile_argmax[(long long)tt * p.stats_ld + r0 + n0 + q]);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) merge_ms(M[q], S[q], st[q].x, st[q].y);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float oM = __shfl_xor_sync(0xffffffffu, M[q], o);
-        const float oS = __shfl_xor_sync(0xffffffffu, S[q], o);
-        merge_ms(M[q], S[q], oM, oS);
-        if (p.greedy) {
-          const float gM = __shfl_xor_sync(0xffffffffu, GM[q], o);
-          const int gA = __shfl_xor_sync(0xffffffffu, GA[q], o);
-          merge_arg(GM[q], GA[q], gM, gA);
+        for (int i = 0; i < kMergeBatch; ++i) {
+          const int tt = t0 + i * tstep;
+          if (live && tt < p.m_tiles) merge_arg(GM, GA, st[i].x, p.tile_argmax[(long long)tt * p.stats_ld + col]);
         }
       }
-      if (lane == 0) {
-        s_m[warp][q] = M[q];
-        s_s[warp][q] = S[q];
-        s_g[warp][q] = GA[q];
+      float cm = M;
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i) cm = fmaxf(cm, st[i].x);
+      if (cm > -INFINITY) {
+        // exp2(-inf) = 0 takes out the empty terms (and the old sum while M = -inf)
+        float acc = S * exp2f((M - cm) * kLog2e);
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) acc += st[i].y * exp2f((st[i].x - cm) * kLog2e);
+        S = acc;
+        M = cm;
       }
+    }
+    for (int o = rp; o < 32; o <<= 1) {
+      const float oM = __shfl_xor_sync(0xffffffffu, M, o);
+      const float oS = __shfl_xor_sync(0xffffffffu, S, o);
+      merge_ms(M, S, oM, oS);
+      if (p.greedy) {
+        const float gM = __shfl_xor_sync(0xffffffffu, GM, o);
+        const int gA = __shfl_xor_sync(0xffffffffu, GA, o);
+        merge_arg(GM, GA, gM, gA);
+      }
+    }
+    if (lane < rp) {
+      s_m[warp][lane] = M;
+      s_s[warp][lane] = S;
+      s_g[warp][lane] = GA;
     }
     __syncthreads();
     if (threadIdx.x < nr) {
-      float Mr = -INFINITY, Sr = 0.f, Gm = -INFINITY;
+      float Mr = -INFINITY, Gm = -INFINITY;
       int Ga = 0x7FFFFFFF;
       for (int w = 0; w < kAccWarps; ++w) {
-        merge_ms(Mr, Sr, s_m[w][threadIdx.x], s_s[w][threadIdx.x]);
+        Mr = fmaxf(Mr, s_m[w][threadIdx.x]);
         merge_arg(Gm, Ga, s_m[w][threadIdx.x], s_g[w][threadIdx.x]);
       }
+      float Sr = 0.f;
+      if (Mr > -INFINITY)
+        for (int w = 0; w < kAccWarps; ++w) Sr += s_s[w][threadIdx.x] * exp2f((s_m[w][threadIdx.x] - Mr) * kLog2e);
       s_st[n0 + threadIdx.x] = make_float2(Mr, Sr);
       if (write_rows) p.row_stats[r0 + n0 + threadIdx.x] = make_float2(Mr, Sr);
       s_arg[n0 + threadIdx.x] = Ga;
@@ -848,13 +864,13 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     }
   }
   __syncthreads();
-  // totals of both weight kinds (each thread owns 4 consecutive chunks)
-  unsigned long long own[4];
+  // totals of both weight kinds (each thread owns kChunksPerThread consecutive chunks)
+  unsigned long long own[kChunksPerThread];
   {
     unsigned long long r4 = 0, p4 = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = threadIdx.x * 4 + q;
+    for (int q = 0; q < kChunksPerThread; ++q) {
+      const int k = threadIdx.x * kChunksPerThread + q;
       r4 += k < nch ? s_cs[0][k] : 0ull;
       p4 += k < nch ? s_cs[1][k] : 0ull;
     }
@@ -892,8 +908,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     const unsigned long long* arr = s_cs[s_mode];
     unsigned long long local = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = threadIdx.x * 4 + q;
+    for (int q = 0; q < kChunksPerThread; ++q) {
+      const int k = threadIdx.x * kChunksPerThread + q;
       own[q] = k < nch ? arr[k] : 0ull;
       local += own[q];
     }
@@ -909,8 +925,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     for (int w = 0; w < warp; ++w) run += s_scan[w];
     const unsigned long long T = s_T;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = threadIdx.x * 4 + q;
+    for (int q = 0; q < kChunksPerThread; ++q) {
+      const int k = threadIdx.x * kChunksPerThread + q;
       if (k < nch && run <= T && T < run + own[q]) {
         s_chunk = k;
         s_base = run;
