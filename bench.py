@@ -818,10 +818,16 @@ def run_reference(args):
 TIMELINE_ROWS = ["prologue", "QKV GEMM", "attention", "attention merge", "O GEMM", "gate/up GEMM", "down GEMM",
                  "final RMSNorm", "LM-head GEMM", "acceptance", "sampling", "realignment", "probabilities",
                  "admission", "planes", "other GEMM"]
-TIMELINE_ORDER = [0, 1, 17, 2, 3, 4, 20, 5, 21, 6, 22, 7, 8, 24, 9, 10, 11]
+# points inside the sampling kernel (stochastic verification from logits):
+# first block to reach each, last block to reach it
+SAMPLE_PHASES = {25: "status read", 26: "row statistics merged", 27: "draft tests done",
+                 28: "chunk sums stored", 29: "slot's last block starts", 30: "draw's chunk found"}
+TIMELINE_ORDER = [0, 1, 17, 2, 3, 4, 20, 5, 21, 6, 22, 7, 8, 24, 9, 10, 25, 26, 27, 28, 29, 30, 11]
 
 
 def timeline_name(k):
+    if k in SAMPLE_PHASES:
+        return "- sampling: " + SAMPLE_PHASES[k]
     return TIMELINE_ROWS[k] if k < 16 else TIMELINE_ROWS[k - 16] + " fixup"
 
 
@@ -865,9 +871,16 @@ def print_timeline(title, live_us, out):
     print("| kernel | entry (us) | wait done | exit | busy (exit - max(wait done, previous exit)) |")
     print("|---|---|---|---|---|")
     prev = 0.0
+    prev_point = 0.0
     for k, ent, wt, ex in out:
+        if k in SAMPLE_PHASES:
+            # a point: first block, -, last block, time since the previous point's last block
+            print(f"| {timeline_name(k)} | {ent:.1f} | - | {ex:.1f} | {ex - prev_point:.1f} |")
+            prev_point = ex
+            continue
         print(f"| {timeline_name(k)} | {ent:.1f} | {wt:.1f} | {ex:.1f} | {ex - max(wt, prev):.1f} |")
         prev = ex
+        prev_point = wt
     print(flush=True)
 
 

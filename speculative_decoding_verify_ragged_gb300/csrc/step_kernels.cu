@@ -443,6 +443,29 @@ __global__ void split_planes_kernel(const float* x, __nv_bfloat16* out, long lon
 // Both read the caller's draft inputs before waiting for the kernel ahead.
 // ---------------------------------------------------------------------------
 
+// Timeline rows of points inside the sampling kernel (rows no GEMM fixup
+// uses): status read, row statistics merged, draft tests done, chunk sums
+// stored, the slot's last block starts, the draw's chunk found.  Columns 0
+// and 1: the earliest block to reach the point; column 2: the latest.
+enum SamplePhase {
+  kTrSmpStatus = 25, kTrSmpMerged = 26, kTrSmpTested = 27, kTrSmpChunks = 28, kTrSmpLast = 29, kTrSmpChunk = 30
+};
+#ifdef SDV_TRACE
+#define SDV_TRACE_PHASE(slot)                            \
+  do {                                                   \
+    if (c_trace && threadIdx.x == 0) {                   \
+      const unsigned long long t_ = trace_clock();       \
+      atomicMin(&c_trace[3 * (slot)], t_);               \
+      atomicMin(&c_trace[3 * (slot) + 1], t_);           \
+      atomicMax(&c_trace[3 * (slot) + 2], t_);           \
+    }                                                    \
+  } while (0)
+#else
+#define SDV_TRACE_PHASE(slot) \
+  do {                        \
+  } while (0)
+#endif
+
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
 constexpr int kVChunk = kSampleChunk;  // vocab entries per sampling warp
@@ -506,7 +529,7 @@ __device__ __forceinline__ void merge_arg(float& m, int& a, float om, int oa) {
 // one exponential.  Lanes of one row meet by shuffles, warps through shared
 // memory (maximum first again).  The order is fixed: every block of a slot
 // that calls it gets the same values.
-constexpr int kMergeBatch = 16;
+constexpr int kMergeBatch = 20;  // 1187 tiles (a 151936-entry vocabulary) in two rounds at 8 rows
 
 __device__ void merge_slot_stats(const AcceptParams& p, int r0, int gam, float2* s_st, int* s_arg, bool write_rows) {
   __shared__ float s_m[kAccWarps][8], s_s[kAccWarps][8];
@@ -769,7 +792,9 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     if (in_range && threadIdx.x < gam && x >= 0 && x < V) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
     if (st != 0) return;
     __syncthreads();  // s_a is set before any test lowers it
+    SDV_TRACE_PHASE(kTrSmpStatus);
     merge_slot_stats(p, r0, gam, s_rst, s_arg, blockIdx.x == 0);
+    SDV_TRACE_PHASE(kTrSmpMerged);
     if (threadIdx.x < gam) {
       const int k = threadIdx.x;
       const float pk = expf(zx - s_rst[k].x) / s_rst[k].y;
@@ -777,6 +802,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     }
     __syncthreads();
     a = s_a;
+    SDV_TRACE_PHASE(kTrSmpTested);
     if (blockIdx.x == 0 && threadIdx.x == 0) p.accepted[b] = a;
   } else {
     SDV_GRIDDEP_WAIT();
@@ -847,6 +873,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     }
   }
   __syncthreads();
+  SDV_TRACE_PHASE(kTrSmpChunks);
   if (threadIdx.x == 0) {
     __threadfence();
     const int old = atomicAdd(&p.chunk_count[b], 1);
@@ -855,6 +882,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  SDV_TRACE_PHASE(kTrSmpLast);
 
   // last block of this sequence: pick the mode, the target and the chunk
   {
@@ -935,6 +963,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     }
   }
   __syncthreads();
+  SDV_TRACE_PHASE(kTrSmpChunk);
   if (s_chunk < 0) {
     if (threadIdx.x == 0) {
       set_status(p.status, SDV_ERR_BAD_INPUT);

@@ -48,8 +48,17 @@ def test_timeline_rows_and_order(trace_engine):
         if prev_exit is not None:
             assert wt >= prev_exit, (k, wt, prev_exit)
         prev_exit = ex
+    # points inside the sampling kernel, between its wait and its exit: every
+    # block passes them in order and the slot's last block starts after every
+    # block stored its chunk sums, so the first and the last arrival both rise
+    smp_wait, smp_exit = int(t[10, 1]), int(t[10, 2])
+    prev_first = prev_last = smp_wait
+    for k in range(25, 31):
+        first, last = int(t[k, 0]), int(t[k, 2])
+        assert prev_first <= first <= last <= smp_exit and last >= prev_last, (k, first, last)
+        prev_first, prev_last = first, last
     # rows of kernels the step does not launch stay as they were set
-    assert t[9, 2] == 0 and (t[12:16, 2] == 0).all() and (t[16:, 2] == 0).all()
+    assert t[9, 2] == 0 and (t[12:16, 2] == 0).all() and (t[16:25, 2] == 0).all() and (t[31:, 2] == 0).all()
     # stamps stop once the table is switched off
     before = table.clone()
     gh.run_step(eng, wl.workload1(), logits=False, probs=False)
