@@ -579,7 +579,6 @@ static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_re
   }
   p.res = *r;
   p.B = b->B;
-  p.R = b->R;
   p.page = c->cfg.page_size;
   p.gamma_max = c->cfg.gamma_max;
   p.max_pages = b->max_pages_per_seq;

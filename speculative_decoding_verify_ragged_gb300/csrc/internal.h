@@ -255,7 +255,7 @@ struct RealignParams {
   __nv_bfloat16* kv_pool = nullptr;
   int n_kv = 0, head_dim = 0;
   sdv_result res;
-  int B = 0, R = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0;
+  int B = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0;
 };
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream);
 

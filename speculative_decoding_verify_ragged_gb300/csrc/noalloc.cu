@@ -160,7 +160,6 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
   rp.gen_limits = b->gen_limits;
   rp.res = *r;
   rp.B = b->B;
-  rp.R = b->R;
   rp.page = cfg->page_size;
   rp.gamma_max = cfg->gamma_max;
   rp.max_pages = b->max_pages_per_seq;

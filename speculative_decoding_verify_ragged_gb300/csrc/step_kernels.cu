@@ -1040,33 +1040,19 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   __shared__ int s_need[kScanThreads], s_src[kScanThreads];
   __shared__ int s_amax;
   griddep_launch_dependents();
+  SDV_GRIDDEP_WAIT();
   const int b = threadIdx.x;
   const bool slot = b < p.B;
-  // Before the wait, from the caller's inputs of this step (no kernel writes
-  // them): the draft lengths, each slot's first row (an exclusive scan of
-  // gamma + 1) and its first kPreTokens draft tokens, every read
-  // bounds-checked until the prologue's verdict is known.
-  constexpr int kPreTokens = 8;
-  const int gam = slot ? p.draft_lens[b] : 0;
-  int tot_rows;
-  const int r0 = block_exscan(slot ? gam + 1 : 0, &tot_rows, s_warp);
-  const bool chain = slot && p.res.emitted_tokens && !p.tree_path;
-  int tok[kPreTokens];
-#pragma unroll
-  for (int i = 0; i < kPreTokens; ++i)
-    tok[i] = chain && i < gam && r0 >= 0 && r0 + 1 + i < p.R ? p.tokens[r0 + 1 + i] : 0;
-  SDV_GRIDDEP_WAIT();
-  // the status word and the slot's results and state are loaded together
-  // (all inside their buffers whatever the verdict); nothing is written
-  // before the check
+  // the status word and the slot's inputs are loaded together (all inside
+  // their buffers whatever the verdict); nothing is written before the check
   const int st = read_status(p.res.status);
   const int top = *p.num_free_in;
-  int a = 0, L = 0, npg = 0, gc = 0, gl = 0, ftok = 0;
+  int a = 0, L = 0, gam = 0, npg = 0, gc = 0, gl = 0;
   if (slot) {
     a = p.accepted[b];
     L = p.seq_lens[b];
+    gam = p.draft_lens[b];
     npg = p.num_pages[b];
-    if (p.res.emitted_tokens) ftok = p.final_tokens[b];
     if (p.gen_counts) gc = p.gen_counts[b];
     if (p.gen_limits) gl = p.gen_limits[b];
   }
@@ -1097,17 +1083,15 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
 
   // per-slot outputs that do not depend on the page moves
   if (slot) {
+    const int r0 = p.row_off[b];
     if (res.emitted_tokens) {
       if (p.tree_path) {
         const int* path = p.tree_path + (r0 - b);  // from the slot's draft offset
         for (int i = 0; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + path[i]];
       } else {
-#pragma unroll
-        for (int i = 0; i < kPreTokens; ++i)
-          if (i < a) res.emitted_tokens[eoff + i] = tok[i];
-        for (int i = kPreTokens; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + 1 + i];
+        for (int i = 0; i < a; ++i) res.emitted_tokens[eoff + i] = p.tokens[r0 + 1 + i];
       }
-      res.emitted_tokens[eoff + a] = ftok;
+      res.emitted_tokens[eoff + a] = p.final_tokens[b];
     }
     if (res.emitted_offsets) res.emitted_offsets[b] = eoff;
     if (res.new_seq_lens) res.new_seq_lens[b] = newlen;
@@ -1145,7 +1129,7 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
     const long long head_stride = (long long)p.page * p.head_dim;
     for (int k = 1; k <= s_amax; ++k) {
       // s_need[b]: this depth's source slot of sequence b, or -1
-      if (slot) s_need[b] = k <= a ? L + p.tree_path[r0 - b + k - 1] : -1;
+      if (slot) s_need[b] = k <= a ? L + p.tree_path[p.row_off[b] - b + k - 1] : -1;
       __syncthreads();
       for (int idx = threadIdx.x; idx < p.B * per_row; idx += blockDim.x) {
         const int sb = idx / per_row, e = idx - sb * per_row;
