@@ -855,7 +855,14 @@ def timeline_of(eng, step, steps):
             rows.append(table.cpu().numpy().astype(np.float64))
     finally:
         eng.set_trace(None)
-    a = np.stack(rows)
+    return live_us, timeline_rows(np.stack(rows))
+
+
+def timeline_rows(a):
+    """(row, entry, wait done, exit) per stamped row of the trace tables `a`
+    [steps, 32, 3] (global-timer ns): medians over the steps, in us from the
+    prologue's entry, in TIMELINE_ORDER; a row some step left unstamped is
+    left out."""
     t0 = a[:, 0, 0]
     out = []
     for k in TIMELINE_ORDER:
@@ -863,7 +870,7 @@ def timeline_of(eng, step, steps):
             continue
         rel = lambda col: float(np.median(a[:, k, col] - t0)) / 1e3  # noqa: E731
         out.append((k, rel(0), rel(1), rel(2)))
-    return live_us, out
+    return out
 
 
 def print_timeline(title, live_us, out):
