@@ -58,7 +58,8 @@ def parse():
                     help="GEMM kernel: 0 auto by row count, 1 mma.sync, 2 tcgen05")
     ap.add_argument("--timeline", action="store_true",
                     help="kernel timeline of one step (builds and loads libsdv_trace.so): per kernel the entry, "
-                         "the end of its wait for the kernel ahead and the exit, medians over --steps steps; "
+                         "the end of its wait for the kernel ahead and the exit, and the first and last block "
+                         "at each point inside the sampling kernel, medians over --steps steps; "
                          "a markdown table, not a bench line")
     ap.add_argument("--timeline-shapes", default=None,
                     help="timeline of the ctx-2048 sweep shapes instead of --workload, as B:gamma pairs")
