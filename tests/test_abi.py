@@ -103,6 +103,9 @@ def test_host_errors_without_device(lib):
     assert lib.sdv_admit(None, None, None, None) == _abi.SDV_ERR_INVALID_ARG
     bad = _abi.SdvConfig(256, 4, 3, 64, 768, 1024, 16, 3, 0, 1e-6, 1e6)     # n_q not a multiple of n_kv
     assert lib.sdv_workspace_size(ctypes.byref(bad), 8, 2) == 0
+    # a vocabulary past the sampling chunk table (2048 chunks of 512 entries)
+    big = _abi.SdvConfig(256, 4, 2, 64, 768, 2048 * 512 + 1, 16, 3, 0, 1e-6, 1e6)
+    assert lib.sdv_workspace_size(ctypes.byref(big), 8, 2) == 0
 
 
 def test_product_has_no_cpu_fallback():
