@@ -196,13 +196,15 @@ sdv_status sdv_accept(sdv_ctx *ctx, const float *probs, const sdv_batch *batch,
  * inside a CUDA-graph capture where cudaMalloc is not allowed, a plugin whose
  * host owns every allocation).  Same inputs, rule and outputs as sdv_accept;
  * cfg supplies vocab, page_size, gamma_max (<= 63), n_kv and head_dim.
- * Scratch lives in one static device array of about 1.1 MB that every GPU
+ * Scratch lives in one static device array of about 2.1 MB that every GPU
  * loading the library holds until exit.  Limits: B <= 256, R <= 2048,
  * vocab <= 262144; beyond them SDV_ERR_CAPACITY and nothing is enqueued.
  * The first call on a device looks the array up (cudaGetSymbolAddress) with
- * that device current; make it before any stream capture.  All calls on a
- * device share the array and it keeps the last call's contents (its
- * counters are cleared by every call); calls that overlap on the GPU race. */
+ * that device current; make it before any stream capture.  The address is
+ * looked up again when a later call finds another CUDA context current (after
+ * a cudaDeviceReset), so the first call after a reset is a set-up call too.
+ * All calls on a device share the array and it keeps the last call's contents
+ * (its counters are cleared by every call); calls that overlap on the GPU race. */
 sdv_status sdv_accept_static(const sdv_config *cfg, const float *probs, const sdv_batch *batch,
                              sdv_result *result, void *stream);
 
@@ -315,6 +317,18 @@ sdv_status sdv_set_sampling(sdv_ctx *ctx, int mode);
  * and sdv_attention when the shape does not fit it).  Results agree up to
  * fp32 summation order.  Host-side setting; takes effect on the next call. */
 sdv_status sdv_set_attention_path(sdv_ctx *ctx, int path);
+
+/* Test hook for the device-side failure path; 0 (the default) turns it off.
+ * The pages describe no such call.  With stall_ns > 0, every later call on
+ * this context that runs the step's first kernel (sdv_verify_step,
+ * sdv_accept, sdv_realign, sdv_attention) has that kernel wait on a barrier
+ * that nothing completes, through the same time-bounded wait every pipelined
+ * kernel uses, for stall_ns nanoseconds; the wait gives up, records
+ * SDV_ERR_TIMEOUT in the status word, and every later kernel of the call
+ * returns without touching its outputs.  The context stays usable: set 0 and
+ * the next call runs normally.  Host-side setting; takes effect on the next
+ * call. */
+sdv_status sdv_set_stall_test(sdv_ctx *ctx, unsigned long long stall_ns);
 
 /* Synchronise `stream` and copy the device status word to *host_status. */
 sdv_status sdv_read_status(const int *status, int *host_status, void *stream);

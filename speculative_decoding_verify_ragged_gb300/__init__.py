@@ -179,6 +179,11 @@ class VerifyEngine:
         """0 auto, 1 mma.sync, 2 tcgen05 (head_dim 128, <= 32 query vectors per item)."""
         self._check(self.lib.sdv_set_attention_path(self.handle, int(path)), "sdv_set_attention_path")
 
+    def set_stall_test(self, stall_ns: int):
+        """Test hook: > 0 makes the next calls' first kernel give up a wait that
+        nothing ends after stall_ns and report SDV_ERR_TIMEOUT; 0 turns it off."""
+        self._check(self.lib.sdv_set_stall_test(self.handle, int(stall_ns)), "sdv_set_stall_test")
+
     def set_phase_events(self, events):
         """Record torch.cuda.Event objects at the step's phase boundaries (None = off).
 

@@ -131,6 +131,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sdv_set_sampling.argtypes = [c_void_p, c_int]
     lib.sdv_set_attention_path.restype = c_int
     lib.sdv_set_attention_path.argtypes = [c_void_p, c_int]
+    lib.sdv_set_stall_test.restype = c_int
+    lib.sdv_set_stall_test.argtypes = [c_void_p, ctypes.c_ulonglong]
     lib.sdv_set_phase_events.restype = c_int
     lib.sdv_set_phase_events.argtypes = [c_void_p, P(c_void_p), c_int]
     lib.sdv_read_status.restype = c_int

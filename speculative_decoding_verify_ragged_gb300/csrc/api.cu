@@ -238,6 +238,7 @@ struct sdv_ctx {
   int gemm_path;
   int attn_path;
   int sampling;
+  unsigned long long stall_ns;  // test hook, 0 = off
   cudaEvent_t phase_ev[SDV_PHASES + 1];
   bool timing;
 };
@@ -286,6 +287,7 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
   c->gemm_path = SDV_GEMM_AUTO;
   c->attn_path = SDV_GEMM_AUTO;
   c->sampling = SDV_SAMPLING_STOCHASTIC;
+  c->stall_ns = 0;
   const uint64_t H = cfg->hidden, QD = static_cast<uint64_t>(cfg->n_q) * cfg->head_dim, F = cfg->ffn,
                  V = cfg->vocab;
   const uint64_t NQKV = static_cast<uint64_t>(cfg->n_q + 2 * cfg->n_kv) * cfg->head_dim;
@@ -343,6 +345,12 @@ sdv_status sdv_set_gemm_path(sdv_ctx* ctx, int path) {
 sdv_status sdv_set_sampling(sdv_ctx* ctx, int mode) {
   if (!ctx || (mode != SDV_SAMPLING_STOCHASTIC && mode != SDV_SAMPLING_GREEDY)) return SDV_ERR_INVALID_ARG;
   ctx->sampling = mode;
+  return SDV_OK;
+}
+
+sdv_status sdv_set_stall_test(sdv_ctx* ctx, unsigned long long stall_ns) {
+  if (!ctx) return SDV_ERR_INVALID_ARG;
+  ctx->stall_ns = stall_ns;
   return SDV_OK;
 }
 
@@ -438,6 +446,7 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   p.target_items = c->L.target_items;
   p.rope_theta = c->cfg.rope_theta;
   p.check_tokens = check_tokens && b->tokens ? 1 : 0;
+  p.stall_ns = c->stall_ns;
   return p;
 }
 
@@ -583,6 +592,7 @@ static RealignParams realign_params(sdv_ctx* c, const sdv_batch* b, const sdv_re
   p.gamma_max = c->cfg.gamma_max;
   p.max_pages = b->max_pages_per_seq;
   p.pool_pages = b->num_pool_pages;
+  p.vocab = c->cfg.vocab;
   return p;
 }
 

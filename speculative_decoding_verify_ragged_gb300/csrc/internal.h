@@ -183,6 +183,10 @@ struct PrologueParams {
   int n_kv = 0, head_dim = 0, target_items = 0;
   float rope_theta = 0.f;
   int check_tokens = 1;
+  // test hook (0 = off): block 0 waits this long on a barrier nothing arrives
+  // at, through the bounded wait the pipelined kernels use, and records
+  // SDV_ERR_TIMEOUT when it gives up
+  unsigned long long stall_ns = 0;
   // embedding + attention pre-norm of every row (verify step only; emb = nullptr skips)
   const __nv_bfloat16* emb = nullptr;
   const __nv_bfloat16* gain = nullptr;
@@ -255,7 +259,7 @@ struct RealignParams {
   __nv_bfloat16* kv_pool = nullptr;
   int n_kv = 0, head_dim = 0;
   sdv_result res;
-  int B = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0;
+  int B = 0, page = 0, gamma_max = 0, max_pages = 0, pool_pages = 0, vocab = 0;
 };
 cudaError_t launch_realign(const RealignParams& p, cudaStream_t stream);
 

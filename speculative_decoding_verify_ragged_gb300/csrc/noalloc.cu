@@ -13,10 +13,15 @@
 // sees a host-side stand-in under the array's name, so the device address is
 // fetched with cudaGetSymbolAddress, once per device, with that device
 // current, on the first call made on it (make that first call before any
-// stream capture).  All calls on a device share the array and it keeps what
-// the last call left: the counters that must start at zero are cleared by
-// each call, and calls whose work overlaps on the GPU (different streams
-// without ordering between them) race on it.
+// stream capture).  The address belongs to the device's current CUDA context:
+// it is looked up again when a call finds another context current (after a
+// cudaDeviceReset, say), which makes that call a set-up call too.  All calls
+// on a device share the array and it keeps what the last call left: the
+// counters that must start at zero are cleared by each call, and calls whose
+// work overlaps on the GPU (different streams without ordering between them)
+// race on it.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -47,10 +52,38 @@ constexpr size_t kCounters = kFinal + al(kMaxSlots * 4);  // sampling chunks fin
 constexpr size_t kChunkSums = kCounters + al(kMaxSlots * 4);
 constexpr size_t kScratchBytes = kChunkSums + al((size_t)kMaxSlots * 2 * kChunkLd * 8);
 
+// What every GPU that loads the library holds (about 2.1 MB, nearly all of it
+// the sampling chunk sums: 256 slots x 2 kinds x 512 chunks x 8 bytes).
+static_assert(kScratchBytes <= 2200000, "the documented size of the static scratch");
+
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_dev[64] = {};  // device address of g_scratch per device ordinal
+// device address of g_scratch per device ordinal, and the context it was
+// looked up in
+void* g_scratch_dev[64] = {};
+CUcontext g_scratch_ctx[64] = {};
+
+// The driver's cuCtxGetCurrent, through the runtime's entry-point query (the
+// library does not link the driver library directly).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  }();
+  return fn;
+}
+
+CUcontext current_context() {
+  CUcontext c = nullptr;
+  const auto fn = ctx_get_current_fn();
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 cudaError_t scratch_for_current_device(unsigned char** out) {
   int dev = 0;
@@ -58,11 +91,13 @@ cudaError_t scratch_for_current_device(unsigned char** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_dev[dev]) {
+  const CUcontext now = current_context();
+  if (!g_scratch_dev[dev] || !now || now != g_scratch_ctx[dev]) {
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_scratch);
+    e = cudaGetSymbolAddress(&ptr, g_scratch);  // makes the device's primary context current if none is
     if (e != cudaSuccess) return e;
     g_scratch_dev[dev] = ptr;
+    g_scratch_ctx[dev] = current_context();
   }
   *out = static_cast<unsigned char*>(g_scratch_dev[dev]);
   return cudaSuccess;
@@ -164,6 +199,7 @@ extern "C" sdv_status sdv_accept_static(const sdv_config* cfg, const float* prob
   rp.gamma_max = cfg->gamma_max;
   rp.max_pages = b->max_pages_per_seq;
   rp.pool_pages = b->num_pool_pages;
+  rp.vocab = cfg->vocab;
   if (launch_realign(rp, st) != cudaSuccess) return SDV_ERR_CUDA;
   return SDV_OK;
 }

@@ -73,6 +73,16 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
     s_err = 0;
   }
   __syncthreads();
+  if (p.stall_ns) {
+    // the test hook: a wait that nothing ends, given up after stall_ns
+    __shared__ __align__(8) uint64_t s_never;
+    if (b == 0) {
+      mbar_init(&s_never, 1);
+      fence_barrier_init();
+      if (!mbar_wait(&s_never, 0, p.stall_ns)) set_status(p.status, SDV_ERR_TIMEOUT);
+    }
+    __syncthreads();
+  }
   const bool slot = b < p.B;
   const int gam = slot ? p.draft_lens[b] : 0;
   const int L = slot ? p.seq_lens[b] : 0;
@@ -774,7 +784,14 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   float u_fin = 0.f;
   if (threadIdx.x == 0 && gam >= 0 && r0 >= 0 && r0 + gam < p.R) u_fin = p.uniforms[r0 + gam];
   __shared__ float2 s_rst[64];
-  int a;
+  // A block that finds the status word set skips the work but still counts
+  // itself on the slot's arrival counter below, so the counter returns to
+  // zero whatever the status: another slot's last block may set the word
+  // while this launch runs, and a counter left short would make a later
+  // call's blocks draw from chunk sums not yet written.  The verdict is made
+  // block-uniform by the barrier that reduces it.
+  bool dead;
+  int a = 0;
   if constexpr (FUSED) {
     __shared__ int s_arg[64], s_a;
     // the drafts' tokens, q values and uniforms are the caller's: read before
@@ -794,20 +811,21 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     const int st = read_status(p.status);
     float zx = 0.f;
     if (in_range && threadIdx.x < gam && x >= 0 && x < V) zx = p.z[(long long)(r0 + threadIdx.x) * V + x];
-    if (st != 0) return;
-    __syncthreads();  // s_a is set before any test lowers it
-    SDV_TRACE_PHASE(kTrSmpStatus);
-    merge_slot_stats(p, r0, gam, s_rst, s_arg, blockIdx.x == 0);
-    SDV_TRACE_PHASE(kTrSmpMerged);
-    if (threadIdx.x < gam) {
-      const int k = threadIdx.x;
-      const float pk = expf(zx - s_rst[k].x) / s_rst[k].y;
-      if (!((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk))) atomicMin(&s_a, k);
+    dead = __syncthreads_or(st != 0) != 0;  // also: s_a is set before any test lowers it
+    if (!dead) {
+      SDV_TRACE_PHASE(kTrSmpStatus);
+      merge_slot_stats(p, r0, gam, s_rst, s_arg, blockIdx.x == 0);
+      SDV_TRACE_PHASE(kTrSmpMerged);
+      if (threadIdx.x < gam) {
+        const int k = threadIdx.x;
+        const float pk = expf(zx - s_rst[k].x) / s_rst[k].y;
+        if (!((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk))) atomicMin(&s_a, k);
+      }
+      __syncthreads();
+      a = s_a;
+      SDV_TRACE_PHASE(kTrSmpTested);
+      if (blockIdx.x == 0 && threadIdx.x == 0) p.accepted[b] = a;
     }
-    __syncthreads();
-    a = s_a;
-    SDV_TRACE_PHASE(kTrSmpTested);
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.accepted[b] = a;
   } else {
     SDV_GRIDDEP_WAIT();
     // the status word, the accepted count and the statistics of every row the
@@ -818,16 +836,17 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
       if (threadIdx.x <= gam && threadIdx.x < 64 && r0 + (int)threadIdx.x < p.R)
         s_rst[threadIdx.x] = p.row_stats[r0 + threadIdx.x];
     }
-    if (st != 0) return;
-    __syncthreads();
+    dead = __syncthreads_or(st != 0) != 0;
   }
   const int rf = r0 + a;
-  const float* qrow = a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
+  const float* qrow = !dead && a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
   float M = 0.f, S = 1.f;
   if constexpr (FROM_LOGITS) {
-    const float2 rs = s_rst[a];
-    M = rs.x;
-    S = 1.f / rs.y;  // weights as exp(z - M) times the reciprocal of the sum
+    if (!dead) {
+      const float2 rs = s_rst[a];
+      M = rs.x;
+      S = 1.f / rs.y;  // weights as exp(z - M) times the reciprocal of the sum
+    }
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
 
@@ -838,7 +857,7 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   const float* prow = (FROM_LOGITS ? p.z : p.probs) + (long long)rf * V;
   const bool vec = (V & 3) == 0;  // rows are 16-byte aligned: float4 loads
   constexpr int kVecPerLane = kVChunk / (4 * kWarp);
-  for (int c = blockIdx.x * kAccWarps + warp; c < nch; c += gridDim.x * kAccWarps) {
+  for (int c = blockIdx.x * kAccWarps + warp; !dead && c < nch; c += gridDim.x * kAccWarps) {
     unsigned long long sr = 0, sp = 0;
     const int j0 = c * kVChunk;
     if (vec) {
@@ -882,6 +901,11 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     __threadfence();
     const int old = atomicAdd(&p.chunk_count[b], 1);
     s_last = old == (int)gridDim.x - 1 ? 1 : 0;
+    // the last block of a call that failed anywhere only resets the counter
+    if (s_last && (dead || read_status(p.status) != 0)) {
+      p.chunk_count[b] = 0;
+      s_last = 0;
+    }
   }
   __syncthreads();
   if (!s_last) return;
@@ -1061,6 +1085,14 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   __syncthreads();
   int newlen = 0, need = 0, fin = 0, gen = 0;
   if (slot) {
+    // the accepted count and the final token may come from the caller
+    // (sdv_realign): both are checked before anything is written
+    int ft = 0;
+    if (p.final_tokens) ft = p.final_tokens[b];
+    if (a < 0 || a > gam || ft < 0 || ft >= p.vocab) {
+      atomicCAS(&s_err, 0, SDV_ERR_BAD_INPUT);
+      a = 0;  // keeps the scans below in range; nothing is written on an error
+    }
     newlen = L + a + 1;
     if (p.gen_counts) gen = gc + a + 1;
     if (p.gen_counts && p.gen_limits) fin = gen >= gl ? 1 : 0;
@@ -1080,6 +1112,14 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
   __syncthreads();
   const int err = s_err;
   const sdv_result& res = p.res;
+  if (err) {
+    // no output is touched; the free-stack count passes through unchanged
+    if (b == 0) {
+      set_status(res.status, err);
+      *p.num_free_out = top;
+    }
+    return;
+  }
 
   // per-slot outputs that do not depend on the page moves
   if (slot) {
@@ -1106,13 +1146,6 @@ __global__ void __launch_bounds__(kScanThreads) realign_kernel(const RealignPara
     }
   }
   if (b == 0 && res.emitted_offsets) res.emitted_offsets[p.B] = tot_emit;
-  if (err) {
-    if (b == 0) {
-      set_status(res.status, err);
-      *p.num_free_out = top;
-    }
-    return;
-  }
 
   // token trees: the K/V of the accepted path's node at depth k moves from
   // cache slot L + node to slot L + k, one depth at a time.  A node's index is
