@@ -606,6 +606,96 @@ def realign(seq_lens, accepted, page_table, num_pages, free_pages, num_free: int
 
 
 # ---------------------------------------------------------------------------
+# admission: the refill half of continuous batching
+# ---------------------------------------------------------------------------
+# "Why Static Batching Wastes an RX 9070 XT Agent Swarm and Continuous
+# Batching Wins It Back", section "Continuous batching refills the slot
+# instead of freezing it": a slot freed by a finished sequence takes a waiting
+# one on the very next step, so the batch stays full while work is queued.
+# The pages say nothing about memory; the reading here: a newcomer arrives
+# with its context already cached (prefill is charged outside the step) and
+# must get the pages of its context plus one step of drafts; it is admitted,
+# in arrival order, while a slot is free and the free pages cover it plus one
+# step of growth for every sequence live after it, so the next realignment
+# can never run out of pages.
+
+ERR_BAD_INPUT = 6
+
+
+def pages_for(length: int, gamma_max: int, page: int) -> int:
+    """Pages a sequence of `length` cached positions holds: room for one more
+    verify block of gamma_max + 1 rows."""
+    return -(-(int(length) + gamma_max + 1) // page)
+
+
+def admission_count(queue_ctx, live: int, free_pages: int, slots: int, gamma_max: int, page: int) -> int:
+    """How many queued sequences (contexts in arrival order) enter this step.
+
+    Newcomer n (0-based) is admitted when live + n < slots and
+    pages_for(L_n) + (live + n + 1) * ceil((gamma_max + 1) / page) does not
+    exceed the free pages left after newcomers 0 .. n-1; the first one that
+    fails stops the admission, so arrival order is never overtaken."""
+    growth = -(-(gamma_max + 1) // page)
+    free = int(free_pages)
+    n = 0
+    for L in queue_ctx:
+        if live + n >= slots:
+            break
+        need = pages_for(L, gamma_max, page)
+        if need + (live + n + 1) * growth > free:
+            break
+        free -= need
+        n += 1
+    return n
+
+
+def admit(table: dict, live: int, ctx_lens, out_lens, free_pages, num_free: int, gamma_max: int, page: int,
+          num_live=None, next_src=None, gen_limits_prev=None):
+    """Append admitted sequences to a slot table (the device half of admission).
+
+    ``table``: seq_lens, num_pages, gen_counts, gen_limits [slots] and
+    page_table [slots, max_pages], with the survivors of the last
+    realignment at slots 0 .. live-1.  When ``next_src`` and
+    ``gen_limits_prev`` are given, the survivors' output lengths are first
+    gathered from the table before the compaction.  Newcomer j goes to slot
+    live + j with length ctx_lens[j], generated count 0, output length
+    out_lens[j] and pages_for(ctx_lens[j]) pages popped from the top of the
+    free stack (``free_pages[:num_free]``, top last) in admission order:
+    newcomer j's k-th page is the (sum of earlier newcomers' pages + k)-th
+    page popped; the rest of its row is -1.
+
+    Returns (status, new table, new num_free).  Errors (nothing changes):
+    num_live given and != live, or a negative context (ERR_BAD_INPUT); a row
+    wider than max_pages, or more pages than the stack holds (ERR_CAPACITY).
+    """
+    t = {k: np.array(v, copy=True) for k, v in table.items()}
+    max_pages = t["page_table"].shape[1]
+    ctx_lens = [int(x) for x in ctx_lens]
+    need = [pages_for(L, gamma_max, page) for L in ctx_lens]
+    if num_live is not None and int(num_live) != live:
+        return ERR_BAD_INPUT, t, num_free
+    if any(L < 0 for L in ctx_lens):
+        return ERR_BAD_INPUT, t, num_free
+    if any(n > max_pages for n in need) or sum(need) > num_free:
+        return ERR_CAPACITY, t, num_free
+    if next_src is not None and gen_limits_prev is not None:
+        for j in range(live):
+            t["gen_limits"][j] = gen_limits_prev[int(next_src[j])]
+    top = int(num_free)
+    for j, (L, out) in enumerate(zip(ctx_lens, out_lens)):
+        s = live + j
+        t["seq_lens"][s] = L
+        t["num_pages"][s] = need[j]
+        t["gen_counts"][s] = 0
+        t["gen_limits"][s] = int(out)
+        t["page_table"][s, :] = -1
+        for k in range(need[j]):
+            top -= 1
+            t["page_table"][s, k] = free_pages[top]
+    return OK, t, top
+
+
+# ---------------------------------------------------------------------------
 # the whole step
 # ---------------------------------------------------------------------------
 

@@ -48,3 +48,15 @@ def nine_b_int4():
     from workloads import device as wd
     W = wl.make_weights(wl.NINE_B, 5, fmt="int4")
     return W, wd.weights_to_device(W)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """How often the GPU step comparisons explained a row by another bf16
+    rounding at a tie (tiny model only; the 9B-class checks never do)."""
+    mod = sys.modules.get("tests.gpu_helpers")
+    if mod is None:
+        return
+    used = getattr(mod, "FLIPS_USED", [])
+    nine_b = sum(1 for h, _, _ in used if h > 256)
+    terminalreporter.write_line(f"parity: other roundings used {len(used)} (tiny model {len(used) - nine_b}, "
+                                f"9B-class layer {nine_b})")

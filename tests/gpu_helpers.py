@@ -58,12 +58,26 @@ def to_numpy(d: dict) -> dict:
 # belong to (one K/V head, or the row of h3): fp32 activations enter the
 # tensor cores as bf16 hi + lo (16 significant bits) and fp32 accumulation
 # adds less; the largest disagreement seen on the 9B-class layer is 2^-17.
-# Any bf16 value that rounds from a point within TIE_WINDOW * rms of the exact
-# value is a valid result: the nearest one, its other neighbour when the
-# exact value sits near a tie, and, for elements much smaller than the rms,
-# values a few spacings away.  The window is 8x the largest seen error.
-TIE_WINDOW = 2.0 ** -14
+#
+# KV_WINDOW: a K/V element in the cache is valid when it is a bf16 rounding of
+# a point within KV_WINDOW * rms of the oracle's exact value (4x the largest
+# error seen): the nearest rounding, or its other neighbour when the exact
+# value sits that close to a tie.
+#
+# TIE_WINDOW: on the tiny model only, a row outside the logit tolerance may be
+# explained by ONE such other rounding per sequence, of an element whose exact
+# value lies within the largest seen error (2^-17 rms) of a tie.  The tiny
+# model needs this because a sequence at position 0 attends to its own V row
+# alone, so one ulp of V moves its logits by about 1 % of their rms.  On the
+# 9B-class layer one ulp moves the logits by ~1e-4 rms, so no 9B test may use
+# it: there every row must be inside the tolerance as computed.
+KV_WINDOW = 2.0 ** -15
+TIE_WINDOW = 2.0 ** -17
 MAX_CANDIDATES = 12
+
+# every other rounding the checker used: (model hidden size, slot, key); the
+# session summary prints them (conftest.pytest_terminal_summary)
+FLIPS_USED: list = []
 
 
 def _tie_distance(pre, axis):
@@ -76,7 +90,7 @@ def _tie_distance(pre, axis):
 
 def check_kv_written(batch, fw, pool, pt_before):
     """Each verified row's K/V sits in its page at position L + i and is a bf16
-    rounding of a point within TIE_WINDOW * rms of the oracle's exact value.
+    rounding of a point within KV_WINDOW * rms of the oracle's exact value.
     Returns the number of elements that differ from the nearest rounding."""
     page = batch.dims["page"]
     offs = wl.row_offsets(batch.draft_lens)
@@ -88,7 +102,7 @@ def check_kv_written(batch, fw, pool, pt_before):
         for kind, kv in (("k", 0), ("v", 1)):
             got = o.bf16_to_f64(pool[pg, :, kv, pos % page, :])
             pre = fw[kind + "_pre"][n]
-            e = TIE_WINDOW * np.sqrt(np.mean(pre ** 2, axis=1, keepdims=True))
+            e = KV_WINDOW * np.sqrt(np.mean(pre ** 2, axis=1, keepdims=True))
             ok = (o.round_bf16(pre - e) <= got) & (got <= o.round_bf16(pre + e))
             assert ok.all(), (kind, b, pos, np.argwhere(~ok)[:4])
             other += int(np.count_nonzero(got != o.round_bf16(pre)))
@@ -105,13 +119,21 @@ def _row_errors(z_gpu, p_gpu, z_or, p_or, tol):
     return dz, bad
 
 
+def flips_allowed(dims) -> bool:
+    """Only the tiny model may explain a row by another rounding at a tie."""
+    return dims["hidden"] <= 256
+
+
 def compare_step(batch, W, fw, z_gpu, p_gpu=None):
     """Logits within LOGIT_TOL_REL_RMS * rms and probabilities within PROB_TOL_ABS
-    (and PROB_TOL_REL) of the oracle.  A sequence with a row outside must match,
-    within the same tolerances, the oracle's result under some choice of the
-    other rounding for K/V/h3 values inside the tie window (its rows up to the
-    failing one, the nearest MAX_CANDIDATES ties): a result that is just as
-    valid.  Returns (probs the acceptance check should use, {slot: flips}).
+    (and PROB_TOL_REL) of the oracle, row by row.
+
+    9B-class layer: every row must pass as computed.  Tiny model: a sequence
+    with a row outside may instead match, within the same tolerances, the
+    oracle re-run with ONE K/V or h3 value of that sequence rounded to its
+    other bf16 neighbour, where the exact value lies within TIE_WINDOW * rms of
+    a tie (so the GPU's own arithmetic error could have rounded it either
+    way).  Returns (probs the acceptance check should use, {slot: flip}).
     """
     z_or, p_or = fw["logits"], fw["probs"]
     rms = float(np.sqrt(np.mean(z_or ** 2)))
@@ -121,10 +143,13 @@ def compare_step(batch, W, fw, z_gpu, p_gpu=None):
     explained = {}
     if not bad.any():
         return p_valid, explained
+    rows_bad = np.nonzero(bad)[0]
+    assert flips_allowed(batch.dims), (f"{len(rows_bad)} rows outside tolerance: max |dz| "
+                                       f"{dz.max() / rms:.3e} rms (rows {rows_bad[:8].tolist()})")
     offs = wl.row_offsets(batch.draft_lens)
     row_slot = np.repeat(np.arange(batch.B), np.asarray(batch.draft_lens) + 1)
-    slots = sorted(set(int(row_slot[r]) for r in np.nonzero(bad)[0]))
-    assert len(slots) <= max(2, batch.B // 4), f"{len(slots)} sequences outside tolerance: {dz.max() / rms:.3e} rms"
+    slots = sorted(set(int(row_slot[r]) for r in rows_bad))
+    assert len(slots) <= max(1, batch.B // 8), f"{len(slots)} sequences outside tolerance: {dz.max() / rms:.3e} rms"
     args = (batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens, batch.tokens)
     for b in slots:
         r0, r1 = int(offs[b]), int(offs[b + 1])
@@ -142,28 +167,23 @@ def compare_step(batch, W, fw, z_gpu, p_gpu=None):
                 cands.append((float(d[j]), ("h3", r, int(j))))
         cands = [c for _, c in sorted(cands)[:MAX_CANDIDATES]]
         assert cands, f"slot {b}: rows {bad_rows} outside tolerance ({dz[bad_rows].max() / rms:.3e} rms), no tie in reach"
+        # one flip: the candidate whose effect on the failing rows best matches the GPU's difference
         sel = [r - r0 for r in bad_rows]
         err = (z_gpu[bad_rows].astype(np.float64) - z_or[bad_rows]).ravel()
-        eff = np.stack([(o.forward(*args, slots=[b], flips={c})["logits"][sel] - z_or[bad_rows]).ravel()
-                        for c in cands])
-        # fewest flips first: the first choice that leaves the rows well inside the
-        # tolerance (half of it, before the exact re-run), else the closest one
         best, best_res = None, np.inf
-        for mask in sorted(range(1, 1 << len(cands)), key=lambda m: (bin(m).count("1"), m)):
-            pick = [i for i in range(len(cands)) if mask >> i & 1]
-            res = float(np.max(np.abs(err - eff[pick].sum(0))))
+        for c in cands:
+            eff = (o.forward(*args, slots=[b], flips={c})["logits"][sel] - z_or[bad_rows]).ravel()
+            res = float(np.max(np.abs(err - eff)))
             if res < best_res:
-                best, best_res = pick, res
-            if res <= 0.5 * tol:
-                break
-        flips = {cands[i] for i in best}
-        alt = o.forward(*args, slots=[b], flips=flips)
+                best, best_res = c, res
+        alt = o.forward(*args, slots=[b], flips={best})
         _, still = _row_errors(z_gpu[r0:r1], None if p_gpu is None else p_gpu[r0:r1], alt["logits"],
                                alt["probs"], tol)
         assert not still.any(), (f"slot {b}: rows {bad_rows} outside tolerance ({dz[bad_rows].max() / rms:.3e} rms) "
-                                 f"under every tie choice tried")
+                                 f"under every single tie choice tried")
         p_valid[r0:r1] = alt["probs"]
-        explained[b] = sorted(flips)
+        explained[b] = best
+        FLIPS_USED.append((int(batch.dims["hidden"]), b, best))
     return p_valid, explained
 
 
@@ -176,7 +196,16 @@ def _ambiguous(p, q, u, rel=DECISION_REL):
 def check_acceptance(batch: wl.Batch, p_or: np.ndarray, acc_gpu, fin_gpu):
     """Acceptance counts and final tokens against the oracle, up to decision margins.
 
-    Returns the number of slots whose result had to be judged by margin.
+    For every slot, with a the GPU's accepted count: each draft before a must
+    be one the oracle accepts and draft a (when a < gamma) one it rejects,
+    unless the oracle's margin at that draft is within DECISION_REL (then
+    either verdict is valid).  The final token must be the oracle's draw at
+    row a in the mode a implies (the residual after a rejection, p for the
+    bonus), or, when it differs, sit at the oracle's CDF point within
+    DECISION_REL of the row's mass.  Nothing is skipped: a slot whose count
+    was judged by margin still has its final token checked at the GPU's count.
+
+    Returns the number of slots that needed a margin.
     """
     p32 = p_or.astype(np.float32)
     roff = wl.row_offsets(batch.draft_lens)
@@ -187,39 +216,72 @@ def check_acceptance(batch: wl.Batch, p_or: np.ndarray, acc_gpu, fin_gpu):
         r0 = int(roff[b])
         drafts = batch.tokens[r0 + 1: r0 + 1 + g]
         q = batch.draft_probs[int(goff[b]): int(goff[b]) + g]
-        u = batch.uniforms[r0: r0 + g + 1]
-        a_or, t_or = o.accept_and_sample(p32[r0: r0 + g + 1], q, drafts, u)
-        amb = None
-        for i in range(g):
-            x = int(drafts[i])
-            if _ambiguous(float(p32[r0 + i, x]), float(q[i, x]), float(u[i])):
-                amb = i
-                break
-            if not o.accepts(p32[r0 + i, x], q[i, x], u[i]):
-                break
+        u = np.asarray(batch.uniforms[r0: r0 + g + 1], dtype=np.float32)
         a_g = int(acc_gpu[b])
-        if amb is None or amb > a_or:
-            assert a_g == a_or, f"slot {b}: accepted {a_g} vs oracle {a_or}"
-        else:
-            judged += 1
-            assert a_g >= amb, f"slot {b}: accepted {a_g} before the ambiguous draft {amb}"
-            continue
-        t_g = int(fin_gpu[b])
-        if t_g == t_or:
-            continue
-        # the GPU's token must sit at the oracle's CDF point within the probability tolerance
-        if a_or < g:
-            w = np.maximum(np.float32(0), p32[r0 + a_or] - q[a_or])
+        assert 0 <= a_g <= g, f"slot {b}: accepted {a_g} outside 0..{g}"
+        by_margin = False
+        for i in range(min(a_g + 1, g)):
+            x = int(drafts[i])
+            keep = o.accepts(p32[r0 + i, x], q[i, x], u[i])
+            if keep != (i < a_g):
+                assert _ambiguous(float(p32[r0 + i, x]), float(q[i, x]), float(u[i])), (
+                    f"slot {b}: draft {i} {'rejected' if i < a_g else 'accepted'} by the oracle with a clear "
+                    f"margin, GPU accepted {a_g}")
+                by_margin = True
+        if a_g < g:
+            w = np.maximum(np.float32(0), p32[r0 + a_g] - q[a_g])
             if not np.any(np.floor(w.astype(np.float64) * 2.0 ** 32) > 0):
-                w = p32[r0 + a_or]
+                w = p32[r0 + a_g]
         else:
             w = p32[r0 + g]
-        W = np.floor(w.astype(np.float64) * 2.0 ** 32)
-        cum = np.cumsum(W)
-        S = cum[-1]
-        T = np.floor(S * np.floor(float(u[g]) * 2 ** 24) / 2 ** 24)
-        lo = cum[t_g - 1] if t_g > 0 else 0.0
-        judged += 1
-        assert lo - DECISION_REL * S <= T <= cum[t_g] + DECISION_REL * S, (
-            f"slot {b}: token {t_g} vs oracle {t_or} outside the tolerance of the CDF")
+        t_or = o.inverse_cdf_int(w, u[g])
+        t_g = int(fin_gpu[b])
+        if t_g != t_or:
+            # the GPU's token must sit at the oracle's CDF point within the probability tolerance
+            W = np.floor(w.astype(np.float64) * 2.0 ** 32)
+            cum = np.cumsum(W)
+            S = cum[-1]
+            T = np.floor(S * np.floor(float(u[g]) * 2 ** 24) / 2 ** 24)
+            assert 0 <= t_g < len(w), f"slot {b}: token {t_g} outside the vocabulary"
+            lo = cum[t_g - 1] if t_g > 0 else 0.0
+            assert lo - DECISION_REL * S <= T <= cum[t_g] + DECISION_REL * S, (
+                f"slot {b}: token {t_g} vs oracle {t_or} outside the tolerance of the CDF")
+            by_margin = True
+        judged += int(by_margin)
     return judged
+
+
+def check_realign(batch: wl.Batch, res: dict, dev: dict):
+    """Realignment bit-exact against the oracle's, always: the oracle realigns
+    the step's input state from the GPU's own accepted counts (which
+    check_acceptance has judged), and the emitted tokens are the GPU's accepted
+    drafts followed by its final token.  res / dev: the step's outputs and the
+    device batch after the step, as numpy arrays."""
+    acc = np.asarray(res["accepted"]).astype(np.int64)
+    fin = np.asarray(res["final_tokens"])
+    ra = o.realign(batch.seq_lens, acc, batch.page_table, batch.num_pages, batch.free_pages, batch.num_free,
+                   batch.dims["page"], batch.gamma_max, gen_counts=batch.gen_counts, gen_limits=batch.gen_limits)
+    assert ra["status"] == 0
+    roff = wl.row_offsets(batch.draft_lens)
+    eoff = np.concatenate([[0], np.cumsum(acc + 1)]).astype(np.int32)
+    emitted = np.concatenate([np.append(batch.tokens[int(roff[b]) + 1: int(roff[b]) + 1 + int(acc[b])], fin[b])
+                              for b in range(batch.B)]).astype(np.int32)
+    assert np.array_equal(res["emitted_offsets"], eoff)
+    assert np.array_equal(res["emitted_tokens"][:eoff[-1]], emitted)
+    assert np.array_equal(res["new_seq_lens"], ra["new_seq_lens"])
+    assert np.array_equal(res["finished"], ra["finished"])
+    assert np.array_equal(dev["page_table"], ra["page_table"])
+    assert np.array_equal(dev["num_pages"], ra["num_pages"])
+    nf = int(dev["num_free_out"][0])
+    assert nf == ra["num_free"]
+    assert np.array_equal(dev["free_pages"][:nf], ra["free_pages"][:nf])
+    if "num_live" in res:
+        nl = int(res["num_live"][0])
+        assert nl == ra["num_live"]
+        assert np.array_equal(res["next_src"][:nl], ra["next_src"])
+        assert np.array_equal(res["next_seq_lens"][:nl], ra["next_seq_lens"])
+        assert np.array_equal(res["next_num_pages"][:nl], ra["next_num_pages"])
+        assert np.array_equal(res["next_page_table"][:nl], ra["next_page_table"])
+        if ra["next_gen_counts"] is not None:
+            assert np.array_equal(res["next_gen_counts"][:nl], ra["next_gen_counts"])
+    return ra

@@ -127,6 +127,8 @@ def _attention_ref(dims, b, q):
     (wl.NINE_B, [16000, 0, 15, 16, 17, 127, 128, 129], [3, 0, 3, 1, 2, 3, 0, 1], 3),
     (wl.NINE_B, [int(x) for x in np.random.default_rng(77).integers(0, 3000, size=40)],
      [int(x) for x in np.random.default_rng(78).integers(0, 4, size=40)], 3),
+    # gamma 8: 9 rows x 4 query heads per KV head = 36 query vectors per item
+    (wl.NINE_B, [2048, 2048, 100, 0, 777, 2047, 16, 1500], [8, 8, 8, 8, 0, 5, 8, 3], 8),
 ])
 @pytest.mark.parametrize("path", [1, 2])
 def test_attention_matches_oracle(torch_cuda, case, path):
@@ -135,6 +137,8 @@ def test_attention_matches_oracle(torch_cuda, case, path):
     dims, lens, gams, gmax = case
     if path == 2 and dims["head_dim"] != 128:
         pytest.skip("the tcgen05 kernel serves head_dim 128")
+    if path == 2 and (gmax + 1) * (dims["n_q"] // dims["n_kv"]) > 32:
+        pytest.skip("the tcgen05 kernel takes at most 32 query vectors per item")
     torch = torch_cuda
     from workloads import device as wd
     W = wl.make_weights(wl.TINY, 1) if dims is wl.TINY else None
@@ -271,18 +275,16 @@ def _full_step_check(eng, W, batch, name):
     assert status == 0, f"{name}: status {status}"
     ref = o.verify_step(batch, W)
     fw = ref["forward"]
+    # every row inside the tolerance (9B-class layer: as computed, no other roundings)
     p_valid, explained = gh.compare_step(batch, W, fw, res["logits"], res["probs"])
+    if not gh.flips_allowed(batch.dims):
+        assert explained == {}
     # every row's K/V landed in its page at position L + i, rounded as the oracle
-    # rounds it (or, within the tie window, to the other neighbour)
+    # rounds it (or, within the window, to the other neighbour)
     gh.check_kv_written(batch, fw, dev["kv_pool"], pt_before)
     judged = gh.check_acceptance(batch, p_valid, res["accepted"], res["final_tokens"])
-    if np.array_equal(res["accepted"], ref["accepted"]):
-        ra = ref["realign"]
-        assert np.array_equal(res["new_seq_lens"], ra["new_seq_lens"])
-        assert np.array_equal(dev["page_table"], ra["page_table"])
-        assert int(dev["num_free_out"][0]) == ra["num_free"]
-        eoff = ref["emitted_offsets"]
-        assert np.array_equal(res["emitted_offsets"], eoff)
+    # realignment from the GPU's counts, bit-exact, whether or not they equal the oracle's
+    gh.check_realign(batch, res, dev)
     return judged
 
 
@@ -389,3 +391,100 @@ def test_device_errors_set_status(tiny_engine, fault):
     ok = wl.workload1()
     status, _, _ = gh.run_step(eng, ok)
     assert status == 0
+
+
+# ---------------------------------------------------------------------------
+# a failed call leaves the context ready for the next one
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dims", [wl.TINY, wl.NINE_B])
+def test_call_after_a_zero_mass_row_is_bit_exact(torch_cuda, dims):
+    """A batch whose bonus row has no probability mass sets SDV_ERR_BAD_INPUT
+    from inside the sampling kernel while the other sequences' blocks still
+    run; the valid call that follows on the same context must be bit-exact
+    with the oracle (every sequence's sampling arrival counter back at zero)."""
+    import torch
+    from workloads import device as wd
+    gmax = 3
+    eng = _attn_only_engine(wd.config(dims, gmax), torch) if dims is not wl.TINY else \
+        gh.engine_for(dims, gmax, wd.weights_to_device(wl.make_weights(wl.TINY, 1)), 256, 64)
+    for rep in range(3):
+        b, p = _accept_case(dims, 48, gmax, 40 + rep, finish=False)
+        # slot 5 drafts nothing; its only row (the bonus distribution) is all zeros
+        bad = wl.make_batch(dims, 940 + rep, seq_lens=b.seq_lens, draft_lens=np.where(np.arange(48) == 5, 0,
+                                                                                           b.draft_lens),
+                            gamma_max=gmax, extra_pages=3 * 48, kv_fill="lazy")
+        pbad = wl.softmax_f32(np.random.default_rng(rep).standard_normal((bad.R, dims["vocab"])).astype(np.float32))
+        pbad[int(wl.row_offsets(bad.draft_lens)[5])] = 0.0
+        bdb = wd.batch_to_device(bad)
+        rb = wd.alloc_result(bad.B, bad.R, dims["vocab"], gmax, bad.page_table.shape[1])
+        eng.accept(torch.from_numpy(pbad).cuda(), bdb, rb)
+        assert eng.read_status(rb["status"]) == 6
+        # the valid call on the same context
+        bd = wd.batch_to_device(b)
+        res = wd.alloc_result(b.B, b.R, dims["vocab"], gmax, b.page_table.shape[1])
+        eng.accept(torch.from_numpy(p).cuda(), bd, res)
+        assert eng.read_status(res["status"]) == 0
+        acc, emitted, eoff, fin = o.accept_batch(p, b.draft_probs, b.tokens, b.uniforms, b.draft_lens)
+        assert np.array_equal(res["accepted"].cpu().numpy(), acc)
+        assert np.array_equal(res["final_tokens"].cpu().numpy(), fin)
+        assert np.array_equal(res["emitted_tokens"].cpu().numpy()[:eoff[-1]], emitted)
+
+
+@pytest.mark.parametrize("fault", ["negative", "beyond_gamma", "token"])
+def test_realign_rejects_bad_counts_and_writes_nothing(tiny_engine, fault):
+    """sdv_realign takes the accepted counts and final tokens from the caller:
+    a count outside 0..gamma_b or a token outside the vocabulary is
+    SDV_ERR_BAD_INPUT, and no output, page or free-stack entry moves."""
+    import torch
+    from workloads import device as wd
+    _, _, eng = tiny_engine
+    b = wl.make_batch(wl.TINY, 77, seq_lens=[30, 60, 5], draft_lens=[3, 2, 1], gamma_max=3, extra_pages=6)
+    acc = np.array([1, 2, 0], np.int32)
+    fin = np.array([7, 8, 9], np.int32)
+    if fault == "negative":
+        acc[1] = -1
+    elif fault == "beyond_gamma":
+        acc[2] = 2          # gamma of slot 2 is 1
+    else:
+        fin[0] = wl.TINY["vocab"]
+    bd = wd.batch_to_device(b)
+    res = wd.alloc_result(b.B, b.R, wl.TINY["vocab"], 3, b.page_table.shape[1])
+    res["accepted"].copy_(torch.from_numpy(acc))
+    res["final_tokens"].copy_(torch.from_numpy(fin))
+    sentinel = -12345
+    for k in ("emitted_tokens", "emitted_offsets", "new_seq_lens", "finished", "next_src", "next_seq_lens"):
+        res[k].fill_(sentinel)
+    eng.realign(bd, res)
+    assert eng.read_status(res["status"]) == 6
+    for k in ("emitted_tokens", "emitted_offsets", "new_seq_lens", "finished", "next_src", "next_seq_lens"):
+        assert (res[k].cpu().numpy() == sentinel).all(), k
+    assert np.array_equal(bd["page_table"].cpu().numpy(), b.page_table)
+    assert np.array_equal(bd["num_pages"].cpu().numpy(), b.num_pages)
+    assert int(bd["num_free_out"].cpu().numpy()[0]) == b.num_free
+    assert np.array_equal(bd["free_pages"].cpu().numpy(), b.free_pages)
+
+
+def test_bounded_wait_times_out_and_the_context_recovers(tiny_engine):
+    """The device timeout path: with the test hook set, the step's first kernel
+    waits on a barrier nothing completes, gives up after 2 ms and records
+    SDV_ERR_TIMEOUT; no output is written; the next step on the same context,
+    hook off, returns SDV_OK and matches the oracle."""
+    import torch
+    from workloads import device as wd
+    W, _, eng = tiny_engine
+    batch = wl.workload1()
+    bd = wd.batch_to_device(batch)
+    res = wd.alloc_result(batch.B, batch.R, batch.dims["vocab"], 3, batch.page_table.shape[1], logits=True)
+    res["accepted"].fill_(-7)
+    res["logits"].fill_(-7.0)
+    eng.set_stall_test(2_000_000)
+    try:
+        eng.verify_step(bd, res)
+        assert eng.read_status(res["status"]) == 5          # SDV_ERR_TIMEOUT
+    finally:
+        eng.set_stall_test(0)
+    assert (res["accepted"].cpu().numpy() == -7).all()
+    assert (res["logits"].cpu().numpy() == -7.0).all()
+    assert np.array_equal(bd["page_table"].cpu().numpy(), batch.page_table)
+    _full_step_check(eng, W, wl.workload1(), "after-timeout")

@@ -1,9 +1,11 @@
-"""Continuous batching on the GPU: sdv_admit against the admission rule, and a
-scheduler-driven swarm whose device slot table equals the host scheduler's
-mirror after every step (through the C ABI)."""
+"""Continuous batching on the GPU: sdv_admit against the oracle's admission
+(o.admit), and a scheduler-driven swarm whose device slot table equals, after
+every step, both the oracle's realignment + admission carried on the host and
+the host scheduler's mirror (through the C ABI)."""
 import numpy as np
 import pytest
 
+from oracle import verify_step as o
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -25,7 +27,11 @@ def _engine(gamma_max, max_rows, max_slots):
                         max_slots=max_slots)
 
 
-def test_admit_matches_the_admission_rule():
+def _host(t):
+    return {k: v.cpu().numpy().astype(np.int64) for k, v in t.items()}
+
+
+def test_admit_matches_the_oracle():
     import torch
     gmax, page, pool, max_pages, slots = 3, 16, 64, 12, 8
     eng = _engine(gmax, 32, slots)
@@ -37,31 +43,27 @@ def test_admit_matches_the_admission_rule():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ctx = np.array([0, 15, 16, 100], np.int32)
     out = np.array([5, 6, 7, 8], np.int32)
+    want_st, want, want_nf = o.admit(_host(t), 0, ctx, out, free, pool, gmax, page)
     eng.admit(t, 0, torch.from_numpy(ctx).cuda(), torch.from_numpy(out).cuda(), free_d, nfree, status)
-    assert eng.read_status(status) == 0
-    top, pt = pool, np.full((slots, max_pages), -1, np.int32)
-    for j, L in enumerate(ctx):
-        need = (L + gmax + 1 + page - 1) // page
-        pt[j, :need] = free[top - need:top][::-1]
-        top -= need
-    assert nfree.item() == top
-    assert np.array_equal(t["page_table"].cpu().numpy(), pt)
-    assert t["seq_lens"].cpu().numpy()[:4].tolist() == ctx.tolist()
-    assert t["gen_limits"].cpu().numpy()[:4].tolist() == out.tolist()
-    assert t["num_pages"].cpu().numpy()[:4].tolist() == [1, 2, 2, 7]
-    # a second admission after 4 live slots, gathering the survivors' limits through next_src
+    assert eng.read_status(status) == want_st == 0
+    assert nfree.item() == want_nf
+    for k, v in _host(t).items():
+        assert np.array_equal(v, want[k]), k
+    # a second admission after 2 survivors, gathering their limits through next_src
     prev_lim = torch.tensor([50, 60, 70, 80], dtype=torch.int32, device="cuda")
     t["gen_limits"].zero_()
+    before = _host(t)
     src = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
     nlive = torch.tensor([2], dtype=torch.int32, device="cuda")
+    want_st, want, want_nf = o.admit(before, 2, [30], [9], free, nfree.item(), gmax, page, num_live=2,
+                                     next_src=[1, 3], gen_limits_prev=[50, 60, 70, 80])
     eng.admit(t, 2, torch.tensor([30], dtype=torch.int32, device="cuda"),
               torch.tensor([9], dtype=torch.int32, device="cuda"), free_d, nfree, status,
               num_live=nlive, next_src=src, gen_limits_prev=prev_lim)
-    assert eng.read_status(status) == 0
-    assert t["gen_limits"].cpu().numpy()[:3].tolist() == [60, 80, 9]
-    need = (30 + gmax + 1 + page - 1) // page
-    assert t["page_table"].cpu().numpy()[2, :need].tolist() == free[top - need:top][::-1].tolist()
-    assert nfree.item() == top - need
+    assert eng.read_status(status) == want_st == 0
+    assert nfree.item() == want_nf
+    for k, v in _host(t).items():
+        assert np.array_equal(v, want[k]), k
 
 
 def test_admit_device_errors_write_nothing():
@@ -115,21 +117,53 @@ def test_swarm_runner_device_table_equals_the_scheduler_mirror(budget, slots):
     wd.normal_bf16_device_(pool, wl._key(9, wl.S_KV, 0))
     run = SwarmRunner(eng, pool, pool_pages, slots, budget, max_pages)
     g = np.random.default_rng(budget)
-    outs = []
+    outs, queue, admitted = [], [], 0
     for i in range(24):
         outs.append(int(g.integers(2, 30)))
-        run.submit(i, int(g.integers(0, 200)), outs[-1])
+        queue.append((int(g.integers(0, 200)), outs[-1]))
+        run.submit(i, queue[-1][0], outs[-1])
     drafter = _random_drafter(d["vocab"], budget)
+    # the oracle's state: admission and realignment carried on the host from
+    # the scheduler's plans and the GPU's accepted counts
+    ot = _host(_table(slots, max_pages))
+    ofree, onf, olive = np.arange(pool_pages, dtype=np.int64), pool_pages, 0
     steps = 0
     while True:
-        st, fin = run.step(drafter)
+        st, batch = run.plan()
         if st["live"] == 0:
             break
+        assert st["admitted"] == o.admission_count(
+            [c for c, _ in queue[admitted:]], olive, onf, slots, gmax, page)
+        code, ot, onf = o.admit(ot, olive, st["admit_ctx"], st["admit_out"], ofree, onf, gmax, page)
+        assert code == o.OK
+        admitted += st["admitted"]
+        olive += st["admitted"]
+        assert np.array_equal(_host(run.table())["page_table"][:olive], ot["page_table"][:olive])
+        drafter(st, batch)
+        run.verify(st, batch)
+        fin = run.complete(st)
+        acc = run.res["accepted"][:olive].cpu().numpy()
+        ra = o.realign(ot["seq_lens"][:olive], acc, ot["page_table"][:olive], ot["num_pages"][:olive], ofree,
+                       onf, page, gmax, ot["gen_counts"][:olive], ot["gen_limits"][:olive])
+        assert ra["status"] == o.OK
+        src, nl = ra["next_src"], ra["num_live"]
+        nt = _host(_table(slots, max_pages))
+        nt["seq_lens"][:nl], nt["num_pages"][:nl] = ra["next_seq_lens"], ra["next_num_pages"]
+        nt["gen_counts"][:nl], nt["page_table"][:nl] = ra["next_gen_counts"], ra["next_page_table"]
+        nt["gen_limits"][:nl] = ot["gen_limits"][:olive][src]
+        ot, ofree, onf, olive = nt, ra["free_pages"].astype(np.int64), ra["num_free"], nl
         steps += 1
         assert st["rows"] == st["live"] * (st["gamma"] + 1)
         m = run.sched.slots()
         n = len(m["seq_lens"])
+        assert n == olive
         t = run.table()
+        # the device table against the oracle (the limits are gathered at the next admission)
+        for k in ("seq_lens", "gen_counts", "num_pages", "page_table"):
+            assert np.array_equal(_host(t)[k][:n], ot[k][:n]), k
+        assert run.num_free.item() == onf
+        assert np.array_equal(run.free_pages[:onf].cpu().numpy(), ofree[:onf])
+        # and against the scheduler's own mirror
         assert t["seq_lens"][:n].cpu().tolist() == m["seq_lens"]
         assert t["gen_counts"][:n].cpu().tolist() == m["gen_counts"]
         assert t["num_pages"][:n].cpu().tolist() == m["num_pages"]

@@ -44,24 +44,12 @@ def test_swarm_tiny_against_oracle_every_step(tiny_int4_swarm_engine):
         p_valid, _ = gh.compare_step(batch, W, fw, res["logits"], res["probs"])
         gh.check_kv_written(batch, fw, dev["kv_pool"], pt_before)
         judged += gh.check_acceptance(batch, p_valid, res["accepted"], res["final_tokens"])
-        if np.array_equal(res["accepted"], ref["accepted"]):
-            ra = ref["realign"]
-            assert np.array_equal(res["new_seq_lens"], ra["new_seq_lens"])
-            assert np.array_equal(res["finished"], ra["finished"])
-            assert np.array_equal(dev["page_table"], ra["page_table"])
-            nf = int(dev["num_free_out"][0])
-            assert nf == ra["num_free"]
-            assert np.array_equal(dev["free_pages"][:nf], ra["free_pages"][:nf])
-            nl = int(res["num_live"][0])
-            assert nl == ra["num_live"]
-            assert np.array_equal(res["next_src"][:nl], ra["next_src"])
-            assert np.array_equal(res["next_seq_lens"][:nl], ra["next_seq_lens"])
-            assert np.array_equal(res["next_page_table"][:nl], ra["next_page_table"])
-            assert np.array_equal(res["next_gen_counts"][:nl], ra["next_gen_counts"])
-            assert np.array_equal(res["emitted_tokens"][:ref["emitted_offsets"][-1]], ref["emitted_tokens"])
+        # realignment from the GPU's own counts, bit-exact, at every step
+        gh.check_realign(batch, res, dev)
         finished += s.advance(batch, ref)
     assert finished >= 10, finished          # slots turned over
-    assert judged <= 24 * 24 // 10
+    # slots whose count or token differs from the oracle's (each within its margin): at most 5 %
+    assert judged <= 24 * 24 // 20, judged
 
 
 def test_swarm_full_size_int4(nine_b_int4):
@@ -81,7 +69,8 @@ def test_swarm_full_size_int4(nine_b_int4):
     fw = ref["forward"]
     z = res["logits"].cpu().numpy()[rows]
     p = res["probs"].cpu().numpy()[rows]
-    p_valid, _ = gh.compare_step(sub, W, fw, z, p)
+    p_valid, explained = gh.compare_step(sub, W, fw, z, p)
+    assert explained == {}
     gh.check_kv_written(sub, fw, sw.read_pages(bd["kv_pool"], pages), sub.page_table)
     fin = res["final_tokens"].cpu().numpy()
     gh.check_acceptance(sub, p_valid, acc[slots], fin[slots])

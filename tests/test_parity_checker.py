@@ -1,6 +1,7 @@
-"""The flip-aware comparison the GPU step tests use, exercised on the CPU with
-results made by the oracle itself: a valid alternative rounding of a value at
-a bf16 tie passes, a planted logit error of the same size does not.
+"""The comparison the GPU step tests use, exercised on the CPU with results
+made by the oracle itself: on the tiny model, ONE valid alternative rounding
+of a value at a bf16 tie passes, a planted logit error of the same size does
+not, and on the 9B-class layer no alternative rounding is tried at all.
 
 The case is a wide tiny-model batch in which V element 36 of head 0 in row 0
 (a one-token sequence at position 0) lies 6.4e-7 relative from a bf16 tie;
@@ -47,7 +48,7 @@ def test_other_rounding_at_a_tie_is_accepted(wide):
     assert np.abs(alt["logits"][0] - fw["logits"][0]).max() > gh.LOGIT_TOL_REL_RMS * rms
     p, ex = gh.compare_step(batch, W, fw, _noise(alt["logits"], 1).astype(np.float32),
                             alt["probs"].astype(np.float32))
-    assert ex == {0: [("v", 0, 0, 36)]}
+    assert ex == {0: ("v", 0, 0, 36)}
     assert np.array_equal(p[0], alt["probs"][0])
 
 
@@ -84,3 +85,23 @@ def test_kv_check_rejects_a_far_rounding(wide):
     with pytest.raises(AssertionError):
         gh.check_kv_written(batch, fw, bad, batch.page_table)
     del offs
+
+
+def test_nine_b_rows_get_no_other_rounding(wide):
+    """The same result, presented as a 9B-class batch: the row outside the
+    tolerance fails outright (the checker tries no other rounding there)."""
+    import dataclasses
+    W, batch, fw = wide
+    alt = o.forward(batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens,
+                    batch.tokens, flips={("v", 0, 0, 36)})
+    big = dataclasses.replace(batch, dims=dict(batch.dims, hidden=4096))
+    assert not gh.flips_allowed(big.dims)
+    with pytest.raises(AssertionError, match="outside tolerance"):
+        gh.compare_step(big, W, fw, alt["logits"].astype(np.float32), alt["probs"].astype(np.float32))
+
+
+def test_tie_window_is_the_measured_error():
+    """A candidate for another rounding must lie within 2^-17 rms of a tie (the
+    largest error seen on the GPU), not a multiple of it."""
+    assert gh.TIE_WINDOW == 2.0 ** -17
+    assert gh.KV_WINDOW <= 2.0 ** -15

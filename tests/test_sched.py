@@ -116,40 +116,46 @@ def test_continuous_batching_holds_the_full_batch(sched_mod):
     assert abs(one - g["batch1_tok_s"][0]) <= g["batch1_tok_s"][1]
 
 
-def _admit_model(state, ctx_lens, out_lens, gamma_max, page):
-    """Admission as sdv_admit defines it: newcomers appended in order, each
-    popping ceil((L + gamma_max + 1) / page) pages off the free-stack top."""
-    for L, out in zip(ctx_lens, out_lens):
-        need = (L + gamma_max + 1 + page - 1) // page
-        top = state["num_free"]
-        assert need <= top
-        row = np.full(state["page_table"].shape[1], -1, np.int32)
-        row[:need] = state["free_pages"][top - need:top][::-1]
-        state["num_free"] = top - need
-        state["page_table"] = np.vstack([state["page_table"], row[None]])
-        state["seq_lens"] = np.append(state["seq_lens"], L)
-        state["num_pages"] = np.append(state["num_pages"], need)
-        state["gen_counts"] = np.append(state["gen_counts"], 0)
-        state["gen_limits"] = np.append(state["gen_limits"], out)
+def _admit_oracle(state, ctx_lens, out_lens, gamma_max, page):
+    """The oracle's admission (o.admit) on the variable-length mirror state."""
+    live, n = len(state["seq_lens"]), len(ctx_lens)
+    max_pages = state["page_table"].shape[1]
+    pad = lambda a, fill: np.concatenate([a, np.full(n, fill, a.dtype)])  # noqa: E731
+    table = dict(seq_lens=pad(state["seq_lens"], 0), num_pages=pad(state["num_pages"], 0),
+                 gen_counts=pad(state["gen_counts"], 0), gen_limits=pad(state["gen_limits"], 0),
+                 page_table=np.vstack([state["page_table"], np.full((n, max_pages), -1, np.int32)]))
+    st, t, nf = o.admit(table, live, ctx_lens, out_lens, state["free_pages"], state["num_free"], gamma_max, page)
+    assert st == o.OK
+    state.update(seq_lens=t["seq_lens"], num_pages=t["num_pages"], gen_counts=t["gen_counts"],
+                 gen_limits=t["gen_limits"], page_table=t["page_table"], num_free=nf)
 
 
 @pytest.mark.parametrize("seed,gamma_max,budget,slots", [(0, 3, 64, 16), (1, 7, 24, 6), (2, 0, 8, 8)])
 def test_mirror_follows_the_oracle_realignment(sched_mod, seed, gamma_max, budget, slots):
-    """The scheduler's slot mirror equals the oracle's realignment + admission
-    state after every step of a random run with turnover."""
+    """The scheduler admits what the oracle's admission rule admits, and its
+    slot mirror equals the oracle's realignment + admission state after every
+    step of a random run with turnover."""
     g = np.random.default_rng(seed)
     page, pool, max_pages = 16, 600, 96
     s = sched_mod.Scheduler(max_slots=slots, gamma_max=gamma_max, budget_rows=budget, pool_pages=pool,
                             max_pages_per_seq=max_pages, page_size=page)
+    queue = []
     for i in range(60):
-        s.submit(i, int(g.integers(0, 300)), int(g.integers(1, 40)))
+        queue.append((int(g.integers(0, 300)), int(g.integers(1, 40))))
+        s.submit(i, *queue[-1])
     state = dict(seq_lens=np.zeros(0, np.int64), num_pages=np.zeros(0, np.int32),
                  page_table=np.zeros((0, max_pages), np.int32), gen_counts=np.zeros(0, np.int64),
                  gen_limits=np.zeros(0, np.int64), free_pages=g.permutation(pool).astype(np.int32), num_free=pool)
     steps = 0
     while True:
+        # the scheduler admits exactly what the oracle's admission rule admits, in arrival order
+        k = o.admission_count([c for c, _ in queue], len(state["seq_lens"]), state["num_free"], slots,
+                              gamma_max, page)
         st = s.plan()
-        _admit_model(state, st["admit_ctx"], st["admit_out"], gamma_max, page)
+        assert st["admitted"] == k
+        assert list(zip(st["admit_ctx"], st["admit_out"])) == queue[:k]
+        queue = queue[k:]
+        _admit_oracle(state, st["admit_ctx"], st["admit_out"], gamma_max, page)
         B = st["live"]
         if B == 0:
             break
