@@ -1,24 +1,34 @@
 """Benchmark of the ragged batched speculative-verify step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2|3]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 2|3|4|5] [--points B:gamma,...] [--sweep]
 
 One step = one verify pass of the whole hot path (embedding, QKV + RoPE + KV
 append, paged attention, O, SwiGLU FFN, LM head + softmax statistics,
 acceptance + sampling, realignment) over one batch of synthetic inputs that
-stay resident in HBM.  Default workload: B = 1 sequence with 7 drafts on a
-9B-class layer (hidden 4096, 32/8 heads of 128, FFN 12288, vocab 151936,
-bf16), KV context 2048 in 16-token pages, per-draft acceptance 0.8.  The
-weights (1.63 GB) are larger than L2 (129 MB), so no L2 flush is needed
-between steps.  Every step draws fresh uniforms, so emitted tokens follow the
-acceptance statistics.
+stay resident in HBM.  Every step draws fresh uniforms, so emitted tokens
+follow the acceptance statistics.
+
+Default (workload 4): the metric's own curve, verified tokens/s and step time
+against the verify rows B * (gamma + 1), on the crossover sweep's shapes (a
+9B-class layer, hidden 4096, 32/8 heads of 128, FFN 12288, vocab 151936,
+bf16, KV context 2048 in 16-token pages, per-draft acceptance 0.8).  K timed
+steps run at each point of the curve; the line's headline `value` is the
+point B = 128, gamma = 3 (512 verify rows: past the memory-to-compute
+crossover, and the draft length the pages find throughput-optimal at 128
+sequences), and every point is listed in `curve` with its roofline fraction.
+Weights (1.63 GB) and, from 8 sequences on, the KV cache exceed L2 (129 MB),
+so no L2 flush is needed between steps.
 
 Metric: verified (emitted) tokens per second, sum over sequences of
 (accepted + 1) per step / step time; ms per step beside it.  Multi-GPU: one
 independent replica per GPU (the step does not shard: every sequence needs
-all weights), value = all ranks' tokens / slowest rank's time.
+all weights), value = all ranks' tokens / slowest rank's time.  Without an
+outer torchrun, --gpus N > 1 launches the N replicas itself.
 
 ``--impl reference`` times the CPU oracle (float64 numpy, the plain
-restatement of the method) on the same workload on the host cores.
+restatement of the method, BLAS pinned to one thread) on a bounded sample of
+the same workload on the host.
 """
 from __future__ import annotations
 
@@ -38,19 +48,32 @@ sys.path.insert(0, ROOT)
 METRIC = "verified tokens/s & verify-step us vs B*(gamma+1); % of HBM/tensor roofline"
 UNIT = "tokens/s"
 
+# the curve of the default run: (B, gamma) at verify rows 8, 128, 256, 320, 512, 1152
+CURVE_POINTS = ((1, 7), (32, 3), (64, 3), (64, 4), (128, 3), (128, 8))
+HEADLINE = (128, 3)
+# environment that pins the oracle's BLAS to one thread
+ONE_THREAD = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+              "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1"}
+
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 5])
+    ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4, 5],
+                    help="4: the verify-row curve on the sweep's shapes (default); 2: batch of one; "
+                         "3: eight agents; 5: the continuous-batching swarm")
+    ap.add_argument("--points", default=None,
+                    help="workload 4: the curve's points as B:gamma pairs (default "
+                         + ",".join(f"{b}:{g}" for b, g in CURVE_POINTS) + "); the headline is 128:3 when listed, "
+                         "else the last point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling run: no clock pre-roll, no e2e or CPU legs (its numbers are not bench values)")
     ap.add_argument("--sweep", action="store_true",
-                    help="roofline crossover sweep: B in {1,4,16,32,64,128} x gamma in {0,1,2,3,4,7,8}, ctx 2048; "
+                    help="the whole crossover sweep: B in {1,4,16,32,64,128} x gamma in {0,1,2,3,4,7,8}, ctx 2048; "
                          "one JSON line per point, then a summary line")
     ap.add_argument("--sweep-points", default=None,
                     help="subset of the sweep as B:gamma pairs, e.g. 1:7,32:7,128:8")
@@ -63,6 +86,7 @@ def parse():
                          "a markdown table, not a bench line")
     ap.add_argument("--timeline-shapes", default=None,
                     help="timeline of the ctx-2048 sweep shapes instead of --workload, as B:gamma pairs")
+    ap.add_argument("--cpu-oracle-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -73,31 +97,43 @@ def dist_env():
     return rank, world, local
 
 
+def parse_points(text):
+    return [tuple(int(v) for v in pt.split(":")) for pt in text.split(",")]
+
+
 # ---------------------------------------------------------------------------
-# workload
+# workloads
 # ---------------------------------------------------------------------------
 
-def workload_desc(wid):
+LAYER_DESC = "9B-class layer bf16 (hidden 4096, 32/8 heads x 128, FFN 12288), vocab 151936"
+
+
+def workload_desc(wid, points=None, headline=None):
     import workloads as wl
     if wid == 2:
-        return dict(workload="batch-of-one: B=1, gamma=7, 9B-class layer bf16 (hidden 4096, 32/8 heads x 128, "
-                             "FFN 12288), vocab 151936, ctx 2048, acceptance 0.8",
+        return dict(workload=f"batch-of-one: B=1, gamma=7, {LAYER_DESC}, ctx 2048, acceptance 0.8",
                     B=1, gamma=[7], ctx=[2048], rows=8, l2="inputs larger than L2 (weights 1.63 GB)")
+    if wid == 4:
+        B, g = headline
+        return dict(workload=f"verify-row curve on the roofline crossover sweep's shapes: {LAYER_DESC}, "
+                             f"ctx 2048, acceptance 0.8; headline point B={B}, gamma={g} "
+                             f"({B * (g + 1)} verify rows), curve points (B, gamma) {list(points)}",
+                    B=B, gamma=g, ctx=2048, rows=B * (g + 1), points=[list(p) for p in points],
+                    l2="inputs larger than L2 (weights 1.63 GB, KV 1.07 GB at the headline)")
     lens, gam, _ = wl.workload3_shape()
-    return dict(workload="eight-agent ragged: B=8, gamma_b in {1,2,3} (sum<=16), ctx U{512..8192}, "
-                         "acceptance {0.97,0.8,0.14}, 9B-class layer bf16, vocab 151936",
+    return dict(workload=f"eight-agent ragged: B=8, gamma_b in {{1,2,3}} (sum<=16), ctx U{{512..8192}}, "
+                         f"acceptance {{0.97,0.8,0.14}}, {LAYER_DESC}",
                 B=8, gamma=[int(x) for x in gam], ctx=[int(x) for x in lens], rows=int((gam + 1).sum()),
                 l2="inputs larger than L2 (weights 1.63 GB)")
 
 
-def make_host_workload(wid):
+def host_batch(wid, B=None, gamma=None, lazy=False):
     import workloads as wl
-    W = wl.make_weights(wl.NINE_B, wid)
     if wid == 2:
-        batch = wl.workload2(extra_pages=8)
-    else:
-        batch = wl.workload3(extra_pages=16)
-    return W, batch
+        return wl.workload2(extra_pages=8)
+    if wid == 3:
+        return wl.workload3(extra_pages=16)
+    return wl.workload4(B, gamma, kv_fill="lazy" if lazy else "normal", extra_pages=4 * B + 8)
 
 
 # ---------------------------------------------------------------------------
@@ -149,22 +185,8 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# our arm
+# algorithmic work
 # ---------------------------------------------------------------------------
-
-def lm_head_algorithmic_bytes(R, V=151936, H=4096, vtile=128):
-    """Bytes the LM-head launch must move: the weights once, the normed rows,
-    and the per-(vocab tile, row) softmax statistics it produces."""
-    return V * H * 2 + R * H * 2 + ((V + vtile - 1) // vtile) * R * 8
-
-
-def step_algorithmic_bytes(batch):
-    """Per-step bytes of the whole hot path: layer + LM-head weights once, every
-    sequence's KV read, the new rows' KV written, the draft probabilities the
-    rule reads (q at each draft token, plus the full q row of each sequence's
-    final position), the target logits of the final rows."""
-    return sum(b for _, b in phase_work(batch).values())
-
 
 def phase_work(batch):
     """Algorithmic (flops, bytes) of each phase of one step on the 9B-class layer.
@@ -194,26 +216,28 @@ def phase_work(batch):
     }
 
 
-# DRAM traffic of one LM-head launch (dram__bytes_read.sum + dram__bytes_write.sum) from an ncu capture,
-# recorded with a hash of the GEMM sources it was taken on; once those sources change the number no
-# longer describes the kernel and the bench reports null.  Source: profiles/lm_head_gemm_batch_of_one_9b.md
-LM_HEAD_TRAFFIC = {"sources_sha": "0b6a06260b44a0eb", "bytes": {2: 1249.57e6}}
+# DRAM traffic of one LM-head launch (dram__bytes_read.sum + dram__bytes_write.sum) from ncu
+# captures of this bench's own command, keyed by the launch's row count and recorded with a hash of
+# the GEMM sources they were taken on; once those sources change the numbers no longer describe the
+# kernel and the bench reports null.
+LM_HEAD_TRAFFIC = {"sources_sha": None, "bytes": {}}
+GEMM_SOURCES = ("gemm.cu", "gemm_tc.cu", "gemm_common.cuh", "common.cuh", "tcgen05.cuh")
 
 
 def gemm_sources_sha():
     import hashlib
     d = os.path.join(ROOT, "speculative_decoding_verify_ragged_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm.cu", "gemm_common.cuh", "common.cuh"):
+    for f in GEMM_SOURCES:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def lm_head_traffic(workload):
+def lm_head_traffic(rows):
     if gemm_sources_sha() != LM_HEAD_TRAFFIC["sources_sha"]:
         return None
-    return LM_HEAD_TRAFFIC["bytes"].get(workload)
+    return LM_HEAD_TRAFFIC["bytes"].get(int(rows))
 
 
 def measured_peaks():
@@ -245,149 +269,329 @@ def box_copy_gbps():
     return 2 * (1 << 30) * 2 / (best / 1e3) / 1e9
 
 
-def run_ours(args):
-    import torch
-    import workloads as wl
-    from workloads import device as wd
-    from speculative_decoding_verify_ragged_gb300 import PHASES, VerifyEngine, kernel_launches
+# ---------------------------------------------------------------------------
+# our arm: K timed steps of one batch resident on the device
+# ---------------------------------------------------------------------------
 
+def lm_head_work(R, V=151936, H=4096):
+    """(flops, bytes) one LM-head launch must do/move: the contraction once,
+    the weights once, the normed rows and the per-(vocab tile, row) softmax
+    statistics it produces."""
+    return 2 * R * V * H, V * H * 2 + R * H * 2 + ((V + 127) // 128) * R * 8
+
+
+def kernel_roofline(R, avg_us, hbm, tflops, peak_kind, traffic):
+    """The LM-head launch against the roofline that binds it at R rows."""
+    flops, nbytes = lm_head_work(R)
+    t = avg_us * 1e-6
+    tensor = flops / (tflops * 1e12) > nbytes / (hbm * 1e9)
+    if tensor:
+        achieved, peak, unit = flops / t / 1e12, tflops, "TFLOP/s"
+    else:
+        achieved, peak, unit = nbytes / t / 1e9, hbm, "GB/s"
+    return {"bound": "tensor" if tensor else "hbm", "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "kernel": "LM-head GEMM (EPI_LMHEAD)",
+            "peak_kind": peak_kind, "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+            "avg_launch_us": avg_us}
+
+
+def step_roofline(batch, ms, hbm, tflops):
+    work = phase_work(batch)
+    flops = sum(f for f, _ in work.values())
+    nbytes = sum(b for _, b in work.values())
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tflops * 1e12)
+    return {"bound": "tensor" if t_tc > t_hbm else "hbm", "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "roofline_us": max(t_hbm, t_tc) * 1e6, "t_hbm_us": t_hbm * 1e6, "t_tensor_us": t_tc * 1e6,
+            "achieved_GBps": nbytes / (ms / 1e3) / 1e9, "achieved_TFLOPs": flops / (ms / 1e3) / 1e12,
+            "frac": max(t_hbm, t_tc) / (ms / 1e3)}
+
+
+class Bench:
+    """The device-side state shared by the points of a run: the weights on the
+    device and one verify context per draft-length cap."""
+
+    def __init__(self, seed, max_rows, max_slots, gemm_path=0, fmt="bf16"):
+        import torch
+        import workloads as wl
+        from workloads import device as wd
+        W = wl.make_weights(wl.NINE_B, seed, fmt=fmt)
+        self.Wd = wd.weights_to_device(W)
+        del W
+        self.max_rows, self.max_slots, self.gemm_path, self.fmt = max_rows, max_slots, gemm_path, fmt
+        self.engines = {}
+        self.stream = torch.cuda.current_stream()
+
+    def engine(self, gamma_max):
+        import torch
+        import workloads as wl
+        from workloads import device as wd
+        from speculative_decoding_verify_ragged_gb300 import VerifyEngine
+        if gamma_max not in self.engines:
+            self.engines.clear()
+            torch.cuda.empty_cache()
+            e = VerifyEngine(wd.config(wl.NINE_B, gamma_max, self.fmt), self.Wd, max_rows=self.max_rows,
+                             max_slots=self.max_slots)
+            e.set_gemm_path(self.gemm_path)
+            self.engines[gamma_max] = e
+        return self.engines[gamma_max]
+
+    def inputs(self, eng, batch, wid, kv_key=None):
+        """The batch on the device with q rebuilt around the target's own p (the
+        input recipe: each draft accepted with its sequence's alpha), from an
+        untimed prepass of the step."""
+        import torch
+        import workloads as wl
+        from workloads import device as wd
+        bd = wd.batch_to_device(batch)
+        if kv_key is not None:
+            wd.normal_bf16_device_(bd["kv_pool"], kv_key)
+        if batch.G == 0:
+            return bd
+        res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1],
+                              probs=True)
+        eng.verify_step(bd, res)
+        assert eng.read_status(res["status"]) == 0
+        gam = batch.draft_lens
+        if (gam == gam[0]).all():
+            alphas = torch.as_tensor(batch.alphas, dtype=torch.float64)
+            wd.retarget_draft_probs_device(bd["draft_probs"], res["probs"], bd["tokens"], int(gam[0]), alphas)
+            batch.draft_probs = bd["draft_probs"].cpu().numpy()
+        else:
+            wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), wid)
+            bd["draft_probs"].copy_(torch.from_numpy(batch.draft_probs.reshape(batch.G, -1)))
+        del res
+        # the prepass realigned the page tables: put the step's inputs back
+        bd["page_table"].copy_(torch.from_numpy(batch.page_table))
+        bd["num_pages"].copy_(torch.from_numpy(batch.num_pages))
+        bd["free_pages"].copy_(torch.from_numpy(batch.free_pages))
+        bd["num_free_in"].fill_(batch.num_free)
+        torch.cuda.synchronize()
+        return bd
+
+    def time_steps(self, eng, batch, bd, args, u_key, world, clocks_for=None):
+        """W untimed steps, then K steps back to back between two events on the
+        launching stream (barrier + synchronize on both sides), with the
+        LM-head launch of each step bracketed by its own event pair; then a few
+        steps with every phase boundary recorded (serialised, informational)."""
+        import torch
+        import workloads as wl
+        from workloads import device as wd
+        from speculative_decoding_verify_ragged_gb300 import PHASES, kernel_launches
+        stream = self.stream
+        nsteps = args.warmup + args.steps
+        g = wl.rng(*u_key)
+        U = torch.from_numpy(np.stack([wl.uniform24(g, batch.R) for _ in range(nsteps)])).cuda()
+        res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1])
+        # one emitted-offsets row per step, so the token count is read after the timed region
+        EO = torch.zeros((nsteps, batch.B + 1), dtype=torch.int32, device="cuda")
+
+        def step(i):
+            bd["uniforms"] = U[i]
+            res["emitted_offsets"] = EO[i]
+            eng.verify_step(bd, res, stream)
+
+        for i in range(args.warmup):
+            step(i)
+        assert eng.read_status(res["status"]) == 0
+        torch.cuda.synchronize()
+        K_LM = PHASES.index("lm_head")
+        lm_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)]
+        for a_, b_ in lm_pairs:
+            a_.record(stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        clocks = None
+        if clocks_for is not None and not args.quick:
+            clocks = ClockSampler(clocks_for)
+            # pre-roll: the same step back to back for ~1 s so the clock samples see the GPU under load
+            t_end = time.perf_counter() + 1.0
+            while time.perf_counter() < t_end:
+                step(args.warmup - 1)
+                torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        launches0 = kernel_launches()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for j, i in enumerate(range(args.warmup, nsteps)):
+            evs = [None] * (len(PHASES) + 1)
+            evs[K_LM], evs[K_LM + 1] = lm_pairs[j]
+            eng.set_phase_events(evs)
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        launches = kernel_launches() - launches0
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop() if clocks else None
+        eng.set_phase_events(None)
+        assert eng.read_status(res["status"]) == 0
+        lm_ms = [a_.elapsed_time(b_) for a_, b_ in lm_pairs]
+        # phase breakdown, every boundary recorded (serialised), outside the timed region
+        nph = min(10, args.steps)
+        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
+        for j in range(nph):
+            eng.set_phase_events(evsets[j])
+            step(args.warmup + j)
+        torch.cuda.synchronize()
+        eng.set_phase_events(None)
+        assert eng.read_status(res["status"]) == 0
+        phase_us = {p: statistics.mean(es[k].elapsed_time(es[k + 1]) for es in evsets) * 1e3
+                    for k, p in enumerate(PHASES)}
+        tokens = int(EO[args.warmup:, batch.B].sum().item())
+        return dict(elapsed_ms=t0.elapsed_time(t1), tokens=tokens, lm_us=statistics.mean(lm_ms) * 1e3,
+                    phase_us=phase_us, launches=int(launches), clocks=clk, U=U)
+
+
+def point_summary(batch, ms, tokens_per_s, lm_us, phase_us, hbm, tflops, peak_kind, traffic=None):
+    """One curve point: step time, tokens/s, the step's and the LM head's
+    roofline fractions, and each phase's fractions (serialised timings)."""
+    work = phase_work(batch)
+    phases = {}
+    for p, us in phase_us.items():
+        f, b = work[p]
+        t = us * 1e-6
+        phases[p] = {"us": us, "hbm_frac": b / t / 1e9 / hbm if t > 0 else None,
+                     "tensor_frac": f / t / 1e12 / tflops if t > 0 else None}
+    gemm = ("qkv", "o_proj", "ffn", "lm_head")
+    g_t = sum(phase_us[p] for p in gemm) * 1e-6
+    g_f = sum(work[p][0] for p in gemm)
+    g_b = sum(work[p][1] for p in gemm)
+    lay = ("qkv", "o_proj", "ffn")
+    l_t = sum(phase_us[p] for p in lay) * 1e-6
+    l_f = sum(work[p][0] for p in lay)
+    B, gam = int(batch.B), [int(x) for x in batch.draft_lens]
+    return {"B": B, "gamma": gam[0] if len(set(gam)) == 1 else gam, "rows": int(batch.R), "ms_per_step": ms,
+            "tokens_per_s": tokens_per_s, "rows_per_s": batch.R / (ms / 1e3),
+            "step_roofline": step_roofline(batch, ms, hbm, tflops),
+            "lm_head": kernel_roofline(int(batch.R), lm_us, hbm, tflops, peak_kind, traffic),
+            "gemm_hbm_frac": g_b / g_t / 1e9 / hbm, "gemm_tensor_frac": g_f / g_t / 1e12 / tflops,
+            "layer_gemm_tensor_frac": l_f / l_t / 1e12 / tflops,
+            "phases_serialised": phases}
+
+
+def init_dist():
+    import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    W, batch = make_host_workload(args.workload)
-    Wd = wd.weights_to_device(W)
-    gmax = int(batch.gamma_max)
-    eng = VerifyEngine(wd.config(wl.NINE_B, gmax), Wd, max_rows=max(64, batch.R), max_slots=max(16, batch.B))
+    return rank, world, local
 
-    # input recipe: q built around the target's own p so each draft is accepted w.p. alpha
-    bd = wd.batch_to_device(batch)
-    res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1], probs=True)
-    eng.verify_step(bd, res)
-    assert eng.read_status(res["status"]) == 0
-    wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), args.workload)
-    del res
 
-    # device-resident inputs; one set of uniforms per step
-    bd = wd.batch_to_device(batch)
-    nsteps = args.warmup + args.steps
-    g = wl.rng(args.workload, wl.S_U, 1000 + rank)
-    U = torch.from_numpy(np.stack([wl.uniform24(g, batch.R) for _ in range(nsteps)])).cuda()
-    res = wd.alloc_result(batch.B, batch.R, wl.NINE_B["vocab"], gmax, batch.page_table.shape[1])
-    stream = torch.cuda.current_stream()
-    # one emitted-offsets row per step, so the step count is read after the timed region
-    EO = torch.zeros((nsteps, batch.B + 1), dtype=torch.int32, device="cuda")
-
-    def step(i):
-        bd["uniforms"] = U[i]
-        res["emitted_offsets"] = EO[i]
-        eng.verify_step(bd, res, stream)
-
-    for i in range(args.warmup):
-        step(i)
-    assert eng.read_status(res["status"]) == 0
-    torch.cuda.synchronize()
-
-    # the dominant kernel (LM head) is timed live inside the timed region with one
-    # event pair per step on the launching stream, read after the region; no
-    # other boundary is recorded, so the other kernels keep overlapping
-    K_LM = PHASES.index("lm_head")
-    lm_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
-    for a_, b_ in lm_pairs:
-        a_.record(stream)
-        b_.record(stream)
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(local) if not args.quick else None
-    # pre-roll: the same step back to back for ~1 s so the clock samples see the GPU under load
-    t_end = time.perf_counter() + (0.0 if args.quick else 1.0)
-    while time.perf_counter() < t_end:
-        step(args.warmup - 1)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    launches0 = kernel_launches()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for j, i in enumerate(range(args.warmup, nsteps)):
-        evs = [None] * (len(PHASES) + 1)
-        evs[K_LM], evs[K_LM + 1] = lm_pairs[j]
-        eng.set_phase_events(evs)
-        step(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    launches = kernel_launches() - launches0
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop() if clocks else None
-    lm_ms = [a_.elapsed_time(b_) for a_, b_ in lm_pairs]
-
-    # phase breakdown (informational, outside the timed region): every boundary
-    # recorded, which serialises the kernels at the boundaries
-    nph = min(20, args.steps)
-    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
-    for j in range(nph):
-        eng.set_phase_events(evsets[j])
-        step(args.warmup + j)
-    torch.cuda.synchronize()
-    eng.set_phase_events(None)
-    assert eng.read_status(res["status"]) == 0
-    phase_ms = {p: [es[k].elapsed_time(es[k + 1]) for es in evsets] for k, p in enumerate(PHASES)}
-
-    tokens_rank = int(EO[args.warmup:, batch.B].sum().item())
-    # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(eng, batch, bd, U, args, stream, tokens_rank) if not args.quick else None
-    elapsed_ms, tokens, e2e_ms = reduce_over_ranks(t0.elapsed_time(t1), tokens_rank,
-                                                   e2e["ms_per_step"] if e2e else None, "cuda")
-    value = tokens / (elapsed_ms / 1e3)
-    ms_per_step = elapsed_ms / args.steps
-    if e2e is not None:
-        e2e["ms_per_step"] = e2e_ms
-        e2e["value"] = tokens / (e2e_ms * args.steps / 1e3)
-
-    copy_gbs = box_copy_gbps() if not args.quick else None
-    hbm, tflops, peak_kind = measured_peaks()
-    lm_avg = statistics.mean(lm_ms)
-    lm_bytes = lm_head_algorithmic_bytes(batch.R)
-    achieved = lm_bytes / (lm_avg / 1e3) / 1e9
-    step_bytes = step_algorithmic_bytes(batch)
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**workload_desc(args.workload), "parallelism": f"replicas{world}",
-                   "verify_rows_per_step": batch.R},
-        "e2e": e2e,
-        "gpu_launches": int(launches),
-        "clocks": clk,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": lm_head_traffic(args.workload),
-                     "kernel": "LM-head GEMM (EPI_LMHEAD)",
-                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lm_bytes,
-                     "avg_launch_us": lm_avg * 1e3},
-        "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes,
-                          "achieved_GBps": step_bytes / (ms_per_step / 1e3) / 1e9,
-                          "frac": step_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
-        "phases_us_serialised": {p: statistics.mean(v) * 1e3 for p, v in phase_ms.items()},
-        "emitted_tokens_per_step": tokens / (args.steps * world),
-        "box_copy_GBps": copy_gbs,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
-        line["cpu_baseline"] = cpu_baseline(W, batch)
+def finish_dist(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_curve(args):
+    """Workload 4: K timed steps at each point of the verify-row curve; the
+    line's value, e2e and roofline are the headline point's."""
+    import torch
+    import workloads as wl
+    rank, world, local = init_dist()
+    points = parse_points(args.points) if args.points else list(CURVE_POINTS)
+    headline = HEADLINE if HEADLINE in points else points[-1]
+    bench = Bench(4, max(B * (g + 1) for B, g in points), max(B for B, _ in points), args.gemm_path)
+    hbm, tflops, peak_kind = measured_peaks()
+    curve, head = [], None
+    for B, g in points:
+        eng = bench.engine(max(1, g))
+        batch = host_batch(4, B, g, lazy=True)
+        bd = bench.inputs(eng, batch, 4, kv_key=wl._key(4, wl.S_KV, 1000 * B + g))
+        is_head = (B, g) == headline
+        t = bench.time_steps(eng, batch, bd, args, (4, wl.S_U, 1000 + 16 * B + g + rank), world,
+                             clocks_for=local if is_head else None)
+        elapsed, tokens, _ = reduce_over_ranks(t["elapsed_ms"], t["tokens"], None, "cuda")
+        ms = elapsed / args.steps
+        pt = point_summary(batch, ms, tokens / (elapsed / 1e3), t["lm_us"], t["phase_us"], hbm, tflops, peak_kind,
+                           lm_head_traffic(batch.R))
+        curve.append(pt)
+        if is_head:
+            e2e = run_e2e(eng, batch, bd, t["U"], args, bench.stream, t["tokens"]) if not args.quick else None
+            head = (batch, pt, t, e2e)
+        del bd
+        torch.cuda.empty_cache()
+    batch, pt, t, e2e = head
+    elapsed, tokens, e2e_ms = reduce_over_ranks(t["elapsed_ms"], t["tokens"],
+                                                e2e["ms_per_step"] if e2e else None, "cuda")
+    if e2e is not None:
+        e2e["ms_per_step"] = e2e_ms
+        e2e["value"] = tokens / (e2e_ms * args.steps / 1e3)
+    # the measured crossover: the first row count whose GEMMs run closer to the
+    # tensor peak than to the HBM peak; the modelled one from the weights' bytes and flops
+    cross = next((p["rows"] for p in sorted(curve, key=lambda x: x["rows"])
+                  if p["gemm_tensor_frac"] >= p["gemm_hbm_frac"]), None)
+    w_bytes = 2 * (48 * 128 * 4096 + 4096 * 4096 + 3 * 12288 * 4096 + 151936 * 4096)
+    model = (w_bytes / (hbm * 1e9)) / (w_bytes / (tflops * 1e12))
+    line = {
+        "metric": METRIC, "value": tokens / (elapsed / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_desc(4, points, headline), "parallelism": f"replicas{world}"},
+        "e2e": e2e, "gpu_launches": t["launches"], "clocks": t["clocks"],
+        "roofline": pt["lm_head"], "step_roofline": pt["step_roofline"],
+        "curve": curve,
+        "crossover": {"measured_rows": cross, "model_rows": model,
+                      "rule": "first curve point whose GEMMs reach a larger fraction of the tensor peak than of "
+                              "the HBM peak"},
+        "peaks": {"hbm_GBps": hbm, "bf16_TFLOPs": tflops, "kind": peak_kind},
+        "box_copy_GBps": box_copy_gbps() if not args.quick else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        line["cpu_baseline"] = cpu_baseline(headline)
+    finish_dist(world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    """Workloads 2 and 3: one batch, K timed steps."""
+    import workloads as wl
+    rank, world, local = init_dist()
+    batch = host_batch(args.workload)
+    bench = Bench(args.workload, max(64, batch.R), max(16, batch.B), args.gemm_path)
+    eng = bench.engine(int(batch.gamma_max))
+    bd = bench.inputs(eng, batch, args.workload)
+    t = bench.time_steps(eng, batch, bd, args, (args.workload, wl.S_U, 1000 + rank), world, clocks_for=local)
+    tokens_rank = t["tokens"]
+    e2e = run_e2e(eng, batch, bd, t["U"], args, bench.stream, tokens_rank) if not args.quick else None
+    elapsed_ms, tokens, e2e_ms = reduce_over_ranks(t["elapsed_ms"], tokens_rank,
+                                                   e2e["ms_per_step"] if e2e else None, "cuda")
+    if e2e is not None:
+        e2e["ms_per_step"] = e2e_ms
+        e2e["value"] = tokens / (e2e_ms * args.steps / 1e3)
+    hbm, tflops, peak_kind = measured_peaks()
+    ms = elapsed_ms / args.steps
+    pt = point_summary(batch, ms, tokens / (elapsed_ms / 1e3), t["lm_us"], t["phase_us"], hbm, tflops, peak_kind,
+                       lm_head_traffic(batch.R))
+    line = {
+        "metric": METRIC, "value": tokens / (elapsed_ms / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_desc(args.workload), "parallelism": f"replicas{world}",
+                   "verify_rows_per_step": batch.R},
+        "e2e": e2e, "gpu_launches": t["launches"], "clocks": t["clocks"],
+        "roofline": pt["lm_head"], "step_roofline": pt["step_roofline"],
+        "phases_us_serialised": t["phase_us"],
+        "emitted_tokens_per_step": tokens / (args.steps * world),
+        "box_copy_GBps": box_copy_gbps() if not args.quick else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
+        line["cpu_baseline"] = cpu_baseline((1, 7) if args.workload == 2 else None)
+    finish_dist(world)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------
-# roofline crossover sweep (9B-class layer, ctx 2048, uniform gamma)
+# the whole roofline crossover sweep (9B-class layer, ctx 2048, uniform gamma)
 # ---------------------------------------------------------------------------
 
 SWEEP_B = (1, 4, 16, 32, 64, 128)
@@ -397,123 +601,27 @@ SWEEP_GAMMA = (0, 1, 2, 3, 4, 7, 8)
 def run_sweep(args):
     import torch
     import workloads as wl
-    from workloads import device as wd
-    from speculative_decoding_verify_ragged_gb300 import PHASES, VerifyEngine
-
-    torch.cuda.set_device(0)
-    if args.sweep_points:
-        points = [tuple(int(v) for v in pt.split(":")) for pt in args.sweep_points.split(",")]
-    else:
-        points = [(B, g) for B in SWEEP_B for g in SWEEP_GAMMA]
-    max_rows = max(B * (g + 1) for B, g in points)
-    max_slots = max(B for B, _ in points)
-    W = wl.make_weights(wl.NINE_B, 4)
-    Wd = wd.weights_to_device(W)
-    del W
-    engines = {}
-
-    def engine_for(g):
-        # one context per draft length: gamma_max sizes the attention's query tile
-        gm = max(1, g)
-        if gm not in engines:
-            engines.clear()
-            torch.cuda.empty_cache()
-            e = VerifyEngine(wd.config(wl.NINE_B, gm), Wd, max_rows=max_rows, max_slots=max_slots)
-            e.set_gemm_path(args.gemm_path)
-            engines[gm] = e
-        return engines[gm]
+    init_dist()
+    points = parse_points(args.sweep_points) if args.sweep_points else \
+        [(B, g) for B in SWEEP_B for g in SWEEP_GAMMA]
+    bench = Bench(4, max(B * (g + 1) for B, g in points), max(B for B, _ in points), args.gemm_path)
     hbm, tflops, peak_kind = measured_peaks()
-    stream = torch.cuda.current_stream()
     results = []
     for B, g in points:
-        eng = engine_for(g)
-        batch = wl.workload4(B, g, kv_fill="lazy", extra_pages=4 * B + 8)
-        bd = wd.batch_to_device(batch)
-        # the KV pool: bf16 N(0,1) drawn on the device (seeded), the same recipe as the host fill
-        gen = torch.Generator(device="cuda")
-        gen.manual_seed(4_000_000 + 1000 * B + g)
-        bd["kv_pool"].normal_(generator=gen)
-        # q rebuilt around the target's p for per-draft acceptance 0.8
-        if batch.G > 0:
-            res = wd.alloc_result(B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1],
-                                  probs=True)
-            eng.verify_step(bd, res)
-            assert eng.read_status(res["status"]) == 0
-            wl.retarget_draft_probs(batch, res["probs"].cpu().numpy(), 4)
-            del res
-            bd["draft_probs"] = torch.from_numpy(batch.draft_probs.reshape(batch.G, -1)).cuda()
-            # the prepass realigned the page tables: put the step's inputs back
-            bd["page_table"].copy_(torch.from_numpy(batch.page_table))
-            bd["num_pages"].copy_(torch.from_numpy(batch.num_pages))
-            bd["free_pages"].copy_(torch.from_numpy(batch.free_pages))
-            bd["num_free_in"].fill_(batch.num_free)
-        nsteps = args.warmup + args.steps
-        gu = wl.rng(4, wl.S_U, 1000 + B * 16 + g)
-        U = torch.from_numpy(np.stack([wl.uniform24(gu, batch.R) for _ in range(nsteps)])).cuda()
-        res = wd.alloc_result(B, batch.R, wl.NINE_B["vocab"], batch.gamma_max, batch.page_table.shape[1])
-        EO = torch.zeros((nsteps, B + 1), dtype=torch.int32, device="cuda")
-
-        def step(i):
-            bd["uniforms"] = U[i]
-            res["emitted_offsets"] = EO[i]
-            eng.verify_step(bd, res, stream)
-
-        for i in range(args.warmup):
-            step(i)
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.warmup, nsteps):
-            step(i)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        assert eng.read_status(res["status"]) == 0
-        ms = t0.elapsed_time(t1) / args.steps
-        tokens = int(EO[args.warmup:, B].sum().item())
-        # phases, every boundary recorded (serialised), outside the timed loop
-        nph = min(10, args.steps)
-        evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(len(PHASES) + 1)] for _ in range(nph)]
-        for j in range(nph):
-            eng.set_phase_events(evsets[j])
-            step(args.warmup + j)
-        torch.cuda.synchronize()
-        eng.set_phase_events(None)
-        ph_us = {p: statistics.mean(es[k].elapsed_time(es[k + 1]) for es in evsets) * 1e3
-                 for k, p in enumerate(PHASES)}
-        work = phase_work(batch)
-        flops = sum(f for f, _ in work.values())
-        nbytes = sum(b for _, b in work.values())
-        t_hbm = nbytes / (hbm * 1e9) * 1e6
-        t_tc = flops / (tflops * 1e12) * 1e6
-        phases = {}
-        for p in PHASES:
-            f, b = work[p]
-            t = ph_us[p] * 1e-6
-            phases[p] = {"us": ph_us[p], "hbm_frac": b / t / 1e9 / hbm if t > 0 else None,
-                         "tensor_frac": f / t / 1e12 / tflops if t > 0 else None}
-        gemm = ("qkv", "o_proj", "ffn", "lm_head")
-        g_t = sum(ph_us[p] for p in gemm) * 1e-6
-        g_f = sum(work[p][0] for p in gemm)
-        g_b = sum(work[p][1] for p in gemm)
-        pt = {"sweep": "crossover", "B": B, "gamma": g, "rows": batch.R, "ms_per_step": ms,
-              "tokens_per_s": tokens / (ms * args.steps / 1e3), "rows_per_s": batch.R / (ms / 1e3),
-              "step_bound": "tensor" if t_tc > t_hbm else "hbm",
-              "step_roofline_us": max(t_hbm, t_tc), "step_frac": max(t_hbm, t_tc) / (ms * 1e3),
-              "t_hbm_us": t_hbm, "t_tensor_us": t_tc,
-              "gemm_hbm_frac": g_b / g_t / 1e9 / hbm, "gemm_tensor_frac": g_f / g_t / 1e12 / tflops,
-              "phases": phases, "gemm_path": args.gemm_path}
+        eng = bench.engine(max(1, g))
+        batch = host_batch(4, B, g, lazy=True)
+        bd = bench.inputs(eng, batch, 4, kv_key=wl._key(4, wl.S_KV, 1000 * B + g))
+        t = bench.time_steps(eng, batch, bd, args, (4, wl.S_U, 1000 + 16 * B + g), 1)
+        ms = t["elapsed_ms"] / args.steps
+        pt = point_summary(batch, ms, t["tokens"] / (t["elapsed_ms"] / 1e3), t["lm_us"], t["phase_us"], hbm,
+                           tflops, peak_kind)
+        pt.update(sweep="crossover", gemm_path=args.gemm_path)
         results.append(pt)
         print(json.dumps(pt), flush=True)
-        del bd, res, U, EO
+        del bd
         torch.cuda.empty_cache()
-    # crossover: the first row count whose GEMMs run closer to the tensor peak than to the HBM peak
-    cross = None
-    for pt in sorted(results, key=lambda x: x["rows"]):
-        if pt["gemm_tensor_frac"] >= pt["gemm_hbm_frac"]:
-            cross = pt["rows"]
-            break
-    # the weights' bytes against the flops per row they carry (2 per weight)
+    cross = next((p["rows"] for p in sorted(results, key=lambda x: x["rows"])
+                  if p["gemm_tensor_frac"] >= p["gemm_hbm_frac"]), None)
     w_bytes = 2 * (48 * 128 * 4096 + 4096 * 4096 + 3 * 12288 * 4096 + 151936 * 4096)
     model = (w_bytes / (hbm * 1e9)) / (w_bytes / (tflops * 1e12))
     # the pages' step model fitted to these steps (ms): B*, best gamma per B, break-even
@@ -715,7 +823,8 @@ def run_e2e(eng, batch, bd, U, args, stream, tokens):
 
     host_in = {
         "seq_lens": pin(batch.seq_lens.astype(np.int32)), "draft_lens": pin(batch.draft_lens.astype(np.int32)),
-        "tokens": pin(batch.tokens.astype(np.int32)), "draft_probs": pin(batch.draft_probs.astype(np.float32)),
+        "tokens": pin(batch.tokens.astype(np.int32)),
+        "draft_probs": pin(batch.draft_probs.astype(np.float32).reshape(batch.G, -1)),
         "page_table": pin(batch.page_table.astype(np.int32)), "num_pages": pin(batch.num_pages.astype(np.int32)),
         "num_free_in": pin(np.array([batch.num_free], np.int32)),
     }
@@ -758,55 +867,100 @@ def run_e2e(eng, batch, bd, U, args, stream, tokens):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def cpu_baseline(W, batch):
-    """The oracle as it stands, timed on this host on one full step of the workload."""
+# ---------------------------------------------------------------------------
+# the oracle on the host: the CPU baseline and the reference arm
+# ---------------------------------------------------------------------------
+# A bounded sample of the workload: ONE sequence of the point's shape (its
+# gamma + 1 rows, context 2048, its own pages of bf16 N(0,1) KV) through the
+# whole step, q rebuilt around the oracle's own p.  The oracle runs with its
+# BLAS pinned to one thread (the environment below is set before numpy loads,
+# in a child process), warmed once before timing.
+
+def oracle_sample(gamma, ctx=2048):
+    import workloads as wl
     from oracle import verify_step as o
-    t = time.perf_counter()
-    out = o.verify_step(batch, W)
-    dt = time.perf_counter() - t
-    toks = int(out["emitted_offsets"][-1])
-    return {"value": toks / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one full verify step of the bench workload ({batch.R} rows), {dt:.1f} s"}
+    W = wl.make_weights(wl.NINE_B, 4)
+    batch = wl.make_batch(wl.NINE_B, 4, seq_lens=[ctx], draft_lens=[gamma], gamma_max=max(1, gamma),
+                          alphas=[0.8])
+    if batch.G:
+        fw = o.forward(batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens,
+                       batch.tokens)
+        wl.retarget_draft_probs(batch, fw["probs"].astype(np.float32), 4)
+    return W, batch
 
 
-# ---------------------------------------------------------------------------
-# reference arm: the oracle
-# ---------------------------------------------------------------------------
+def oracle_steps(W, batch, n_min, seconds_min, seconds_max, key):
+    """Time oracle steps (fresh uniforms each) until both n_min steps and
+    seconds_min have passed (stopping at seconds_max)."""
+    import workloads as wl
+    from oracle import verify_step as o
+    g = wl.rng(4, wl.S_U, key)
+    times, tokens = [], []
+    while len(times) < n_min or (sum(times) < seconds_min and sum(times) < seconds_max):
+        batch.uniforms = wl.uniform24(g, batch.R)
+        t = time.perf_counter()
+        out = o.verify_step(batch, W)
+        times.append(time.perf_counter() - t)
+        tokens.append(int(out["emitted_offsets"][-1]))
+    return times, tokens
+
+
+def cpu_oracle_child(spec):
+    """In the child process: warm the oracle once, then time it."""
+    gamma, ctx, n_min, s_min, s_max = (int(x) for x in spec.split(":"))
+    W, batch = oracle_sample(gamma, ctx)
+    oracle_steps(W, batch, 1, 0, 0, 3000)
+    times, tokens = oracle_steps(W, batch, n_min, s_min, s_max, 3001)
+    print(json.dumps({"times": times, "tokens": tokens, "rows": batch.R}), flush=True)
+
+
+def run_oracle_child(gamma, ctx, n_min, s_min, s_max):
+    env = dict(os.environ, **ONE_THREAD)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-child",
+                        f"{gamma}:{ctx}:{n_min}:{s_min}:{s_max}"], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(shape):
+    """The oracle as it stands, one thread, on one sequence of the point's shape
+    (about 10 to 30 s of CPU work)."""
+    gamma, ctx = (shape[1], 2048) if shape is not None else (2, 4352)
+    d = run_oracle_child(gamma, ctx, 1, 10, 30)
+    total = sum(d["times"])
+    return {"value": sum(d["tokens"]) / total, "unit": UNIT, "cores": os.cpu_count(), "threads": 1, "kind": "oracle",
+            "sample": f"{len(d['times'])} oracle steps of one sequence of the workload's shape ({d['rows']} rows, "
+                      f"gamma {gamma}, ctx {ctx}), BLAS on one thread, warmed once, {total:.1f} s"}
+
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import workloads as wl
-    from oracle import verify_step as o
-    W, batch = make_host_workload(args.workload)
-    # the same recipe for q, built from the oracle's own target probabilities
-    fw = o.forward(batch.dims, W, batch.kv_pool, batch.page_table, batch.seq_lens, batch.draft_lens,
-                   batch.tokens)
-    wl.retarget_draft_probs(batch, fw["probs"].astype(np.float32), args.workload)
-    g = wl.rng(args.workload, wl.S_U, 1000)
-    nsteps = args.warmup + args.steps
-    U = [wl.uniform24(g, batch.R) for _ in range(nsteps)]
-    # a step of the oracle takes seconds: each step is a bounded sample of the
-    # workload (the first draft block's rows of the batch)
-    times, tokens = [], 0
-    for i in range(nsteps):
-        batch.uniforms = U[i]
-        t = time.perf_counter()
-        out = o.verify_step(batch, W)
-        dt = time.perf_counter() - t
-        if i >= args.warmup:
-            times.append(dt)
-            tokens += int(out["emitted_offsets"][-1])
+    if args.workload == 4:
+        points = parse_points(args.points) if args.points else list(CURVE_POINTS)
+        headline = HEADLINE if HEADLINE in points else points[-1]
+        gamma, ctx, desc = headline[1], 2048, workload_desc(4, points, headline)
+    elif args.workload == 2:
+        gamma, ctx, desc = 7, 2048, workload_desc(2)
+    else:
+        gamma, ctx, desc = 2, 4352, workload_desc(3)
+    # the oracle as it stands: each step one verify pass over one sequence of the
+    # workload's shape (a bounded sample), W untimed steps then K timed ones
+    d = run_oracle_child(gamma, ctx, args.warmup + args.steps, 0, 0)
+    times = d["times"][args.warmup:]
     total = sum(times)
-    value = tokens / total
+    value = sum(d["tokens"][args.warmup:]) / total
+    sample = (f"each step: one oracle verify pass over one sequence of the workload's shape ({d['rows']} rows, "
+              f"gamma {gamma}, ctx {ctx}), BLAS on one thread")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {**workload_desc(args.workload), "parallelism": "host"},
+            "config": {**desc, "parallelism": "host"},
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{args.steps} full verify steps of the workload on the host"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "threads": 1, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -943,8 +1097,21 @@ def run_timeline(args):
 
 def main():
     args = parse()
+    if args.cpu_oracle_child:
+        cpu_oracle_child(args.cpu_oracle_child)
+        return
     if args.warmup < 3:
         args.warmup = 3
+    rank, world, _ = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # no outer launcher: start the N replicas here, one process per GPU
+        port = 29400 + (os.getpid() % 1000)
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.run(cmd).returncode)
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args)
     elif args.timeline:
@@ -953,6 +1120,8 @@ def main():
         run_sweep(args)
     elif args.workload == 5:
         run_swarm(args)
+    elif args.workload == 4:
+        run_curve(args)
     else:
         run_ours(args)
 

@@ -58,6 +58,15 @@ def test_single_process_is_unchanged():
 
 def test_reference_arm_other_ranks_exit_without_work():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_gpu_count_must_match_the_launcher():
+    """Under a launcher, --gpus N must equal WORLD_SIZE (a mismatch would report
+    the wrong job size); the run stops with a non-zero code before any work."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="3", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "WORLD_SIZE 3" in r.stderr
