@@ -483,7 +483,7 @@ static bool use_tc(const sdv_ctx* c, int R) {
 }
 
 // Run one GEMM: pick the kernel and the activation tile height, then launch
-// over min(SMs, units) CTAs.  xmaps: the activation map for each tile height;
+// over min(SMs, units) CTAs (tcgen05 bf16: clusters of CTAs, see gemm_tc.cu).  xmaps: the activation map for each tile height;
 // s0, s1: the scale maps of int4 weights (a0, a1 are then code maps).
 static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
                             const CUtensorMap* xmaps, GemmParams g, cudaStream_t s,
@@ -502,17 +502,14 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
     if (e == cudaSuccess && g.defer_fixup) e = launch_gemm_tc_fixup(epi, nt, g, grid, s);
     return e;
   }
-  const bool tc = use_tc(c, g.R);
-  const int nt = tc ? gemm_tc_tile_rows(g.R) : gemm_tile_rows(g.R);
+  // bf16 weights on tcgen05: the kernel's own launcher picks the tile height
+  // and the cluster size that shares each weight tile
+  if (use_tc(c, g.R)) return launch_gemm_tc(epi, xp, a0, a1, xmaps, g, c->L.grid_gemm, s);
+  const int nt = gemm_tile_rows(g.R);
   g.n_tiles = (g.R + nt - 1) / nt;
   const long long units = (long long)g.m_tiles * g.n_tiles * g.kb;
   const int grid = static_cast<int>(units < c->L.grid_gemm ? units : c->L.grid_gemm);
-  const CUtensorMap* x = &xmaps[nt_index(nt)];
-  if (!tc) return launch_gemm(epi, nt, xp, a0, a1, x, g, grid, s);
-  g.defer_fixup = nt >= kDeferFixupRows ? 1 : 0;
-  cudaError_t e = launch_gemm_tc(epi, nt, xp, a0, a1, x, g, grid, s);
-  if (e == cudaSuccess && g.defer_fixup) e = launch_gemm_tc_fixup(epi, nt, g, grid, s);
-  return e;
+  return launch_gemm(epi, nt, xp, a0, a1, &xmaps[nt_index(nt)], g, grid, s);
 }
 
 static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,

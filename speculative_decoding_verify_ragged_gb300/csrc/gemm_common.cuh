@@ -51,9 +51,13 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) 
 // weight row within the tile); 128 threads, tid = m for the column-wise kinds.
 // Every per-row global load of a batch of rows is issued before any is used,
 // so a batch costs one memory latency instead of one per row.
+//
+// SWIGLU with an RMSNorm row scale: `row_scale`, when given, holds each row's
+// 1 / rms already reduced from the partial sums (row_scale[r - rs_base] for
+// row r); otherwise each chunk reduces them itself.
 template <int EPI, int LD>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, int tm, int row0, int nrows,
-                                              int tid) {
+                                              int tid, const float* row_scale = nullptr, int rs_base = 0) {
   const EpiParams& e = p.epi;
   constexpr int RB = 16;  // rows per batch
   if constexpr (EPI == EPI_RESID) {
@@ -116,7 +120,10 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, i
     // is the next GEMM's input, written as bf16 hi + lo planes
     const int j = tid & 63;
     const int f = tm * 64 + j;
-    if (e.sq_in) {
+    if (e.sq_in && row_scale) {
+      for (int n = tid; n < nrows; n += 4 * kWarp) epi[n * LD + BM] = row_scale[row0 + n - rs_base];
+      named_sync(1, 4 * kWarp);
+    } else if (e.sq_in) {
       // the input was x * gain: each row's 1 / rms(x) from the partial sums of x^2
       const int warp = tid >> 5, lane = tid & 31;
       for (int n = warp; n < nrows; n += 4) {
@@ -176,37 +183,47 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, i
       }
     }
   } else if constexpr (EPI == EPI_LMHEAD) {
+    // eight lanes per activation row, four rows per warp, sixteen rows per
+    // pass: a lane holds 16 of the tile's 128 logits of its row (columns
+    // sub + 8 i), so the row's maximum and sum of exp take three shuffle
+    // levels, and the four rows of a warp run side by side
     const int warp = tid >> 5, lane = tid & 31;
-    for (int n = warp; n < nrows; n += 4) {
+    const int sub = lane & 7;
+    for (int n0 = 0; n0 < nrows; n0 += 16) {
+      const int n = n0 + warp * 4 + (lane >> 3);
+      const bool live = n < nrows;
       const int r = row0 + n;
-      float v[4];
+      float v[16];
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = tm * BM + lane + 32 * i;
-        v[i] = epi[n * LD + lane + 32 * i];
-        if (col < p.N) {
+      for (int i = 0; i < 16; ++i) v[i] = live ? epi[n * LD + sub + 8 * i] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int col = tm * BM + sub + 8 * i;
+        if (live && col < p.N) {
           e.out_f32[(long long)r * e.ld_f32 + col] = v[i];
           mx = fmaxf(mx, v[i]);
         }
       }
-      mx = warp_max(mx);
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       float s = 0.f;
       int arg = 0x7FFFFFFF;  // smallest column holding the tile's maximum (greedy verification)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int col = tm * BM + lane + 32 * i;
-        if (col < p.N) {
+      for (int i = 0; i < 16; ++i) {
+        const int col = tm * BM + sub + 8 * i;
+        if (live && col < p.N) {
           s += exp2f((v[i] - mx) * kLog2e);
           if (v[i] == mx) arg = min(arg, col);
         }
       }
-      s = warp_sum(s);
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       if (e.argmax) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
+        for (int o = 1; o < 8; o <<= 1) arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, o));
       }
-      if (lane == 0) {
+      if (live && sub == 0) {
         e.stats[(long long)tm * e.stats_ld + r] = make_float2(mx, s);
         if (e.argmax) e.argmax[(long long)tm * e.stats_ld + r] = arg;
       }
@@ -320,15 +337,15 @@ __device__ __forceinline__ void tc_store_part16(float* slot_base, int c0, int m,
 // order, 16 columns at a time, and each 16-column chunk goes through the fused
 // epilogue.  The loads of up to four parts are issued together, and the next
 // chunk's first loads are in flight while the current chunk's epilogue runs.
-template <int EPI, int NT, int LD>
+template <int EPI, int LD>
 __device__ __forceinline__ void tc_fixup_tile(const GemmParams& p, int tile, int c_first, int c_last,
-                                              long long total, float* epi, int m, int rows) {
+                                              long long total, float* epi, int m, int rows, int nt) {
   const int P = gridDim.x;
   const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
   auto src_of = [&](int cc, int c0) {
     const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
     const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
-    return p.partials + (size_t)slot * BM * NT + (size_t)c0 * BM + m;
+    return p.partials + (size_t)slot * BM * nt + (size_t)c0 * BM + m;
   };
   auto issue = [&](float (&w)[4][16], int cc0, int c0) {
 #pragma unroll
@@ -362,7 +379,7 @@ __device__ __forceinline__ void tc_fixup_tile(const GemmParams& p, int tile, int
 #pragma unroll
     for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
     named_sync(1, 4 * kWarp);
-    epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(16, rows - c0), m);
+    epilogue_rows<EPI, LD>(p, epi, tm, tn * nt + c0, min(16, rows - c0), m);
     named_sync(1, 4 * kWarp);
   }
 }

@@ -9,6 +9,18 @@
 // mma.sync path (about 300 TFLOP/s on this GPU) cannot keep up with the weight
 // stream; these instructions run at the full dense bf16 rate.
 //
+// Arithmetic intensity: a weight tile streamed against NT activation rows
+// carries 2 * NT flops per weight byte pair, so at NT = 256 the weights alone
+// ask 7.5 TB/s of the HBM at the tensor peak, and a second 256-row activation
+// tile would stream the same weights again.  Past one tile, the CTAs of a
+// thread-block cluster therefore share each weight tile: two of them load its
+// two 64-row halves with TMA multicast into every CTA of the cluster, and CTA
+// r multiplies it with its own activation tile tg * cs + r.  The weights cross
+// HBM once for any row count up to 8 tiles, and a tile of about R / cs rows
+// keeps the activation stage small enough for four pipeline stages.  A stage
+// is refilled only when every CTA of the cluster has released it (each MMA
+// commit arrives on the stage's barrier in every CTA).
+//
 // Warp roles (192 threads):
 //  * warp 0: TMA producer (one lane) -- weight half-tiles and activation planes
 //    into a multi-stage ring; weights are streamed before waiting for the
@@ -19,6 +31,8 @@
 //  * warps 2-5: epilogue -- tcgen05.ld the accumulator (lane = weight row),
 //    then the stream-K partial/fixup and the fused epilogue shared with the
 //    mma.sync kernel, while the MMAs fill the other accumulator.
+#include <mutex>
+
 #include "gemm_common.cuh"
 #include "tcgen05.cuh"
 
@@ -29,47 +43,106 @@ namespace {
 using namespace gemm;
 using namespace tc;
 constexpr int TC_THREADS = 6 * kWarp;
-constexpr int EC = 16;  // accumulator columns per tcgen05.ld / epilogue chunk
+constexpr int EC = 16;           // accumulator columns per tcgen05.ld / epilogue chunk
+constexpr int kMaxStages = 10;
+constexpr int kMaxCluster = 8;   // portable cluster size
+// staging row stride: eight lanes of a row reading columns sub + 8 i of four
+// consecutive rows hit 32 different banks
+constexpr int EPI_LD = BM + 8;
+constexpr int EPI_BYTES = EC * EPI_LD * 4;
+constexpr int kScaleRows = 256;  // rows of the per-CTA RMSNorm row-scale cache (gate/up)
+// alignment slack + epilogue staging + barriers (full, empty, 2 x 2 accumulator) + TMEM slot and flag +
+// the row-scale cache
+constexpr int FIXED_BYTES = 1024 + EPI_BYTES + (2 * kMaxStages + 4) * 8 + 16 + kScaleRows * 4;
 
-template <int NT, int XP>
-struct TcCfg {
-  static constexpr int B_BYTES = XP * NT * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int EPI_LD = BM + 4;
-  static constexpr int EPI_BYTES = EC * EPI_LD * 4;
-  static constexpr int FIXED = 1024 + EPI_BYTES + 512;
-  static constexpr int FIT = (kSmemBudget - FIXED) / STAGE;
-  static constexpr int STAGES = FIT > 10 ? 10 : FIT;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + EPI_BYTES + (2 * STAGES + 4) * 8 + 16;
-  static constexpr int TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;  // power of two for NT in {16..256}
-  static_assert(STAGES >= 2, "pipeline too shallow");
-  static_assert(SMEM <= kSmemBudget, "shared memory");
-  static_assert(NT % 16 == 0 && NT >= 16 && NT <= 256, "tcgen05 N for M = 128");
-};
+__host__ __device__ constexpr int tc_stage_bytes(int nt, int xp) { return A_BYTES + xp * nt * BK * 2; }
+__host__ __device__ constexpr int tc_stages(int nt, int xp) {
+  return (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp) > kMaxStages
+             ? kMaxStages
+             : (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp);
+}
+static_assert(tc_stages(256, 2) >= 2, "pipeline too shallow");
 
-template <int EPI, int NT, int XP>
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// TMA tile load into the same shared-memory offset of every CTA in `mask`,
+// each CTA's barrier at `bar`'s offset receiving the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask), "l"(policy)
+      : "memory");
+}
+
+// Arrive on the barrier at `bar`'s offset in every CTA of `mask` once every
+// tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t tmem_columns(int nt) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(2 * nt)) c <<= 1;
+  return c;
+}
+
+// Unit u of the GEMM (weight tile, activation-tile group, k-block) and the
+// cluster that owns it: cluster q of Q owns [q * T / Q, (q + 1) * T / Q).
+__device__ __forceinline__ int cluster_of_unit(long long u, long long total, int Q) {
+  return static_cast<int>(((u + 1) * Q - 1) / total);
+}
+
+template <int EPI, int XP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
   SDV_TRACE_SCOPE(SDV_GEMM_SLOT(EPI, p));
-  using C = TcCfg<NT, XP>;
   extern __shared__ uint8_t smem_raw[];
   griddep_launch_dependents();
 
+  const int NT = p.nt, S = p.stages, cs = p.cs;
+  const int STAGE = tc_stage_bytes(NT, XP);
   uint8_t* smem = align1024(smem_raw);
-  float* epi = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + C::EPI_BYTES);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;  // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;         // [2] accumulator drained
+  float* epi = reinterpret_cast<float*>(smem + S * STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + EPI_BYTES);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;  // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;          // [2] accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* row_scale = reinterpret_cast<float*>(tmem_slot + 4);  // [kScaleRows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = cs > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int q = cs > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int Q = static_cast<int>(gridDim.x) / cs;
+  const uint16_t everyone = static_cast<uint16_t>((1u << cs) - 1u);
+  const uint32_t ncols = tmem_columns(NT);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], cs);  // one release per CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -79,44 +152,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(C::TMEM_COLS)
+                 "r"(ncols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA's barriers exist before a peer's multicast can land on them
+  if (cs > 1) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
 
-  const long long total = (long long)p.m_tiles * p.n_tiles * p.kb;
-  const int P = gridDim.x;
-  const int c = blockIdx.x;
-  const long long u_begin = (long long)c * total / P;
-  const long long u_end = (long long)(c + 1) * total / P;
+  const long long total = (long long)p.m_tiles * p.n_groups * p.kb;
+  const long long u_begin = (long long)q * total / Q;
+  const long long u_end = (long long)(q + 1) * total / Q;
+  const int first_tg = static_cast<int>(u_begin / p.kb);  // first (weight tile, group) of this cluster
 
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const int my_units = static_cast<int>(u_end - u_begin);
-      const int pre = my_units < C::STAGES ? my_units : C::STAGES;
+      const int pre = my_units < S ? my_units : S;
       struct Cursor {
-        int tile, k, tm, tn;
+        int tg, k, tm, grp;
       };
       auto start_at = [&](long long u) {
         Cursor cu;
-        cu.tile = static_cast<int>(u / p.kb);
-        cu.k = static_cast<int>(u - (long long)cu.tile * p.kb);
-        cu.tm = cu.tile / p.n_tiles;
-        cu.tn = cu.tile - cu.tm * p.n_tiles;
+        cu.tg = static_cast<int>(u / p.kb);
+        cu.k = static_cast<int>(u - (long long)cu.tg * p.kb);
+        cu.tm = cu.tg / p.n_groups;
+        cu.grp = cu.tg - cu.tm * p.n_groups;
         return cu;
       };
       auto advance = [&](Cursor& cu) {
         if (++cu.k == p.kb) {
           cu.k = 0;
-          ++cu.tile;
-          if (++cu.tn == p.n_tiles) {
-            cu.tn = 0;
+          ++cu.tg;
+          if (++cu.grp == p.n_groups) {
+            cu.grp = 0;
             ++cu.tm;
           }
         }
@@ -124,14 +198,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       auto weights = [&](const Cursor& cu, int stage) {
         const int rowA0 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM;
         const int rowA1 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM + 64;
-        uint8_t* sa = smem + stage * C::STAGE;
-        tma_load_2d_hint(sa, &tmA0, &full[stage], cu.k * BK, rowA0, pol);
-        tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, pol);
+        uint8_t* sa = smem + stage * STAGE;
+        if (cs == 1) {
+          tma_load_2d_hint(sa, &tmA0, &full[stage], cu.k * BK, rowA0, pol);
+          tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, pol);
+        } else if (rank == 0) {
+          tma_load_2d_mc(sa, &tmA0, &full[stage], cu.k * BK, rowA0, everyone, pol);
+        } else if (rank == 1) {
+          tma_load_2d_mc(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, everyone, pol);
+        }
       };
       auto acts = [&](const Cursor& cu, int stage) {
-        uint8_t* sb = smem + stage * C::STAGE + A_BYTES;
-        tma_load_2d(sb, &tmX, &full[stage], cu.k * BK, cu.tn * NT);
-        if constexpr (XP == 2) tma_load_2d(sb + NT * 128, &tmX, &full[stage], cu.k * BK, p.x_lo_row + cu.tn * NT);
+        uint8_t* sb = smem + stage * STAGE + A_BYTES;
+        const int row0 = (cu.grp * cs + rank) * NT;
+        for (int b = 0; b < NT; b += p.x_box) {
+          tma_load_2d(sb + b * 128, &tmX, &full[stage], cu.k * BK, row0 + b);
+          if constexpr (XP == 2)
+            tma_load_2d(sb + (NT + b) * 128, &tmX, &full[stage], cu.k * BK, p.x_lo_row + row0 + b);
+        }
       };
       Cursor cw = start_at(u_begin);
       for (int j = 0; j < pre; ++j) {
@@ -146,60 +230,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       } else {
         Cursor ca = start_at(u_begin);
         for (int j = 0; j < pre; ++j) {
-          mbar_arrive_expect_tx(&full[j], C::STAGE - A_BYTES);
+          mbar_arrive_expect_tx(&full[j], STAGE - A_BYTES);
           acts(ca, j);
           advance(ca);
         }
-        int stage = pre % C::STAGES;
-        uint32_t phase = pre == C::STAGES ? 1u : 0u;
+        int stage = pre % S;
+        uint32_t phase = pre == S ? 1u : 0u;
         bool dead = false;
         for (int j = pre; j < my_units; ++j) {
+          // every CTA of the cluster has released this stage
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             set_status(p.status, SDV_ERR_TIMEOUT);
             dead = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE);
+          mbar_arrive_expect_tx(&full[stage], STAGE);
           weights(cw, stage);
           acts(cw, stage);
           advance(cw);
-          if (++stage == C::STAGES) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
         }
-        // stay until the MMAs have released every stage (no copy in flight at exit)
-        for (int i = 0; i < C::STAGES && !dead; ++i) {
+        // stay until the MMAs of the whole cluster have released every stage
+        // (no copy in flight and no release still to arrive at exit)
+        for (int i = 0; i < S && !dead; ++i) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             set_status(p.status, SDV_ERR_TIMEOUT);
             break;
           }
-          if (++stage == C::STAGES) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
     }
-    return;
-  }
-
-  if (warp == 1) {
+  } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       SDV_GRIDDEP_WAIT();
       if (read_status(p.status) == 0) {
-        constexpr uint32_t idesc = idesc_bf16(BM, NT);
+        const uint32_t idesc = idesc_bf16(BM, NT);
         bool dead = false;
         int stage = 0;
         uint32_t phase = 0;
-        int q = 0;  // piece index
-        for (long long u = u_begin; u < u_end; ++q) {
-          const int tile = static_cast<int>(u / p.kb);
-          const int k0 = static_cast<int>(u - (long long)tile * p.kb);
+        int pc = 0;  // piece index
+        for (long long u = u_begin; u < u_end; ++pc) {
+          const int tg = static_cast<int>(u / p.kb);
+          const int k0 = static_cast<int>(u - (long long)tg * p.kb);
           const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
-          const int buf = q & 1;
-          if (!dead && !mbar_wait(&tempty[buf], ((q >> 1) & 1) ^ 1)) {
+          const int buf = pc & 1;
+          if (!dead && !mbar_wait(&tempty[buf], ((pc >> 1) & 1) ^ 1)) {
             set_status(p.status, SDV_ERR_TIMEOUT);
             dead = true;
           }
@@ -211,7 +294,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               dead = true;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + stage * C::STAGE);
+            const uint32_t a_base = smem_u32(smem + stage * STAGE);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t a = desc_sw128(a_base + kk * 32);
@@ -221,8 +304,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 umma_bf16(d, a, b, idesc, (k > k0 || kk > 0 || pl > 0) ? 1u : 0u);
               }
             }
-            umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
-            if (++stage == C::STAGES) {
+            // frees the stage, in every CTA of the cluster, once these MMAs have read it
+            if (cs > 1) umma_commit_mc(&empty[stage], everyone);
+            else umma_commit(&empty[stage]);
+            if (++stage == S) {
               stage = 0;
               phase ^= 1;
             }
@@ -232,207 +317,369 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
     }
-    __syncwarp();
-    named_sync(2, 5 * kWarp);  // every accumulator read
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
-    return;
-  }
-
-  // ---------------- epilogue warps 2..5 ----------------
-  const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-  const int m = quarter * 32 + lane;     // weight row within the tile
-  const int tid = m;
-  SDV_GRIDDEP_WAIT();
-  if (read_status(p.status) == 0) {
-    constexpr int LD = C::EPI_LD;
-    bool dead = false;
-    int q = 0;
-    for (long long u = u_begin; u < u_end; ++q) {
-      const int tile = static_cast<int>(u / p.kb);
-      const int k0 = static_cast<int>(u - (long long)tile * p.kb);
-      const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
-      const int tm = tile / p.n_tiles, tn = tile - tm * p.n_tiles;
-      const int buf = q & 1;
-      if (!dead && !mbar_wait(&tfull[buf], (q >> 1) & 1)) {
-        set_status(p.status, SDV_ERR_TIMEOUT);
-        dead = true;
-      }
-      tc_fence_after();
-      const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * NT;
-      const int rows = min(NT, p.R - tn * NT);
-
-      // accumulator columns past the last activation row are never read
-      const int cols = (rows + EC - 1) / EC * EC;
-      if (k0 == 0 && k1 == p.kb) {
-        // whole tile in this CTA: epilogue straight from tensor memory
-        for (int c0 = 0; c0 < cols; c0 += EC) {
-          float v[16];
-          tmem_ld16(t_row + c0, v);
-          if (c0 + EC == cols) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
-          }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int m = quarter * 32 + lane;     // weight row within the tile
+    SDV_GRIDDEP_WAIT();
+    // gate/up after the FFN pre-norm: every row's 1 / rms, reduced once from
+    // the O projection's partial sums of x^2 (lanes over rows, so each load
+    // is one coalesced line; the four warps take every fourth partial and
+    // meet in a fixed order) while the first tile's MMAs run; the rows are
+    // this CTA's activation tile (or all rows, when one CTA walks several
+    // tiles of at most kScaleRows rows in total)
+    int rs_base = 0;
+    bool have_scale = false;
+    if constexpr (EPI == EPI_SWIGLU) {
+      if (p.epi.sq_in && read_status(p.status) == 0) {
+        int nrs = 0;
+        if (p.n_groups == 1) {
+          rs_base = rank * NT;
+          nrs = min(NT, p.R - rs_base);
+        } else if (p.R <= kScaleRows) {
+          nrs = p.R;
+        }
+        have_scale = nrs > 0;
+        const EpiParams& e = p.epi;
+        for (int rb = 0; rb < nrs; rb += kWarp) {
+          const int r = rb + lane;
+          float acc = 0.f;
+          if (r < nrs) {
+            constexpr int U = 8;
+            for (int q0 = quarter; q0 < e.sq_parts; q0 += 4 * U) {
+              float w[U];
 #pragma unroll
-          for (int n = 0; n < EC; ++n) epi[n * LD + m] = v[n];
+              for (int u = 0; u < U; ++u) {
+                const int qq = q0 + 4 * u;
+                w[u] = qq < e.sq_parts ? e.sq_in[(long long)qq * e.sq_ld + rs_base + r] : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u) acc += w[u];
+            }
+          }
+          epi[quarter * kWarp + lane] = acc;
           named_sync(1, 4 * kWarp);
-          epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(EC, rows - c0), tid);
+          if (quarter == 0 && r < nrs) {
+            const float ss = ((epi[lane] + epi[kWarp + lane]) + epi[2 * kWarp + lane]) + epi[3 * kWarp + lane];
+            row_scale[r] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
+          }
           named_sync(1, 4 * kWarp);
-        }
-      } else {
-        // tile cut between CTAs: store this piece, the last arrival sums them in CTA order
-        const long long tu = (long long)tile * p.kb;
-        const int c_first = cta_of_unit(tu, total, P);
-        const int c_last = cta_of_unit(tu + p.kb - 1, total, P);
-        const int my_slot = 2 * c + (tile == static_cast<int>(u_begin / p.kb) ? 0 : 1);
-        float* mine = p.partials + (size_t)my_slot * BM * NT;
-        for (int c0 = 0; c0 < cols; c0 += EC) {
-          float v[16];
-          tmem_ld16(t_row + c0, v);
-          tc_store_part16(mine, c0, m, v);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
-        if (p.defer_fixup) {  // the fixup kernel sums the parts once this grid is done
-          u += k1 - k0;
-          continue;
-        }
-        __threadfence();
-        named_sync(1, 4 * kWarp);
-        if (m == 0) {
-          const int old = atomicAdd(&p.counters[tile], 1);
-          *flag = (old == c_last - c_first) ? 1 : 0;
-        }
-        named_sync(1, 4 * kWarp);
-        const bool last = *flag != 0;
-        if (last) {
-          __threadfence();
-          static_assert(EC == 16, "16-column epilogue chunks");
-          tc_fixup_tile<EPI, NT, LD>(p, tile, c_first, c_last, total, epi, m, rows);
-          if (m == 0) p.counters[tile] = 0;  // ready for the next launch
         }
       }
-      u += k1 - k0;
+    }
+    const float* rs = have_scale ? row_scale : nullptr;
+    if (read_status(p.status) == 0) {
+      constexpr int LD = EPI_LD;
+      bool dead = false;
+      int pc = 0;
+      for (long long u = u_begin; u < u_end; ++pc) {
+        const int tg = static_cast<int>(u / p.kb);
+        const int k0 = static_cast<int>(u - (long long)tg * p.kb);
+        const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
+        const int tm = tg / p.n_groups;
+        const int tn = (tg - tm * p.n_groups) * cs + rank;
+        const int tile = tm * p.n_tiles + tn;
+        const int buf = pc & 1;
+        if (!dead && !mbar_wait(&tfull[buf], (pc >> 1) & 1)) {
+          set_status(p.status, SDV_ERR_TIMEOUT);
+          dead = true;
+        }
+        tc_fence_after();
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * NT;
+        const int rows = min(NT, p.R - tn * NT);
+
+        // accumulator columns past the last activation row are never read
+        const int cols = (rows + EC - 1) / EC * EC;
+        if (k0 == 0 && k1 == p.kb) {
+          // whole tile in this CTA: epilogue straight from tensor memory
+          for (int c0 = 0; c0 < cols; c0 += EC) {
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+            if (c0 + EC == cols) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[buf]);
+            }
+#pragma unroll
+            for (int n = 0; n < EC; ++n) epi[n * LD + m] = v[n];
+            named_sync(1, 4 * kWarp);
+            epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(EC, rows - c0), m, rs, rs_base);
+            named_sync(1, 4 * kWarp);
+          }
+        } else {
+          // tile cut between clusters: store this piece, the fixup sums them in cluster order
+          const int my_slot = 2 * (q * cs + rank) + (tg == first_tg ? 0 : 1);
+          float* mine = p.partials + (size_t)my_slot * BM * NT;
+          for (int c0 = 0; c0 < cols; c0 += EC) {
+            float v[16];
+            tmem_ld16(t_row + c0, v);
+            tc_store_part16(mine, c0, m, v);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+          if (!p.defer_fixup) {
+            // one CTA per cluster (cs == 1): the last CTA to arrive sums the parts in CTA order
+            const long long tu = (long long)tg * p.kb;
+            const int c_first = cta_of_unit(tu, total, Q);
+            const int c_last = cta_of_unit(tu + p.kb - 1, total, Q);
+            __threadfence();
+            named_sync(1, 4 * kWarp);
+            if (m == 0) {
+              const int old = atomicAdd(&p.counters[tile], 1);
+              *flag = (old == c_last - c_first) ? 1 : 0;
+            }
+            named_sync(1, 4 * kWarp);
+            if (*flag != 0) {
+              __threadfence();
+              static_assert(EC == 16, "16-column epilogue chunks");
+              tc_fixup_tile<EPI, LD>(p, tile, c_first, c_last, total, epi, m, rows, NT);
+              if (m == 0) p.counters[tile] = 0;  // ready for the next launch
+            }
+          }
+        }
+        u += k1 - k0;
+      }
     }
   }
+  // every role is done: the producer saw every stage released by the whole
+  // cluster, every accumulator has been read; then no peer touches this CTA's
+  // shared memory or barriers any more
   tc_fence_before();
-  named_sync(2, 5 * kWarp);  // let warp 1 free the tensor memory
-}
-
-template <int EPI, int NT, int XP>
-cudaError_t launch_tc_t(const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x, const GemmParams& p,
-                        int grid, cudaStream_t stream) {
-  auto kern = gemm_tc_kernel<EPI, NT, XP>;
-  constexpr int smem = TcCfg<NT, XP>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(grid), dim3(TC_THREADS), smem, stream, *a0, *a1, *x, p);
-}
-
-template <int EPI, int XP>
-cudaError_t launch_tc_nt(int nt, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
-                         const GemmParams& p, int grid, cudaStream_t stream) {
-  switch (nt) {
-    case 16: return launch_tc_t<EPI, 16, XP>(a0, a1, x, p, grid, stream);
-    case 32: return launch_tc_t<EPI, 32, XP>(a0, a1, x, p, grid, stream);
-    case 64: return launch_tc_t<EPI, 64, XP>(a0, a1, x, p, grid, stream);
-    case 128: return launch_tc_t<EPI, 128, XP>(a0, a1, x, p, grid, stream);
-    case 256: return launch_tc_t<EPI, 256, XP>(a0, a1, x, p, grid, stream);
-    default: return cudaErrorInvalidValue;
+  __syncthreads();
+  if (cs > 1) cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
   }
 }
 
+// Deferred stream-K fixup: block (b, y) handles the boundary between clusters
+// b and b + 1 of the GEMM's grid when it cuts a (weight tile, group) and is
+// that unit range's first such boundary (the others exit), for the
+// activation tile of cluster rank y / chunks and its 16-row chunk y % chunks;
+// 128 threads, thread m = weight row m.  The parts are summed in cluster
+// order, the same order the last-arriving CTA of a one-CTA cluster uses, so
+// the result does not depend on the mode.
 template <int EPI>
-cudaError_t launch_tc_x(int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* x,
-                        const GemmParams& p, int grid, cudaStream_t stream) {
-  return xp == 2 ? launch_tc_nt<EPI, 2>(nt, a0, a1, x, p, grid, stream)
-                 : launch_tc_nt<EPI, 1>(nt, a0, a1, x, p, grid, stream);
-}
-
-// Deferred stream-K fixup: block (b, chunk) handles the tile holding the
-// first unit of CTA b + 1 of the GEMM's grid, when that CTA boundary cuts the
-// tile and is the tile's first such boundary (the tile's other boundaries
-// exit), for 16-row chunk `chunk` of the tile; 128 threads, thread m = weight
-// row m.  The parts are summed in CTA order, exactly as the last-arriving CTA
-// would, so the result does not depend on the mode.
-template <int EPI, int NT>
-__global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, int P) {
+__global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, int Q) {
   SDV_TRACE_SCOPE(kTrFixup + SDV_GEMM_SLOT(EPI, p));
-  constexpr int LD = BM + 4;
+  constexpr int LD = EPI_LD;
   __shared__ float epi[16 * LD];
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
-  const long long total = (long long)p.m_tiles * p.n_tiles * p.kb;
-  const int c = blockIdx.x + 1;
-  const long long ub = (long long)c * total / P;
-  const int tile = static_cast<int>(ub / p.kb);
-  const long long t0 = (long long)tile * p.kb;
-  if (ub == t0) return;                                 // the boundary falls on a tile edge
-  if (c > 1 && (long long)(c - 1) * total / P > t0) return;  // an earlier boundary cuts the same tile
-  const int tn = tile % p.n_tiles;
+  const int NT = p.nt, cs = p.cs;
+  const long long total = (long long)p.m_tiles * p.n_groups * p.kb;
+  const int qb = blockIdx.x + 1;
+  const long long ub = (long long)qb * total / Q;
+  const int tg = static_cast<int>(ub / p.kb);
+  const long long t0 = (long long)tg * p.kb;
+  if (ub == t0) return;                                      // the boundary falls on a tile edge
+  if (qb > 1 && (long long)(qb - 1) * total / Q > t0) return;  // an earlier boundary cuts the same tile
+  const int chunks = (NT + 15) / 16;
+  const int rank = blockIdx.y / chunks;
+  const int tm = tg / p.n_groups;
+  const int tn = (tg - tm * p.n_groups) * cs + rank;
+  if (tn >= p.n_tiles) return;
   const int rows = min(NT, p.R - tn * NT);
-  const int c0 = blockIdx.y * 16;
+  const int c0 = (blockIdx.y - rank * chunks) * 16;
   if (c0 >= rows) return;
   const int m = threadIdx.x;
-  const int c_first = cta_of_unit(t0, total, P);
-  const int c_last = cta_of_unit(t0 + p.kb - 1, total, P);
+  const int q_first = cluster_of_unit(t0, total, Q);
+  const int q_last = cluster_of_unit(t0 + p.kb - 1, total, Q);
   float v[16];
 #pragma unroll
   for (int n = 0; n < 16; ++n) v[n] = 0.f;
-  for (int cc0 = c_first; cc0 <= c_last; cc0 += 4) {
+  for (int qq0 = q_first; qq0 <= q_last; qq0 += 4) {
     float w[4][16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (cc0 + q <= c_last) {
-        const int cc = cc0 + q;
-        const int first_tile_cc = static_cast<int>(((long long)cc * total / P) / p.kb);
-        const int slot = 2 * cc + (tile == first_tile_cc ? 0 : 1);
+    for (int i = 0; i < 4; ++i)
+      if (qq0 + i <= q_last) {
+        const int qq = qq0 + i;
+        const int first_tg_qq = static_cast<int>(((long long)qq * total / Q) / p.kb);
+        const int slot = 2 * (qq * cs + rank) + (tg == first_tg_qq ? 0 : 1);
         const float* src = p.partials + (size_t)slot * BM * NT + (size_t)c0 * BM + m;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) w[q][n] = __ldcg(src + (size_t)n * BM);
+        for (int n = 0; n < 16; ++n) w[i][n] = __ldcg(src + (size_t)n * BM);
       }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (cc0 + q <= c_last) {
+    for (int i = 0; i < 4; ++i)
+      if (qq0 + i <= q_last) {
 #pragma unroll
-        for (int n = 0; n < 16; ++n) v[n] += w[q][n];
+        for (int n = 0; n < 16; ++n) v[n] += w[i][n];
       }
   }
 #pragma unroll
   for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
   __syncthreads();
-  epilogue_rows<EPI, LD>(p, epi, tile / p.n_tiles, tn * NT + c0, min(16, rows - c0), m);
+  epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(16, rows - c0), m);
 }
 
 template <int EPI>
-cudaError_t launch_fixup_e(int nt, const GemmParams& p, int grid, cudaStream_t stream) {
-  if (grid < 2) return cudaSuccess;  // one CTA cuts no tile
-  const dim3 g(grid - 1, (nt + 15) / 16);
-  switch (nt) {
-    case 16: return launch_pdl(gemm_tc_fixup_kernel<EPI, 16>, g, dim3(128), 0, stream, p, grid);
-    case 32: return launch_pdl(gemm_tc_fixup_kernel<EPI, 32>, g, dim3(128), 0, stream, p, grid);
-    case 64: return launch_pdl(gemm_tc_fixup_kernel<EPI, 64>, g, dim3(128), 0, stream, p, grid);
-    case 128: return launch_pdl(gemm_tc_fixup_kernel<EPI, 128>, g, dim3(128), 0, stream, p, grid);
-    case 256: return launch_pdl(gemm_tc_fixup_kernel<EPI, 256>, g, dim3(128), 0, stream, p, grid);
+cudaError_t launch_fixup_e(const GemmParams& p, int Q, cudaStream_t stream) {
+  if (Q < 2) return cudaSuccess;  // one cluster cuts no tile
+  const dim3 g(Q - 1, p.cs * ((p.nt + 15) / 16));
+  return launch_pdl(gemm_tc_fixup_kernel<EPI>, g, dim3(128), 0, stream, p, Q);
+}
+
+cudaError_t launch_fixup(int epi, const GemmParams& p, int Q, cudaStream_t stream) {
+  switch (epi) {
+    case EPI_F32: return launch_fixup_e<EPI_F32>(p, Q, stream);
+    case EPI_RESID: return launch_fixup_e<EPI_RESID>(p, Q, stream);
+    case EPI_SWIGLU: return launch_fixup_e<EPI_SWIGLU>(p, Q, stream);
+    case EPI_QKV: return launch_fixup_e<EPI_QKV>(p, Q, stream);
+    case EPI_LMHEAD: return launch_fixup_e<EPI_LMHEAD>(p, Q, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host: the launch configuration
+// ---------------------------------------------------------------------------
+
+// Activation tile heights at and above which cut tiles go to the parallel
+// fixup kernel (one 16-row chunk per block) rather than to the last CTA to
+// arrive, which would walk every chunk of the tile.
+constexpr int kDeferFixupRows = 32;
+
+using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, GemmParams);
+
+template <int EPI, int XP>
+Kern kernel_of() {
+  return reinterpret_cast<Kern>(gemm_tc_kernel<EPI, XP>);
+}
+
+Kern pick_kernel(int epi, int xp) {
+  switch (epi) {
+    case EPI_F32: return xp == 2 ? kernel_of<EPI_F32, 2>() : kernel_of<EPI_F32, 1>();
+    case EPI_RESID: return xp == 2 ? kernel_of<EPI_RESID, 2>() : kernel_of<EPI_RESID, 1>();
+    case EPI_SWIGLU: return xp == 2 ? kernel_of<EPI_SWIGLU, 2>() : kernel_of<EPI_SWIGLU, 1>();
+    case EPI_QKV: return xp == 2 ? kernel_of<EPI_QKV, 2>() : kernel_of<EPI_QKV, 1>();
+    case EPI_LMHEAD: return kernel_of<EPI_LMHEAD, 1>();
+    default: return nullptr;
+  }
+}
+
+int smem_for(int nt, int xp) { return FIXED_BYTES + tc_stages(nt, xp) * tc_stage_bytes(nt, xp); }
+
+// How many clusters of `cs` CTAs of this kernel fit on the GPU at once (cached).
+int active_clusters(Kern k, int cs, int smem, int sms) {
+  static std::mutex mu;
+  struct Entry {
+    Kern k;
+    int dev, cs, smem, n;
+  };
+  static Entry cache[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].k == k && cache[i].dev == dev && cache[i].cs == cs && cache[i].smem == smem) return cache[i].n;
+  }
+  int n = 0;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    if (cs == 1) {
+      n = sms;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(sms / cs * cs));
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      if (n * cs > sms) n = sms / cs;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 64) cache[used++] = Entry{k, dev, cs, smem, n};
+  return n;
+}
+
+struct TcChoice {
+  int nt = 0, cs = 1, n_tiles = 0, n_groups = 0, grid = 0;
+};
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// The tile height and cluster size for R rows: among one CTA per tile group
+// (power-of-two tiles, each weight tile streamed once per activation tile) and
+// clusters of 2..8 CTAs sharing each weight tile (tiles of about R / cs rows,
+// a multiple of 16), the one with the least modelled time: the larger of the
+// MMA work per SM (columns actually multiplied, over the SMs the clusters
+// occupy, slowed by a shallow pipeline) and the weight stream (passes over the
+// weights at the HBM rate).
+TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
+  const Kern k = pick_kernel(epi, xp);
+  const double w_bytes = (double)g.m_tiles * (epi == EPI_SWIGLU ? 64 : BM) * g.kb * BK * 2 * (epi == EPI_SWIGLU ? 2 : 1);
+  // cycles of MMA per (weight k-block x activation column x plane) at the
+  // measured dense rate, and HBM bytes per cycle across the GPU (~1.9 GHz)
+  constexpr double kMmaCyc = 2.5, kHbmBytesPerCyc = 3490.0;
+  TcChoice best;
+  double best_t = 1e300;
+  for (int cs = 1; cs <= kMaxCluster; ++cs) {
+    TcChoice c;
+    c.cs = cs;
+    if (cs == 1) {
+      c.nt = gemm_tc_tile_rows(g.R);
+      c.n_tiles = (g.R + c.nt - 1) / c.nt;
+      c.n_groups = c.n_tiles;
+    } else {
+      c.nt = round_up((g.R + cs - 1) / cs, 16);
+      if (c.nt > 256) continue;
+      c.n_tiles = (g.R + c.nt - 1) / c.nt;
+      if (c.n_tiles != cs) continue;  // every CTA of the cluster has rows
+      c.n_groups = 1;
+    }
+    const int smem = smem_for(c.nt, xp);
+    const int clusters = active_clusters(k, cs, smem, sms);
+    if (clusters < 1) continue;
+    const long long units = (long long)g.m_tiles * c.n_groups * g.kb;
+    const int q = static_cast<int>(units < clusters ? units : clusters);
+    c.grid = q * cs;
+    const int stages = tc_stages(c.nt, xp);
+    const double shallow = stages >= 4 ? 1.0 : 1.0 + 0.2 * (4 - stages);
+    const double mma = (double)units * cs * c.nt * xp * kMmaCyc / c.grid * shallow;
+    const double passes = cs == 1 ? c.n_tiles : c.n_groups;
+    const double mem = w_bytes * passes / kHbmBytesPerCyc;
+    const double t = mma > mem ? mma : mem;
+    if (t < best_t * 0.98) {  // a larger cluster must win clearly
+      best_t = t;
+      best = c;
+    }
+  }
+  return best;
+}
+
+int box_for(int nt) {
+  for (int b = 256; b >= 8; b >>= 1)
+    if (nt % b == 0) return b;
+  return 8;
+}
+
+int box_index(int box) {
+  switch (box) {
+    case 8: return 0;
+    case 16: return 1;
+    case 32: return 2;
+    case 64: return 3;
+    case 128: return 4;
+    default: return 5;
   }
 }
 
 }  // namespace
-
-cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid, cudaStream_t stream) {
-  switch (epi) {
-    case EPI_F32: return launch_fixup_e<EPI_F32>(nt, p, grid, stream);
-    case EPI_RESID: return launch_fixup_e<EPI_RESID>(nt, p, grid, stream);
-    case EPI_SWIGLU: return launch_fixup_e<EPI_SWIGLU>(nt, p, grid, stream);
-    case EPI_QKV: return launch_fixup_e<EPI_QKV>(nt, p, grid, stream);
-    case EPI_LMHEAD: return launch_fixup_e<EPI_LMHEAD>(nt, p, grid, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
 
 int gemm_tc_tile_rows(int R) {
   if (R <= 16) return 16;
@@ -442,16 +689,58 @@ int gemm_tc_tile_rows(int R) {
   return 256;
 }
 
-cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
-                           const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream) {
-  switch (epi) {
-    case EPI_F32: return launch_tc_x<EPI_F32>(nt, xp, a0, a1, x, p, grid, stream);
-    case EPI_RESID: return launch_tc_x<EPI_RESID>(nt, xp, a0, a1, x, p, grid, stream);
-    case EPI_SWIGLU: return launch_tc_x<EPI_SWIGLU>(nt, xp, a0, a1, x, p, grid, stream);
-    case EPI_QKV: return launch_tc_x<EPI_QKV>(nt, xp, a0, a1, x, p, grid, stream);
-    case EPI_LMHEAD: return launch_tc_nt<EPI_LMHEAD, 1>(nt, a0, a1, x, p, grid, stream);
-    default: return cudaErrorInvalidValue;
+cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid, cudaStream_t stream) {
+  // one CTA per cluster (the int4 kernel): units over (weight tile, activation tile, k-block)
+  GemmParams g = p;
+  g.nt = nt;
+  g.cs = 1;
+  g.n_groups = g.n_tiles;
+  return launch_fixup(epi, g, grid, stream);
+}
+
+cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* xmaps,
+                           GemmParams p, int sms, cudaStream_t stream) {
+  if (epi == EPI_LMHEAD) xp = 1;
+  const Kern k = pick_kernel(epi, xp);
+  if (!k) return cudaErrorInvalidValue;
+  const TcChoice c = choose(epi, xp, p, sms);
+  if (c.grid < 1) return cudaErrorInvalidConfiguration;
+  p.nt = c.nt;
+  p.cs = c.cs;
+  p.n_tiles = c.n_tiles;
+  p.n_groups = c.n_groups;
+  p.x_box = box_for(c.nt);
+  p.stages = tc_stages(c.nt, xp);
+  p.defer_fixup = (c.cs > 1 || c.nt >= kDeferFixupRows) ? 1 : 0;
+  const int smem = smem_for(c.nt, xp);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c.grid));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
+  if (c.cs > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(c.cs);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  note_launch();
+  const CUtensorMap* x = &xmaps[box_index(p.x_box)];
+  e = cudaLaunchKernelEx(&cfg, k, *a0, *a1, *x, p);
+  if (e != cudaSuccess || !p.defer_fixup) return e;
+  return launch_fixup(epi, p, c.grid / c.cs, stream);
 }
 
 SDV_TRACE_UNIT(gemm_tc)

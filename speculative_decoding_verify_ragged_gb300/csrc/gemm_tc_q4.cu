@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(Q4_THREADS, 1)
         if (last) {
           __threadfence();
           static_assert(EC == 16, "16-column epilogue chunks");
-          tc_fixup_tile<EPI, NT, LD>(p, tile, c_first, c_last, total, epi, m, rows);
+          tc_fixup_tile<EPI, LD>(p, tile, c_first, c_last, total, epi, m, rows, NT);
           if (m == 0) p.counters[tile] = 0;  // ready for the next launch
         }
       }

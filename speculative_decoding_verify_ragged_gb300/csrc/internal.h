@@ -69,6 +69,12 @@ struct GemmParams {
   // fixup kernel (one block per cut tile and 16-row chunk) instead of having
   // the last CTA to arrive sum them
   int defer_fixup = 0;
+  // tcgen05 kernels: activation rows per tile, thread-block cluster size (the
+  // CTAs of a cluster share one multicast read of each weight tile, CTA r of
+  // the cluster taking activation tile tg * cs + r of tile group tg), tile
+  // groups (n_tiles = n_groups * cs when cs > 1), the activation map's box
+  // height and the pipeline depth
+  int nt = 0, cs = 1, n_groups = 0, x_box = 0, stages = 0;
   int* status = nullptr;
   EpiParams epi;
 };
@@ -112,8 +118,12 @@ cudaError_t trace_set_gemm_tc(unsigned long long* table);
 cudaError_t trace_set_gemm_tc_q4(unsigned long long* table);
 cudaError_t trace_set_step_kernels(unsigned long long* table);
 #endif
-cudaError_t launch_gemm_tc(int epi, int nt, int xp, const CUtensorMap* a0, const CUtensorMap* a1,
-                           const CUtensorMap* x, const GemmParams& p, int grid, cudaStream_t stream);
+// bf16 weights on tcgen05: picks the activation tile height and the cluster
+// size for p.R rows (a cost model over the weight stream and the MMA work),
+// then launches the GEMM over the SMs and, for tiles cut between CTAs, the
+// fixup.  xmaps: the activation map for each box height 8..256.
+cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* xmaps,
+                           GemmParams p, int sms, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
 cudaError_t launch_split_planes(const float* x, __nv_bfloat16* out, long long lo_off, long long n,
                                 cudaStream_t stream);
