@@ -12,14 +12,15 @@
 // Arithmetic intensity: a weight tile streamed against NT activation rows
 // carries 2 * NT flops per weight byte pair, so at NT = 256 the weights alone
 // ask 7.5 TB/s of the HBM at the tensor peak, and a second 256-row activation
-// tile would stream the same weights again.  Past one tile, the CTAs of a
-// thread-block cluster therefore share each weight tile: two of them load its
-// two 64-row halves with TMA multicast into every CTA of the cluster, and CTA
-// r multiplies it with its own activation tile tg * cs + r.  The weights cross
-// HBM once for any row count up to 8 tiles, and a tile of about R / cs rows
-// keeps the activation stage small enough for four pipeline stages.  A stage
-// is refilled only when every CTA of the cluster has released it (each MMA
-// commit arrives on the stage's barrier in every CTA).
+// tile would stream the same weights again.  Past one tile, a group of cs
+// CTAs therefore shares each weight tile, CTA r of the group multiplying it
+// with its own activation tile tg * cs + r of about R / cs rows, so the
+// weights cross HBM once.  The group's CTAs walk the same units at the same
+// pace, and the first to ask for a weight line brings it into L2 for the
+// others.  (A thread-block cluster sharing the tile by TMA multicast -- two
+// CTAs each load one 64-row half into every CTA of the cluster, and a stage
+// is refilled only once every CTA has released it -- measured the same; it
+// stays selectable for A/B timing.)
 //
 // Warp roles (192 threads):
 //  * warp 0: TMA producer (one lane) -- weight half-tiles and activation planes
@@ -31,6 +32,8 @@
 //  * warps 2-5: epilogue -- tcgen05.ld the accumulator (lane = weight row),
 //    then the stream-K partial/fixup and the fused epilogue shared with the
 //    mma.sync kernel, while the MMAs fill the other accumulator.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -122,6 +125,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   griddep_launch_dependents();
 
   const int NT = p.nt, S = p.stages, cs = p.cs;
+  const bool mc = p.multicast != 0;  // a cluster shares weight tiles by multicast (else through L2)
   const int STAGE = tc_stage_bytes(NT, XP);
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + S * STAGE);
@@ -134,15 +138,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   float* row_scale = reinterpret_cast<float*>(tmem_slot + 4);  // [kScaleRows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = cs > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int q = cs > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int rank = mc ? static_cast<int>(cluster_ctarank()) : static_cast<int>(blockIdx.x) % cs;
+  const int q = mc ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x) / cs;
   const int Q = static_cast<int>(gridDim.x) / cs;
   const uint16_t everyone = static_cast<uint16_t>((1u << cs) - 1u);
   const uint32_t ncols = tmem_columns(NT);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], cs);  // one release per CTA of the cluster
+      mbar_init(&empty[s], mc ? cs : 1);  // one release per CTA of a multicast cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   // every CTA's barriers exist before a peer's multicast can land on them
-  if (cs > 1) cluster_sync_all();
+  if (mc) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
 
   const long long total = (long long)p.m_tiles * p.n_groups * p.kb;
@@ -202,6 +206,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (cs == 1) {
           tma_load_2d_hint(sa, &tmA0, &full[stage], cu.k * BK, rowA0, pol);
           tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, pol);
+        } else if (!mc) {
+          // the group's CTAs read the same weight tile at about the same time:
+          // the first brings it into L2 (normal priority), the others hit there
+          tma_load_2d(sa, &tmA0, &full[stage], cu.k * BK, rowA0);
+          tma_load_2d(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1);
         } else if (rank == 0) {
           tma_load_2d_mc(sa, &tmA0, &full[stage], cu.k * BK, rowA0, everyone, pol);
         } else if (rank == 1) {
@@ -305,7 +314,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               }
             }
             // frees the stage, in every CTA of the cluster, once these MMAs have read it
-            if (cs > 1) umma_commit_mc(&empty[stage], everyone);
+            if (mc) umma_commit_mc(&empty[stage], everyone);
             else umma_commit(&empty[stage]);
             if (++stage == S) {
               stage = 0;
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // shared memory or barriers any more
   tc_fence_before();
   __syncthreads();
-  if (cs > 1) cluster_sync_all();
+  if (mc) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
@@ -561,6 +570,21 @@ Kern pick_kernel(int epi, int xp) {
   }
 }
 
+// How the CTAs that take different activation tiles of the same weight tile
+// share its read: multicast within a thread-block cluster, or a group of
+// consecutive CTAs reading it at about the same time through L2.
+// SDV_GEMM_SHARE=mc|l2|off in the environment picks one (A/B timing); the
+// default is l2.
+int share_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("SDV_GEMM_SHARE");
+    if (v && std::strcmp(v, "mc") == 0) return 1;
+    if (v && std::strcmp(v, "off") == 0) return 0;
+    return 2;
+  }();
+  return mode;
+}
+
 int smem_for(int nt, int xp) { return FIXED_BYTES + tc_stages(nt, xp) * tc_stage_bytes(nt, xp); }
 
 // How many clusters of `cs` CTAs of this kernel fit on the GPU at once (cached).
@@ -581,8 +605,8 @@ int active_clusters(Kern k, int cs, int smem, int sms) {
   }
   int n = 0;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
-    if (cs == 1) {
-      n = sms;
+    if (cs == 1 || share_mode() != 1) {
+      n = sms / cs;
     } else {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(sms / cs * cs));
@@ -613,53 +637,57 @@ struct TcChoice {
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
-// The tile height and cluster size for R rows: among one CTA per tile group
-// (power-of-two tiles, each weight tile streamed once per activation tile) and
-// clusters of 2..8 CTAs sharing each weight tile (tiles of about R / cs rows,
-// a multiple of 16), the one with the least modelled time: the larger of the
-// MMA work per SM (columns actually multiplied, over the SMs the clusters
-// occupy, slowed by a shallow pipeline) and the weight stream (passes over the
-// weights at the HBM rate).
+// The tile height and group size for R rows.  One CTA per activation tile of
+// at most 256 rows (a power of two) streams each weight tile once per tile;
+// a group of cs CTAs shares each weight tile, each with an activation tile of
+// about R / cs rows.  Which pays was measured on the crossover sweep's shapes
+// (GEMM times in the step, 9B-class layer): for the LM head (one activation
+// plane) groups of two at 384 and 512 rows (512: 535 -> 469 us) and nothing
+// else (320 rows with 160-row tiles: 501 -> 581 us; 640 and 1152 rows lost
+// with every group size); for the layer GEMMs (two planes) groups of two
+// from 257 to 512 rows (gate/up at 320: 313 -> 240 us, at 512: 343 -> 296),
+// three at 640 (441 -> 417) and six at 1152 (715 -> 537).  Group sizes that
+// were not measured to pay are not used.
 TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
-  const Kern k = pick_kernel(epi, xp);
-  const double w_bytes = (double)g.m_tiles * (epi == EPI_SWIGLU ? 64 : BM) * g.kb * BK * 2 * (epi == EPI_SWIGLU ? 2 : 1);
-  // cycles of MMA per (weight k-block x activation column x plane) at the
-  // measured dense rate, and HBM bytes per cycle across the GPU (~1.9 GHz)
-  constexpr double kMmaCyc = 2.5, kHbmBytesPerCyc = 3490.0;
-  TcChoice best;
-  double best_t = 1e300;
-  for (int cs = 1; cs <= kMaxCluster; ++cs) {
-    TcChoice c;
-    c.cs = cs;
-    if (cs == 1) {
-      c.nt = gemm_tc_tile_rows(g.R);
-      c.n_tiles = (g.R + c.nt - 1) / c.nt;
-      c.n_groups = c.n_tiles;
-    } else {
-      c.nt = round_up((g.R + cs - 1) / cs, 16);
-      if (c.nt > 256) continue;
-      c.n_tiles = (g.R + c.nt - 1) / c.nt;
-      if (c.n_tiles != cs) continue;  // every CTA of the cluster has rows
-      c.n_groups = 1;
-    }
-    const int smem = smem_for(c.nt, xp);
-    const int clusters = active_clusters(k, cs, smem, sms);
-    if (clusters < 1) continue;
-    const long long units = (long long)g.m_tiles * c.n_groups * g.kb;
-    const int q = static_cast<int>(units < clusters ? units : clusters);
-    c.grid = q * cs;
-    const int stages = tc_stages(c.nt, xp);
-    const double shallow = stages >= 4 ? 1.0 : 1.0 + 0.2 * (4 - stages);
-    const double mma = (double)units * cs * c.nt * xp * kMmaCyc / c.grid * shallow;
-    const double passes = cs == 1 ? c.n_tiles : c.n_groups;
-    const double mem = w_bytes * passes / kHbmBytesPerCyc;
-    const double t = mma > mem ? mma : mem;
-    if (t < best_t * 0.98) {  // a larger cluster must win clearly
-      best_t = t;
-      best = c;
+  static const int forced = [] {
+    // SDV_GEMM_CS=n in the environment: groups of n wherever n tiles cover
+    // the rows (A/B timing of the choice)
+    const char* v = std::getenv("SDV_GEMM_CS");
+    return v ? std::atoi(v) : 0;
+  }();
+  (void)epi;
+  const int R = g.R;
+  int cs = 1;
+  if (forced > 0) {
+    cs = forced;
+  } else if (share_mode() != 0) {
+    if (xp == 1) cs = (R > 320 && R <= 512) ? 2 : 1;
+    else if (R > 256 && R <= 512) cs = 2;
+    else if (R > 512 && R <= 768) cs = 3;
+    else if (R > 1024 && R <= 1536) cs = 6;
+  }
+  TcChoice c;
+  if (cs > 1 && cs <= kMaxCluster) {
+    c.nt = round_up((R + cs - 1) / cs, 16);
+    c.n_tiles = (R + c.nt - 1) / c.nt;
+    if (c.nt <= 256 && c.n_tiles == cs) {
+      const int groups = active_clusters(pick_kernel(epi, xp), cs, smem_for(c.nt, xp), sms);
+      if (groups > 0) {
+        const long long units = (long long)g.m_tiles * g.kb;
+        c.cs = cs;
+        c.n_groups = 1;
+        c.grid = static_cast<int>(units < groups ? units : groups) * cs;
+        return c;
+      }
     }
   }
-  return best;
+  c.cs = 1;
+  c.nt = gemm_tc_tile_rows(R);
+  c.n_tiles = (R + c.nt - 1) / c.nt;
+  c.n_groups = c.n_tiles;
+  const long long units = (long long)g.m_tiles * c.n_tiles * g.kb;
+  c.grid = static_cast<int>(units < sms ? units : sms);
+  return c;
 }
 
 int box_for(int nt) {
@@ -712,6 +740,7 @@ cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtenso
   p.x_box = box_for(c.nt);
   p.stages = tc_stages(c.nt, xp);
   p.defer_fixup = (c.cs > 1 || c.nt >= kDeferFixupRows) ? 1 : 0;
+  p.multicast = c.cs > 1 && share_mode() == 1 ? 1 : 0;
   const int smem = smem_for(c.nt, xp);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -727,7 +756,7 @@ cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtenso
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (c.cs > 1) {
+  if (p.multicast) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = static_cast<unsigned>(c.cs);
     attr[na].val.clusterDim.y = 1;

@@ -69,12 +69,12 @@ struct GemmParams {
   // fixup kernel (one block per cut tile and 16-row chunk) instead of having
   // the last CTA to arrive sum them
   int defer_fixup = 0;
-  // tcgen05 kernels: activation rows per tile, thread-block cluster size (the
-  // CTAs of a cluster share one multicast read of each weight tile, CTA r of
-  // the cluster taking activation tile tg * cs + r of tile group tg), tile
-  // groups (n_tiles = n_groups * cs when cs > 1), the activation map's box
-  // height and the pipeline depth
+  // tcgen05 kernels: activation rows per tile, group size (the cs CTAs of a
+  // group share each weight tile, CTA r of the group taking activation tile
+  // tg * cs + r of tile group tg), tile groups (n_tiles = n_groups * cs when
+  // cs > 1), the activation map's box height and the pipeline depth
   int nt = 0, cs = 1, n_groups = 0, x_box = 0, stages = 0;
+  int multicast = 0;  // the cluster's CTAs share weight tiles by TMA multicast (else a group reads them via L2)
   int* status = nullptr;
   EpiParams epi;
 };
@@ -118,10 +118,10 @@ cudaError_t trace_set_gemm_tc(unsigned long long* table);
 cudaError_t trace_set_gemm_tc_q4(unsigned long long* table);
 cudaError_t trace_set_step_kernels(unsigned long long* table);
 #endif
-// bf16 weights on tcgen05: picks the activation tile height and the cluster
-// size for p.R rows (a cost model over the weight stream and the MMA work),
-// then launches the GEMM over the SMs and, for tiles cut between CTAs, the
-// fixup.  xmaps: the activation map for each box height 8..256.
+// bf16 weights on tcgen05: picks the activation tile height and the size of
+// the CTA groups that share each weight tile for p.R rows (measured choices,
+// see gemm_tc.cu), then launches the GEMM over the SMs and, for tiles cut
+// between CTAs, the fixup.  xmaps: the activation map for each box height 8..256.
 cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* xmaps,
                            GemmParams p, int sms, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
