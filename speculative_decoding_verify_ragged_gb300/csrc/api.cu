@@ -64,7 +64,10 @@ static bool config_ok(const sdv_config* c) {
   if (c->head_dim != 64 && c->head_dim != 128) return false;
   if (c->n_q % c->n_kv) return false;
   if (c->page_size != 16) return false;
-  if (c->gamma_max < 0 || (c->gamma_max + 1) * (c->n_q / c->n_kv) > kAttnQMax) return false;
+  // query vectors per (slot, kv head): 48 on the mma.sync attention kernel, 64
+  // with head_dim 128 (the tcgen05 kernel splits them over two items)
+  if (c->gamma_max < 0 || (c->gamma_max + 1) * (c->n_q / c->n_kv) > (c->head_dim == 128 ? kAttnQVecs : kAttnQMax))
+    return false;
   const int kmul = c->weight_format == SDV_WEIGHTS_INT4_G32 ? 256 : 64;
   if (c->weight_format != SDV_WEIGHTS_BF16 && c->weight_format != SDV_WEIGHTS_INT4_G32) return false;
   if (c->hidden % kmul || (c->n_q * c->head_dim) % kmul || c->ffn % kmul) return false;
@@ -91,7 +94,9 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.max_tiles = mt * rt;
   L.grid_gemm = sms;
   L.target_items = 4 * sms;
-  L.items_max = L.target_items + static_cast<int>(B) * c.n_kv + 8;
+  // items split by query vectors (more than 32 per slot and kv head) double
+  const int parts = (c.gamma_max + 1) * (c.n_q / c.n_kv) > 32 ? 2 : 1;
+  L.items_max = parts * (L.target_items + static_cast<int>(B) * c.n_kv) + 8;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -447,6 +452,8 @@ static PrologueParams prologue_params(sdv_ctx* c, const sdv_batch* b, int* statu
   p.rope_theta = c->cfg.rope_theta;
   p.check_tokens = check_tokens && b->tokens ? 1 : 0;
   p.stall_ns = c->stall_ns;
+  p.n_q = c->cfg.n_q;
+  p.qsplit = 0;
   return p;
 }
 
@@ -512,6 +519,33 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
   return launch_gemm(epi, nt, xp, a0, a1, &xmaps[nt_index(nt)], g, grid, s);
 }
 
+// Which attention kernel a batch takes and how its work items split the query
+// vectors.  The tcgen05 kernel takes head_dim 128 with up to 64 query vectors
+// per (sequence, kv head) -- past 32 in items of 32, two items per chunk of
+// pages, adjacent so that the second reads the pages from L2 -- and in auto
+// mode from kTcAttnSlots sequences up, or whenever the mma.sync kernel's 48
+// vectors would not hold them.
+struct AttnPlan {
+  sdv_status st = SDV_OK;
+  bool tc = false;
+  int qsplit = 0, nq = 0;
+};
+
+static AttnPlan attn_plan(const sdv_ctx* c, int B) {
+  AttnPlan a;
+  const int nqv_max = (c->cfg.gamma_max + 1) * (c->cfg.n_q / c->cfg.n_kv);
+  const bool fits = c->cfg.head_dim == 128 && nqv_max <= kAttnQVecs;
+  if (c->attn_path == SDV_GEMM_TCGEN05 && !fits) a.st = SDV_ERR_UNSUPPORTED;
+  a.tc = fits && (c->attn_path == SDV_GEMM_TCGEN05 ||
+                  (c->attn_path == SDV_GEMM_AUTO && (B >= kTcAttnSlots || nqv_max > kAttnQMax)));
+  if (!a.tc && nqv_max > kAttnQMax) a.st = SDV_ERR_UNSUPPORTED;
+  if (a.tc) {
+    a.qsplit = nqv_max > 32 ? 32 : 0;
+    a.nq = (a.qsplit || nqv_max > 16) ? 32 : 16;
+  }
+  return a;
+}
+
 static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,
                                 long long out_lo_off, int* status, cudaStream_t s) {
   CUtensorMap kv;
@@ -538,16 +572,14 @@ static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, 
   a.n_kv = c->cfg.n_kv;
   a.page = c->cfg.page_size;
   const int grid = c->sms;  // one CTA per SM (the ring and the combine buffer take most of shared memory)
-  // tcgen05 kernel: head_dim 128 and at most 32 query vectors per (sequence, KV head)
-  const int nqv_max = (c->cfg.gamma_max + 1) * (c->cfg.n_q / c->cfg.n_kv);
-  const bool fits = c->cfg.head_dim == 128 && nqv_max <= 32;
-  if (c->attn_path == SDV_GEMM_TCGEN05 && !fits) return SDV_ERR_UNSUPPORTED;
   // in auto mode a batch of fewer than kTcAttnSlots sequences keeps the
-  // mma.sync kernel: too little KV per CTA to hide the tcgen05 pipeline's fill
-  const bool tc = fits && (c->attn_path == SDV_GEMM_TCGEN05 ||
-                           (c->attn_path == SDV_GEMM_AUTO && b->B >= kTcAttnSlots));
-  if (tc) {
-    SDV_CUDA(launch_attention_tc(nqv_max <= 16 ? 16 : 32, &kv, a, grid, s));
+  // mma.sync kernel (too little KV per CTA to hide the tcgen05 pipeline's
+  // fill) unless its vectors do not fit it
+  const AttnPlan plan = attn_plan(c, b->B);
+  if (plan.st != SDV_OK) return plan.st;
+  a.qsplit = plan.qsplit;
+  if (plan.tc) {
+    SDV_CUDA(launch_attention_tc(plan.nq, &kv, a, grid, s));
     SDV_CUDA(launch_attention_merge(c->cfg.head_dim, a, b->R, s, ws_ptr<int>(c, c->L.row_seq)));
     return SDV_OK;
   }
@@ -631,8 +663,11 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     return c->timing && c->phase_ev[k] ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess;
   };
 
+  const AttnPlan plan = attn_plan(c, b->B);
+  if (plan.st != SDV_OK) return plan.st;
   SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
   PrologueParams pp = prologue_params(c, b, status, true);
+  pp.qsplit = plan.qsplit;
   pp.emb = static_cast<const __nv_bfloat16*>(c->w.emb);
   pp.gain = static_cast<const __nv_bfloat16*>(c->w.g_attn);
   pp.x0 = f32(c->L.x0);
@@ -858,7 +893,10 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
 sdv_status sdv_attention(sdv_ctx* c, const void* q, const sdv_batch* b, void* out, int* status, void* stream) {
   if (!c || !q || !out || !status || !batch_ok(c, b, false) || !b->kv_pool) return SDV_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const AttnPlan plan = attn_plan(c, b->B);
+  if (plan.st != SDV_OK) return plan.st;
   PrologueParams pp = prologue_params(c, b, status, false);
+  pp.qsplit = plan.qsplit;
   SDV_CUDA(launch_prologue(pp, s));
   // the kernel writes bf16 hi + lo planes; a plain fp32 result is their sum,
   // so stage the planes in the workspace and add them into `out`

@@ -71,7 +71,7 @@ __device__ __forceinline__ Item load_item(const AttnParams& p, int item) {
   const int4 a = p.items[2 * item], c = p.items[2 * item + 1];
   Item it;
   it.b = a.x;
-  it.g = a.y;
+  it.g = a.y & 0xFFFF;  // the mma.sync kernel's items hold every vector (no part offset)
   it.p0 = a.z;
   it.p1 = a.w;
   it.L = c.x;
@@ -472,8 +472,15 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   const int group = p.n_q / p.n_kv;
   const int i = r - p.row_off[b];
   const int g = h / group;
-  const int v = i * group + (h - g * group);
-  const long long item0 = p.item_off[b] + (long long)g * chunks;
+  int v = i * group + (h - g * group);
+  // items split by query vectors: the part holding v, and v within it
+  int parts = 1, part = 0;
+  if (p.qsplit > 0) {
+    parts = ((p.draft_lens[b] + 1) * group + p.qsplit - 1) / p.qsplit;
+    part = v / p.qsplit;
+    v -= part * p.qsplit;
+  }
+  const long long item0 = p.item_off[b] + ((long long)g * parts + part) * chunks;
   const float2* ml = p.part_ml + item0 * kAttnQMax + v;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + (item0 * kAttnQMax + v) * D) + d4;
   constexpr long long kO4 = (long long)kAttnQMax * D / 4;  // float4 stride between chunks

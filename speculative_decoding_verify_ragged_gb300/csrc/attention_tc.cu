@@ -130,13 +130,15 @@ __device__ __forceinline__ int f2ord(float x) {
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF); }
 
+// v0: the item's first query vector (items of one (slot, kv head) split by
+// vectors when there are more than one item holds)
 struct Item {
-  int b, g, p0, p1, L, gamma, r0, chunks;
+  int b, g, p0, p1, L, gamma, r0, chunks, v0;
 };
 
 __device__ __forceinline__ Item load_item(const AttnParams& p, int item) {
   const int4 a = p.items[2 * item], c = p.items[2 * item + 1];
-  return Item{a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+  return Item{a.x, a.y & 0xFFFF, a.z, a.w, c.x, c.y, c.z, c.w, a.y >> 16};
 }
 
 template <int NQ>
@@ -400,14 +402,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     constexpr int QPT = NH * (D / 4) / 128;  // float4s of Q per thread
     static_assert(NH * (D / 4) % 128 == 0, "Q rows split evenly over the group");
     auto fetch_q = [&](const Item& iq, float4 (&dst)[QPT]) {
-      const int nq = (iq.gamma + 1) * group;
+      const int nq = (iq.gamma + 1) * group - iq.v0;  // this item's vectors (NQ at most)
 #pragma unroll
       for (int q = 0; q < QPT; ++q) {
         const int idx = t + q * 128;
         const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
         dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (v < nq) {
-          const int i = v / group, h = iq.g * group + (v - i * group);
+          const int va = iq.v0 + v;
+          const int i = va / group, h = iq.g * group + (va - i * group);
           dst[q] = *reinterpret_cast<const float4*>(p.q + ((long long)(iq.r0 + i) * p.n_q + h) * D + ch * 4);
         }
       }
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int item = blockIdx.x; item < total_items; item += gridDim.x, ++kitem) {
       const Item it = it_cur;
-      const int nqv = (it.gamma + 1) * group;
+      const int nqv = (it.gamma + 1) * group - it.v0;  // this item's vectors, from v0
       const int nblk = (it.p1 - it.p0 + PAGES - 1) / PAGES;
       // the last key position each of the group's query vectors may see (-1:
       // padding); in a token tree every node's keys end within L + 63 and the
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const bool tree = p.row_anc != nullptr;
       int qlim[NH];
 #pragma unroll
-      for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (tree ? 63 : (col0 + j) / group) : -1;
+      for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (tree ? 63 : (it.v0 + col0 + j) / group) : -1;
 
       // the next item's Q rows into the other buffer, once item k - 1's last
       // QK^T has read it; then the Q rows and the record of the item after it
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const int d = key - it.L;
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            const bool in = col0 + j < nqv && ((p.row_anc[it.r0 + (col0 + j) / group] >> d) & 1ull);
+            const bool in = col0 + j < nqv && ((p.row_anc[it.r0 + (it.v0 + col0 + j) / group] >> d) & 1ull);
             s[j] = in ? s[j] * scale : -INFINITY;
             up |= s[j] > m[j] + kLazy;
           }
@@ -613,7 +616,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int j = 0; j < NH; ++j) {
             const int v = col0 + j;
             if (v < nqv) {
-              const int i = v / group, h = it.g * group + (v - i * group);
+              const int va = it.v0 + v;
+              const int i = va / group, h = it.g * group + (va - i * group);
               store_planes(p.out, p.out_lo_off, ((long long)(it.r0 + i) * p.n_q + h) * D + t, o[j] / l[j]);
             }
           }

@@ -150,8 +150,12 @@ struct AttnParams {
   const unsigned long long* row_anc = nullptr;  // [R] token trees: ancestor sets (null: block-causal chains)
   int* status = nullptr;
   int B = 0, n_q = 0, n_kv = 0, page = 0;
+  // query vectors per work item (0: all of a (slot, kv head) in one item);
+  // the items of a (slot, kv head, chunk) then take vectors [h * qsplit, ...)
+  int qsplit = 0;
 };
-constexpr int kAttnQMax = 48;  // query vectors per (slot, kv head): (gamma+1) * group
+constexpr int kAttnQMax = 48;   // query vectors per work item of the mma.sync kernel (and partial slot)
+constexpr int kAttnQVecs = 64;  // query vectors per (slot, kv head), (gamma+1) * group, with items split
 
 // The tcgen05 attention kernel (head_dim 128, nq = 16 or 32 query vectors per
 // item); split sequences still need launch_attention_merge afterwards.
@@ -193,6 +197,8 @@ struct PrologueParams {
   int n_kv = 0, head_dim = 0, target_items = 0;
   float rope_theta = 0.f;
   int check_tokens = 1;
+  // attention work items: query vectors per item (0: no split) and query heads
+  int qsplit = 0, n_q = 0;
   // test hook (0 = off): block 0 waits this long on a barrier nothing arrives
   // at, through the bounded wait the pipelined kernels use, and records
   // SDV_ERR_TIMEOUT when it gives up

@@ -184,21 +184,27 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   // a whole item's pipeline fill)
   int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
   if (chunks_b > 1 && used - (chunks_b - 1) * chunk <= chunk / 4) --chunks_b;
+  // the slot's query vectors of one kv head, in items of at most qsplit
+  const int nqv = (gam + 1) * (p.n_q / p.n_kv);
+  const int halves = (slot && p.qsplit > 0) ? (nqv + p.qsplit - 1) / p.qsplit : 1;
   int tot_items;
-  const int ioff = block_exscan(chunks_b * p.n_kv, &tot_items, s_warp);
+  const int ioff = block_exscan(chunks_b * p.n_kv * halves, &tot_items, s_warp);
   if (slot) {
     p.t.chunks[b] = chunks_b;
     p.t.item_off[b] = ioff;
     if (p.t.items) {
-      // one record per (kv head, chunk) of this slot, item = (kv head) * chunks + chunk
+      // one record per (kv head, vector part, chunk) of this slot, item =
+      // (kv head * parts + part) * chunks + chunk; the part's first vector
+      // rides in the upper half of the kv head field
       for (int c = 0; c < chunks_b; ++c) {
         const int p0 = c * chunk;
         const int p1 = c == chunks_b - 1 ? used : p0 + chunk;
-        for (int g = 0; g < p.n_kv; ++g) {
-          const int item = ioff + g * chunks_b + c;
-          p.t.items[2 * item] = make_int4(b, g, p0, p1);
-          p.t.items[2 * item + 1] = make_int4(L, gam, roff, chunks_b);
-        }
+        for (int g = 0; g < p.n_kv; ++g)
+          for (int h = 0; h < halves; ++h) {
+            const int item = ioff + (g * halves + h) * chunks_b + c;
+            p.t.items[2 * item] = make_int4(b, g | ((h * p.qsplit) << 16), p0, p1);
+            p.t.items[2 * item + 1] = make_int4(L, gam, roff, chunks_b);
+          }
       }
     }
   }

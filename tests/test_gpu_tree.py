@@ -212,8 +212,8 @@ def test_tree_step_tiny(torch_cuda):
 
 @pytest.mark.parametrize("path", [1, 2])
 def test_tree_step_nine_b(torch_cuda, nine_b_weights, path):
-    """The 9B-class layer: both attention kernels (tcgen05 takes at most 32
-    query vectors per KV head: 8 nodes at 4 query heads per KV head)."""
+    """The 9B-class layer: both attention kernels, trees of up to 8 nodes (32
+    query vectors per KV head at 4 query heads per KV head)."""
     W, Wd = nine_b_weights
     gmax = 7
     eng = gh.engine_for(wl.NINE_B, gmax, Wd, 64, 8)
@@ -226,6 +226,27 @@ def test_tree_step_nine_b(torch_cuda, nine_b_weights, path):
     _plant(batch, W, trees, par, g)
     ref = _check_tree_step(eng, W, batch, trees, par, f"nine-b-tree-{path}")
     assert int(ref["accepted"].max()) >= 2
+
+
+def test_tree_step_nine_b_sixteen_nodes(torch_cuda, nine_b_weights):
+    """The tree size the pages name for one agent, ~8 to 16 deep ("Speculative
+    Decoding and Batching Compete for the Same Compute Slack on RDNA4", table
+    in "What the budget says to build"): 16-node trees on the 9B-class layer,
+    64 query vectors per KV head, which the tcgen05 attention kernel takes in
+    two items of 32."""
+    W, Wd = nine_b_weights
+    gmax = 15
+    eng = gh.engine_for(wl.NINE_B, gmax, Wd, 64, 8)
+    eng.set_sampling(GREEDY)
+    eng.set_attention_path(2)
+    g = np.random.default_rng(16)
+    chain16 = list(range(-1, 15))
+    trees = [_random_tree(g, 16), chain16, [-1] + [0] * 15, _random_tree(g, 11)]
+    lens = [2048, 700, 3000, 31]
+    batch, par = _tree_batch(wl.NINE_B, trees, lens, 16, gmax)
+    _plant(batch, W, trees, par, g)
+    ref = _check_tree_step(eng, W, batch, trees, par, "nine-b-tree-16")
+    assert int(ref["accepted"].max()) >= 3
 
 
 @pytest.mark.parametrize("path", [1, 2])
