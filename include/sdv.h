@@ -68,7 +68,8 @@ enum { SDV_WEIGHTS_BF16 = 0, SDV_WEIGHTS_INT4_G32 = 1 };
 
 /* Model and step dimensions.  head_dim in {64, 128}; n_q a multiple of n_kv;
  * hidden, n_q*head_dim and ffn multiples of 64 (of 256 for int4); page_size 16.
- * gamma_max bounds every gamma_b and sets how many pages realignment keeps. */
+ * gamma_max bounds every gamma_b and sets how many pages realignment keeps;
+ * (gamma_max + 1) * n_q / n_kv is at most 64 with head_dim 128, 48 with 64. */
 typedef struct {
   int hidden, n_q, n_kv, head_dim, ffn, vocab, page_size, gamma_max;
   int weight_format; /* SDV_WEIGHTS_BF16 or SDV_WEIGHTS_INT4_G32 */
@@ -311,11 +312,13 @@ enum { SDV_SAMPLING_STOCHASTIC = 0, SDV_SAMPLING_GREEDY = 1 };
 sdv_status sdv_set_sampling(sdv_ctx *ctx, int mode);
 
 /* Which kernel runs the step's attention: SDV_GEMM_AUTO (tcgen05 when
- * head_dim is 128, (gamma_max + 1) * n_q / n_kv <= 32 and the batch has at
- * least 4 sequences, else mma.sync),
- * SDV_GEMM_MMA_SYNC, or SDV_GEMM_TCGEN05 (SDV_ERR_UNSUPPORTED from the step
- * and sdv_attention when the shape does not fit it).  Results agree up to
- * fp32 summation order.  Host-side setting; takes effect on the next call. */
+ * head_dim is 128 and the batch has at least 4 sequences, or whenever
+ * (gamma_max + 1) * n_q / n_kv exceeds 48; else mma.sync), SDV_GEMM_MMA_SYNC
+ * (up to 48 query vectors per sequence and kv head), or SDV_GEMM_TCGEN05
+ * (head_dim 128, up to 64 query vectors, taken 32 per work item).  A shape
+ * the chosen kernel does not take is SDV_ERR_UNSUPPORTED from the step and
+ * sdv_attention, before anything is enqueued.  Results agree up to fp32
+ * summation order.  Host-side setting; takes effect on the next call. */
 sdv_status sdv_set_attention_path(sdv_ctx *ctx, int path);
 
 /* Test hook for the device-side failure path; 0 (the default) turns it off.

@@ -176,7 +176,8 @@ class VerifyEngine:
         self._check(self.lib.sdv_trace_enable(_ptr(table)), "sdv_trace_enable")
 
     def set_attention_path(self, path: int):
-        """0 auto, 1 mma.sync, 2 tcgen05 (head_dim 128, <= 32 query vectors per item)."""
+        """0 auto, 1 mma.sync (<= 48 query vectors per sequence and kv head), 2 tcgen05
+        (head_dim 128, <= 64 query vectors, 32 per work item)."""
         self._check(self.lib.sdv_set_attention_path(self.handle, int(path)), "sdv_set_attention_path")
 
     def set_stall_test(self, stall_ns: int):

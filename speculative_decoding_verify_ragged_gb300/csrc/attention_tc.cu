@@ -1,5 +1,6 @@
 // Block-causal GQA attention on the 5th-generation tensor cores (head_dim 128,
-// up to 32 query vectors per (sequence, KV head)).
+// up to 32 query vectors per work item; a (sequence, KV head) with more --
+// up to 64 -- comes as adjacent items of 32 from its first vector v0).
 //
 // Same work items, masking and outputs as the mma.sync kernel (attention.cu):
 // row i of sequence b sees positions 0 .. L_b + i of its own paged cache
