@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // order, the same order the last-arriving CTA of a one-CTA cluster uses, so
 // the result does not depend on the mode.
 template <int EPI>
-__global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, int Q) {
+__global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams p, int Q) {
   SDV_TRACE_SCOPE(kTrFixup + SDV_GEMM_SLOT(EPI, p));
   constexpr int LD = EPI_LD;
   __shared__ float epi[16 * LD];
@@ -500,10 +500,10 @@ __global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, 
   float v[16];
 #pragma unroll
   for (int n = 0; n < 16; ++n) v[n] = 0.f;
-  for (int qq0 = q_first; qq0 <= q_last; qq0 += 4) {
-    float w[4][16];
+  for (int qq0 = q_first; qq0 <= q_last; qq0 += 2) {
+    float w[2][16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 2; ++i)
       if (qq0 + i <= q_last) {
         const int qq = qq0 + i;
         const int first_tg_qq = static_cast<int>(((long long)qq * total / Q) / p.kb);
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(128) gemm_tc_fixup_kernel(const GemmParams p, 
         for (int n = 0; n < 16; ++n) w[i][n] = __ldcg(src + (size_t)n * BM);
       }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 2; ++i)
       if (qq0 + i <= q_last) {
 #pragma unroll
         for (int n = 0; n < 16; ++n) v[n] += w[i][n];

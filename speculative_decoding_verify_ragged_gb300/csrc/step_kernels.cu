@@ -189,23 +189,37 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   const int halves = (slot && p.qsplit > 0) ? (nqv + p.qsplit - 1) / p.qsplit : 1;
   int tot_items;
   const int ioff = block_exscan(chunks_b * p.n_kv * halves, &tot_items, s_warp);
+  // the slot of an item is found by binary search over the item offsets, so
+  // that consecutive threads write consecutive records (one thread per slot
+  // would write a lone sequence's hundreds of records serially)
+  __shared__ int s_ioff[kScanThreads];
+  __shared__ int4 s_rec[kScanThreads];
   if (slot) {
     p.t.chunks[b] = chunks_b;
     p.t.item_off[b] = ioff;
-    if (p.t.items) {
-      // one record per (kv head, vector part, chunk) of this slot, item =
-      // (kv head * parts + part) * chunks + chunk; the part's first vector
-      // rides in the upper half of the kv head field
-      for (int c = 0; c < chunks_b; ++c) {
-        const int p0 = c * chunk;
-        const int p1 = c == chunks_b - 1 ? used : p0 + chunk;
-        for (int g = 0; g < p.n_kv; ++g)
-          for (int h = 0; h < halves; ++h) {
-            const int item = ioff + (g * halves + h) * chunks_b + c;
-            p.t.items[2 * item] = make_int4(b, g | ((h * p.qsplit) << 16), p0, p1);
-            p.t.items[2 * item + 1] = make_int4(L, gam, roff, chunks_b);
-          }
+    s_ioff[b] = ioff;
+    s_rec[b] = make_int4(L, gam, roff, chunks_b);
+  }
+  __syncthreads();
+  if (p.t.items) {
+    // item = ioff + (kv head * parts + part) * chunks + chunk; the part's first
+    // query vector rides in the upper half of the kv head field
+    for (int it = threadIdx.x; it < tot_items; it += blockDim.x) {
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_ioff[mid] <= it) lo = mid; else hi = mid - 1;
       }
+      const int4 rec = s_rec[lo];
+      const int nb = rec.w;
+      const int parts = p.qsplit > 0 ? ((rec.y + 1) * (p.n_q / p.n_kv) + p.qsplit - 1) / p.qsplit : 1;
+      const int local = it - s_ioff[lo];
+      const int c = local % nb, gh = local / nb;
+      const int g = gh / parts, h = gh - g * parts;
+      const int p0 = c * chunk;
+      const int p1 = c == nb - 1 ? (rec.x + rec.y + 1 + p.page - 1) / p.page : p0 + chunk;
+      p.t.items[2 * it] = make_int4(lo, g | ((h * p.qsplit) << 16), p0, p1);
+      p.t.items[2 * it + 1] = rec;
     }
   }
   if (b == 0) {
@@ -488,29 +502,65 @@ constexpr int kVChunk = kSampleChunk;  // vocab entries per sampling warp
 constexpr int kPerThread = kVChunk / kAccThreads;
 constexpr int kChunksPerThread = kMaxSampleChunks / kAccThreads;  // last block's scan
 
+// The sampling weights are floor(w * 2^32) (fixed point, summed exactly).
+// Kernels carry x = w * 2^32, an exact scaling of w, and take the floor in two
+// 16-bit halves: x = h * 2^16 + r with h = floor(x / 2^16), r < 2^16 exact, and
+// floor(x) = h * 2^16 + floor(r).  A round-down add of 2^23 to a value v in
+// [0, 2^23) gives 2^23 + floor(v) exactly, whose bits are kFixBias + floor(v):
+// two adds per floor on the FMA pipe instead of a float -> integer conversion
+// or 64-bit shifts.  Valid for x in [0, 2^33), i.e. w in [0, 2).
+constexpr uint32_t kFixBias = 0x4B000000u;  // the bits of 2^23
+constexpr float kFixScale = 4294967296.0f;   // 2^32
+
+__device__ __forceinline__ void fixed_split(float x, uint32_t& hb, uint32_t& lb) {
+  const float h = __fadd_rd(__fmul_rn(x, 1.0f / 65536.0f), 8388608.0f);
+  hb = __float_as_uint(h);
+  lb = __float_as_uint(__fadd_rd(__fmaf_rn(__fsub_rn(h, 8388608.0f), -65536.0f, x), 8388608.0f));
+}
+
+// floor(x) of one x in [0, 2^33)
+__device__ __forceinline__ unsigned long long fixed_of(float x) {
+  uint32_t hb, lb;
+  fixed_split(x, hb, lb);
+  return (static_cast<unsigned long long>(hb - kFixBias) << 16) + (lb - kFixBias);
+}
+
+// Running sums of the biased halves of a lane's terms; the bias comes out once
+// (n terms: n * kFixBias, wrapping) and the true halves, below n * 2^17, stay
+// exact in 32 bits for n * 32 lanes <= 2^15 terms.
+struct FixedAcc {
+  uint32_t h = 0, l = 0;
+  __device__ __forceinline__ void add(float x) {
+    uint32_t hb, lb;
+    fixed_split(x, hb, lb);
+    h += hb;
+    l += lb;
+  }
+};
+
+// The sampled distribution's x = w * 2^32 for the raw value v of a row: from
+// logits 2^((v - M) log2 e) * 2^32 / sum, with nml = -M log2 e and s32 = 2^32 /
+// sum; given probabilities times 2^32, clamped to [0, 2) (the weights' range;
+// NaN reads as 0).
 template <bool FROM_LOGITS>
 struct PSource {
   const float* base;  // logits or probabilities
   int V;
-  __device__ __forceinline__ float p(int row, int j, float M, float S) const {
+  __device__ __forceinline__ float x_of(float v, float nml, float s32) const {
     if constexpr (FROM_LOGITS) {
-      return expf(base[(long long)row * V + j] - M) * S;  // S: the reciprocal of the row's sum
+      return __fmul_rn(exp2f(__fmaf_rn(v, kLog2e, nml)), s32);
     } else {
-      return base[(long long)row * V + j];
+      return __fmul_rn(fminf(fmaxf(v, 0.f), 1.99999988f), kFixScale);
     }
+  }
+  __device__ __forceinline__ float x(int row, int j, float nml, float s32) const {
+    return x_of(base[(long long)row * V + j], nml, s32);
   }
 };
 
-// floor(w * 2^32) for w in [0, 2), from the bits: w = m * 2^(e - 150) with the
-// 24-bit significand m, so w * 2^32 = m * 2^(e - 118); the same value as the
-// truncating float -> uint64 conversion, in integer shifts.
-__device__ __forceinline__ unsigned long long fixed_weight(float w) {
-  const uint32_t bits = __float_as_uint(w);
-  const int e = static_cast<int>((bits >> 23) & 0xFFu);
-  if (e == 0 || (bits >> 31)) return 0ull;  // zero, subnormal (< 2^-126) or negative
-  const unsigned long long m = (bits & 0x7FFFFFu) | 0x800000u;
-  const int sh = e - 118;
-  return sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
+// x of the residual max(0, p - q): (p - q) * 2^32 rounded once, as p - q is
+__device__ __forceinline__ float residual_x(float x, float q) {
+  return fmaxf(0.f, __fmaf_rn(q, -kFixScale, x));
 }
 
 // First row of slot b: the sum of (gamma + 1) over the earlier slots, from the
@@ -664,7 +714,6 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
   }
   if (st != 0) return;
   __syncthreads();  // s_a is set before any test lowers it
-  PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
   if constexpr (FROM_LOGITS) {
     merge_slot_stats(p, r0, gam, s_st, s_arg, true);
   }
@@ -738,29 +787,11 @@ __global__ void __launch_bounds__(kAccThreads) accept_kernel(const AcceptParams 
     const int k = threadIdx.x;
     float pk;
     if constexpr (FROM_LOGITS) pk = expf(zx - s_st[k].x) / s_st[k].y;
-    else pk = src.p(r0 + k, x, 0.f, 1.f);
+    else pk = p.probs[(long long)(r0 + k) * V + x];
     if (!((pk >= qk && pk > 0.f) || (__fmul_rn(uk, qk) < pk))) atomicMin(&s_a, k);
   }
   __syncthreads();
   if (threadIdx.x == 0) p.accepted[b] = s_a;
-}
-
-// Fixed-point weights of one float4 of p (and of the residual against q).
-template <bool FROM_LOGITS>
-__device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M, float S, unsigned long long& sr,
-                                         unsigned long long& sp) {
-  float pj[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (FROM_LOGITS) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pj[e] = expf(pj[e] - M) * S;  // S: the reciprocal of the row's sum
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) sp += fixed_weight(pj[e]);
-  if (has_q) {
-    const float qj[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sr += fixed_weight(fmaxf(0.f, pj[e] - qj[e]));
-  }
 }
 
 // FUSED (from logits, stochastic): every block of a slot also merges the
@@ -768,7 +799,7 @@ __device__ __forceinline__ void weights4(float4 v, float4 q, bool has_q, float M
 // in the same order as the acceptance kernel, so all blocks agree on the
 // accepted count); block 0 stores the count and the row statistics.
 template <bool FROM_LOGITS, bool FUSED>
-__global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams p) {
+__global__ void __launch_bounds__(kAccThreads, 4) sample_kernel(const AcceptParams p) {
   static_assert(FROM_LOGITS || !FUSED, "the fused tests read logits");
   SDV_TRACE_SCOPE(kTrSample);
   __shared__ unsigned long long s_red[2][kAccWarps];
@@ -846,28 +877,32 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   }
   const int rf = r0 + a;
   const float* qrow = !dead && a < gam ? p.draft_probs + (long long)(g0 + a) * V : nullptr;
-  float M = 0.f, S = 1.f;
+  // x = w * 2^32 of the row: from logits 2^((z - M) log2 e) * 2^32 / sum
+  float nml = 0.f, s32 = kFixScale;
   if constexpr (FROM_LOGITS) {
     if (!dead) {
       const float2 rs = s_rst[a];
-      M = rs.x;
-      S = 1.f / rs.y;  // weights as exp(z - M) times the reciprocal of the sum
+      nml = -rs.x * kLog2e;
+      s32 = __fmul_rn(1.f / rs.y, kFixScale);
     }
   }
   PSource<FROM_LOGITS> src{FROM_LOGITS ? p.z : p.probs, V};
 
   // chunk sums of the residual weights max(0, p - q) and of the plain weights
   // p: warp w of block x takes chunks x * warps + w, stepping over the slot's
-  // blocks; each lane issues all its loads of a chunk before using them
+  // blocks; each lane issues all its loads of a chunk before using them and
+  // adds 16 terms to each sum (entries past the vocabulary as zeros)
   unsigned long long* cs = p.chunk_sums + (long long)b * p.chunk_ld * 2;
   const float* prow = (FROM_LOGITS ? p.z : p.probs) + (long long)rf * V;
   const bool vec = (V & 3) == 0;  // rows are 16-byte aligned: float4 loads
   constexpr int kVecPerLane = kVChunk / (4 * kWarp);
+  constexpr uint32_t kLaneTerms = kVChunk / kWarp;
+  static_assert(kLaneTerms * kWarp <= (1u << 15), "the halves' sums stay exact in 32 bits");
+  const bool has_q = qrow != nullptr;
   for (int c = blockIdx.x * kAccWarps + warp; !dead && c < nch; c += gridDim.x * kAccWarps) {
-    unsigned long long sr = 0, sp = 0;
+    FixedAcc ap, ar;
     const int j0 = c * kVChunk;
     if (vec) {
-      const bool has_q = qrow != nullptr;
       float4 zv[kVecPerLane], qv[kVecPerLane];
 #pragma unroll
       for (int e = 0; e < kVecPerLane; ++e) {
@@ -881,24 +916,38 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
       }
 #pragma unroll
       for (int e = 0; e < kVecPerLane; ++e) {
-        const int j = j0 + (e * kWarp + lane) * 4;
-        if (j < V) weights4<FROM_LOGITS>(zv[e], qv[e], has_q, M, S, sr, sp);
+        const bool in = j0 + (e * kWarp + lane) * 4 < V;
+        const float zz[4] = {zv[e].x, zv[e].y, zv[e].z, zv[e].w};
+        const float qq[4] = {qv[e].x, qv[e].y, qv[e].z, qv[e].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float x = in ? src.x_of(zz[k], nml, s32) : 0.f;
+          ap.add(x);
+          if (has_q) ar.add(residual_x(x, qq[k]));
+        }
       }
     } else {
       for (int e = lane; e < kVChunk; e += kWarp) {
         const int j = j0 + e;
-        if (j < V) {
-          const float pj = src.p(rf, j, M, S);
-          sp += fixed_weight(pj);
-          if (qrow) sr += fixed_weight(fmaxf(0.f, pj - qrow[j]));
-        }
+        const float x = j < V ? src.x(rf, j, nml, s32) : 0.f;
+        ap.add(x);
+        if (has_q) ar.add(j < V ? residual_x(x, qrow[j]) : 0.f);
       }
     }
-    sr = warp_sum_u64(sr);
-    sp = warp_sum_u64(sp);
+    uint32_t ph = ap.h - kLaneTerms * kFixBias, pl = ap.l - kLaneTerms * kFixBias;
+    uint32_t rh = has_q ? ar.h - kLaneTerms * kFixBias : 0u, rl = has_q ? ar.l - kLaneTerms * kFixBias : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ph += __shfl_xor_sync(0xffffffffu, ph, o);
+      pl += __shfl_xor_sync(0xffffffffu, pl, o);
+      if (has_q) {
+        rh += __shfl_xor_sync(0xffffffffu, rh, o);
+        rl += __shfl_xor_sync(0xffffffffu, rl, o);
+      }
+    }
     if (lane == 0) {
-      cs[c] = sr;
-      cs[p.chunk_ld + c] = sp;
+      cs[c] = (static_cast<unsigned long long>(rh) << 16) + rl;
+      cs[p.chunk_ld + c] = (static_cast<unsigned long long>(ph) << 16) + pl;
     }
   }
   __syncthreads();
@@ -1012,8 +1061,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
   for (int e = 0; e < kPerThread; ++e) {
     const int j = j0 + e;
     if (j < V) {
-      const float pj = src.p(rf, j, M, S);
-      mine += fixed_weight(mode == 0 ? fmaxf(0.f, pj - qrow[j]) : pj);
+      const float x = src.x(rf, j, nml, s32);
+      mine += fixed_of(mode == 0 ? residual_x(x, qrow[j]) : x);
     }
   }
   unsigned long long incl = mine;
@@ -1033,8 +1082,8 @@ __global__ void __launch_bounds__(kAccThreads) sample_kernel(const AcceptParams 
     for (int e = 0; e < kPerThread; ++e) {
       const int j = j0 + e;
       if (j >= V) break;
-      const float pj = src.p(rf, j, M, S);
-      run += fixed_weight(mode == 0 ? fmaxf(0.f, pj - qrow[j]) : pj);
+      const float x = src.x(rf, j, nml, s32);
+      run += fixed_of(mode == 0 ? residual_x(x, qrow[j]) : x);
       if (run > T) {
         s_tok = j;
         break;
@@ -1286,12 +1335,13 @@ static int sms_of_current_device() {
 }
 
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
-  // sampling: about two blocks per SM over the whole batch (what the kernel's
-  // registers let an SM hold), never more blocks per slot than its vocabulary
-  // has chunks for (one warp per chunk)
+  // sampling: about eight blocks per SM over the whole batch, two waves of
+  // what the kernel's registers let an SM hold, so that the blocks of slots
+  // whose rows need both weight kinds even out across SMs; never more blocks
+  // per slot than its vocabulary has chunks for (one warp per chunk)
   const int nch = (p.V + kVChunk - 1) / kVChunk;
   const int max_per_slot = (nch + kAccWarps - 1) / kAccWarps;
-  const int want = (2 * sms_of_current_device() + p.B - 1) / p.B;
+  const int want = (8 * sms_of_current_device() + p.B - 1) / p.B;
   const dim3 grid(want < 1 ? 1 : (want > max_per_slot ? max_per_slot : want), p.B);
   cudaError_t e;
   if (from_logits) {
