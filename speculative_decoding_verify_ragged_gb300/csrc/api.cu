@@ -239,7 +239,7 @@ struct sdv_ctx {
   CUtensorMap tm_qkv, tm_o, tm_gate, tm_up, tm_down, tm_lm;
   CUtensorMap ts_qkv, ts_o, ts_gate, ts_up, ts_down;
   bool int4;
-  CUtensorMap tm_h[6], tm_attn[6], tm_act[6], tm_h3[6];  // activation tiles of 8..256 rows
+  CUtensorMap tm_h[kXMaps], tm_attn[kXMaps], tm_act[kXMaps], tm_h3[kXMaps];  // activation boxes kXBoxes
   int gemm_path;
   int attn_path;
   int sampling;
@@ -309,12 +309,11 @@ sdv_status sdv_create(const sdv_config* cfg, const sdv_weights* w, void* workspa
          encode_bf16_2d(&c->tm_gate, w->w_gate, F, H, 64) && encode_bf16_2d(&c->tm_up, w->w_up, F, H, 64) &&
          encode_bf16_2d(&c->tm_down, w->w_down, H, F, 64);
   }
-  const int nts[6] = {8, 16, 32, 64, 128, 256};
-  for (int i = 0; i < 6 && ok; ++i) {
-    ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, 2ull * max_rows, H, nts[i]) &&
-         encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, 2ull * max_rows, QD, nts[i]) &&
-         encode_bf16_2d(&c->tm_act[i], c->ws + L.act, 2ull * max_rows, F, nts[i]) &&
-         encode_bf16_2d(&c->tm_h3[i], c->ws + L.h3, max_rows, H, nts[i]);
+  for (int i = 0; i < kXMaps && ok; ++i) {
+    ok = encode_bf16_2d(&c->tm_h[i], c->ws + L.h, 2ull * max_rows, H, kXBoxes[i]) &&
+         encode_bf16_2d(&c->tm_attn[i], c->ws + L.attn, 2ull * max_rows, QD, kXBoxes[i]) &&
+         encode_bf16_2d(&c->tm_act[i], c->ws + L.act, 2ull * max_rows, F, kXBoxes[i]) &&
+         encode_bf16_2d(&c->tm_h3[i], c->ws + L.h3, max_rows, H, kXBoxes[i]);
   }
   if (!ok) {
     delete c;
@@ -880,10 +879,9 @@ sdv_status sdv_linear(sdv_ctx* c, int which, const void* x, int x_format, float*
     xsrc = planes;
     g.x_lo_row = rows;
   }
-  CUtensorMap xm[6];
-  const int nts[6] = {8, 16, 32, 64, 128, 256};
-  for (int i = 0; i < 6; ++i)
-    if (!encode_bf16_2d(&xm[i], xsrc, (xf32 ? 2ull : 1ull) * rows, K, nts[i])) return SDV_ERR_CUDA;
+  CUtensorMap xm[kXMaps];
+  for (int i = 0; i < kXMaps; ++i)
+    if (!encode_bf16_2d(&xm[i], xsrc, (xf32 ? 2ull : 1ull) * rows, K, kXBoxes[i])) return SDV_ERR_CUDA;
   g.epi.out_f32 = y;
   g.epi.ld_f32 = N;
   SDV_CUDA(run_gemm(c, EPI_F32, xf32 ? 2 : 1, wm, wm, xm, g, s, sm, sm));

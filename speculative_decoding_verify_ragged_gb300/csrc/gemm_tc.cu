@@ -22,6 +22,20 @@
 // is refilled only once every CTA has released it -- measured the same; it
 // stays selectable for A/B timing.)
 //
+// From 128 activation rows the CTAs work in pairs (a cluster of two, tcgen05
+// cta_group::2): one MMA of M = 256 weight rows (128 in each CTA's shared
+// memory) x N = NT activation rows (each CTA holding NT / 2 of them) writes
+// each CTA's 128 rows of the product into its own tensor memory.  Per SM a
+// k-block then moves 16 KB of weights and NT / 2 activation rows instead of NT
+// -- at NT = 256 two thirds of the bytes for the same flops -- and the ring
+// holds half again as many stages.  The first CTA of the pair issues the MMAs
+// and owns the stage barriers: both CTAs' copies complete on its barriers,
+// its commits free the stage and signal the accumulator in both CTAs, and the
+// epilogue warps of both CTAs release an accumulator on its barrier.  Each
+// CTA loads its activation rows of a stage with one copy per plane (a map of
+// that box height exists for every multiple of 16 up to 256): copies of 16 or
+// 32 rows measured as much as a third slower than the MMAs they feed.
+//
 // Warp roles (192 threads):
 //  * warp 0: TMA producer (one lane) -- weight half-tiles and activation planes
 //    into a multi-stage ring; weights are streamed before waiting for the
@@ -58,11 +72,15 @@ constexpr int kScaleRows = 256;  // rows of the per-CTA RMSNorm row-scale cache 
 // the row-scale cache
 constexpr int FIXED_BYTES = 1024 + EPI_BYTES + (2 * kMaxStages + 4) * 8 + 16 + kScaleRows * 4;
 
-__host__ __device__ constexpr int tc_stage_bytes(int nt, int xp) { return A_BYTES + xp * nt * BK * 2; }
-__host__ __device__ constexpr int tc_stages(int nt, int xp) {
-  return (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp) > kMaxStages
+// Bytes of one ring stage in one CTA: the CTA's 128 weight rows and its
+// activation rows (all nt of them, or half in a CTA pair) per plane.
+__host__ __device__ constexpr int tc_stage_bytes(int nt, int xp, bool pair = false) {
+  return A_BYTES + xp * (pair ? nt / 2 : nt) * BK * 2;
+}
+__host__ __device__ constexpr int tc_stages(int nt, int xp, bool pair = false) {
+  return (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp, pair) > kMaxStages
              ? kMaxStages
-             : (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp);
+             : (kSmemBudget - FIXED_BYTES) / tc_stage_bytes(nt, xp, pair);
 }
 static_assert(tc_stages(256, 2) >= 2, "pipeline too shallow");
 
@@ -104,6 +122,63 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
+// ---- CTA pairs (tcgen05 cta_group::2) ----
+// The address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+
+// TMA tile load into this CTA's shared memory whose completion counts on the
+// barrier at cluster address `bar` -- in either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Arrive on the barrier at cluster address `bar` (this CTA's or the peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One MMA of the pair: M = 256 weight rows (128 from each CTA's shared
+// memory, at the same offsets), N activation rows (the first half from this
+// CTA, the second from the peer), accumulating into the same tensor-memory
+// columns of both CTAs (each its own 128 rows).
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t acc) {
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// Arrive on the barrier at `bar`'s offset in both CTAs of the pair once the
+// pair's tcgen05 operations issued so far by this thread complete.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t tmem_columns(int nt) {
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(2 * nt)) c <<= 1;
@@ -116,7 +191,7 @@ __device__ __forceinline__ int cluster_of_unit(long long u, long long total, int
   return static_cast<int>(((u + 1) * Q - 1) / total);
 }
 
-template <int EPI, int XP>
+template <int EPI, int XP, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmX, const GemmParams p) {
@@ -125,8 +200,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   griddep_launch_dependents();
 
   const int NT = p.nt, S = p.stages, cs = p.cs;
-  const bool mc = p.multicast != 0;  // a cluster shares weight tiles by multicast (else through L2)
-  const int STAGE = tc_stage_bytes(NT, XP);
+  const bool mc = !PAIR && p.multicast != 0;  // a cluster shares weight tiles by multicast (else through L2)
+  const int STAGE = tc_stage_bytes(NT, XP, PAIR);
+  const int NTC = PAIR ? NT / 2 : NT;  // activation rows this CTA loads per stage
   uint8_t* smem = align1024(smem_raw);
   float* epi = reinterpret_cast<float*>(smem + S * STAGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + EPI_BYTES);
@@ -138,9 +214,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   float* row_scale = reinterpret_cast<float*>(tmem_slot + 4);  // [kScaleRows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = mc ? static_cast<int>(cluster_ctarank()) : static_cast<int>(blockIdx.x) % cs;
-  const int q = mc ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x) / cs;
-  const int Q = static_cast<int>(gridDim.x) / cs;
+  // CTA pairs: half 0 issues the pair's MMAs; the pairs form the groups
+  const int half = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int team = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int rank = mc ? static_cast<int>(cluster_ctarank()) : team % cs;
+  const int q = mc ? static_cast<int>(cluster_id_x()) : team / cs;
+  const int Q = static_cast<int>(gridDim.x) / (PAIR ? 2 * cs : cs);
   const uint16_t everyone = static_cast<uint16_t>((1u << cs) - 1u);
   const uint32_t ncols = tmem_columns(NT);
   if (threadIdx.x == 0) {
@@ -150,24 +229,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (of both CTAs of a pair: the issuer's
+      // barrier is the one that counts)
+      mbar_init(&tempty[b], PAIR ? 8 : 4);
     }
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // a pair allocates the same columns in both CTAs, one warp of each
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(ncols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(ncols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA's barriers exist before a peer's multicast can land on them
-  if (mc) cluster_sync_all();
+  // every CTA's barriers exist before a peer's multicast, copy or arrival can land on them
+  if (mc || PAIR) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
+  // a pair's stage fills and accumulator releases count on the issuing CTA's barriers
+  const uint32_t lead_full = PAIR ? cluster_addr(full, 0) : 0u;
+  const uint32_t lead_tempty = PAIR ? cluster_addr(tempty, 0) : 0u;
 
-  const long long total = (long long)p.m_tiles * p.n_groups * p.kb;
+  // units: (weight tile -- of a pair: 256 rows --, activation group, k-block)
+  const int m_units = PAIR ? (p.m_tiles + 1) / 2 : p.m_tiles;
+  const long long total = (long long)m_units * p.n_groups * p.kb;
   const long long u_begin = (long long)q * total / Q;
   const long long u_end = (long long)(q + 1) * total / Q;
   const int first_tg = static_cast<int>(u_begin / p.kb);  // first (weight tile, group) of this cluster
@@ -200,10 +294,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       };
       auto weights = [&](const Cursor& cu, int stage) {
-        const int rowA0 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM;
-        const int rowA1 = EPI == EPI_SWIGLU ? cu.tm * 64 : cu.tm * BM + 64;
+        const int tmc = PAIR ? 2 * cu.tm + half : cu.tm;  // this CTA's 128-row weight tile
+        const int rowA0 = EPI == EPI_SWIGLU ? tmc * 64 : tmc * BM;
+        const int rowA1 = EPI == EPI_SWIGLU ? tmc * 64 : tmc * BM + 64;
         uint8_t* sa = smem + stage * STAGE;
-        if (cs == 1) {
+        if constexpr (PAIR) {
+          const uint32_t bar = lead_full + 8u * stage;
+          if (cs == 1) {
+            tma_load_2d_pair_hint(sa, &tmA0, bar, cu.k * BK, rowA0, pol);
+            tma_load_2d_pair_hint(sa + A_BYTES / 2, &tmA1, bar, cu.k * BK, rowA1, pol);
+          } else {
+            tma_load_2d_pair(sa, &tmA0, bar, cu.k * BK, rowA0);
+            tma_load_2d_pair(sa + A_BYTES / 2, &tmA1, bar, cu.k * BK, rowA1);
+          }
+        } else if (cs == 1) {
           tma_load_2d_hint(sa, &tmA0, &full[stage], cu.k * BK, rowA0, pol);
           tma_load_2d_hint(sa + A_BYTES / 2, &tmA1, &full[stage], cu.k * BK, rowA1, pol);
         } else if (!mc) {
@@ -219,27 +323,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       };
       auto acts = [&](const Cursor& cu, int stage) {
         uint8_t* sb = smem + stage * STAGE + A_BYTES;
-        const int row0 = (cu.grp * cs + rank) * NT;
-        for (int b = 0; b < NT; b += p.x_box) {
-          tma_load_2d(sb + b * 128, &tmX, &full[stage], cu.k * BK, row0 + b);
-          if constexpr (XP == 2)
-            tma_load_2d(sb + (NT + b) * 128, &tmX, &full[stage], cu.k * BK, p.x_lo_row + row0 + b);
+        // a pair's first CTA loads the first half of the activation tile
+        const int row0 = (cu.grp * cs + rank) * NT + half * NTC;
+        for (int b = 0; b < NTC; b += p.x_box) {
+          if constexpr (PAIR) {
+            const uint32_t bar = lead_full + 8u * stage;
+            tma_load_2d_pair(sb + b * 128, &tmX, bar, cu.k * BK, row0 + b);
+            if constexpr (XP == 2) tma_load_2d_pair(sb + (NTC + b) * 128, &tmX, bar, cu.k * BK, p.x_lo_row + row0 + b);
+          } else {
+            tma_load_2d(sb + b * 128, &tmX, &full[stage], cu.k * BK, row0 + b);
+            if constexpr (XP == 2)
+              tma_load_2d(sb + (NTC + b) * 128, &tmX, &full[stage], cu.k * BK, p.x_lo_row + row0 + b);
+          }
         }
       };
+      // the issuing CTA's barrier expects the bytes of both CTAs of a pair (a
+      // peer's copy may land before the expectation: the barrier's pending
+      // arrival keeps the phase open until then)
+      const bool lead = !PAIR || half == 0;
+      const uint32_t mult = PAIR ? 2u : 1u;
       Cursor cw = start_at(u_begin);
       for (int j = 0; j < pre; ++j) {
-        mbar_expect_tx(&full[j], A_BYTES);
+        if (lead) mbar_expect_tx(&full[j], mult * A_BYTES);
         weights(cw, j);
         advance(cw);
       }
       SDV_GRIDDEP_WAIT();
       if (read_status(p.status) != 0) {
-        for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
-        for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
+        // the weight copies land before anyone leaves (a peer's are counted
+        // on the issuer's barriers; the final cluster barrier holds it)
+        if (lead) {
+          for (int j = 0; j < pre; ++j) mbar_arrive(&full[j]);
+          for (int j = 0; j < pre; ++j) mbar_wait(&full[j], 0);
+        }
       } else {
         Cursor ca = start_at(u_begin);
         for (int j = 0; j < pre; ++j) {
-          mbar_arrive_expect_tx(&full[j], STAGE - A_BYTES);
+          if (lead) mbar_arrive_expect_tx(&full[j], mult * (STAGE - A_BYTES));
           acts(ca, j);
           advance(ca);
         }
@@ -253,7 +373,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             dead = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE);
+          if (lead) mbar_arrive_expect_tx(&full[stage], mult * STAGE);
           weights(cw, stage);
           acts(cw, stage);
           advance(cw);
@@ -277,11 +397,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (a pair's first CTA) ----------------
+    if (lane == 0 && half == 0) {
       SDV_GRIDDEP_WAIT();
       if (read_status(p.status) == 0) {
-        const uint32_t idesc = idesc_bf16(BM, NT);
+        const uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, NT);
         bool dead = false;
         int stage = 0;
         uint32_t phase = 0;
@@ -309,19 +429,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               const uint64_t a = desc_sw128(a_base + kk * 32);
 #pragma unroll
               for (int pl = 0; pl < XP; ++pl) {
-                const uint64_t b = desc_sw128(a_base + A_BYTES + pl * (NT * 128) + kk * 32);
-                umma_bf16(d, a, b, idesc, (k > k0 || kk > 0 || pl > 0) ? 1u : 0u);
+                const uint64_t b = desc_sw128(a_base + A_BYTES + pl * (NTC * 128) + kk * 32);
+                if constexpr (PAIR) umma_bf16_pair(d, a, b, idesc, (k > k0 || kk > 0 || pl > 0) ? 1u : 0u);
+                else umma_bf16(d, a, b, idesc, (k > k0 || kk > 0 || pl > 0) ? 1u : 0u);
               }
             }
             // frees the stage, in every CTA of the cluster, once these MMAs have read it
-            if (mc) umma_commit_mc(&empty[stage], everyone);
+            if constexpr (PAIR) umma_commit_pair(&empty[stage]);
+            else if (mc) umma_commit_mc(&empty[stage], everyone);
             else umma_commit(&empty[stage]);
             if (++stage == S) {
               stage = 0;
               phase ^= 1;
             }
           }
-          umma_commit(&tfull[buf]);  // accumulator complete
+          // accumulator complete (in both CTAs of a pair)
+          if constexpr (PAIR) umma_commit_pair(&tfull[buf]);
+          else umma_commit(&tfull[buf]);
           u += k1 - k0;
         }
       }
@@ -385,8 +509,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int tg = static_cast<int>(u / p.kb);
         const int k0 = static_cast<int>(u - (long long)tg * p.kb);
         const int k1 = static_cast<int>(min((long long)p.kb, k0 + (u_end - u)));
-        const int tm = tg / p.n_groups;
-        const int tn = (tg - tm * p.n_groups) * cs + rank;
+        const int tmu = tg / p.n_groups;
+        const int tn = (tg - tmu * p.n_groups) * cs + rank;
+        const int tm = PAIR ? 2 * tmu + half : tmu;  // this CTA's 128-row weight tile
         const int tile = tm * p.n_tiles + tn;
         const int buf = pc & 1;
         if (!dead && !mbar_wait(&tfull[buf], (pc >> 1) & 1)) {
@@ -399,16 +524,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
         // accumulator columns past the last activation row are never read
         const int cols = (rows + EC - 1) / EC * EC;
-        if (k0 == 0 && k1 == p.kb) {
+        // releases the accumulator (a pair's on the issuing CTA's barrier)
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PAIR) mbar_arrive_cluster(lead_tempty + 8u * buf);
+            else mbar_arrive(&tempty[buf]);
+          }
+        };
+        if (PAIR && tm >= p.m_tiles) {
+          // the second half of a pair past the last weight tile: nothing to store
+          release();
+        } else if (k0 == 0 && k1 == p.kb) {
           // whole tile in this CTA: epilogue straight from tensor memory
           for (int c0 = 0; c0 < cols; c0 += EC) {
             float v[16];
             tmem_ld16(t_row + c0, v);
-            if (c0 + EC == cols) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[buf]);
-            }
+            if (c0 + EC == cols) release();
 #pragma unroll
             for (int n = 0; n < EC; ++n) epi[n * LD + m] = v[n];
             named_sync(1, 4 * kWarp);
@@ -417,17 +550,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         } else {
           // tile cut between clusters: store this piece, the fixup sums them in cluster order
-          const int my_slot = 2 * (q * cs + rank) + (tg == first_tg ? 0 : 1);
+          const int my_slot = 2 * ((q * cs + rank) * (PAIR ? 2 : 1) + half) + (tg == first_tg ? 0 : 1);
           float* mine = p.partials + (size_t)my_slot * BM * NT;
           for (int c0 = 0; c0 < cols; c0 += EC) {
             float v[16];
             tmem_ld16(t_row + c0, v);
             tc_store_part16(mine, c0, m, v);
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
-          if (!p.defer_fixup) {
+          release();
+          if (!PAIR && !p.defer_fixup) {
             // one CTA per cluster (cs == 1): the last CTA to arrive sums the parts in CTA order
             const long long tu = (long long)tg * p.kb;
             const int c_first = cta_of_unit(tu, total, Q);
@@ -456,20 +587,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // shared memory or barriers any more
   tc_fence_before();
   __syncthreads();
-  if (mc) cluster_sync_all();
+  if (mc || PAIR) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
   }
 }
 
-// Deferred stream-K fixup: block (b, y) handles the boundary between clusters
+// Deferred stream-K fixup: block (b, y) handles the boundary between groups
 // b and b + 1 of the GEMM's grid when it cuts a (weight tile, group) and is
 // that unit range's first such boundary (the others exit), for the
-// activation tile of cluster rank y / chunks and its 16-row chunk y % chunks;
-// 128 threads, thread m = weight row m.  The parts are summed in cluster
-// order, the same order the last-arriving CTA of a one-CTA cluster uses, so
-// the result does not depend on the mode.
+// activation tile of group rank y / (H chunks), the 128-row weight tile
+// (y / chunks) % H of the unit (H = 2 with CTA pairs) and the 16-row chunk
+// y % chunks; 128 threads, thread m = weight row m.  The parts are summed in
+// group order, the same order the last-arriving CTA of a one-CTA group uses,
+// so the result does not depend on the mode.
 template <int EPI>
 __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams p, int Q) {
   SDV_TRACE_SCOPE(kTrFixup + SDV_GEMM_SLOT(EPI, p));
@@ -479,7 +614,8 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
   SDV_GRIDDEP_WAIT();
   if (read_status(p.status) != 0) return;
   const int NT = p.nt, cs = p.cs;
-  const long long total = (long long)p.m_tiles * p.n_groups * p.kb;
+  const int H = p.pair ? 2 : 1;  // 128-row weight tiles per unit
+  const long long total = (long long)((p.m_tiles + H - 1) / H) * p.n_groups * p.kb;
   const int qb = blockIdx.x + 1;
   const long long ub = (long long)qb * total / Q;
   const int tg = static_cast<int>(ub / p.kb);
@@ -487,12 +623,15 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
   if (ub == t0) return;                                      // the boundary falls on a tile edge
   if (qb > 1 && (long long)(qb - 1) * total / Q > t0) return;  // an earlier boundary cuts the same tile
   const int chunks = (NT + 15) / 16;
-  const int rank = blockIdx.y / chunks;
-  const int tm = tg / p.n_groups;
-  const int tn = (tg - tm * p.n_groups) * cs + rank;
-  if (tn >= p.n_tiles) return;
+  const int rank = blockIdx.y / (H * chunks);
+  const int hc = blockIdx.y - rank * H * chunks;
+  const int half = hc / chunks;
+  const int tmu = tg / p.n_groups;
+  const int tm = tmu * H + half;
+  const int tn = (tg - tmu * p.n_groups) * cs + rank;
+  if (tn >= p.n_tiles || tm >= p.m_tiles) return;
   const int rows = min(NT, p.R - tn * NT);
-  const int c0 = (blockIdx.y - rank * chunks) * 16;
+  const int c0 = (hc - half * chunks) * 16;
   if (c0 >= rows) return;
   const int m = threadIdx.x;
   const int q_first = cluster_of_unit(t0, total, Q);
@@ -507,7 +646,7 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
       if (qq0 + i <= q_last) {
         const int qq = qq0 + i;
         const int first_tg_qq = static_cast<int>(((long long)qq * total / Q) / p.kb);
-        const int slot = 2 * (qq * cs + rank) + (tg == first_tg_qq ? 0 : 1);
+        const int slot = 2 * ((qq * cs + rank) * H + half) + (tg == first_tg_qq ? 0 : 1);
         const float* src = p.partials + (size_t)slot * BM * NT + (size_t)c0 * BM + m;
 #pragma unroll
         for (int n = 0; n < 16; ++n) w[i][n] = __ldcg(src + (size_t)n * BM);
@@ -528,7 +667,7 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
 template <int EPI>
 cudaError_t launch_fixup_e(const GemmParams& p, int Q, cudaStream_t stream) {
   if (Q < 2) return cudaSuccess;  // one cluster cuts no tile
-  const dim3 g(Q - 1, p.cs * ((p.nt + 15) / 16));
+  const dim3 g(Q - 1, p.cs * (p.pair ? 2 : 1) * ((p.nt + 15) / 16));
   return launch_pdl(gemm_tc_fixup_kernel<EPI>, g, dim3(128), 0, stream, p, Q);
 }
 
@@ -555,23 +694,41 @@ constexpr int kDeferFixupRows = 32;
 using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, GemmParams);
 
 template <int EPI, int XP>
-Kern kernel_of() {
-  return reinterpret_cast<Kern>(gemm_tc_kernel<EPI, XP>);
+Kern kernel_of(bool pair) {
+  return pair ? reinterpret_cast<Kern>(gemm_tc_kernel<EPI, XP, true>)
+              : reinterpret_cast<Kern>(gemm_tc_kernel<EPI, XP, false>);
 }
 
-Kern pick_kernel(int epi, int xp) {
+Kern pick_kernel(int epi, int xp, bool pair) {
   switch (epi) {
-    case EPI_F32: return xp == 2 ? kernel_of<EPI_F32, 2>() : kernel_of<EPI_F32, 1>();
-    case EPI_RESID: return xp == 2 ? kernel_of<EPI_RESID, 2>() : kernel_of<EPI_RESID, 1>();
-    case EPI_SWIGLU: return xp == 2 ? kernel_of<EPI_SWIGLU, 2>() : kernel_of<EPI_SWIGLU, 1>();
-    case EPI_QKV: return xp == 2 ? kernel_of<EPI_QKV, 2>() : kernel_of<EPI_QKV, 1>();
-    case EPI_LMHEAD: return kernel_of<EPI_LMHEAD, 1>();
+    case EPI_F32: return xp == 2 ? kernel_of<EPI_F32, 2>(pair) : kernel_of<EPI_F32, 1>(pair);
+    case EPI_RESID: return xp == 2 ? kernel_of<EPI_RESID, 2>(pair) : kernel_of<EPI_RESID, 1>(pair);
+    case EPI_SWIGLU: return xp == 2 ? kernel_of<EPI_SWIGLU, 2>(pair) : kernel_of<EPI_SWIGLU, 1>(pair);
+    case EPI_QKV: return xp == 2 ? kernel_of<EPI_QKV, 2>(pair) : kernel_of<EPI_QKV, 1>(pair);
+    case EPI_LMHEAD: return kernel_of<EPI_LMHEAD, 1>(pair);
     default: return nullptr;
   }
 }
 
-// How the CTAs that take different activation tiles of the same weight tile
-// share its read: multicast within a thread-block cluster, or a group of
+// CTA pairs from kPairRows activation rows up: measured in the step of the
+// 9B-class layer, pairs against single CTAs at 320 rows took QKV 53.6 -> 44.0
+// us, gate/up 240.8 -> 184.4, the LM head 497.9 -> 362.9; at 1152 rows 120.6
+// -> 92.4, 535.6 -> 426.2 and 1239 -> 1072; below 128 rows, where both are
+// bound by the weight stream, they were within 2 % either way.
+// SDV_GEMM_PAIR=0|1 in the environment forces them off or on (A/B timing).
+constexpr int kPairRows = 128;
+int pair_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("SDV_GEMM_PAIR");
+    if (v && std::strcmp(v, "0") == 0) return 0;
+    if (v && std::strcmp(v, "1") == 0) return 1;
+    return 2;
+  }();
+  return mode;
+}
+
+// How the single CTAs that take different activation tiles of the same weight
+// tile share its read: multicast within a thread-block cluster, or a group of
 // consecutive CTAs reading it at about the same time through L2.
 // SDV_GEMM_SHARE=mc|l2|off in the environment picks one (A/B timing); the
 // default is l2.
@@ -585,10 +742,12 @@ int share_mode() {
   return mode;
 }
 
-int smem_for(int nt, int xp) { return FIXED_BYTES + tc_stages(nt, xp) * tc_stage_bytes(nt, xp); }
+int smem_for(int nt, int xp, bool pair = false) {
+  return FIXED_BYTES + tc_stages(nt, xp, pair) * tc_stage_bytes(nt, xp, pair);
+}
 
 // How many clusters of `cs` CTAs of this kernel fit on the GPU at once (cached).
-int active_clusters(Kern k, int cs, int smem, int sms) {
+int active_clusters(Kern k, int cs, int smem, int sms, bool hw_cluster) {
   static std::mutex mu;
   struct Entry {
     Kern k;
@@ -605,7 +764,7 @@ int active_clusters(Kern k, int cs, int smem, int sms) {
   }
   int n = 0;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
-    if (cs == 1 || share_mode() != 1) {
+    if (cs == 1 || !hw_cluster) {
       n = sms / cs;
     } else {
       cudaLaunchConfig_t cfg = {};
@@ -633,6 +792,7 @@ int active_clusters(Kern k, int cs, int smem, int sms) {
 
 struct TcChoice {
   int nt = 0, cs = 1, n_tiles = 0, n_groups = 0, grid = 0;
+  bool pair = false;
 };
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
@@ -648,6 +808,58 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // from 257 to 512 rows (gate/up at 320: 313 -> 240 us, at 512: 343 -> 296),
 // three at 640 (441 -> 417) and six at 1152 (715 -> 537).  Group sizes that
 // were not measured to pay are not used.
+// CTA pairs: a pair takes 256 weight rows against up to 256 activation rows,
+// each CTA loading half the activation tile, so that per SM a k-block moves
+// two thirds of the bytes of a one-CTA 128 x 256 tile and the ring holds half
+// again as many stages.  Tiles of about R / n rows (n = ceil(R / 256)), and
+// pairs in groups of n sharing each weight tile through L2, or one pair per
+// group walking the activation tiles of a weight tile back to back.
+TcChoice choose_pair(int epi, int xp, const GemmParams& g, int sms, int forced_cs) {
+  TcChoice c;
+  c.pair = true;
+  const int R = g.R;
+  const int pairs = active_clusters(pick_kernel(epi, xp, true), 2, smem_for(256, xp, true), sms, true);
+  if (pairs < 1) return TcChoice{};
+  // tile height: a multiple of 32 (each CTA's half in TMA boxes of at least
+  // 16 rows -- narrow boxes cost the producer more copies than the stage's
+  // MMAs take), the tile count n that keeps the busiest group's work, NT /
+  // (groups of n pairs), smallest
+  const int n0 = (R + 255) / 256;
+  double best = 0.0;
+  for (int n = n0; n <= n0 + 2; ++n) {
+    const int nt = round_up((R + n - 1) / n, 32);
+    if (nt > 256) continue;
+    const int tiles = (R + nt - 1) / nt;
+    const int groups = pairs / tiles;
+    if (groups < 1) continue;
+    const double cost = static_cast<double>(nt) / groups;
+    if (c.nt == 0 || cost < best * 0.999) {
+      best = cost;
+      c.nt = nt;
+      c.n_tiles = tiles;
+    }
+  }
+  if (c.nt == 0) {
+    c.nt = 256;
+    c.n_tiles = (R + 255) / 256;
+  }
+  const long long m_units = (g.m_tiles + 1) / 2;
+  const int cs = forced_cs > 0 ? forced_cs : c.n_tiles;
+  if (cs > 1 && cs == c.n_tiles && cs <= pairs) {
+    c.cs = cs;
+    c.n_groups = 1;
+    const long long units = m_units * g.kb;
+    const int groups = pairs / cs;
+    c.grid = static_cast<int>(units < groups ? units : groups) * cs * 2;
+    return c;
+  }
+  c.cs = 1;
+  c.n_groups = c.n_tiles;
+  const long long units = m_units * c.n_tiles * g.kb;
+  c.grid = static_cast<int>(units < pairs ? units : pairs) * 2;
+  return c;
+}
+
 TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
   static const int forced = [] {
     // SDV_GEMM_CS=n in the environment: groups of n wherever n tiles cover
@@ -655,8 +867,11 @@ TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
     const char* v = std::getenv("SDV_GEMM_CS");
     return v ? std::atoi(v) : 0;
   }();
-  (void)epi;
   const int R = g.R;
+  if (pair_mode() == 1 || (pair_mode() == 2 && R >= kPairRows)) {
+    const TcChoice c = choose_pair(epi, xp, g, sms, forced);
+    if (c.grid > 0) return c;
+  }
   int cs = 1;
   if (forced > 0) {
     cs = forced;
@@ -671,7 +886,8 @@ TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
     c.nt = round_up((R + cs - 1) / cs, 16);
     c.n_tiles = (R + c.nt - 1) / c.nt;
     if (c.nt <= 256 && c.n_tiles == cs) {
-      const int groups = active_clusters(pick_kernel(epi, xp), cs, smem_for(c.nt, xp), sms);
+      const int groups =
+          active_clusters(pick_kernel(epi, xp, false), cs, smem_for(c.nt, xp), sms, share_mode() == 1);
       if (groups > 0) {
         const long long units = (long long)g.m_tiles * g.kb;
         c.cs = cs;
@@ -690,21 +906,13 @@ TcChoice choose(int epi, int xp, const GemmParams& g, int sms) {
   return c;
 }
 
+// The TMA box height for a CTA's nt activation rows: all of them in one copy
+// when a map of that height exists, else the largest power of two dividing nt.
 int box_for(int nt) {
+  if (x_map_index(nt) >= 0) return nt;
   for (int b = 256; b >= 8; b >>= 1)
     if (nt % b == 0) return b;
   return 8;
-}
-
-int box_index(int box) {
-  switch (box) {
-    case 8: return 0;
-    case 16: return 1;
-    case 32: return 2;
-    case 64: return 3;
-    case 128: return 4;
-    default: return 5;
-  }
 }
 
 }  // namespace
@@ -722,6 +930,7 @@ cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid,
   GemmParams g = p;
   g.nt = nt;
   g.cs = 1;
+  g.pair = 0;
   g.n_groups = g.n_tiles;
   return launch_fixup(epi, g, grid, stream);
 }
@@ -729,19 +938,21 @@ cudaError_t launch_gemm_tc_fixup(int epi, int nt, const GemmParams& p, int grid,
 cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* xmaps,
                            GemmParams p, int sms, cudaStream_t stream) {
   if (epi == EPI_LMHEAD) xp = 1;
-  const Kern k = pick_kernel(epi, xp);
-  if (!k) return cudaErrorInvalidValue;
   const TcChoice c = choose(epi, xp, p, sms);
   if (c.grid < 1) return cudaErrorInvalidConfiguration;
+  const Kern k = pick_kernel(epi, xp, c.pair);
+  if (!k) return cudaErrorInvalidValue;
   p.nt = c.nt;
   p.cs = c.cs;
   p.n_tiles = c.n_tiles;
   p.n_groups = c.n_groups;
-  p.x_box = box_for(c.nt);
-  p.stages = tc_stages(c.nt, xp);
-  p.defer_fixup = (c.cs > 1 || c.nt >= kDeferFixupRows) ? 1 : 0;
-  p.multicast = c.cs > 1 && share_mode() == 1 ? 1 : 0;
-  const int smem = smem_for(c.nt, xp);
+  p.pair = c.pair ? 1 : 0;
+  // a pair's CTA loads half the activation tile
+  p.x_box = box_for(c.pair ? c.nt / 2 : c.nt);
+  p.stages = tc_stages(c.nt, xp, c.pair);
+  p.defer_fixup = (c.pair || c.cs > 1 || c.nt >= kDeferFixupRows) ? 1 : 0;
+  p.multicast = !c.pair && c.cs > 1 && share_mode() == 1 ? 1 : 0;
+  const int smem = smem_for(c.nt, xp, c.pair);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -756,9 +967,9 @@ cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtenso
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (p.multicast) {
+  if (p.multicast || c.pair) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = static_cast<unsigned>(c.cs);
+    attr[na].val.clusterDim.x = static_cast<unsigned>(c.pair ? 2 : c.cs);
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -766,10 +977,10 @@ cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = na;
   note_launch();
-  const CUtensorMap* x = &xmaps[box_index(p.x_box)];
+  const CUtensorMap* x = &xmaps[x_map_index(p.x_box)];
   e = cudaLaunchKernelEx(&cfg, k, *a0, *a1, *x, p);
   if (e != cudaSuccess || !p.defer_fixup) return e;
-  return launch_fixup(epi, p, c.grid / c.cs, stream);
+  return launch_fixup(epi, p, c.grid / (c.cs * (c.pair ? 2 : 1)), stream);
 }
 
 SDV_TRACE_UNIT(gemm_tc)

@@ -75,6 +75,9 @@ struct GemmParams {
   // cs > 1), the activation map's box height and the pipeline depth
   int nt = 0, cs = 1, n_groups = 0, x_box = 0, stages = 0;
   int multicast = 0;  // the cluster's CTAs share weight tiles by TMA multicast (else a group reads them via L2)
+  // tcgen05 kernels: CTA pairs (cta_group::2) -- a unit is 256 weight rows,
+  // 128 in each CTA, against the pair's nt activation rows, half loaded by each
+  int pair = 0;
   int* status = nullptr;
   EpiParams epi;
 };
@@ -118,10 +121,21 @@ cudaError_t trace_set_gemm_tc(unsigned long long* table);
 cudaError_t trace_set_gemm_tc_q4(unsigned long long* table);
 cudaError_t trace_set_step_kernels(unsigned long long* table);
 #endif
+// Activation tensor maps, one per TMA box height: the powers of two 8..256
+// (indices 0..5, the mma.sync and int4 kernels' tile heights) and the other
+// multiples of 16 up to 256, so that a tcgen05 CTA loads its activation rows
+// of a stage with one copy per plane.
+constexpr int kXMaps = 17;
+constexpr int kXBoxes[kXMaps] = {8, 16, 32, 64, 128, 256, 48, 80, 96, 112, 144, 160, 176, 192, 208, 224, 240};
+inline int x_map_index(int box) {
+  for (int i = 0; i < kXMaps; ++i)
+    if (kXBoxes[i] == box) return i;
+  return -1;
+}
 // bf16 weights on tcgen05: picks the activation tile height and the size of
 // the CTA groups that share each weight tile for p.R rows (measured choices,
 // see gemm_tc.cu), then launches the GEMM over the SMs and, for tiles cut
-// between CTAs, the fixup.  xmaps: the activation map for each box height 8..256.
+// between CTAs, the fixup.  xmaps: kXMaps activation maps (box heights kXBoxes).
 cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* xmaps,
                            GemmParams p, int sms, cudaStream_t stream);
 // Split fp32 x [n] into bf16 hi (at out) and lo (at out + lo_off) planes.
