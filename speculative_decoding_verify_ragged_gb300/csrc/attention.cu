@@ -457,66 +457,82 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p, con
   constexpr int DV = D / 4;
   griddep_launch_dependents();
   SDV_GRIDDEP_WAIT();
-  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= (long long)R * p.n_q * DV) return;
-  const int d4 = static_cast<int>(gid % DV);
-  const int rh = static_cast<int>(gid / DV);
-  const int r = rh / p.n_q, h = rh - (rh / p.n_q) * p.n_q;
-  // the status word is read alongside the row's slot (row_seq lies inside
-  // its table whatever the verdict; nothing else is read before the check)
+  // the status word and the prologue's split flag first: a step whose slots
+  // all fit one item per (slot, kv head) leaves nothing to merge
   const int st = read_status(p.status);
-  const int b = row_seq[r];
-  if (st != 0) return;
-  const int chunks = p.chunks[b];
-  if (chunks == 1) return;
+  const int split = p.sched[2];
+  if (st != 0 || split == 0) return;
   const int group = p.n_q / p.n_kv;
-  const int i = r - p.row_off[b];
-  const int g = h / group;
-  int v = i * group + (h - g * group);
-  // items split by query vectors: the part holding v, and v within it
-  int parts = 1, part = 0;
-  if (p.qsplit > 0) {
-    parts = ((p.draft_lens[b] + 1) * group + p.qsplit - 1) / p.qsplit;
-    part = v / p.qsplit;
-    v -= part * p.qsplit;
-  }
-  const long long item0 = p.item_off[b] + ((long long)g * parts + part) * chunks;
-  const float2* ml = p.part_ml + item0 * kAttnQMax + v;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + (item0 * kAttnQMax + v) * D) + d4;
-  constexpr long long kO4 = (long long)kAttnQMax * D / 4;  // float4 stride between chunks
-  float M = -INFINITY, L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < chunks; c0 += 8) {
-    float2 m[8];
-    float4 o[8];
+  const long long n = (long long)R * p.n_q * DV;
+  for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < n;
+       gid += (long long)gridDim.x * blockDim.x) {
+    const int d4 = static_cast<int>(gid % DV);
+    const int rh = static_cast<int>(gid / DV);
+    const int r = rh / p.n_q, h = rh - (rh / p.n_q) * p.n_q;
+    const int b = row_seq[r];
+    const int chunks = p.chunks[b];
+    if (chunks == 1) continue;
+    const int i = r - p.row_off[b];
+    const int g = h / group;
+    int v = i * group + (h - g * group);
+    // items split by query vectors: the part holding v, and v within it
+    int parts = 1, part = 0;
+    if (p.qsplit > 0) {
+      parts = ((p.draft_lens[b] + 1) * group + p.qsplit - 1) / p.qsplit;
+      part = v / p.qsplit;
+      v -= part * p.qsplit;
+    }
+    const long long item0 = p.item_off[b] + ((long long)g * parts + part) * chunks;
+    const float2* ml = p.part_ml + item0 * kAttnQMax + v;
+    const float4* po = reinterpret_cast<const float4*>(p.part_o + (item0 * kAttnQMax + v) * D) + d4;
+    constexpr long long kO4 = (long long)kAttnQMax * D / 4;  // float4 stride between chunks
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < chunks; c0 += 8) {
+      float2 m[8];
+      float4 o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (c0 + q < chunks) {
-        m[q] = ml[(long long)(c0 + q) * kAttnQMax];
-        o[q] = po[(long long)(c0 + q) * kO4];
+      for (int q = 0; q < 8; ++q) {
+        if (c0 + q < chunks) {
+          m[q] = ml[(long long)(c0 + q) * kAttnQMax];
+          o[q] = po[(long long)(c0 + q) * kO4];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (c0 + q < chunks && m[q].x != -INFINITY) {
+          const float nm = fmaxf(M, m[q].x);
+          const float a = M == -INFINITY ? 0.f : exp2f(M - nm);
+          const float w = exp2f(m[q].x - nm);
+          L = L * a + w * m[q].y;
+          acc.x = acc.x * a + w * o[q].x;
+          acc.y = acc.y * a + w * o[q].y;
+          acc.z = acc.z * a + w * o[q].z;
+          acc.w = acc.w * a + w * o[q].w;
+          M = nm;
+        }
       }
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (c0 + q < chunks && m[q].x != -INFINITY) {
-        const float nm = fmaxf(M, m[q].x);
-        const float a = M == -INFINITY ? 0.f : exp2f(M - nm);
-        const float w = exp2f(m[q].x - nm);
-        L = L * a + w * m[q].y;
-        acc.x = acc.x * a + w * o[q].x;
-        acc.y = acc.y * a + w * o[q].y;
-        acc.z = acc.z * a + w * o[q].z;
-        acc.w = acc.w * a + w * o[q].w;
-        M = nm;
-      }
-    }
+    const float inv = 1.f / L;
+    const long long base = ((long long)r * p.n_q + h) * D + d4 * 4;
+    store_planes(p.out, p.out_lo_off, base, acc.x * inv);
+    store_planes(p.out, p.out_lo_off, base + 1, acc.y * inv);
+    store_planes(p.out, p.out_lo_off, base + 2, acc.z * inv);
+    store_planes(p.out, p.out_lo_off, base + 3, acc.w * inv);
   }
-  const float inv = 1.f / L;
-  const long long base = ((long long)r * p.n_q + h) * D + d4 * 4;
-  store_planes(p.out, p.out_lo_off, base, acc.x * inv);
-  store_planes(p.out, p.out_lo_off, base + 1, acc.y * inv);
-  store_planes(p.out, p.out_lo_off, base + 2, acc.z * inv);
-  store_planes(p.out, p.out_lo_off, base + 3, acc.w * inv);
+}
+
+// The merge's grid: one thread per (row, query head, 4 dims), at most four
+// 256-thread blocks per SM (the rest by grid stride).
+dim3 merge_grid(int head_dim, int R, int n_q) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const long long n = (long long)R * n_q * (head_dim / 4);
+  long long blocks = (n + 255) / 256;
+  const long long cap = 4LL * sms;
+  if (cap > 0 && blocks > cap) blocks = cap;
+  return dim3(static_cast<unsigned>(blocks < 1 ? 1 : blocks));
 }
 
 template <int D>
@@ -527,9 +543,7 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
   if (e != cudaSuccess) return e;
   if ((e = launch_pdl(kern, dim3(grid), dim3(kThreads), ACfg<D>::SMEM, stream, *kv_map, p)) != cudaSuccess)
     return e;
-  const long long n = (long long)R * p.n_q * (D / 4);
-  return launch_pdl(attn_merge_kernel<D>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream, p,
-                    row_seq, R);
+  return launch_pdl(attn_merge_kernel<D>, merge_grid(D, R, p.n_q), dim3(256), 0, stream, p, row_seq, R);
 }
 
 }  // namespace
@@ -537,8 +551,7 @@ cudaError_t launch_d(const CUtensorMap* kv_map, const AttnParams& p, int grid, i
 size_t attention_smem_bytes(int head_dim) { return head_dim == 64 ? ACfg<64>::SMEM : ACfg<128>::SMEM; }
 
 cudaError_t launch_attention_merge(int head_dim, const AttnParams& p, int R, cudaStream_t stream, const int* row_seq) {
-  const long long n = (long long)R * p.n_q * (head_dim / 4);
-  const dim3 grid(static_cast<unsigned>((n + 255) / 256));
+  const dim3 grid = merge_grid(head_dim, R, p.n_q);
   if (head_dim == 128) return launch_pdl(attn_merge_kernel<128>, grid, dim3(256), 0, stream, p, row_seq, R);
   if (head_dim == 64) return launch_pdl(attn_merge_kernel<64>, grid, dim3(256), 0, stream, p, row_seq, R);
   return cudaErrorInvalidValue;

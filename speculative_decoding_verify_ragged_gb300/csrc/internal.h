@@ -157,7 +157,7 @@ struct AttnParams {
   int max_pages = 0;
   const int* item_off = nullptr;  // [B+1] first work item of each slot
   const int* chunks = nullptr;    // [B] key chunks per (slot, kv head)
-  const int* sched = nullptr;     // [0] chunk pages, [1] total items
+  const int* sched = nullptr;     // [0] chunk pages, [1] total items, [2] 1 if any slot's keys are split
   const int4* items = nullptr;    // [items, 2]: (slot, kv head, first page, end page), (L, gamma, row 0, chunks)
   float* part_o = nullptr;        // [items, QMAX, D]
   float2* part_ml = nullptr;      // [items, QMAX]

@@ -184,6 +184,8 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   // a whole item's pipeline fill)
   int chunks_b = slot ? (used + chunk - 1) / chunk : 0;
   if (chunks_b > 1 && used - (chunks_b - 1) * chunk <= chunk / 4) --chunks_b;
+  // whether any slot's keys are split (else the merge kernel has nothing to do)
+  const int any_split = __syncthreads_or(chunks_b > 1);
   // the slot's query vectors of one kv head, in items of at most qsplit
   const int nqv = (gam + 1) * (p.n_q / p.n_kv);
   const int halves = (slot && p.qsplit > 0) ? (nqv + p.qsplit - 1) / p.qsplit : 1;
@@ -226,6 +228,7 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
     p.t.item_off[p.B] = tot_items;
     p.t.sched[0] = chunk;
     p.t.sched[1] = tot_items;
+    p.t.sched[2] = any_split;
   }
   __syncthreads();
   if (b == 0 && s_err) set_status(p.status, s_err);
