@@ -1338,13 +1338,13 @@ static int sms_of_current_device() {
 }
 
 cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t stream) {
-  // sampling: about eight blocks per SM over the whole batch, two waves of
-  // what the kernel's registers let an SM hold, so that the blocks of slots
-  // whose rows need both weight kinds even out across SMs; never more blocks
-  // per slot than its vocabulary has chunks for (one warp per chunk)
+  // sampling: about four blocks per SM over the whole batch (what the
+  // kernel's registers let an SM hold: one wave; eight and sixteen measured
+  // slower, each block merging its slot's row statistics again), never more
+  // blocks per slot than its vocabulary has chunks for (one warp per chunk)
   const int nch = (p.V + kVChunk - 1) / kVChunk;
   const int max_per_slot = (nch + kAccWarps - 1) / kAccWarps;
-  const int want = (8 * sms_of_current_device() + p.B - 1) / p.B;
+  const int want = (4 * sms_of_current_device() + p.B - 1) / p.B;
   const dim3 grid(want < 1 ? 1 : (want > max_per_slot ? max_per_slot : want), p.B);
   cudaError_t e;
   if (from_logits) {
