@@ -1344,7 +1344,7 @@ cudaError_t launch_accept(const AcceptParams& p, bool from_logits, cudaStream_t 
   // blocks per slot than its vocabulary has chunks for (one warp per chunk)
   const int nch = (p.V + kVChunk - 1) / kVChunk;
   const int max_per_slot = (nch + kAccWarps - 1) / kAccWarps;
-  const int want = (4 * sms_of_current_device() + p.B - 1) / p.B;
+  const int want = 4 * sms_of_current_device() / p.B;  // rounded down: a second wave costs a block's time
   const dim3 grid(want < 1 ? 1 : (want > max_per_slot ? max_per_slot : want), p.B);
   cudaError_t e;
   if (from_logits) {
