@@ -54,10 +54,12 @@ __device__ __forceinline__ int cta_of_unit(long long u, long long total, int P) 
 //
 // SWIGLU with an RMSNorm row scale: `row_scale`, when given, holds each row's
 // 1 / rms already reduced from the partial sums (row_scale[r - rs_base] for
-// row r); otherwise each chunk reduces them itself.
+// row r); otherwise each chunk reduces them itself.  `bar`: the named barrier
+// of the 128 calling threads.
 template <int EPI, int LD>
 __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, int tm, int row0, int nrows,
-                                              int tid, const float* row_scale = nullptr, int rs_base = 0) {
+                                              int tid, const float* row_scale = nullptr, int rs_base = 0,
+                                              int bar = 1) {
   const EpiParams& e = p.epi;
   constexpr int RB = 16;  // rows per batch
   if constexpr (EPI == EPI_RESID) {
@@ -122,7 +124,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, i
     const int f = tm * 64 + j;
     if (e.sq_in && row_scale) {
       for (int n = tid; n < nrows; n += 4 * kWarp) epi[n * LD + BM] = row_scale[row0 + n - rs_base];
-      named_sync(1, 4 * kWarp);
+      named_sync(bar, 4 * kWarp);
     } else if (e.sq_in) {
       // the input was x * gain: each row's 1 / rms(x) from the partial sums of x^2
       const int warp = tid >> 5, lane = tid & 31;
@@ -132,7 +134,7 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, float* epi, i
         ss = warp_sum(ss);
         if (lane == 0) epi[n * LD + BM] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
       }
-      named_sync(1, 4 * kWarp);
+      named_sync(bar, 4 * kWarp);
     }
     if (f < p.N) {
       for (int n = tid >> 6; n < nrows; n += 2) {

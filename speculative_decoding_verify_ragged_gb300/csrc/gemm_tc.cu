@@ -36,16 +36,18 @@
 // that box height exists for every multiple of 16 up to 256): copies of 16 or
 // 32 rows measured as much as a third slower than the MMAs they feed.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //  * warp 0: TMA producer (one lane) -- weight half-tiles and activation planes
 //    into a multi-stage ring; weights are streamed before waiting for the
 //    kernel that writes the activations;
 //  * warp 1: allocates 2 x NT columns of tensor memory (two accumulators) and
 //    one lane issues the MMAs; tcgen05.commit frees each stage when its MMAs
 //    complete and signals each finished accumulator;
-//  * warps 2-5: epilogue -- tcgen05.ld the accumulator (lane = weight row),
-//    then the stream-K partial/fixup and the fused epilogue shared with the
-//    mma.sync kernel, while the MMAs fill the other accumulator.
+//  * warps 2-9: epilogue, two groups of four taking alternate 16-column
+//    chunks -- tcgen05.ld the accumulator (lane = weight row), then the
+//    stream-K partial/fixup and the fused epilogue shared with the mma.sync
+//    kernel, while the MMAs fill the other accumulator.  (With one group the
+//    LM head's epilogue took about as long per tile as the tile's MMAs.)
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -59,7 +61,7 @@ namespace {
 
 using namespace gemm;
 using namespace tc;
-constexpr int TC_THREADS = 6 * kWarp;
+constexpr int TC_THREADS = 10 * kWarp;
 constexpr int EC = 16;           // accumulator columns per tcgen05.ld / epilogue chunk
 constexpr int kMaxStages = 10;
 constexpr int kMaxCluster = 8;   // portable cluster size
@@ -68,9 +70,9 @@ constexpr int kMaxCluster = 8;   // portable cluster size
 constexpr int EPI_LD = BM + 8;
 constexpr int EPI_BYTES = EC * EPI_LD * 4;
 constexpr int kScaleRows = 256;  // rows of the per-CTA RMSNorm row-scale cache (gate/up)
-// alignment slack + epilogue staging + barriers (full, empty, 2 x 2 accumulator) + TMEM slot and flag +
-// the row-scale cache
-constexpr int FIXED_BYTES = 1024 + EPI_BYTES + (2 * kMaxStages + 4) * 8 + 16 + kScaleRows * 4;
+// alignment slack + epilogue staging (one buffer per epilogue group) + barriers (full, empty, 2 x 2
+// accumulator) + TMEM slot and flag + the row-scale cache
+constexpr int FIXED_BYTES = 1024 + 2 * EPI_BYTES + (2 * kMaxStages + 4) * 8 + 16 + kScaleRows * 4;
 
 // Bytes of one ring stage in one CTA: the CTA's 128 weight rows and its
 // activation rows (all nt of them, or half in a CTA pair) per plane.
@@ -204,8 +206,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int STAGE = tc_stage_bytes(NT, XP, PAIR);
   const int NTC = PAIR ? NT / 2 : NT;  // activation rows this CTA loads per stage
   uint8_t* smem = align1024(smem_raw);
-  float* epi = reinterpret_cast<float*>(smem + S * STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + EPI_BYTES);
+  float* epi = reinterpret_cast<float*>(smem + S * STAGE);  // [2 groups][EPI_BYTES]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE + 2 * EPI_BYTES);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;  // [2] accumulator ready
   uint64_t* tempty = tfull + 2;          // [2] accumulator drained
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(&tfull[b], 1);
       // one arrival per epilogue warp (of both CTAs of a pair: the issuer's
       // barrier is the one that counts)
-      mbar_init(&tempty[b], PAIR ? 8 : 4);
+      mbar_init(&tempty[b], PAIR ? 16 : 8);
     }
     fence_barrier_init();
   }
@@ -451,54 +453,62 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5 ----------------
+    // ---------------- epilogue warps 2..9 ----------------
+    // two groups of four (warps 2-5 and 6-9), each covering the 128 TMEM lanes
+    // (a warp reaches lanes 32 * (warp % 4) .. +31) and taking alternate
+    // 16-column chunks of every accumulator, with its own staging buffer and
+    // named barrier, so that one group's loads and stores overlap the other's
+    const int eg = (warp - 2) >> 2;
+    const int ebar = 1 + eg;
+    float* epi_g = epi + eg * (EPI_BYTES / 4);
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int m = quarter * 32 + lane;     // weight row within the tile
     SDV_GRIDDEP_WAIT();
     // gate/up after the FFN pre-norm: every row's 1 / rms, reduced once from
     // the O projection's partial sums of x^2 (lanes over rows, so each load
-    // is one coalesced line; the four warps take every fourth partial and
-    // meet in a fixed order) while the first tile's MMAs run; the rows are
-    // this CTA's activation tile (or all rows, when one CTA walks several
-    // tiles of at most kScaleRows rows in total)
+    // is one coalesced line; the first group's four warps take every fourth
+    // partial and meet in a fixed order) while the first tile's MMAs run; the
+    // rows are this CTA's activation tile (or all rows, when one CTA walks
+    // several tiles of at most kScaleRows rows in total)
     int rs_base = 0;
     bool have_scale = false;
     if constexpr (EPI == EPI_SWIGLU) {
+      int nrs = 0;
       if (p.epi.sq_in && read_status(p.status) == 0) {
-        int nrs = 0;
         if (p.n_groups == 1) {
           rs_base = rank * NT;
           nrs = min(NT, p.R - rs_base);
         } else if (p.R <= kScaleRows) {
           nrs = p.R;
         }
-        have_scale = nrs > 0;
-        const EpiParams& e = p.epi;
-        for (int rb = 0; rb < nrs; rb += kWarp) {
-          const int r = rb + lane;
-          float acc = 0.f;
-          if (r < nrs) {
-            constexpr int U = 8;
-            for (int q0 = quarter; q0 < e.sq_parts; q0 += 4 * U) {
-              float w[U];
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                const int qq = q0 + 4 * u;
-                w[u] = qq < e.sq_parts ? e.sq_in[(long long)qq * e.sq_ld + rs_base + r] : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < U; ++u) acc += w[u];
-            }
-          }
-          epi[quarter * kWarp + lane] = acc;
-          named_sync(1, 4 * kWarp);
-          if (quarter == 0 && r < nrs) {
-            const float ss = ((epi[lane] + epi[kWarp + lane]) + epi[2 * kWarp + lane]) + epi[3 * kWarp + lane];
-            row_scale[r] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
-          }
-          named_sync(1, 4 * kWarp);
-        }
       }
+      have_scale = nrs > 0;
+      const EpiParams& e = p.epi;
+      for (int rb = 0; eg == 0 && rb < nrs; rb += kWarp) {
+        const int r = rb + lane;
+        float acc = 0.f;
+        if (r < nrs) {
+          constexpr int U = 8;
+          for (int q0 = quarter; q0 < e.sq_parts; q0 += 4 * U) {
+            float w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int qq = q0 + 4 * u;
+              w[u] = qq < e.sq_parts ? e.sq_in[(long long)qq * e.sq_ld + rs_base + r] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc += w[u];
+          }
+        }
+        epi[quarter * kWarp + lane] = acc;
+        named_sync(1, 4 * kWarp);
+        if (quarter == 0 && r < nrs) {
+          const float ss = ((epi[lane] + epi[kWarp + lane]) + epi[2 * kWarp + lane]) + epi[3 * kWarp + lane];
+          row_scale[r] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
+        }
+        named_sync(1, 4 * kWarp);
+      }
+      named_sync(3, 8 * kWarp);  // the scales are ready for both groups
     }
     const float* rs = have_scale ? row_scale : nullptr;
     if (read_status(p.status) == 0) {
@@ -537,34 +547,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // the second half of a pair past the last weight tile: nothing to store
           release();
         } else if (k0 == 0 && k1 == p.kb) {
-          // whole tile in this CTA: epilogue straight from tensor memory
-          for (int c0 = 0; c0 < cols; c0 += EC) {
+          // whole tile in this CTA: epilogue straight from tensor memory, this
+          // group's chunks eg, eg + 2, ...; a warp releases the accumulator
+          // after its last read of it
+          bool released = false;
+          for (int c0 = eg * EC; c0 < cols; c0 += 2 * EC) {
             float v[16];
             tmem_ld16(t_row + c0, v);
-            if (c0 + EC == cols) release();
+            if (c0 + 2 * EC >= cols) {
+              release();
+              released = true;
+            }
 #pragma unroll
-            for (int n = 0; n < EC; ++n) epi[n * LD + m] = v[n];
-            named_sync(1, 4 * kWarp);
-            epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(EC, rows - c0), m, rs, rs_base);
-            named_sync(1, 4 * kWarp);
+            for (int n = 0; n < EC; ++n) epi_g[n * LD + m] = v[n];
+            named_sync(ebar, 4 * kWarp);
+            epilogue_rows<EPI, LD>(p, epi_g, tm, tn * NT + c0, min(EC, rows - c0), m, rs, rs_base, ebar);
+            named_sync(ebar, 4 * kWarp);
           }
+          if (!released) release();
         } else {
           // tile cut between clusters: store this piece, the fixup sums them in cluster order
           const int my_slot = 2 * ((q * cs + rank) * (PAIR ? 2 : 1) + half) + (tg == first_tg ? 0 : 1);
           float* mine = p.partials + (size_t)my_slot * BM * NT;
-          for (int c0 = 0; c0 < cols; c0 += EC) {
+          for (int c0 = eg * EC; c0 < cols; c0 += 2 * EC) {
             float v[16];
             tmem_ld16(t_row + c0, v);
             tc_store_part16(mine, c0, m, v);
           }
           release();
           if (!PAIR && !p.defer_fixup) {
-            // one CTA per cluster (cs == 1): the last CTA to arrive sums the parts in CTA order
+            // one CTA per cluster (cs == 1): the last CTA to arrive sums the
+            // parts in CTA order (the first group, once both have stored)
+            __threadfence();
+            named_sync(3, 8 * kWarp);
+          }
+          if (!PAIR && !p.defer_fixup && eg == 0) {
             const long long tu = (long long)tg * p.kb;
             const int c_first = cta_of_unit(tu, total, Q);
             const int c_last = cta_of_unit(tu + p.kb - 1, total, Q);
-            __threadfence();
-            named_sync(1, 4 * kWarp);
             if (m == 0) {
               const int old = atomicAdd(&p.counters[tile], 1);
               *flag = (old == c_last - c_first) ? 1 : 0;
