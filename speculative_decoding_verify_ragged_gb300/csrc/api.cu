@@ -45,7 +45,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Layout {
   size_t row_off, draft_off, row_seq, row_pos, row_anc, tree_path, chunks, item_off, sched, items, rope, kv_row_off,
       inv_freq;
-  size_t x0, h, h3, q, attn, x1, x1sq, act, x2, z, lmstats, lmargmax, rowstats, partials, counters;
+  size_t x0, h, h3, q, attn, x1, x1sq, rscale, act, x2, z, lmstats, lmargmax, rowstats, partials, counters;
   size_t part_o, part_ml, accepted, final_tokens, chunk_count, chunk_sums, total;
   int chunk_ld;
   int lm_tiles, max_tiles, target_items, items_max, grid_gemm;
@@ -125,6 +125,7 @@ static Layout make_layout(const sdv_config& c, int max_rows, int max_slots, int 
   L.attn = take(2 * R * QD * 2);
   L.x1 = take(R * H * 4);
   L.x1sq = take(static_cast<size_t>(H / 32) * R * 4);  // per-32-column partial sums of x1^2
+  L.rscale = take(R * 4);                                // the FFN pre-norm's 1 / rms per row
   L.act = take(2 * R * (F > QD ? (F > H ? F : H) : (QD > H ? QD : H)) * 2);
   L.x2 = take(R * H * 4);
   L.z = take(R * V * 4);
@@ -723,6 +724,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
     g.epi.sq_ld = c->max_rows;
     g.epi.sq_inv_n = 1.0f / static_cast<float>(H);
     g.epi.sq_eps = cf.rms_eps;
+    g.epi.rscale = cf.weight_format == SDV_WEIGHTS_BF16 ? f32(c->L.rscale) : nullptr;
     g.epi.out_bf16 = ws_ptr<__nv_bfloat16>(c, c->L.act);
     g.epi.out_lo_off = (long long)c->max_rows * F;
     g.epi.ld_bf16 = F;

@@ -504,7 +504,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         named_sync(1, 4 * kWarp);
         if (quarter == 0 && r < nrs) {
           const float ss = ((epi[lane] + epi[kWarp + lane]) + epi[2 * kWarp + lane]) + epi[3 * kWarp + lane];
-          row_scale[r] = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
+          const float sc = 1.0f / sqrtf(ss * e.sq_inv_n + e.sq_eps);
+          row_scale[r] = sc;
+          // the fixup kernel reads them back (every CTA of a group writes the same values)
+          if (e.rscale) e.rscale[rs_base + r] = sc;
         }
         named_sync(1, 4 * kWarp);
       }
@@ -681,7 +684,9 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
 #pragma unroll
   for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
   __syncthreads();
-  epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(16, rows - c0), m);
+  // SWIGLU: the rows' 1 / rms as the main kernel reduced them, when it published them
+  const float* rs = EPI == EPI_SWIGLU && p.epi.rscale ? p.epi.rscale : nullptr;
+  epilogue_rows<EPI, LD>(p, epi, tm, tn * NT + c0, min(16, rows - c0), m, rs, 0);
 }
 
 template <int EPI>
@@ -967,6 +972,9 @@ cudaError_t launch_gemm_tc(int epi, int xp, const CUtensorMap* a0, const CUtenso
   p.n_tiles = c.n_tiles;
   p.n_groups = c.n_groups;
   p.pair = c.pair ? 1 : 0;
+  // the kernel reduces the rows' RMSNorm scales once (and publishes them for
+  // its fixup) only for rows it can hold; otherwise each chunk reduces them
+  if (!(c.n_groups == 1 || p.R <= kScaleRows)) p.epi.rscale = nullptr;
   // a pair's CTA loads half the activation tile
   p.x_box = box_for(c.pair ? c.nt / 2 : c.nt);
   p.stages = tc_stages(c.nt, xp, c.pair);

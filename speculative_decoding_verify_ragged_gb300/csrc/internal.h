@@ -39,6 +39,9 @@ struct EpiParams {
   const float* sq_in = nullptr;
   int sq_parts = 0;
   float sq_inv_n = 0.f, sq_eps = 0.f;
+  // tcgen05 bf16 GEMM: each row's 1 / rms as the main kernel reduced it, [R],
+  // written there and read by its fixup kernel (null: the fixup reduces them)
+  float* rscale = nullptr;
   // QKV
   __nv_bfloat16* kv_pool = nullptr;
   const int* page_table = nullptr;
