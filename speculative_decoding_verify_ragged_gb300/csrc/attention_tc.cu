@@ -11,8 +11,8 @@
 // the 16-32 query vectors of an item cannot keep up, so here:
 //
 //  * a KV block is 8 pages = 128 keys; two TMA producer warps land its K and
-//    its V (key rows, 128-byte swizzle) in separate rings, K two blocks deep
-//    (a slot frees as soon as its QK^T is done), V three or four;
+//    its V (key rows, 128-byte swizzle) in separate rings, three blocks each
+//    with 16 query vectors per item (two K and three V with 32);
 //  * one thread issues S^T = K Q^T as tcgen05.mma with M = 128 keys and
 //    N = twice the item's query vectors (16 or 32): q's bf16 hi rows and lo
 //    rows side by side, so each K tile is read once; the softmax adds the two
@@ -54,9 +54,12 @@ constexpr float kLazy = 8.f;                 // log2 headroom of the lazily move
 template <int NQ>
 struct TaCfg {
   // K and V rings, in blocks: a K slot is free once its QK^T is done, a V slot
-  // only after the block's softmax and PV, so the V ring is the deeper one
-  static constexpr int KS = 2;
-  static constexpr int VS = NQ == 16 ? 4 : 3;
+  // only after the block's softmax and PV.  Per-role cycle counters showed
+  // the softmax warps waiting on QK^T 43 % of the time and the MMA thread on
+  // K data: with 16 query vectors three blocks each (R = 512 attention
+  // 225 -> 213 us; two K and four V, or four K and two V, were slower)
+  static constexpr int KS = NQ == 16 ? 3 : 2;
+  static constexpr int VS = 3;
   static constexpr int OFF_V = KS * STAGE_BYTES;
   // Q and P are B operands of 2 NQ rows: the NQ hi rows, then the NQ lo rows
   static constexpr int Q_HALF = 2 * NQ * 128;    // one 64-dim half of the 2 NQ Q rows
