@@ -546,6 +546,15 @@ static AttnPlan attn_plan(const sdv_ctx* c, int B) {
   return a;
 }
 
+// The smallest chunk of pages per attention item.  Items cover about four per
+// SM where the batch has the keys for it; below that, the tcgen05 kernel pays
+// a whole pipeline fill, epilogue and merge share per item, so its items take
+// at least 32 pages (four 128-key blocks), while the mma.sync kernel's small
+// batches keep 8-page items (measured, 9B-class layer, ctx 2048: B = 4,
+// gamma 7 attention 47 -> 27 us, B = 8 gamma 3 40 -> 35 us on tcgen05; B = 1 on
+// mma.sync 20 -> 22 us with 16 pages, 29 with 32).
+static int attn_min_chunk(const AttnPlan& plan) { return plan.tc ? 32 : 8; }
+
 static sdv_status run_attention(sdv_ctx* c, const sdv_batch* b, const float* q, __nv_bfloat16* out,
                                 long long out_lo_off, int* status, cudaStream_t s) {
   CUtensorMap kv;
@@ -668,6 +677,7 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   SDV_CUDA(mark(SDV_PHASE_PROLOGUE));
   PrologueParams pp = prologue_params(c, b, status, true);
   pp.qsplit = plan.qsplit;
+  pp.min_chunk = attn_min_chunk(plan);
   pp.emb = static_cast<const __nv_bfloat16*>(c->w.emb);
   pp.gain = static_cast<const __nv_bfloat16*>(c->w.g_attn);
   pp.x0 = f32(c->L.x0);
@@ -897,6 +907,7 @@ sdv_status sdv_attention(sdv_ctx* c, const void* q, const sdv_batch* b, void* ou
   if (plan.st != SDV_OK) return plan.st;
   PrologueParams pp = prologue_params(c, b, status, false);
   pp.qsplit = plan.qsplit;
+  pp.min_chunk = attn_min_chunk(plan);
   SDV_CUDA(launch_prologue(pp, s));
   // the kernel writes bf16 hi + lo planes; a plain fp32 result is their sum,
   // so stage the planes in the workspace and add them into `out`

@@ -214,8 +214,9 @@ struct PrologueParams {
   int n_kv = 0, head_dim = 0, target_items = 0;
   float rope_theta = 0.f;
   int check_tokens = 1;
-  // attention work items: query vectors per item (0: no split) and query heads
-  int qsplit = 0, n_q = 0;
+  // attention work items: query vectors per item (0: no split) and query heads;
+  // the smallest chunk of pages an item takes (a multiple of 8)
+  int qsplit = 0, n_q = 0, min_chunk = 8;
   // test hook (0 = off): block 0 waits this long on a barrier nothing arrives
   // at, through the bounded wait the pipelined kernels use, and records
   // SDV_ERR_TIMEOUT when it gives up

@@ -178,7 +178,7 @@ __device__ void validate_and_tables(const PrologueParams& p, int* s_warp, int* s
   // attention schedule: chunks of pages sized so that items cover the GPU
   const long long units = (long long)tot_pages * p.n_kv;
   int chunk = static_cast<int>((units + p.target_items - 1) / p.target_items);
-  chunk = (max(chunk, 8) + 7) & ~7;  // whole 128-key blocks
+  chunk = (max(chunk, p.min_chunk) + 7) & ~7;  // whole 128-key blocks
   // a sequence's pages in chunks of `chunk`; a remainder of at most a quarter
   // chunk joins the last whole chunk (an item of a few leftover pages would pay
   // a whole item's pipeline fill)
