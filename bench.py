@@ -70,6 +70,8 @@ def parse():
                          + ",".join(f"{b}:{g}" for b, g in CURVE_POINTS) + "); the headline is 128:3 when listed, "
                          "else the last point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps one by one instead of replaying them as one captured CUDA graph")
     ap.add_argument("--quick", action="store_true",
                     help="profiling run: no clock pre-roll, no e2e or CPU legs (its numbers are not bench values)")
     ap.add_argument("--sweep", action="store_true",
@@ -385,10 +387,10 @@ class Bench:
         # one emitted-offsets row per step, so the token count is read after the timed region
         EO = torch.zeros((nsteps, batch.B + 1), dtype=torch.int32, device="cuda")
 
-        def step(i):
+        def step(i, s=None):
             bd["uniforms"] = U[i]
             res["emitted_offsets"] = EO[i]
-            eng.verify_step(bd, res, stream)
+            eng.verify_step(bd, res, stream if s is None else s)
 
         for i in range(args.warmup):
             step(i)
@@ -413,14 +415,41 @@ class Bench:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         launches0 = kernel_launches()
+
+        def timed_steps(s):
+            for j, i in enumerate(range(args.warmup, nsteps)):
+                evs = [None] * (len(PHASES) + 1)
+                evs[K_LM], evs[K_LM + 1] = lm_pairs[j]
+                eng.set_phase_events(evs)
+                step(i, s)
+            eng.set_phase_events(None)
+
+        # the K timed steps captured once as a CUDA graph (programmatic dependent
+        # launches and the LM-head event pairs included) and launched once, so a
+        # stall of the launching host thread cannot leave the GPU idle inside the
+        # timed region; the steps do the same work as launched one by one
+        graph = None
+        if not args.no_graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream()
+                cap.wait_stream(stream)
+                with torch.cuda.graph(g, stream=cap):
+                    timed_steps(cap)
+                stream.wait_stream(cap)
+                graph = g
+            except Exception as e:  # a driver without capture of these launches: one by one
+                print(f"bench.py: graph capture failed ({e}); timing launches one by one", file=sys.stderr)
+                eng.set_phase_events(None)
+                torch.cuda.synchronize()
+                graph = None
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for j, i in enumerate(range(args.warmup, nsteps)):
-            evs = [None] * (len(PHASES) + 1)
-            evs[K_LM], evs[K_LM + 1] = lm_pairs[j]
-            eng.set_phase_events(evs)
-            step(i)
+        if graph is not None:
+            graph.replay()
+        else:
+            timed_steps(stream)
         t1.record(stream)
         torch.cuda.synchronize()
         launches = kernel_launches() - launches0

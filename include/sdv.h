@@ -284,7 +284,8 @@ enum {
  * boundary: an event recorded between two kernels stops the second from
  * starting while the first finishes, so record only the boundaries you read.
  * events = NULL (n = 0) turns timing off.  The context keeps the handles,
- * not ownership. */
+ * not ownership.  A call recorded into a CUDA graph (stream capture) records
+ * the events as external event nodes, so they time the graph's runs. */
 sdv_status sdv_set_phase_events(sdv_ctx *ctx, void *const *events, int n);
 
 /* Which kernel runs the context's GEMMs: SDV_GEMM_AUTO (by row count),

@@ -671,8 +671,14 @@ sdv_status sdv_verify_step(sdv_ctx* c, const sdv_batch* b, sdv_result* r, void* 
   const int NQKV = (cf.n_q + 2 * cf.n_kv) * D;
   int* status = r->status;
   auto f32 = [&](size_t off) { return ws_ptr<float>(c, off); };
+  // inside a stream capture the marks become graph nodes that record their
+  // timestamps when the graph runs (external event records)
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (c->timing && cudaStreamIsCapturing(s, &capture) != cudaSuccess) capture = cudaStreamCaptureStatusNone;
   auto mark = [&](int k) -> cudaError_t {
-    return c->timing && c->phase_ev[k] ? cudaEventRecord(c->phase_ev[k], s) : cudaSuccess;
+    if (!c->timing || !c->phase_ev[k]) return cudaSuccess;
+    return capture == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(c->phase_ev[k], s, cudaEventRecordExternal)
+                                                    : cudaEventRecord(c->phase_ev[k], s);
   };
 
   const AttnPlan plan = attn_plan(c, b->B);
