@@ -634,8 +634,8 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
   constexpr int LD = EPI_LD;
   __shared__ float epi[16 * LD];
   griddep_launch_dependents();
-  SDV_GRIDDEP_WAIT();
-  if (read_status(p.status) != 0) return;
+  // which chunk of which cut tile, from the launch's parameters alone: blocks
+  // with nothing to do leave before the wait for the GEMM
   const int NT = p.nt, cs = p.cs;
   const int H = p.pair ? 2 : 1;  // 128-row weight tiles per unit
   const long long total = (long long)((p.m_tiles + H - 1) / H) * p.n_groups * p.kb;
@@ -659,6 +659,10 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
   const int m = threadIdx.x;
   const int q_first = cluster_of_unit(t0, total, Q);
   const int q_last = cluster_of_unit(t0 + p.kb - 1, total, Q);
+  SDV_GRIDDEP_WAIT();
+  // the parts (inside the partials buffer whatever the verdict) and the
+  // status word in the same round trip
+  const int st = read_status(p.status);
   float v[16];
 #pragma unroll
   for (int n = 0; n < 16; ++n) v[n] = 0.f;
@@ -681,6 +685,7 @@ __global__ void __launch_bounds__(128, 8) gemm_tc_fixup_kernel(const GemmParams 
         for (int n = 0; n < 16; ++n) v[n] += w[i][n];
       }
   }
+  if (st != 0) return;
 #pragma unroll
   for (int n = 0; n < 16; ++n) epi[n * LD + m] = v[n];
   __syncthreads();
