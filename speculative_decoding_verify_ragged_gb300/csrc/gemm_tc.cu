@@ -856,7 +856,11 @@ TcChoice choose_pair(int epi, int xp, const GemmParams& g, int sms, int forced_c
   // (groups of n pairs), smallest
   const int n0 = (R + 255) / 256;
   double best = 0.0;
-  for (int n = n0; n <= n0 + 2; ++n) {
+  // one activation plane (the LM head): the fewest tiles, 256 rows where they
+  // fill (1152 rows: 5 tiles of 256 in groups of 5 pairs, 1065 -> 955 us
+  // against 6 tiles of 192); two planes: the estimate below
+  const int n_last = xp == 1 ? n0 : n0 + 2;
+  for (int n = n0; n <= n_last; ++n) {
     const int nt = round_up((R + n - 1) / n, 32);
     if (nt > 256) continue;
     const int tiles = (R + nt - 1) / nt;
