@@ -316,7 +316,8 @@ sdv_status sdv_set_sampling(sdv_ctx *ctx, int mode);
  * head_dim is 128 and the batch has at least 4 sequences, or whenever
  * (gamma_max + 1) * n_q / n_kv exceeds 48; else mma.sync), SDV_GEMM_MMA_SYNC
  * (up to 48 query vectors per sequence and kv head), or SDV_GEMM_TCGEN05
- * (head_dim 128, up to 64 query vectors, taken 32 per work item).  A shape
+ * (head_dim 128, up to 64 query vectors: up to 48 in one work item, past
+ * 48 taken 32 per work item).  A shape
  * the chosen kernel does not take is SDV_ERR_UNSUPPORTED from the step and
  * sdv_attention, before anything is enqueued.  Results agree up to fp32
  * summation order.  Host-side setting; takes effect on the next call. */

@@ -177,7 +177,7 @@ class VerifyEngine:
 
     def set_attention_path(self, path: int):
         """0 auto, 1 mma.sync (<= 48 query vectors per sequence and kv head), 2 tcgen05
-        (head_dim 128, <= 64 query vectors, 32 per work item)."""
+        (head_dim 128, <= 64 query vectors: <= 48 in one work item, 32 per item past 48)."""
         self._check(self.lib.sdv_set_attention_path(self.handle, int(path)), "sdv_set_attention_path")
 
     def set_stall_test(self, stall_ns: int):

@@ -524,10 +524,10 @@ static cudaError_t run_gemm(sdv_ctx* c, int epi, int xp, const CUtensorMap* a0, 
 
 // Which attention kernel a batch takes and how its work items split the query
 // vectors.  The tcgen05 kernel takes head_dim 128 with up to 64 query vectors
-// per (sequence, kv head) -- past 32 in items of 32, two items per chunk of
-// pages, adjacent so that the second reads the pages from L2 -- and in auto
-// mode from kTcAttnSlots sequences up, or whenever the mma.sync kernel's 48
-// vectors would not hold them.
+// per (sequence, kv head) -- up to 48 in one item, past 48 in items of 32, two
+// items per chunk of pages, adjacent so that the second reads the pages from
+// L2 -- and in auto mode from kTcAttnSlots sequences up, or whenever the
+// mma.sync kernel's 48 vectors would not hold them.
 struct AttnPlan {
   sdv_status st = SDV_OK;
   bool tc = false;
@@ -543,8 +543,8 @@ static AttnPlan attn_plan(const sdv_ctx* c, int B) {
                   (c->attn_path == SDV_GEMM_AUTO && (B >= kTcAttnSlots || nqv_max > kAttnQMax)));
   if (!a.tc && nqv_max > kAttnQMax) a.st = SDV_ERR_UNSUPPORTED;
   if (a.tc) {
-    a.qsplit = nqv_max > 32 ? 32 : 0;
-    a.nq = (a.qsplit || nqv_max > 16) ? 32 : 16;
+    a.qsplit = nqv_max > 48 ? 32 : 0;
+    a.nq = a.qsplit ? 32 : (nqv_max > 32 ? 48 : (nqv_max > 16 ? 32 : 16));
   }
   return a;
 }

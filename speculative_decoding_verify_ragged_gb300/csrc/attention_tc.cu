@@ -1,5 +1,5 @@
 // Block-causal GQA attention on the 5th-generation tensor cores (head_dim 128,
-// up to 32 query vectors per work item; a (sequence, KV head) with more --
+// up to 48 query vectors per work item; a (sequence, KV head) with more --
 // up to 64 -- comes as adjacent items of 32 from its first vector v0).
 //
 // Same work items, masking and outputs as the mma.sync kernel (attention.cu):
@@ -12,9 +12,10 @@
 //
 //  * a KV block is 8 pages = 128 keys; two TMA producer warps land its K and
 //    its V (key rows, 128-byte swizzle) in separate rings, three blocks each
-//    with 16 query vectors per item (two K and three V with 32);
+//    with 16 query vectors per item (two K and three V with 32, two each with
+//    48, where the Q and P buffers take the rest of shared memory);
 //  * one thread issues S^T = K Q^T as tcgen05.mma with M = 128 keys and
-//    N = twice the item's query vectors (16 or 32): q's bf16 hi rows and lo
+//    N = twice the item's query vectors (16, 32 or 48): q's bf16 hi rows and lo
 //    rows side by side, so each K tile is read once; the softmax adds the two
 //    column halves (S double-buffered across blocks);
 //  * eight softmax warps own the 128 key lanes, in two groups of four that each
@@ -59,7 +60,7 @@ struct TaCfg {
   // K data: with 16 query vectors three blocks each (R = 512 attention
   // 225 -> 213 us; two K and four V, or four K and two V, were slower)
   static constexpr int KS = NQ == 16 ? 3 : 2;
-  static constexpr int VS = 3;
+  static constexpr int VS = NQ == 48 ? 2 : 3;
   static constexpr int OFF_V = KS * STAGE_BYTES;
   // Q and P are B operands of 2 NQ rows: the NQ hi rows, then the NQ lo rows
   static constexpr int Q_HALF = 2 * NQ * 128;    // one 64-dim half of the 2 NQ Q rows
@@ -75,9 +76,10 @@ struct TaCfg {
   static constexpr int NBAR = 2 * KS + 2 * VS + 2 * 2 + 2 * 2 + 2 * 2 + 2;  // k, v, s(2), p(2), q(2), o (full + empty)
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   // S0, S1 and O, each 2 NQ columns (hi part, lo part)
-  static constexpr int TMEM_COLS = 6 * NQ <= 32 ? 32 : (6 * NQ <= 64 ? 64 : (6 * NQ <= 128 ? 128 : 256));
+  static constexpr int TMEM_COLS =
+      6 * NQ <= 32 ? 32 : (6 * NQ <= 64 ? 64 : (6 * NQ <= 128 ? 128 : (6 * NQ <= 256 ? 256 : 512)));
   static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(NQ == 16 || NQ == 32, "query vectors per item");
+  static_assert(NQ == 16 || NQ == 32 || NQ == 48, "query vectors per item");
 };
 
 // Shared-memory descriptor of a 128-byte-swizzled operand given its two
@@ -91,20 +93,6 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo, 
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
-}
-
-// 32 lanes x 16 columns from registers into tensor memory (one lane per thread).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
-      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
-      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
@@ -391,12 +379,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
     };
     auto ld_cols = [&](uint32_t taddr, float (&v)[NH]) {
-      if constexpr (NH == 16) {
+      if constexpr (NH == 24) {
+        float a[16], c[8];
+        tmem_ld16(taddr, a);
+        tmem_ld8(taddr + 16, c);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = a[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[16 + j] = c[j];
+      } else if constexpr (NH == 16) {
         tmem_ld16(taddr, v);
       } else {
         tmem_ld8(taddr, v);
       }
     };
+
     int nb = 0;     // blocks this CTA has processed
     int kitem = 0;  // items this CTA has processed
     // Q buffers alternate by item: item k + 1's Q rows are written at item
@@ -451,13 +448,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const Item it = it_cur;
       const int nqv = (it.gamma + 1) * group - it.v0;  // this item's vectors, from v0
       const int nblk = (it.p1 - it.p0 + PAGES - 1) / PAGES;
-      // the last key position each of the group's query vectors may see (-1:
-      // padding); in a token tree every node's keys end within L + 63 and the
-      // ancestor sets decide the rest
+      // vector va (row va / group of the draft block) sees the keys up to
+      // L + va / group, i.e. key k when (k - L) * group <= va; columns from
+      // nq_g on hold no vector.  In a token tree the ancestor sets decide the
+      // keys L .. L + 63
       const bool tree = p.row_anc != nullptr;
-      int qlim[NH];
-#pragma unroll
-      for (int j = 0; j < NH; ++j) qlim[j] = col0 + j < nqv ? it.L + (tree ? 63 : (it.v0 + col0 + j) / group) : -1;
+      const int nq_g = nqv - col0, va0 = it.v0 + col0;
 
       // the next item's Q rows into the other buffer, once item k - 1's last
       // QK^T has read it; then the Q rows and the record of the item after it
@@ -497,6 +493,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // mask (block-causal; keys of pages past the item never count) and scale to base 2
         const int page = it.p0 + b * PAGES + (t >> 4);
         const int key = page < it.p1 ? page * 16 + (t & 15) : 0x7FFFFFFF;
+        // column j sees this key when j >= dk (and j < nq_g); keys past the item see no column
+        constexpr int kNone = 0x7FFFFFFF, kAll = -0x7FFFFFFF;
+        const int dk = page >= it.p1 ? kNone
+                       : tree        ? (key <= it.L + 63 ? kAll : kNone)
+                                     : (key - it.L) * group - va0;
         bool up = false;
         if (tree && key >= it.L && key <= it.L + 63) {
           // token tree, key L + d: visible to the columns whose node has node d
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            s[j] = key <= qlim[j] ? s[j] * scale : -INFINITY;
+            s[j] = j < nq_g && j >= dk ? s[j] * scale : -INFINITY;
             up |= s[j] > m[j] + kLazy;
           }
         }
@@ -549,15 +550,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (rescale && b > 0) {
           wait(&p_empty[(nb - 1) & 1], ((nb - 1) >> 1) & 1);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {  // the hi and the lo accumulator
-            const uint32_t ta = t_o + lane_off + part * NQ + col0;
-            float o[NH];
-            ld_cols(ta, o);
+          for (int part = 0; part < 2; ++part) {  // the hi and the lo accumulator, 8 columns at a time
 #pragma unroll
-            for (int j = 0; j < NH; ++j) o[j] *= sc[j];
-            if constexpr (NH == 16) {
-              tmem_st16(ta, o);
-            } else {
+            for (int j0 = 0; j0 < NH; j0 += 8) {
+              const uint32_t ta = t_o + lane_off + part * NQ + col0 + j0;
+              float o[8];
+              tmem_ld8(ta, o);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o[j] *= sc[j0 + j];
               tmem_st8(ta, o);
             }
           }
@@ -656,6 +656,7 @@ cudaError_t launch_nq(const CUtensorMap* kv_map, const AttnParams& p, int grid, 
 cudaError_t launch_attention_tc(int nq, const CUtensorMap* kv_map, const AttnParams& p, int grid, cudaStream_t stream) {
   if (nq == 16) return launch_nq<16>(kv_map, p, grid, stream);
   if (nq == 32) return launch_nq<32>(kv_map, p, grid, stream);
+  if (nq == 48) return launch_nq<48>(kv_map, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -128,8 +128,10 @@ def _attention_ref(dims, b, q):
     (wl.NINE_B, [int(x) for x in np.random.default_rng(77).integers(0, 3000, size=40)],
      [int(x) for x in np.random.default_rng(78).integers(0, 4, size=40)], 3),
     # gamma 8: 9 rows x 4 query heads per KV head = 36 query vectors per item
-    # (the tcgen05 kernel splits them over two items of 32 and 4)
+    # (the tcgen05 kernel's 48-vector items)
     (wl.NINE_B, [2048, 2048, 100, 0, 777, 2047, 16, 1500], [8, 8, 8, 8, 0, 5, 8, 3], 8),
+    # gamma 11: 48 query vectors, the most one item holds; a long context cut into chunks
+    (wl.NINE_B, [3000, 0, 47, 2048, 130, 6000], [11, 11, 4, 9, 11, 0], 11),
     # gamma 15: 64 query vectors, two full items; long contexts split into chunks too
     (wl.NINE_B, [9000, 2048, 0, 5000, 31], [15, 15, 15, 7, 12], 15),
 ])

@@ -280,15 +280,19 @@ def test_chain_shaped_tree_equals_chain(torch_cuda, nine_b_weights, path):
     assert np.array_equal(d0["page_table"], d1["page_table"])
 
 
-def test_tree_attention_matches_oracle(torch_cuda):
+@pytest.mark.parametrize("gmax", [7, 11])
+def test_tree_attention_matches_oracle(torch_cuda, gmax):
     """Attention alone (sdv_attention, both kernels) on a 9B-shaped batch of
-    trees: node i's query sees the cache and its ancestors' keys only."""
+    trees: node i's query sees the cache and its ancestors' keys only.  Trees
+    of up to 8 nodes fill the tcgen05 kernel's 32-vector items, up to 12 its
+    48-vector items."""
     torch = torch_cuda
     from workloads import device as wd
     from tests.test_gpu_parity import _attn_only_engine
-    dims, gmax = wl.NINE_B, 7
-    g = np.random.default_rng(9)
-    trees = [_random_tree(g, int(g.integers(1, 9))) for _ in range(12)]
+    dims = wl.NINE_B
+    g = np.random.default_rng(9 + gmax)
+    trees = [_random_tree(g, int(g.integers(1, gmax + 2))) for _ in range(12)]
+    trees[0] = _random_tree(g, gmax + 1)
     lens = [int(x) for x in g.integers(0, 2500, size=12)]
     b, par = _tree_batch(dims, trees, lens, 9, gmax)
     R, nq, nkv, D, P = b.R, dims["n_q"], dims["n_kv"], dims["head_dim"], dims["page"]
