@@ -19,8 +19,8 @@
 //    rows side by side, so each K tile is read once; the softmax adds the two
 //    column halves (S double-buffered across blocks);
 //  * eight softmax warps own the 128 key lanes, in two groups of four that each
-//    take half of the query columns (two warps per SM sub-partition): they mask, rescale the logits
-//    to base 2, and keep a per-query reference maximum that moves only when a
+//    take half of the query columns (two warps per SM sub-partition): they mask
+//    (q comes pre-scaled to base-2 logits) and keep a per-query reference maximum that moves only when a
 //    logit exceeds it by more than 8 (then O is rescaled in TMEM), so the
 //    weights p = 2^(s - m) stay <= 256 and need no per-block reduction; they
 //    write p as bf16 hi + lo planes (K-major, key columns; two buffers, so the
@@ -51,6 +51,10 @@ constexpr int PAGES = KEYS / 16;
 constexpr int HALF = KEYS * 128;             // one 64-dim half of K or V for 128 keys: 16 KB
 constexpr int STAGE_BYTES = 2 * HALF;       // K or V of one block (2 halves): 32 KB
 constexpr float kLazy = 8.f;                 // log2 headroom of the lazily moved reference maximum
+// the reference maximum before a column's first visible key: finite, so that
+// 2^(s - m) and 2^(m - m') need no special case (the first visible logit
+// always moves it; a column with no visible key keeps l = 0 and weights 0)
+constexpr float kNoMax = -1e30f;
 
 template <int NQ>
 struct TaCfg {
@@ -113,6 +117,14 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x on the special-function unit, subnormal results flushed to zero: a
+// softmax weight below 2^-126 of the reference maximum changes no sum.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Order-preserving float <-> int map, so that an integer warp max is a float max.
@@ -359,6 +371,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // ---------------- softmax + epilogue: warps 2..9, two groups of four ----------------
   {
     constexpr int NH = NQ / 2;                   // query columns per group
+    static_assert(NH % 8 == 0, "a group's first column is a multiple of 8 (the P rows' swizzle)");
     const int grp = (warp - 2) >> 2;             // columns [grp * NH, grp * NH + NH)
     const int quarter = warp & 3;                // TMEM lanes 32 * quarter .. + 31
     const int t = quarter * 32 + lane;           // key lane of S, head dim of O
@@ -422,9 +435,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int q = 0; q < QPT; ++q) {
         const int idx = t + q * 128;
         const int v = col0 + idx / (D / 4), ch = idx % (D / 4);
+        // q scaled by log2(e) / sqrt(D): the MMA yields base-2 logits
         uint2 hi, lo;
-        split_bf16x2(src[q].x, src[q].y, hi.x, lo.x);
-        split_bf16x2(src[q].z, src[q].w, hi.y, lo.y);
+        split_bf16x2(src[q].x * scale, src[q].y * scale, hi.x, lo.x);
+        split_bf16x2(src[q].z * scale, src[q].w * scale, hi.y, lo.y);
         const int off = (ch >> 4) * C::Q_HALF + v * 128 + ((((ch & 15) >> 1) ^ (v & 7)) << 4) + (ch & 1) * 8;
         *reinterpret_cast<uint2*>(qdst + off) = hi;
         *reinterpret_cast<uint2*>(qdst + NQ * 128 + off) = lo;  // lo rows follow the hi rows
@@ -469,7 +483,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       float m[NH], l[NH];
 #pragma unroll
       for (int j = 0; j < NH; ++j) {
-        m[j] = -INFINITY;
+        m[j] = kNoMax;
         l[j] = 0.f;
       }
       // this thread's P column: half of the key range, 16-byte chunk, byte within it
@@ -490,7 +504,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sb]);
-        // mask (block-causal; keys of pages past the item never count) and scale to base 2
+        // mask (block-causal; keys of pages past the item never count); s is in base 2 already
         const int page = it.p0 + b * PAGES + (t >> 4);
         const int key = page < it.p1 ? page * 16 + (t & 15) : 0x7FFFFFFF;
         // column j sees this key when j >= dk (and j < nq_g); keys past the item see no column
@@ -506,13 +520,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
             const bool in = col0 + j < nqv && ((p.row_anc[it.r0 + (it.v0 + col0 + j) / group] >> d) & 1ull);
-            s[j] = in ? s[j] * scale : -INFINITY;
+            s[j] = in ? s[j] : -INFINITY;
             up |= s[j] > m[j] + kLazy;
           }
+        } else if (dk <= 0) {
+          // a key every column sees (the columns past the item's vectors have
+          // zero q rows and nothing reads them: they are left unmasked)
+#pragma unroll
+          for (int j = 0; j < NH; ++j) up |= s[j] > m[j] + kLazy;
         } else {
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            s[j] = j < nq_g && j >= dk ? s[j] * scale : -INFINITY;
+            s[j] = j < nq_g && j >= dk ? s[j] : -INFINITY;
             up |= s[j] > m[j] + kLazy;
           }
         }
@@ -534,7 +553,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int j = 0; j < NH; ++j) {
             const float bm = fmaxf(fmaxf(redb[j], redb[NH + j]), fmaxf(redb[2 * NH + j], redb[3 * NH + j]));
             const float mn = fmaxf(m[j], bm);
-            const float av = mn == -INFINITY ? 1.f : exp2f(m[j] - mn);
+            const float av = exp2f(m[j] - mn);
             rescale |= av != 1.f;
             m[j] = mn;
             l[j] *= av;
@@ -543,7 +562,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
-          s[j] = exp2f(s[j] - (m[j] == -INFINITY ? 0.f : m[j]));  // the weight p, in place
+          s[j] = ex2_ftz(s[j] - m[j]);  // the weight p, in place (0 for masked keys)
           l[j] += s[j];
         }
         // O is rescaled only once the previous block's PV has finished
@@ -566,13 +585,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (nb >= 2) wait(&p_empty[nb & 1], ((nb - 2) >> 1) & 1);
         {
           // P^T as bf16 hi + lo: row v, key column t (K-major over keys, 128-byte swizzle)
-          uint8_t* pbuf = smem + C::OFF_P + (nb & 1) * C::P_BUF + p_half * C::P_HALF + p_byte;
+          // (col0 is a multiple of 8, so row col0 + j swizzles like row j)
+          uint8_t* pbuf = smem + C::OFF_P + (nb & 1) * C::P_BUF + p_half * C::P_HALF + p_byte + col0 * 128;
+          const int pc16 = p_chunk << 4;
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            const int v = col0 + j;
             const __nv_bfloat16 h = __float2bfloat16_rn(s[j]);
             const __nv_bfloat16 lo = __float2bfloat16_rn(s[j] - __bfloat162float(h));
-            const int off = v * 128 + ((p_chunk ^ (v & 7)) << 4);
+            const int off = j * 128 + (pc16 ^ ((j & 7) << 4));
             *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = h;
             *reinterpret_cast<__nv_bfloat16*>(pbuf + NQ * 128 + off) = lo;  // lo rows follow the hi rows
           }
