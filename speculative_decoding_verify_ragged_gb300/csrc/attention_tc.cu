@@ -20,9 +20,10 @@
 //    column halves (S double-buffered across blocks);
 //  * eight softmax warps own the 128 key lanes, in two groups of four that each
 //    take half of the query columns (two warps per SM sub-partition): they mask
-//    (q comes pre-scaled to base-2 logits) and keep a per-query reference maximum that moves only when a
-//    logit exceeds it by more than 8 (then O is rescaled in TMEM), so the
-//    weights p = 2^(s - m) stay <= 256 and need no per-block reduction; they
+//    (q comes pre-scaled to base-2 logits) and keep a per-query bound m, 8
+//    above the largest logit seen when it last moved, that moves only when a
+//    logit exceeds it (then O is rescaled in TMEM), so the weights
+//    p = 2^(s - m) stay <= 1 and need no per-block reduction; they
 //    write p as bf16 hi + lo planes (K-major, key columns; two buffers, so the
 //    softmax of a block overlaps the PV of the one before) and keep per-lane
 //    partial sums of p;
@@ -50,10 +51,10 @@ constexpr int KEYS = 128;                    // keys per block (8 pages of 16)
 constexpr int PAGES = KEYS / 16;
 constexpr int HALF = KEYS * 128;             // one 64-dim half of K or V for 128 keys: 16 KB
 constexpr int STAGE_BYTES = 2 * HALF;       // K or V of one block (2 halves): 32 KB
-constexpr float kLazy = 8.f;                 // log2 headroom of the lazily moved reference maximum
-// the reference maximum before a column's first visible key: finite, so that
-// 2^(s - m) and 2^(m - m') need no special case (the first visible logit
-// always moves it; a column with no visible key keeps l = 0 and weights 0)
+constexpr float kLazy = 8.f;                 // log2 headroom of the lazily moved bound over the logits
+// the bound before a column's first visible key: finite, so that 2^(s - m)
+// and 2^(m - m') need no special case (the first visible logit always moves
+// it; a column with no visible key keeps l = 0 and weights 0)
 constexpr float kNoMax = -1e30f;
 
 template <int NQ>
@@ -120,7 +121,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 }
 
 // 2^x on the special-function unit, subnormal results flushed to zero: a
-// softmax weight below 2^-126 of the reference maximum changes no sum.
+// softmax weight below 2^-126 of the bound changes no sum.
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -521,21 +522,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int j = 0; j < NH; ++j) {
             const bool in = col0 + j < nqv && ((p.row_anc[it.r0 + (it.v0 + col0 + j) / group] >> d) & 1ull);
             s[j] = in ? s[j] : -INFINITY;
-            up |= s[j] > m[j] + kLazy;
+            up |= s[j] > m[j];
           }
         } else if (dk <= 0) {
           // a key every column sees (the columns past the item's vectors have
           // zero q rows and nothing reads them: they are left unmasked)
 #pragma unroll
-          for (int j = 0; j < NH; ++j) up |= s[j] > m[j] + kLazy;
+          for (int j = 0; j < NH; ++j) up |= s[j] > m[j];
         } else {
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
             s[j] = j < nq_g && j >= dk ? s[j] : -INFINITY;
-            up |= s[j] > m[j] + kLazy;
+            up |= s[j] > m[j];
           }
         }
-        // does any logit of the block exceed its reference by more than kLazy?
+        // does any logit of the block exceed its bound m?
         const unsigned any_w = __ballot_sync(0xffffffffu, up);
         if (lane == 0) flags[quarter] = any_w != 0u;
         named_sync(bar_id, 128);
@@ -552,7 +553,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
             const float bm = fmaxf(fmaxf(redb[j], redb[NH + j]), fmaxf(redb[2 * NH + j], redb[3 * NH + j]));
-            const float mn = fmaxf(m[j], bm);
+            const float mn = fmaxf(m[j], bm + kLazy);
             const float av = exp2f(m[j] - mn);
             rescale |= av != 1.f;
             m[j] = mn;
@@ -562,7 +563,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
-          s[j] = ex2_ftz(s[j] - m[j]);  // the weight p, in place (0 for masked keys)
+          s[j] = ex2_ftz(s[j] - m[j]);  // the weight p <= 1, in place (0 for masked keys)
           l[j] += s[j];
         }
         // O is rescaled only once the previous block's PV has finished
@@ -589,12 +590,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           uint8_t* pbuf = smem + C::OFF_P + (nb & 1) * C::P_BUF + p_half * C::P_HALF + p_byte + col0 * 128;
           const int pc16 = p_chunk << 4;
 #pragma unroll
-          for (int j = 0; j < NH; ++j) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(s[j]);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(s[j] - __bfloat162float(h));
-            const int off = j * 128 + (pc16 ^ ((j & 7) << 4));
-            *reinterpret_cast<__nv_bfloat16*>(pbuf + off) = h;
-            *reinterpret_cast<__nv_bfloat16*>(pbuf + NQ * 128 + off) = lo;  // lo rows follow the hi rows
+          for (int j = 0; j < NH; j += 2) {  // two columns per packed conversion
+            uint32_t h, lo;
+            split_bf16x2(s[j], s[j + 1], h, lo);
+            const int off0 = j * 128 + (pc16 ^ ((j & 7) << 4));
+            const int off1 = (j + 1) * 128 + (pc16 ^ (((j + 1) & 7) << 4));
+            *reinterpret_cast<uint16_t*>(pbuf + off0) = static_cast<uint16_t>(h);
+            *reinterpret_cast<uint16_t*>(pbuf + off1) = static_cast<uint16_t>(h >> 16);
+            *reinterpret_cast<uint16_t*>(pbuf + NQ * 128 + off0) = static_cast<uint16_t>(lo);  // lo rows follow
+            *reinterpret_cast<uint16_t*>(pbuf + NQ * 128 + off1) = static_cast<uint16_t>(lo >> 16);
           }
         }
         fence_proxy_async_smem();
