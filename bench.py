@@ -1073,14 +1073,16 @@ def timeline_rows(a):
     """(row, entry, wait done, exit) per stamped row of the trace tables `a`
     [steps, 32, 3] (global-timer ns): medians over the steps, in us from the
     prologue's entry, in TIMELINE_ORDER; a row some step left unstamped is
-    left out."""
+    left out, and a kernel none of whose blocks passed its wait in some step
+    (a fixup with no cut tile: every block leaves before it) has wait None."""
     t0 = a[:, 0, 0]
     out = []
     for k in TIMELINE_ORDER:
         if not (a[:, k, 2] > 0).all():
             continue
         rel = lambda col: float(np.median(a[:, k, col] - t0)) / 1e3  # noqa: E731
-        out.append((k, rel(0), rel(1), rel(2)))
+        waited = (a[:, k, 1] < 2 ** 62).all()
+        out.append((k, rel(0), rel(1) if waited else None, rel(2)))
     return out
 
 
@@ -1095,6 +1097,11 @@ def print_timeline(title, live_us, out):
             # a point: first block, -, last block, time since the previous point's last block
             print(f"| {timeline_name(k)} | {ent:.1f} | - | {ex:.1f} | {ex - prev_point:.1f} |")
             prev_point = ex
+            continue
+        if wt is None:
+            # no block waited for the kernel ahead: it added nothing after it
+            print(f"| {timeline_name(k)} | {ent:.1f} | - | {ex:.1f} | {max(0.0, ex - prev):.1f} |")
+            prev = max(prev, ex)
             continue
         print(f"| {timeline_name(k)} | {ent:.1f} | {wt:.1f} | {ex:.1f} | {ex - max(wt, prev):.1f} |")
         prev = ex

@@ -68,3 +68,26 @@ def test_printed_busy_column(capsys):
     # after its own wait stamp here), not from the last point (312.0)
     assert busy["realignment"] == 321.0 - 313.0
     assert "| - sampling: status read | 301.5 | - | 302.0 |" in "\n".join(lines)
+
+
+def test_a_kernel_whose_blocks_all_left_before_the_wait():
+    """A fixup kernel with no cut tile: every block leaves before its wait, so
+    the wait stamp keeps its initial value; the row shows no wait and adds
+    nothing to the step, and the next kernel still counts from the GEMM."""
+    a = _tables()
+    for s in range(a.shape[0]):
+        t0 = a[s, 0, 0]
+        a[s, 17] = [t0 + 6.0e3, 2 ** 62, t0 + 8.0e3]  # the QKV GEMM's fixup: entry and exit only
+    out = bench.timeline_rows(a)
+    row = [r for r in out if r[0] == 17]
+    assert len(row) == 1 and row[0][2] is None
+    import io
+    import contextlib
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.print_timeline("synthetic", 320.0, out)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("| ") and "---" not in ln]
+    busy = {ln.split(" | ")[0][2:]: float(ln.rstrip(" |").split(" | ")[-1]) for ln in lines[1:]}
+    assert busy["QKV GEMM fixup"] == 0.0
+    assert busy["attention"] == 32.0 - 22.0
+    assert "| QKV GEMM fixup | 6.0 | - | 8.0 |" in "\n".join(lines)
